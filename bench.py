@@ -1,0 +1,440 @@
+#!/usr/bin/env python
+"""Benchmark of the SSD core: forward + analytic backward tokens/s on one GPU.
+
+Workload (default): batch 4, T 2048, 32 heads x headdim 64 (d_inner 2048),
+d_state 128, one group, chunk 256, bf16 storage with fp32 accumulation;
+seeded synthetic inputs (state_space_model_analytic_gb300.synth).  A step is
+one ssd_forward (y, final state, chunk history) followed by one ssd_backward
+(consuming that history) through the C ABI.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Prints one JSON line (rank 0).  Under torchrun each rank runs an independent
+replica (the path has no data-parallel exchange); value = all ranks' tokens /
+the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "SSD fwd+bwd tokens/sec (d_inner 2048, d_state 128, T 2048); % of roofline"
+UNIT = "tokens/s"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+L2_FLUSH_BYTES = 256 << 20
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", type=int, default=1, help="workload index (default 1)")
+    ap.add_argument("--cpu-budget", type=float, default=15.0,
+                    help="seconds of oracle work for the cpu_baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# algorithmic bytes (each tensor read or written once) of one launch of each
+# kernel, for the problem dims `d`; see the kernel table in the design doc.
+
+def _sizes(d, has_h0):
+    s = 2 if d.dtype == "bf16" else 4
+    B, T, H, P, N, G, nc = d.batch, d.seqlen, d.nheads, d.headdim, d.dstate, d.ngroups, d.nchunks
+    return dict(
+        x=B * T * H * P * s, bc=B * T * G * N * s, dt=B * T * H * 4, st=B * nc * H * P * N * 4,
+        hs=B * H * P * N * 4, h0=(B * H * P * N * 4 if has_h0 else 0), tokh=B * T * H * 4,
+        cl=B * H * nc * 4, small=d.nheads * 4)
+
+
+def kernel_bytes(name, d, has_h0):
+    z = _sizes(d, has_h0)
+    base = name.rsplit("_", 1)[0] if name.endswith(("_simt", "_tc")) else name
+    table = {
+        "chunk_state": z["x"] + z["dt"] + z["bc"] + z["st"] + z["cl"],
+        "state_pass_fwd": 2 * z["st"] + z["h0"] + z["hs"] + z["cl"],
+        "chunk_scan": 2 * z["x"] + z["dt"] + 2 * z["bc"] + z["st"],
+        "chunk_dstate": z["x"] + z["dt"] + z["bc"] + z["st"] + z["cl"],
+        "state_pass_bwd": 2 * z["st"] + z["hs"] + z["cl"],
+        "bwd_col": 3 * z["x"] + z["dt"] + 3 * z["bc"] + z["st"] + 3 * z["tokh"],
+        "bwd_row": 2 * z["x"] + z["dt"] + 3 * z["bc"] + z["st"] + 2 * z["tokh"],
+        "bwd_dt": 2 * z["dt"] + 2 * z["st"] + 5 * z["tokh"],
+        "reduce_heads": 2 * z["small"],
+    }
+    return table.get(base)
+
+
+def step_bytes(d, has_h0):
+    """Inputs read + outputs written by ssd_forward and ssd_backward, once each."""
+    z = _sizes(d, has_h0)
+    fwd = z["x"] + z["dt"] + 2 * z["bc"] + 2 * z["small"] + z["h0"] + z["x"] + z["hs"] + z["st"]
+    bwd = (2 * z["x"] + z["dt"] + 2 * z["bc"] + 2 * z["small"] + z["h0"] + z["st"]
+           + z["x"] + z["dt"] + 2 * z["bc"] + 2 * z["small"] + z["hs"])
+    return fwd + bwd
+
+
+def step_flops(d):
+    """Tensor-contraction FLOPs, causal halves only (fwd G*Q^2*N + H*(Q^2*P + 4QPN),
+    bwd G*3Q^2*N + H*(2Q^2*P + 8QPN), per chunk)."""
+    Q, N, P, G, H = d.chunk, d.dstate, d.headdim, d.ngroups, d.nheads
+    per_chunk = G * Q * Q * N + H * (Q * Q * P + 4 * Q * P * N) \
+        + G * 3 * Q * Q * N + H * (2 * Q * Q * P + 8 * Q * P * N)
+    return per_chunk * d.nchunks * d.batch
+
+
+def read_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            pk = json.load(open(path))
+            hbm = pk.get("hbm_gbs") or pk.get("hbm_GBs")
+            if hbm:
+                return float(hbm), pk.get("bf16_tflops"), "measured"
+        except Exception:
+            pass
+    return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def source_digest():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "state_space_model_analytic_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def read_traffic(kernel, workload):
+    """dram bytes per launch of `kernel` from the committed ncu summary, if it
+    was captured on the current kernel sources."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    try:
+        rec = json.load(open(path))
+    except Exception:
+        return None
+    if rec.get("source_digest") != source_digest():
+        return None
+    ent = rec.get("kernels", {}).get(kernel)
+    if not ent or ent.get("workload") != workload:
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.idx = gpu_index
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        rows = [r.strip().split(",") for r in self.file.read().splitlines() if r.strip()]
+        os.unlink(self.file.name)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            r = [c.strip() for c in r]
+            try:
+                sm.append(float(r[0]))
+                mx.append(float(r[1]))
+            except (ValueError, IndexError):
+                continue
+            for n, v in zip(names, r[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+def oracle_sample_time(dims, inp, tokens, threads):
+    """Seconds of one oracle forward + backward on batch row 0, all heads,
+    the first `tokens` steps (a complete problem in its own right)."""
+    import oracle
+    sl = {k: (None if v is None else v) for k, v in inp.items()}
+    x = sl["x"][:1, :tokens]
+    dt = sl["dt"][:1, :tokens]
+    Bm = sl["B"][:1, :tokens]
+    Cm = sl["C"][:1, :tokens]
+    dy = sl["dy"][:1, :tokens]
+    h0 = None if sl["h0"] is None else sl["h0"][:1]
+    t0 = time.perf_counter()
+    oracle.ssd_forward(x, dt, sl["A"], Bm, Cm, sl["D"], h0, chunk=dims.chunk, threads=threads)
+    oracle.ssd_backward(x, dt, sl["A"], Bm, Cm, sl["D"], h0, dy, threads=threads)
+    return time.perf_counter() - t0
+
+
+def calibrate_tokens(dims, inp, threads, seconds):
+    probe = min(64, dims.seqlen)
+    t = oracle_sample_time(dims, inp, probe, threads)
+    tokens = int(probe * seconds / max(t, 1e-6))
+    return max(16, min(dims.seqlen, tokens))
+
+
+def run_reference(args, dims, inp, name):
+    import oracle
+    oracle.build_oracle()
+    threads = os.cpu_count() or 1
+    total = args.steps + args.warmup
+    per_step = min(2.0, 150.0 / max(total, 1))
+    tokens = calibrate_tokens(dims, inp, threads, per_step)
+    for _ in range(args.warmup):
+        oracle_sample_time(dims, inp, tokens, threads)
+    times = [oracle_sample_time(dims, inp, tokens, threads) for _ in range(args.steps)]
+    sec = sum(times)
+    value = tokens * args.steps / sec
+    sample = f"batch row 0 of {dims.batch}, all {dims.nheads} heads, first {tokens} of {dims.seqlen} steps"
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sec / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded; same inputs as the GPU arm)",
+        "config": {"workload": name, "batch": dims.batch, "seqlen": dims.seqlen,
+                   "nheads": dims.nheads, "headdim": dims.headdim, "dstate": dims.dstate,
+                   "ngroups": dims.ngroups, "chunk": dims.chunk, "storage": dims.dtype},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse_args()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    from state_space_model_analytic_gb300 import synth
+    name, dims, has_h0, _ = synth.CONFIGS[args.config]
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        _, inp = synth.config_inputs(args.config)
+        print(json.dumps(run_reference(args, dims, inp, name)), flush=True)
+        return 0
+
+    import numpy as np
+    import torch
+    import state_space_model_analytic_gb300 as ssd
+    from state_space_model_analytic_gb300 import _native as nat
+
+    ssd.build()
+    torch.cuda.set_device(local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+
+    _, inp = synth.config_inputs(args.config)
+    dev = torch.device("cuda", local_rank)
+    io = torch.bfloat16 if dims.dtype == "bf16" else torch.float32
+
+    def to(a, dtype):
+        return None if a is None else torch.from_numpy(
+            np.ascontiguousarray(a, dtype=np.float32)).to(dtype).to(dev)
+
+    t_in = {"x": to(inp["x"], io), "dt": to(inp["dt"], torch.float32),
+            "A": to(inp["A"], torch.float32), "B": to(inp["B"], io), "C": to(inp["C"], io),
+            "D": to(inp["D"], torch.float32), "h0": to(inp["h0"], torch.float32),
+            "dy": to(inp["dy"], io)}
+    Q = dims.chunk
+    Bz, T, H, P, N, G, nc = (dims.batch, dims.seqlen, dims.nheads, dims.headdim, dims.dstate,
+                             dims.ngroups, dims.nchunks)
+    fwd_out = {"y": torch.empty_like(t_in["x"]),
+               "final_state": torch.empty(Bz, H, P, N, device=dev),
+               "chunk_states": torch.empty(Bz, nc, H, P, N, device=dev)}
+    bwd_out = {"dx": torch.empty_like(t_in["x"]), "ddt": torch.empty_like(t_in["dt"]),
+               "dA": torch.empty_like(t_in["A"]), "dB": torch.empty_like(t_in["B"]),
+               "dC": torch.empty_like(t_in["C"]), "dD": torch.empty_like(t_in["D"]),
+               "dh0": torch.empty(Bz, H, P, N, device=dev)}
+    cdims = ssd.dims_of(t_in["x"], t_in["B"], Q)
+    ws_f = ssd.alloc_workspace(cdims, 0, dev)
+    ws_b = ssd.alloc_workspace(cdims, 1, dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(ti=t_in):
+        ssd.forward(ti["x"], ti["dt"], ti["A"], ti["B"], ti["C"], ti["D"], ti["h0"], chunk=Q,
+                    out=fwd_out, workspace=ws_f)
+        ssd.backward(ti["x"], ti["dt"], ti["A"], ti["B"], ti["C"], ti["D"], ti["h0"], ti["dy"],
+                     fwd_out["chunk_states"], chunk=Q, out=bwd_out, workspace=ws_b)
+
+    for _ in range(args.warmup):
+        step()
+        flush.fill_(1.0)
+    torch.cuda.synchronize()
+
+    # ---- timed region: exactly K steps; L2 flushed between steps (not timed)
+    nat.trace_begin(args.steps * 16)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    clocks = ClockSampler(local_rank)
+    if rank == 0:
+        clocks.start()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    launches0 = ssd.launch_count()
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+        flush.fill_(float(i))
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    launches = ssd.launch_count() - launches0
+    if dist:
+        dist.barrier()
+    clk = clocks.stop() if rank == 0 else None
+    nat.trace_end()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    ms = sum(step_ms) / len(step_ms)
+    kern = nat.trace_read()
+    nat.trace_reset()
+    ms_max = ms
+    if dist:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_max = float(t.item())
+    tokens = dims.tokens
+    value = tokens * world / (ms_max / 1e3)
+
+    # ---- e2e: host buffers through the public API, copies inside the timed region
+    e2e = None
+    if not args.no_e2e:
+        host_in = {k: (None if v is None else v.cpu().pin_memory()) for k, v in t_in.items()}
+        dev_in = {k: (None if v is None else torch.empty_like(v)) for k, v in t_in.items()}
+        outs = ["y", "dx", "ddt", "dA", "dB", "dC", "dD", "dh0"]
+        srcs = {**{"y": fwd_out["y"]}, **bwd_out}
+        host_out = {k: torch.empty(srcs[k].shape, dtype=srcs[k].dtype).pin_memory() for k in outs}
+        h2d = sum(v.numel() * v.element_size() for v in host_in.values() if v is not None)
+        d2h = sum(v.numel() * v.element_size() for v in host_out.values())
+        n_e2e = max(3, min(args.steps, 50))
+
+        def e2e_step():
+            for k, v in host_in.items():
+                if v is not None:
+                    dev_in[k].copy_(v, non_blocking=True)
+            step(dev_in)
+            for k in outs:
+                host_out[k].copy_(srcs[k], non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e_ms = e0.elapsed_time(e1) / n_e2e
+        e2e = {"value": tokens * world / (e_ms / 1e3), "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n_e2e,
+               "ms_per_step": e_ms}
+
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return 0
+
+    # ---- roofline of the dominant kernel (live CUDA-event durations)
+    hbm, bf16_tf, peak_src = read_peaks()
+    total_k = sum(k["ms"] for k in kern) or 1.0
+    kern_sorted = sorted(kern, key=lambda k: -k["ms"])
+    top = kern_sorted[0]
+    top_avg_ms = top["ms"] / max(top["launches"], 1)
+    kb = kernel_bytes(top["name"], dims, has_h0)
+    achieved = kb / (top_avg_ms / 1e3) / 1e9 if kb else None
+    traffic = read_traffic(top["name"], name)
+    sb = step_bytes(dims, has_h0)
+    roofline = {"bound": "hbm", "kernel": top["name"], "achieved": achieved, "peak": hbm,
+                "unit": "GB/s", "frac": (achieved / hbm) if achieved else None,
+                "traffic": traffic, "algorithmic_bytes_per_launch": kb,
+                "avg_launch_ms": top_avg_ms, "peak_source": f"{peak_src} (stream copy)"}
+    step_roof = {"bound": "hbm", "algorithmic_bytes": sb,
+                 "achieved": sb / (ms / 1e3) / 1e9, "peak": hbm, "unit": "GB/s",
+                 "frac": sb / (ms / 1e3) / 1e9 / hbm,
+                 "tensor_flops": step_flops(dims),
+                 "tensor_frac": (step_flops(dims) / (ms / 1e3) / 1e12 / bf16_tf) if bf16_tf else None}
+    kernels = [{"name": k["name"], "launches": k["launches"], "ms_total": round(k["ms"], 4),
+                "share": round(k["ms"] / total_k, 4),
+                "avg_us": round(1e3 * k["ms"] / max(k["launches"], 1), 2)} for k in kern_sorted]
+
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        import oracle
+        oracle.build_oracle()
+        threads = os.cpu_count() or 1
+        ntok = calibrate_tokens(dims, inp, threads, args.cpu_budget)
+        sec = oracle_sample_time(dims, inp, ntok, threads)
+        cpu = {"value": ntok / sec, "unit": UNIT, "cores": threads, "kind": "oracle",
+               "sample": f"batch row 0 of {Bz}, all {H} heads, first {ntok} of {T} steps "
+                         f"(float64 C oracle, {sec:.1f} s)"}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if dims.dtype == "bf16" else "f32",
+        "data": "synthetic (seeded PCG64; distributions of the SSD-core workloads)",
+        "config": {"workload": name, "batch": Bz, "seqlen": T, "nheads": H, "headdim": P,
+                   "dstate": N, "ngroups": G, "chunk": Q, "storage": dims.dtype,
+                   "accumulate": "fp32", "history": "saved by forward, consumed by backward",
+                   "l2": "flushed between timed steps (256 MiB write, outside the step events)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "kernel_path": "tcgen05" if ssd.kernel_path(cdims) == 1 else "simt"},
+        "roofline": roofline, "step_roofline": step_roof, "kernels": kernels,
+        "gpu_launches": launches, "wall_s_timed": wall,
+        "clocks": clk, "cpu_baseline": cpu, "e2e": e2e,
+    }
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,152 @@
+/*
+ * ssd.h — C ABI of the GB300 (sm_103a) Mamba-2 SSD core: forward and analytic
+ * backward of the selective state-space scan.
+ *
+ * What is computed (burn_dragon_kernel 0.5.0, src/sequence/mamba2/backward.rs,
+ * `ssd_forward_state_history_reference` for the recurrence and the `y_grouped`
+ * expression of `tensorized_mamba2_backward_impl` for the output): for every
+ * batch row b and head h, with g the group of h,
+ *
+ *     h_t = exp(dt_t * A_h) * h_{t-1} + dt_t * x_t B_t^T        ([P x N] state)
+ *     y_t = h_t C_t + D_h * x_t
+ *
+ * starting from h_{-1} = h0 (or zeros).  The backward returns the gradients
+ * of L = sum(dy * y) w.r.t. x, dt, A, B, C, D and h0, the quantities of
+ * `ssd_backward_reference` on the same page (that page returns the gradient
+ * w.r.t. a_log = log(-A); here dA is returned, and d a_log = dA * A).
+ *
+ * Heads map to groups as h = g * (H / G) + j (the page reshapes nheads into
+ * [ngroups, heads_per_group]); the heads of one group share B and C.
+ *
+ * Layouts: every tensor is dense row-major, in device memory, 16-byte aligned.
+ *   x, y, dy, dx      [B][T][H][P]          `dtype`
+ *   B, C, dB, dC      [B][T][G][N]          `dtype`
+ *   dt, ddt           [B][T][H]             fp32
+ *   A, D, dA, dD      [H]                   fp32
+ *   h0, final, dh0    [B][H][P][N]          fp32
+ *   chunk_states      [B][nc][H][P][N]      fp32, nc = T / chunk; entry c is
+ *                                           the state *before* step c*chunk
+ *                                           (entry 0 is h0 or zeros)
+ * The caller owns all memory, including the workspace.  Nothing is allocated
+ * by the library on the device or the host.
+ *
+ * Calls are asynchronous on `cuda_stream` (a cudaStream_t; NULL = legacy
+ * default stream).  They return after launching; launch errors are returned,
+ * device-side faults surface at the caller's next synchronisation.  Outputs
+ * are overwritten, never accumulated.  Results are deterministic: no floating
+ * point atomics; every reduction runs in a fixed order.
+ */
+#ifndef SSD_GB300_H
+#define SSD_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define SSD_API __attribute__((visibility("default")))
+#else
+#define SSD_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Storage type of x, B, C, dy, y, dx, dB, dC.  Every other tensor is fp32 and
+ * every accumulation runs in fp32. */
+typedef enum { SSD_F32 = 0, SSD_BF16 = 1 } ssd_dtype;
+
+/* Return codes. */
+enum {
+  SSD_OK = 0,
+  SSD_ERR_INVALID_ARG = 1,    /* null required pointer, bad size, small workspace */
+  SSD_ERR_UNSUPPORTED = 2,    /* valid but unsupported shape (see ssd_forward) */
+  SSD_ERR_ALIGNMENT = 3,      /* a pointer is not 16-byte aligned */
+  SSD_ERR_CUDA = 4,           /* a CUDA runtime call failed (message has it) */
+  SSD_ERR_DEVICE_TIMEOUT = 5  /* a bounded device-side wait gave up */
+};
+
+typedef struct {
+  int64_t batch;    /* B  >= 1 */
+  int64_t seqlen;   /* T  >= 1, multiple of chunk */
+  int64_t nheads;   /* H  >= 1, multiple of ngroups */
+  int64_t headdim;  /* P  in [16, 128], multiple of 16 */
+  int64_t dstate;   /* N  in [16, 256], multiple of 16; P * N <= 16384 */
+  int64_t ngroups;  /* G  >= 1 */
+  int64_t chunk;    /* Q  one of 16, 32, 64, 128, 256 */
+  int32_t dtype;    /* ssd_dtype */
+  int32_t reserved; /* must be 0 */
+} ssd_dims;
+
+/* Bytes of device workspace needed for these dims.  which = 0: ssd_forward;
+ * 1: ssd_backward given the chunk history; 2: ssd_backward with
+ * chunk_states = NULL (history recomputed inside the call).  Returns 0 for
+ * dims the library rejects (ssd_last_error then says why). */
+SSD_API size_t ssd_workspace_bytes(const ssd_dims* dims, int which);
+
+/*
+ * Forward.  Inputs x, dt, A, B, C, D (required) and h0 (NULL = zeros).
+ * Outputs: y (required); final_state (NULL = not written); chunk_states
+ * (NULL = not written; pass it to ssd_backward to skip the recompute).
+ * workspace: device memory of at least ssd_workspace_bytes(dims, 0) bytes,
+ * 256-byte aligned, contents ignored and clobbered.
+ * Errors: SSD_ERR_INVALID_ARG, SSD_ERR_UNSUPPORTED (T % chunk != 0, chunk not
+ * in {16..256}, P or N out of range), SSD_ERR_ALIGNMENT, SSD_ERR_CUDA.  On an
+ * error nothing is launched.
+ */
+SSD_API int ssd_forward(const ssd_dims* dims,
+                        const void* x, const float* dt, const float* A,
+                        const void* B, const void* C, const float* D,
+                        const float* h0,
+                        void* y, float* final_state, float* chunk_states,
+                        void* workspace, size_t workspace_bytes, void* cuda_stream);
+
+/*
+ * Backward of L = sum(dy * y).  Same inputs as ssd_forward plus dy.
+ * chunk_states: the history ssd_forward wrote for the same inputs, or NULL to
+ * recompute it inside this call (needs ssd_workspace_bytes(dims, 2)).
+ * Outputs (all required except dh0): dx, ddt, dA, dB, dC, dD; dh0 (NULL = not
+ * written; when h0 is NULL it is the gradient w.r.t. the zero initial state).
+ * The gradient w.r.t. the final state is taken as zero.
+ */
+SSD_API int ssd_backward(const ssd_dims* dims,
+                         const void* x, const float* dt, const float* A,
+                         const void* B, const void* C, const float* D,
+                         const float* h0, const void* dy, const float* chunk_states,
+                         void* dx, float* ddt, float* dA, void* dB, void* dC, float* dD,
+                         float* dh0,
+                         void* workspace, size_t workspace_bytes, void* cuda_stream);
+
+/* Message for the last non-zero return on this thread ("" if none). */
+SSD_API const char* ssd_last_error(void);
+
+/* Number of kernels this process has launched through the library so far
+ * (all threads).  Diagnostic counter for benchmarks. */
+SSD_API uint64_t ssd_kernel_launch_count(void);
+
+/* Per-kernel timing trace (diagnostics).  While a trace is open, every kernel
+ * the library launches is bracketed by a pair of CUDA events recorded on the
+ * launch stream.  ssd_trace_begin(capacity) opens a trace for up to
+ * `capacity` launches (creates 2*capacity events; needs a current device);
+ * ssd_trace_end() stops recording; ssd_trace_read(i, ...) synchronises on the
+ * recorded events and returns, for the i-th distinct kernel name in first
+ * launch order, its name, the summed event time in milliseconds and its
+ * launch count (returns SSD_ERR_INVALID_ARG past the last name);
+ * ssd_trace_reset() destroys the events.  Launches beyond `capacity` are
+ * counted but not timed (ssd_trace_read reports them in `untimed`).  Not
+ * thread-safe against concurrent library calls on other threads. */
+SSD_API int ssd_trace_begin(int capacity);
+SSD_API int ssd_trace_end(void);
+SSD_API int ssd_trace_read(int index, char* name, int name_len, double* total_ms,
+                           int* launches, int* untimed);
+SSD_API int ssd_trace_reset(void);
+
+/* Which kernel family ssd_forward/ssd_backward select for these dims:
+ * 0 = SIMT fp32 kernels, 1 = tcgen05 tensor-core kernels.  -1 if rejected. */
+SSD_API int ssd_kernel_path(const ssd_dims* dims);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SSD_GB300_H */

@@ -1,0 +1,341 @@
+// C ABI of the SSD core: argument validation, workspace carve-up and the
+// launch sequence of each call.  Declarations and contracts: include/ssd.h.
+#include <atomic>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "../../include/ssd.h"
+#include "ssd_internal.h"
+
+namespace ssd {
+
+static std::atomic<uint64_t> g_launches{0};
+void count_launch(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+
+namespace {
+struct TraceEvent {
+  int name_id;
+  cudaEvent_t start, stop;
+};
+std::mutex g_trace_mu;
+bool g_trace_on = false;
+std::vector<TraceEvent> g_trace_slots;  // created by ssd_trace_begin
+size_t g_trace_used = 0;
+std::vector<std::string> g_trace_names;
+std::vector<int> g_trace_untimed;
+
+int trace_name_id(const char* name) {
+  for (size_t i = 0; i < g_trace_names.size(); ++i)
+    if (g_trace_names[i] == name) return (int)i;
+  g_trace_names.emplace_back(name);
+  g_trace_untimed.push_back(0);
+  return (int)g_trace_names.size() - 1;
+}
+}  // namespace
+
+int trace_open_slot(const char* name, cudaStream_t s) {
+  std::lock_guard<std::mutex> lk(g_trace_mu);
+  if (!g_trace_on) return -1;
+  const int id = trace_name_id(name);
+  if (g_trace_used >= g_trace_slots.size()) {
+    g_trace_untimed[id] += 1;
+    return -1;
+  }
+  TraceEvent& ev = g_trace_slots[g_trace_used];
+  ev.name_id = id;
+  if (cudaEventRecord(ev.start, s) != cudaSuccess) return -1;
+  return (int)g_trace_used++;
+}
+
+void trace_close_slot(int slot, cudaStream_t s) {
+  if (slot < 0) return;
+  std::lock_guard<std::mutex> lk(g_trace_mu);
+  cudaEventRecord(g_trace_slots[slot].stop, s);
+}
+
+size_t simt_smem_need(const Problem& p);
+int simt_row_tile(const Problem& p);
+bool tc_supported(const Problem& p);
+cudaError_t tc_forward_scan(const Problem& p);
+cudaError_t tc_backward(const Problem& p);
+
+namespace {
+
+thread_local std::string g_err;
+
+int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return code;
+}
+
+int cuda_fail(cudaError_t e, const char* where) {
+  return fail(SSD_ERR_CUDA, "%s: %s (%s)", where, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+constexpr size_t kAlign = 256;
+size_t up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+int validate(const ssd_dims* d) {
+  if (!d) return fail(SSD_ERR_INVALID_ARG, "dims is NULL");
+  if (d->batch < 1 || d->seqlen < 1 || d->nheads < 1 || d->headdim < 1 || d->dstate < 1 ||
+      d->ngroups < 1 || d->chunk < 1)
+    return fail(SSD_ERR_INVALID_ARG, "every dimension must be >= 1");
+  if (d->reserved != 0) return fail(SSD_ERR_INVALID_ARG, "dims.reserved must be 0");
+  if (d->dtype != SSD_F32 && d->dtype != SSD_BF16)
+    return fail(SSD_ERR_INVALID_ARG, "dtype %d is not SSD_F32 or SSD_BF16", (int)d->dtype);
+  if (d->nheads % d->ngroups)
+    return fail(SSD_ERR_INVALID_ARG, "nheads %lld is not a multiple of ngroups %lld",
+                (long long)d->nheads, (long long)d->ngroups);
+  const int64_t q = d->chunk;
+  if (q != 16 && q != 32 && q != 64 && q != 128 && q != 256)
+    return fail(SSD_ERR_UNSUPPORTED, "chunk %lld not in {16,32,64,128,256}", (long long)q);
+  if (d->seqlen % q)
+    return fail(SSD_ERR_UNSUPPORTED, "seqlen %lld is not a multiple of chunk %lld",
+                (long long)d->seqlen, (long long)q);
+  if (d->headdim % 16 || d->headdim > 128)
+    return fail(SSD_ERR_UNSUPPORTED, "headdim %lld must be a multiple of 16 in [16,128]",
+                (long long)d->headdim);
+  if (d->dstate % 16 || d->dstate > 256)
+    return fail(SSD_ERR_UNSUPPORTED, "dstate %lld must be a multiple of 16 in [16,256]",
+                (long long)d->dstate);
+  if (d->headdim * d->dstate > 16384)
+    return fail(SSD_ERR_UNSUPPORTED, "headdim * dstate must be <= 16384");
+  // every flat index must fit comfortably in 63 bits and grid limits
+  if (d->batch > 65535 / 2 || d->nheads > 65535)
+    return fail(SSD_ERR_UNSUPPORTED, "batch or nheads too large for the launch grid");
+  const double elems = (double)d->batch * (double)d->seqlen * (double)d->nheads * (double)d->headdim;
+  if (elems > 4.0e12) return fail(SSD_ERR_UNSUPPORTED, "problem too large");
+  return SSD_OK;
+}
+
+Problem base_problem(const ssd_dims* d) {
+  Problem p;
+  memset(&p, 0, sizeof p);
+  p.B = (int)d->batch;
+  p.T = (int)d->seqlen;
+  p.H = (int)d->nheads;
+  p.P = (int)d->headdim;
+  p.N = (int)d->dstate;
+  p.G = (int)d->ngroups;
+  p.Q = (int)d->chunk;
+  p.nc = p.T / p.Q;
+  p.hpg = p.H / p.G;
+  p.bf16 = d->dtype == SSD_BF16;
+  return p;
+}
+
+// Workspace layout.  which: 0 forward, 1 backward with history, 2 backward
+// recomputing the history.  Carves into `p` when base != nullptr.
+size_t carve(Problem* p, char* base, int which) {
+  const size_t B = p->B, T = p->T, H = p->H, P = p->P, N = p->N, nc = p->nc, Q = p->Q;
+  const size_t states = B * nc * H * P * N * sizeof(float);
+  const size_t tokh = B * T * H * sizeof(float);
+  size_t off = 0;
+  auto take = [&](size_t bytes) -> char* {
+    char* r = base ? base + off : nullptr;
+    off += up(bytes);
+    return r;
+  };
+  p->cs_last = (float*)take(B * H * nc * sizeof(float));
+  if (which == 0) {
+    float* h = (float*)take(states);
+    if (!p->hist) p->hist = h;
+    return off;
+  }
+  p->dstate = (float*)take(states);
+  p->rowsum = (float*)take(tokh);
+  p->colsum = (float*)take(tokh);
+  p->statein = (float*)take(tokh);
+  p->eout = (float*)take(tokh);
+  p->drive = (float*)take(tokh);
+  p->dA_part = (float*)take(B * nc * H * sizeof(float));
+  p->dD_part = (float*)take(B * nc * (Q / 16) * H * sizeof(float));
+  if (which == 2) p->hist = (float*)take(states);
+  return off;
+}
+
+int check_smem(const Problem& p) {
+  if (simt_smem_need(p) > 227 * 1024)
+    return fail(SSD_ERR_UNSUPPORTED, "shape needs %zu bytes of shared memory per block",
+                simt_smem_need(p));
+  return SSD_OK;
+}
+
+}  // namespace
+}  // namespace ssd
+
+using namespace ssd;
+
+extern "C" {
+
+const char* ssd_last_error(void) { return g_err.c_str(); }
+
+int ssd_trace_reset(void) {
+  std::lock_guard<std::mutex> lk(g_trace_mu);
+  for (auto& e : g_trace_slots) {
+    cudaEventDestroy(e.start);
+    cudaEventDestroy(e.stop);
+  }
+  g_trace_slots.clear();
+  g_trace_used = 0;
+  g_trace_names.clear();
+  g_trace_untimed.clear();
+  g_trace_on = false;
+  return SSD_OK;
+}
+
+int ssd_trace_begin(int capacity) {
+  g_err.clear();
+  if (capacity < 1 || capacity > (1 << 20))
+    return fail(SSD_ERR_INVALID_ARG, "trace capacity %d out of range", capacity);
+  ssd_trace_reset();
+  std::lock_guard<std::mutex> lk(g_trace_mu);
+  g_trace_slots.reserve((size_t)capacity);
+  for (int i = 0; i < capacity; ++i) {
+    TraceEvent e{0, nullptr, nullptr};
+    cudaError_t r = cudaEventCreate(&e.start);
+    if (r == cudaSuccess) r = cudaEventCreate(&e.stop);
+    if (r != cudaSuccess) return cuda_fail(r, "ssd_trace_begin: cudaEventCreate");
+    g_trace_slots.push_back(e);
+  }
+  g_trace_on = true;
+  return SSD_OK;
+}
+
+int ssd_trace_end(void) {
+  std::lock_guard<std::mutex> lk(g_trace_mu);
+  g_trace_on = false;
+  return SSD_OK;
+}
+
+int ssd_trace_read(int index, char* name, int name_len, double* total_ms, int* launches,
+                   int* untimed) {
+  g_err.clear();
+  std::lock_guard<std::mutex> lk(g_trace_mu);
+  if (index < 0 || index >= (int)g_trace_names.size())
+    return fail(SSD_ERR_INVALID_ARG, "trace index %d out of range", index);
+  double ms = 0.0;
+  int n = 0;
+  for (size_t i = 0; i < g_trace_used; ++i) {
+    const TraceEvent& e = g_trace_slots[i];
+    if (e.name_id != index) continue;
+    cudaError_t r = cudaEventSynchronize(e.stop);
+    float t = 0.f;
+    if (r == cudaSuccess) r = cudaEventElapsedTime(&t, e.start, e.stop);
+    if (r != cudaSuccess) return cuda_fail(r, "ssd_trace_read");
+    ms += t;
+    ++n;
+  }
+  if (name && name_len > 0) snprintf(name, (size_t)name_len, "%s", g_trace_names[index].c_str());
+  if (total_ms) *total_ms = ms;
+  if (launches) *launches = n;
+  if (untimed) *untimed = g_trace_untimed[index];
+  return SSD_OK;
+}
+
+uint64_t ssd_kernel_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+size_t ssd_workspace_bytes(const ssd_dims* dims, int which) {
+  if (validate(dims) != SSD_OK || which < 0 || which > 2) return 0;
+  Problem p = base_problem(dims);
+  return carve(&p, nullptr, which);
+}
+
+int ssd_kernel_path(const ssd_dims* dims) {
+  if (validate(dims) != SSD_OK) return -1;
+  Problem p = base_problem(dims);
+  return tc_supported(p) ? 1 : 0;
+}
+
+int ssd_forward(const ssd_dims* dims, const void* x, const float* dt, const float* A,
+                const void* B, const void* C, const float* D, const float* h0, void* y,
+                float* final_state, float* chunk_states, void* workspace, size_t workspace_bytes,
+                void* cuda_stream) {
+  g_err.clear();
+  int rc = validate(dims);
+  if (rc) return rc;
+  if (!x || !dt || !A || !B || !C || !D || !y || !workspace)
+    return fail(SSD_ERR_INVALID_ARG, "ssd_forward: a required pointer is NULL");
+  const void* ptrs[] = {x, dt, A, B, C, D, h0, y, final_state, chunk_states};
+  for (const void* q : ptrs)
+    if (q && !aligned16(q)) return fail(SSD_ERR_ALIGNMENT, "ssd_forward: pointer %p is not 16-byte aligned", q);
+  if (((uintptr_t)workspace & 255u) != 0)
+    return fail(SSD_ERR_ALIGNMENT, "ssd_forward: workspace must be 256-byte aligned");
+  Problem p = base_problem(dims);
+  if ((rc = check_smem(p))) return rc;
+  p.x = x; p.dt = dt; p.A = A; p.Bm = B; p.Cm = C; p.D = D; p.h0 = h0;
+  p.y = y; p.final_state = final_state; p.hist = chunk_states;
+  const size_t need = carve(&p, nullptr, 0);
+  if (workspace_bytes < need)
+    return fail(SSD_ERR_INVALID_ARG, "ssd_forward: workspace %zu bytes < %zu needed",
+                workspace_bytes, need);
+  p.hist = chunk_states;
+  carve(&p, (char*)workspace, 0);
+  p.stream = (cudaStream_t)cuda_stream;
+
+  cudaError_t e = simt_forward_states(p, p.hist, p.cs_last);
+  if (e != cudaSuccess) return cuda_fail(e, "forward chunk-state kernel");
+  e = simt_state_pass_fwd(p, p.hist, p.cs_last);
+  if (e != cudaSuccess) return cuda_fail(e, "forward state-pass kernel");
+  e = tc_supported(p) ? tc_forward_scan(p) : simt_forward_scan(p);
+  if (e != cudaSuccess) return cuda_fail(e, "forward chunk-scan kernel");
+  return SSD_OK;
+}
+
+int ssd_backward(const ssd_dims* dims, const void* x, const float* dt, const float* A,
+                 const void* B, const void* C, const float* D, const float* h0, const void* dy,
+                 const float* chunk_states, void* dx, float* ddt, float* dA, void* dB, void* dC,
+                 float* dD, float* dh0, void* workspace, size_t workspace_bytes,
+                 void* cuda_stream) {
+  g_err.clear();
+  int rc = validate(dims);
+  if (rc) return rc;
+  if (!x || !dt || !A || !B || !C || !D || !dy || !dx || !ddt || !dA || !dB || !dC || !dD ||
+      !workspace)
+    return fail(SSD_ERR_INVALID_ARG, "ssd_backward: a required pointer is NULL");
+  const void* ptrs[] = {x, dt, A, B, C, D, h0, dy, chunk_states, dx, ddt, dA, dB, dC, dD, dh0};
+  for (const void* q : ptrs)
+    if (q && !aligned16(q)) return fail(SSD_ERR_ALIGNMENT, "ssd_backward: pointer %p is not 16-byte aligned", q);
+  if (((uintptr_t)workspace & 255u) != 0)
+    return fail(SSD_ERR_ALIGNMENT, "ssd_backward: workspace must be 256-byte aligned");
+  Problem p = base_problem(dims);
+  if ((rc = check_smem(p))) return rc;
+  const int which = chunk_states ? 1 : 2;
+  const size_t need = carve(&p, nullptr, which);
+  if (workspace_bytes < need)
+    return fail(SSD_ERR_INVALID_ARG, "ssd_backward: workspace %zu bytes < %zu needed%s",
+                workspace_bytes, need, chunk_states ? "" : " (recomputing chunk states)");
+  p.x = x; p.dt = dt; p.A = A; p.Bm = B; p.Cm = C; p.D = D; p.h0 = h0; p.dy = dy;
+  p.dx = dx; p.ddt = ddt; p.dA = dA; p.dB = dB; p.dC = dC; p.dD = dD; p.dh0 = dh0;
+  p.hist = nullptr;
+  carve(&p, (char*)workspace, which);
+  if (chunk_states) p.hist = const_cast<float*>(chunk_states);
+  p.stream = (cudaStream_t)cuda_stream;
+
+  cudaError_t e;
+  if (!chunk_states) {
+    // recompute the chunk-start states into the workspace (final state not needed)
+    Problem f = p;
+    f.final_state = nullptr;
+    e = simt_forward_states(f, f.hist, f.cs_last);
+    if (e != cudaSuccess) return cuda_fail(e, "backward recompute chunk-state kernel");
+    e = simt_state_pass_fwd(f, f.hist, f.cs_last);
+    if (e != cudaSuccess) return cuda_fail(e, "backward recompute state-pass kernel");
+  }
+  e = tc_supported(p) ? tc_backward(p) : simt_backward(p);
+  if (e != cudaSuccess) return cuda_fail(e, "backward kernels");
+  return SSD_OK;
+}
+
+}  // extern "C"

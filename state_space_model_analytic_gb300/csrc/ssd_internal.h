@@ -1,0 +1,79 @@
+// Host-side problem description shared by the C-ABI layer and the kernel
+// launchers.  Not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace ssd {
+
+struct Problem {
+  int B, T, H, P, N, G, Q, nc, hpg;
+  int bf16;  // storage type of x, B, C, dy, y, dx, dB, dC: 0 fp32, 1 bf16
+
+  // inputs
+  const void* x;
+  const float* dt;
+  const float* A;
+  const void* Bm;
+  const void* Cm;
+  const float* D;
+  const float* h0;  // nullable
+  const void* dy;   // backward only
+
+  // forward outputs
+  void* y;
+  float* final_state;  // nullable
+  float* hist;         // [B][nc][H][P][N]: chunk-start states (user buffer or workspace)
+
+  // backward outputs
+  void* dx;
+  float* ddt;
+  float* dA;
+  void* dB;
+  void* dC;
+  float* dD;
+  float* dh0;  // nullable
+
+  // workspace carve-up
+  float* cs_last;  // [B][H][nc]   total log-decay of each chunk
+  float* dstate;   // [B][nc][H][P][N]  R_c, then the state gradient at chunk end
+  float* rowsum;   // [B][T][H]
+  float* colsum;   // [B][T][H]
+  float* statein;  // [B][T][H]
+  float* eout;     // [B][T][H]
+  float* drive;    // [B][T][H]
+  float* dA_part;  // [B][nc][H]
+  float* dD_part;  // [B][nc][Q/16][H]  (tile-count upper bound)
+
+  cudaStream_t stream;
+};
+
+// Kernel launchers (SIMT family).  Each returns the CUDA launch status and
+// bumps the launch counter.
+cudaError_t simt_forward_states(const Problem& p, float* hist, float* cs_last);
+cudaError_t simt_state_pass_fwd(const Problem& p, float* hist, const float* cs_last);
+cudaError_t simt_forward_scan(const Problem& p);
+cudaError_t simt_backward(const Problem& p);
+
+void count_launch(int n = 1);
+
+// Per-kernel event trace (see ssd_trace_begin in include/ssd.h).  A
+// LaunchScope brackets exactly one kernel launch: it records the start event
+// (when a trace is open), and on destruction the end event plus the launch
+// count.
+int trace_open_slot(const char* name, cudaStream_t s);
+void trace_close_slot(int slot, cudaStream_t s);
+
+struct LaunchScope {
+  int slot;
+  cudaStream_t stream;
+  LaunchScope(const char* name, cudaStream_t s) : slot(trace_open_slot(name, s)), stream(s) {}
+  ~LaunchScope() {
+    trace_close_slot(slot, stream);
+    count_launch();
+  }
+};
+
+}  // namespace ssd

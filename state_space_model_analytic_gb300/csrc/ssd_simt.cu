@@ -1,0 +1,841 @@
+// SIMT (CUDA-core, fp32 accumulate) kernels of the chunked SSD core.
+//
+// These kernels cover every shape the C ABI accepts, and are the path for
+// fp32 storage.  They follow the chunked form of the recurrence of
+// `ssd_forward_state_history_reference` / `ssd_backward_reference`
+// (burn_dragon_kernel 0.5.0, src/sequence/mamba2/backward.rs), exact in real
+// arithmetic: within chunk c with chunk-local cumulative log-decay
+// cs_i = sum_{r<=i} dt_r A_h,
+//   forward
+//     S_c      = sum_j exp(cs_last - cs_j) dt_j x_j B_j^T          (chunk state)
+//     H_c      = exp(cs_last) H_{c-1} + S_c                        (state pass)
+//     y_i      = sum_{j<=i} exp(cs_i - cs_j) dt_j (C_i.B_j) x_j
+//                + exp(cs_i) H_{c-1} C_i + D x_i                    (chunk scan)
+//   backward (g_c = dL/dH_c, L = sum dy*y)
+//     R_c      = sum_i exp(cs_i) dy_i C_i^T ; g_{c-1} = exp(cs_last[c]) g_c + R_c
+//     Gx_j     = sum_{i>=j} exp(cs_i-cs_j)(C_i.B_j) dy_i + exp(cs_last-cs_j) g_c B_j
+//     dx_j     = D dy_j + dt_j Gx_j ;  drive_j = x_j . Gx_j
+//     W_ij     = exp(cs_i-cs_j) dt_j (dy_i.x_j)          (i >= j)
+//     dC_i     = sum_h [ sum_j W_ij B_j + exp(cs_i) H_{c-1}^T dy_i ]
+//     dB_j     = sum_h [ sum_i W_ij C_i + exp(cs_last-cs_j) dt_j g_c^T x_j ]
+//     dcs_i    = sum_{j<i} M_ij - sum_{k>i} M_ki + exp(cs_i) dy_i.(H_{c-1} C_i) - e_i
+//                (+ sum_j e_j + exp(cs_last) <g_c, H_{c-1}> at i = Q-1),
+//       with M_ij = W_ij (C_i.B_j), e_j = exp(cs_last-cs_j) dt_j x_j.(g_c B_j)
+//     da_j     = sum_{i>=j} dcs_i ; ddt_j = drive_j + A da_j ; dA = sum dt da
+//     dD       = sum dy.x
+// Masked entries (i < j) never evaluate exp: the exponent is formed only for
+// i >= j, where it is <= 0 because dt >= 0 and A <= 0.
+#include <algorithm>
+
+#include "ssd_common.cuh"
+#include "ssd_internal.h"
+
+namespace ssd {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kOutPerSlice = 8192;  // outputs of one chunk-outer-product CTA
+
+struct Dev {
+  int B, T, H, P, N, G, Q, nc, hpg;
+};
+
+Dev dev_of(const Problem& p) { return Dev{p.B, p.T, p.H, p.P, p.N, p.G, p.Q, p.nc, p.hpg}; }
+
+// s_cs[i] = chunk-local inclusive cumsum of dt*A, s_dt[i] = dt; ends synced.
+__device__ __forceinline__ void load_chunk_decay(const Dev& d, const float* __restrict__ dt,
+                                                 const float* __restrict__ A, int b, int c, int h,
+                                                 float* s_cs, float* s_dt, float* scratch) {
+  const int tid = threadIdx.x;
+  float dtv = 0.f, a = 0.f;
+  if (tid < d.Q) {
+    dtv = dt[((size_t)b * d.T + (size_t)c * d.Q + tid) * d.H + h];
+    a = dtv * A[h];
+  }
+  const float cs = block_inclusive_scan(a, scratch);
+  if (tid < d.Q) {
+    s_cs[tid] = cs;
+    s_dt[tid] = dtv;
+  }
+  __syncthreads();
+}
+
+// ---------------------------------------------------------------------------
+// Chunk outer product: out[b][c][h] = sum_j w_j u_j (outer) v_j  ([P][N]).
+// MODE 0 (forward chunk state):  u = x, v = B, w_j = exp(cs_last - cs_j) dt_j
+// MODE 1 (backward chunk dstate): u = dy, v = C, w_j = exp(cs_j)
+// Both write cs_last[b][h][c].
+template <typename TIO, int MODE>
+__global__ void __launch_bounds__(kThreads)
+k_chunk_outer(Dev d, const TIO* __restrict__ u, const TIO* __restrict__ v,
+              const float* __restrict__ dt, const float* __restrict__ A, float* __restrict__ out,
+              float* __restrict__ cs_last, int nslice) {
+  extern __shared__ float sm[];
+  __shared__ float scratch[kThreads / 32];
+  const int c = blockIdx.x, h = blockIdx.y;
+  const int b = blockIdx.z / nslice, slice = blockIdx.z % nslice;
+  const int g = h / d.hpg, P = d.P, N = d.N, Q = d.Q, tid = threadIdx.x;
+  float* s_cs = sm;
+  float* s_dt = s_cs + Q;
+  float* s_w = s_dt + Q;
+  float* s_u = s_w + Q;       // [32][P]
+  float* s_v = s_u + 32 * P;  // [32][N]
+  load_chunk_decay(d, dt, A, b, c, h, s_cs, s_dt, scratch);
+  const float last = s_cs[Q - 1];
+  if (tid < Q) s_w[tid] = (MODE == 0) ? expf(last - s_cs[tid]) * s_dt[tid] : expf(s_cs[tid]);
+  if (tid == 0 && slice == 0) cs_last[((size_t)b * d.H + h) * d.nc + c] = last;
+
+  const int PN = P * N, o0 = slice * kOutPerSlice;
+  constexpr int K = kOutPerSlice / kThreads;
+  float acc[K];
+#pragma unroll
+  for (int k = 0; k < K; ++k) acc[k] = 0.f;
+  const size_t tok0 = (size_t)b * d.T + (size_t)c * Q;
+  for (int j0 = 0; j0 < Q; j0 += 32) {
+    const int jn = min(32, Q - j0);
+    __syncthreads();
+    for (int e = tid; e < jn * P; e += kThreads) {
+      const int jj = e / P, pp = e - jj * P;
+      s_u[e] = s_w[j0 + jj] * to_f32(u[((tok0 + j0 + jj) * d.H + h) * P + pp]);
+    }
+    for (int e = tid; e < jn * N; e += kThreads) {
+      const int jj = e / N, nn = e - jj * N;
+      s_v[e] = to_f32(v[((tok0 + j0 + jj) * d.G + g) * N + nn]);
+    }
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+      const int o = o0 + tid + k * kThreads;
+      if (o < PN) {
+        const int pp = o / N, nn = o - pp * N;
+        float a = acc[k];
+        for (int jj = 0; jj < jn; ++jj) a = fmaf(s_u[jj * P + pp], s_v[jj * N + nn], a);
+        acc[k] = a;
+      }
+    }
+  }
+  float* dst = out + (((size_t)b * d.nc + c) * d.H + h) * (size_t)PN;
+#pragma unroll
+  for (int k = 0; k < K; ++k) {
+    const int o = o0 + tid + k * kThreads;
+    if (o < PN) dst[o] = acc[k];
+  }
+}
+
+// Forward state pass, in place: hist[c] holds S_c on entry and H_{c-1} on exit.
+__global__ void __launch_bounds__(kThreads)
+k_state_pass_fwd(Dev d, float* __restrict__ hist, const float* __restrict__ cs_last,
+                 const float* __restrict__ h0, float* __restrict__ final_state) {
+  const int PN = d.P * d.N;
+  const int pn = blockIdx.x * blockDim.x + threadIdx.x;
+  const int h = blockIdx.y, b = blockIdx.z;
+  if (pn >= PN) return;
+  const size_t bh = (size_t)b * d.H + h;
+  float hc = h0 ? h0[bh * PN + pn] : 0.f;
+  const float* cl = cs_last + bh * d.nc;
+  float s_next = hist[(((size_t)b * d.nc + 0) * d.H + h) * PN + pn];
+  for (int c = 0; c < d.nc; ++c) {
+    const size_t idx = (((size_t)b * d.nc + c) * d.H + h) * PN + pn;
+    const float s = s_next;
+    if (c + 1 < d.nc) s_next = hist[idx + (size_t)d.H * PN];
+    hist[idx] = hc;
+    hc = fmaf(expf(cl[c]), hc, s);
+  }
+  if (final_state) final_state[bh * PN + pn] = hc;
+}
+
+// Backward state pass, in place: dstate[c] holds R_c on entry and g_c on exit.
+__global__ void __launch_bounds__(kThreads)
+k_state_pass_bwd(Dev d, float* __restrict__ dstate, const float* __restrict__ cs_last,
+                 float* __restrict__ dh0) {
+  const int PN = d.P * d.N;
+  const int pn = blockIdx.x * blockDim.x + threadIdx.x;
+  const int h = blockIdx.y, b = blockIdx.z;
+  if (pn >= PN) return;
+  const size_t bh = (size_t)b * d.H + h;
+  const float* cl = cs_last + bh * d.nc;
+  float gc = 0.f;
+  float r_next = dstate[(((size_t)b * d.nc + (d.nc - 1)) * d.H + h) * PN + pn];
+  for (int c = d.nc - 1; c >= 0; --c) {
+    const size_t idx = (((size_t)b * d.nc + c) * d.H + h) * PN + pn;
+    const float r = r_next;
+    if (c > 0) r_next = dstate[idx - (size_t)d.H * PN];
+    dstate[idx] = gc;
+    gc = fmaf(expf(cl[c]), gc, r);
+  }
+  if (dh0) dh0[bh * PN + pn] = gc;
+}
+
+// ---------------------------------------------------------------------------
+// Forward chunk scan: one CTA per (b, chunk, head, row tile of TQ rows).
+template <typename TIO, int TQ>
+__global__ void __launch_bounds__(kThreads)
+k_fwd_scan(Dev d, const TIO* __restrict__ x, const float* __restrict__ dt,
+           const float* __restrict__ A, const TIO* __restrict__ Bm, const TIO* __restrict__ Cm,
+           const float* __restrict__ D, const float* __restrict__ hist, TIO* __restrict__ y) {
+  extern __shared__ float sm[];
+  __shared__ float scratch[kThreads / 32];
+  const int nit = d.Q / TQ;
+  const int c = blockIdx.x / nit, it = blockIdx.x % nit, h = blockIdx.y, b = blockIdx.z;
+  const int g = h / d.hpg, P = d.P, N = d.N, Q = d.Q, tid = threadIdx.x;
+  const int LN = N + 1, LT = TQ + 1;
+  float* s_cs = sm;
+  float* s_dt = s_cs + Q;
+  float* s_C = s_dt + Q;         // [TQ][LN]
+  float* s_B = s_C + TQ * LN;    // [TQ][LN]
+  float* s_X = s_B + TQ * LN;    // [TQ][P]
+  float* s_M = s_X + TQ * P;     // [TQ][LT]
+  float* s_H = s_M + TQ * LT;    // [P][17]
+  load_chunk_decay(d, dt, A, b, c, h, s_cs, s_dt, scratch);
+  const int i0 = it * TQ;
+  const size_t tok0 = (size_t)b * d.T + (size_t)c * Q;
+  for (int e = tid; e < TQ * N; e += kThreads) {
+    const int ii = e / N, nn = e - ii * N;
+    s_C[ii * LN + nn] = to_f32(Cm[((tok0 + i0 + ii) * d.G + g) * N + nn]);
+  }
+  constexpr int KY = (TQ * 128) / kThreads;  // P <= 128
+  float acc[KY], st[KY];
+#pragma unroll
+  for (int k = 0; k < KY; ++k) { acc[k] = 0.f; st[k] = 0.f; }
+  const int TP = TQ * P;
+  for (int jt = 0; jt <= it; ++jt) {
+    const int j0 = jt * TQ;
+    __syncthreads();
+    for (int e = tid; e < TQ * N; e += kThreads) {
+      const int jj = e / N, nn = e - jj * N;
+      s_B[jj * LN + nn] = to_f32(Bm[((tok0 + j0 + jj) * d.G + g) * N + nn]);
+    }
+    for (int e = tid; e < TP; e += kThreads) {
+      const int jj = e / P, pp = e - jj * P;
+      s_X[e] = to_f32(x[((tok0 + j0 + jj) * d.H + h) * P + pp]);
+    }
+    __syncthreads();
+    for (int e = tid; e < TQ * TQ; e += kThreads) {
+      const int ii = e / TQ, jj = e - ii * TQ;
+      const int i = i0 + ii, j = j0 + jj;
+      float m = 0.f;
+      if (i >= j) {
+        float dot = 0.f;
+        for (int n = 0; n < N; ++n) dot = fmaf(s_C[ii * LN + n], s_B[jj * LN + n], dot);
+        m = dot * expf(s_cs[i] - s_cs[j]) * s_dt[j];
+      }
+      s_M[ii * LT + jj] = m;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < KY; ++k) {
+      const int o = tid + k * kThreads;
+      if (o < TP) {
+        const int ii = o / P, pp = o - ii * P;
+        float a = acc[k];
+#pragma unroll 8
+        for (int jj = 0; jj < TQ; ++jj) a = fmaf(s_M[ii * LT + jj], s_X[jj * P + pp], a);
+        acc[k] = a;
+      }
+    }
+  }
+  // inter-chunk term: exp(cs_i) * sum_n C_i[n] H_{c-1}[p][n]
+  const float* Hp = hist + (((size_t)b * d.nc + c) * d.H + h) * (size_t)(P * N);
+  for (int n0 = 0; n0 < N; n0 += 16) {
+    __syncthreads();
+    for (int e = tid; e < P * 16; e += kThreads) {
+      const int pp = e >> 4, nn = e & 15;
+      s_H[pp * 17 + nn] = Hp[(size_t)pp * N + n0 + nn];
+    }
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < KY; ++k) {
+      const int o = tid + k * kThreads;
+      if (o < TP) {
+        const int ii = o / P, pp = o - ii * P;
+        float a = st[k];
+#pragma unroll
+        for (int nn = 0; nn < 16; ++nn) a = fmaf(s_C[ii * LN + n0 + nn], s_H[pp * 17 + nn], a);
+        st[k] = a;
+      }
+    }
+  }
+  const float Dh = D[h];
+#pragma unroll
+  for (int k = 0; k < KY; ++k) {
+    const int o = tid + k * kThreads;
+    if (o < TP) {
+      const int ii = o / P, pp = o - ii * P;
+      const size_t gi = ((tok0 + i0 + ii) * d.H + h) * P + pp;
+      const float yv = acc[k] + expf(s_cs[i0 + ii]) * st[k] + Dh * to_f32(x[gi]);
+      y[gi] = from_f32<TIO>(yv);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Backward, column side: one CTA per (b, chunk, group, column tile j).
+// Writes dx, dB (summed over the group's heads in head order), and per
+// (token, head) the column sums of M, e_j and drive_j; per (chunk, tile,
+// head) the dD partial.
+template <typename TIO, int TQ>
+__global__ void __launch_bounds__(kThreads)
+k_bwd_col(Dev d, const TIO* __restrict__ x, const float* __restrict__ dt,
+          const float* __restrict__ A, const TIO* __restrict__ Bm, const TIO* __restrict__ Cm,
+          const float* __restrict__ D, const TIO* __restrict__ dy,
+          const float* __restrict__ dstate, TIO* __restrict__ dx, TIO* __restrict__ dB,
+          float* __restrict__ colsum, float* __restrict__ eout, float* __restrict__ drive,
+          float* __restrict__ dD_part) {
+  extern __shared__ float sm[];
+  __shared__ float scratch[kThreads / 32];
+  const int nit = d.Q / TQ;
+  const int c = blockIdx.x / nit, jt = blockIdx.x % nit, g = blockIdx.y, b = blockIdx.z;
+  const int P = d.P, N = d.N, Q = d.Q, tid = threadIdx.x;
+  const int LN = N + 1, LP = P + 1, LT = TQ + 1;
+  float* s_cs = sm;
+  float* s_dt = s_cs + Q;
+  float* s_CB = s_dt + Q;         // [Q][LT]   CB[i][j0+jj]
+  float* s_Bj = s_CB + Q * LT;    // [TQ][LN]
+  float* s_Ci = s_Bj + TQ * LN;   // [TQ][LN]
+  float* s_xj = s_Ci + TQ * LN;   // [TQ][LP]
+  float* s_dyj = s_xj + TQ * LP;  // [TQ][LP]
+  float* s_dyi = s_dyj + TQ * LP; // [TQ][LP]
+  float* s_gx = s_dyi + TQ * LP;  // [TQ][LP]
+  float* s_sb = s_gx + TQ * LP;   // [TQ][LP]
+  float* s_W = s_sb + TQ * LP;    // [TQ][LT]
+  float* s_L = s_W + TQ * LT;     // [TQ][LT]
+  float* s_g = s_L + TQ * LT;     // [P][LN]
+  float* s_dd = s_g + P * LN;     // [TQ]
+  const int j0 = jt * TQ;
+  const size_t tok0 = (size_t)b * d.T + (size_t)c * Q;
+
+  for (int e = tid; e < TQ * N; e += kThreads) {
+    const int jj = e / N, nn = e - jj * N;
+    s_Bj[jj * LN + nn] = to_f32(Bm[((tok0 + j0 + jj) * d.G + g) * N + nn]);
+  }
+  for (int it = jt; it < nit; ++it) {
+    const int i0 = it * TQ;
+    __syncthreads();
+    for (int e = tid; e < TQ * N; e += kThreads) {
+      const int ii = e / N, nn = e - ii * N;
+      s_Ci[ii * LN + nn] = to_f32(Cm[((tok0 + i0 + ii) * d.G + g) * N + nn]);
+    }
+    __syncthreads();
+    for (int e = tid; e < TQ * TQ; e += kThreads) {
+      const int ii = e / TQ, jj = e - ii * TQ;
+      float dot = 0.f;
+      for (int n = 0; n < N; ++n) dot = fmaf(s_Ci[ii * LN + n], s_Bj[jj * LN + n], dot);
+      s_CB[(i0 + ii) * LT + jj] = dot;
+    }
+  }
+
+  constexpr int KB = (TQ * 256) / kThreads;  // N <= 256
+  constexpr int KG = (TQ * 128) / kThreads;  // P <= 128
+  float dBacc[KB];
+#pragma unroll
+  for (int k = 0; k < KB; ++k) dBacc[k] = 0.f;
+  const int TN = TQ * N, TP = TQ * P;
+
+  for (int hh = 0; hh < d.hpg; ++hh) {
+    const int h = g * d.hpg + hh;
+    __syncthreads();
+    load_chunk_decay(d, dt, A, b, c, h, s_cs, s_dt, scratch);
+    for (int e = tid; e < TP; e += kThreads) {
+      const int jj = e / P, pp = e - jj * P;
+      const size_t gi = ((tok0 + j0 + jj) * d.H + h) * P + pp;
+      s_xj[jj * LP + pp] = to_f32(x[gi]);
+      s_dyj[jj * LP + pp] = to_f32(dy[gi]);
+    }
+    float gx[KG];
+#pragma unroll
+    for (int k = 0; k < KG; ++k) gx[k] = 0.f;
+    float colacc = 0.f;
+    for (int it = jt; it < nit; ++it) {
+      const int i0 = it * TQ;
+      __syncthreads();
+      for (int e = tid; e < TP; e += kThreads) {
+        const int ii = e / P, pp = e - ii * P;
+        s_dyi[ii * LP + pp] = to_f32(dy[((tok0 + i0 + ii) * d.H + h) * P + pp]);
+      }
+      for (int e = tid; e < TN; e += kThreads) {
+        const int ii = e / N, nn = e - ii * N;
+        s_Ci[ii * LN + nn] = to_f32(Cm[((tok0 + i0 + ii) * d.G + g) * N + nn]);
+      }
+      __syncthreads();
+      for (int e = tid; e < TQ * TQ; e += kThreads) {
+        const int ii = e / TQ, jj = e - ii * TQ;
+        const int i = i0 + ii, j = j0 + jj;
+        float w = 0.f, l = 0.f;
+        if (i >= j) {
+          const float dec = expf(s_cs[i] - s_cs[j]);
+          float dot = 0.f;
+          for (int p = 0; p < P; ++p) dot = fmaf(s_dyi[ii * LP + p], s_xj[jj * LP + p], dot);
+          w = dec * s_dt[j] * dot;
+          l = dec * s_CB[i * LT + jj];
+        }
+        s_W[ii * LT + jj] = w;
+        s_L[ii * LT + jj] = l;
+      }
+      __syncthreads();
+      if (tid < TQ) {
+        const int j = j0 + tid;
+        for (int ii = 0; ii < TQ; ++ii)
+          if (i0 + ii > j) colacc = fmaf(s_W[ii * LT + tid], s_CB[(i0 + ii) * LT + tid], colacc);
+      }
+#pragma unroll
+      for (int k = 0; k < KG; ++k) {
+        const int o = tid + k * kThreads;
+        if (o < TP) {
+          const int jj = o / P, pp = o - jj * P;
+          float a = gx[k];
+          for (int ii = 0; ii < TQ; ++ii) a = fmaf(s_L[ii * LT + jj], s_dyi[ii * LP + pp], a);
+          gx[k] = a;
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < KB; ++k) {
+        const int o = tid + k * kThreads;
+        if (o < TN) {
+          const int jj = o / N, nn = o - jj * N;
+          float a = dBacc[k];
+          for (int ii = 0; ii < TQ; ++ii) a = fmaf(s_W[ii * LT + jj], s_Ci[ii * LN + nn], a);
+          dBacc[k] = a;
+        }
+      }
+    }
+    // state terms with g_c = dL/dH_c
+    __syncthreads();
+    const float* gp = dstate + (((size_t)b * d.nc + c) * d.H + h) * (size_t)(P * N);
+    for (int e = tid; e < P * N; e += kThreads) {
+      const int pp = e / N, nn = e - pp * N;
+      s_g[pp * LN + nn] = gp[e];
+    }
+    __syncthreads();
+    const float cl = s_cs[Q - 1];
+    const float Dh = D[h];
+#pragma unroll
+    for (int k = 0; k < KG; ++k) {
+      const int o = tid + k * kThreads;
+      if (o < TP) {
+        const int jj = o / P, pp = o - jj * P;
+        float sb = 0.f;
+        for (int n = 0; n < N; ++n) sb = fmaf(s_Bj[jj * LN + n], s_g[pp * LN + n], sb);
+        const int j = j0 + jj;
+        const float gxv = gx[k] + expf(cl - s_cs[j]) * sb;
+        s_sb[jj * LP + pp] = sb;
+        s_gx[jj * LP + pp] = gxv;
+        const size_t gi = ((tok0 + j) * d.H + h) * P + pp;
+        dx[gi] = from_f32<TIO>(Dh * s_dyj[jj * LP + pp] + s_dt[j] * gxv);
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < KB; ++k) {
+      const int o = tid + k * kThreads;
+      if (o < TN) {
+        const int jj = o / N, nn = o - jj * N;
+        const int j = j0 + jj;
+        float a = 0.f;
+        for (int p = 0; p < P; ++p) a = fmaf(s_xj[jj * LP + p], s_g[p * LN + nn], a);
+        dBacc[k] = fmaf(expf(cl - s_cs[j]) * s_dt[j], a, dBacc[k]);
+      }
+    }
+    __syncthreads();
+    if (tid < TQ) {
+      const int jj = tid, j = j0 + jj;
+      float dr = 0.f, xs = 0.f, dd = 0.f;
+      for (int p = 0; p < P; ++p) {
+        const float xv = s_xj[jj * LP + p];
+        dr = fmaf(xv, s_gx[jj * LP + p], dr);
+        xs = fmaf(xv, s_sb[jj * LP + p], xs);
+        dd = fmaf(xv, s_dyj[jj * LP + p], dd);
+      }
+      const size_t th = (tok0 + j) * d.H + h;
+      colsum[th] = colacc;
+      eout[th] = expf(cl - s_cs[j]) * s_dt[j] * xs;
+      drive[th] = dr;
+      s_dd[jj] = dd;
+    }
+    __syncthreads();
+    if (tid == 0) {
+      float s = 0.f;
+      for (int jj = 0; jj < TQ; ++jj) s += s_dd[jj];
+      dD_part[(((size_t)b * d.nc + c) * nit + jt) * d.H + h] = s;
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < KB; ++k) {
+    const int o = tid + k * kThreads;
+    if (o < TN) {
+      const int jj = o / N, nn = o - jj * N;
+      dB[((tok0 + j0 + jj) * d.G + g) * N + nn] = from_f32<TIO>(dBacc[k]);
+    }
+  }
+}
+
+// Backward, row side: one CTA per (b, chunk, group, row tile i).  Writes dC
+// (summed over the group's heads in head order) and per (token, head) the
+// strict row sums of M and the state-in term of dcs.
+template <typename TIO, int TQ>
+__global__ void __launch_bounds__(kThreads)
+k_bwd_row(Dev d, const TIO* __restrict__ x, const float* __restrict__ dt,
+          const float* __restrict__ A, const TIO* __restrict__ Bm, const TIO* __restrict__ Cm,
+          const TIO* __restrict__ dy, const float* __restrict__ hist, TIO* __restrict__ dC,
+          float* __restrict__ rowsum, float* __restrict__ statein) {
+  extern __shared__ float sm[];
+  __shared__ float scratch[kThreads / 32];
+  const int nit = d.Q / TQ;
+  const int c = blockIdx.x / nit, it = blockIdx.x % nit, g = blockIdx.y, b = blockIdx.z;
+  const int P = d.P, N = d.N, Q = d.Q, tid = threadIdx.x;
+  const int LN = N + 1, LP = P + 1, LT = TQ + 1, LQ = Q + 1;
+  float* s_cs = sm;
+  float* s_dt = s_cs + Q;
+  float* s_Ci = s_dt + Q;          // [TQ][LN]
+  float* s_Bj = s_Ci + TQ * LN;    // [TQ][LN]
+  float* s_CB = s_Bj + TQ * LN;    // [TQ][LQ]   CB[i0+ii][j]
+  float* s_xj = s_CB + TQ * LQ;    // [TQ][LP]
+  float* s_dyi = s_xj + TQ * LP;   // [TQ][LP]
+  float* s_hc = s_dyi + TQ * LP;   // [TQ][LP]
+  float* s_W = s_hc + TQ * LP;     // [TQ][LT]
+  float* s_H = s_W + TQ * LT;      // [P][LN]
+  const int i0 = it * TQ;
+  const size_t tok0 = (size_t)b * d.T + (size_t)c * Q;
+  const int TN = TQ * N, TP = TQ * P;
+
+  for (int e = tid; e < TN; e += kThreads) {
+    const int ii = e / N, nn = e - ii * N;
+    s_Ci[ii * LN + nn] = to_f32(Cm[((tok0 + i0 + ii) * d.G + g) * N + nn]);
+  }
+  for (int jt = 0; jt <= it; ++jt) {
+    const int j0 = jt * TQ;
+    __syncthreads();
+    for (int e = tid; e < TN; e += kThreads) {
+      const int jj = e / N, nn = e - jj * N;
+      s_Bj[jj * LN + nn] = to_f32(Bm[((tok0 + j0 + jj) * d.G + g) * N + nn]);
+    }
+    __syncthreads();
+    for (int e = tid; e < TQ * TQ; e += kThreads) {
+      const int ii = e / TQ, jj = e - ii * TQ;
+      float dot = 0.f;
+      for (int n = 0; n < N; ++n) dot = fmaf(s_Ci[ii * LN + n], s_Bj[jj * LN + n], dot);
+      s_CB[ii * LQ + j0 + jj] = dot;
+    }
+  }
+
+  constexpr int KB = (TQ * 256) / kThreads;
+  float dCacc[KB];
+#pragma unroll
+  for (int k = 0; k < KB; ++k) dCacc[k] = 0.f;
+
+  for (int hh = 0; hh < d.hpg; ++hh) {
+    const int h = g * d.hpg + hh;
+    __syncthreads();
+    load_chunk_decay(d, dt, A, b, c, h, s_cs, s_dt, scratch);
+    for (int e = tid; e < TP; e += kThreads) {
+      const int ii = e / P, pp = e - ii * P;
+      s_dyi[ii * LP + pp] = to_f32(dy[((tok0 + i0 + ii) * d.H + h) * P + pp]);
+    }
+    float rowacc = 0.f;
+    for (int jt = 0; jt <= it; ++jt) {
+      const int j0 = jt * TQ;
+      __syncthreads();
+      for (int e = tid; e < TP; e += kThreads) {
+        const int jj = e / P, pp = e - jj * P;
+        s_xj[jj * LP + pp] = to_f32(x[((tok0 + j0 + jj) * d.H + h) * P + pp]);
+      }
+      for (int e = tid; e < TN; e += kThreads) {
+        const int jj = e / N, nn = e - jj * N;
+        s_Bj[jj * LN + nn] = to_f32(Bm[((tok0 + j0 + jj) * d.G + g) * N + nn]);
+      }
+      __syncthreads();
+      for (int e = tid; e < TQ * TQ; e += kThreads) {
+        const int ii = e / TQ, jj = e - ii * TQ;
+        const int i = i0 + ii, j = j0 + jj;
+        float w = 0.f;
+        if (i >= j) {
+          float dot = 0.f;
+          for (int p = 0; p < P; ++p) dot = fmaf(s_dyi[ii * LP + p], s_xj[jj * LP + p], dot);
+          w = expf(s_cs[i] - s_cs[j]) * s_dt[j] * dot;
+        }
+        s_W[ii * LT + jj] = w;
+      }
+      __syncthreads();
+      if (tid < TQ) {
+        const int i = i0 + tid;
+        for (int jj = 0; jj < TQ; ++jj)
+          if (i > j0 + jj) rowacc = fmaf(s_W[tid * LT + jj], s_CB[tid * LQ + j0 + jj], rowacc);
+      }
+#pragma unroll
+      for (int k = 0; k < KB; ++k) {
+        const int o = tid + k * kThreads;
+        if (o < TN) {
+          const int ii = o / N, nn = o - ii * N;
+          float a = dCacc[k];
+          for (int jj = 0; jj < TQ; ++jj) a = fmaf(s_W[ii * LT + jj], s_Bj[jj * LN + nn], a);
+          dCacc[k] = a;
+        }
+      }
+    }
+    // state-in terms with H_{c-1}
+    __syncthreads();
+    const float* hp = hist + (((size_t)b * d.nc + c) * d.H + h) * (size_t)(P * N);
+    for (int e = tid; e < P * N; e += kThreads) {
+      const int pp = e / N, nn = e - pp * N;
+      s_H[pp * LN + nn] = hp[e];
+    }
+    __syncthreads();
+    for (int e = tid; e < TP; e += kThreads) {
+      const int ii = e / P, pp = e - ii * P;
+      float a = 0.f;
+      for (int n = 0; n < N; ++n) a = fmaf(s_H[pp * LN + n], s_Ci[ii * LN + n], a);
+      s_hc[ii * LP + pp] = a;
+    }
+#pragma unroll
+    for (int k = 0; k < KB; ++k) {
+      const int o = tid + k * kThreads;
+      if (o < TN) {
+        const int ii = o / N, nn = o - ii * N;
+        float a = 0.f;
+        for (int p = 0; p < P; ++p) a = fmaf(s_dyi[ii * LP + p], s_H[p * LN + nn], a);
+        dCacc[k] = fmaf(expf(s_cs[i0 + ii]), a, dCacc[k]);
+      }
+    }
+    __syncthreads();
+    if (tid < TQ) {
+      float a = 0.f;
+      for (int p = 0; p < P; ++p) a = fmaf(s_dyi[tid * LP + p], s_hc[tid * LP + p], a);
+      const size_t th = (tok0 + i0 + tid) * d.H + h;
+      rowsum[th] = rowacc;
+      statein[th] = expf(s_cs[i0 + tid]) * a;
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < KB; ++k) {
+    const int o = tid + k * kThreads;
+    if (o < TN) {
+      const int ii = o / N, nn = o - ii * N;
+      dC[((tok0 + i0 + ii) * d.G + g) * N + nn] = from_f32<TIO>(dCacc[k]);
+    }
+  }
+}
+
+// Backward, per (b, chunk, head): assemble dcs, reverse cumsum to da, ddt and
+// the dA partial of the chunk.
+__global__ void __launch_bounds__(kThreads)
+k_bwd_dt(Dev d, const float* __restrict__ dt, const float* __restrict__ A,
+         const float* __restrict__ hist, const float* __restrict__ dstate,
+         const float* __restrict__ rowsum, const float* __restrict__ colsum,
+         const float* __restrict__ statein, const float* __restrict__ eout,
+         const float* __restrict__ drive, float* __restrict__ ddt, float* __restrict__ dA_part) {
+  __shared__ float scratch[kThreads / 32];
+  __shared__ float s_cs[256], s_dt[256], s_v[256];
+  const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z, tid = threadIdx.x;
+  const int Q = d.Q, PN = d.P * d.N;
+  load_chunk_decay(d, dt, A, b, c, h, s_cs, s_dt, scratch);
+  const size_t off = (((size_t)b * d.nc + c) * d.H + h) * (size_t)PN;
+  float part = 0.f;
+  for (int e = tid; e < PN; e += kThreads) part = fmaf(dstate[off + e], hist[off + e], part);
+  const float gh = block_sum(part, scratch);
+  const size_t tok0 = (size_t)b * d.T + (size_t)c * Q;
+  const float ev = tid < Q ? eout[(tok0 + tid) * d.H + h] : 0.f;
+  const float esum = block_sum(ev, scratch);
+  if (tid < Q) {
+    const size_t th = (tok0 + tid) * d.H + h;
+    float dcs = rowsum[th] - colsum[th] + statein[th] - ev;
+    if (tid == Q - 1) dcs += esum + expf(s_cs[Q - 1]) * gh;
+    s_v[tid] = dcs;
+  }
+  __syncthreads();
+  // da_j = sum_{i >= j} dcs_i : inclusive scan over the reversed index
+  const float v = tid < Q ? s_v[Q - 1 - tid] : 0.f;
+  const float da = block_inclusive_scan(v, scratch);
+  float contrib = 0.f;
+  if (tid < Q) {
+    const int j = Q - 1 - tid;
+    const size_t th = (tok0 + j) * d.H + h;
+    ddt[th] = drive[th] + A[h] * da;
+    contrib = s_dt[j] * da;
+  }
+  const float s = block_sum(contrib, scratch);
+  if (tid == 0) dA_part[((size_t)b * d.nc + c) * d.H + h] = s;
+}
+
+// dA[h], dD[h]: fixed-order sums of the per-chunk partials (one warp per head).
+__global__ void k_reduce_heads(int H, int n_a, int n_d, const float* __restrict__ dA_part,
+                               const float* __restrict__ dD_part, float* __restrict__ dA,
+                               float* __restrict__ dD) {
+  const int h = blockIdx.x, lane = threadIdx.x;
+  float sa = 0.f, sd = 0.f;
+  for (int k = lane; k < n_a; k += 32) sa += dA_part[(size_t)k * H + h];
+  for (int k = lane; k < n_d; k += 32) sd += dD_part[(size_t)k * H + h];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    sa += __shfl_xor_sync(0xffffffffu, sa, o);
+    sd += __shfl_xor_sync(0xffffffffu, sd, o);
+  }
+  if (lane == 0) {
+    dA[h] = sa;
+    dD[h] = sd;
+  }
+}
+
+// ---------------------------------------------------------------------------
+size_t outer_smem(const Problem& p) { return sizeof(float) * (3 * p.Q + 32 * p.P + 32 * p.N); }
+
+template <int TQ>
+size_t scan_smem(const Problem& p) {
+  return sizeof(float) *
+         (2 * p.Q + 2 * TQ * (p.N + 1) + TQ * p.P + TQ * (TQ + 1) + p.P * 17);
+}
+template <int TQ>
+size_t col_smem(const Problem& p) {
+  return sizeof(float) * (2 * p.Q + p.Q * (TQ + 1) + 2 * TQ * (p.N + 1) + 5 * TQ * (p.P + 1) +
+                          2 * TQ * (TQ + 1) + p.P * (p.N + 1) + TQ);
+}
+template <int TQ>
+size_t row_smem(const Problem& p) {
+  return sizeof(float) * (2 * p.Q + 2 * TQ * (p.N + 1) + TQ * (p.Q + 1) + 3 * TQ * (p.P + 1) +
+                          TQ * (TQ + 1) + p.P * (p.N + 1));
+}
+
+constexpr size_t kSmemLimit = 227 * 1024;
+
+template <typename K>
+cudaError_t set_smem(K kernel, size_t bytes) {
+  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+}
+
+int pick_tq(const Problem& p) {
+  if (p.Q < 32) return 16;
+  if (col_smem<32>(p) <= kSmemLimit && row_smem<32>(p) <= kSmemLimit) return 32;
+  return 16;
+}
+
+template <typename TIO>
+cudaError_t forward_states_t(const Problem& p, float* hist, float* cs_last) {
+  const Dev d = dev_of(p);
+  const int nslice = (p.P * p.N + kOutPerSlice - 1) / kOutPerSlice;
+  auto kern = k_chunk_outer<TIO, 0>;
+  const size_t sm = outer_smem(p);
+  cudaError_t e = set_smem(kern, sm);
+  if (e != cudaSuccess) return e;
+  {
+    LaunchScope ls_("chunk_state_simt", p.stream);
+    kern<<<dim3(p.nc, p.H, p.B * nslice), kThreads, sm, p.stream>>>(
+        d, (const TIO*)p.x, (const TIO*)p.Bm, p.dt, p.A, hist, cs_last, nslice);
+  }
+  return cudaGetLastError();
+}
+
+template <typename TIO, int TQ>
+cudaError_t forward_scan_t(const Problem& p) {
+  const Dev d = dev_of(p);
+  auto kern = k_fwd_scan<TIO, TQ>;
+  const size_t sm = scan_smem<TQ>(p);
+  cudaError_t e = set_smem(kern, sm);
+  if (e != cudaSuccess) return e;
+  {
+    LaunchScope ls_("chunk_scan_simt", p.stream);
+    kern<<<dim3(p.nc * (p.Q / TQ), p.H, p.B), kThreads, sm, p.stream>>>(
+        d, (const TIO*)p.x, p.dt, p.A, (const TIO*)p.Bm, (const TIO*)p.Cm, p.D, p.hist, (TIO*)p.y);
+  }
+  return cudaGetLastError();
+}
+
+template <typename TIO, int TQ>
+cudaError_t backward_t(const Problem& p) {
+  const Dev d = dev_of(p);
+  cudaError_t e;
+  // R_c, then the reverse state pass (g_c and dh0)
+  {
+    const int nslice = (p.P * p.N + kOutPerSlice - 1) / kOutPerSlice;
+    auto kern = k_chunk_outer<TIO, 1>;
+    const size_t sm = outer_smem(p);
+    if ((e = set_smem(kern, sm)) != cudaSuccess) return e;
+    {
+      LaunchScope ls_("chunk_dstate_simt", p.stream);
+      kern<<<dim3(p.nc, p.H, p.B * nslice), kThreads, sm, p.stream>>>(
+          d, (const TIO*)p.dy, (const TIO*)p.Cm, p.dt, p.A, p.dstate, p.cs_last, nslice);
+    }
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    {
+      LaunchScope ls_("state_pass_bwd", p.stream);
+      k_state_pass_bwd<<<dim3((p.P * p.N + kThreads - 1) / kThreads, p.H, p.B), kThreads, 0,
+                         p.stream>>>(d, p.dstate, p.cs_last, p.dh0);
+    }
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  const int nit = p.Q / TQ;
+  {
+    auto kern = k_bwd_col<TIO, TQ>;
+    const size_t sm = col_smem<TQ>(p);
+    if ((e = set_smem(kern, sm)) != cudaSuccess) return e;
+    {
+      LaunchScope ls_("bwd_col_simt", p.stream);
+      kern<<<dim3(p.nc * nit, p.G, p.B), kThreads, sm, p.stream>>>(
+          d, (const TIO*)p.x, p.dt, p.A, (const TIO*)p.Bm, (const TIO*)p.Cm, p.D,
+          (const TIO*)p.dy, p.dstate, (TIO*)p.dx, (TIO*)p.dB, p.colsum, p.eout, p.drive,
+          p.dD_part);
+    }
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  {
+    auto kern = k_bwd_row<TIO, TQ>;
+    const size_t sm = row_smem<TQ>(p);
+    if ((e = set_smem(kern, sm)) != cudaSuccess) return e;
+    {
+      LaunchScope ls_("bwd_row_simt", p.stream);
+      kern<<<dim3(p.nc * nit, p.G, p.B), kThreads, sm, p.stream>>>(
+          d, (const TIO*)p.x, p.dt, p.A, (const TIO*)p.Bm, (const TIO*)p.Cm, (const TIO*)p.dy,
+          p.hist, (TIO*)p.dC, p.rowsum, p.statein);
+    }
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  {
+    LaunchScope ls_("bwd_dt", p.stream);
+    k_bwd_dt<<<dim3(p.nc, p.H, p.B), kThreads, 0, p.stream>>>(
+        d, p.dt, p.A, p.hist, p.dstate, p.rowsum, p.colsum, p.statein, p.eout, p.drive, p.ddt,
+        p.dA_part);
+  }
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  {
+    LaunchScope ls_("reduce_heads", p.stream);
+    k_reduce_heads<<<p.H, 32, 0, p.stream>>>(p.H, p.B * p.nc, p.B * p.nc * nit, p.dA_part,
+                                             p.dD_part, p.dA, p.dD);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t simt_forward_states(const Problem& p, float* hist, float* cs_last) {
+  return p.bf16 ? forward_states_t<__nv_bfloat16>(p, hist, cs_last)
+                : forward_states_t<float>(p, hist, cs_last);
+}
+
+cudaError_t simt_state_pass_fwd(const Problem& p, float* hist, const float* cs_last) {
+  const Dev d = dev_of(p);
+  {
+    LaunchScope ls_("state_pass_fwd", p.stream);
+    k_state_pass_fwd<<<dim3((p.P * p.N + kThreads - 1) / kThreads, p.H, p.B), kThreads, 0,
+                       p.stream>>>(d, hist, cs_last, p.h0, p.final_state);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t simt_forward_scan(const Problem& p) {
+  const int tq = pick_tq(p);
+  if (p.bf16)
+    return tq == 32 ? forward_scan_t<__nv_bfloat16, 32>(p) : forward_scan_t<__nv_bfloat16, 16>(p);
+  return tq == 32 ? forward_scan_t<float, 32>(p) : forward_scan_t<float, 16>(p);
+}
+
+cudaError_t simt_backward(const Problem& p) {
+  const int tq = pick_tq(p);
+  if (p.bf16) return tq == 32 ? backward_t<__nv_bfloat16, 32>(p) : backward_t<__nv_bfloat16, 16>(p);
+  return tq == 32 ? backward_t<float, 32>(p) : backward_t<float, 16>(p);
+}
+
+size_t simt_smem_need(const Problem& p) {
+  const int tq = pick_tq(p);
+  if (tq == 32) return std::max({outer_smem(p), scan_smem<32>(p), col_smem<32>(p), row_smem<32>(p)});
+  return std::max({outer_smem(p), scan_smem<16>(p), col_smem<16>(p), row_smem<16>(p)});
+}
+
+int simt_row_tile(const Problem& p) { return pick_tq(p); }
+
+}  // namespace ssd

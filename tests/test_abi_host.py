@@ -1,0 +1,114 @@
+"""Host-side checks of the C ABI: the library builds for sm_103a, loads
+without a GPU, exports every entry point include/ssd.h declares, and rejects
+bad arguments before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from state_space_model_analytic_gb300 import _native as nat
+from state_space_model_analytic_gb300 import build as build_lib
+from state_space_model_analytic_gb300 import synth
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    build_lib()
+    return nat.lib()
+
+
+def declared_entry_points():
+    src = open(os.path.join(ROOT, "include", "ssd.h")).read()
+    return re.findall(r"SSD_API\s+[\w\s\*]+?\b(ssd_\w+)\s*\(", src)
+
+
+def test_exports_every_declared_symbol(L):
+    names = declared_entry_points()
+    assert set(names) == set(nat.EXPORTS), names
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def dims(**kw):
+    base = dict(batch=2, seqlen=64, nheads=4, headdim=16, dstate=16, ngroups=2, chunk=16,
+                bf16=False)
+    base.update(kw)
+    return nat.make_dims(**base)
+
+
+def test_workspace_sizes(L):
+    d = dims()
+    f, b1, b2 = (L.ssd_workspace_bytes(d, w) for w in (0, 1, 2))
+    states = 2 * 4 * 4 * 16 * 16 * 4
+    assert f >= states and b1 >= states and b2 >= b1 + states
+    assert L.ssd_workspace_bytes(d, 3) == 0
+    for i in range(5):
+        dd = synth.config_dims(i)
+        d = nat.make_dims(dd.batch, dd.seqlen, dd.nheads, dd.headdim, dd.dstate, dd.ngroups,
+                          dd.chunk, dd.dtype == "bf16")
+        assert L.ssd_workspace_bytes(d, 0) > 0 and L.ssd_kernel_path(d) in (0, 1)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(nheads=3), nat.SSD_ERR_INVALID_ARG),      # H % G
+    (dict(batch=0), nat.SSD_ERR_INVALID_ARG),
+    (dict(chunk=48), nat.SSD_ERR_UNSUPPORTED),
+    (dict(seqlen=40), nat.SSD_ERR_UNSUPPORTED),    # T % Q
+    (dict(headdim=24), nat.SSD_ERR_UNSUPPORTED),
+    (dict(dstate=272), nat.SSD_ERR_UNSUPPORTED),
+    (dict(headdim=128, dstate=256), nat.SSD_ERR_UNSUPPORTED),
+])
+def test_rejects_bad_dims(L, kw, code):
+    d = dims(**kw)
+    fake = ctypes.c_void_p(1 << 20)
+    rc = L.ssd_forward(d, fake, fake, fake, fake, fake, fake, None, fake, None, None, fake,
+                       1 << 30, None)
+    assert rc == code, nat.last_error()
+    assert nat.last_error()
+    assert L.ssd_workspace_bytes(d, 0) == 0
+    assert L.ssd_kernel_path(d) == -1
+
+
+def test_rejects_null_misaligned_and_small_workspace(L):
+    d = dims()
+    f = ctypes.c_void_p(1 << 20)
+    ws = L.ssd_workspace_bytes(d, 0)
+    rc = L.ssd_forward(d, None, f, f, f, f, f, None, f, None, None, f, ws, None)
+    assert rc == nat.SSD_ERR_INVALID_ARG
+    bad = ctypes.c_void_p((1 << 20) + 4)
+    rc = L.ssd_forward(d, bad, f, f, f, f, f, None, f, None, None, f, ws, None)
+    assert rc == nat.SSD_ERR_ALIGNMENT
+    rc = L.ssd_forward(d, f, f, f, f, f, f, None, f, None, None, ctypes.c_void_p((1 << 20) + 16),
+                       ws, None)
+    assert rc == nat.SSD_ERR_ALIGNMENT
+    rc = L.ssd_forward(d, f, f, f, f, f, f, None, f, None, None, f, ws - 1, None)
+    assert rc == nat.SSD_ERR_INVALID_ARG and "workspace" in nat.last_error()
+    wsb = L.ssd_workspace_bytes(d, 1)
+    rc = L.ssd_backward(d, f, f, f, f, f, f, None, f, f, f, f, f, f, f, f, None, f, wsb - 1, None)
+    assert rc == nat.SSD_ERR_INVALID_ARG
+    # without a history the backward needs the larger workspace
+    rc = L.ssd_backward(d, f, f, f, f, f, f, None, f, None, f, f, f, f, f, f, None, f, wsb, None)
+    assert rc == nat.SSD_ERR_INVALID_ARG and "recomput" in nat.last_error()
+    rc = L.ssd_backward(d, f, f, f, f, f, f, None, None, f, f, f, f, f, f, f, None, f, wsb, None)
+    assert rc == nat.SSD_ERR_INVALID_ARG
+
+
+def test_reserved_and_dtype_fields(L):
+    d = dims()
+    d.reserved = 1
+    assert L.ssd_workspace_bytes(d, 0) == 0
+    d = dims()
+    d.dtype = 7
+    assert L.ssd_workspace_bytes(d, 0) == 0
+
+
+def test_cpu_tensors_rejected_by_front_end():
+    import torch
+    import state_space_model_analytic_gb300 as ssd
+    x = torch.zeros(1, 16, 2, 16)
+    with pytest.raises(ValueError, match="CUDA"):
+        ssd.forward(x, torch.zeros(1, 16, 2), torch.zeros(2), torch.zeros(1, 16, 1, 16),
+                    torch.zeros(1, 16, 1, 16), torch.zeros(2), chunk=16)

@@ -1,0 +1,156 @@
+"""GPU parity: the CUDA path through the C ABI against the float64 oracle.
+
+Small problems are compared element by element on every output; the five
+SSD-core workloads are run at full size in the same launch configuration as
+the benchmark and compared on one whole group (all batch rows, every head of
+the group), which the oracle computes exactly because groups are
+independent.
+"""
+import numpy as np
+import pytest
+
+from state_space_model_analytic_gb300 import synth
+
+from parity_util import (TOL, compare, group_slice, rel_err, run_gpu, run_oracle,
+                         slice_outputs, to_device)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from state_space_model_analytic_gb300 import build
+    build()
+
+
+def check_problem(dims, inp, history="given"):
+    gpu = run_gpu(dims, to_device(dims, inp), history)
+    ref = run_oracle(dims, inp)
+    errs, bad = compare(gpu, ref, TOL[dims.dtype])
+    assert not bad, f"{dims}: {errs}"
+    return errs
+
+
+SMALL = [
+    # (B, T, H, P, N, G, Q, dtype, h0, mode)
+    (1, 64, 2, 16, 16, 1, 16, "f32", False, "softplus"),
+    (2, 96, 4, 32, 16, 2, 32, "f32", True, "softplus"),
+    (1, 128, 3, 16, 48, 3, 64, "f32", True, "softplus"),
+    (2, 256, 2, 64, 64, 1, 128, "f32", True, "softplus"),
+    (1, 512, 2, 64, 128, 2, 256, "f32", True, "decay_span"),
+    (1, 256, 4, 64, 128, 1, 256, "bf16", False, "softplus"),
+    (2, 512, 4, 64, 128, 2, 256, "bf16", True, "decay_span"),
+    (1, 256, 2, 128, 128, 1, 128, "f32", True, "softplus"),
+    (1, 128, 2, 64, 256, 1, 64, "bf16", True, "softplus"),
+    (1, 32, 8, 16, 32, 8, 32, "f32", True, "softplus"),  # one chunk, G = H
+]
+
+
+@pytest.mark.parametrize("case", SMALL, ids=lambda c: "x".join(map(str, c[:7])) + c[7])
+def test_small_problems_every_output(case):
+    Bz, T, H, P, N, G, Q, dt_, h0, mode = case
+    dims = synth.Dims(Bz, T, H, P, N, G, Q, dt_)
+    inp = synth.make_inputs(dims, 7 + T + H, h0, mode)
+    check_problem(dims, inp)
+
+
+def test_modular_case_and_recompute_mode():
+    dims, inp = synth.modular_inputs(chunk=16)
+    e1 = check_problem(dims, inp, "given")
+    e2 = check_problem(dims, inp, "recompute")
+    assert e1 == e2
+
+
+def test_tiny_workload_config0_every_output():
+    dims, inp = synth.config_inputs(0)
+    check_problem(dims, inp)
+
+
+def test_history_given_or_recomputed_is_bitwise_equal_and_deterministic():
+    dims = synth.Dims(2, 512, 4, 64, 128, 2, 128, "bf16")
+    inp = synth.make_inputs(dims, 3, True, "softplus")
+    dev = to_device(dims, inp)
+    a = run_gpu(dims, dev, "given")
+    b = run_gpu(dims, dev, "recompute")
+    c = run_gpu(dims, dev, "given")
+    for k in a:
+        assert np.array_equal(a[k], b[k]), k
+        assert np.array_equal(a[k], c[k]), k
+
+
+def test_chunk_size_invariance():
+    base = synth.Dims(1, 512, 2, 64, 64, 1, 64, "f32")
+    inp = synth.make_inputs(base, 5, True, "softplus")
+    outs = {}
+    for q in (32, 64, 128, 256):
+        d = synth.Dims(1, 512, 2, 64, 64, 1, q, "f32")
+        outs[q] = run_gpu(d, to_device(d, inp))
+    for q in (32, 128, 256):
+        for k in ("y", "final_state", "dx", "ddt", "dA", "dB", "dC", "dD", "dh0"):
+            assert rel_err(outs[q][k], outs[64][k]) < 1e-4, (q, k)
+        # history at a coarser chunk is a subsample of the finer one
+    np.testing.assert_allclose(outs[128]["chunk_states"], outs[64]["chunk_states"][:, ::2],
+                               rtol=0, atol=1e-4 * np.abs(outs[64]["chunk_states"]).max())
+
+
+def test_A_zero_no_decay():
+    dims = synth.Dims(1, 256, 2, 32, 32, 1, 64, "f32")
+    inp = synth.make_inputs(dims, 9, True, "softplus")
+    inp["A"] = np.zeros_like(inp["A"])
+    check_problem(dims, inp)
+
+
+def test_outputs_stay_inside_their_buffers():
+    """Canary words after every output survive a forward + backward."""
+    import torch
+    import state_space_model_analytic_gb300 as ssd
+    dims = synth.Dims(1, 96, 3, 16, 32, 1, 32, "f32")
+    inp = synth.make_inputs(dims, 4, True, "softplus")
+    dev = to_device(dims, inp)
+    pad = 64
+    canary = -12345.0
+
+    def padded(shape, dtype=torch.float32):
+        n = int(np.prod(shape))
+        buf = torch.full((n + pad,), canary, dtype=dtype, device="cuda")
+        return buf, buf[:n].view(*shape)
+
+    bufs = {}
+    Bz, T, H, P, N, G, Q = 1, 96, 3, 16, 32, 1, 32
+    shapes = {"y": (Bz, T, H, P), "final_state": (Bz, H, P, N), "chunk_states": (Bz, T // Q, H, P, N),
+              "dx": (Bz, T, H, P), "ddt": (Bz, T, H), "dA": (H,), "dB": (Bz, T, G, N),
+              "dC": (Bz, T, G, N), "dD": (H,), "dh0": (Bz, H, P, N)}
+    views = {}
+    for k, s in shapes.items():
+        bufs[k], views[k] = padded(s)
+    y, fs, cs = ssd.forward(dev["x"], dev["dt"], dev["A"], dev["B"], dev["C"], dev["D"], dev["h0"],
+                            chunk=Q, out={"y": views["y"], "final_state": views["final_state"],
+                                          "chunk_states": views["chunk_states"]})
+    ssd.backward(dev["x"], dev["dt"], dev["A"], dev["B"], dev["C"], dev["D"], dev["h0"], dev["dy"],
+                 cs, chunk=Q, out={k: views[k] for k in ("dx", "ddt", "dA", "dB", "dC", "dD", "dh0")})
+    torch.cuda.synchronize()
+    for k, b in bufs.items():
+        tail = b[-pad:].cpu().numpy()
+        assert (tail == canary).all(), k
+
+
+FULL = [1, 2, 3, 4]
+
+
+@pytest.mark.parametrize("idx", FULL)
+def test_full_size_workload_one_group(idx):
+    """Full-size workload, benchmark launch configuration; the oracle
+    computes one whole group (last group) over every batch row."""
+    dims, inp = synth.config_inputs(idx)
+    gpu = run_gpu(dims, to_device(dims, inp))
+    g = dims.ngroups - 1
+    sdims, sub = group_slice(dims, inp, g)
+    ref = run_oracle(sdims, sub)
+    errs, bad = compare(slice_outputs(dims, gpu, g), ref, TOL[dims.dtype])
+    print(f"config {idx}: " + ", ".join(f"{k}={v:.2e}" for k, v in errs.items()))
+    assert not bad, errs
+    for v in gpu.values():
+        assert np.isfinite(v).all()

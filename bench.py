@@ -24,6 +24,8 @@ import sys
 import tempfile
 import time
 
+import numpy as np
+
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
@@ -187,28 +189,43 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------------------
-def oracle_sample_time(dims, inp, tokens, threads):
-    """Seconds of one oracle forward + backward on batch row 0, all heads,
-    the first `tokens` steps (a complete problem in its own right)."""
+def oracle_sample_time(dims, inp, rows, tokens, threads):
+    """Seconds of one oracle forward + backward on the first `rows` batch rows,
+    all heads, the first `tokens` steps (a complete problem in its own right)."""
     import oracle
-    sl = {k: (None if v is None else v) for k, v in inp.items()}
-    x = sl["x"][:1, :tokens]
-    dt = sl["dt"][:1, :tokens]
-    Bm = sl["B"][:1, :tokens]
-    Cm = sl["C"][:1, :tokens]
-    dy = sl["dy"][:1, :tokens]
-    h0 = None if sl["h0"] is None else sl["h0"][:1]
+    cut = lambda a: a[:rows, :tokens]
+    x, dt, Bm, Cm, dy = (np.ascontiguousarray(cut(inp[k])) for k in ("x", "dt", "B", "C", "dy"))
+    h0 = None if inp["h0"] is None else np.ascontiguousarray(inp["h0"][:rows])
     t0 = time.perf_counter()
-    oracle.ssd_forward(x, dt, sl["A"], Bm, Cm, sl["D"], h0, chunk=dims.chunk, threads=threads)
-    oracle.ssd_backward(x, dt, sl["A"], Bm, Cm, sl["D"], h0, dy, threads=threads)
+    oracle.ssd_forward(x, dt, inp["A"], Bm, Cm, inp["D"], h0, chunk=dims.chunk, threads=threads)
+    oracle.ssd_backward(x, dt, inp["A"], Bm, Cm, inp["D"], h0, dy, threads=threads)
     return time.perf_counter() - t0
 
 
-def calibrate_tokens(dims, inp, threads, seconds):
-    probe = min(64, dims.seqlen)
-    t = oracle_sample_time(dims, inp, probe, threads)
-    tokens = int(probe * seconds / max(t, 1e-6))
-    return max(16, min(dims.seqlen, tokens))
+def plan_sample(dims, inp, threads, seconds):
+    """Pick (rows, tokens, repeats) so one repeat is a slice of the workload
+    and repeats x one-repeat time is about `seconds`."""
+    probe_tokens = min(256, dims.seqlen)
+    t = oracle_sample_time(dims, inp, 1, probe_tokens, threads)
+    per_token = t / probe_tokens                      # one batch row
+    full = per_token * dims.seqlen * dims.batch
+    if full <= seconds:
+        return dims.batch, dims.seqlen, max(1, int(seconds / max(full, 1e-9)))
+    rows = max(1, min(dims.batch, int(seconds / (per_token * dims.seqlen))))
+    if rows >= 1 and per_token * dims.seqlen * rows <= seconds:
+        return rows, dims.seqlen, 1
+    return 1, max(16, min(dims.seqlen, int(seconds / per_token))), 1
+
+
+def cpu_baseline_run(dims, inp, threads, seconds):
+    rows, tokens, reps = plan_sample(dims, inp, threads, seconds)
+    total = 0.0
+    for _ in range(reps):
+        total += oracle_sample_time(dims, inp, rows, tokens, threads)
+    value = rows * tokens * reps / total
+    sample = (f"{rows} of {dims.batch} batch rows x first {tokens} of {dims.seqlen} steps, all "
+              f"{dims.nheads} heads, x{reps} repeats (float64 C oracle, {total:.1f} s)")
+    return value, sample, rows * tokens, total / reps
 
 
 def run_reference(args, dims, inp, name):
@@ -216,14 +233,15 @@ def run_reference(args, dims, inp, name):
     oracle.build_oracle()
     threads = os.cpu_count() or 1
     total = args.steps + args.warmup
-    per_step = min(2.0, 150.0 / max(total, 1))
-    tokens = calibrate_tokens(dims, inp, threads, per_step)
+    per_step = min(5.0, 150.0 / max(total, 1))
+    rows, tokens, _ = plan_sample(dims, inp, threads, per_step)
     for _ in range(args.warmup):
-        oracle_sample_time(dims, inp, tokens, threads)
-    times = [oracle_sample_time(dims, inp, tokens, threads) for _ in range(args.steps)]
+        oracle_sample_time(dims, inp, rows, tokens, threads)
+    times = [oracle_sample_time(dims, inp, rows, tokens, threads) for _ in range(args.steps)]
     sec = sum(times)
-    value = tokens * args.steps / sec
-    sample = f"batch row 0 of {dims.batch}, all {dims.nheads} heads, first {tokens} of {dims.seqlen} steps"
+    value = rows * tokens * args.steps / sec
+    sample = (f"each step: {rows} of {dims.batch} batch rows x first {tokens} of {dims.seqlen} "
+              f"steps, all {dims.nheads} heads (float64 C oracle)")
     return {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sec / args.steps,
@@ -409,11 +427,9 @@ def main():
         import oracle
         oracle.build_oracle()
         threads = os.cpu_count() or 1
-        ntok = calibrate_tokens(dims, inp, threads, args.cpu_budget)
-        sec = oracle_sample_time(dims, inp, ntok, threads)
-        cpu = {"value": ntok / sec, "unit": UNIT, "cores": threads, "kind": "oracle",
-               "sample": f"batch row 0 of {Bz}, all {H} heads, first {ntok} of {T} steps "
-                         f"(float64 C oracle, {sec:.1f} s)"}
+        value_c, sample_c, _, _ = cpu_baseline_run(dims, inp, threads, args.cpu_budget)
+        cpu = {"value": value_c, "unit": UNIT, "cores": threads, "kind": "oracle",
+               "sample": sample_c}
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,

@@ -145,6 +145,15 @@ SSD_API int ssd_trace_reset(void);
  * 0 = SIMT fp32 kernels, 1 = tcgen05 tensor-core kernels.  -1 if rejected. */
 SSD_API int ssd_kernel_path(const ssd_dims* dims);
 
+/* Restrict kernel selection: path = 0 uses the SIMT kernels for every shape,
+ * path = -1 restores automatic selection.  Process-wide; for tests. */
+SSD_API int ssd_force_kernel_path(int path);
+
+/* Reads and clears the device-side error word that bounded waits inside the
+ * tensor-core kernels set when they give up (synchronous: it copies from the
+ * device).  Returns SSD_OK, SSD_ERR_DEVICE_TIMEOUT or SSD_ERR_CUDA. */
+SSD_API int ssd_device_status(void);
+
 #ifdef __cplusplus
 }
 #endif

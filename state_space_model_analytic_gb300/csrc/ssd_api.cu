@@ -60,8 +60,12 @@ void trace_close_slot(int slot, cudaStream_t s) {
 size_t simt_smem_need(const Problem& p);
 int simt_row_tile(const Problem& p);
 bool tc_supported(const Problem& p);
+bool tc_backward_supported(const Problem& p);
+void tc_force_path(int path);
+cudaError_t tc_chunk_outer(const Problem& p, int mode, float* out);
 cudaError_t tc_forward_scan(const Problem& p);
 cudaError_t tc_backward(const Problem& p);
+cudaError_t tc_read_and_clear_error(unsigned int* out);
 
 namespace {
 
@@ -252,6 +256,21 @@ size_t ssd_workspace_bytes(const ssd_dims* dims, int which) {
   return carve(&p, nullptr, which);
 }
 
+int ssd_force_kernel_path(int path) {
+  if (path != -1 && path != 0) return fail(SSD_ERR_INVALID_ARG, "path must be -1 or 0");
+  tc_force_path(path);
+  return SSD_OK;
+}
+
+int ssd_device_status(void) {
+  g_err.clear();
+  unsigned int flag = 0;
+  cudaError_t e = tc_read_and_clear_error(&flag);
+  if (e != cudaSuccess) return cuda_fail(e, "ssd_device_status");
+  if (flag) return fail(SSD_ERR_DEVICE_TIMEOUT, "a device-side wait gave up (flag 0x%x)", flag);
+  return SSD_OK;
+}
+
 int ssd_kernel_path(const ssd_dims* dims) {
   if (validate(dims) != SSD_OK) return -1;
   Problem p = base_problem(dims);
@@ -284,11 +303,12 @@ int ssd_forward(const ssd_dims* dims, const void* x, const float* dt, const floa
   carve(&p, (char*)workspace, 0);
   p.stream = (cudaStream_t)cuda_stream;
 
-  cudaError_t e = simt_forward_states(p, p.hist, p.cs_last);
+  const bool tc = tc_supported(p);
+  cudaError_t e = tc ? tc_chunk_outer(p, 0, p.hist) : simt_forward_states(p, p.hist, p.cs_last);
   if (e != cudaSuccess) return cuda_fail(e, "forward chunk-state kernel");
   e = simt_state_pass_fwd(p, p.hist, p.cs_last);
   if (e != cudaSuccess) return cuda_fail(e, "forward state-pass kernel");
-  e = tc_supported(p) ? tc_forward_scan(p) : simt_forward_scan(p);
+  e = tc ? tc_forward_scan(p) : simt_forward_scan(p);
   if (e != cudaSuccess) return cuda_fail(e, "forward chunk-scan kernel");
   return SSD_OK;
 }
@@ -328,12 +348,12 @@ int ssd_backward(const ssd_dims* dims, const void* x, const float* dt, const flo
     // recompute the chunk-start states into the workspace (final state not needed)
     Problem f = p;
     f.final_state = nullptr;
-    e = simt_forward_states(f, f.hist, f.cs_last);
+    e = tc_supported(f) ? tc_chunk_outer(f, 0, f.hist) : simt_forward_states(f, f.hist, f.cs_last);
     if (e != cudaSuccess) return cuda_fail(e, "backward recompute chunk-state kernel");
     e = simt_state_pass_fwd(f, f.hist, f.cs_last);
     if (e != cudaSuccess) return cuda_fail(e, "backward recompute state-pass kernel");
   }
-  e = tc_supported(p) ? tc_backward(p) : simt_backward(p);
+  e = tc_backward_supported(p) ? tc_backward(p) : simt_backward(p);
   if (e != cudaSuccess) return cuda_fail(e, "backward kernels");
   return SSD_OK;
 }

@@ -56,6 +56,8 @@ cudaError_t simt_forward_states(const Problem& p, float* hist, float* cs_last);
 cudaError_t simt_state_pass_fwd(const Problem& p, float* hist, const float* cs_last);
 cudaError_t simt_forward_scan(const Problem& p);
 cudaError_t simt_backward(const Problem& p);
+cudaError_t simt_state_pass_bwd(const Problem& p);
+cudaError_t simt_reduce_heads(const Problem& p, int n_a, int n_d);
 
 void count_launch(int n = 1);
 

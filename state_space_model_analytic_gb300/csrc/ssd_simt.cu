@@ -817,6 +817,24 @@ cudaError_t simt_state_pass_fwd(const Problem& p, float* hist, const float* cs_l
   return cudaGetLastError();
 }
 
+cudaError_t simt_state_pass_bwd(const Problem& p) {
+  const Dev d = dev_of(p);
+  {
+    LaunchScope ls_("state_pass_bwd", p.stream);
+    k_state_pass_bwd<<<dim3((p.P * p.N + kThreads - 1) / kThreads, p.H, p.B), kThreads, 0,
+                       p.stream>>>(d, p.dstate, p.cs_last, p.dh0);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t simt_reduce_heads(const Problem& p, int n_a, int n_d) {
+  {
+    LaunchScope ls_("reduce_heads", p.stream);
+    k_reduce_heads<<<p.H, 32, 0, p.stream>>>(p.H, n_a, n_d, p.dA_part, p.dD_part, p.dA, p.dD);
+  }
+  return cudaGetLastError();
+}
+
 cudaError_t simt_forward_scan(const Problem& p) {
   const int tq = pick_tq(p);
   if (p.bf16)

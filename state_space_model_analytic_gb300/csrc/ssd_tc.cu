@@ -1,10 +1,1137 @@
 // Tensor-core (tcgen05 / TMEM / TMA) kernels of the chunked SSD core.
+//
+// Scope: bf16 storage, headdim P = 64, d_state N = 128, chunk Q in {128, 256}.
+// A chunk is processed as Q/128 blocks of 128 rows (the MMA M size).  Inside a
+// chunk the second block reaches the first through the mid-chunk state
+//     H_mid = exp(cs_127) H_{c-1} + S_0,
+//     S_0   = sum_{j<128} exp(cs_127 - cs_j) dt_j x_j B_j^T,
+// which is exact in real arithmetic (it is the recurrence of
+// `ssd_forward_state_history_reference`, burn_dragon_kernel 0.5.0,
+// src/sequence/mamba2/backward.rs, unrolled over 128 steps) and replaces the
+// off-diagonal 128 x 128 block of the quadratic form by two rank-N products.
+//
+// Decay masks.  For a 128-row block, warp w owns rows r..r+31, r = 32 w.  For
+// a column j < r (a 32-column chunk left of the warp's diagonal chunk)
+//     exp(cs_i - cs_j) = exp(cs_i - cs_r) * exp(cs_r - cs_j),
+// both factors <= 1 because cs is non-increasing (dt >= 0, A <= 0), so no
+// factor overflows and an underflowed factor means the product underflows.
+// The column factors are a per-warp table in shared memory; only the 32 x 32
+// diagonal chunk evaluates one exp per element, with the exponent set to
+// -inf above the diagonal before exp.
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include <mutex>
+
+#include "ssd_common.cuh"
 #include "ssd_internal.h"
+#include "tc_util.cuh"
 
 namespace ssd {
 
-bool tc_supported(const Problem&) { return false; }
-cudaError_t tc_forward_scan(const Problem&) { return cudaErrorNotSupported; }
-cudaError_t tc_backward(const Problem&) { return cudaErrorNotSupported; }
+using namespace tc;
+
+namespace {
+
+constexpr int kTcThreads = 128;
+constexpr float kLog2e = 1.4426950408889634f;
+// Polls of an mbarrier before a kernel gives up and records a timeout.
+constexpr uint32_t kWaitLimit = 1u << 22;
+
+// ---------------------------------------------------------------------------
+// Device error word: a bounded wait that gives up sets it; the host reads it
+// only through the test hooks.  Kernels finish (no trap) after a timeout.
+__device__ unsigned int g_tc_error;
+
+// Every thread of the CTA waits; the outcome is made uniform across the CTA
+// (so a timeout never splits the threads at a later barrier).
+__device__ __forceinline__ bool wait_or_flag(uint64_t* bar, uint32_t parity) {
+  const bool mine = mbar_wait(bar, parity, kWaitLimit);
+  const bool all = __syncthreads_and(mine) != 0;
+  if (!all && threadIdx.x == 0) atomicOr(&g_tc_error, 1u);
+  return all;
+}
+
+struct TcDims {
+  int B, T, H, P, N, G, Q, nc, hpg;
+};
+
+// Chunk-local inclusive cumsum of dt*A in log2 units (cs2 = cs * log2 e) and dt,
+// for Q <= 256 values, with 128 threads (Q/128 consecutive values each).
+__device__ __forceinline__ void chunk_cumsum_tc(const TcDims& d, const float* __restrict__ dt,
+                                                const float* __restrict__ A, int b, int c, int h,
+                                                float* s_cs2, float* s_dt, float* scratch) {
+  const int tid = threadIdx.x;
+  const int per = d.Q / kTcThreads;  // 1 or 2
+  float v[2] = {0.f, 0.f}, dv[2] = {0.f, 0.f};
+  const float a = A[h] * kLog2e;
+  float run = 0.f;
+  for (int k = 0; k < per; ++k) {
+    const int t = tid * per + k;
+    dv[k] = dt[((size_t)b * d.T + (size_t)c * d.Q + t) * d.H + h];
+    run += dv[k] * a;
+    v[k] = run;
+  }
+  const float incl = block_inclusive_scan(run, scratch);
+  const float excl = incl - run;
+  for (int k = 0; k < per; ++k) {
+    const int t = tid * per + k;
+    s_cs2[t] = v[k] + excl;
+    s_dt[t] = dv[k];
+  }
+  __syncthreads();
+}
+
+// Scale every 128-byte row r of a SW128 bf16 tile by w[r] (rows x 64 values).
+__device__ __forceinline__ void scale_rows_bf16(const uint8_t* src, uint8_t* dst, int rows,
+                                                const float* w) {
+  for (int e = threadIdx.x; e < rows * 8; e += kTcThreads) {
+    const int r = e >> 3;
+    const uint32_t off = (uint32_t)e * 16u;  // row-uniform scale: swizzle irrelevant
+    const uint4 v = *(const uint4*)(src + off);
+    const float s = w[r];
+    const __nv_bfloat162* p = (const __nv_bfloat162*)&v;
+    uint4 o;
+    uint32_t* q = (uint32_t*)&o;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float2 f = __bfloat1622float2(p[k]);
+      q[k] = pack_bf16(f.x * s, f.y * s);
+    }
+    *(uint4*)(dst + off) = o;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Chunk outer product on tensor cores: out[b][c][h] (P x N, fp32) =
+//   MODE 0: sum_j exp(cs_last - cs_j) dt_j x_j B_j^T   (chunk state S_c)
+//   MODE 1: sum_j exp(cs_j) dy_j C_j^T                 (chunk dstate R_c)
+// computed transposed, D[n][p] = V^T (w o U), M = N = 128 rows (n), N = P = 64.
+struct OuterMaps {
+  CUtensorMap u;  // x or dy: [B*T][H*P] bf16, box {64, Q}
+  CUtensorMap v;  // B or C:  [B*T][G*N] bf16, box {64, Q}
+};
+
+template <int MODE>
+__global__ void __launch_bounds__(kTcThreads)
+k_chunk_outer_tc(const __grid_constant__ OuterMaps maps, TcDims d, const float* __restrict__ dt,
+                 const float* __restrict__ A, float* __restrict__ out,
+                 float* __restrict__ cs_last) {
+  extern __shared__ __align__(1024) uint8_t smraw[];
+  uint8_t* sm = (uint8_t*)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
+  const int Q = d.Q;
+  uint8_t* sV = sm;                      // 2 MN blocks of [Q rows][128 B]
+  uint8_t* sU = sm + 2 * Q * 128;        // [Q rows][128 B]
+  __shared__ float s_cs2[256], s_dt[256], s_w[256], scratch[4];
+  __shared__ uint64_t bar_load, bar_mma;
+  __shared__ uint32_t tmem_base;
+  const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int g = h / d.hpg, tid = threadIdx.x, warp = tid >> 5;
+  const int row0 = b * d.T + c * Q;
+
+  if (tid == 0) {
+    prefetch_tmap(&maps.u);
+    prefetch_tmap(&maps.v);
+    mbar_init(&bar_load, 1);
+    mbar_init(&bar_mma, 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(&tmem_base, 64);
+    tmem_relinquish();
+  }
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  const uint32_t tm = tmem_base;
+  if (tid == 0) {
+    mbar_expect_tx(&bar_load, (uint32_t)(3 * Q * 128));
+    tma_load_2d(sV, &maps.v, g * d.N, row0, &bar_load);
+    tma_load_2d(sV + Q * 128, &maps.v, g * d.N + 64, row0, &bar_load);
+    tma_load_2d(sU, &maps.u, h * d.P, row0, &bar_load);
+  }
+  chunk_cumsum_tc(d, dt, A, b, c, h, s_cs2, s_dt, scratch);
+  const float last2 = s_cs2[Q - 1];
+  for (int t = tid; t < Q; t += kTcThreads)
+    s_w[t] = (MODE == 0) ? exp2f(last2 - s_cs2[t]) * s_dt[t] : exp2f(s_cs2[t]);
+  if (tid == 0) cs_last[((size_t)b * d.H + h) * d.nc + c] = last2 * (1.0f / kLog2e);
+  __syncthreads();
+  const bool loaded = wait_or_flag(&bar_load, 0);
+  if (loaded) scale_rows_bf16(sU, sU, Q, s_w);
+  fence_async_smem();
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  if (tid == 0 && loaded) {
+    const uint32_t idesc = idesc_bf16(128, 64, true, true);
+    for (int ks = 0; ks < Q / 16; ++ks) {
+      const uint64_t ad = desc_sw128(smem_u32(sV) + ks * 2048, Q * 128, 1024);
+      const uint64_t bd = desc_sw128(smem_u32(sU) + ks * 2048, Q * 128, 1024);
+      mma_bf16(tm, ad, bd, idesc, ks > 0);
+    }
+    mma_commit(&bar_mma);
+  }
+  __syncthreads();
+  const bool done = loaded && wait_or_flag(&bar_mma, 0);
+  fence_after_sync();
+  if (done) {
+    const int n = warp * 32 + (tid & 31);
+    float* dst = out + (((size_t)b * d.nc + c) * d.H + h) * (size_t)(d.P * d.N) + n;
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      float v[32];
+      tmem_ld32(tm + ((uint32_t)(warp * 32) << 16) + half * 32, v);
+      tmem_wait_ld();
+#pragma unroll
+      for (int i = 0; i < 32; ++i) dst[(size_t)(half * 32 + i) * d.N] = v[i];
+    }
+  }
+  fence_before_sync();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tm, 64);
+}
+
+// ---------------------------------------------------------------------------
+// Forward chunk scan: y for one (b, chunk, head) per CTA, block by block.
+struct ScanMaps {
+  CUtensorMap x;  // [B*T][H*P] bf16, box {64, 128}
+  CUtensorMap B;  // [B*T][G*N] bf16, box {64, 128}
+  CUtensorMap C;  // [B*T][G*N] bf16, box {64, 128}
+  CUtensorMap y;  // [B*T][H*P] bf16, box {64, 128} (store)
+};
+
+// shared-memory layout of k_fwd_scan_tc (offsets from the 1024-aligned base)
+constexpr uint32_t kScanR1 = 0;            // C tile (32K) + B tile (32K); later M (32K), y staging
+constexpr uint32_t kScanX = 65536;         // X block [128][128 B]
+constexpr uint32_t kScanXw = 81920;        // w-scaled X block 0 (Q = 256)
+constexpr uint32_t kScanH = 98304;         // H as bf16 B operand (16K)
+constexpr uint32_t kScanBytes = 114688;
+
+__global__ void __launch_bounds__(kTcThreads)
+k_fwd_scan_tc(const __grid_constant__ ScanMaps maps, TcDims d, const float* __restrict__ dt,
+              const float* __restrict__ A, const float* __restrict__ D,
+              const float* __restrict__ hist) {
+  extern __shared__ __align__(1024) uint8_t smraw[];
+  uint8_t* sm = (uint8_t*)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
+  uint8_t* sC = sm + kScanR1;
+  uint8_t* sB = sm + kScanR1 + 32768;
+  uint8_t* sM = sm + kScanR1;   // after the CB / Ys / S_0 products are done
+  uint8_t* sY = sm + kScanR1;   // after the Y product is done
+  uint8_t* sX = sm + kScanX;
+  uint8_t* sXw = sm + kScanXw;
+  uint8_t* sH = sm + kScanH;
+  __shared__ float s_cs2[256], s_dt[256], scratch[4];
+  __shared__ float s_E[4][128];  // per-warp column factors exp(cs_r - cs_j) dt_j
+  __shared__ uint64_t bar_load, bar_mma;
+  __shared__ uint32_t tmem_base;
+  const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int g = h / d.hpg, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int Q = d.Q, nblk = Q / 128;
+  const float Dh = D[h];
+  const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+
+  if (tid == 0) {
+    prefetch_tmap(&maps.x);
+    prefetch_tmap(&maps.B);
+    prefetch_tmap(&maps.C);
+    prefetch_tmap(&maps.y);
+    mbar_init(&bar_load, 1);
+    mbar_init(&bar_mma, 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(&tmem_base, 256);
+    tmem_relinquish();
+  }
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  const uint32_t tm = tmem_base;
+  const uint32_t tCB = tm, tY = tm, tYs = tm + 128, tS0 = tm + 192;
+  uint32_t load_phase = 0, mma_phase = 0;
+  bool ok = true;
+
+  // H_{c-1} (fp32 [P][N]) -> bf16 K-major operand: row p, K = n (two 64-wide tiles)
+  const float* Hg = hist + (((size_t)b * d.nc + c) * d.H + h) * (size_t)(64 * 128);
+  chunk_cumsum_tc(d, dt, A, b, c, h, s_cs2, s_dt, scratch);
+  for (int e = tid; e < 64 * 16; e += kTcThreads) {
+    const int p = e >> 4, ch = e & 15;  // 16 chunks of 8 n per row
+    const float4 lo = *(const float4*)(Hg + p * 128 + ch * 8);
+    const float4 hi = *(const float4*)(Hg + p * 128 + ch * 8 + 4);
+    uint4 o;
+    o.x = pack_bf16(lo.x, lo.y);
+    o.y = pack_bf16(lo.z, lo.w);
+    o.z = pack_bf16(hi.x, hi.y);
+    o.w = pack_bf16(hi.z, hi.w);
+    *(uint4*)(sH + (ch >> 3) * 8192 + sw128(p, ch & 7)) = o;
+  }
+
+  for (int blk = 0; blk < nblk && ok; ++blk) {
+    const int row0 = b * d.T + c * Q + blk * 128;
+    if (tid == 0) {
+      mbar_expect_tx(&bar_load, 80 * 1024);
+      tma_load_2d(sC, &maps.C, g * d.N, row0, &bar_load);
+      tma_load_2d(sC + 16384, &maps.C, g * d.N + 64, row0, &bar_load);
+      tma_load_2d(sB, &maps.B, g * d.N, row0, &bar_load);
+      tma_load_2d(sB + 16384, &maps.B, g * d.N + 64, row0, &bar_load);
+      tma_load_2d(sX, &maps.x, h * d.P, row0, &bar_load);
+    }
+    // per-warp column factors of this block: E[w][jj] = exp(cs_r - cs_J) dt_J, J < r
+    const int base = blk * 128;
+    for (int e = tid; e < 4 * 128; e += kTcThreads) {
+      const int w = e >> 7, jj = e & 127;
+      const int r = base + 32 * w, J = base + jj;
+      s_E[w][jj] = (J < r) ? exp2f(s_cs2[r] - s_cs2[J]) * s_dt[J] : 0.f;
+    }
+    // reference log-decay of the block's state term: cs before row `base`
+    const float ref2 = blk == 0 ? 0.f : s_cs2[base - 1];
+    __syncthreads();
+    ok = wait_or_flag(&bar_load, load_phase);
+    load_phase ^= 1;
+    if (!ok) break;
+    const bool need_s0 = (blk == 0 && nblk == 2);
+    if (need_s0) {
+      // w o X_0 with w_j = exp(cs_127 - cs_j) dt_j, for the mid-chunk state
+      for (int e = tid; e < 128 * 8; e += kTcThreads) {
+        const int r = e >> 3;
+        const uint32_t off = (uint32_t)e * 16u;
+        const float s = exp2f(s_cs2[127] - s_cs2[r]) * s_dt[r];
+        const uint4 v = *(const uint4*)(sX + off);
+        const __nv_bfloat162* p = (const __nv_bfloat162*)&v;
+        uint4 o;
+        uint32_t* q = (uint32_t*)&o;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float2 f = __bfloat1622float2(p[k]);
+          q[k] = pack_bf16(f.x * s, f.y * s);
+        }
+        *(uint4*)(sXw + off) = o;
+      }
+    }
+    fence_async_smem();
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    if (tid == 0) {
+      // CB = C_blk B_blk^T  (128 x 128, K = N)
+      const uint32_t id_cb = idesc_bf16(128, 128, false, false);
+      for (int kk = 0; kk < 8; ++kk) {
+        const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+        mma_bf16(tCB, desc_sw128(smem_u32(sC) + off, 16, 1024),
+                 desc_sw128(smem_u32(sB) + off, 16, 1024), id_cb, kk > 0);
+      }
+      // Ys = C_blk Hin^T  (128 x 64, K = N); Hin K-major (blk 0) or MN-major (blk 1)
+      const uint32_t id_ys = idesc_bf16(128, 64, false, blk > 0);
+      for (int kk = 0; kk < 8; ++kk) {
+        const uint32_t aoff = (kk >> 2) * 16384 + (kk & 3) * 32;
+        const uint32_t boff = blk == 0 ? (kk >> 2) * 8192 + (kk & 3) * 32 : kk * 2048;
+        mma_bf16(tYs, desc_sw128(smem_u32(sC) + aoff, 16, 1024),
+                 desc_sw128(smem_u32(sH) + boff, 16384, 1024), id_ys, kk > 0);
+      }
+      if (need_s0) {
+        // S_0^T = B_0^T (w o X_0): M = n (two 64-wide MN blocks 16K apart), N = p, K = j
+        const uint32_t id_s0 = idesc_bf16(128, 64, true, true);
+        for (int kk = 0; kk < 8; ++kk)
+          mma_bf16(tS0, desc_sw128(smem_u32(sB) + kk * 2048, 16384, 1024),
+                   desc_sw128(smem_u32(sXw) + kk * 2048, 16384, 1024), id_s0, kk > 0);
+      }
+      mma_commit(&bar_mma);
+    }
+    __syncthreads();
+    ok = wait_or_flag(&bar_mma, mma_phase);
+    mma_phase ^= 1;
+    fence_after_sync();
+    if (!ok) break;
+
+    const int il = warp * 32 + lane;  // row inside the block (TMEM lane)
+    const int I = base + il;          // row inside the chunk
+    if (need_s0) {
+      // H_mid^T[n][p] = exp(cs_127) H[p][n] + S_0^T[n][p] -> bf16 MN-major (row n)
+      const float e127 = exp2f(s_cs2[127]);
+      const int n = il;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        float v[32];
+        tmem_ld32(tS0 + lane_base + half * 32, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          uint4 o;
+          uint32_t* q = (uint32_t*)&o;
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            const int p0 = half * 32 + k * 8 + 2 * t;
+            const float a0 = fmaf(e127, Hg[(size_t)p0 * 128 + n], v[k * 8 + 2 * t]);
+            const float a1 = fmaf(e127, Hg[(size_t)(p0 + 1) * 128 + n], v[k * 8 + 2 * t + 1]);
+            q[t] = pack_bf16(a0, a1);
+          }
+          *(uint4*)(sH + sw128(n, half * 4 + k)) = o;
+        }
+      }
+    }
+    // M = CB o L o dt (masked), bf16 K-major A operand: row il, K = j (two 64-wide tiles)
+    {
+      const int r = base + 32 * warp;
+      const float fi = exp2f(s_cs2[I] - s_cs2[r]);
+      const float csI = s_cs2[I];
+#pragma unroll
+      for (int jc = 0; jc < 4; ++jc) {
+        float v[32];
+        tmem_ld32(tCB + lane_base + jc * 32, v);
+        tmem_wait_ld();
+        if (jc < warp) {
+#pragma unroll
+          for (int k = 0; k < 32; ++k) v[k] *= fi * s_E[warp][jc * 32 + k];
+        } else if (jc == warp) {
+#pragma unroll
+          for (int k = 0; k < 32; ++k) {
+            const int J = base + jc * 32 + k;
+            const float ex = (J <= I) ? exp2f(csI - s_cs2[J]) : 0.f;
+            v[k] *= ex * s_dt[J];
+          }
+        } else {
+#pragma unroll
+          for (int k = 0; k < 32; ++k) v[k] = 0.f;
+        }
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          uint4 o;
+          o.x = pack_bf16(v[q4 * 8 + 0], v[q4 * 8 + 1]);
+          o.y = pack_bf16(v[q4 * 8 + 2], v[q4 * 8 + 3]);
+          o.z = pack_bf16(v[q4 * 8 + 4], v[q4 * 8 + 5]);
+          o.w = pack_bf16(v[q4 * 8 + 6], v[q4 * 8 + 7]);
+          const int j = jc * 32 + q4 * 8;
+          *(uint4*)(sM + (j >> 6) * 16384 + sw128(il, (j & 63) >> 3)) = o;
+        }
+      }
+    }
+    fence_async_smem();
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    if (tid == 0) {
+      // Y = M X_blk (128 x 64, K = j); X is MN-major (row j, 64 p)
+      const uint32_t id_y = idesc_bf16(128, 64, false, true);
+      for (int kk = 0; kk < 8; ++kk) {
+        const uint32_t aoff = (kk >> 2) * 16384 + (kk & 3) * 32;
+        mma_bf16(tY, desc_sw128(smem_u32(sM) + aoff, 16, 1024),
+                 desc_sw128(smem_u32(sX) + kk * 2048, 16384, 1024), id_y, kk > 0);
+      }
+      mma_commit(&bar_mma);
+    }
+    __syncthreads();
+    ok = wait_or_flag(&bar_mma, mma_phase);
+    mma_phase ^= 1;
+    fence_after_sync();
+    if (!ok) break;
+    // epilogue: y = Y + exp(cs_I - ref) Ys + D x  -> bf16 staging -> TMA store
+    {
+      const float sc = exp2f(s_cs2[I] - ref2);
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        float yv[32], ys[32];
+        tmem_ld32(tY + lane_base + half * 32, yv);
+        tmem_ld32(tYs + lane_base + half * 32, ys);
+        tmem_wait_ld();
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int ch = half * 4 + k;
+          const uint4 xv = *(const uint4*)(sX + sw128(il, ch));
+          const __nv_bfloat162* xp = (const __nv_bfloat162*)&xv;
+          uint4 o;
+          uint32_t* q = (uint32_t*)&o;
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            const float2 xf = __bfloat1622float2(xp[t]);
+            const int m = k * 8 + 2 * t;
+            q[t] = pack_bf16(fmaf(sc, ys[m], yv[m]) + Dh * xf.x,
+                             fmaf(sc, ys[m + 1], yv[m + 1]) + Dh * xf.y);
+          }
+          *(uint4*)(sY + sw128(il, ch)) = o;
+        }
+      }
+    }
+    fence_async_smem();
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    if (tid == 0) {
+      tma_store_2d(&maps.y, sY, h * d.P, row0);
+      bulk_commit();
+      bulk_wait_read0();  // staging (region R1) is reloaded by the next block
+    }
+    __syncthreads();
+  }
+  if (tid == 0) bulk_wait0();
+  fence_before_sync();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tm, 256);
+}
+
+// ---------------------------------------------------------------------------
+// Backward on tensor cores.  One CTA per (128-row block k, chunk c, group g,
+// head subset, batch b); the CTA loops over its heads and accumulates dC and
+// dB of the block over those heads in TMEM (fixed head order, deterministic).
+// Each block is treated as a chunk of 128 steps with
+//   state in  Hin  = H_{c-1} (k = 0) or H_mid  (k = 1),
+//   grad out  gout = g_c     (last block) or g_mid = exp(cs_255 - cs_127) g_c + R_1 (k = 0 of 2),
+//   R_1 = sum_{i >= 128} exp(cs_i - cs_127) dy_i C_i^T,
+// and the per-block formulas of the chunked backward (see ssd_simt.cu).  The
+// strict row and column sums of M_ij = W_ij (C_i.B_j) come from the rows the
+// threads hold (row sums) and a warp-transposed reduction (column sums).
+struct BwdMaps {
+  CUtensorMap x;   // [B*T][H*P] bf16, box {64, 128}
+  CUtensorMap dy;  // [B*T][H*P] bf16, box {64, 128}
+  CUtensorMap B;   // [B*T][G*N] bf16, box {64, 128}
+  CUtensorMap C;   // [B*T][G*N] bf16, box {64, 128}
+  CUtensorMap dx;  // [B*T][H*P] bf16, box {64, 128} (store)
+  CUtensorMap dB;  // [B*T][G*N] bf16, box {64, 128} (store)
+  CUtensorMap dC;  // [B*T][G*N] bf16, box {64, 128} (store)
+};
+
+constexpr uint32_t kBwC = 0;          // C_k: 2 K-major tiles [128][128 B]
+constexpr uint32_t kBwB = 32768;      // B_k
+constexpr uint32_t kBwO = 65536;      // B_0 (k = 1) or C_1 (k = 0) when the chunk has 2 blocks
+constexpr uint32_t kBwX = 98304;      // X_k  [128 rows][64 p]
+constexpr uint32_t kBwDY = 114688;    // dY_k
+constexpr uint32_t kBwXO = 131072;    // X_0 (k = 1) or dY_1 (k = 0), row-scaled
+constexpr uint32_t kBwH = 147456;     // Hin  bf16, row n, 64 p
+constexpr uint32_t kBwG = 163840;     // gout bf16, row n, 64 p
+constexpr uint32_t kBwW = 180224;     // W, then L o CB, then staging (2 tiles)
+constexpr uint32_t kBwBytes = 212992;
+
+// Column sums over the 32 lanes of a warp: lane l returns sum over lanes of v[l].
+__device__ __forceinline__ float warp_column_sum(float (&v)[32]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int s = 16; s >= 1; s >>= 1) {
+    const bool upper = (lane & s) != 0;
+#pragma unroll
+    for (int k = 0; k < s; ++k) {
+      const float send = upper ? v[k] : v[k + s];
+      const float keep = upper ? v[k + s] : v[k];
+      v[k] = keep + __shfl_xor_sync(0xffffffffu, send, s);
+    }
+  }
+  return v[0];
+}
+
+__device__ __forceinline__ void store_row_bf16(uint8_t* tile, int row, int chunk0,
+                                               const float* v8) {
+  uint4 o;
+  o.x = pack_bf16(v8[0], v8[1]);
+  o.y = pack_bf16(v8[2], v8[3]);
+  o.z = pack_bf16(v8[4], v8[5]);
+  o.w = pack_bf16(v8[6], v8[7]);
+  *(uint4*)(tile + sw128(row, chunk0)) = o;
+}
+
+__global__ void __launch_bounds__(kTcThreads, 1)
+k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, int nsub, const float* __restrict__ dt,
+         const float* __restrict__ A, const float* __restrict__ D,
+         const float* __restrict__ hist, const float* __restrict__ gstate,
+         float* __restrict__ ddt, float* __restrict__ dA_part, float* __restrict__ dD_part) {
+  extern __shared__ __align__(1024) uint8_t smraw[];
+  uint8_t* sm = (uint8_t*)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
+  uint8_t* sC = sm + kBwC;
+  uint8_t* sB = sm + kBwB;
+  uint8_t* sO = sm + kBwO;
+  uint8_t* sX = sm + kBwX;
+  uint8_t* sDY = sm + kBwDY;
+  uint8_t* sXO = sm + kBwXO;
+  uint8_t* sH = sm + kBwH;
+  uint8_t* sG = sm + kBwG;
+  uint8_t* sW = sm + kBwW;
+  __shared__ float s_cs2[256], s_dt[256], scratch[4];
+  __shared__ float s_E[4][128];    // exp(cs_r - cs_J), J < r = base + 32 w
+  __shared__ float s_col[4][128];  // per-warp strict column sums of M
+  __shared__ float s_v[128];
+  __shared__ uint64_t bar_shared, bar_head, bar_mma;
+  __shared__ uint32_t tmem_base;
+
+  const int nblk = d.Q / 128;
+  const int k = blockIdx.x % nblk, c = blockIdx.x / nblk;
+  const int g = blockIdx.y / nsub, sub = blockIdx.y % nsub, b = blockIdx.z;
+  const int kh = d.hpg / nsub;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int base = 128 * k;
+  const int crow = b * d.T + c * d.Q;  // first row of the chunk
+  const int row0 = crow + base;
+  const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+  const bool two = nblk == 2;
+  const uint32_t head_bytes = two ? 48 * 1024 : 32 * 1024;
+
+  if (tid == 0) {
+    prefetch_tmap(&maps.x);
+    prefetch_tmap(&maps.dy);
+    prefetch_tmap(&maps.B);
+    prefetch_tmap(&maps.C);
+    mbar_init(&bar_shared, 1);
+    mbar_init(&bar_head, 1);
+    mbar_init(&bar_mma, 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(&tmem_base, 512);
+    tmem_relinquish();
+  }
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  const uint32_t tm = tmem_base;
+  const uint32_t T0 = tm, T1 = tm + 128, TdC = tm + 256, TdB = tm + 384;
+
+  auto issue_head_loads = [&](int h) {
+    mbar_expect_tx(&bar_head, head_bytes);
+    tma_load_2d(sX, &maps.x, h * d.P, row0, &bar_head);
+    tma_load_2d(sDY, &maps.dy, h * d.P, row0, &bar_head);
+    if (two) {
+      if (k == 1) tma_load_2d(sXO, &maps.x, h * d.P, crow, &bar_head);
+      else tma_load_2d(sXO, &maps.dy, h * d.P, crow + 128, &bar_head);
+    }
+  };
+  const int h_first = g * d.hpg + sub * kh;
+  if (tid == 0) {
+    mbar_expect_tx(&bar_shared, two ? 96 * 1024 : 64 * 1024);
+    tma_load_2d(sC, &maps.C, g * d.N, row0, &bar_shared);
+    tma_load_2d(sC + 16384, &maps.C, g * d.N + 64, row0, &bar_shared);
+    tma_load_2d(sB, &maps.B, g * d.N, row0, &bar_shared);
+    tma_load_2d(sB + 16384, &maps.B, g * d.N + 64, row0, &bar_shared);
+    if (two) {
+      if (k == 1) {
+        tma_load_2d(sO, &maps.B, g * d.N, crow, &bar_shared);
+        tma_load_2d(sO + 16384, &maps.B, g * d.N + 64, crow, &bar_shared);
+      } else {
+        tma_load_2d(sO, &maps.C, g * d.N, crow + 128, &bar_shared);
+        tma_load_2d(sO + 16384, &maps.C, g * d.N + 64, crow + 128, &bar_shared);
+      }
+    }
+    issue_head_loads(h_first);
+  }
+  bool ok = wait_or_flag(&bar_shared, 0);
+  uint32_t mma_phase = 0;
+
+  for (int hh = 0; hh < kh && ok; ++hh) {
+    const int h = h_first + hh;
+    chunk_cumsum_tc(d, dt, A, b, c, h, s_cs2, s_dt, scratch);
+    for (int e = tid; e < 4 * 128; e += kTcThreads) {
+      const int w = e >> 7, jj = e & 127;
+      const int r = base + 32 * w, J = base + jj;
+      s_E[w][jj] = (J < r) ? exp2f(s_cs2[r] - s_cs2[J]) : 0.f;
+    }
+    const float ref2 = k == 0 ? 0.f : s_cs2[base - 1];
+    const float end2 = s_cs2[base + 127];
+    __syncthreads();
+    ok = wait_or_flag(&bar_head, hh & 1);
+    if (!ok) break;
+
+    // ---- state in (Hin) and state gradient out (gout), as bf16 rows n
+    const int n = tid;
+    const size_t soff = (((size_t)b * d.nc + c) * d.H + h) * (size_t)(64 * 128);
+    const float* Hg = hist + soff;
+    const float* Gg = gstate + soff;
+    if (two) {
+      if (k == 1) {
+        for (int e = tid; e < 128 * 8; e += kTcThreads) {  // X_0 rows j by exp(cs_127 - cs_j) dt_j
+          const int r = e >> 3;
+          const float s = exp2f(s_cs2[127] - s_cs2[r]) * s_dt[r];
+          const uint4 v = *(const uint4*)(sXO + e * 16);
+          const __nv_bfloat162* q2 = (const __nv_bfloat162*)&v;
+          uint4 o;
+          uint32_t* q = (uint32_t*)&o;
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            const float2 f = __bfloat1622float2(q2[t]);
+            q[t] = pack_bf16(f.x * s, f.y * s);
+          }
+          *(uint4*)(sXO + e * 16) = o;
+        }
+      } else {
+        for (int e = tid; e < 128 * 8; e += kTcThreads) {  // dY_1 rows i by exp(cs_i - cs_127)
+          const int r = e >> 3;
+          const float s = exp2f(s_cs2[128 + r] - s_cs2[127]);
+          const uint4 v = *(const uint4*)(sXO + e * 16);
+          const __nv_bfloat162* q2 = (const __nv_bfloat162*)&v;
+          uint4 o;
+          uint32_t* q = (uint32_t*)&o;
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            const float2 f = __bfloat1622float2(q2[t]);
+            q[t] = pack_bf16(f.x * s, f.y * s);
+          }
+          *(uint4*)(sXO + e * 16) = o;
+        }
+      }
+      fence_async_smem();
+      fence_before_sync();
+      __syncthreads();
+      fence_after_sync();
+      if (tid == 0) {
+        // S_0^T = B_0^T (w o X_0)  or  R_1^T = C_1^T (e o dY_1):  M = n, N = p, K = rows
+        const uint32_t id = idesc_bf16(128, 64, true, true);
+        for (int kk = 0; kk < 8; ++kk)
+          mma_bf16(T1, desc_sw128(smem_u32(sO) + kk * 2048, 16384, 1024),
+                   desc_sw128(smem_u32(sXO) + kk * 2048, 16384, 1024), id, kk > 0);
+        mma_commit(&bar_mma);
+      }
+      __syncthreads();
+      ok = wait_or_flag(&bar_mma, mma_phase);
+      mma_phase ^= 1;
+      fence_after_sync();
+      if (!ok) break;
+    }
+    float hg = 0.f;  // <gout, Hin> partial of row n
+    {
+      const float e127 = two ? exp2f(s_cs2[127]) : 0.f;
+      const float eg = two ? exp2f(s_cs2[d.Q - 1] - s_cs2[127]) : 0.f;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        float v[32];
+        if (two) {
+          tmem_ld32(T1 + lane_base + half * 32, v);
+          tmem_wait_ld();
+        }
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          float hv[8], gv[8];
+#pragma unroll
+          for (int t = 0; t < 8; ++t) {
+            const int p = half * 32 + q4 * 8 + t;
+            float hval = Hg[(size_t)p * 128 + n];
+            float gval = Gg[(size_t)p * 128 + n];
+            if (two && k == 1) hval = fmaf(e127, hval, v[q4 * 8 + t]);
+            if (two && k == 0) gval = fmaf(eg, gval, v[q4 * 8 + t]);
+            hv[t] = hval;
+            gv[t] = gval;
+            hg = fmaf(hval, gval, hg);
+          }
+          store_row_bf16(sH, n, half * 4 + q4, hv);
+          store_row_bf16(sG, n, half * 4 + q4, gv);
+        }
+      }
+    }
+    hg = block_sum(hg, scratch);
+    fence_async_smem();
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+
+    // ---- phase A: CB = C_k B_k^T -> T0 ; dYX = dY_k X_k^T -> T1
+    if (tid == 0) {
+      const uint32_t id = idesc_bf16(128, 128, false, false);
+      for (int kk = 0; kk < 8; ++kk) {
+        const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+        mma_bf16(T0, desc_sw128(smem_u32(sC) + off, 16, 1024),
+                 desc_sw128(smem_u32(sB) + off, 16, 1024), id, kk > 0);
+      }
+      for (int kk = 0; kk < 4; ++kk)
+        mma_bf16(T1, desc_sw128(smem_u32(sDY) + kk * 32, 16, 1024),
+                 desc_sw128(smem_u32(sX) + kk * 32, 16, 1024), id, kk > 0);
+      mma_commit(&bar_mma);
+    }
+    __syncthreads();
+    ok = wait_or_flag(&bar_mma, mma_phase);
+    mma_phase ^= 1;
+    fence_after_sync();
+    if (!ok) break;
+
+    // ---- W = L o dt_j o dYX -> sW (bf16), L o CB -> registers, row / column sums of M
+    const int il = tid, I = base + il;
+    const int r0 = base + 32 * warp;
+    const float fi = exp2f(s_cs2[I] - s_cs2[r0]);
+    const float csI = s_cs2[I];
+    float rowsum = 0.f;
+    uint32_t lcb[64];
+#pragma unroll
+    for (int jc = 0; jc < 4; ++jc) {
+      float cb[32], xy[32];
+      tmem_ld32(T0 + lane_base + jc * 32, cb);
+      tmem_ld32(T1 + lane_base + jc * 32, xy);
+      tmem_wait_ld();
+      float wv[32];
+#pragma unroll
+      for (int t = 0; t < 32; ++t) {
+        const int J = base + jc * 32 + t;
+        float L;
+        if (jc < warp) L = fi * s_E[warp][jc * 32 + t];
+        else if (jc == warp) L = (J <= I) ? exp2f(csI - s_cs2[J]) : 0.f;
+        else L = 0.f;
+        wv[t] = L * s_dt[J] * xy[t];
+        const float mm = (J < I) ? wv[t] * cb[t] : 0.f;
+        rowsum += mm;
+        xy[t] = mm;  // column-sum input
+        cb[t] *= L;  // L o CB
+      }
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        const int j = jc * 32 + q4 * 8;
+        store_row_bf16(sW + (j >> 6) * 16384, il, (j & 63) >> 3, &wv[q4 * 8]);
+      }
+#pragma unroll
+      for (int t = 0; t < 16; ++t) lcb[jc * 16 + t] = pack_bf16(cb[2 * t], cb[2 * t + 1]);
+      if (jc <= warp) {
+        const float cs = warp_column_sum(xy);
+        s_col[warp][jc * 32 + lane] = cs;
+      }
+    }
+    fence_async_smem();
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+
+    // ---- phase B: dC += W B_k ; dB += W^T C_k
+    if (tid == 0) {
+      const uint32_t id_dc = idesc_bf16(128, 128, false, true);
+      const uint32_t id_db = idesc_bf16(128, 128, true, true);
+      for (int kk = 0; kk < 8; ++kk) {
+        const uint32_t aoff = (kk >> 2) * 16384 + (kk & 3) * 32;
+        mma_bf16(TdC, desc_sw128(smem_u32(sW) + aoff, 16, 1024),
+                 desc_sw128(smem_u32(sB) + kk * 2048, 16384, 1024), id_dc, (hh > 0) || (kk > 0));
+      }
+      for (int kk = 0; kk < 8; ++kk)
+        mma_bf16(TdB, desc_sw128(smem_u32(sW) + kk * 2048, 16384, 1024),
+                 desc_sw128(smem_u32(sC) + kk * 2048, 16384, 1024), id_db, (hh > 0) || (kk > 0));
+      mma_commit(&bar_mma);
+    }
+    __syncthreads();
+    ok = wait_or_flag(&bar_mma, mma_phase);
+    mma_phase ^= 1;
+    fence_after_sync();
+    if (!ok) break;
+    // L o CB into sW (same physical layout: row i, j contiguous)
+#pragma unroll
+    for (int jc = 0; jc < 4; ++jc)
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        const int j = jc * 32 + q4 * 8;
+        uint4 o;
+        o.x = lcb[jc * 16 + q4 * 4 + 0];
+        o.y = lcb[jc * 16 + q4 * 4 + 1];
+        o.z = lcb[jc * 16 + q4 * 4 + 2];
+        o.w = lcb[jc * 16 + q4 * 4 + 3];
+        *(uint4*)(sW + (j >> 6) * 16384 + sw128(il, (j & 63) >> 3)) = o;
+      }
+    fence_async_smem();
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+
+    // ---- phase C: Gx = (L o CB)^T dY_k -> T0[0,64) ; Gs = B_k gout^T -> T0[64,128) ;
+    //               CH = C_k Hin^T -> T1[0,64)
+    if (tid == 0) {
+      const uint32_t id_mm = idesc_bf16(128, 64, true, true);
+      const uint32_t id_km = idesc_bf16(128, 64, false, true);
+      for (int kk = 0; kk < 8; ++kk)
+        mma_bf16(T0, desc_sw128(smem_u32(sW) + kk * 2048, 16384, 1024),
+                 desc_sw128(smem_u32(sDY) + kk * 2048, 16384, 1024), id_mm, kk > 0);
+      for (int kk = 0; kk < 8; ++kk) {
+        const uint32_t aoff = (kk >> 2) * 16384 + (kk & 3) * 32;
+        mma_bf16(T0 + 64, desc_sw128(smem_u32(sB) + aoff, 16, 1024),
+                 desc_sw128(smem_u32(sG) + kk * 2048, 16384, 1024), id_km, kk > 0);
+        mma_bf16(T1, desc_sw128(smem_u32(sC) + aoff, 16, 1024),
+                 desc_sw128(smem_u32(sH) + kk * 2048, 16384, 1024), id_km, kk > 0);
+      }
+      mma_commit(&bar_mma);
+    }
+    __syncthreads();
+    ok = wait_or_flag(&bar_mma, mma_phase);
+    mma_phase ^= 1;
+    fence_after_sync();
+    if (!ok) break;
+
+    // rows x_j and dy_i (unscaled) into registers, then scale the tiles in place:
+    // X rows j by exp(cs_end - cs_j) dt_j, dY rows i by exp(cs_i - ref)
+    uint4 xr[8], dyr[8];
+#pragma unroll
+    for (int ch = 0; ch < 8; ++ch) {
+      xr[ch] = *(const uint4*)(sX + sw128(il, ch));
+      dyr[ch] = *(const uint4*)(sDY + sw128(il, ch));
+    }
+    __syncthreads();
+    for (int e = tid; e < 128 * 8; e += kTcThreads) {
+      const int r = e >> 3;
+      const int R = base + r;
+      const float sx = exp2f(end2 - s_cs2[R]) * s_dt[R];
+      const float sy = exp2f(s_cs2[R] - ref2);
+      const uint4 vx = *(const uint4*)(sX + e * 16);
+      const uint4 vy = *(const uint4*)(sDY + e * 16);
+      const __nv_bfloat162* px = (const __nv_bfloat162*)&vx;
+      const __nv_bfloat162* py = (const __nv_bfloat162*)&vy;
+      uint4 ox, oy;
+      uint32_t* qx = (uint32_t*)&ox;
+      uint32_t* qy = (uint32_t*)&oy;
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const float2 fx = __bfloat1622float2(px[t]);
+        const float2 fy = __bfloat1622float2(py[t]);
+        qx[t] = pack_bf16(fx.x * sx, fx.y * sx);
+        qy[t] = pack_bf16(fy.x * sy, fy.y * sy);
+      }
+      *(uint4*)(sX + e * 16) = ox;
+      *(uint4*)(sDY + e * 16) = oy;
+    }
+    fence_async_smem();
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+
+    // ---- phase D: dC += (e o dY_k) Hin ; dB += (f o X_k) gout   (K = p)
+    if (tid == 0) {
+      const uint32_t id = idesc_bf16(128, 128, false, false);
+      for (int kk = 0; kk < 4; ++kk) {
+        mma_bf16(TdC, desc_sw128(smem_u32(sDY) + kk * 32, 16, 1024),
+                 desc_sw128(smem_u32(sH) + kk * 32, 16, 1024), id, 1);
+        mma_bf16(TdB, desc_sw128(smem_u32(sX) + kk * 32, 16, 1024),
+                 desc_sw128(smem_u32(sG) + kk * 32, 16, 1024), id, 1);
+      }
+      mma_commit(&bar_mma);
+    }
+
+    // ---- epilogue of the head (overlaps phase D): dx, drive, e, statein, dD
+    float drive = 0.f, ej = 0.f, stin = 0.f, dd = 0.f;
+    {
+      const float sgs = exp2f(end2 - s_cs2[I]);
+      const float dtI = s_dt[I];
+      const float Dh = D[h];
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        float gx[32], gs[32], ch[32];
+        tmem_ld32(T0 + lane_base + half * 32, gx);
+        tmem_ld32(T0 + lane_base + 64 + half * 32, gs);
+        tmem_ld32(T1 + lane_base + half * 32, ch);
+        tmem_wait_ld();
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const int cidx = half * 4 + q4;
+          const __nv_bfloat162* px = (const __nv_bfloat162*)&xr[cidx];
+          const __nv_bfloat162* py = (const __nv_bfloat162*)&dyr[cidx];
+          float o8[8];
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            const float2 xf = __bfloat1622float2(px[t]);
+            const float2 yf = __bfloat1622float2(py[t]);
+            const int m = q4 * 8 + 2 * t;
+            const float g0 = fmaf(sgs, gs[m], gx[m]);
+            const float g1 = fmaf(sgs, gs[m + 1], gx[m + 1]);
+            o8[2 * t] = fmaf(dtI, g0, Dh * yf.x);
+            o8[2 * t + 1] = fmaf(dtI, g1, Dh * yf.y);
+            drive = fmaf(xf.x, g0, fmaf(xf.y, g1, drive));
+            ej = fmaf(xf.x, gs[m], fmaf(xf.y, gs[m + 1], ej));
+            stin = fmaf(yf.x, ch[m], fmaf(yf.y, ch[m + 1], stin));
+            dd = fmaf(yf.x, xf.x, fmaf(yf.y, xf.y, dd));
+          }
+          store_row_bf16(sW, il, cidx, o8);  // dx staging: tile [128 rows][64 p]
+        }
+      }
+      ej *= sgs * dtI;
+      stin *= exp2f(s_cs2[I] - ref2);
+    }
+    fence_async_smem();
+    __syncthreads();
+    if (tid == 0) {
+      tma_store_2d(&maps.dx, sW, h * d.P, row0);
+      bulk_commit();
+    }
+    // ---- dcs, reverse cumsum, ddt, dA and dD partials
+    const float esum = block_sum(ej, scratch);
+    {
+      float colsum = 0.f;
+      for (int w = il >> 5; w < 4; ++w) colsum += s_col[w][il];
+      float dcs = rowsum - colsum + stin - ej;
+      if (il == 127) dcs += esum + exp2f(end2 - ref2) * hg;
+      s_v[il] = dcs;
+    }
+    __syncthreads();
+    const float rv = s_v[127 - il];
+    const float da = block_inclusive_scan(rv, scratch);  // syncs: every rv read before reuse
+    const int Jr = base + 127 - il;                        // row whose da this thread holds
+    s_v[il] = drive;
+    __syncthreads();
+    ddt[((size_t)crow + Jr) * d.H + h] = s_v[127 - il] + A[h] * da;
+    const float a_sum = block_sum(s_dt[Jr] * da, scratch);
+    const float d_sum = block_sum(dd, scratch);
+    if (tid == 0) {
+      const size_t slot = (((size_t)b * d.nc + c) * nblk + k) * d.H + h;
+      dA_part[slot] = a_sum;
+      dD_part[slot] = d_sum;
+    }
+    // ---- end of head: phase D done, dx staging read, before sW / sX / sDY / sH / sG reuse
+    __syncthreads();
+    ok = wait_or_flag(&bar_mma, mma_phase);
+    mma_phase ^= 1;
+    fence_after_sync();
+    if (tid == 0) {
+      bulk_wait_read0();
+      if (ok && hh + 1 < kh) issue_head_loads(h + 1);
+    }
+    __syncthreads();
+  }
+
+  // ---- dC and dB of the block (summed over the CTA's heads) -> bf16 -> TMA store
+  if (ok) {
+    const int il = tid;
+    uint8_t* stC = sW;           // 2 tiles [128][128 B]
+    uint8_t* stB = sm + kBwX;    // sX + sDY: 2 tiles
+#pragma unroll
+    for (int jc = 0; jc < 4; ++jc) {
+      float vc[32], vb[32];
+      tmem_ld32(TdC + lane_base + jc * 32, vc);
+      tmem_ld32(TdB + lane_base + jc * 32, vb);
+      tmem_wait_ld();
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        const int nn = jc * 32 + q4 * 8;
+        store_row_bf16(stC + (nn >> 6) * 16384, il, (nn & 63) >> 3, &vc[q4 * 8]);
+        store_row_bf16(stB + (nn >> 6) * 16384, il, (nn & 63) >> 3, &vb[q4 * 8]);
+      }
+    }
+    fence_async_smem();
+    __syncthreads();
+    if (tid == 0) {
+      tma_store_2d(&maps.dC, stC, g * d.N, row0);
+      tma_store_2d(&maps.dC, stC + 16384, g * d.N + 64, row0);
+      tma_store_2d(&maps.dB, stB, g * d.N, row0);
+      tma_store_2d(&maps.dB, stB + 16384, g * d.N + 64, row0);
+      bulk_commit();
+    }
+  }
+  if (tid == 0) bulk_wait0();
+  fence_before_sync();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tm, 512);
+}
+
+// ---------------------------------------------------------------------------
+// Host side: tensor maps through the driver entry point (no libcuda link).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = (EncodeTiledFn)p;
+  });
+  return fn;
+}
+
+// 2D bf16 row-major [rows][cols] map with a {64, box_rows} SW128 box.
+bool map_bf16(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+TcDims tc_dims(const Problem& p) { return TcDims{p.B, p.T, p.H, p.P, p.N, p.G, p.Q, p.nc, p.hpg}; }
+
+template <typename K>
+cudaError_t set_smem_tc(K kernel, size_t bytes) {
+  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+}
+
+}  // namespace
+
+static int g_force_path = -1;  // -1 automatic, 0 SIMT only
+
+bool tc_supported(const Problem& p) {
+  if (g_force_path == 0) return false;
+  return p.bf16 && p.P == 64 && p.N == 128 && (p.Q == 128 || p.Q == 256) && encode_fn() != nullptr;
+}
+
+void tc_force_path(int path) { g_force_path = path; }
+
+bool tc_backward_supported(const Problem& p) { return tc_supported(p); }
+
+// S_c (mode 0, from x and B) or R_c (mode 1, from dy and C) into `out`; cs_last.
+cudaError_t tc_chunk_outer(const Problem& p, int mode, float* out) {
+  OuterMaps maps;
+  const void* u = mode == 0 ? p.x : p.dy;
+  const void* v = mode == 0 ? p.Bm : p.Cm;
+  if (!map_bf16(&maps.u, u, (uint64_t)p.B * p.T, (uint64_t)p.H * p.P, p.Q) ||
+      !map_bf16(&maps.v, v, (uint64_t)p.B * p.T, (uint64_t)p.G * p.N, p.Q))
+    return cudaErrorInvalidValue;
+  const size_t smem = 3 * (size_t)p.Q * 128 + 1024;
+  const TcDims d = tc_dims(p);
+  cudaError_t e;
+  if (mode == 0) {
+    if ((e = set_smem_tc(k_chunk_outer_tc<0>, smem)) != cudaSuccess) return e;
+    LaunchScope ls("chunk_state_tc", p.stream);
+    k_chunk_outer_tc<0><<<dim3(p.nc, p.H, p.B), kTcThreads, smem, p.stream>>>(maps, d, p.dt, p.A,
+                                                                              out, p.cs_last);
+  } else {
+    if ((e = set_smem_tc(k_chunk_outer_tc<1>, smem)) != cudaSuccess) return e;
+    LaunchScope ls("chunk_dstate_tc", p.stream);
+    k_chunk_outer_tc<1><<<dim3(p.nc, p.H, p.B), kTcThreads, smem, p.stream>>>(maps, d, p.dt, p.A,
+                                                                              out, p.cs_last);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t tc_forward_scan(const Problem& p) {
+  ScanMaps maps;
+  const uint64_t rows = (uint64_t)p.B * p.T;
+  if (!map_bf16(&maps.x, p.x, rows, (uint64_t)p.H * p.P, 128) ||
+      !map_bf16(&maps.B, p.Bm, rows, (uint64_t)p.G * p.N, 128) ||
+      !map_bf16(&maps.C, p.Cm, rows, (uint64_t)p.G * p.N, 128) ||
+      !map_bf16(&maps.y, p.y, rows, (uint64_t)p.H * p.P, 128))
+    return cudaErrorInvalidValue;
+  const size_t smem = kScanBytes + 1024;
+  cudaError_t e = set_smem_tc(k_fwd_scan_tc, smem);
+  if (e != cudaSuccess) return e;
+  {
+    LaunchScope ls("chunk_scan_tc", p.stream);
+    k_fwd_scan_tc<<<dim3(p.nc, p.H, p.B), kTcThreads, smem, p.stream>>>(maps, tc_dims(p), p.dt,
+                                                                       p.A, p.D, p.hist);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t tc_backward(const Problem& p) {
+  cudaError_t e = tc_chunk_outer(p, 1, p.dstate);
+  if (e != cudaSuccess) return e;
+  if ((e = simt_state_pass_bwd(p)) != cudaSuccess) return e;
+  BwdMaps maps;
+  const uint64_t rows = (uint64_t)p.B * p.T;
+  if (!map_bf16(&maps.x, p.x, rows, (uint64_t)p.H * p.P, 128) ||
+      !map_bf16(&maps.dy, p.dy, rows, (uint64_t)p.H * p.P, 128) ||
+      !map_bf16(&maps.B, p.Bm, rows, (uint64_t)p.G * p.N, 128) ||
+      !map_bf16(&maps.C, p.Cm, rows, (uint64_t)p.G * p.N, 128) ||
+      !map_bf16(&maps.dx, p.dx, rows, (uint64_t)p.H * p.P, 128) ||
+      !map_bf16(&maps.dB, p.dB, rows, (uint64_t)p.G * p.N, 128) ||
+      !map_bf16(&maps.dC, p.dC, rows, (uint64_t)p.G * p.N, 128))
+    return cudaErrorInvalidValue;
+  const size_t smem = kBwBytes + 1024;
+  if ((e = set_smem_tc(k_bwd_tc, smem)) != cudaSuccess) return e;
+  const int nblk = p.Q / 128;
+  const int nsub = 1;
+  {
+    LaunchScope ls("bwd_tc", p.stream);
+    k_bwd_tc<<<dim3(nblk * p.nc, p.G * nsub, p.B), kTcThreads, smem, p.stream>>>(
+        maps, tc_dims(p), nsub, p.dt, p.A, p.D, p.hist, p.dstate, p.ddt, p.dA_part, p.dD_part);
+  }
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  const int nparts = p.B * p.nc * nblk;
+  return simt_reduce_heads(p, nparts, nparts);
+}
+
+cudaError_t tc_read_and_clear_error(unsigned int* out) {
+  cudaError_t e = cudaMemcpyFromSymbol(out, g_tc_error, sizeof(unsigned int));
+  if (e != cudaSuccess) return e;
+  const unsigned int zero = 0;
+  return cudaMemcpyToSymbol(g_tc_error, &zero, sizeof(unsigned int));
+}
 
 }  // namespace ssd

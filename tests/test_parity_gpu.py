@@ -46,6 +46,9 @@ SMALL = [
     (1, 256, 2, 128, 128, 1, 128, "f32", True, "softplus"),
     (1, 128, 2, 64, 256, 1, 64, "bf16", True, "softplus"),
     (1, 32, 8, 16, 32, 8, 32, "f32", True, "softplus"),  # one chunk, G = H
+    (1, 384, 2, 64, 128, 1, 128, "bf16", True, "decay_span"),
+    (2, 256, 6, 64, 128, 3, 128, "bf16", False, "softplus"),
+    (1, 128, 2, 64, 128, 2, 128, "bf16", True, "softplus"),  # one chunk
 ]
 
 
@@ -154,3 +157,26 @@ def test_full_size_workload_one_group(idx):
     assert not bad, errs
     for v in gpu.values():
         assert np.isfinite(v).all()
+
+
+@pytest.mark.parametrize("q", [128, 256])
+def test_tensor_core_and_simt_paths_agree(q):
+    """The tcgen05 path and the SIMT path (forced) give the same results
+    within the bf16 tolerance, and both match the oracle."""
+    from state_space_model_analytic_gb300 import _native as nat
+    dims = synth.Dims(2, 512, 4, 64, 128, 2, q, "bf16")
+    inp = synth.make_inputs(dims, 21, True, "softplus")
+    dev = to_device(dims, inp)
+    assert nat.lib().ssd_kernel_path(nat.make_dims(2, 512, 4, 64, 128, 2, q, True)) == 1
+    tc = run_gpu(dims, dev)
+    nat.check(nat.lib().ssd_force_kernel_path(0))
+    try:
+        simt = run_gpu(dims, dev)
+    finally:
+        nat.check(nat.lib().ssd_force_kernel_path(-1))
+    ref = run_oracle(dims, inp)
+    for k in tc:
+        assert rel_err(tc[k], ref[k]) < TOL["bf16"], k
+        assert rel_err(simt[k], ref[k]) < TOL["bf16"], k
+        assert rel_err(tc[k], simt[k]) < TOL["bf16"], k
+    nat.check(nat.lib().ssd_device_status())

@@ -75,6 +75,9 @@ def kernel_bytes(name, d, has_h0):
         "bwd_col": 3 * z["x"] + z["dt"] + 3 * z["bc"] + z["st"] + 3 * z["tokh"],
         "bwd_row": 2 * z["x"] + z["dt"] + 3 * z["bc"] + z["st"] + 2 * z["tokh"],
         "bwd_dt": 2 * z["dt"] + 2 * z["st"] + 5 * z["tokh"],
+        # tensor-core backward: x, dy, dt, B, C, history, state gradient in;
+        # dx, ddt, dB, dC out (dA, dD partials are negligible)
+        "bwd": 3 * z["x"] + 2 * z["dt"] + 4 * z["bc"] + 2 * z["st"],
         "reduce_heads": 2 * z["small"],
     }
     return table.get(base)

@@ -154,6 +154,13 @@ SSD_API int ssd_force_kernel_path(int path);
  * device).  Returns SSD_OK, SSD_ERR_DEVICE_TIMEOUT or SSD_ERR_CUDA. */
 SSD_API int ssd_device_status(void);
 
+/* Failure-path self test: launches one CTA whose bounded wait on an mbarrier
+ * that nothing completes gives up after about one second and sets the
+ * device error word; the kernel then returns normally.  After the caller
+ * synchronises, ssd_device_status() reports SSD_ERR_DEVICE_TIMEOUT (once).
+ * Returns SSD_OK or SSD_ERR_CUDA (launch failure). */
+SSD_API int ssd_selftest_wait_timeout(void* cuda_stream);
+
 #ifdef __cplusplus
 }
 #endif

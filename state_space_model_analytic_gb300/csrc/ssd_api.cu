@@ -66,6 +66,7 @@ cudaError_t tc_chunk_outer(const Problem& p, int mode, float* out);
 cudaError_t tc_forward_scan(const Problem& p);
 cudaError_t tc_backward(const Problem& p);
 cudaError_t tc_read_and_clear_error(unsigned int* out);
+cudaError_t tc_selftest_timeout(cudaStream_t s);
 
 namespace {
 
@@ -163,7 +164,7 @@ size_t carve(Problem* p, char* base, int which) {
   p->statein = (float*)take(tokh);
   p->eout = (float*)take(tokh);
   p->drive = (float*)take(tokh);
-  p->dA_part = (float*)take(B * nc * H * sizeof(float));
+  p->dA_part = (float*)take(B * nc * (Q / 16) * H * sizeof(float));  // per (chunk, tile or block)
   p->dD_part = (float*)take(B * nc * (Q / 16) * H * sizeof(float));
   if (which == 2) p->hist = (float*)take(states);
   return off;
@@ -268,6 +269,13 @@ int ssd_device_status(void) {
   cudaError_t e = tc_read_and_clear_error(&flag);
   if (e != cudaSuccess) return cuda_fail(e, "ssd_device_status");
   if (flag) return fail(SSD_ERR_DEVICE_TIMEOUT, "a device-side wait gave up (flag 0x%x)", flag);
+  return SSD_OK;
+}
+
+int ssd_selftest_wait_timeout(void* cuda_stream) {
+  g_err.clear();
+  cudaError_t e = tc_selftest_timeout((cudaStream_t)cuda_stream);
+  if (e != cudaSuccess) return cuda_fail(e, "ssd_selftest_wait_timeout");
   return SSD_OK;
 }
 

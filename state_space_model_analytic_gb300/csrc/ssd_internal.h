@@ -44,7 +44,7 @@ struct Problem {
   float* statein;  // [B][T][H]
   float* eout;     // [B][T][H]
   float* drive;    // [B][T][H]
-  float* dA_part;  // [B][nc][H]
+  float* dA_part;  // [B][nc][Q/16][H]  (the used prefix depends on the kernel family)
   float* dD_part;  // [B][nc][Q/16][H]  (tile-count upper bound)
 
   cudaStream_t stream;

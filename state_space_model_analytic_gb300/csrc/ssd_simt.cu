@@ -123,25 +123,34 @@ k_chunk_outer(Dev d, const TIO* __restrict__ u, const TIO* __restrict__ v,
 }
 
 // Forward state pass, in place: hist[c] holds S_c on entry and H_{c-1} on exit.
+// Each thread owns 4 consecutive (p, n) elements (float4); the loads of the
+// next chunks are issued ahead of the dependent update.
 __global__ void __launch_bounds__(kThreads)
 k_state_pass_fwd(Dev d, float* __restrict__ hist, const float* __restrict__ cs_last,
                  const float* __restrict__ h0, float* __restrict__ final_state) {
   const int PN = d.P * d.N;
-  const int pn = blockIdx.x * blockDim.x + threadIdx.x;
+  const int q = blockIdx.x * blockDim.x + threadIdx.x;  // float4 index within [P*N]
   const int h = blockIdx.y, b = blockIdx.z;
-  if (pn >= PN) return;
+  if (q * 4 >= PN) return;
   const size_t bh = (size_t)b * d.H + h;
-  float hc = h0 ? h0[bh * PN + pn] : 0.f;
+  float4 hc = h0 ? reinterpret_cast<const float4*>(h0 + bh * PN)[q] : make_float4(0.f, 0.f, 0.f, 0.f);
   const float* cl = cs_last + bh * d.nc;
-  float s_next = hist[(((size_t)b * d.nc + 0) * d.H + h) * PN + pn];
+  const size_t stride4 = (size_t)d.H * PN / 4;  // float4 step between chunks
+  float4* p4 = reinterpret_cast<float4*>(hist + (((size_t)b * d.nc) * d.H + h) * PN) + q;
+  float4 s0 = p4[0];
+  float4 s1 = d.nc > 1 ? p4[stride4] : s0;
   for (int c = 0; c < d.nc; ++c) {
-    const size_t idx = (((size_t)b * d.nc + c) * d.H + h) * PN + pn;
-    const float s = s_next;
-    if (c + 1 < d.nc) s_next = hist[idx + (size_t)d.H * PN];
-    hist[idx] = hc;
-    hc = fmaf(expf(cl[c]), hc, s);
+    const float4 s = s0;
+    s0 = s1;
+    if (c + 2 < d.nc) s1 = p4[(size_t)(c + 2) * stride4];
+    p4[(size_t)c * stride4] = hc;
+    const float e = expf(cl[c]);
+    hc.x = fmaf(e, hc.x, s.x);
+    hc.y = fmaf(e, hc.y, s.y);
+    hc.z = fmaf(e, hc.z, s.z);
+    hc.w = fmaf(e, hc.w, s.w);
   }
-  if (final_state) final_state[bh * PN + pn] = hc;
+  if (final_state) reinterpret_cast<float4*>(final_state + bh * PN)[q] = hc;
 }
 
 // Backward state pass, in place: dstate[c] holds R_c on entry and g_c on exit.
@@ -149,21 +158,29 @@ __global__ void __launch_bounds__(kThreads)
 k_state_pass_bwd(Dev d, float* __restrict__ dstate, const float* __restrict__ cs_last,
                  float* __restrict__ dh0) {
   const int PN = d.P * d.N;
-  const int pn = blockIdx.x * blockDim.x + threadIdx.x;
+  const int q = blockIdx.x * blockDim.x + threadIdx.x;
   const int h = blockIdx.y, b = blockIdx.z;
-  if (pn >= PN) return;
+  if (q * 4 >= PN) return;
   const size_t bh = (size_t)b * d.H + h;
   const float* cl = cs_last + bh * d.nc;
-  float gc = 0.f;
-  float r_next = dstate[(((size_t)b * d.nc + (d.nc - 1)) * d.H + h) * PN + pn];
-  for (int c = d.nc - 1; c >= 0; --c) {
-    const size_t idx = (((size_t)b * d.nc + c) * d.H + h) * PN + pn;
-    const float r = r_next;
-    if (c > 0) r_next = dstate[idx - (size_t)d.H * PN];
-    dstate[idx] = gc;
-    gc = fmaf(expf(cl[c]), gc, r);
+  const size_t stride4 = (size_t)d.H * PN / 4;
+  float4* p4 = reinterpret_cast<float4*>(dstate + (((size_t)b * d.nc) * d.H + h) * PN) + q;
+  float4 gc = make_float4(0.f, 0.f, 0.f, 0.f);
+  const int last = d.nc - 1;
+  float4 r0 = p4[(size_t)last * stride4];
+  float4 r1 = last > 0 ? p4[(size_t)(last - 1) * stride4] : r0;
+  for (int c = last; c >= 0; --c) {
+    const float4 r = r0;
+    r0 = r1;
+    if (c - 2 >= 0) r1 = p4[(size_t)(c - 2) * stride4];
+    p4[(size_t)c * stride4] = gc;
+    const float e = expf(cl[c]);
+    gc.x = fmaf(e, gc.x, r.x);
+    gc.y = fmaf(e, gc.y, r.y);
+    gc.z = fmaf(e, gc.z, r.z);
+    gc.w = fmaf(e, gc.w, r.w);
   }
-  if (dh0) dh0[bh * PN + pn] = gc;
+  if (dh0) reinterpret_cast<float4*>(dh0 + bh * PN)[q] = gc;
 }
 
 // ---------------------------------------------------------------------------
@@ -754,7 +771,7 @@ cudaError_t backward_t(const Problem& p) {
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     {
       LaunchScope ls_("state_pass_bwd", p.stream);
-      k_state_pass_bwd<<<dim3((p.P * p.N + kThreads - 1) / kThreads, p.H, p.B), kThreads, 0,
+      k_state_pass_bwd<<<dim3((p.P * p.N / 4 + kThreads - 1) / kThreads, p.H, p.B), kThreads, 0,
                          p.stream>>>(d, p.dstate, p.cs_last, p.dh0);
     }
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
@@ -811,7 +828,7 @@ cudaError_t simt_state_pass_fwd(const Problem& p, float* hist, const float* cs_l
   const Dev d = dev_of(p);
   {
     LaunchScope ls_("state_pass_fwd", p.stream);
-    k_state_pass_fwd<<<dim3((p.P * p.N + kThreads - 1) / kThreads, p.H, p.B), kThreads, 0,
+    k_state_pass_fwd<<<dim3((p.P * p.N / 4 + kThreads - 1) / kThreads, p.H, p.B), kThreads, 0,
                        p.stream>>>(d, hist, cs_last, p.h0, p.final_state);
   }
   return cudaGetLastError();
@@ -821,7 +838,7 @@ cudaError_t simt_state_pass_bwd(const Problem& p) {
   const Dev d = dev_of(p);
   {
     LaunchScope ls_("state_pass_bwd", p.stream);
-    k_state_pass_bwd<<<dim3((p.P * p.N + kThreads - 1) / kThreads, p.H, p.B), kThreads, 0,
+    k_state_pass_bwd<<<dim3((p.P * p.N / 4 + kThreads - 1) / kThreads, p.H, p.B), kThreads, 0,
                        p.stream>>>(d, p.dstate, p.cs_last, p.dh0);
   }
   return cudaGetLastError();

@@ -35,8 +35,9 @@ namespace {
 
 constexpr int kTcThreads = 128;
 constexpr float kLog2e = 1.4426950408889634f;
-// Polls of an mbarrier before a kernel gives up and records a timeout.
-constexpr uint32_t kWaitLimit = 1u << 22;
+// Wall time (ns) an mbarrier wait may take before the kernel gives up and
+// records a timeout.
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
 
 // ---------------------------------------------------------------------------
 // Device error word: a bounded wait that gives up sets it; the host reads it
@@ -46,7 +47,7 @@ __device__ unsigned int g_tc_error;
 // Every thread of the CTA waits; the outcome is made uniform across the CTA
 // (so a timeout never splits the threads at a later barrier).
 __device__ __forceinline__ bool wait_or_flag(uint64_t* bar, uint32_t parity) {
-  const bool mine = mbar_wait(bar, parity, kWaitLimit);
+  const bool mine = mbar_wait(bar, parity, kWaitLimitNs);
   const bool all = __syncthreads_and(mine) != 0;
   if (!all && threadIdx.x == 0) atomicOr(&g_tc_error, 1u);
   return all;
@@ -200,12 +201,12 @@ struct ScanMaps {
   CUtensorMap y;  // [B*T][H*P] bf16, box {64, 128} (store)
 };
 
-// shared-memory layout of k_fwd_scan_tc (offsets from the 1024-aligned base)
-constexpr uint32_t kScanR1 = 0;            // C tile (32K) + B tile (32K); later M (32K), y staging
-constexpr uint32_t kScanX = 65536;         // X block [128][128 B]
-constexpr uint32_t kScanXw = 81920;        // w-scaled X block 0 (Q = 256)
-constexpr uint32_t kScanH = 98304;         // H as bf16 B operand (16K)
-constexpr uint32_t kScanBytes = 114688;
+// shared-memory layout of k_fwd_scan_tc (offsets from the 1024-aligned base);
+// 96 KB so that two CTAs fit on one SM
+constexpr uint32_t kScanR1 = 0;       // C tile (32K) + B tile (32K); M and y staging reuse the C part
+constexpr uint32_t kScanX = 65536;    // X block [128 rows][64 p]
+constexpr uint32_t kScanH = 81920;    // state as bf16 B operand, row n, 64 p (MN-major)
+constexpr uint32_t kScanBytes = 98304;
 
 __global__ void __launch_bounds__(kTcThreads)
 k_fwd_scan_tc(const __grid_constant__ ScanMaps maps, TcDims d, const float* __restrict__ dt,
@@ -215,10 +216,9 @@ k_fwd_scan_tc(const __grid_constant__ ScanMaps maps, TcDims d, const float* __re
   uint8_t* sm = (uint8_t*)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
   uint8_t* sC = sm + kScanR1;
   uint8_t* sB = sm + kScanR1 + 32768;
-  uint8_t* sM = sm + kScanR1;   // after the CB / Ys / S_0 products are done
+  uint8_t* sM = sm + kScanR1;   // after the CB / Ys products are done
   uint8_t* sY = sm + kScanR1;   // after the Y product is done
   uint8_t* sX = sm + kScanX;
-  uint8_t* sXw = sm + kScanXw;
   uint8_t* sH = sm + kScanH;
   __shared__ float s_cs2[256], s_dt[256], scratch[4];
   __shared__ float s_E[4][128];  // per-warp column factors exp(cs_r - cs_j) dt_j
@@ -251,31 +251,38 @@ k_fwd_scan_tc(const __grid_constant__ ScanMaps maps, TcDims d, const float* __re
   uint32_t load_phase = 0, mma_phase = 0;
   bool ok = true;
 
-  // H_{c-1} (fp32 [P][N]) -> bf16 K-major operand: row p, K = n (two 64-wide tiles)
+  auto issue_loads = [&](int row0) {
+    mbar_expect_tx(&bar_load, 80 * 1024);
+    tma_load_2d(sC, &maps.C, g * d.N, row0, &bar_load);
+    tma_load_2d(sC + 16384, &maps.C, g * d.N + 64, row0, &bar_load);
+    tma_load_2d(sB, &maps.B, g * d.N, row0, &bar_load);
+    tma_load_2d(sB + 16384, &maps.B, g * d.N + 64, row0, &bar_load);
+    tma_load_2d(sX, &maps.x, h * d.P, row0, &bar_load);
+  };
+  const int crow = b * d.T + c * Q;
+  if (tid == 0) issue_loads(crow);
+
+  // H_{c-1} (fp32 [P][N]) -> bf16 rows n (64 p each): the MN-major B operand of C H^T
   const float* Hg = hist + (((size_t)b * d.nc + c) * d.H + h) * (size_t)(64 * 128);
   chunk_cumsum_tc(d, dt, A, b, c, h, s_cs2, s_dt, scratch);
-  for (int e = tid; e < 64 * 16; e += kTcThreads) {
-    const int p = e >> 4, ch = e & 15;  // 16 chunks of 8 n per row
-    const float4 lo = *(const float4*)(Hg + p * 128 + ch * 8);
-    const float4 hi = *(const float4*)(Hg + p * 128 + ch * 8 + 4);
-    uint4 o;
-    o.x = pack_bf16(lo.x, lo.y);
-    o.y = pack_bf16(lo.z, lo.w);
-    o.z = pack_bf16(hi.x, hi.y);
-    o.w = pack_bf16(hi.z, hi.w);
-    *(uint4*)(sH + (ch >> 3) * 8192 + sw128(p, ch & 7)) = o;
+  {
+    const int n = tid;
+#pragma unroll
+    for (int ch = 0; ch < 8; ++ch) {
+      float v8[8];
+#pragma unroll
+      for (int t = 0; t < 8; ++t) v8[t] = Hg[(size_t)(ch * 8 + t) * 128 + n];
+      uint4 o;
+      o.x = pack_bf16(v8[0], v8[1]);
+      o.y = pack_bf16(v8[2], v8[3]);
+      o.z = pack_bf16(v8[4], v8[5]);
+      o.w = pack_bf16(v8[6], v8[7]);
+      *(uint4*)(sH + sw128(n, ch)) = o;
+    }
   }
 
   for (int blk = 0; blk < nblk && ok; ++blk) {
-    const int row0 = b * d.T + c * Q + blk * 128;
-    if (tid == 0) {
-      mbar_expect_tx(&bar_load, 80 * 1024);
-      tma_load_2d(sC, &maps.C, g * d.N, row0, &bar_load);
-      tma_load_2d(sC + 16384, &maps.C, g * d.N + 64, row0, &bar_load);
-      tma_load_2d(sB, &maps.B, g * d.N, row0, &bar_load);
-      tma_load_2d(sB + 16384, &maps.B, g * d.N + 64, row0, &bar_load);
-      tma_load_2d(sX, &maps.x, h * d.P, row0, &bar_load);
-    }
+    const int row0 = crow + blk * 128;
     // per-warp column factors of this block: E[w][jj] = exp(cs_r - cs_J) dt_J, J < r
     const int base = blk * 128;
     for (int e = tid; e < 4 * 128; e += kTcThreads) {
@@ -285,32 +292,10 @@ k_fwd_scan_tc(const __grid_constant__ ScanMaps maps, TcDims d, const float* __re
     }
     // reference log-decay of the block's state term: cs before row `base`
     const float ref2 = blk == 0 ? 0.f : s_cs2[base - 1];
-    __syncthreads();
+    fence_async_smem();
     ok = wait_or_flag(&bar_load, load_phase);
     load_phase ^= 1;
     if (!ok) break;
-    const bool need_s0 = (blk == 0 && nblk == 2);
-    if (need_s0) {
-      // w o X_0 with w_j = exp(cs_127 - cs_j) dt_j, for the mid-chunk state
-      for (int e = tid; e < 128 * 8; e += kTcThreads) {
-        const int r = e >> 3;
-        const uint32_t off = (uint32_t)e * 16u;
-        const float s = exp2f(s_cs2[127] - s_cs2[r]) * s_dt[r];
-        const uint4 v = *(const uint4*)(sX + off);
-        const __nv_bfloat162* p = (const __nv_bfloat162*)&v;
-        uint4 o;
-        uint32_t* q = (uint32_t*)&o;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const float2 f = __bfloat1622float2(p[k]);
-          q[k] = pack_bf16(f.x * s, f.y * s);
-        }
-        *(uint4*)(sXw + off) = o;
-      }
-    }
-    fence_async_smem();
-    fence_before_sync();
-    __syncthreads();
     fence_after_sync();
     if (tid == 0) {
       // CB = C_blk B_blk^T  (128 x 128, K = N)
@@ -320,24 +305,15 @@ k_fwd_scan_tc(const __grid_constant__ ScanMaps maps, TcDims d, const float* __re
         mma_bf16(tCB, desc_sw128(smem_u32(sC) + off, 16, 1024),
                  desc_sw128(smem_u32(sB) + off, 16, 1024), id_cb, kk > 0);
       }
-      // Ys = C_blk Hin^T  (128 x 64, K = N); Hin K-major (blk 0) or MN-major (blk 1)
-      const uint32_t id_ys = idesc_bf16(128, 64, false, blk > 0);
+      // Ys = C_blk Hin^T  (128 x 64, K = N); Hin rows n, MN-major
+      const uint32_t id_ys = idesc_bf16(128, 64, false, true);
       for (int kk = 0; kk < 8; ++kk) {
         const uint32_t aoff = (kk >> 2) * 16384 + (kk & 3) * 32;
-        const uint32_t boff = blk == 0 ? (kk >> 2) * 8192 + (kk & 3) * 32 : kk * 2048;
         mma_bf16(tYs, desc_sw128(smem_u32(sC) + aoff, 16, 1024),
-                 desc_sw128(smem_u32(sH) + boff, 16384, 1024), id_ys, kk > 0);
-      }
-      if (need_s0) {
-        // S_0^T = B_0^T (w o X_0): M = n (two 64-wide MN blocks 16K apart), N = p, K = j
-        const uint32_t id_s0 = idesc_bf16(128, 64, true, true);
-        for (int kk = 0; kk < 8; ++kk)
-          mma_bf16(tS0, desc_sw128(smem_u32(sB) + kk * 2048, 16384, 1024),
-                   desc_sw128(smem_u32(sXw) + kk * 2048, 16384, 1024), id_s0, kk > 0);
+                 desc_sw128(smem_u32(sH) + kk * 2048, 16384, 1024), id_ys, kk > 0);
       }
       mma_commit(&bar_mma);
     }
-    __syncthreads();
     ok = wait_or_flag(&bar_mma, mma_phase);
     mma_phase ^= 1;
     fence_after_sync();
@@ -345,30 +321,6 @@ k_fwd_scan_tc(const __grid_constant__ ScanMaps maps, TcDims d, const float* __re
 
     const int il = warp * 32 + lane;  // row inside the block (TMEM lane)
     const int I = base + il;          // row inside the chunk
-    if (need_s0) {
-      // H_mid^T[n][p] = exp(cs_127) H[p][n] + S_0^T[n][p] -> bf16 MN-major (row n)
-      const float e127 = exp2f(s_cs2[127]);
-      const int n = il;
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        float v[32];
-        tmem_ld32(tS0 + lane_base + half * 32, v);
-        tmem_wait_ld();
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          uint4 o;
-          uint32_t* q = (uint32_t*)&o;
-#pragma unroll
-          for (int t = 0; t < 4; ++t) {
-            const int p0 = half * 32 + k * 8 + 2 * t;
-            const float a0 = fmaf(e127, Hg[(size_t)p0 * 128 + n], v[k * 8 + 2 * t]);
-            const float a1 = fmaf(e127, Hg[(size_t)(p0 + 1) * 128 + n], v[k * 8 + 2 * t + 1]);
-            q[t] = pack_bf16(a0, a1);
-          }
-          *(uint4*)(sH + sw128(n, half * 4 + k)) = o;
-        }
-      }
-    }
     // M = CB o L o dt (masked), bf16 K-major A operand: row il, K = j (two 64-wide tiles)
     {
       const int r = base + 32 * warp;
@@ -419,7 +371,6 @@ k_fwd_scan_tc(const __grid_constant__ ScanMaps maps, TcDims d, const float* __re
       }
       mma_commit(&bar_mma);
     }
-    __syncthreads();
     ok = wait_or_flag(&bar_mma, mma_phase);
     mma_phase ^= 1;
     fence_after_sync();
@@ -458,9 +409,72 @@ k_fwd_scan_tc(const __grid_constant__ ScanMaps maps, TcDims d, const float* __re
     if (tid == 0) {
       tma_store_2d(&maps.y, sY, h * d.P, row0);
       bulk_commit();
-      bulk_wait_read0();  // staging (region R1) is reloaded by the next block
     }
-    __syncthreads();
+    if (blk + 1 < nblk) {
+      // mid-chunk state: X_0 rows j scaled in place by exp(cs_127 - cs_j) dt_j,
+      // S_0^T = B_0^T (w o X_0) (M = n, N = p, K = j), H_mid = exp(cs_127) H + S_0
+      for (int e = tid; e < 128 * 8; e += kTcThreads) {
+        const int r = e >> 3;
+        const float s = exp2f(s_cs2[127] - s_cs2[r]) * s_dt[r];
+        const uint4 v = *(const uint4*)(sX + e * 16);
+        const __nv_bfloat162* q2 = (const __nv_bfloat162*)&v;
+        uint4 o;
+        uint32_t* q = (uint32_t*)&o;
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const float2 f = __bfloat1622float2(q2[t]);
+          q[t] = pack_bf16(f.x * s, f.y * s);
+        }
+        *(uint4*)(sX + e * 16) = o;
+      }
+      fence_async_smem();
+      fence_before_sync();
+      __syncthreads();
+      fence_after_sync();
+      if (tid == 0) {
+        const uint32_t id_s0 = idesc_bf16(128, 64, true, true);
+        for (int kk = 0; kk < 8; ++kk)
+          mma_bf16(tS0, desc_sw128(smem_u32(sB) + kk * 2048, 16384, 1024),
+                   desc_sw128(smem_u32(sX) + kk * 2048, 16384, 1024), id_s0, kk > 0);
+        mma_commit(&bar_mma);
+      }
+      ok = wait_or_flag(&bar_mma, mma_phase);
+      mma_phase ^= 1;
+      fence_after_sync();
+      if (!ok) break;
+      const float e127 = exp2f(s_cs2[127]);
+      const int n = il;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        float v[32];
+        tmem_ld32(tS0 + lane_base + half * 32, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          float v8[8];
+#pragma unroll
+          for (int t = 0; t < 8; ++t) {
+            const int p0 = half * 32 + k * 8 + t;
+            v8[t] = fmaf(e127, Hg[(size_t)p0 * 128 + n], v[k * 8 + t]);
+          }
+          uint4 o;
+          o.x = pack_bf16(v8[0], v8[1]);
+          o.y = pack_bf16(v8[2], v8[3]);
+          o.z = pack_bf16(v8[4], v8[5]);
+          o.w = pack_bf16(v8[6], v8[7]);
+          *(uint4*)(sH + sw128(n, half * 4 + k)) = o;
+        }
+      }
+      if (tid == 0) {
+        bulk_wait_read0();  // y staging (region R1) is reloaded next
+        issue_loads(row0 + 128);
+      }
+      // sH written by every thread: visible to the next block's MMA
+      fence_async_smem();
+      fence_before_sync();
+      __syncthreads();
+      fence_after_sync();
+    }
   }
   if (tid == 0) bulk_wait0();
   fence_before_sync();
@@ -530,7 +544,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, int nsub, const float* __restrict__ dt,
          const float* __restrict__ A, const float* __restrict__ D,
          const float* __restrict__ hist, const float* __restrict__ gstate,
-         float* __restrict__ ddt, float* __restrict__ dA_part, float* __restrict__ dD_part) {
+         float* __restrict__ ddt, float* __restrict__ dA_part, float* __restrict__ dD_part,
+         void* __restrict__ dB_out, void* __restrict__ dC_out) {
   extern __shared__ __align__(1024) uint8_t smraw[];
   uint8_t* sm = (uint8_t*)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
   uint8_t* sC = sm + kBwC;
@@ -967,33 +982,88 @@ k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, int nsub, const float* 
     __syncthreads();
   }
 
-  // ---- dC and dB of the block (summed over the CTA's heads) -> bf16 -> TMA store
-  if (ok) {
-    const int il = tid;
-    uint8_t* stC = sW;           // 2 tiles [128][128 B]
-    uint8_t* stB = sm + kBwX;    // sX + sDY: 2 tiles
+  // ---- dC and dB of the block, summed over the CTA's heads in TMEM
+  if (nsub == 1) {
+    if (ok) {  // -> bf16 -> TMA store
+      const int il = tid;
+      uint8_t* stC = sW;         // 2 tiles [128][128 B]
+      uint8_t* stB = sm + kBwX;  // sX + sDY: 2 tiles
 #pragma unroll
-    for (int jc = 0; jc < 4; ++jc) {
-      float vc[32], vb[32];
-      tmem_ld32(TdC + lane_base + jc * 32, vc);
-      tmem_ld32(TdB + lane_base + jc * 32, vb);
-      tmem_wait_ld();
+      for (int jc = 0; jc < 4; ++jc) {
+        float vc[32], vb[32];
+        tmem_ld32(TdC + lane_base + jc * 32, vc);
+        tmem_ld32(TdB + lane_base + jc * 32, vb);
+        tmem_wait_ld();
 #pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        const int nn = jc * 32 + q4 * 8;
-        store_row_bf16(stC + (nn >> 6) * 16384, il, (nn & 63) >> 3, &vc[q4 * 8]);
-        store_row_bf16(stB + (nn >> 6) * 16384, il, (nn & 63) >> 3, &vb[q4 * 8]);
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const int nn = jc * 32 + q4 * 8;
+          store_row_bf16(stC + (nn >> 6) * 16384, il, (nn & 63) >> 3, &vc[q4 * 8]);
+          store_row_bf16(stB + (nn >> 6) * 16384, il, (nn & 63) >> 3, &vb[q4 * 8]);
+        }
+      }
+      fence_async_smem();
+      __syncthreads();
+      if (tid == 0) {
+        tma_store_2d(&maps.dC, stC, g * d.N, row0);
+        tma_store_2d(&maps.dC, stC + 16384, g * d.N + 64, row0);
+        tma_store_2d(&maps.dB, stB, g * d.N, row0);
+        tma_store_2d(&maps.dB, stB + 16384, g * d.N + 64, row0);
+        bulk_commit();
       }
     }
-    fence_async_smem();
-    __syncthreads();
-    if (tid == 0) {
-      tma_store_2d(&maps.dC, stC, g * d.N, row0);
-      tma_store_2d(&maps.dC, stC + 16384, g * d.N + 64, row0);
-      tma_store_2d(&maps.dB, stB, g * d.N, row0);
-      tma_store_2d(&maps.dB, stB + 16384, g * d.N + 64, row0);
-      bulk_commit();
+  } else {
+    // The nsub CTAs of a cluster hold partial sums over disjoint head subsets.
+    // Each dumps its fp32 rows to shared memory (16-byte chunks XOR-swizzled by
+    // row), then CTA `rank` sums rows [rank*128/nsub, ...) over ranks 0..nsub-1
+    // in order and writes bf16 dC, dB.  Every CTA reaches both cluster
+    // barriers, also after a timeout.
+    float* dumpC = (float*)(sm + kBwC);  // 64 KB: C_k, B_k tiles are dead
+    float* dumpB = (float*)(sm + kBwO);  // 64 KB: sO, sX, sDY are dead
+    if (ok) {
+      const int il = tid;
+#pragma unroll
+      for (int jc = 0; jc < 4; ++jc) {
+        float vc[32], vb[32];
+        tmem_ld32(TdC + lane_base + jc * 32, vc);
+        tmem_ld32(TdB + lane_base + jc * 32, vb);
+        tmem_wait_ld();
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const int cc = jc * 8 + q;
+          const int off = il * 128 + ((cc ^ (il & 31)) << 2);
+          *(float4*)(dumpC + off) = make_float4(vc[4 * q], vc[4 * q + 1], vc[4 * q + 2], vc[4 * q + 3]);
+          *(float4*)(dumpB + off) = make_float4(vb[4 * q], vb[4 * q + 1], vb[4 * q + 2], vb[4 * q + 3]);
+        }
+      }
     }
+    cluster_sync();
+    if (ok) {
+      const uint32_t rank = cluster_rank();
+      const int rows_per = 128 / nsub;
+      const uint32_t baseC = smem_u32(dumpC), baseB = smem_u32(dumpB);
+      __nv_bfloat16* gC = (__nv_bfloat16*)dC_out;
+      __nv_bfloat16* gB = (__nv_bfloat16*)dB_out;
+      for (int e = tid; e < rows_per * 32; e += kTcThreads) {
+        const int row = (int)rank * rows_per + (e >> 5), cc = e & 31;
+        const uint32_t off = (uint32_t)(row * 128 + ((cc ^ (row & 31)) << 2)) * 4u;
+        float4 sc = make_float4(0.f, 0.f, 0.f, 0.f), sb = sc;
+        for (int r = 0; r < nsub; ++r) {
+          const float4 a = ld_cluster_f4(map_cluster(baseC + off, (uint32_t)r));
+          const float4 bq = ld_cluster_f4(map_cluster(baseB + off, (uint32_t)r));
+          sc.x += a.x; sc.y += a.y; sc.z += a.z; sc.w += a.w;
+          sb.x += bq.x; sb.y += bq.y; sb.z += bq.z; sb.w += bq.w;
+        }
+        const size_t gi = ((size_t)(row0 + row) * d.G + g) * d.N + cc * 4;
+        uint2 pc, pb;
+        pc.x = pack_bf16(sc.x, sc.y);
+        pc.y = pack_bf16(sc.z, sc.w);
+        pb.x = pack_bf16(sb.x, sb.y);
+        pb.y = pack_bf16(sb.z, sb.w);
+        *(uint2*)(gC + gi) = pc;
+        *(uint2*)(gB + gi) = pb;
+      }
+    }
+    cluster_sync();
   }
   if (tid == 0) bulk_wait0();
   fence_before_sync();
@@ -1116,15 +1186,57 @@ cudaError_t tc_backward(const Problem& p) {
   const size_t smem = kBwBytes + 1024;
   if ((e = set_smem_tc(k_bwd_tc, smem)) != cudaSuccess) return e;
   const int nblk = p.Q / 128;
-  const int nsub = 1;
+  // split a group's heads over a cluster of nsub CTAs when there are too few
+  // (block, chunk, group, batch) units to fill the GPU
+  int nsm = 0, dev = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+  const long units = (long)nblk * p.nc * p.G * p.B;
+  int nsub = 1;
+  while (nsub < 8 && units * nsub < 2L * nsm && p.hpg % (2 * nsub) == 0) nsub *= 2;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(nblk * p.nc, p.G * nsub, p.B);
+  cfg.blockDim = dim3(kTcThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = p.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = nsub;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   {
     LaunchScope ls("bwd_tc", p.stream);
-    k_bwd_tc<<<dim3(nblk * p.nc, p.G * nsub, p.B), kTcThreads, smem, p.stream>>>(
-        maps, tc_dims(p), nsub, p.dt, p.A, p.D, p.hist, p.dstate, p.ddt, p.dA_part, p.dD_part);
+    e = cudaLaunchKernelEx(&cfg, k_bwd_tc, maps, tc_dims(p), nsub, p.dt, p.A, p.D,
+                           (const float*)p.hist, (const float*)p.dstate, p.ddt, p.dA_part,
+                           p.dD_part, p.dB, p.dC);
   }
+  if (e != cudaSuccess) return e;
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const int nparts = p.B * p.nc * nblk;
   return simt_reduce_heads(p, nparts, nparts);
+}
+
+// One CTA waits on an mbarrier that nothing arrives on; the bounded wait gives
+// up after kWaitLimitNs and sets the device error word.  Exercises the
+// timeout path without faulting or hanging the GPU.
+__global__ void k_selftest_wait() {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  (void)wait_or_flag(&bar, 0);
+}
+
+cudaError_t tc_selftest_timeout(cudaStream_t s) {
+  {
+    LaunchScope ls("selftest_wait", s);
+    k_selftest_wait<<<1, kTcThreads, 0, s>>>();
+  }
+  return cudaGetLastError();
 }
 
 cudaError_t tc_read_and_clear_error(unsigned int* out) {

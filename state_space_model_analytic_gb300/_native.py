@@ -19,7 +19,7 @@ SSD_OK, SSD_ERR_INVALID_ARG, SSD_ERR_UNSUPPORTED, SSD_ERR_ALIGNMENT, SSD_ERR_CUD
 EXPORTS = ("ssd_workspace_bytes", "ssd_forward", "ssd_backward", "ssd_last_error",
            "ssd_kernel_launch_count", "ssd_trace_begin", "ssd_trace_end", "ssd_trace_read",
            "ssd_trace_reset", "ssd_kernel_path", "ssd_force_kernel_path", "ssd_device_status",
-           "ssd_selftest_wait_timeout")
+           "ssd_selftest_wait_timeout", "ssd_forward_noalloc")
 
 
 class SsdDims(ctypes.Structure):
@@ -67,6 +67,8 @@ def lib() -> ctypes.CDLL:
             L.ssd_force_kernel_path.argtypes = [ctypes.c_int]
             L.ssd_device_status.restype = ctypes.c_int
             L.ssd_device_status.argtypes = []
+            L.ssd_forward_noalloc.restype = ctypes.c_int
+            L.ssd_forward_noalloc.argtypes = [D] + [_VP] * 11
             L.ssd_selftest_wait_timeout.restype = ctypes.c_int
             L.ssd_selftest_wait_timeout.argtypes = [_VP]
             L.ssd_trace_begin.restype = ctypes.c_int

@@ -178,6 +178,9 @@ int check_smem(const Problem& p) {
 }
 
 }  // namespace
+
+void set_last_error(const char* msg) { g_err = msg; }
+
 }  // namespace ssd
 
 using namespace ssd;

@@ -103,6 +103,76 @@ __device__ __forceinline__ void scale_rows_bf16(const uint8_t* src, uint8_t* dst
   }
 }
 
+// Column sums over the 32 lanes of a warp: lane l returns sum over lanes of v[l].
+__device__ __forceinline__ float warp_column_sum(float (&v)[32]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int s = 16; s >= 1; s >>= 1) {
+    const bool upper = (lane & s) != 0;
+#pragma unroll
+    for (int k = 0; k < s; ++k) {
+      const float send = upper ? v[k] : v[k + s];
+      const float keep = upper ? v[k + s] : v[k];
+      v[k] = keep + __shfl_xor_sync(0xffffffffu, send, s);
+    }
+  }
+  return v[0];
+}
+
+__device__ __forceinline__ void store_row_bf16(uint8_t* tile, int row, int chunk0,
+                                               const float* v8) {
+  uint4 o;
+  o.x = pack_bf16(v8[0], v8[1]);
+  o.y = pack_bf16(v8[2], v8[3]);
+  o.z = pack_bf16(v8[4], v8[5]);
+  o.w = pack_bf16(v8[6], v8[7]);
+  *(uint4*)(tile + sw128(row, chunk0)) = o;
+}
+
+__device__ __forceinline__ void unpack8(const uint4& v, float* f) {
+  const __nv_bfloat162* p = (const __nv_bfloat162*)&v;
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    const float2 x = __bfloat1622float2(p[t]);
+    f[2 * t] = x.x;
+    f[2 * t + 1] = x.y;
+  }
+}
+
+// Scale the 16-byte chunks e = first, first + step, ... of a SW128 bf16 tile
+// (rows of 8 chunks) by a per-row factor.
+template <typename F>
+__device__ __forceinline__ void scale_tile_rows(uint8_t* tile, int nchunks, F&& factor) {
+  for (int e = threadIdx.x; e < nchunks; e += blockDim.x) {
+    const float s = factor(e >> 3);
+    float f[8];
+    unpack8(*(const uint4*)(tile + e * 16), f);
+#pragma unroll
+    for (int t = 0; t < 8; ++t) f[t] *= s;
+    uint4 o;
+    o.x = pack_bf16(f[0], f[1]);
+    o.y = pack_bf16(f[2], f[3]);
+    o.z = pack_bf16(f[4], f[5]);
+    o.w = pack_bf16(f[6], f[7]);
+    *(uint4*)(tile + e * 16) = o;
+  }
+}
+
+// Chunk-local inclusive cumsum (log2 units) with 256 threads, one value each.
+__device__ __forceinline__ void chunk_cumsum_256(const TcDims& d, const float* __restrict__ dt,
+                                                 const float* __restrict__ A, int b, int c, int h,
+                                                 float* s_cs2, float* s_dt, float* scratch) {
+  const int tid = threadIdx.x;
+  float dv = 0.f;
+  if (tid < d.Q) dv = dt[((size_t)b * d.T + (size_t)c * d.Q + tid) * d.H + h];
+  const float cs = block_inclusive_scan(dv * (A[h] * kLog2e), scratch);
+  if (tid < d.Q) {
+    s_cs2[tid] = cs;
+    s_dt[tid] = dv;
+  }
+  __syncthreads();
+}
+
 // ---------------------------------------------------------------------------
 // Chunk outer product on tensor cores: out[b][c][h] (P x N, fp32) =
 //   MODE 0: sum_j exp(cs_last - cs_j) dt_j x_j B_j^T   (chunk state S_c)
@@ -114,7 +184,7 @@ struct OuterMaps {
 };
 
 template <int MODE>
-__global__ void __launch_bounds__(kTcThreads)
+__global__ void __launch_bounds__(256)
 k_chunk_outer_tc(const __grid_constant__ OuterMaps maps, TcDims d, const float* __restrict__ dt,
                  const float* __restrict__ A, float* __restrict__ out,
                  float* __restrict__ cs_last) {
@@ -123,11 +193,11 @@ k_chunk_outer_tc(const __grid_constant__ OuterMaps maps, TcDims d, const float* 
   const int Q = d.Q;
   uint8_t* sV = sm;                      // 2 MN blocks of [Q rows][128 B]
   uint8_t* sU = sm + 2 * Q * 128;        // [Q rows][128 B]
-  __shared__ float s_cs2[256], s_dt[256], s_w[256], scratch[4];
+  __shared__ float s_cs2[256], s_dt[256], s_w[256], scratch[8];
   __shared__ uint64_t bar_load, bar_mma;
   __shared__ uint32_t tmem_base;
   const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-  const int g = h / d.hpg, tid = threadIdx.x, warp = tid >> 5;
+  const int g = h / d.hpg, tid = threadIdx.x, wg = tid >> 7, q = (tid >> 5) & 3;
   const int row0 = b * d.T + c * Q;
 
   if (tid == 0) {
@@ -137,7 +207,7 @@ k_chunk_outer_tc(const __grid_constant__ OuterMaps maps, TcDims d, const float* 
     mbar_init(&bar_mma, 1);
     fence_mbar_init();
   }
-  if (warp == 0) {
+  if (tid < 32) {
     tmem_alloc(&tmem_base, 64);
     tmem_relinquish();
   }
@@ -151,14 +221,12 @@ k_chunk_outer_tc(const __grid_constant__ OuterMaps maps, TcDims d, const float* 
     tma_load_2d(sV + Q * 128, &maps.v, g * d.N + 64, row0, &bar_load);
     tma_load_2d(sU, &maps.u, h * d.P, row0, &bar_load);
   }
-  chunk_cumsum_tc(d, dt, A, b, c, h, s_cs2, s_dt, scratch);
+  chunk_cumsum_256(d, dt, A, b, c, h, s_cs2, s_dt, scratch);
   const float last2 = s_cs2[Q - 1];
-  for (int t = tid; t < Q; t += kTcThreads)
-    s_w[t] = (MODE == 0) ? exp2f(last2 - s_cs2[t]) * s_dt[t] : exp2f(s_cs2[t]);
+  if (tid < Q) s_w[tid] = (MODE == 0) ? exp2f(last2 - s_cs2[tid]) * s_dt[tid] : exp2f(s_cs2[tid]);
   if (tid == 0) cs_last[((size_t)b * d.H + h) * d.nc + c] = last2 * (1.0f / kLog2e);
-  __syncthreads();
-  const bool loaded = wait_or_flag(&bar_load, 0);
-  if (loaded) scale_rows_bf16(sU, sU, Q, s_w);
+  const bool loaded = wait_or_flag(&bar_load, 0);  // also publishes s_w
+  if (loaded) scale_tile_rows(sU, Q * 8, [&](int r) { return s_w[r]; });
   fence_async_smem();
   fence_before_sync();
   __syncthreads();
@@ -172,24 +240,21 @@ k_chunk_outer_tc(const __grid_constant__ OuterMaps maps, TcDims d, const float* 
     }
     mma_commit(&bar_mma);
   }
-  __syncthreads();
   const bool done = loaded && wait_or_flag(&bar_mma, 0);
   fence_after_sync();
   if (done) {
-    const int n = warp * 32 + (tid & 31);
+    // thread (wg, n): columns p in [32 wg, 32 wg + 32) of row n of D = out^T
+    const int n = tid & 127;
     float* dst = out + (((size_t)b * d.nc + c) * d.H + h) * (size_t)(d.P * d.N) + n;
+    float v[32];
+    tmem_ld32(tm + ((uint32_t)(q * 32) << 16) + wg * 32, v);
+    tmem_wait_ld();
 #pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      float v[32];
-      tmem_ld32(tm + ((uint32_t)(warp * 32) << 16) + half * 32, v);
-      tmem_wait_ld();
-#pragma unroll
-      for (int i = 0; i < 32; ++i) dst[(size_t)(half * 32 + i) * d.N] = v[i];
-    }
+    for (int i = 0; i < 32; ++i) dst[(size_t)(wg * 32 + i) * d.N] = v[i];
   }
   fence_before_sync();
   __syncthreads();
-  if (warp == 0) tmem_dealloc(tm, 64);
+  if (tid < 32) tmem_dealloc(tm, 64);
 }
 
 // ---------------------------------------------------------------------------
@@ -208,7 +273,7 @@ constexpr uint32_t kScanX = 65536;    // X block [128 rows][64 p]
 constexpr uint32_t kScanH = 81920;    // state as bf16 B operand, row n, 64 p (MN-major)
 constexpr uint32_t kScanBytes = 98304;
 
-__global__ void __launch_bounds__(kTcThreads)
+__global__ void __launch_bounds__(256, 2)
 k_fwd_scan_tc(const __grid_constant__ ScanMaps maps, TcDims d, const float* __restrict__ dt,
               const float* __restrict__ A, const float* __restrict__ D,
               const float* __restrict__ hist) {
@@ -220,15 +285,16 @@ k_fwd_scan_tc(const __grid_constant__ ScanMaps maps, TcDims d, const float* __re
   uint8_t* sY = sm + kScanR1;   // after the Y product is done
   uint8_t* sX = sm + kScanX;
   uint8_t* sH = sm + kScanH;
-  __shared__ float s_cs2[256], s_dt[256], scratch[4];
-  __shared__ float s_E[4][128];  // per-warp column factors exp(cs_r - cs_j) dt_j
+  __shared__ float s_cs2[256], s_dt[256], scratch[8];
+  __shared__ __align__(16) float s_E[4][128];  // per-warp column factors exp(cs_r - cs_j) dt_j
   __shared__ uint64_t bar_load, bar_mma;
   __shared__ uint32_t tmem_base;
   const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-  const int g = h / d.hpg, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = h / d.hpg, tid = threadIdx.x, wg = tid >> 7, q = (tid >> 5) & 3;
+  const int row = tid & 127;  // TMEM lane / tile row, shared by the two warpgroups
   const int Q = d.Q, nblk = Q / 128;
   const float Dh = D[h];
-  const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+  const uint32_t lane_base = (uint32_t)(q * 32) << 16;
 
   if (tid == 0) {
     prefetch_tmap(&maps.x);
@@ -239,7 +305,7 @@ k_fwd_scan_tc(const __grid_constant__ ScanMaps maps, TcDims d, const float* __re
     mbar_init(&bar_mma, 1);
     fence_mbar_init();
   }
-  if (warp == 0) {
+  if (tid < 32) {
     tmem_alloc(&tmem_base, 256);
     tmem_relinquish();
   }
@@ -262,22 +328,18 @@ k_fwd_scan_tc(const __grid_constant__ ScanMaps maps, TcDims d, const float* __re
   const int crow = b * d.T + c * Q;
   if (tid == 0) issue_loads(crow);
 
-  // H_{c-1} (fp32 [P][N]) -> bf16 rows n (64 p each): the MN-major B operand of C H^T
+  // H_{c-1} (fp32 [P][N]) -> bf16 rows n (64 p each): the MN-major B operand of
+  // C H^T.  Thread (wg, n) converts p in [32 wg, 32 wg + 32).
   const float* Hg = hist + (((size_t)b * d.nc + c) * d.H + h) * (size_t)(64 * 128);
-  chunk_cumsum_tc(d, dt, A, b, c, h, s_cs2, s_dt, scratch);
+  chunk_cumsum_256(d, dt, A, b, c, h, s_cs2, s_dt, scratch);
   {
-    const int n = tid;
+    const int n = row;
 #pragma unroll
-    for (int ch = 0; ch < 8; ++ch) {
+    for (int ch = 0; ch < 4; ++ch) {
       float v8[8];
 #pragma unroll
-      for (int t = 0; t < 8; ++t) v8[t] = Hg[(size_t)(ch * 8 + t) * 128 + n];
-      uint4 o;
-      o.x = pack_bf16(v8[0], v8[1]);
-      o.y = pack_bf16(v8[2], v8[3]);
-      o.z = pack_bf16(v8[4], v8[5]);
-      o.w = pack_bf16(v8[6], v8[7]);
-      *(uint4*)(sH + sw128(n, ch)) = o;
+      for (int t = 0; t < 8; ++t) v8[t] = Hg[(size_t)(wg * 32 + ch * 8 + t) * 128 + n];
+      store_row_bf16(sH, n, wg * 4 + ch, v8);
     }
   }
 
@@ -285,7 +347,7 @@ k_fwd_scan_tc(const __grid_constant__ ScanMaps maps, TcDims d, const float* __re
     const int row0 = crow + blk * 128;
     // per-warp column factors of this block: E[w][jj] = exp(cs_r - cs_J) dt_J, J < r
     const int base = blk * 128;
-    for (int e = tid; e < 4 * 128; e += kTcThreads) {
+    for (int e = tid; e < 4 * 128; e += 256) {
       const int w = e >> 7, jj = e & 127;
       const int r = base + 32 * w, J = base + jj;
       s_E[w][jj] = (J < r) ? exp2f(s_cs2[r] - s_cs2[J]) * s_dt[J] : 0.f;
@@ -319,27 +381,35 @@ k_fwd_scan_tc(const __grid_constant__ ScanMaps maps, TcDims d, const float* __re
     fence_after_sync();
     if (!ok) break;
 
-    const int il = warp * 32 + lane;  // row inside the block (TMEM lane)
-    const int I = base + il;          // row inside the chunk
-    // M = CB o L o dt (masked), bf16 K-major A operand: row il, K = j (two 64-wide tiles)
+    const int I = base + row;  // row inside the chunk
+    // M = CB o L o dt (masked), bf16 K-major A operand: row, K = j (two 64-wide tiles).
+    // Warpgroup wg writes columns [64 wg, 64 wg + 64).
     {
-      const int r = base + 32 * warp;
-      const float fi = exp2f(s_cs2[I] - s_cs2[r]);
+      const float fi = exp2f(s_cs2[I] - s_cs2[base + 32 * q]);
       const float csI = s_cs2[I];
 #pragma unroll
-      for (int jc = 0; jc < 4; ++jc) {
+      for (int u = 0; u < 2; ++u) {
+        const int jc = 2 * wg + u;
         float v[32];
-        tmem_ld32(tCB + lane_base + jc * 32, v);
-        tmem_wait_ld();
-        if (jc < warp) {
+        if (jc <= q) {  // warp-uniform
+          tmem_ld32(tCB + lane_base + jc * 32, v);
+          tmem_wait_ld();
+          if (jc < q) {
 #pragma unroll
-          for (int k = 0; k < 32; ++k) v[k] *= fi * s_E[warp][jc * 32 + k];
-        } else if (jc == warp) {
+            for (int t4 = 0; t4 < 8; ++t4) {
+              const float4 e4 = *(const float4*)&s_E[q][jc * 32 + t4 * 4];
+              v[t4 * 4 + 0] *= fi * e4.x;
+              v[t4 * 4 + 1] *= fi * e4.y;
+              v[t4 * 4 + 2] *= fi * e4.z;
+              v[t4 * 4 + 3] *= fi * e4.w;
+            }
+          } else {
 #pragma unroll
-          for (int k = 0; k < 32; ++k) {
-            const int J = base + jc * 32 + k;
-            const float ex = (J <= I) ? exp2f(csI - s_cs2[J]) : 0.f;
-            v[k] *= ex * s_dt[J];
+            for (int k = 0; k < 32; ++k) {
+              const int J = base + jc * 32 + k;
+              const float ex = (J <= I) ? exp2f(csI - s_cs2[J]) : 0.f;
+              v[k] *= ex * s_dt[J];
+            }
           }
         } else {
 #pragma unroll
@@ -347,13 +417,8 @@ k_fwd_scan_tc(const __grid_constant__ ScanMaps maps, TcDims d, const float* __re
         }
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
-          uint4 o;
-          o.x = pack_bf16(v[q4 * 8 + 0], v[q4 * 8 + 1]);
-          o.y = pack_bf16(v[q4 * 8 + 2], v[q4 * 8 + 3]);
-          o.z = pack_bf16(v[q4 * 8 + 4], v[q4 * 8 + 5]);
-          o.w = pack_bf16(v[q4 * 8 + 6], v[q4 * 8 + 7]);
           const int j = jc * 32 + q4 * 8;
-          *(uint4*)(sM + (j >> 6) * 16384 + sw128(il, (j & 63) >> 3)) = o;
+          store_row_bf16(sM + (j >> 6) * 16384, row, (j & 63) >> 3, &v[q4 * 8]);
         }
       }
     }
@@ -375,31 +440,22 @@ k_fwd_scan_tc(const __grid_constant__ ScanMaps maps, TcDims d, const float* __re
     mma_phase ^= 1;
     fence_after_sync();
     if (!ok) break;
-    // epilogue: y = Y + exp(cs_I - ref) Ys + D x  -> bf16 staging -> TMA store
+    // epilogue: y = Y + exp(cs_I - ref) Ys + D x  -> bf16 staging -> TMA store;
+    // warpgroup wg handles p in [32 wg, 32 wg + 32)
     {
       const float sc = exp2f(s_cs2[I] - ref2);
+      float yv[32], ys[32];
+      tmem_ld32(tY + lane_base + wg * 32, yv);
+      tmem_ld32(tYs + lane_base + wg * 32, ys);
+      tmem_wait_ld();
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        float yv[32], ys[32];
-        tmem_ld32(tY + lane_base + half * 32, yv);
-        tmem_ld32(tYs + lane_base + half * 32, ys);
-        tmem_wait_ld();
+      for (int k = 0; k < 4; ++k) {
+        const int ch = wg * 4 + k;
+        float xf[8], o8[8];
+        unpack8(*(const uint4*)(sX + sw128(row, ch)), xf);
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int ch = half * 4 + k;
-          const uint4 xv = *(const uint4*)(sX + sw128(il, ch));
-          const __nv_bfloat162* xp = (const __nv_bfloat162*)&xv;
-          uint4 o;
-          uint32_t* q = (uint32_t*)&o;
-#pragma unroll
-          for (int t = 0; t < 4; ++t) {
-            const float2 xf = __bfloat1622float2(xp[t]);
-            const int m = k * 8 + 2 * t;
-            q[t] = pack_bf16(fmaf(sc, ys[m], yv[m]) + Dh * xf.x,
-                             fmaf(sc, ys[m + 1], yv[m + 1]) + Dh * xf.y);
-          }
-          *(uint4*)(sY + sw128(il, ch)) = o;
-        }
+        for (int t = 0; t < 8; ++t) o8[t] = fmaf(sc, ys[k * 8 + t], yv[k * 8 + t]) + Dh * xf[t];
+        store_row_bf16(sY, row, ch, o8);
       }
     }
     fence_async_smem();
@@ -413,20 +469,7 @@ k_fwd_scan_tc(const __grid_constant__ ScanMaps maps, TcDims d, const float* __re
     if (blk + 1 < nblk) {
       // mid-chunk state: X_0 rows j scaled in place by exp(cs_127 - cs_j) dt_j,
       // S_0^T = B_0^T (w o X_0) (M = n, N = p, K = j), H_mid = exp(cs_127) H + S_0
-      for (int e = tid; e < 128 * 8; e += kTcThreads) {
-        const int r = e >> 3;
-        const float s = exp2f(s_cs2[127] - s_cs2[r]) * s_dt[r];
-        const uint4 v = *(const uint4*)(sX + e * 16);
-        const __nv_bfloat162* q2 = (const __nv_bfloat162*)&v;
-        uint4 o;
-        uint32_t* q = (uint32_t*)&o;
-#pragma unroll
-        for (int t = 0; t < 4; ++t) {
-          const float2 f = __bfloat1622float2(q2[t]);
-          q[t] = pack_bf16(f.x * s, f.y * s);
-        }
-        *(uint4*)(sX + e * 16) = o;
-      }
+      scale_tile_rows(sX, 128 * 8, [&](int r) { return exp2f(s_cs2[127] - s_cs2[r]) * s_dt[r]; });
       fence_async_smem();
       fence_before_sync();
       __syncthreads();
@@ -443,27 +486,17 @@ k_fwd_scan_tc(const __grid_constant__ ScanMaps maps, TcDims d, const float* __re
       fence_after_sync();
       if (!ok) break;
       const float e127 = exp2f(s_cs2[127]);
-      const int n = il;
+      const int n = row;
+      float v[32];
+      tmem_ld32(tS0 + lane_base + wg * 32, v);
+      tmem_wait_ld();
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        float v[32];
-        tmem_ld32(tS0 + lane_base + half * 32, v);
-        tmem_wait_ld();
+      for (int k = 0; k < 4; ++k) {
+        float v8[8];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          float v8[8];
-#pragma unroll
-          for (int t = 0; t < 8; ++t) {
-            const int p0 = half * 32 + k * 8 + t;
-            v8[t] = fmaf(e127, Hg[(size_t)p0 * 128 + n], v[k * 8 + t]);
-          }
-          uint4 o;
-          o.x = pack_bf16(v8[0], v8[1]);
-          o.y = pack_bf16(v8[2], v8[3]);
-          o.z = pack_bf16(v8[4], v8[5]);
-          o.w = pack_bf16(v8[6], v8[7]);
-          *(uint4*)(sH + sw128(n, half * 4 + k)) = o;
-        }
+        for (int t = 0; t < 8; ++t)
+          v8[t] = fmaf(e127, Hg[(size_t)(wg * 32 + k * 8 + t) * 128 + n], v[k * 8 + t]);
+        store_row_bf16(sH, n, wg * 4 + k, v8);
       }
       if (tid == 0) {
         bulk_wait_read0();  // y staging (region R1) is reloaded next
@@ -479,7 +512,7 @@ k_fwd_scan_tc(const __grid_constant__ ScanMaps maps, TcDims d, const float* __re
   if (tid == 0) bulk_wait0();
   fence_before_sync();
   __syncthreads();
-  if (warp == 0) tmem_dealloc(tm, 256);
+  if (tid < 32) tmem_dealloc(tm, 256);
 }
 
 // ---------------------------------------------------------------------------
@@ -501,8 +534,11 @@ struct BwdMaps {
   CUtensorMap dx;  // [B*T][H*P] bf16, box {64, 128} (store)
   CUtensorMap dB;  // [B*T][G*N] bf16, box {64, 128} (store)
   CUtensorMap dC;  // [B*T][G*N] bf16, box {64, 128} (store)
+  CUtensorMap ht;  // chunk-start states, bf16 rows n: [B*nc*H*N][P], box {64, 128}
+  CUtensorMap gt;  // chunk-end state gradients, same layout
 };
 
+constexpr int kBwThreads = 256;       // two warpgroups share each TMEM row
 constexpr uint32_t kBwC = 0;          // C_k: 2 K-major tiles [128][128 B]
 constexpr uint32_t kBwB = 32768;      // B_k
 constexpr uint32_t kBwO = 65536;      // B_0 (k = 1) or C_1 (k = 0) when the chunk has 2 blocks
@@ -514,38 +550,11 @@ constexpr uint32_t kBwG = 163840;     // gout bf16, row n, 64 p
 constexpr uint32_t kBwW = 180224;     // W, then L o CB, then staging (2 tiles)
 constexpr uint32_t kBwBytes = 212992;
 
-// Column sums over the 32 lanes of a warp: lane l returns sum over lanes of v[l].
-__device__ __forceinline__ float warp_column_sum(float (&v)[32]) {
-  const int lane = threadIdx.x & 31;
-#pragma unroll
-  for (int s = 16; s >= 1; s >>= 1) {
-    const bool upper = (lane & s) != 0;
-#pragma unroll
-    for (int k = 0; k < s; ++k) {
-      const float send = upper ? v[k] : v[k + s];
-      const float keep = upper ? v[k + s] : v[k];
-      v[k] = keep + __shfl_xor_sync(0xffffffffu, send, s);
-    }
-  }
-  return v[0];
-}
-
-__device__ __forceinline__ void store_row_bf16(uint8_t* tile, int row, int chunk0,
-                                               const float* v8) {
-  uint4 o;
-  o.x = pack_bf16(v8[0], v8[1]);
-  o.y = pack_bf16(v8[2], v8[3]);
-  o.z = pack_bf16(v8[4], v8[5]);
-  o.w = pack_bf16(v8[6], v8[7]);
-  *(uint4*)(tile + sw128(row, chunk0)) = o;
-}
-
-__global__ void __launch_bounds__(kTcThreads, 1)
+__global__ void __launch_bounds__(kBwThreads, 1)
 k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, int nsub, const float* __restrict__ dt,
-         const float* __restrict__ A, const float* __restrict__ D,
-         const float* __restrict__ hist, const float* __restrict__ gstate,
-         float* __restrict__ ddt, float* __restrict__ dA_part, float* __restrict__ dD_part,
-         void* __restrict__ dB_out, void* __restrict__ dC_out) {
+         const float* __restrict__ A, const float* __restrict__ D, float* __restrict__ ddt,
+         float* __restrict__ dA_part, float* __restrict__ dD_part, void* __restrict__ dB_out,
+         void* __restrict__ dC_out) {
   extern __shared__ __align__(1024) uint8_t smraw[];
   uint8_t* sm = (uint8_t*)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
   uint8_t* sC = sm + kBwC;
@@ -557,9 +566,11 @@ k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, int nsub, const float* 
   uint8_t* sH = sm + kBwH;
   uint8_t* sG = sm + kBwG;
   uint8_t* sW = sm + kBwW;
-  __shared__ float s_cs2[256], s_dt[256], scratch[4];
-  __shared__ float s_E[4][128];    // exp(cs_r - cs_J), J < r = base + 32 w
-  __shared__ float s_col[4][128];  // per-warp strict column sums of M
+  __shared__ float s_cs2[256], s_dt[256], scratch[8];
+  __shared__ __align__(16) float s_E[4][128];    // exp(cs_r - cs_J), J < r = base + 32 q
+  __shared__ __align__(16) float s_Edt[4][128];  // the same times dt_J
+  __shared__ float s_col[4][128];                // per-warp strict column sums of M
+  __shared__ float s_red[5][128];                // second warpgroup's row partials
   __shared__ float s_v[128];
   __shared__ uint64_t bar_shared, bar_head, bar_mma;
   __shared__ uint32_t tmem_base;
@@ -568,25 +579,28 @@ k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, int nsub, const float* 
   const int k = blockIdx.x % nblk, c = blockIdx.x / nblk;
   const int g = blockIdx.y / nsub, sub = blockIdx.y % nsub, b = blockIdx.z;
   const int kh = d.hpg / nsub;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int tid = threadIdx.x, wg = tid >> 7, q = (tid >> 5) & 3, lane = tid & 31;
+  const int row = tid & 127;  // TMEM lane / tile row owned (with the other warpgroup)
   const int base = 128 * k;
   const int crow = b * d.T + c * d.Q;  // first row of the chunk
   const int row0 = crow + base;
-  const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+  const uint32_t lane_base = (uint32_t)(q * 32) << 16;
   const bool two = nblk == 2;
-  const uint32_t head_bytes = two ? 48 * 1024 : 32 * 1024;
+  const uint32_t head_bytes = (two ? 48 : 32) * 1024 + 32 * 1024;
 
   if (tid == 0) {
     prefetch_tmap(&maps.x);
     prefetch_tmap(&maps.dy);
     prefetch_tmap(&maps.B);
     prefetch_tmap(&maps.C);
+    prefetch_tmap(&maps.ht);
+    prefetch_tmap(&maps.gt);
     mbar_init(&bar_shared, 1);
     mbar_init(&bar_head, 1);
     mbar_init(&bar_mma, 1);
     fence_mbar_init();
   }
-  if (warp == 0) {
+  if (tid < 32) {
     tmem_alloc(&tmem_base, 512);
     tmem_relinquish();
   }
@@ -604,6 +618,9 @@ k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, int nsub, const float* 
       if (k == 1) tma_load_2d(sXO, &maps.x, h * d.P, crow, &bar_head);
       else tma_load_2d(sXO, &maps.dy, h * d.P, crow + 128, &bar_head);
     }
+    const int srow = ((b * d.nc + c) * d.H + h) * d.N;
+    tma_load_2d(sH, &maps.ht, 0, srow, &bar_head);
+    tma_load_2d(sG, &maps.gt, 0, srow, &bar_head);
   };
   const int h_first = g * d.hpg + sub * kh;
   if (tid == 0) {
@@ -628,55 +645,25 @@ k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, int nsub, const float* 
 
   for (int hh = 0; hh < kh && ok; ++hh) {
     const int h = h_first + hh;
-    chunk_cumsum_tc(d, dt, A, b, c, h, s_cs2, s_dt, scratch);
-    for (int e = tid; e < 4 * 128; e += kTcThreads) {
+    chunk_cumsum_256(d, dt, A, b, c, h, s_cs2, s_dt, scratch);
+    for (int e = tid; e < 4 * 128; e += kBwThreads) {
       const int w = e >> 7, jj = e & 127;
       const int r = base + 32 * w, J = base + jj;
-      s_E[w][jj] = (J < r) ? exp2f(s_cs2[r] - s_cs2[J]) : 0.f;
+      const float ev = (J < r) ? exp2f(s_cs2[r] - s_cs2[J]) : 0.f;
+      s_E[w][jj] = ev;
+      s_Edt[w][jj] = ev * s_dt[J];
     }
     const float ref2 = k == 0 ? 0.f : s_cs2[base - 1];
     const float end2 = s_cs2[base + 127];
-    __syncthreads();
-    ok = wait_or_flag(&bar_head, hh & 1);
+    ok = wait_or_flag(&bar_head, hh & 1);  // also publishes the tables
     if (!ok) break;
 
-    // ---- state in (Hin) and state gradient out (gout), as bf16 rows n
-    const int n = tid;
-    const size_t soff = (((size_t)b * d.nc + c) * d.H + h) * (size_t)(64 * 128);
-    const float* Hg = hist + soff;
-    const float* Gg = gstate + soff;
+    // ---- mid-chunk state or state gradient (chunks of two blocks)
     if (two) {
-      if (k == 1) {
-        for (int e = tid; e < 128 * 8; e += kTcThreads) {  // X_0 rows j by exp(cs_127 - cs_j) dt_j
-          const int r = e >> 3;
-          const float s = exp2f(s_cs2[127] - s_cs2[r]) * s_dt[r];
-          const uint4 v = *(const uint4*)(sXO + e * 16);
-          const __nv_bfloat162* q2 = (const __nv_bfloat162*)&v;
-          uint4 o;
-          uint32_t* q = (uint32_t*)&o;
-#pragma unroll
-          for (int t = 0; t < 4; ++t) {
-            const float2 f = __bfloat1622float2(q2[t]);
-            q[t] = pack_bf16(f.x * s, f.y * s);
-          }
-          *(uint4*)(sXO + e * 16) = o;
-        }
-      } else {
-        for (int e = tid; e < 128 * 8; e += kTcThreads) {  // dY_1 rows i by exp(cs_i - cs_127)
-          const int r = e >> 3;
-          const float s = exp2f(s_cs2[128 + r] - s_cs2[127]);
-          const uint4 v = *(const uint4*)(sXO + e * 16);
-          const __nv_bfloat162* q2 = (const __nv_bfloat162*)&v;
-          uint4 o;
-          uint32_t* q = (uint32_t*)&o;
-#pragma unroll
-          for (int t = 0; t < 4; ++t) {
-            const float2 f = __bfloat1622float2(q2[t]);
-            q[t] = pack_bf16(f.x * s, f.y * s);
-          }
-          *(uint4*)(sXO + e * 16) = o;
-        }
-      }
+      if (k == 1)  // X_0 rows j by exp(cs_127 - cs_j) dt_j
+        scale_tile_rows(sXO, 128 * 8, [&](int r) { return exp2f(s_cs2[127] - s_cs2[r]) * s_dt[r]; });
+      else  // dY_1 rows i by exp(cs_i - cs_127)
+        scale_tile_rows(sXO, 128 * 8, [&](int r) { return exp2f(s_cs2[128 + r] - s_cs2[127]); });
       fence_async_smem();
       fence_before_sync();
       __syncthreads();
@@ -689,41 +676,34 @@ k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, int nsub, const float* 
                    desc_sw128(smem_u32(sXO) + kk * 2048, 16384, 1024), id, kk > 0);
         mma_commit(&bar_mma);
       }
-      __syncthreads();
       ok = wait_or_flag(&bar_mma, mma_phase);
       mma_phase ^= 1;
       fence_after_sync();
       if (!ok) break;
-    }
-    float hg = 0.f;  // <gout, Hin> partial of row n
-    {
-      const float e127 = two ? exp2f(s_cs2[127]) : 0.f;
-      const float eg = two ? exp2f(s_cs2[d.Q - 1] - s_cs2[127]) : 0.f;
+      // row n, p in [32 wg, 32 wg + 32): H_mid = e^{cs_127} H + S_0 or g_mid = e^{..} g + R_1
+      float v[32];
+      tmem_ld32(T1 + lane_base + wg * 32, v);
+      tmem_wait_ld();
+      uint8_t* tile = (k == 1) ? sH : sG;
+      const float sc = (k == 1) ? exp2f(s_cs2[127]) : exp2f(s_cs2[d.Q - 1] - s_cs2[127]);
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        float v[32];
-        if (two) {
-          tmem_ld32(T1 + lane_base + half * 32, v);
-          tmem_wait_ld();
-        }
+      for (int q4 = 0; q4 < 4; ++q4) {
+        float f[8];
+        unpack8(*(const uint4*)(tile + sw128(row, wg * 4 + q4)), f);
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          float hv[8], gv[8];
-#pragma unroll
-          for (int t = 0; t < 8; ++t) {
-            const int p = half * 32 + q4 * 8 + t;
-            float hval = Hg[(size_t)p * 128 + n];
-            float gval = Gg[(size_t)p * 128 + n];
-            if (two && k == 1) hval = fmaf(e127, hval, v[q4 * 8 + t]);
-            if (two && k == 0) gval = fmaf(eg, gval, v[q4 * 8 + t]);
-            hv[t] = hval;
-            gv[t] = gval;
-            hg = fmaf(hval, gval, hg);
-          }
-          store_row_bf16(sH, n, half * 4 + q4, hv);
-          store_row_bf16(sG, n, half * 4 + q4, gv);
-        }
+        for (int t = 0; t < 8; ++t) f[t] = fmaf(sc, f[t], v[q4 * 8 + t]);
+        store_row_bf16(tile, row, wg * 4 + q4, f);
       }
+    }
+    // <gout, Hin> over this thread's half row (bf16 operands, fp32 sum)
+    float hg = 0.f;
+#pragma unroll
+    for (int q4 = 0; q4 < 4; ++q4) {
+      float fh[8], fg[8];
+      unpack8(*(const uint4*)(sH + sw128(row, wg * 4 + q4)), fh);
+      unpack8(*(const uint4*)(sG + sw128(row, wg * 4 + q4)), fg);
+#pragma unroll
+      for (int t = 0; t < 8; ++t) hg = fmaf(fh[t], fg[t], hg);
     }
     hg = block_sum(hg, scratch);
     fence_async_smem();
@@ -744,51 +724,73 @@ k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, int nsub, const float* 
                  desc_sw128(smem_u32(sX) + kk * 32, 16, 1024), id, kk > 0);
       mma_commit(&bar_mma);
     }
-    __syncthreads();
     ok = wait_or_flag(&bar_mma, mma_phase);
     mma_phase ^= 1;
     fence_after_sync();
     if (!ok) break;
 
-    // ---- W = L o dt_j o dYX -> sW (bf16), L o CB -> registers, row / column sums of M
-    const int il = tid, I = base + il;
-    const int r0 = base + 32 * warp;
-    const float fi = exp2f(s_cs2[I] - s_cs2[r0]);
+    // ---- W = L o dt_j o dYX -> sW, L o CB -> registers, row / column sums of M.
+    // Warpgroup wg covers columns [64 wg, 64 wg + 64) of row `row` (chunks 2wg, 2wg+1).
+    const int I = base + row;
+    const float fi = exp2f(s_cs2[I] - s_cs2[base + 32 * q]);
     const float csI = s_cs2[I];
     float rowsum = 0.f;
-    uint32_t lcb[64];
+    uint32_t lcb[32];
 #pragma unroll
-    for (int jc = 0; jc < 4; ++jc) {
-      float cb[32], xy[32];
-      tmem_ld32(T0 + lane_base + jc * 32, cb);
-      tmem_ld32(T1 + lane_base + jc * 32, xy);
-      tmem_wait_ld();
-      float wv[32];
+    for (int u = 0; u < 2; ++u) {
+      const int jc = 2 * wg + u;
+      float cb[32], xy[32], wv[32];
+      if (jc <= q) {  // warp-uniform
+        tmem_ld32(T0 + lane_base + jc * 32, cb);
+        tmem_ld32(T1 + lane_base + jc * 32, xy);
+        tmem_wait_ld();
+        if (jc < q) {
 #pragma unroll
-      for (int t = 0; t < 32; ++t) {
-        const int J = base + jc * 32 + t;
-        float L;
-        if (jc < warp) L = fi * s_E[warp][jc * 32 + t];
-        else if (jc == warp) L = (J <= I) ? exp2f(csI - s_cs2[J]) : 0.f;
-        else L = 0.f;
-        wv[t] = L * s_dt[J] * xy[t];
-        const float mm = (J < I) ? wv[t] * cb[t] : 0.f;
-        rowsum += mm;
-        xy[t] = mm;  // column-sum input
-        cb[t] *= L;  // L o CB
+          for (int t4 = 0; t4 < 8; ++t4) {
+            const float4 e4 = *(const float4*)&s_E[q][jc * 32 + t4 * 4];
+            const float4 d4 = *(const float4*)&s_Edt[q][jc * 32 + t4 * 4];
+            const float ee[4] = {e4.x, e4.y, e4.z, e4.w};
+            const float dd4[4] = {d4.x, d4.y, d4.z, d4.w};
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+              const int m = t4 * 4 + t;
+              wv[m] = fi * dd4[t] * xy[m];
+              const float mm = wv[m] * cb[m];
+              rowsum += mm;
+              xy[m] = mm;
+              cb[m] *= fi * ee[t];
+            }
+          }
+        } else {
+#pragma unroll
+          for (int m = 0; m < 32; ++m) {
+            const int J = base + jc * 32 + m;
+            const float L = (J <= I) ? exp2f(csI - s_cs2[J]) : 0.f;
+            wv[m] = L * s_dt[J] * xy[m];
+            const float mm = (J < I) ? wv[m] * cb[m] : 0.f;
+            rowsum += mm;
+            xy[m] = mm;
+            cb[m] *= L;
+          }
+        }
+        const float cs = warp_column_sum(xy);
+        s_col[q][jc * 32 + lane] = cs;
+      } else {
+#pragma unroll
+        for (int m = 0; m < 32; ++m) {
+          wv[m] = 0.f;
+          cb[m] = 0.f;
+        }
       }
 #pragma unroll
       for (int q4 = 0; q4 < 4; ++q4) {
         const int j = jc * 32 + q4 * 8;
-        store_row_bf16(sW + (j >> 6) * 16384, il, (j & 63) >> 3, &wv[q4 * 8]);
+        store_row_bf16(sW + (j >> 6) * 16384, row, (j & 63) >> 3, &wv[q4 * 8]);
       }
 #pragma unroll
-      for (int t = 0; t < 16; ++t) lcb[jc * 16 + t] = pack_bf16(cb[2 * t], cb[2 * t + 1]);
-      if (jc <= warp) {
-        const float cs = warp_column_sum(xy);
-        s_col[warp][jc * 32 + lane] = cs;
-      }
+      for (int t = 0; t < 16; ++t) lcb[u * 16 + t] = pack_bf16(cb[2 * t], cb[2 * t + 1]);
     }
+    if (wg == 1) s_red[0][row] = rowsum;
     fence_async_smem();
     fence_before_sync();
     __syncthreads();
@@ -808,23 +810,22 @@ k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, int nsub, const float* 
                  desc_sw128(smem_u32(sC) + kk * 2048, 16384, 1024), id_db, (hh > 0) || (kk > 0));
       mma_commit(&bar_mma);
     }
-    __syncthreads();
     ok = wait_or_flag(&bar_mma, mma_phase);
     mma_phase ^= 1;
     fence_after_sync();
     if (!ok) break;
     // L o CB into sW (same physical layout: row i, j contiguous)
 #pragma unroll
-    for (int jc = 0; jc < 4; ++jc)
+    for (int u = 0; u < 2; ++u)
 #pragma unroll
       for (int q4 = 0; q4 < 4; ++q4) {
-        const int j = jc * 32 + q4 * 8;
+        const int j = (2 * wg + u) * 32 + q4 * 8;
         uint4 o;
-        o.x = lcb[jc * 16 + q4 * 4 + 0];
-        o.y = lcb[jc * 16 + q4 * 4 + 1];
-        o.z = lcb[jc * 16 + q4 * 4 + 2];
-        o.w = lcb[jc * 16 + q4 * 4 + 3];
-        *(uint4*)(sW + (j >> 6) * 16384 + sw128(il, (j & 63) >> 3)) = o;
+        o.x = lcb[u * 16 + q4 * 4 + 0];
+        o.y = lcb[u * 16 + q4 * 4 + 1];
+        o.z = lcb[u * 16 + q4 * 4 + 2];
+        o.w = lcb[u * 16 + q4 * 4 + 3];
+        *(uint4*)(sW + (j >> 6) * 16384 + sw128(row, (j & 63) >> 3)) = o;
       }
     fence_async_smem();
     fence_before_sync();
@@ -848,43 +849,22 @@ k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, int nsub, const float* 
       }
       mma_commit(&bar_mma);
     }
-    __syncthreads();
     ok = wait_or_flag(&bar_mma, mma_phase);
     mma_phase ^= 1;
     fence_after_sync();
     if (!ok) break;
 
-    // rows x_j and dy_i (unscaled) into registers, then scale the tiles in place:
-    // X rows j by exp(cs_end - cs_j) dt_j, dY rows i by exp(cs_i - ref)
-    uint4 xr[8], dyr[8];
+    // this thread's half rows of x_j and dy_i (unscaled) into registers, then
+    // scale the tiles in place: X rows j by exp(cs_end - cs_j) dt_j, dY rows i by exp(cs_i - ref)
+    uint4 xr[4], dyr[4];
 #pragma unroll
-    for (int ch = 0; ch < 8; ++ch) {
-      xr[ch] = *(const uint4*)(sX + sw128(il, ch));
-      dyr[ch] = *(const uint4*)(sDY + sw128(il, ch));
+    for (int q4 = 0; q4 < 4; ++q4) {
+      xr[q4] = *(const uint4*)(sX + sw128(row, wg * 4 + q4));
+      dyr[q4] = *(const uint4*)(sDY + sw128(row, wg * 4 + q4));
     }
     __syncthreads();
-    for (int e = tid; e < 128 * 8; e += kTcThreads) {
-      const int r = e >> 3;
-      const int R = base + r;
-      const float sx = exp2f(end2 - s_cs2[R]) * s_dt[R];
-      const float sy = exp2f(s_cs2[R] - ref2);
-      const uint4 vx = *(const uint4*)(sX + e * 16);
-      const uint4 vy = *(const uint4*)(sDY + e * 16);
-      const __nv_bfloat162* px = (const __nv_bfloat162*)&vx;
-      const __nv_bfloat162* py = (const __nv_bfloat162*)&vy;
-      uint4 ox, oy;
-      uint32_t* qx = (uint32_t*)&ox;
-      uint32_t* qy = (uint32_t*)&oy;
-#pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        const float2 fx = __bfloat1622float2(px[t]);
-        const float2 fy = __bfloat1622float2(py[t]);
-        qx[t] = pack_bf16(fx.x * sx, fx.y * sx);
-        qy[t] = pack_bf16(fy.x * sy, fy.y * sy);
-      }
-      *(uint4*)(sX + e * 16) = ox;
-      *(uint4*)(sDY + e * 16) = oy;
-    }
+    scale_tile_rows(sX, 128 * 8, [&](int r) { return exp2f(end2 - s_cs2[base + r]) * s_dt[base + r]; });
+    scale_tile_rows(sDY, 128 * 8, [&](int r) { return exp2f(s_cs2[base + r] - ref2); });
     fence_async_smem();
     fence_before_sync();
     __syncthreads();
@@ -903,43 +883,39 @@ k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, int nsub, const float* 
     }
 
     // ---- epilogue of the head (overlaps phase D): dx, drive, e, statein, dD
+    const float sgs = exp2f(end2 - s_cs2[I]);
+    const float dtI = s_dt[I];
     float drive = 0.f, ej = 0.f, stin = 0.f, dd = 0.f;
     {
-      const float sgs = exp2f(end2 - s_cs2[I]);
-      const float dtI = s_dt[I];
       const float Dh = D[h];
+      float gx[32], gs[32], ch[32];
+      tmem_ld32(T0 + lane_base + wg * 32, gx);
+      tmem_ld32(T0 + lane_base + 64 + wg * 32, gs);
+      tmem_ld32(T1 + lane_base + wg * 32, ch);
+      tmem_wait_ld();
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        float gx[32], gs[32], ch[32];
-        tmem_ld32(T0 + lane_base + half * 32, gx);
-        tmem_ld32(T0 + lane_base + 64 + half * 32, gs);
-        tmem_ld32(T1 + lane_base + half * 32, ch);
-        tmem_wait_ld();
+      for (int q4 = 0; q4 < 4; ++q4) {
+        float xf[8], yf[8], o8[8];
+        unpack8(xr[q4], xf);
+        unpack8(dyr[q4], yf);
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          const int cidx = half * 4 + q4;
-          const __nv_bfloat162* px = (const __nv_bfloat162*)&xr[cidx];
-          const __nv_bfloat162* py = (const __nv_bfloat162*)&dyr[cidx];
-          float o8[8];
-#pragma unroll
-          for (int t = 0; t < 4; ++t) {
-            const float2 xf = __bfloat1622float2(px[t]);
-            const float2 yf = __bfloat1622float2(py[t]);
-            const int m = q4 * 8 + 2 * t;
-            const float g0 = fmaf(sgs, gs[m], gx[m]);
-            const float g1 = fmaf(sgs, gs[m + 1], gx[m + 1]);
-            o8[2 * t] = fmaf(dtI, g0, Dh * yf.x);
-            o8[2 * t + 1] = fmaf(dtI, g1, Dh * yf.y);
-            drive = fmaf(xf.x, g0, fmaf(xf.y, g1, drive));
-            ej = fmaf(xf.x, gs[m], fmaf(xf.y, gs[m + 1], ej));
-            stin = fmaf(yf.x, ch[m], fmaf(yf.y, ch[m + 1], stin));
-            dd = fmaf(yf.x, xf.x, fmaf(yf.y, xf.y, dd));
-          }
-          store_row_bf16(sW, il, cidx, o8);  // dx staging: tile [128 rows][64 p]
+        for (int t = 0; t < 8; ++t) {
+          const int m = q4 * 8 + t;
+          const float gg = fmaf(sgs, gs[m], gx[m]);
+          o8[t] = fmaf(dtI, gg, Dh * yf[t]);
+          drive = fmaf(xf[t], gg, drive);
+          ej = fmaf(xf[t], gs[m], ej);
+          stin = fmaf(yf[t], ch[m], stin);
+          dd = fmaf(yf[t], xf[t], dd);
         }
+        store_row_bf16(sW, row, wg * 4 + q4, o8);  // dx staging: tile [128 rows][64 p]
       }
-      ej *= sgs * dtI;
-      stin *= exp2f(s_cs2[I] - ref2);
+    }
+    if (wg == 1) {
+      s_red[1][row] = drive;
+      s_red[2][row] = ej;
+      s_red[3][row] = stin;
+      s_red[4][row] = dd;
     }
     fence_async_smem();
     __syncthreads();
@@ -947,31 +923,40 @@ k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, int nsub, const float* 
       tma_store_2d(&maps.dx, sW, h * d.P, row0);
       bulk_commit();
     }
-    // ---- dcs, reverse cumsum, ddt, dA and dD partials
+    if (wg == 0) {
+      rowsum += s_red[0][row];
+      drive += s_red[1][row];
+      ej = (ej + s_red[2][row]) * sgs * dtI;
+      stin = (stin + s_red[3][row]) * exp2f(s_cs2[I] - ref2);
+      dd += s_red[4][row];
+    } else {
+      ej = 0.f;
+      dd = 0.f;
+    }
+    // ---- dcs, reverse cumsum, ddt, dA and dD partials (rows held by warpgroup 0)
     const float esum = block_sum(ej, scratch);
-    {
+    if (wg == 0) {
       float colsum = 0.f;
-      for (int w = il >> 5; w < 4; ++w) colsum += s_col[w][il];
+      for (int w = row >> 5; w < 4; ++w) colsum += s_col[w][row];
       float dcs = rowsum - colsum + stin - ej;
-      if (il == 127) dcs += esum + exp2f(end2 - ref2) * hg;
-      s_v[il] = dcs;
+      if (row == 127) dcs += esum + exp2f(end2 - ref2) * hg;
+      s_v[row] = dcs;
     }
     __syncthreads();
-    const float rv = s_v[127 - il];
+    const float rv = (wg == 0) ? s_v[127 - row] : 0.f;
     const float da = block_inclusive_scan(rv, scratch);  // syncs: every rv read before reuse
-    const int Jr = base + 127 - il;                        // row whose da this thread holds
-    s_v[il] = drive;
+    const int Jr = base + 127 - row;                       // row whose da this thread holds
+    if (wg == 0) s_v[row] = drive;
     __syncthreads();
-    ddt[((size_t)crow + Jr) * d.H + h] = s_v[127 - il] + A[h] * da;
-    const float a_sum = block_sum(s_dt[Jr] * da, scratch);
+    if (wg == 0) ddt[((size_t)crow + Jr) * d.H + h] = s_v[127 - row] + A[h] * da;
+    const float a_sum = block_sum(wg == 0 ? s_dt[Jr] * da : 0.f, scratch);
     const float d_sum = block_sum(dd, scratch);
     if (tid == 0) {
       const size_t slot = (((size_t)b * d.nc + c) * nblk + k) * d.H + h;
       dA_part[slot] = a_sum;
       dD_part[slot] = d_sum;
     }
-    // ---- end of head: phase D done, dx staging read, before sW / sX / sDY / sH / sG reuse
-    __syncthreads();
+    // ---- end of head: phase D done, dx staging read, before the tiles are reloaded
     ok = wait_or_flag(&bar_mma, mma_phase);
     mma_phase ^= 1;
     fence_after_sync();
@@ -982,14 +967,15 @@ k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, int nsub, const float* 
     __syncthreads();
   }
 
-  // ---- dC and dB of the block, summed over the CTA's heads in TMEM
+  // ---- dC and dB of the block, summed over the CTA's heads in TMEM.
+  // Warpgroup wg handles columns [64 wg, 64 wg + 64).
   if (nsub == 1) {
     if (ok) {  // -> bf16 -> TMA store
-      const int il = tid;
       uint8_t* stC = sW;         // 2 tiles [128][128 B]
       uint8_t* stB = sm + kBwX;  // sX + sDY: 2 tiles
 #pragma unroll
-      for (int jc = 0; jc < 4; ++jc) {
+      for (int u = 0; u < 2; ++u) {
+        const int jc = 2 * wg + u;
         float vc[32], vb[32];
         tmem_ld32(TdC + lane_base + jc * 32, vc);
         tmem_ld32(TdB + lane_base + jc * 32, vb);
@@ -997,8 +983,8 @@ k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, int nsub, const float* 
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
           const int nn = jc * 32 + q4 * 8;
-          store_row_bf16(stC + (nn >> 6) * 16384, il, (nn & 63) >> 3, &vc[q4 * 8]);
-          store_row_bf16(stB + (nn >> 6) * 16384, il, (nn & 63) >> 3, &vb[q4 * 8]);
+          store_row_bf16(stC + (nn >> 6) * 16384, row, (nn & 63) >> 3, &vc[q4 * 8]);
+          store_row_bf16(stB + (nn >> 6) * 16384, row, (nn & 63) >> 3, &vb[q4 * 8]);
         }
       }
       fence_async_smem();
@@ -1020,19 +1006,19 @@ k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, int nsub, const float* 
     float* dumpC = (float*)(sm + kBwC);  // 64 KB: C_k, B_k tiles are dead
     float* dumpB = (float*)(sm + kBwO);  // 64 KB: sO, sX, sDY are dead
     if (ok) {
-      const int il = tid;
 #pragma unroll
-      for (int jc = 0; jc < 4; ++jc) {
+      for (int u = 0; u < 2; ++u) {
+        const int jc = 2 * wg + u;
         float vc[32], vb[32];
         tmem_ld32(TdC + lane_base + jc * 32, vc);
         tmem_ld32(TdB + lane_base + jc * 32, vb);
         tmem_wait_ld();
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const int cc = jc * 8 + q;
-          const int off = il * 128 + ((cc ^ (il & 31)) << 2);
-          *(float4*)(dumpC + off) = make_float4(vc[4 * q], vc[4 * q + 1], vc[4 * q + 2], vc[4 * q + 3]);
-          *(float4*)(dumpB + off) = make_float4(vb[4 * q], vb[4 * q + 1], vb[4 * q + 2], vb[4 * q + 3]);
+        for (int q8 = 0; q8 < 8; ++q8) {
+          const int cc = jc * 8 + q8;
+          const int off = row * 128 + ((cc ^ (row & 31)) << 2);
+          *(float4*)(dumpC + off) = make_float4(vc[4 * q8], vc[4 * q8 + 1], vc[4 * q8 + 2], vc[4 * q8 + 3]);
+          *(float4*)(dumpB + off) = make_float4(vb[4 * q8], vb[4 * q8 + 1], vb[4 * q8 + 2], vb[4 * q8 + 3]);
         }
       }
     }
@@ -1043,9 +1029,9 @@ k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, int nsub, const float* 
       const uint32_t baseC = smem_u32(dumpC), baseB = smem_u32(dumpB);
       __nv_bfloat16* gC = (__nv_bfloat16*)dC_out;
       __nv_bfloat16* gB = (__nv_bfloat16*)dB_out;
-      for (int e = tid; e < rows_per * 32; e += kTcThreads) {
-        const int row = (int)rank * rows_per + (e >> 5), cc = e & 31;
-        const uint32_t off = (uint32_t)(row * 128 + ((cc ^ (row & 31)) << 2)) * 4u;
+      for (int e = tid; e < rows_per * 32; e += kBwThreads) {
+        const int rr = (int)rank * rows_per + (e >> 5), cc = e & 31;
+        const uint32_t off = (uint32_t)(rr * 128 + ((cc ^ (rr & 31)) << 2)) * 4u;
         float4 sc = make_float4(0.f, 0.f, 0.f, 0.f), sb = sc;
         for (int r = 0; r < nsub; ++r) {
           const float4 a = ld_cluster_f4(map_cluster(baseC + off, (uint32_t)r));
@@ -1053,7 +1039,7 @@ k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, int nsub, const float* 
           sc.x += a.x; sc.y += a.y; sc.z += a.z; sc.w += a.w;
           sb.x += bq.x; sb.y += bq.y; sb.z += bq.z; sb.w += bq.w;
         }
-        const size_t gi = ((size_t)(row0 + row) * d.G + g) * d.N + cc * 4;
+        const size_t gi = ((size_t)(row0 + rr) * d.G + g) * d.N + cc * 4;
         uint2 pc, pb;
         pc.x = pack_bf16(sc.x, sc.y);
         pc.y = pack_bf16(sc.z, sc.w);
@@ -1068,7 +1054,62 @@ k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, int nsub, const float* 
   if (tid == 0) bulk_wait0();
   fence_before_sync();
   __syncthreads();
-  if (warp == 0) tmem_dealloc(tm, 512);
+  if (tid < 32) tmem_dealloc(tm, 512);
+}
+
+// Reverse state pass of the tensor-core backward.  Per (b, h) and a tile of
+// 16 columns n, walks the chunks from last to first: g_c (gradient of the
+// state at the end of chunk c) = exp(cs_last[c+1]) g_{c+1} + R_{c+1}, g_{nc-1}
+// = 0, dh0 = exp(cs_last[0]) g_0 + R_0.  Writes g_c and the chunk-start state
+// H_{c-1} (read from the history) as bf16 rows n x 64 p ([b][c][h][n][p]),
+// the operand layout of k_bwd_tc, through a shared-memory transpose.
+__global__ void __launch_bounds__(256)
+k_state_pass_bwd_t(TcDims d, const float* __restrict__ R, const float* __restrict__ hist,
+                   const float* __restrict__ cs_last, __nv_bfloat16* __restrict__ gT,
+                   __nv_bfloat16* __restrict__ hT, float* __restrict__ dh0) {
+  __shared__ __align__(16) __nv_bfloat16 s_g[16][72];  // [n][p], padded rows
+  __shared__ __align__(16) __nv_bfloat16 s_h[16][72];
+  const int nt = blockIdx.x, h = blockIdx.y, b = blockIdx.z, tid = threadIdx.x;
+  const int p = tid >> 2, n4 = (tid & 3) * 4;  // this thread: row p, columns n0 + n4 .. + 3
+  const int n0 = nt * 16;
+  const int PN = d.P * d.N;
+  const size_t bh = (size_t)b * d.H + h;
+  const float* cl = cs_last + bh * d.nc;
+  auto at = [&](int c) { return (((size_t)b * d.nc + c) * d.H + h) * (size_t)PN + (size_t)p * d.N + n0 + n4; };
+  float4 gc = make_float4(0.f, 0.f, 0.f, 0.f);
+  const int last = d.nc - 1;
+  float4 r_next = *(const float4*)(R + at(last));
+  float4 h_next = *(const float4*)(hist + at(last));
+  for (int c = last; c >= 0; --c) {
+    const float4 r = r_next, hv = h_next;
+    if (c > 0) {
+      r_next = *(const float4*)(R + at(c - 1));
+      h_next = *(const float4*)(hist + at(c - 1));
+    }
+    __syncthreads();  // previous chunk's rows are written out
+    s_g[n4 + 0][p] = __float2bfloat16_rn(gc.x);
+    s_g[n4 + 1][p] = __float2bfloat16_rn(gc.y);
+    s_g[n4 + 2][p] = __float2bfloat16_rn(gc.z);
+    s_g[n4 + 3][p] = __float2bfloat16_rn(gc.w);
+    s_h[n4 + 0][p] = __float2bfloat16_rn(hv.x);
+    s_h[n4 + 1][p] = __float2bfloat16_rn(hv.y);
+    s_h[n4 + 2][p] = __float2bfloat16_rn(hv.z);
+    s_h[n4 + 3][p] = __float2bfloat16_rn(hv.w);
+    __syncthreads();
+    {
+      // 16 rows x 64 p bf16 = 16 x 8 chunks of 16 bytes per tile
+      const int t = tid & 127, rr = t >> 3, ch = t & 7;
+      const size_t orow = ((((size_t)b * d.nc + c) * d.H + h) * d.N + n0 + rr) * d.P + ch * 8;
+      if (tid < 128) *(uint4*)(gT + orow) = *(const uint4*)&s_g[rr][ch * 8];
+      else *(uint4*)(hT + orow) = *(const uint4*)&s_h[rr][ch * 8];
+    }
+    const float e = expf(cl[c]);
+    gc.x = fmaf(e, gc.x, r.x);
+    gc.y = fmaf(e, gc.y, r.y);
+    gc.z = fmaf(e, gc.z, r.z);
+    gc.w = fmaf(e, gc.w, r.w);
+  }
+  if (dh0) *(float4*)(dh0 + bh * PN + (size_t)p * d.N + n0 + n4) = gc;
 }
 
 // ---------------------------------------------------------------------------
@@ -1139,12 +1180,12 @@ cudaError_t tc_chunk_outer(const Problem& p, int mode, float* out) {
   if (mode == 0) {
     if ((e = set_smem_tc(k_chunk_outer_tc<0>, smem)) != cudaSuccess) return e;
     LaunchScope ls("chunk_state_tc", p.stream);
-    k_chunk_outer_tc<0><<<dim3(p.nc, p.H, p.B), kTcThreads, smem, p.stream>>>(maps, d, p.dt, p.A,
+    k_chunk_outer_tc<0><<<dim3(p.nc, p.H, p.B), 256, smem, p.stream>>>(maps, d, p.dt, p.A,
                                                                               out, p.cs_last);
   } else {
     if ((e = set_smem_tc(k_chunk_outer_tc<1>, smem)) != cudaSuccess) return e;
     LaunchScope ls("chunk_dstate_tc", p.stream);
-    k_chunk_outer_tc<1><<<dim3(p.nc, p.H, p.B), kTcThreads, smem, p.stream>>>(maps, d, p.dt, p.A,
+    k_chunk_outer_tc<1><<<dim3(p.nc, p.H, p.B), 256, smem, p.stream>>>(maps, d, p.dt, p.A,
                                                                               out, p.cs_last);
   }
   return cudaGetLastError();
@@ -1163,7 +1204,7 @@ cudaError_t tc_forward_scan(const Problem& p) {
   if (e != cudaSuccess) return e;
   {
     LaunchScope ls("chunk_scan_tc", p.stream);
-    k_fwd_scan_tc<<<dim3(p.nc, p.H, p.B), kTcThreads, smem, p.stream>>>(maps, tc_dims(p), p.dt,
+    k_fwd_scan_tc<<<dim3(p.nc, p.H, p.B), 256, smem, p.stream>>>(maps, tc_dims(p), p.dt,
                                                                        p.A, p.D, p.hist);
   }
   return cudaGetLastError();
@@ -1172,16 +1213,25 @@ cudaError_t tc_forward_scan(const Problem& p) {
 cudaError_t tc_backward(const Problem& p) {
   cudaError_t e = tc_chunk_outer(p, 1, p.dstate);
   if (e != cudaSuccess) return e;
-  if ((e = simt_state_pass_bwd(p)) != cudaSuccess) return e;
+  {
+    LaunchScope ls("state_pass_bwd_tc", p.stream);
+    k_state_pass_bwd_t<<<dim3(p.N / 16, p.H, p.B), 256, 0, p.stream>>>(
+        tc_dims(p), p.dstate, p.hist, p.cs_last, (__nv_bfloat16*)p.gT, (__nv_bfloat16*)p.hT,
+        p.dh0);
+  }
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
   BwdMaps maps;
   const uint64_t rows = (uint64_t)p.B * p.T;
+  const uint64_t srows = (uint64_t)p.B * p.nc * p.H * p.N;
   if (!map_bf16(&maps.x, p.x, rows, (uint64_t)p.H * p.P, 128) ||
       !map_bf16(&maps.dy, p.dy, rows, (uint64_t)p.H * p.P, 128) ||
       !map_bf16(&maps.B, p.Bm, rows, (uint64_t)p.G * p.N, 128) ||
       !map_bf16(&maps.C, p.Cm, rows, (uint64_t)p.G * p.N, 128) ||
       !map_bf16(&maps.dx, p.dx, rows, (uint64_t)p.H * p.P, 128) ||
       !map_bf16(&maps.dB, p.dB, rows, (uint64_t)p.G * p.N, 128) ||
-      !map_bf16(&maps.dC, p.dC, rows, (uint64_t)p.G * p.N, 128))
+      !map_bf16(&maps.dC, p.dC, rows, (uint64_t)p.G * p.N, 128) ||
+      !map_bf16(&maps.ht, p.hT, srows, (uint64_t)p.P, 128) ||
+      !map_bf16(&maps.gt, p.gT, srows, (uint64_t)p.P, 128))
     return cudaErrorInvalidValue;
   const size_t smem = kBwBytes + 1024;
   if ((e = set_smem_tc(k_bwd_tc, smem)) != cudaSuccess) return e;
@@ -1196,7 +1246,7 @@ cudaError_t tc_backward(const Problem& p) {
   while (nsub < 8 && units * nsub < 2L * nsm && p.hpg % (2 * nsub) == 0) nsub *= 2;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(nblk * p.nc, p.G * nsub, p.B);
-  cfg.blockDim = dim3(kTcThreads, 1, 1);
+  cfg.blockDim = dim3(kBwThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = p.stream;
   cudaLaunchAttribute attr[1];
@@ -1208,9 +1258,8 @@ cudaError_t tc_backward(const Problem& p) {
   cfg.numAttrs = 1;
   {
     LaunchScope ls("bwd_tc", p.stream);
-    e = cudaLaunchKernelEx(&cfg, k_bwd_tc, maps, tc_dims(p), nsub, p.dt, p.A, p.D,
-                           (const float*)p.hist, (const float*)p.dstate, p.ddt, p.dA_part,
-                           p.dD_part, p.dB, p.dC);
+    e = cudaLaunchKernelEx(&cfg, k_bwd_tc, maps, tc_dims(p), nsub, p.dt, p.A, p.D, p.ddt,
+                           p.dA_part, p.dD_part, p.dB, p.dC);
   }
   if (e != cudaSuccess) return e;
   if ((e = cudaGetLastError()) != cudaSuccess) return e;

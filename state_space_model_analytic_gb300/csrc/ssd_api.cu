@@ -64,6 +64,8 @@ bool tc_backward_supported(const Problem& p);
 void tc_force_path(int path);
 cudaError_t tc_chunk_outer(const Problem& p, int mode, float* out);
 cudaError_t tc_forward_scan(const Problem& p);
+bool tc_fused_states(const Problem& p);
+cudaError_t tc_forward_states(const Problem& p);
 cudaError_t tc_backward(const Problem& p);
 cudaError_t tc_read_and_clear_error(unsigned int* out);
 cudaError_t tc_selftest_timeout(cudaStream_t s);
@@ -317,10 +319,16 @@ int ssd_forward(const ssd_dims* dims, const void* x, const float* dt, const floa
   p.stream = (cudaStream_t)cuda_stream;
 
   const bool tc = tc_supported(p);
-  cudaError_t e = tc ? tc_chunk_outer(p, 0, p.hist) : simt_forward_states(p, p.hist, p.cs_last);
-  if (e != cudaSuccess) return cuda_fail(e, "forward chunk-state kernel");
-  e = simt_state_pass_fwd(p, p.hist, p.cs_last);
-  if (e != cudaSuccess) return cuda_fail(e, "forward state-pass kernel");
+  cudaError_t e;
+  if (tc && tc_fused_states(p)) {
+    e = tc_forward_states(p);
+    if (e != cudaSuccess) return cuda_fail(e, "forward state-scan kernel");
+  } else {
+    e = tc ? tc_chunk_outer(p, 0, p.hist) : simt_forward_states(p, p.hist, p.cs_last);
+    if (e != cudaSuccess) return cuda_fail(e, "forward chunk-state kernel");
+    e = simt_state_pass_fwd(p, p.hist, p.cs_last);
+    if (e != cudaSuccess) return cuda_fail(e, "forward state-pass kernel");
+  }
   e = tc ? tc_forward_scan(p) : simt_forward_scan(p);
   if (e != cudaSuccess) return cuda_fail(e, "forward chunk-scan kernel");
   return SSD_OK;
@@ -361,10 +369,15 @@ int ssd_backward(const ssd_dims* dims, const void* x, const float* dt, const flo
     // recompute the chunk-start states into the workspace (final state not needed)
     Problem f = p;
     f.final_state = nullptr;
-    e = tc_supported(f) ? tc_chunk_outer(f, 0, f.hist) : simt_forward_states(f, f.hist, f.cs_last);
-    if (e != cudaSuccess) return cuda_fail(e, "backward recompute chunk-state kernel");
-    e = simt_state_pass_fwd(f, f.hist, f.cs_last);
-    if (e != cudaSuccess) return cuda_fail(e, "backward recompute state-pass kernel");
+    if (tc_supported(f) && tc_fused_states(f)) {
+      e = tc_forward_states(f);
+      if (e != cudaSuccess) return cuda_fail(e, "backward recompute state-scan kernel");
+    } else {
+      e = tc_supported(f) ? tc_chunk_outer(f, 0, f.hist) : simt_forward_states(f, f.hist, f.cs_last);
+      if (e != cudaSuccess) return cuda_fail(e, "backward recompute chunk-state kernel");
+      e = simt_state_pass_fwd(f, f.hist, f.cs_last);
+      if (e != cudaSuccess) return cuda_fail(e, "backward recompute state-pass kernel");
+    }
   }
   e = tc_backward_supported(p) ? tc_backward(p) : simt_backward(p);
   if (e != cudaSuccess) return cuda_fail(e, "backward kernels");

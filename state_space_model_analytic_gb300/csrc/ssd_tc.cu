@@ -158,13 +158,31 @@ __device__ __forceinline__ void scale_tile_rows(uint8_t* tile, int nchunks, F&& 
   }
 }
 
+// dt of step `tid` of chunk c, head h (0 past the chunk), for 256 threads.
+__device__ __forceinline__ float load_dt_256(const TcDims& d, const float* __restrict__ dt, int b,
+                                             int c, int h) {
+  const int tid = threadIdx.x;
+  return tid < d.Q ? dt[((size_t)b * d.T + (size_t)c * d.Q + tid) * d.H + h] : 0.f;
+}
+
+// Chunk-local inclusive cumsum (log2 units) of the dt values the 256 threads hold.
+__device__ __forceinline__ void chunk_cumsum_256v(const TcDims& d, float dv, float a2,
+                                                  float* s_cs2, float* s_dt, float* scratch) {
+  const int tid = threadIdx.x;
+  const float cs = block_inclusive_scan(dv * a2, scratch);
+  if (tid < d.Q) {
+    s_cs2[tid] = cs;
+    s_dt[tid] = dv;
+  }
+  __syncthreads();
+}
+
 // Chunk-local inclusive cumsum (log2 units) with 256 threads, one value each.
 __device__ __forceinline__ void chunk_cumsum_256(const TcDims& d, const float* __restrict__ dt,
                                                  const float* __restrict__ A, int b, int c, int h,
                                                  float* s_cs2, float* s_dt, float* scratch) {
   const int tid = threadIdx.x;
-  float dv = 0.f;
-  if (tid < d.Q) dv = dt[((size_t)b * d.T + (size_t)c * d.Q + tid) * d.H + h];
+  const float dv = load_dt_256(d, dt, b, c, h);
   const float cs = block_inclusive_scan(dv * (A[h] * kLog2e), scratch);
   if (tid < d.Q) {
     s_cs2[tid] = cs;
@@ -181,6 +199,7 @@ __device__ __forceinline__ void chunk_cumsum_256(const TcDims& d, const float* _
 struct OuterMaps {
   CUtensorMap u;  // x or dy: [B*T][H*P] bf16, box {64, Q}
   CUtensorMap v;  // B or C:  [B*T][G*N] bf16, box {64, Q}
+  CUtensorMap o;  // output [B*nc*H*P][N] fp32, box {32, 64} (store)
 };
 
 template <int MODE>
@@ -189,7 +208,7 @@ k_chunk_outer_tc(const __grid_constant__ OuterMaps maps, TcDims d, const float* 
                  const float* __restrict__ A, float* __restrict__ out,
                  float* __restrict__ cs_last) {
   extern __shared__ __align__(1024) uint8_t smraw[];
-  uint8_t* sm = (uint8_t*)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
+  uint8_t* sm = align1024(smraw);
   const int Q = d.Q;
   uint8_t* sV = sm;                      // 2 MN blocks of [Q rows][128 B]
   uint8_t* sU = sm + 2 * Q * 128;        // [Q rows][128 B]
@@ -243,14 +262,187 @@ k_chunk_outer_tc(const __grid_constant__ OuterMaps maps, TcDims d, const float* 
   const bool done = loaded && wait_or_flag(&bar_mma, 0);
   fence_after_sync();
   if (done) {
-    // thread (wg, n): columns p in [32 wg, 32 wg + 32) of row n of D = out^T
-    const int n = tid & 127;
-    float* dst = out + (((size_t)b * d.nc + c) * d.H + h) * (size_t)(d.P * d.N) + n;
+    // thread (wg, n): columns p in [32 wg, 32 wg + 32) of row n of D = out^T,
+    // written as out[p][n] into four SW128 fp32 staging boxes [64 p][32 n]
+    // (the dead operand tiles), then stored by TMA
+    const int n = tid & 127, box = n >> 5, cc = (n & 31) >> 2, w4 = n & 3;
     float v[32];
     tmem_ld32(tm + ((uint32_t)(q * 32) << 16) + wg * 32, v);
     tmem_wait_ld();
 #pragma unroll
-    for (int i = 0; i < 32; ++i) dst[(size_t)(wg * 32 + i) * d.N] = v[i];
+    for (int i = 0; i < 32; ++i) {
+      const int pp = wg * 32 + i;
+      *(float*)(sV + box * 8192 + pp * 128 + ((cc ^ (pp & 7)) << 4) + w4 * 4) = v[i];
+    }
+    fence_async_smem();
+  }
+  __syncthreads();
+  if (tid == 0 && done) {
+    const int srow = ((b * d.nc + c) * d.H + h) * d.P;
+    for (int k = 0; k < 4; ++k) tma_store_2d(&maps.o, sV + k * 8192, 32 * k, srow);
+    bulk_commit();
+    bulk_wait0();
+  }
+  fence_before_sync();
+  __syncthreads();
+  if (tid < 32) tmem_dealloc(tm, 64);
+}
+
+// ---------------------------------------------------------------------------
+// Fused chunk-state + state pass, one CTA per (b, h), walking the chunks with a
+// two-stage TMA pipeline; the running state lives in registers (thread
+// (wg, n) holds row n, p in [32 wg, 32 wg + 32) of the transposed state).
+// MODE 0 (forward, chunks in order):
+//   S_c^T = B_c^T (w o X_c), w_j = exp(cs_last - cs_j) dt_j;
+//   hist[c] = H_{c-1};  H_c = exp(cs_last) H_{c-1} + S_c;  final = H_{nc-1}.
+// MODE 1 (backward, chunks in reverse):
+//   R_c^T = C_c^T (e o dY_c), e_i = exp(cs_i);
+//   gT[c] = g_c (bf16 rows n), hT[c] = H_{c-1} from hist (bf16 rows n);
+//   g_{c-1} = exp(cs_last) g_c + R_c;  dh0 = g_{-1}.
+struct ScanStateMaps {
+  CUtensorMap u;  // x or dy: [B*T][H*P] bf16, box {64, Q}
+  CUtensorMap v;  // B or C:  [B*T][G*N] bf16, box {64, Q}
+};
+
+template <int MODE>
+__global__ void __launch_bounds__(256, 1)
+k_state_scan_tc(const __grid_constant__ ScanStateMaps maps, TcDims d, const float* __restrict__ dt,
+                const float* __restrict__ A, const float* __restrict__ h0,
+                float* __restrict__ hist, float* __restrict__ final_or_dh0,
+                __nv_bfloat16* __restrict__ gT, __nv_bfloat16* __restrict__ hT) {
+  extern __shared__ __align__(1024) uint8_t smraw[];
+  uint8_t* sm = align1024(smraw);
+  const int Q = d.Q;
+  const uint32_t stage_bytes = 3u * Q * 128;  // V: 2 MN blocks of [Q][128 B]; U: [Q][128 B]
+  __shared__ float s_cs2[256], s_dt[256], s_w[256], scratch[8];
+  __shared__ uint64_t bar_load[2], bar_mma;
+  __shared__ uint32_t tmem_base;
+  const int h = blockIdx.x, b = blockIdx.y;
+  const int g = h / d.hpg, tid = threadIdx.x, wg = tid >> 7, q = (tid >> 5) & 3;
+  const int n = tid & 127;
+  const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+  const float a2 = A[h] * kLog2e;
+  const int nc = d.nc;
+  const size_t PN = (size_t)d.P * d.N;
+
+  if (tid == 0) {
+    prefetch_tmap(&maps.u);
+    prefetch_tmap(&maps.v);
+    mbar_init(&bar_load[0], 1);
+    mbar_init(&bar_load[1], 1);
+    mbar_init(&bar_mma, 1);
+    fence_mbar_init();
+  }
+  if (tid < 32) {
+    tmem_alloc(&tmem_base, 64);
+    tmem_relinquish();
+  }
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  const uint32_t tm = tmem_base;
+
+  auto chunk_of = [&](int it) { return MODE == 0 ? it : nc - 1 - it; };
+  auto issue = [&](int it) {
+    const int c = chunk_of(it);
+    uint8_t* st = sm + (it & 1) * stage_bytes;
+    const int row0 = b * d.T + c * Q;
+    mbar_expect_tx(&bar_load[it & 1], stage_bytes);
+    tma_load_2d(st, &maps.v, g * d.N, row0, &bar_load[it & 1]);
+    tma_load_2d(st + Q * 128, &maps.v, g * d.N + 64, row0, &bar_load[it & 1]);
+    tma_load_2d(st + 2 * Q * 128, &maps.u, h * d.P, row0, &bar_load[it & 1]);
+  };
+  if (tid == 0) {
+    issue(0);
+    if (nc > 1) issue(1);
+  }
+
+  // running state (forward) or state gradient (backward): row n, p = 32 wg + i
+  float st[32];
+  if (MODE == 0 && h0) {
+    const float* src = h0 + ((size_t)b * d.H + h) * PN + n;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) st[i] = src[(size_t)(wg * 32 + i) * d.N];
+  } else {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) st[i] = 0.f;
+  }
+  float dt_next = load_dt_256(d, dt, b, chunk_of(0), h);
+  bool ok = true;
+  uint32_t mma_phase = 0;
+
+  for (int it = 0; it < nc && ok; ++it) {
+    const int c = chunk_of(it);
+    const float dv = dt_next;
+    if (it + 1 < nc) dt_next = load_dt_256(d, dt, b, chunk_of(it + 1), h);
+    chunk_cumsum_256v(d, dv, a2, s_cs2, s_dt, scratch);
+    const float last2 = s_cs2[Q - 1];
+    if (tid < Q) s_w[tid] = MODE == 0 ? exp2f(last2 - s_cs2[tid]) * s_dt[tid] : exp2f(s_cs2[tid]);
+    // the chunk's state entry (history) as it stands before this chunk
+    const size_t soff = (((size_t)b * nc + c) * d.H + h) * PN;
+    if (MODE == 0) {
+      float* dst = hist + soff + n;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) dst[(size_t)(wg * 32 + i) * d.N] = st[i];
+    } else {
+      // g_c and H_{c-1} as bf16 rows n (this thread: bytes [64 wg, 64 wg + 64) of row n)
+      const size_t orow = (((size_t)b * nc + c) * d.H + h) * d.N + n;
+      const float* hsrc = hist + soff + n;
+      float hv[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) hv[i] = hsrc[(size_t)(wg * 32 + i) * d.N];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        uint4 og, oh;
+        og.x = pack_bf16(st[k * 8 + 0], st[k * 8 + 1]);
+        og.y = pack_bf16(st[k * 8 + 2], st[k * 8 + 3]);
+        og.z = pack_bf16(st[k * 8 + 4], st[k * 8 + 5]);
+        og.w = pack_bf16(st[k * 8 + 6], st[k * 8 + 7]);
+        oh.x = pack_bf16(hv[k * 8 + 0], hv[k * 8 + 1]);
+        oh.y = pack_bf16(hv[k * 8 + 2], hv[k * 8 + 3]);
+        oh.z = pack_bf16(hv[k * 8 + 4], hv[k * 8 + 5]);
+        oh.w = pack_bf16(hv[k * 8 + 6], hv[k * 8 + 7]);
+        *(uint4*)(gT + orow * d.P + wg * 32 + k * 8) = og;
+        *(uint4*)(hT + orow * d.P + wg * 32 + k * 8) = oh;
+      }
+    }
+    ok = wait_or_flag(&bar_load[it & 1], (it >> 1) & 1);  // also publishes s_w
+    if (!ok) break;
+    uint8_t* stg = sm + (it & 1) * stage_bytes;
+    uint8_t* sV = stg;
+    uint8_t* sU = stg + 2 * Q * 128;
+    scale_tile_rows(sU, Q * 8, [&](int r) { return s_w[r]; });
+    fence_async_smem();
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    if (tid == 0) {
+      const uint32_t idesc = idesc_bf16(128, 64, true, true);
+      for (int ks = 0; ks < Q / 16; ++ks)
+        mma_bf16(tm, desc_sw128(smem_u32(sV) + ks * 2048, Q * 128, 1024),
+                 desc_sw128(smem_u32(sU) + ks * 2048, Q * 128, 1024), idesc, ks > 0);
+      mma_commit(&bar_mma);
+    }
+    ok = wait_or_flag(&bar_mma, mma_phase);
+    mma_phase ^= 1;
+    fence_after_sync();
+    if (!ok) break;
+    // the stage is free: prefetch chunk it + 2 into it
+    if (tid == 0 && it + 2 < nc) issue(it + 2);
+    float v[32];
+    tmem_ld32(tm + lane_base + wg * 32, v);
+    tmem_wait_ld();
+    const float e = exp2f(last2);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) st[i] = fmaf(e, st[i], v[i]);
+    fence_before_sync();
+    __syncthreads();  // TMEM and s_w reused by the next chunk
+    fence_after_sync();
+  }
+  if (ok && final_or_dh0) {
+    float* dst = final_or_dh0 + ((size_t)b * d.H + h) * PN + n;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) dst[(size_t)(wg * 32 + i) * d.N] = st[i];
   }
   fence_before_sync();
   __syncthreads();
@@ -278,7 +470,7 @@ k_fwd_scan_tc(const __grid_constant__ ScanMaps maps, TcDims d, const float* __re
               const float* __restrict__ A, const float* __restrict__ D,
               const float* __restrict__ hist) {
   extern __shared__ __align__(1024) uint8_t smraw[];
-  uint8_t* sm = (uint8_t*)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
+  uint8_t* sm = align1024(smraw);
   uint8_t* sC = sm + kScanR1;
   uint8_t* sB = sm + kScanR1 + 32768;
   uint8_t* sM = sm + kScanR1;   // after the CB / Ys products are done
@@ -556,7 +748,7 @@ k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, int nsub, const float* 
          float* __restrict__ dA_part, float* __restrict__ dD_part, void* __restrict__ dB_out,
          void* __restrict__ dC_out) {
   extern __shared__ __align__(1024) uint8_t smraw[];
-  uint8_t* sm = (uint8_t*)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
+  uint8_t* sm = align1024(smraw);
   uint8_t* sC = sm + kBwC;
   uint8_t* sB = sm + kBwB;
   uint8_t* sO = sm + kBwO;
@@ -640,12 +832,21 @@ k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, int nsub, const float* 
     }
     issue_head_loads(h_first);
   }
+  // dt, A and D of the next head are loaded one head ahead
+  float dt_next = load_dt_256(d, dt, b, c, h_first);
+  float A_next = A[h_first], D_next = D[h_first];
   bool ok = wait_or_flag(&bar_shared, 0);
   uint32_t mma_phase = 0;
 
   for (int hh = 0; hh < kh && ok; ++hh) {
     const int h = h_first + hh;
-    chunk_cumsum_256(d, dt, A, b, c, h, s_cs2, s_dt, scratch);
+    const float dv = dt_next, Ah = A_next, Dh = D_next;
+    if (hh + 1 < kh) {
+      dt_next = load_dt_256(d, dt, b, c, h + 1);
+      A_next = A[h + 1];
+      D_next = D[h + 1];
+    }
+    chunk_cumsum_256v(d, dv, Ah * kLog2e, s_cs2, s_dt, scratch);
     for (int e = tid; e < 4 * 128; e += kBwThreads) {
       const int w = e >> 7, jj = e & 127;
       const int r = base + 32 * w, J = base + jj;
@@ -856,15 +1057,28 @@ k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, int nsub, const float* 
 
     // this thread's half rows of x_j and dy_i (unscaled) into registers, then
     // scale the tiles in place: X rows j by exp(cs_end - cs_j) dt_j, dY rows i by exp(cs_i - ref)
+    // (every 16-byte chunk belongs to exactly one thread: row `row`, chunks 4wg..4wg+3)
     uint4 xr[4], dyr[4];
+    {
+      const float sx = exp2f(end2 - s_cs2[base + row]) * s_dt[base + row];
+      const float sy = exp2f(s_cs2[base + row] - ref2);
 #pragma unroll
-    for (int q4 = 0; q4 < 4; ++q4) {
-      xr[q4] = *(const uint4*)(sX + sw128(row, wg * 4 + q4));
-      dyr[q4] = *(const uint4*)(sDY + sw128(row, wg * 4 + q4));
+      for (int q4 = 0; q4 < 4; ++q4) {
+        uint8_t* px = sX + sw128(row, wg * 4 + q4);
+        uint8_t* py = sDY + sw128(row, wg * 4 + q4);
+        xr[q4] = *(const uint4*)px;
+        dyr[q4] = *(const uint4*)py;
+        float f[8];
+        unpack8(xr[q4], f);
+#pragma unroll
+        for (int t = 0; t < 8; ++t) f[t] *= sx;
+        store_row_bf16(sX, row, wg * 4 + q4, f);
+        unpack8(dyr[q4], f);
+#pragma unroll
+        for (int t = 0; t < 8; ++t) f[t] *= sy;
+        store_row_bf16(sDY, row, wg * 4 + q4, f);
+      }
     }
-    __syncthreads();
-    scale_tile_rows(sX, 128 * 8, [&](int r) { return exp2f(end2 - s_cs2[base + r]) * s_dt[base + r]; });
-    scale_tile_rows(sDY, 128 * 8, [&](int r) { return exp2f(s_cs2[base + r] - ref2); });
     fence_async_smem();
     fence_before_sync();
     __syncthreads();
@@ -887,7 +1101,6 @@ k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, int nsub, const float* 
     const float dtI = s_dt[I];
     float drive = 0.f, ej = 0.f, stin = 0.f, dd = 0.f;
     {
-      const float Dh = D[h];
       float gx[32], gs[32], ch[32];
       tmem_ld32(T0 + lane_base + wg * 32, gx);
       tmem_ld32(T0 + lane_base + 64 + wg * 32, gs);
@@ -948,7 +1161,7 @@ k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, int nsub, const float* 
     const int Jr = base + 127 - row;                       // row whose da this thread holds
     if (wg == 0) s_v[row] = drive;
     __syncthreads();
-    if (wg == 0) ddt[((size_t)crow + Jr) * d.H + h] = s_v[127 - row] + A[h] * da;
+    if (wg == 0) ddt[((size_t)crow + Jr) * d.H + h] = s_v[127 - row] + Ah * da;
     const float a_sum = block_sum(wg == 0 ? s_dt[Jr] * da : 0.f, scratch);
     const float d_sum = block_sum(dd, scratch);
     if (tid == 0) {
@@ -1032,13 +1245,21 @@ k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, int nsub, const float* 
       for (int e = tid; e < rows_per * 32; e += kBwThreads) {
         const int rr = (int)rank * rows_per + (e >> 5), cc = e & 31;
         const uint32_t off = (uint32_t)(rr * 128 + ((cc ^ (rr & 31)) << 2)) * 4u;
+        // all remote loads first (independent), then the fixed-order sums
+        float4 pa[8], pb8[8];
+#pragma unroll
+        for (int r = 0; r < 8; ++r)
+          if (r < nsub) {
+            pa[r] = ld_cluster_f4(map_cluster(baseC + off, (uint32_t)r));
+            pb8[r] = ld_cluster_f4(map_cluster(baseB + off, (uint32_t)r));
+          }
         float4 sc = make_float4(0.f, 0.f, 0.f, 0.f), sb = sc;
-        for (int r = 0; r < nsub; ++r) {
-          const float4 a = ld_cluster_f4(map_cluster(baseC + off, (uint32_t)r));
-          const float4 bq = ld_cluster_f4(map_cluster(baseB + off, (uint32_t)r));
-          sc.x += a.x; sc.y += a.y; sc.z += a.z; sc.w += a.w;
-          sb.x += bq.x; sb.y += bq.y; sb.z += bq.z; sb.w += bq.w;
-        }
+#pragma unroll
+        for (int r = 0; r < 8; ++r)
+          if (r < nsub) {
+            sc.x += pa[r].x; sc.y += pa[r].y; sc.z += pa[r].z; sc.w += pa[r].w;
+            sb.x += pb8[r].x; sb.y += pb8[r].y; sb.z += pb8[r].z; sb.w += pb8[r].w;
+          }
         const size_t gi = ((size_t)(row0 + rr) * d.G + g) * d.N + cc * 4;
         uint2 pc, pb;
         pc.x = pack_bf16(sc.x, sc.y);
@@ -1146,6 +1367,21 @@ bool map_bf16(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, ui
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2D fp32 row-major [rows][cols] map with a {box_cols, box_rows} SW128 box
+// (box_cols * 4 = 128 bytes).
+bool map_f32(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_cols,
+             uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 4};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 TcDims tc_dims(const Problem& p) { return TcDims{p.B, p.T, p.H, p.P, p.N, p.G, p.Q, p.nc, p.hpg}; }
 
 template <typename K>
@@ -1172,7 +1408,8 @@ cudaError_t tc_chunk_outer(const Problem& p, int mode, float* out) {
   const void* u = mode == 0 ? p.x : p.dy;
   const void* v = mode == 0 ? p.Bm : p.Cm;
   if (!map_bf16(&maps.u, u, (uint64_t)p.B * p.T, (uint64_t)p.H * p.P, p.Q) ||
-      !map_bf16(&maps.v, v, (uint64_t)p.B * p.T, (uint64_t)p.G * p.N, p.Q))
+      !map_bf16(&maps.v, v, (uint64_t)p.B * p.T, (uint64_t)p.G * p.N, p.Q) ||
+      !map_f32(&maps.o, out, (uint64_t)p.B * p.nc * p.H * p.P, (uint64_t)p.N, 32, 64))
     return cudaErrorInvalidValue;
   const size_t smem = 3 * (size_t)p.Q * 128 + 1024;
   const TcDims d = tc_dims(p);
@@ -1189,6 +1426,38 @@ cudaError_t tc_chunk_outer(const Problem& p, int mode, float* out) {
                                                                               out, p.cs_last);
   }
   return cudaGetLastError();
+}
+
+// Whether the fused per-(b, h) state scans have enough CTAs to fill the GPU.
+bool tc_fused_states(const Problem& p) {
+  int nsm = 0, dev = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+  return (long)p.B * p.H * 4 >= 3L * nsm;
+}
+
+template <int MODE>
+cudaError_t tc_state_scan(const Problem& p, const char* name, float* final_or_dh0) {
+  ScanStateMaps maps;
+  const void* u = MODE == 0 ? p.x : p.dy;
+  const void* v = MODE == 0 ? p.Bm : p.Cm;
+  if (!map_bf16(&maps.u, u, (uint64_t)p.B * p.T, (uint64_t)p.H * p.P, p.Q) ||
+      !map_bf16(&maps.v, v, (uint64_t)p.B * p.T, (uint64_t)p.G * p.N, p.Q))
+    return cudaErrorInvalidValue;
+  const size_t smem = 2 * 3 * (size_t)p.Q * 128 + 1024;
+  cudaError_t e = set_smem_tc(k_state_scan_tc<MODE>, smem);
+  if (e != cudaSuccess) return e;
+  {
+    LaunchScope ls(name, p.stream);
+    k_state_scan_tc<MODE><<<dim3(p.H, p.B), 256, smem, p.stream>>>(
+        maps, tc_dims(p), p.dt, p.A, p.h0, p.hist, final_or_dh0, (__nv_bfloat16*)p.gT,
+        (__nv_bfloat16*)p.hT);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t tc_forward_states(const Problem& p) {
+  return tc_state_scan<0>(p, "state_scan_fwd_tc", p.final_state);
 }
 
 cudaError_t tc_forward_scan(const Problem& p) {
@@ -1211,15 +1480,19 @@ cudaError_t tc_forward_scan(const Problem& p) {
 }
 
 cudaError_t tc_backward(const Problem& p) {
-  cudaError_t e = tc_chunk_outer(p, 1, p.dstate);
-  if (e != cudaSuccess) return e;
-  {
-    LaunchScope ls("state_pass_bwd_tc", p.stream);
-    k_state_pass_bwd_t<<<dim3(p.N / 16, p.H, p.B), 256, 0, p.stream>>>(
-        tc_dims(p), p.dstate, p.hist, p.cs_last, (__nv_bfloat16*)p.gT, (__nv_bfloat16*)p.hT,
-        p.dh0);
+  cudaError_t e;
+  if (tc_fused_states(p)) {
+    if ((e = tc_state_scan<1>(p, "state_scan_bwd_tc", p.dh0)) != cudaSuccess) return e;
+  } else {
+    if ((e = tc_chunk_outer(p, 1, p.dstate)) != cudaSuccess) return e;
+    {
+      LaunchScope ls("state_pass_bwd_tc", p.stream);
+      k_state_pass_bwd_t<<<dim3(p.N / 16, p.H, p.B), 256, 0, p.stream>>>(
+          tc_dims(p), p.dstate, p.hist, p.cs_last, (__nv_bfloat16*)p.gT, (__nv_bfloat16*)p.hT,
+          p.dh0);
+    }
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
   BwdMaps maps;
   const uint64_t rows = (uint64_t)p.B * p.T;
   const uint64_t srows = (uint64_t)p.B * p.nc * p.H * p.N;

@@ -28,6 +28,14 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
 }
 
+// First 1024-byte boundary at or after a dynamic shared-memory base.  The
+// offset is added to the shared pointer itself (not through an integer cast)
+// so the compiler keeps emitting shared-memory instructions for accesses.
+__device__ __forceinline__ uint8_t* align1024(uint8_t* base) {
+  const uint32_t a = smem_u32(base);
+  return base + ((1024u - (a & 1023u)) & 1023u);
+}
+
 // byte offset of (row, 16-byte chunk) inside a SW128 tile
 __device__ __forceinline__ uint32_t sw128(uint32_t row, uint32_t chunk) {
   return row * 128u + ((chunk ^ (row & 7u)) << 4);

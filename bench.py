@@ -70,15 +70,23 @@ def kernel_bytes(name, d, has_h0):
         "chunk_state": z["x"] + z["dt"] + z["bc"] + z["st"] + z["cl"],
         "state_pass_fwd": 2 * z["st"] + z["h0"] + z["hs"] + z["cl"],
         "chunk_scan": 2 * z["x"] + z["dt"] + 2 * z["bc"] + z["st"],
+        # the scan variant that reads the bf16 copy of the chunk states
+        "chunk_scan_ht": 2 * z["x"] + z["dt"] + 2 * z["bc"] + z["st"] // 2,
         "chunk_dstate": z["x"] + z["dt"] + z["bc"] + z["st"] + z["cl"],
         "state_pass_bwd": 2 * z["st"] + z["hs"] + z["cl"],
         "bwd_col": 3 * z["x"] + z["dt"] + 3 * z["bc"] + z["st"] + 3 * z["tokh"],
         "bwd_row": 2 * z["x"] + z["dt"] + 3 * z["bc"] + z["st"] + 2 * z["tokh"],
         "bwd_dt": 2 * z["dt"] + 2 * z["st"] + 5 * z["tokh"],
-        # tensor-core backward: x, dy, dt, B, C, history, state gradient in;
-        # dx, ddt, dB, dC out (dA, dD partials are negligible)
-        "bwd": 3 * z["x"] + 2 * z["dt"] + 4 * z["bc"] + 2 * z["st"],
         "reduce_heads": 2 * z["small"],
+        # fused forward state scan: x, B, dt (+h0) in; fp32 history, final state
+        # and the bf16 copy of the history out
+        "state_scan_fwd": z["x"] + z["dt"] + z["bc"] + z["h0"] + z["st"] + z["hs"] + z["st"] // 2,
+        # fused backward state scan: dy, C, dt, fp32 history in; bf16 state and
+        # state-gradient rows and dh0 out
+        "state_scan_bwd": z["x"] + z["dt"] + z["bc"] + z["st"] + z["st"] + z["hs"],
+        # tensor-core backward: x, dy, dt, B, C, bf16 state and state-gradient
+        # rows in; dx, ddt, dB, dC out (dA, dD partials are negligible)
+        "bwd": 3 * z["x"] + 2 * z["dt"] + 4 * z["bc"] + z["st"],
     }
     return table.get(base)
 
@@ -138,6 +146,19 @@ def read_traffic(kernel, workload):
     if not ent or ent.get("workload") != workload:
         return None
     return ent.get("dram_bytes_per_launch")
+
+
+def aggregate_ranks(ms_local, tokens_local, dist=None, device=None):
+    """Whole-job throughput of independent replicas: the slowest rank's
+    per-step time and the tokens of all ranks over that time."""
+    import torch
+    world = dist.get_world_size() if dist else 1
+    ms_max = ms_local
+    if dist:
+        t = torch.tensor([ms_local], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_max = float(t.item())
+    return ms_max, tokens_local * world / (ms_max / 1e3)
 
 
 # ---------------------------------------------------------------------------
@@ -355,13 +376,8 @@ def main():
     ms = sum(step_ms) / len(step_ms)
     kern = nat.trace_read()
     nat.trace_reset()
-    ms_max = ms
-    if dist:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_max = float(t.item())
     tokens = dims.tokens
-    value = tokens * world / (ms_max / 1e3)
+    ms_max, value = aggregate_ranks(ms, tokens, dist, dev)
 
     # ---- e2e: host buffers through the public API, copies inside the timed region
     e2e = None

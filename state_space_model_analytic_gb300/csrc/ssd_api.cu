@@ -158,6 +158,7 @@ size_t carve(Problem* p, char* base, int which) {
   if (which == 0) {
     float* h = (float*)take(states);
     if (!p->hist) p->hist = h;
+    p->hT = take(states / 2);  // bf16 copy of the chunk states for the tensor-core scan
     return off;
   }
   p->dstate = (float*)take(states);
@@ -321,9 +322,10 @@ int ssd_forward(const ssd_dims* dims, const void* x, const float* dt, const floa
   const bool tc = tc_supported(p);
   cudaError_t e;
   if (tc && tc_fused_states(p)) {
-    e = tc_forward_states(p);
+    e = tc_forward_states(p);  // also writes the bf16 state rows (p.hT) the scan reads
     if (e != cudaSuccess) return cuda_fail(e, "forward state-scan kernel");
   } else {
+    p.hT = nullptr;  // the scan converts the fp32 history itself
     e = tc ? tc_chunk_outer(p, 0, p.hist) : simt_forward_states(p, p.hist, p.cs_last);
     if (e != cudaSuccess) return cuda_fail(e, "forward chunk-state kernel");
     e = simt_state_pass_fwd(p, p.hist, p.cs_last);

@@ -50,4 +50,48 @@ __device__ __forceinline__ float block_sum(float v, float* scratch) {
   return s;
 }
 
+// Inclusive prefix sums of two values at once (same fixed order as above).
+// `scratch` holds at least blockDim.x / 32 float2.
+__device__ __forceinline__ float2 block_inclusive_scan2(float2 v, float2* scratch) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float tx = __shfl_up_sync(0xffffffffu, v.x, o);
+    const float ty = __shfl_up_sync(0xffffffffu, v.y, o);
+    if (lane >= o) {
+      v.x += tx;
+      v.y += ty;
+    }
+  }
+  __syncthreads();
+  if (lane == 31) scratch[warp] = v;
+  __syncthreads();
+  float2 base = make_float2(0.f, 0.f);
+  for (int w = 0; w < warp; ++w) {
+    base.x += scratch[w].x;
+    base.y += scratch[w].y;
+  }
+  return make_float2(v.x + base.x, v.y + base.y);
+}
+
+// Sum of two values over the block in a fixed order; every thread gets both.
+__device__ __forceinline__ float2 block_sum2(float2 v, float2* scratch) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    v.x += __shfl_xor_sync(0xffffffffu, v.x, o);
+    v.y += __shfl_xor_sync(0xffffffffu, v.y, o);
+  }
+  __syncthreads();
+  if (lane == 0) scratch[warp] = v;
+  __syncthreads();
+  float2 t = make_float2(0.f, 0.f);
+  const int nw = blockDim.x >> 5;
+  for (int w = 0; w < nw; ++w) {
+    t.x += scratch[w].x;
+    t.y += scratch[w].y;
+  }
+  return t;
+}
+
 }  // namespace ssd

@@ -21,6 +21,7 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 
+#include <cstdlib>
 #include <mutex>
 
 #include "ssd_common.cuh"
@@ -368,6 +369,14 @@ k_state_scan_tc(const __grid_constant__ ScanStateMaps maps, TcDims d, const floa
     for (int i = 0; i < 32; ++i) st[i] = 0.f;
   }
   float dt_next = load_dt_256(d, dt, b, chunk_of(0), h);
+  // backward: this thread's 32 history values of the next chunk, one chunk ahead
+  float hv_next[32];
+  auto load_hist = [&](int c, float (&dst)[32]) {
+    const float* hsrc = hist + (((size_t)b * nc + c) * d.H + h) * PN + n;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) dst[i] = hsrc[(size_t)(wg * 32 + i) * d.N];
+  };
+  if (MODE == 1) load_hist(chunk_of(0), hv_next);
   bool ok = true;
   uint32_t mma_phase = 0;
 
@@ -375,6 +384,12 @@ k_state_scan_tc(const __grid_constant__ ScanStateMaps maps, TcDims d, const floa
     const int c = chunk_of(it);
     const float dv = dt_next;
     if (it + 1 < nc) dt_next = load_dt_256(d, dt, b, chunk_of(it + 1), h);
+    float hv[32];
+    if (MODE == 1) {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) hv[i] = hv_next[i];
+      if (it + 1 < nc) load_hist(chunk_of(it + 1), hv_next);
+    }
     chunk_cumsum_256v(d, dv, a2, s_cs2, s_dt, scratch);
     const float last2 = s_cs2[Q - 1];
     if (tid < Q) s_w[tid] = MODE == 0 ? exp2f(last2 - s_cs2[tid]) * s_dt[tid] : exp2f(s_cs2[tid]);
@@ -384,13 +399,21 @@ k_state_scan_tc(const __grid_constant__ ScanStateMaps maps, TcDims d, const floa
       float* dst = hist + soff + n;
 #pragma unroll
       for (int i = 0; i < 32; ++i) dst[(size_t)(wg * 32 + i) * d.N] = st[i];
+      if (hT) {  // the same state as bf16 rows n, for the forward chunk scan
+        const size_t orow = (((size_t)b * nc + c) * d.H + h) * d.N + n;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          uint4 oh;
+          oh.x = pack_bf16(st[k * 8 + 0], st[k * 8 + 1]);
+          oh.y = pack_bf16(st[k * 8 + 2], st[k * 8 + 3]);
+          oh.z = pack_bf16(st[k * 8 + 4], st[k * 8 + 5]);
+          oh.w = pack_bf16(st[k * 8 + 6], st[k * 8 + 7]);
+          *(uint4*)(hT + orow * d.P + wg * 32 + k * 8) = oh;
+        }
+      }
     } else {
       // g_c and H_{c-1} as bf16 rows n (this thread: bytes [64 wg, 64 wg + 64) of row n)
       const size_t orow = (((size_t)b * nc + c) * d.H + h) * d.N + n;
-      const float* hsrc = hist + soff + n;
-      float hv[32];
-#pragma unroll
-      for (int i = 0; i < 32; ++i) hv[i] = hsrc[(size_t)(wg * 32 + i) * d.N];
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         uint4 og, oh;
@@ -452,10 +475,11 @@ k_state_scan_tc(const __grid_constant__ ScanStateMaps maps, TcDims d, const floa
 // ---------------------------------------------------------------------------
 // Forward chunk scan: y for one (b, chunk, head) per CTA, block by block.
 struct ScanMaps {
-  CUtensorMap x;  // [B*T][H*P] bf16, box {64, 128}
-  CUtensorMap B;  // [B*T][G*N] bf16, box {64, 128}
-  CUtensorMap C;  // [B*T][G*N] bf16, box {64, 128}
-  CUtensorMap y;  // [B*T][H*P] bf16, box {64, 128} (store)
+  CUtensorMap x;   // [B*T][H*P] bf16, box {64, 128}
+  CUtensorMap B;   // [B*T][G*N] bf16, box {64, 128}
+  CUtensorMap C;   // [B*T][G*N] bf16, box {64, 128}
+  CUtensorMap y;   // [B*T][H*P] bf16, box {64, 128} (store)
+  CUtensorMap ht;  // chunk-start states as bf16 rows n: [B*nc*H*N][P], box {64, 128}
 };
 
 // shared-memory layout of k_fwd_scan_tc (offsets from the 1024-aligned base);
@@ -465,6 +489,9 @@ constexpr uint32_t kScanX = 65536;    // X block [128 rows][64 p]
 constexpr uint32_t kScanH = 81920;    // state as bf16 B operand, row n, 64 p (MN-major)
 constexpr uint32_t kScanBytes = 98304;
 
+// kHT: the chunk-start state comes as bf16 rows (TMA) instead of fp32 [P][N]
+// loaded by the threads.
+template <bool kHT>
 __global__ void __launch_bounds__(256, 2)
 k_fwd_scan_tc(const __grid_constant__ ScanMaps maps, TcDims d, const float* __restrict__ dt,
               const float* __restrict__ A, const float* __restrict__ D,
@@ -509,22 +536,22 @@ k_fwd_scan_tc(const __grid_constant__ ScanMaps maps, TcDims d, const float* __re
   uint32_t load_phase = 0, mma_phase = 0;
   bool ok = true;
 
-  auto issue_loads = [&](int row0) {
-    mbar_expect_tx(&bar_load, 80 * 1024);
+  auto issue_loads = [&](int row0, bool with_state) {
+    mbar_expect_tx(&bar_load, (with_state ? 96 : 80) * 1024);
     tma_load_2d(sC, &maps.C, g * d.N, row0, &bar_load);
     tma_load_2d(sC + 16384, &maps.C, g * d.N + 64, row0, &bar_load);
     tma_load_2d(sB, &maps.B, g * d.N, row0, &bar_load);
     tma_load_2d(sB + 16384, &maps.B, g * d.N + 64, row0, &bar_load);
     tma_load_2d(sX, &maps.x, h * d.P, row0, &bar_load);
+    if (with_state) tma_load_2d(sH, &maps.ht, 0, ((b * d.nc + c) * d.H + h) * d.N, &bar_load);
   };
   const int crow = b * d.T + c * Q;
-  if (tid == 0) issue_loads(crow);
+  if (tid == 0) issue_loads(crow, kHT);
 
-  // H_{c-1} (fp32 [P][N]) -> bf16 rows n (64 p each): the MN-major B operand of
-  // C H^T.  Thread (wg, n) converts p in [32 wg, 32 wg + 32).
+  // H_{c-1} as bf16 rows n (64 p each): the MN-major B operand of C H^T.
   const float* Hg = hist + (((size_t)b * d.nc + c) * d.H + h) * (size_t)(64 * 128);
   chunk_cumsum_256(d, dt, A, b, c, h, s_cs2, s_dt, scratch);
-  {
+  if (!kHT) {  // thread (wg, n) converts p in [32 wg, 32 wg + 32) from fp32 [P][N]
     const int n = row;
 #pragma unroll
     for (int ch = 0; ch < 4; ++ch) {
@@ -685,14 +712,21 @@ k_fwd_scan_tc(const __grid_constant__ ScanMaps maps, TcDims d, const float* __re
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         float v8[8];
+        if (kHT) {
+          float hf[8];
+          unpack8(*(const uint4*)(sH + sw128(n, wg * 4 + k)), hf);
 #pragma unroll
-        for (int t = 0; t < 8; ++t)
-          v8[t] = fmaf(e127, Hg[(size_t)(wg * 32 + k * 8 + t) * 128 + n], v[k * 8 + t]);
+          for (int t = 0; t < 8; ++t) v8[t] = fmaf(e127, hf[t], v[k * 8 + t]);
+        } else {
+#pragma unroll
+          for (int t = 0; t < 8; ++t)
+            v8[t] = fmaf(e127, Hg[(size_t)(wg * 32 + k * 8 + t) * 128 + n], v[k * 8 + t]);
+        }
         store_row_bf16(sH, n, wg * 4 + k, v8);
       }
       if (tid == 0) {
         bulk_wait_read0();  // y staging (region R1) is reloaded next
-        issue_loads(row0 + 128);
+        issue_loads(row0 + 128, false);
       }
       // sH written by every thread: visible to the next block's MMA
       fence_async_smem();
@@ -733,13 +767,13 @@ struct BwdMaps {
 constexpr int kBwThreads = 256;       // two warpgroups share each TMEM row
 constexpr uint32_t kBwC = 0;          // C_k: 2 K-major tiles [128][128 B]
 constexpr uint32_t kBwB = 32768;      // B_k
-constexpr uint32_t kBwO = 65536;      // B_0 (k = 1) or C_1 (k = 0) when the chunk has 2 blocks
+constexpr uint32_t kBwO = 65536;      // L o CB (2 tiles, same layout as W)
 constexpr uint32_t kBwX = 98304;      // X_k  [128 rows][64 p]
 constexpr uint32_t kBwDY = 114688;    // dY_k
 constexpr uint32_t kBwXO = 131072;    // X_0 (k = 1) or dY_1 (k = 0), row-scaled
 constexpr uint32_t kBwH = 147456;     // Hin  bf16, row n, 64 p
 constexpr uint32_t kBwG = 163840;     // gout bf16, row n, 64 p
-constexpr uint32_t kBwW = 180224;     // W, then L o CB, then staging (2 tiles)
+constexpr uint32_t kBwW = 180224;     // B_0 (k = 1) / C_1 (k = 0) per head, then W, then dx staging
 constexpr uint32_t kBwBytes = 212992;
 
 __global__ void __launch_bounds__(kBwThreads, 1)
@@ -764,6 +798,8 @@ k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, int nsub, const float* 
   __shared__ float s_col[4][128];                // per-warp strict column sums of M
   __shared__ float s_red[5][128];                // second warpgroup's row partials
   __shared__ float s_v[128];
+  __shared__ float2 s_v2[128], scratch2[8];
+  __shared__ float s_esum;
   __shared__ uint64_t bar_shared, bar_head, bar_mma;
   __shared__ uint32_t tmem_base;
 
@@ -778,7 +814,7 @@ k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, int nsub, const float* 
   const int row0 = crow + base;
   const uint32_t lane_base = (uint32_t)(q * 32) << 16;
   const bool two = nblk == 2;
-  const uint32_t head_bytes = (two ? 48 : 32) * 1024 + 32 * 1024;
+  const uint32_t head_bytes = (two ? 80 : 32) * 1024 + 32 * 1024;
 
   if (tid == 0) {
     prefetch_tmap(&maps.x);
@@ -806,9 +842,16 @@ k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, int nsub, const float* 
     mbar_expect_tx(&bar_head, head_bytes);
     tma_load_2d(sX, &maps.x, h * d.P, row0, &bar_head);
     tma_load_2d(sDY, &maps.dy, h * d.P, row0, &bar_head);
-    if (two) {
-      if (k == 1) tma_load_2d(sXO, &maps.x, h * d.P, crow, &bar_head);
-      else tma_load_2d(sXO, &maps.dy, h * d.P, crow + 128, &bar_head);
+    if (two) {  // the other block's tiles for the mid-chunk state / state gradient
+      if (k == 1) {
+        tma_load_2d(sXO, &maps.x, h * d.P, crow, &bar_head);
+        tma_load_2d(sW, &maps.B, g * d.N, crow, &bar_head);
+        tma_load_2d(sW + 16384, &maps.B, g * d.N + 64, crow, &bar_head);
+      } else {
+        tma_load_2d(sXO, &maps.dy, h * d.P, crow + 128, &bar_head);
+        tma_load_2d(sW, &maps.C, g * d.N, crow + 128, &bar_head);
+        tma_load_2d(sW + 16384, &maps.C, g * d.N + 64, crow + 128, &bar_head);
+      }
     }
     const int srow = ((b * d.nc + c) * d.H + h) * d.N;
     tma_load_2d(sH, &maps.ht, 0, srow, &bar_head);
@@ -816,20 +859,11 @@ k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, int nsub, const float* 
   };
   const int h_first = g * d.hpg + sub * kh;
   if (tid == 0) {
-    mbar_expect_tx(&bar_shared, two ? 96 * 1024 : 64 * 1024);
+    mbar_expect_tx(&bar_shared, 64 * 1024);
     tma_load_2d(sC, &maps.C, g * d.N, row0, &bar_shared);
     tma_load_2d(sC + 16384, &maps.C, g * d.N + 64, row0, &bar_shared);
     tma_load_2d(sB, &maps.B, g * d.N, row0, &bar_shared);
     tma_load_2d(sB + 16384, &maps.B, g * d.N + 64, row0, &bar_shared);
-    if (two) {
-      if (k == 1) {
-        tma_load_2d(sO, &maps.B, g * d.N, crow, &bar_shared);
-        tma_load_2d(sO + 16384, &maps.B, g * d.N + 64, crow, &bar_shared);
-      } else {
-        tma_load_2d(sO, &maps.C, g * d.N, crow + 128, &bar_shared);
-        tma_load_2d(sO + 16384, &maps.C, g * d.N + 64, crow + 128, &bar_shared);
-      }
-    }
     issue_head_loads(h_first);
   }
   // dt, A and D of the next head are loaded one head ahead
@@ -873,7 +907,7 @@ k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, int nsub, const float* 
         // S_0^T = B_0^T (w o X_0)  or  R_1^T = C_1^T (e o dY_1):  M = n, N = p, K = rows
         const uint32_t id = idesc_bf16(128, 64, true, true);
         for (int kk = 0; kk < 8; ++kk)
-          mma_bf16(T1, desc_sw128(smem_u32(sO) + kk * 2048, 16384, 1024),
+          mma_bf16(T1, desc_sw128(smem_u32(sW) + kk * 2048, 16384, 1024),
                    desc_sw128(smem_u32(sXO) + kk * 2048, 16384, 1024), id, kk > 0);
         mma_commit(&bar_mma);
       }
@@ -936,7 +970,6 @@ k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, int nsub, const float* 
     const float fi = exp2f(s_cs2[I] - s_cs2[base + 32 * q]);
     const float csI = s_cs2[I];
     float rowsum = 0.f;
-    uint32_t lcb[32];
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
       const int jc = 2 * wg + u;
@@ -987,9 +1020,8 @@ k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, int nsub, const float* 
       for (int q4 = 0; q4 < 4; ++q4) {
         const int j = jc * 32 + q4 * 8;
         store_row_bf16(sW + (j >> 6) * 16384, row, (j & 63) >> 3, &wv[q4 * 8]);
+        store_row_bf16(sO + (j >> 6) * 16384, row, (j & 63) >> 3, &cb[q4 * 8]);
       }
-#pragma unroll
-      for (int t = 0; t < 16; ++t) lcb[u * 16 + t] = pack_bf16(cb[2 * t], cb[2 * t + 1]);
     }
     if (wg == 1) s_red[0][row] = rowsum;
     fence_async_smem();
@@ -997,7 +1029,9 @@ k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, int nsub, const float* 
     __syncthreads();
     fence_after_sync();
 
-    // ---- phase B: dC += W B_k ; dB += W^T C_k
+    // ---- phases B and C together: dC += W B_k ; dB += W^T C_k ;
+    //      Gx = (L o CB)^T dY_k -> T0[0,64) ; Gs = B_k gout^T -> T0[64,128) ;
+    //      CH = C_k Hin^T -> T1[0,64)
     if (tid == 0) {
       const uint32_t id_dc = idesc_bf16(128, 128, false, true);
       const uint32_t id_db = idesc_bf16(128, 128, true, true);
@@ -1009,37 +1043,10 @@ k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, int nsub, const float* 
       for (int kk = 0; kk < 8; ++kk)
         mma_bf16(TdB, desc_sw128(smem_u32(sW) + kk * 2048, 16384, 1024),
                  desc_sw128(smem_u32(sC) + kk * 2048, 16384, 1024), id_db, (hh > 0) || (kk > 0));
-      mma_commit(&bar_mma);
-    }
-    ok = wait_or_flag(&bar_mma, mma_phase);
-    mma_phase ^= 1;
-    fence_after_sync();
-    if (!ok) break;
-    // L o CB into sW (same physical layout: row i, j contiguous)
-#pragma unroll
-    for (int u = 0; u < 2; ++u)
-#pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        const int j = (2 * wg + u) * 32 + q4 * 8;
-        uint4 o;
-        o.x = lcb[u * 16 + q4 * 4 + 0];
-        o.y = lcb[u * 16 + q4 * 4 + 1];
-        o.z = lcb[u * 16 + q4 * 4 + 2];
-        o.w = lcb[u * 16 + q4 * 4 + 3];
-        *(uint4*)(sW + (j >> 6) * 16384 + sw128(row, (j & 63) >> 3)) = o;
-      }
-    fence_async_smem();
-    fence_before_sync();
-    __syncthreads();
-    fence_after_sync();
-
-    // ---- phase C: Gx = (L o CB)^T dY_k -> T0[0,64) ; Gs = B_k gout^T -> T0[64,128) ;
-    //               CH = C_k Hin^T -> T1[0,64)
-    if (tid == 0) {
       const uint32_t id_mm = idesc_bf16(128, 64, true, true);
       const uint32_t id_km = idesc_bf16(128, 64, false, true);
       for (int kk = 0; kk < 8; ++kk)
-        mma_bf16(T0, desc_sw128(smem_u32(sW) + kk * 2048, 16384, 1024),
+        mma_bf16(T0, desc_sw128(smem_u32(sO) + kk * 2048, 16384, 1024),
                  desc_sw128(smem_u32(sDY) + kk * 2048, 16384, 1024), id_mm, kk > 0);
       for (int kk = 0; kk < 8; ++kk) {
         const uint32_t aoff = (kk >> 2) * 16384 + (kk & 3) * 32;
@@ -1146,28 +1153,28 @@ k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, int nsub, const float* 
       ej = 0.f;
       dd = 0.f;
     }
-    // ---- dcs, reverse cumsum, ddt, dA and dD partials (rows held by warpgroup 0)
-    const float esum = block_sum(ej, scratch);
+    // ---- dcs, reverse cumsum, ddt, dA and dD partials (rows held by warpgroup 0).
+    // The end-of-block term (sum_j e_j + exp(cs_end - ref) <gout, Hin>) sits at the
+    // last row, so it adds to every da_j: scan dcs without it, together with e.
     if (wg == 0) {
       float colsum = 0.f;
       for (int w = row >> 5; w < 4; ++w) colsum += s_col[w][row];
-      float dcs = rowsum - colsum + stin - ej;
-      if (row == 127) dcs += esum + exp2f(end2 - ref2) * hg;
-      s_v[row] = dcs;
+      s_v2[row] = make_float2(rowsum - colsum + stin - ej, ej);
     }
     __syncthreads();
-    const float rv = (wg == 0) ? s_v[127 - row] : 0.f;
-    const float da = block_inclusive_scan(rv, scratch);  // syncs: every rv read before reuse
-    const int Jr = base + 127 - row;                       // row whose da this thread holds
+    const float2 rv = (wg == 0) ? s_v2[127 - row] : make_float2(0.f, 0.f);
+    const float2 sc2 = block_inclusive_scan2(rv, scratch2);  // syncs: every rv read before reuse
+    const int Jr = base + 127 - row;                          // row whose da this thread holds
     if (wg == 0) s_v[row] = drive;
+    if (tid == 127) s_esum = sc2.y;  // all e summed
     __syncthreads();
+    const float da = sc2.x + s_esum + exp2f(end2 - ref2) * hg;
     if (wg == 0) ddt[((size_t)crow + Jr) * d.H + h] = s_v[127 - row] + Ah * da;
-    const float a_sum = block_sum(wg == 0 ? s_dt[Jr] * da : 0.f, scratch);
-    const float d_sum = block_sum(dd, scratch);
+    const float2 ad = block_sum2(make_float2(wg == 0 ? s_dt[Jr] * da : 0.f, dd), scratch2);
     if (tid == 0) {
       const size_t slot = (((size_t)b * d.nc + c) * nblk + k) * d.H + h;
-      dA_part[slot] = a_sum;
-      dD_part[slot] = d_sum;
+      dA_part[slot] = ad.x;
+      dD_part[slot] = ad.y;
     }
     // ---- end of head: phase D done, dx staging read, before the tiles are reloaded
     ok = wait_or_flag(&bar_mma, mma_phase);
@@ -1246,16 +1253,16 @@ k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, int nsub, const float* 
         const int rr = (int)rank * rows_per + (e >> 5), cc = e & 31;
         const uint32_t off = (uint32_t)(rr * 128 + ((cc ^ (rr & 31)) << 2)) * 4u;
         // all remote loads first (independent), then the fixed-order sums
-        float4 pa[8], pb8[8];
+        float4 pa[16], pb8[16];
 #pragma unroll
-        for (int r = 0; r < 8; ++r)
+        for (int r = 0; r < 16; ++r)
           if (r < nsub) {
             pa[r] = ld_cluster_f4(map_cluster(baseC + off, (uint32_t)r));
             pb8[r] = ld_cluster_f4(map_cluster(baseB + off, (uint32_t)r));
           }
         float4 sc = make_float4(0.f, 0.f, 0.f, 0.f), sb = sc;
 #pragma unroll
-        for (int r = 0; r < 8; ++r)
+        for (int r = 0; r < 16; ++r)
           if (r < nsub) {
             sc.x += pa[r].x; sc.y += pa[r].y; sc.z += pa[r].z; sc.w += pa[r].w;
             sb.x += pb8[r].x; sb.y += pb8[r].y; sb.z += pb8[r].z; sb.w += pb8[r].w;
@@ -1463,18 +1470,26 @@ cudaError_t tc_forward_states(const Problem& p) {
 cudaError_t tc_forward_scan(const Problem& p) {
   ScanMaps maps;
   const uint64_t rows = (uint64_t)p.B * p.T;
+  const bool ht = p.hT != nullptr;
   if (!map_bf16(&maps.x, p.x, rows, (uint64_t)p.H * p.P, 128) ||
       !map_bf16(&maps.B, p.Bm, rows, (uint64_t)p.G * p.N, 128) ||
       !map_bf16(&maps.C, p.Cm, rows, (uint64_t)p.G * p.N, 128) ||
       !map_bf16(&maps.y, p.y, rows, (uint64_t)p.H * p.P, 128))
     return cudaErrorInvalidValue;
+  if (ht && !map_bf16(&maps.ht, p.hT, (uint64_t)p.B * p.nc * p.H * p.N, (uint64_t)p.P, 128))
+    return cudaErrorInvalidValue;
+  if (!ht) maps.ht = maps.x;  // unused
   const size_t smem = kScanBytes + 1024;
-  cudaError_t e = set_smem_tc(k_fwd_scan_tc, smem);
+  cudaError_t e = ht ? set_smem_tc(k_fwd_scan_tc<true>, smem) : set_smem_tc(k_fwd_scan_tc<false>, smem);
   if (e != cudaSuccess) return e;
   {
-    LaunchScope ls("chunk_scan_tc", p.stream);
-    k_fwd_scan_tc<<<dim3(p.nc, p.H, p.B), 256, smem, p.stream>>>(maps, tc_dims(p), p.dt,
-                                                                       p.A, p.D, p.hist);
+    LaunchScope ls(ht ? "chunk_scan_ht_tc" : "chunk_scan_tc", p.stream);
+    if (ht)
+      k_fwd_scan_tc<true><<<dim3(p.nc, p.H, p.B), 256, smem, p.stream>>>(maps, tc_dims(p), p.dt,
+                                                                        p.A, p.D, p.hist);
+    else
+      k_fwd_scan_tc<false><<<dim3(p.nc, p.H, p.B), 256, smem, p.stream>>>(maps, tc_dims(p), p.dt,
+                                                                         p.A, p.D, p.hist);
   }
   return cudaGetLastError();
 }
@@ -1517,6 +1532,15 @@ cudaError_t tc_backward(const Problem& p) {
   const long units = (long)nblk * p.nc * p.G * p.B;
   int nsub = 1;
   while (nsub < 8 && units * nsub < 2L * nsm && p.hpg % (2 * nsub) == 0) nsub *= 2;
+  // tuning override (power of two dividing the heads per group, at most 16)
+  if (const char* env = getenv("SSD_BWD_HEAD_SPLIT")) {
+    const int v = atoi(env);
+    if (v >= 1 && v <= 16 && (v & (v - 1)) == 0 && p.hpg % v == 0) nsub = v;
+  }
+  if (nsub > 8) {
+    e = cudaFuncSetAttribute(k_bwd_tc, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(nblk * p.nc, p.G * nsub, p.B);
   cfg.blockDim = dim3(kBwThreads, 1, 1);

@@ -315,8 +315,9 @@ k_state_scan_tc(const __grid_constant__ ScanStateMaps maps, TcDims d, const floa
   uint8_t* sm = align1024(smraw);
   const int Q = d.Q;
   const uint32_t stage_bytes = 3u * Q * 128;  // V: 2 MN blocks of [Q][128 B]; U: [Q][128 B]
-  __shared__ float s_cs2[256], s_dt[256], s_w[256], scratch[8];
-  __shared__ uint64_t bar_load[2], bar_mma;
+  // decay tables of two chunks in flight
+  __shared__ float s_cs2[2][256], s_dt[2][256], s_w[2][256], s_last[2], scratch[8];
+  __shared__ uint64_t bar_load[2], bar_mma[2];
   __shared__ uint32_t tmem_base;
   const int h = blockIdx.x, b = blockIdx.y;
   const int g = h / d.hpg, tid = threadIdx.x, wg = tid >> 7, q = (tid >> 5) & 3;
@@ -331,11 +332,12 @@ k_state_scan_tc(const __grid_constant__ ScanStateMaps maps, TcDims d, const floa
     prefetch_tmap(&maps.v);
     mbar_init(&bar_load[0], 1);
     mbar_init(&bar_load[1], 1);
-    mbar_init(&bar_mma, 1);
+    mbar_init(&bar_mma[0], 1);
+    mbar_init(&bar_mma[1], 1);
     fence_mbar_init();
   }
   if (tid < 32) {
-    tmem_alloc(&tmem_base, 64);
+    tmem_alloc(&tmem_base, 128);  // two 64-column accumulators
     tmem_relinquish();
   }
   fence_before_sync();
@@ -357,6 +359,36 @@ k_state_scan_tc(const __grid_constant__ ScanStateMaps maps, TcDims d, const floa
     issue(0);
     if (nc > 1) issue(1);
   }
+  // decay tables of chunk `it` into buffer it & 1 (ends synced)
+  auto tables = [&](int it, float dv) {
+    const int k = it & 1;
+    chunk_cumsum_256v(d, dv, a2, s_cs2[k], s_dt[k], scratch);
+    const float last2 = s_cs2[k][Q - 1];
+    if (tid < Q)
+      s_w[k][tid] = MODE == 0 ? exp2f(last2 - s_cs2[k][tid]) * s_dt[k][tid] : exp2f(s_cs2[k][tid]);
+    if (tid == 0) s_last[k] = last2;
+  };
+  // wait for chunk `it`'s tiles, scale its U rows, issue its product into TMEM buffer it & 1
+  auto launch_product = [&](int it) -> bool {
+    const int k = it & 1;
+    if (!wait_or_flag(&bar_load[k], (it >> 1) & 1)) return false;  // also publishes s_w[k]
+    uint8_t* stg = sm + k * stage_bytes;
+    uint8_t* sV = stg;
+    uint8_t* sU = stg + 2 * Q * 128;
+    scale_tile_rows(sU, Q * 8, [&](int r) { return s_w[k][r]; });
+    fence_async_smem();
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    if (tid == 0) {
+      const uint32_t idesc = idesc_bf16(128, 64, true, true);
+      for (int ks = 0; ks < Q / 16; ++ks)
+        mma_bf16(tm + 64 * k, desc_sw128(smem_u32(sV) + ks * 2048, Q * 128, 1024),
+                 desc_sw128(smem_u32(sU) + ks * 2048, Q * 128, 1024), idesc, ks > 0);
+      mma_commit(&bar_mma[k]);
+    }
+    return true;
+  };
 
   // running state (forward) or state gradient (backward): row n, p = 32 wg + i
   float st[32];
@@ -368,7 +400,6 @@ k_state_scan_tc(const __grid_constant__ ScanStateMaps maps, TcDims d, const floa
 #pragma unroll
     for (int i = 0; i < 32; ++i) st[i] = 0.f;
   }
-  float dt_next = load_dt_256(d, dt, b, chunk_of(0), h);
   // backward: this thread's 32 history values of the next chunk, one chunk ahead
   float hv_next[32];
   auto load_hist = [&](int c, float (&dst)[32]) {
@@ -377,22 +408,14 @@ k_state_scan_tc(const __grid_constant__ ScanStateMaps maps, TcDims d, const floa
     for (int i = 0; i < 32; ++i) dst[i] = hsrc[(size_t)(wg * 32 + i) * d.N];
   };
   if (MODE == 1) load_hist(chunk_of(0), hv_next);
-  bool ok = true;
-  uint32_t mma_phase = 0;
+
+  // prologue: chunk 0's product in flight, chunk 1's dt in registers
+  tables(0, load_dt_256(d, dt, b, chunk_of(0), h));
+  float dt_next = nc > 1 ? load_dt_256(d, dt, b, chunk_of(1), h) : 0.f;
+  bool ok = launch_product(0);
 
   for (int it = 0; it < nc && ok; ++it) {
-    const int c = chunk_of(it);
-    const float dv = dt_next;
-    if (it + 1 < nc) dt_next = load_dt_256(d, dt, b, chunk_of(it + 1), h);
-    float hv[32];
-    if (MODE == 1) {
-#pragma unroll
-      for (int i = 0; i < 32; ++i) hv[i] = hv_next[i];
-      if (it + 1 < nc) load_hist(chunk_of(it + 1), hv_next);
-    }
-    chunk_cumsum_256v(d, dv, a2, s_cs2, s_dt, scratch);
-    const float last2 = s_cs2[Q - 1];
-    if (tid < Q) s_w[tid] = MODE == 0 ? exp2f(last2 - s_cs2[tid]) * s_dt[tid] : exp2f(s_cs2[tid]);
+    const int c = chunk_of(it), k = it & 1;
     // the chunk's state entry (history) as it stands before this chunk
     const size_t soff = (((size_t)b * nc + c) * d.H + h) * PN;
     if (MODE == 0) {
@@ -402,64 +425,58 @@ k_state_scan_tc(const __grid_constant__ ScanStateMaps maps, TcDims d, const floa
       if (hT) {  // the same state as bf16 rows n, for the forward chunk scan
         const size_t orow = (((size_t)b * nc + c) * d.H + h) * d.N + n;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
+        for (int kk = 0; kk < 4; ++kk) {
           uint4 oh;
-          oh.x = pack_bf16(st[k * 8 + 0], st[k * 8 + 1]);
-          oh.y = pack_bf16(st[k * 8 + 2], st[k * 8 + 3]);
-          oh.z = pack_bf16(st[k * 8 + 4], st[k * 8 + 5]);
-          oh.w = pack_bf16(st[k * 8 + 6], st[k * 8 + 7]);
-          *(uint4*)(hT + orow * d.P + wg * 32 + k * 8) = oh;
+          oh.x = pack_bf16(st[kk * 8 + 0], st[kk * 8 + 1]);
+          oh.y = pack_bf16(st[kk * 8 + 2], st[kk * 8 + 3]);
+          oh.z = pack_bf16(st[kk * 8 + 4], st[kk * 8 + 5]);
+          oh.w = pack_bf16(st[kk * 8 + 6], st[kk * 8 + 7]);
+          *(uint4*)(hT + orow * d.P + wg * 32 + kk * 8) = oh;
         }
       }
     } else {
       // g_c and H_{c-1} as bf16 rows n (this thread: bytes [64 wg, 64 wg + 64) of row n)
+      float hv[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) hv[i] = hv_next[i];
+      if (it + 1 < nc) load_hist(chunk_of(it + 1), hv_next);
       const size_t orow = (((size_t)b * nc + c) * d.H + h) * d.N + n;
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
+      for (int kk = 0; kk < 4; ++kk) {
         uint4 og, oh;
-        og.x = pack_bf16(st[k * 8 + 0], st[k * 8 + 1]);
-        og.y = pack_bf16(st[k * 8 + 2], st[k * 8 + 3]);
-        og.z = pack_bf16(st[k * 8 + 4], st[k * 8 + 5]);
-        og.w = pack_bf16(st[k * 8 + 6], st[k * 8 + 7]);
-        oh.x = pack_bf16(hv[k * 8 + 0], hv[k * 8 + 1]);
-        oh.y = pack_bf16(hv[k * 8 + 2], hv[k * 8 + 3]);
-        oh.z = pack_bf16(hv[k * 8 + 4], hv[k * 8 + 5]);
-        oh.w = pack_bf16(hv[k * 8 + 6], hv[k * 8 + 7]);
-        *(uint4*)(gT + orow * d.P + wg * 32 + k * 8) = og;
-        *(uint4*)(hT + orow * d.P + wg * 32 + k * 8) = oh;
+        og.x = pack_bf16(st[kk * 8 + 0], st[kk * 8 + 1]);
+        og.y = pack_bf16(st[kk * 8 + 2], st[kk * 8 + 3]);
+        og.z = pack_bf16(st[kk * 8 + 4], st[kk * 8 + 5]);
+        og.w = pack_bf16(st[kk * 8 + 6], st[kk * 8 + 7]);
+        oh.x = pack_bf16(hv[kk * 8 + 0], hv[kk * 8 + 1]);
+        oh.y = pack_bf16(hv[kk * 8 + 2], hv[kk * 8 + 3]);
+        oh.z = pack_bf16(hv[kk * 8 + 4], hv[kk * 8 + 5]);
+        oh.w = pack_bf16(hv[kk * 8 + 6], hv[kk * 8 + 7]);
+        *(uint4*)(gT + orow * d.P + wg * 32 + kk * 8) = og;
+        *(uint4*)(hT + orow * d.P + wg * 32 + kk * 8) = oh;
       }
     }
-    ok = wait_or_flag(&bar_load[it & 1], (it >> 1) & 1);  // also publishes s_w
-    if (!ok) break;
-    uint8_t* stg = sm + (it & 1) * stage_bytes;
-    uint8_t* sV = stg;
-    uint8_t* sU = stg + 2 * Q * 128;
-    scale_tile_rows(sU, Q * 8, [&](int r) { return s_w[r]; });
-    fence_async_smem();
-    fence_before_sync();
-    __syncthreads();
-    fence_after_sync();
-    if (tid == 0) {
-      const uint32_t idesc = idesc_bf16(128, 64, true, true);
-      for (int ks = 0; ks < Q / 16; ++ks)
-        mma_bf16(tm, desc_sw128(smem_u32(sV) + ks * 2048, Q * 128, 1024),
-                 desc_sw128(smem_u32(sU) + ks * 2048, Q * 128, 1024), idesc, ks > 0);
-      mma_commit(&bar_mma);
+    // the next chunk's product goes in while this chunk's result is read out
+    if (it + 1 < nc) {
+      const float dv = dt_next;
+      if (it + 2 < nc) dt_next = load_dt_256(d, dt, b, chunk_of(it + 2), h);
+      tables(it + 1, dv);
+      ok = launch_product(it + 1);
+      if (!ok) break;
     }
-    ok = wait_or_flag(&bar_mma, mma_phase);
-    mma_phase ^= 1;
+    ok = wait_or_flag(&bar_mma[k], (it >> 1) & 1);
     fence_after_sync();
     if (!ok) break;
-    // the stage is free: prefetch chunk it + 2 into it
+    // stage k is free again: prefetch chunk it + 2 into it
     if (tid == 0 && it + 2 < nc) issue(it + 2);
     float v[32];
-    tmem_ld32(tm + lane_base + wg * 32, v);
+    tmem_ld32(tm + 64 * k + lane_base + wg * 32, v);
     tmem_wait_ld();
-    const float e = exp2f(last2);
+    const float e = exp2f(s_last[k]);
 #pragma unroll
     for (int i = 0; i < 32; ++i) st[i] = fmaf(e, st[i], v[i]);
     fence_before_sync();
-    __syncthreads();  // TMEM and s_w reused by the next chunk
+    __syncthreads();  // TMEM buffer k and tables k are reused by chunk it + 2
     fence_after_sync();
   }
   if (ok && final_or_dh0) {
@@ -469,7 +486,7 @@ k_state_scan_tc(const __grid_constant__ ScanStateMaps maps, TcDims d, const floa
   }
   fence_before_sync();
   __syncthreads();
-  if (tid < 32) tmem_dealloc(tm, 64);
+  if (tid < 32) tmem_dealloc(tm, 128);
 }
 
 // ---------------------------------------------------------------------------
@@ -1525,13 +1542,15 @@ cudaError_t tc_backward(const Problem& p) {
   if ((e = set_smem_tc(k_bwd_tc, smem)) != cudaSuccess) return e;
   const int nblk = p.Q / 128;
   // split a group's heads over a cluster of nsub CTAs when there are too few
-  // (block, chunk, group, batch) units to fill the GPU
+  // (block, chunk, group, batch) units to fill the GPU.  With one CTA per SM,
+  // large clusters schedule poorly (a cluster waits for nsub free SMs of one
+  // GPC), so the split stops at the first size giving ~0.8 CTA per SM.
   int nsm = 0, dev = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
   const long units = (long)nblk * p.nc * p.G * p.B;
   int nsub = 1;
-  while (nsub < 8 && units * nsub < 2L * nsm && p.hpg % (2 * nsub) == 0) nsub *= 2;
+  while (nsub < 8 && units * nsub * 5 < 4L * nsm && p.hpg % (2 * nsub) == 0) nsub *= 2;
   // tuning override (power of two dividing the heads per group, at most 16)
   if (const char* env = getenv("SSD_BWD_HEAD_SPLIT")) {
     const int v = atoi(env);

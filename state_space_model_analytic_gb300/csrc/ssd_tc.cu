@@ -58,52 +58,6 @@ struct TcDims {
   int B, T, H, P, N, G, Q, nc, hpg;
 };
 
-// Chunk-local inclusive cumsum of dt*A in log2 units (cs2 = cs * log2 e) and dt,
-// for Q <= 256 values, with 128 threads (Q/128 consecutive values each).
-__device__ __forceinline__ void chunk_cumsum_tc(const TcDims& d, const float* __restrict__ dt,
-                                                const float* __restrict__ A, int b, int c, int h,
-                                                float* s_cs2, float* s_dt, float* scratch) {
-  const int tid = threadIdx.x;
-  const int per = d.Q / kTcThreads;  // 1 or 2
-  float v[2] = {0.f, 0.f}, dv[2] = {0.f, 0.f};
-  const float a = A[h] * kLog2e;
-  float run = 0.f;
-  for (int k = 0; k < per; ++k) {
-    const int t = tid * per + k;
-    dv[k] = dt[((size_t)b * d.T + (size_t)c * d.Q + t) * d.H + h];
-    run += dv[k] * a;
-    v[k] = run;
-  }
-  const float incl = block_inclusive_scan(run, scratch);
-  const float excl = incl - run;
-  for (int k = 0; k < per; ++k) {
-    const int t = tid * per + k;
-    s_cs2[t] = v[k] + excl;
-    s_dt[t] = dv[k];
-  }
-  __syncthreads();
-}
-
-// Scale every 128-byte row r of a SW128 bf16 tile by w[r] (rows x 64 values).
-__device__ __forceinline__ void scale_rows_bf16(const uint8_t* src, uint8_t* dst, int rows,
-                                                const float* w) {
-  for (int e = threadIdx.x; e < rows * 8; e += kTcThreads) {
-    const int r = e >> 3;
-    const uint32_t off = (uint32_t)e * 16u;  // row-uniform scale: swizzle irrelevant
-    const uint4 v = *(const uint4*)(src + off);
-    const float s = w[r];
-    const __nv_bfloat162* p = (const __nv_bfloat162*)&v;
-    uint4 o;
-    uint32_t* q = (uint32_t*)&o;
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const float2 f = __bfloat1622float2(p[k]);
-      q[k] = pack_bf16(f.x * s, f.y * s);
-    }
-    *(uint4*)(dst + off) = o;
-  }
-}
-
 // Column sums over the 32 lanes of a warp: lane l returns sum over lanes of v[l].
 __device__ __forceinline__ float warp_column_sum(float (&v)[32]) {
   const int lane = threadIdx.x & 31;
@@ -290,54 +244,110 @@ k_chunk_outer_tc(const __grid_constant__ OuterMaps maps, TcDims d, const float* 
 }
 
 // ---------------------------------------------------------------------------
-// Fused chunk-state + state pass, one CTA per (b, h), walking the chunks with a
-// two-stage TMA pipeline; the running state lives in registers (thread
-// (wg, n) holds row n, p in [32 wg, 32 wg + 32) of the transposed state).
+// Fused chunk-state + state pass, one CTA per (b, h), warp-specialised.
+// Warp 8 (issuer) streams the chunks' tiles in by TMA (two stages) and issues
+// the product D[n][p] = V^T (w o U) of each chunk on tcgen05 into one of
+// kScanBufs TMEM buffers of 64 columns.  Warps 4-7 (scalers) build each
+// chunk's decay tables and scale the rows of U by w in shared memory (MODE 1:
+// they also convert the fp32 history into bf16 rows).  Warps 0-3 (consumer)
+// hold the
+// running state, thread n owning row n (64 p values): per chunk they wait for
+// the product, read it out of TMEM, free the buffer and advance the
+// recurrence, so the products of later chunks overlap the recurrence and the
+// state writes of earlier ones.  The bf16 rows go out through a 128-byte
+// swizzled shared-memory tile and a TMA store (one coalesced 16 KB block per
+// (b, chunk, h)).
 // MODE 0 (forward, chunks in order):
 //   S_c^T = B_c^T (w o X_c), w_j = exp(cs_last - cs_j) dt_j;
-//   hist[c] = H_{c-1};  H_c = exp(cs_last) H_{c-1} + S_c;  final = H_{nc-1}.
+//   hist[c] = H_{c-1} (fp32) and its bf16 copy as rows n (hT);
+//   H_c = exp(cs_last) H_{c-1} + S_c;  final = H_{nc-1}.
 // MODE 1 (backward, chunks in reverse):
 //   R_c^T = C_c^T (e o dY_c), e_i = exp(cs_i);
-//   gT[c] = g_c (bf16 rows n), hT[c] = H_{c-1} from hist (bf16 rows n);
+//   gT[c] = g_c and hT[c] = H_{c-1} from hist, both bf16 rows n;
 //   g_{c-1} = exp(cs_last) g_c + R_c;  dh0 = g_{-1}.
 struct ScanStateMaps {
-  CUtensorMap u;  // x or dy: [B*T][H*P] bf16, box {64, Q}
-  CUtensorMap v;  // B or C:  [B*T][G*N] bf16, box {64, Q}
+  CUtensorMap u;     // x or dy: [B*T][H*P] bf16, box {64, Q}
+  CUtensorMap v;     // B or C:  [B*T][G*N] bf16, box {64, Q}
+  CUtensorMap rows;  // hT (MODE 0) or gT (MODE 1): [B*nc*H*N][P] bf16, box {64, 128} (store)
+  CUtensorMap rows2; // hT (MODE 1), same layout (store)
 };
 
+constexpr int kScanBufs = 4;  // TMEM product buffers (64 columns each)
+
+__device__ __forceinline__ void named_sync(uint32_t id, uint32_t nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+// Barrier over `nthreads` threads that also returns the OR of `pred` over them.
+__device__ __forceinline__ bool named_sync_or(uint32_t id, uint32_t nthreads, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "barrier.red.or.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0;
+}
+
+// Bounded wait that also gives up as soon as another warp of the CTA has
+// recorded a timeout in *abort (then the caller stops touching guarded data).
+__device__ __forceinline__ bool wait_ws(uint64_t* bar, uint32_t parity, volatile int* abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (*abort) return false;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      *abort = 1;
+      atomicOr(&g_tc_error, 1u);
+      return false;
+    }
+  }
+}
+
+constexpr int kScanThreads = 288;  // consumer warps 0-3, scaler warps 4-7, issuer warp 8
+
 template <int MODE>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(kScanThreads, 1)
 k_state_scan_tc(const __grid_constant__ ScanStateMaps maps, TcDims d, const float* __restrict__ dt,
                 const float* __restrict__ A, const float* __restrict__ h0,
-                float* __restrict__ hist, float* __restrict__ final_or_dh0,
-                __nv_bfloat16* __restrict__ gT, __nv_bfloat16* __restrict__ hT) {
+                float* __restrict__ hist, float* __restrict__ final_or_dh0) {
   extern __shared__ __align__(1024) uint8_t smraw[];
   uint8_t* sm = align1024(smraw);
   const int Q = d.Q;
   const uint32_t stage_bytes = 3u * Q * 128;  // V: 2 MN blocks of [Q][128 B]; U: [Q][128 B]
-  // decay tables of two chunks in flight
-  __shared__ float s_cs2[2][256], s_dt[2][256], s_w[2][256], s_last[2], scratch[8];
-  __shared__ uint64_t bar_load[2], bar_mma[2];
+  __shared__ float s_wsum[2][4], s_lastq[4], s_last[kScanBufs];
+  __shared__ uint64_t bar_load[2], bar_sfree[2], bar_scaled[2], bar_full[kScanBufs],
+      bar_free[kScanBufs];
   __shared__ uint32_t tmem_base;
+  __shared__ volatile int s_abort;
   const int h = blockIdx.x, b = blockIdx.y;
-  const int g = h / d.hpg, tid = threadIdx.x, wg = tid >> 7, q = (tid >> 5) & 3;
-  const int n = tid & 127;
-  const uint32_t lane_base = (uint32_t)(q * 32) << 16;
-  const float a2 = A[h] * kLog2e;
+  const int g = h / d.hpg, tid = threadIdx.x;
   const int nc = d.nc;
   const size_t PN = (size_t)d.P * d.N;
+  auto chunk_of = [&](int it) { return MODE == 0 ? it : nc - 1 - it; };
 
   if (tid == 0) {
     prefetch_tmap(&maps.u);
     prefetch_tmap(&maps.v);
-    mbar_init(&bar_load[0], 1);
-    mbar_init(&bar_load[1], 1);
-    mbar_init(&bar_mma[0], 1);
-    mbar_init(&bar_mma[1], 1);
+    for (int k = 0; k < 2; ++k) {
+      mbar_init(&bar_load[k], 1);
+      mbar_init(&bar_sfree[k], 1);
+      mbar_init(&bar_scaled[k], 4);  // one arrive per scaler warp
+    }
+    for (int k = 0; k < kScanBufs; ++k) {
+      mbar_init(&bar_full[k], 2);   // the product's commit + the issuer's table arrive
+      mbar_init(&bar_free[k], 4);   // one arrive per consumer warp
+    }
+    s_abort = 0;
     fence_mbar_init();
   }
   if (tid < 32) {
-    tmem_alloc(&tmem_base, 128);  // two 64-column accumulators
+    tmem_alloc(&tmem_base, 64 * kScanBufs);
     tmem_relinquish();
   }
   fence_before_sync();
@@ -345,148 +355,229 @@ k_state_scan_tc(const __grid_constant__ ScanStateMaps maps, TcDims d, const floa
   fence_after_sync();
   const uint32_t tm = tmem_base;
 
-  auto chunk_of = [&](int it) { return MODE == 0 ? it : nc - 1 - it; };
-  auto issue = [&](int it) {
-    const int c = chunk_of(it);
-    uint8_t* st = sm + (it & 1) * stage_bytes;
-    const int row0 = b * d.T + c * Q;
-    mbar_expect_tx(&bar_load[it & 1], stage_bytes);
-    tma_load_2d(st, &maps.v, g * d.N, row0, &bar_load[it & 1]);
-    tma_load_2d(st + Q * 128, &maps.v, g * d.N + 64, row0, &bar_load[it & 1]);
-    tma_load_2d(st + 2 * Q * 128, &maps.u, h * d.P, row0, &bar_load[it & 1]);
-  };
-  if (tid == 0) {
-    issue(0);
-    if (nc > 1) issue(1);
-  }
-  // decay tables of chunk `it` into buffer it & 1 (ends synced)
-  auto tables = [&](int it, float dv) {
-    const int k = it & 1;
-    chunk_cumsum_256v(d, dv, a2, s_cs2[k], s_dt[k], scratch);
-    const float last2 = s_cs2[k][Q - 1];
-    if (tid < Q)
-      s_w[k][tid] = MODE == 0 ? exp2f(last2 - s_cs2[k][tid]) * s_dt[k][tid] : exp2f(s_cs2[k][tid]);
-    if (tid == 0) s_last[k] = last2;
-  };
-  // wait for chunk `it`'s tiles, scale its U rows, issue its product into TMEM buffer it & 1
-  auto launch_product = [&](int it) -> bool {
-    const int k = it & 1;
-    if (!wait_or_flag(&bar_load[k], (it >> 1) & 1)) return false;  // also publishes s_w[k]
-    uint8_t* stg = sm + k * stage_bytes;
-    uint8_t* sV = stg;
-    uint8_t* sU = stg + 2 * Q * 128;
-    scale_tile_rows(sU, Q * 8, [&](int r) { return s_w[k][r]; });
-    fence_async_smem();
-    fence_before_sync();
-    __syncthreads();
-    fence_after_sync();
-    if (tid == 0) {
+  if (tid >= 256) {
+    // ===================== issuer (warp 8) =====================
+    if (tid == 256) {
+      auto issue = [&](int it) {
+        const int c = chunk_of(it), k = it & 1;
+        uint8_t* st = sm + k * stage_bytes;
+        const int row0 = b * d.T + c * Q;
+        mbar_expect_tx(&bar_load[k], stage_bytes);
+        tma_load_2d(st, &maps.v, g * d.N, row0, &bar_load[k]);
+        tma_load_2d(st + Q * 128, &maps.v, g * d.N + 64, row0, &bar_load[k]);
+        tma_load_2d(st + 2 * Q * 128, &maps.u, h * d.P, row0, &bar_load[k]);
+      };
+      issue(0);
+      if (nc > 1) issue(1);
+      int loads_issued = nc > 1 ? 2 : 1, mma_issued = 0;
       const uint32_t idesc = idesc_bf16(128, 64, true, true);
-      for (int ks = 0; ks < Q / 16; ++ks)
-        mma_bf16(tm + 64 * k, desc_sw128(smem_u32(sV) + ks * 2048, Q * 128, 1024),
-                 desc_sw128(smem_u32(sU) + ks * 2048, Q * 128, 1024), idesc, ks > 0);
-      mma_commit(&bar_mma[k]);
-    }
-    return true;
-  };
-
-  // running state (forward) or state gradient (backward): row n, p = 32 wg + i
-  float st[32];
-  if (MODE == 0 && h0) {
-    const float* src = h0 + ((size_t)b * d.H + h) * PN + n;
-#pragma unroll
-    for (int i = 0; i < 32; ++i) st[i] = src[(size_t)(wg * 32 + i) * d.N];
-  } else {
-#pragma unroll
-    for (int i = 0; i < 32; ++i) st[i] = 0.f;
-  }
-  // backward: this thread's 32 history values of the next chunk, one chunk ahead
-  float hv_next[32];
-  auto load_hist = [&](int c, float (&dst)[32]) {
-    const float* hsrc = hist + (((size_t)b * nc + c) * d.H + h) * PN + n;
-#pragma unroll
-    for (int i = 0; i < 32; ++i) dst[i] = hsrc[(size_t)(wg * 32 + i) * d.N];
-  };
-  if (MODE == 1) load_hist(chunk_of(0), hv_next);
-
-  // prologue: chunk 0's product in flight, chunk 1's dt in registers
-  tables(0, load_dt_256(d, dt, b, chunk_of(0), h));
-  float dt_next = nc > 1 ? load_dt_256(d, dt, b, chunk_of(1), h) : 0.f;
-  bool ok = launch_product(0);
-
-  for (int it = 0; it < nc && ok; ++it) {
-    const int c = chunk_of(it), k = it & 1;
-    // the chunk's state entry (history) as it stands before this chunk
-    const size_t soff = (((size_t)b * nc + c) * d.H + h) * PN;
-    if (MODE == 0) {
-      float* dst = hist + soff + n;
-#pragma unroll
-      for (int i = 0; i < 32; ++i) dst[(size_t)(wg * 32 + i) * d.N] = st[i];
-      if (hT) {  // the same state as bf16 rows n, for the forward chunk scan
-        const size_t orow = (((size_t)b * nc + c) * d.H + h) * d.N + n;
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          uint4 oh;
-          oh.x = pack_bf16(st[kk * 8 + 0], st[kk * 8 + 1]);
-          oh.y = pack_bf16(st[kk * 8 + 2], st[kk * 8 + 3]);
-          oh.z = pack_bf16(st[kk * 8 + 4], st[kk * 8 + 5]);
-          oh.w = pack_bf16(st[kk * 8 + 6], st[kk * 8 + 7]);
-          *(uint4*)(hT + orow * d.P + wg * 32 + kk * 8) = oh;
+      for (int it = 0; it < nc; ++it) {
+        const int k = it & 1, buf = it % kScanBufs;
+        // chunk it scaled; its decay total; the buffer's previous product read out
+        if (!wait_ws(&bar_scaled[k], (it >> 1) & 1, &s_abort)) break;
+        const float last2 = s_lastq[it & 3];
+        if (it >= kScanBufs && !wait_ws(&bar_free[buf], ((it / kScanBufs) - 1) & 1, &s_abort)) break;
+        s_last[buf] = last2;
+        mbar_arrive(&bar_full[buf]);
+        fence_after_sync();
+        uint8_t* sV = sm + k * stage_bytes;
+        uint8_t* sU = sV + 2 * Q * 128;
+        for (int ks = 0; ks < Q / 16; ++ks)
+          mma_bf16(tm + 64 * buf, desc_sw128(smem_u32(sV) + ks * 2048, Q * 128, 1024),
+                   desc_sw128(smem_u32(sU) + ks * 2048, Q * 128, 1024), idesc, ks > 0);
+        mma_commit(&bar_full[buf]);
+        mma_commit(&bar_sfree[k]);
+        ++mma_issued;
+        // stage k takes chunk it + 2 once this product has read it
+        if (it + 2 < nc) {
+          if (!wait_ws(&bar_sfree[k], (it >> 1) & 1, &s_abort)) break;
+          issue(it + 2);
+          ++loads_issued;
         }
       }
-    } else {
-      // g_c and H_{c-1} as bf16 rows n (this thread: bytes [64 wg, 64 wg + 64) of row n)
-      float hv[32];
+      // drain: no TMA write or product may still be in flight when the CTA ends
+      // (bounded waits; in the normal case all have completed already)
+      for (int i = mma_issued; i < loads_issued; ++i)
+        (void)mbar_wait(&bar_load[i & 1], (i >> 1) & 1, kWaitLimitNs);
+      if (mma_issued > 0)
+        (void)mbar_wait(&bar_sfree[(mma_issued - 1) & 1], ((mma_issued - 1) >> 1) & 1, kWaitLimitNs);
+    }
+    __syncwarp();
+  } else if (tid >= 128) {
+    // ===================== scalers (warps 4-7) =====================
+    const int pt = tid - 128, lane = tid & 31, pw = pt >> 5;
+    const float a2 = A[h] * kLog2e;
+    const int per = Q / 128;  // dt values per thread: 1 or 2, consecutive
+    auto load_dt = [&](int it, float (&v)[2]) {
+      const size_t t0 = (size_t)b * d.T + (size_t)chunk_of(it) * Q + (size_t)pt * per;
+      v[0] = dt[t0 * d.H + h];
+      v[1] = per == 2 ? dt[(t0 + 1) * d.H + h] : 0.f;
+    };
+    float dv[2], dv_next[2] = {0.f, 0.f};
+    load_dt(0, dv);
+    if (nc > 1) load_dt(1, dv_next);
+    uint8_t* sRows2 = sm + 2 * stage_bytes + 16384;  // MODE 1: [128 rows n][64 p] bf16, SW128
+    if (MODE == 1 && pt == 0) prefetch_tmap(&maps.rows2);
+    for (int it = 0; it < nc; ++it) {
+      const int k = it & 1;
+      // MODE 1: H_{c-1} from the fp32 history, 16-byte loads: this thread takes
+      // p in [16 pw, 16 pw + 16) of rows n = 4 lane .. 4 lane + 3; stored as
+      // bf16 rows after the scaling
+      float4 hv[16];
+      if (MODE == 1) {
+        const float* hsrc = hist + (((size_t)b * nc + chunk_of(it)) * d.H + h) * PN +
+                            (size_t)(16 * pw) * d.N + 4 * lane;
 #pragma unroll
-      for (int i = 0; i < 32; ++i) hv[i] = hv_next[i];
-      if (it + 1 < nc) load_hist(chunk_of(it + 1), hv_next);
-      const size_t orow = (((size_t)b * nc + c) * d.H + h) * d.N + n;
+        for (int pp = 0; pp < 16; ++pp) hv[pp] = *(const float4*)(hsrc + (size_t)pp * d.N);
+      }
+      // ---- decay tables: chunk-local inclusive cumsum of dt * A (log2 units)
+      const float x0 = dv[0] * a2, x1 = dv[1] * a2;
+      float run = x0 + x1;
 #pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        uint4 og, oh;
-        og.x = pack_bf16(st[kk * 8 + 0], st[kk * 8 + 1]);
-        og.y = pack_bf16(st[kk * 8 + 2], st[kk * 8 + 3]);
-        og.z = pack_bf16(st[kk * 8 + 4], st[kk * 8 + 5]);
-        og.w = pack_bf16(st[kk * 8 + 6], st[kk * 8 + 7]);
-        oh.x = pack_bf16(hv[kk * 8 + 0], hv[kk * 8 + 1]);
-        oh.y = pack_bf16(hv[kk * 8 + 2], hv[kk * 8 + 3]);
-        oh.z = pack_bf16(hv[kk * 8 + 4], hv[kk * 8 + 5]);
-        oh.w = pack_bf16(hv[kk * 8 + 6], hv[kk * 8 + 7]);
-        *(uint4*)(gT + orow * d.P + wg * 32 + kk * 8) = og;
-        *(uint4*)(hT + orow * d.P + wg * 32 + kk * 8) = oh;
+      for (int o = 1; o < 32; o <<= 1) {
+        const float t = __shfl_up_sync(0xffffffffu, run, o);
+        if (lane >= o) run += t;
+      }
+      if (lane == 31) s_wsum[k][pw] = run;
+      named_sync(1, 128);
+      float base = 0.f, last2 = 0.f;
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        const float ws = s_wsum[k][w];
+        if (w < pw) base += ws;
+        last2 += ws;
+      }
+      const float cs0 = base + run - x1;  // cs of this thread's first value
+      const float cs1 = base + run;       // and of its second
+      // weights of this thread's rows pt * per + {0, 1}
+      const float w0 = MODE == 0 ? exp2f(last2 - cs0) * dv[0] : exp2f(cs0);
+      const float w1 = MODE == 0 ? exp2f(last2 - cs1) * dv[1] : exp2f(cs1);
+      if (pt == 0) s_lastq[it & 3] = last2;
+      dv[0] = dv_next[0];
+      dv[1] = dv_next[1];
+      if (it + 2 < nc) load_dt(it + 2, dv_next);
+      // ---- this chunk's tiles; U rows times w (bf16 pairs).  The barrier
+      // makes the decision to stop uniform over the scalers.
+      const bool got = wait_ws(&bar_load[k], (it >> 1) & 1, &s_abort);
+      if (named_sync_or(1, 128, !got || s_abort)) break;
+      uint8_t* sU = sm + k * stage_bytes + 2 * Q * 128;
+      for (int rr = 0; rr < per; ++rr) {
+        // a whole 128-byte row has one factor, so the swizzle does not matter;
+        // the lane-rotated chunk order keeps the accesses bank-conflict free
+        uint8_t* row = sU + (pt * per + rr) * 128;
+        const __nv_bfloat162 w2 = __float2bfloat162_rn(rr ? w1 : w0);
+        uint4 v[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[j] = *(const uint4*)(row + 16 * ((j + lane) & 7));
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          __nv_bfloat162* hv2 = (__nv_bfloat162*)&v[j];
+#pragma unroll
+          for (int t = 0; t < 4; ++t) hv2[t] = __hmul2(hv2[t], w2);
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) *(uint4*)(row + 16 * ((j + lane) & 7)) = v[j];
+      }
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar_scaled[k]);  // s_lastq too (release)
+      if (MODE == 1) {  // hT[c] = H_{c-1} as bf16 row n = pt, through the staging tile
+        if (pt == 0) bulk_wait_read0();
+        named_sync(1, 128);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {  // row n = 4 lane + i: chunks 2 pw, 2 pw + 1
+          float v8[8];
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+              const float4 f = hv[8 * half + t];
+              v8[t] = i == 0 ? f.x : i == 1 ? f.y : i == 2 ? f.z : f.w;
+            }
+            store_row_bf16(sRows2, 4 * lane + i, 2 * pw + half, v8);
+          }
+        }
+        fence_async_smem();
+        named_sync(1, 128);
+        if (pt == 0) {
+          tma_store_2d(&maps.rows2, sRows2, 0, ((b * nc + chunk_of(it)) * d.H + h) * d.N);
+          bulk_commit();
+        }
       }
     }
-    // the next chunk's product goes in while this chunk's result is read out
-    if (it + 1 < nc) {
-      const float dv = dt_next;
-      if (it + 2 < nc) dt_next = load_dt_256(d, dt, b, chunk_of(it + 2), h);
-      tables(it + 1, dv);
-      ok = launch_product(it + 1);
-      if (!ok) break;
+    if (pt == 0) bulk_wait0();
+  } else {
+    // ===================== consumer (warps 0-3) =====================
+    const int n = tid, q = tid >> 5;
+    const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+    uint8_t* sRows = sm + 2 * stage_bytes;  // [128 rows n][64 p] bf16, SW128
+    if (tid == 0) prefetch_tmap(&maps.rows);
+    // 64 values of row n as bf16 into the staging tile, then one TMA store of
+    // the tile to rows [srow, srow + 128) (the tile is free again once the
+    // previous store has read it)
+    auto put_rows = [&](const float (&v)[64], const CUtensorMap* map, int srow) {
+      if (tid == 0) bulk_wait_read0();
+      named_sync(2, 128);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) store_row_bf16(sRows, n, j, &v[8 * j]);
+      fence_async_smem();
+      named_sync(2, 128);
+      if (tid == 0) {
+        tma_store_2d(map, sRows, 0, srow);
+        bulk_commit();
+      }
+    };
+    float st[64];
+    if (MODE == 0 && h0) {
+      const float* src = h0 + ((size_t)b * d.H + h) * PN + n;
+#pragma unroll
+      for (int p = 0; p < 64; ++p) st[p] = src[(size_t)p * d.N];
+    } else {
+#pragma unroll
+      for (int p = 0; p < 64; ++p) st[p] = 0.f;
     }
-    ok = wait_or_flag(&bar_mma[k], (it >> 1) & 1);
-    fence_after_sync();
-    if (!ok) break;
-    // stage k is free again: prefetch chunk it + 2 into it
-    if (tid == 0 && it + 2 < nc) issue(it + 2);
-    float v[32];
-    tmem_ld32(tm + 64 * k + lane_base + wg * 32, v);
-    tmem_wait_ld();
-    const float e = exp2f(s_last[k]);
+    bool ok = true;
+    for (int it = 0; it < nc; ++it) {
+      const int c = chunk_of(it), buf = it % kScanBufs;
+      const int srow = ((b * nc + c) * d.H + h) * d.N;
+      if (MODE == 0) {  // hist[c] = H_{c-1}: fp32 [P][N] (coalesced over n) and bf16 rows n
+        float* hblk = hist + (((size_t)b * nc + c) * d.H + h) * PN + n;
 #pragma unroll
-    for (int i = 0; i < 32; ++i) st[i] = fmaf(e, st[i], v[i]);
-    fence_before_sync();
-    __syncthreads();  // TMEM buffer k and tables k are reused by chunk it + 2
-    fence_after_sync();
-  }
-  if (ok && final_or_dh0) {
-    float* dst = final_or_dh0 + ((size_t)b * d.H + h) * PN + n;
+        for (int p = 0; p < 64; ++p) hblk[(size_t)p * d.N] = st[p];
+      }
+      put_rows(st, &maps.rows, srow);  // MODE 0: hT[c] = H_{c-1}; MODE 1: gT[c] = g_c
+      ok = __all_sync(0xffffffffu, wait_ws(&bar_full[buf], (it / kScanBufs) & 1, &s_abort));
+      // warp-uniform; the other consumer warps still reach the named barriers
+      if (ok) {
+        fence_after_sync();
+        const float e = exp2f(s_last[buf]);
 #pragma unroll
-    for (int i = 0; i < 32; ++i) dst[(size_t)(wg * 32 + i) * d.N] = st[i];
+        for (int half = 0; half < 2; ++half) {
+          float v[32];
+          tmem_ld32(tm + 64 * buf + 32 * half + lane_base, v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) st[32 * half + i] = fmaf(e, st[32 * half + i], v[i]);
+        }
+        fence_before_sync();
+        __syncwarp();
+        if ((tid & 31) == 0) mbar_arrive(&bar_free[buf]);
+      }
+      if (named_sync_or(2, 128, !ok)) {
+        ok = false;
+        break;
+      }
+    }
+    if (ok && final_or_dh0) {
+      float* dst = final_or_dh0 + ((size_t)b * d.H + h) * PN + n;
+#pragma unroll
+      for (int p = 0; p < 64; ++p) dst[(size_t)p * d.N] = st[p];
+    }
+    if (tid == 0) bulk_wait0();
   }
   fence_before_sync();
   __syncthreads();
-  if (tid < 32) tmem_dealloc(tm, 128);
+  if (tid < 32) tmem_dealloc(tm, 64 * kScanBufs);
 }
 
 // ---------------------------------------------------------------------------
@@ -1160,6 +1251,16 @@ k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, int nsub, const float* 
       tma_store_2d(&maps.dx, sW, h * d.P, row0);
       bulk_commit();
     }
+    // phase D done: X, dY, Hin, gout are free and the next head's tiles go out
+    // now, under this head's dcs work (the B_0 / C_1 tile of chunks of two
+    // blocks lands in sW once the dx store has read it)
+    ok = wait_or_flag(&bar_mma, mma_phase);
+    mma_phase ^= 1;
+    fence_after_sync();
+    if (tid == 0 && ok && hh + 1 < kh) {
+      if (two) bulk_wait_read0();
+      issue_head_loads(h + 1);
+    }
     if (wg == 0) {
       rowsum += s_red[0][row];
       drive += s_red[1][row];
@@ -1193,14 +1294,9 @@ k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, int nsub, const float* 
       dA_part[slot] = ad.x;
       dD_part[slot] = ad.y;
     }
-    // ---- end of head: phase D done, dx staging read, before the tiles are reloaded
-    ok = wait_or_flag(&bar_mma, mma_phase);
-    mma_phase ^= 1;
-    fence_after_sync();
-    if (tid == 0) {
-      bulk_wait_read0();
-      if (ok && hh + 1 < kh) issue_head_loads(h + 1);
-    }
+    // ---- end of head: the tables are rebuilt by the next head, and the dx
+    // staging (sW) by the next head's W or the final dC, dB sums
+    if (tid == 0) bulk_wait_read0();
     __syncthreads();
   }
 
@@ -1465,17 +1561,20 @@ cudaError_t tc_state_scan(const Problem& p, const char* name, float* final_or_dh
   ScanStateMaps maps;
   const void* u = MODE == 0 ? p.x : p.dy;
   const void* v = MODE == 0 ? p.Bm : p.Cm;
+  const uint64_t srows = (uint64_t)p.B * p.nc * p.H * p.N;
   if (!map_bf16(&maps.u, u, (uint64_t)p.B * p.T, (uint64_t)p.H * p.P, p.Q) ||
-      !map_bf16(&maps.v, v, (uint64_t)p.B * p.T, (uint64_t)p.G * p.N, p.Q))
+      !map_bf16(&maps.v, v, (uint64_t)p.B * p.T, (uint64_t)p.G * p.N, p.Q) ||
+      !map_bf16(&maps.rows, MODE == 0 ? p.hT : p.gT, srows, (uint64_t)p.P, 128) ||
+      !map_bf16(&maps.rows2, p.hT, srows, (uint64_t)p.P, 128))
     return cudaErrorInvalidValue;
-  const size_t smem = 2 * 3 * (size_t)p.Q * 128 + 1024;
+  // two pipeline stages of tiles + the bf16 row staging tile(s)
+  const size_t smem = 2 * 3 * (size_t)p.Q * 128 + (MODE == 1 ? 2 : 1) * 16384 + 1024;
   cudaError_t e = set_smem_tc(k_state_scan_tc<MODE>, smem);
   if (e != cudaSuccess) return e;
   {
     LaunchScope ls(name, p.stream);
-    k_state_scan_tc<MODE><<<dim3(p.H, p.B), 256, smem, p.stream>>>(
-        maps, tc_dims(p), p.dt, p.A, p.h0, p.hist, final_or_dh0, (__nv_bfloat16*)p.gT,
-        (__nv_bfloat16*)p.hT);
+    k_state_scan_tc<MODE><<<dim3(p.H, p.B), kScanThreads, smem, p.stream>>>(
+        maps, tc_dims(p), p.dt, p.A, p.h0, p.hist, final_or_dh0);
   }
   return cudaGetLastError();
 }

@@ -58,11 +58,12 @@ struct TcDims {
   int B, T, H, P, N, G, Q, nc, hpg;
 };
 
-// Column sums over the 32 lanes of a warp: lane l returns sum over lanes of v[l].
-__device__ __forceinline__ float warp_column_sum(float (&v)[32]) {
+// Column sums over the 32 lanes of a warp, for 16 columns: lane l returns the
+// sum over all lanes of v[l % 16].
+__device__ __forceinline__ float warp_column_sum16(float (&v)[16]) {
   const int lane = threadIdx.x & 31;
 #pragma unroll
-  for (int s = 16; s >= 1; s >>= 1) {
+  for (int s = 8; s >= 1; s >>= 1) {
     const bool upper = (lane & s) != 0;
 #pragma unroll
     for (int k = 0; k < s; ++k) {
@@ -71,7 +72,7 @@ __device__ __forceinline__ float warp_column_sum(float (&v)[32]) {
       v[k] = keep + __shfl_xor_sync(0xffffffffu, send, s);
     }
   }
-  return v[0];
+  return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 16);
 }
 
 __device__ __forceinline__ void store_row_bf16(uint8_t* tile, int row, int chunk0,
@@ -872,7 +873,7 @@ struct BwdMaps {
   CUtensorMap gt;  // chunk-end state gradients, same layout
 };
 
-constexpr int kBwThreads = 256;       // two warpgroups share each TMEM row
+constexpr int kBwThreads = 512;       // four warpgroups share each TMEM lane quarter
 constexpr uint32_t kBwC = 0;          // C_k: 2 K-major tiles [128][128 B]
 constexpr uint32_t kBwB = 32768;      // B_k
 constexpr uint32_t kBwO = 65536;      // L o CB (2 tiles, same layout as W)
@@ -900,13 +901,13 @@ k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, int nsub, const float* 
   uint8_t* sH = sm + kBwH;
   uint8_t* sG = sm + kBwG;
   uint8_t* sW = sm + kBwW;
-  __shared__ float s_cs2[256], s_dt[256], scratch[8];
+  __shared__ float s_cs2[256], s_dt[256], scratch[16];
   __shared__ __align__(16) float s_E[4][128];    // exp(cs_r - cs_J), J < r = base + 32 q
   __shared__ __align__(16) float s_Edt[4][128];  // the same times dt_J
   __shared__ float s_col[4][128];                // per-warp strict column sums of M
-  __shared__ float s_red[5][128];                // second warpgroup's row partials
+  __shared__ float s_rs[3][128];                 // row-sum partials of warpgroups 1-3
   __shared__ float s_v[128];
-  __shared__ float2 s_v2[128], scratch2[8];
+  __shared__ float2 s_v2[128], scratch2[16];
   __shared__ float s_esum;
   __shared__ uint64_t bar_shared, bar_head, bar_mma;
   __shared__ uint32_t tmem_base;
@@ -916,7 +917,7 @@ k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, int nsub, const float* 
   const int g = blockIdx.y / nsub, sub = blockIdx.y % nsub, b = blockIdx.z;
   const int kh = d.hpg / nsub;
   const int tid = threadIdx.x, wg = tid >> 7, q = (tid >> 5) & 3, lane = tid & 31;
-  const int row = tid & 127;  // TMEM lane / tile row owned (with the other warpgroup)
+  const int row = tid & 127;  // TMEM lane / tile row owned (with the other warpgroups)
   const int base = 128 * k;
   const int crow = b * d.T + c * d.Q;  // first row of the chunk
   const int row0 = crow + base;
@@ -1023,28 +1024,28 @@ k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, int nsub, const float* 
       mma_phase ^= 1;
       fence_after_sync();
       if (!ok) break;
-      // row n, p in [32 wg, 32 wg + 32): H_mid = e^{cs_127} H + S_0 or g_mid = e^{..} g + R_1
-      float v[32];
-      tmem_ld32(T1 + lane_base + wg * 32, v);
+      // row n, p in [16 wg, 16 wg + 16): H_mid = e^{cs_127} H + S_0 or g_mid = e^{..} g + R_1
+      float v[16];
+      tmem_ld16(T1 + lane_base + wg * 16, v);
       tmem_wait_ld();
       uint8_t* tile = (k == 1) ? sH : sG;
       const float sc = (k == 1) ? exp2f(s_cs2[127]) : exp2f(s_cs2[d.Q - 1] - s_cs2[127]);
 #pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
+      for (int q4 = 0; q4 < 2; ++q4) {
         float f[8];
-        unpack8(*(const uint4*)(tile + sw128(row, wg * 4 + q4)), f);
+        unpack8(*(const uint4*)(tile + sw128(row, wg * 2 + q4)), f);
 #pragma unroll
         for (int t = 0; t < 8; ++t) f[t] = fmaf(sc, f[t], v[q4 * 8 + t]);
-        store_row_bf16(tile, row, wg * 4 + q4, f);
+        store_row_bf16(tile, row, wg * 2 + q4, f);
       }
     }
-    // <gout, Hin> over this thread's half row (bf16 operands, fp32 sum)
+    // <gout, Hin> over this thread's quarter row (bf16 operands, fp32 sum)
     float hg = 0.f;
 #pragma unroll
-    for (int q4 = 0; q4 < 4; ++q4) {
+    for (int q4 = 0; q4 < 2; ++q4) {
       float fh[8], fg[8];
-      unpack8(*(const uint4*)(sH + sw128(row, wg * 4 + q4)), fh);
-      unpack8(*(const uint4*)(sG + sw128(row, wg * 4 + q4)), fg);
+      unpack8(*(const uint4*)(sH + sw128(row, wg * 2 + q4)), fh);
+      unpack8(*(const uint4*)(sG + sw128(row, wg * 2 + q4)), fg);
 #pragma unroll
       for (int t = 0; t < 8; ++t) hg = fmaf(fh[t], fg[t], hg);
     }
@@ -1072,66 +1073,72 @@ k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, int nsub, const float* 
     fence_after_sync();
     if (!ok) break;
 
-    // ---- W = L o dt_j o dYX -> sW, L o CB -> registers, row / column sums of M.
-    // Warpgroup wg covers columns [64 wg, 64 wg + 64) of row `row` (chunks 2wg, 2wg+1).
+    // ---- W = L o dt_j o dYX -> sW, L o CB -> sO, row / column sums of M.
+    // Warpgroup wg covers the 32 columns [32 wg, 32 wg + 32) of row `row`, in
+    // two halves of 16.
     const int I = base + row;
     const float fi = exp2f(s_cs2[I] - s_cs2[base + 32 * q]);
     const float csI = s_cs2[I];
     float rowsum = 0.f;
-#pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      const int jc = 2 * wg + u;
-      float cb[32], xy[32], wv[32];
+    {
+      const int jc = wg;
       if (jc <= q) {  // warp-uniform
-        tmem_ld32(T0 + lane_base + jc * 32, cb);
-        tmem_ld32(T1 + lane_base + jc * 32, xy);
-        tmem_wait_ld();
-        if (jc < q) {
 #pragma unroll
-          for (int t4 = 0; t4 < 8; ++t4) {
-            const float4 e4 = *(const float4*)&s_E[q][jc * 32 + t4 * 4];
-            const float4 d4 = *(const float4*)&s_Edt[q][jc * 32 + t4 * 4];
-            const float ee[4] = {e4.x, e4.y, e4.z, e4.w};
-            const float dd4[4] = {d4.x, d4.y, d4.z, d4.w};
+        for (int hf = 0; hf < 2; ++hf) {
+          const int col0 = jc * 32 + hf * 16;
+          float cb[16], xy[16], wv[16];
+          tmem_ld16(T0 + lane_base + col0, cb);
+          tmem_ld16(T1 + lane_base + col0, xy);
+          tmem_wait_ld();
+          if (jc < q) {
 #pragma unroll
-            for (int t = 0; t < 4; ++t) {
-              const int m = t4 * 4 + t;
-              wv[m] = fi * dd4[t] * xy[m];
-              const float mm = wv[m] * cb[m];
+            for (int t4 = 0; t4 < 4; ++t4) {
+              const float4 e4 = *(const float4*)&s_E[q][col0 + t4 * 4];
+              const float4 d4 = *(const float4*)&s_Edt[q][col0 + t4 * 4];
+              const float ee[4] = {e4.x, e4.y, e4.z, e4.w};
+              const float dd4[4] = {d4.x, d4.y, d4.z, d4.w};
+#pragma unroll
+              for (int t = 0; t < 4; ++t) {
+                const int m = t4 * 4 + t;
+                wv[m] = fi * dd4[t] * xy[m];
+                const float mm = wv[m] * cb[m];
+                rowsum += mm;
+                xy[m] = mm;
+                cb[m] *= fi * ee[t];
+              }
+            }
+          } else {
+#pragma unroll
+            for (int m = 0; m < 16; ++m) {
+              const int J = base + col0 + m;
+              const float L = (J <= I) ? exp2f(csI - s_cs2[J]) : 0.f;
+              wv[m] = L * s_dt[J] * xy[m];
+              const float mm = (J < I) ? wv[m] * cb[m] : 0.f;
               rowsum += mm;
               xy[m] = mm;
-              cb[m] *= fi * ee[t];
+              cb[m] *= L;
             }
           }
-        } else {
+          const float cs = warp_column_sum16(xy);
+          if (lane < 16) s_col[q][col0 + lane] = cs;
 #pragma unroll
-          for (int m = 0; m < 32; ++m) {
-            const int J = base + jc * 32 + m;
-            const float L = (J <= I) ? exp2f(csI - s_cs2[J]) : 0.f;
-            wv[m] = L * s_dt[J] * xy[m];
-            const float mm = (J < I) ? wv[m] * cb[m] : 0.f;
-            rowsum += mm;
-            xy[m] = mm;
-            cb[m] *= L;
+          for (int q4 = 0; q4 < 2; ++q4) {
+            const int j = col0 + q4 * 8;
+            store_row_bf16(sW + (j >> 6) * 16384, row, (j & 63) >> 3, &wv[q4 * 8]);
+            store_row_bf16(sO + (j >> 6) * 16384, row, (j & 63) >> 3, &cb[q4 * 8]);
           }
         }
-        const float cs = warp_column_sum(xy);
-        s_col[q][jc * 32 + lane] = cs;
-      } else {
+      } else {  // above the diagonal: zeros
+        const float z[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int m = 0; m < 32; ++m) {
-          wv[m] = 0.f;
-          cb[m] = 0.f;
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const int j = jc * 32 + q4 * 8;
+          store_row_bf16(sW + (j >> 6) * 16384, row, (j & 63) >> 3, z);
+          store_row_bf16(sO + (j >> 6) * 16384, row, (j & 63) >> 3, z);
         }
       }
-#pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        const int j = jc * 32 + q4 * 8;
-        store_row_bf16(sW + (j >> 6) * 16384, row, (j & 63) >> 3, &wv[q4 * 8]);
-        store_row_bf16(sO + (j >> 6) * 16384, row, (j & 63) >> 3, &cb[q4 * 8]);
-      }
     }
-    if (wg == 1) s_red[0][row] = rowsum;
+    if (wg > 0) s_rs[wg - 1][row] = rowsum;
     fence_async_smem();
     fence_before_sync();
     __syncthreads();
@@ -1170,28 +1177,28 @@ k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, int nsub, const float* 
     fence_after_sync();
     if (!ok) break;
 
-    // this thread's half rows of x_j and dy_i (unscaled) into registers, then
+    // this thread's quarter rows of x_j and dy_i (unscaled) into registers, then
     // scale the tiles in place: X rows j by exp(cs_end - cs_j) dt_j, dY rows i by exp(cs_i - ref)
-    // (every 16-byte chunk belongs to exactly one thread: row `row`, chunks 4wg..4wg+3)
-    uint4 xr[4], dyr[4];
+    // (every 16-byte chunk belongs to exactly one thread: row `row`, chunks 2wg, 2wg+1)
+    uint4 xr[2], dyr[2];
     {
       const float sx = exp2f(end2 - s_cs2[base + row]) * s_dt[base + row];
       const float sy = exp2f(s_cs2[base + row] - ref2);
 #pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        uint8_t* px = sX + sw128(row, wg * 4 + q4);
-        uint8_t* py = sDY + sw128(row, wg * 4 + q4);
+      for (int q4 = 0; q4 < 2; ++q4) {
+        uint8_t* px = sX + sw128(row, wg * 2 + q4);
+        uint8_t* py = sDY + sw128(row, wg * 2 + q4);
         xr[q4] = *(const uint4*)px;
         dyr[q4] = *(const uint4*)py;
         float f[8];
         unpack8(xr[q4], f);
 #pragma unroll
         for (int t = 0; t < 8; ++t) f[t] *= sx;
-        store_row_bf16(sX, row, wg * 4 + q4, f);
+        store_row_bf16(sX, row, wg * 2 + q4, f);
         unpack8(dyr[q4], f);
 #pragma unroll
         for (int t = 0; t < 8; ++t) f[t] *= sy;
-        store_row_bf16(sDY, row, wg * 4 + q4, f);
+        store_row_bf16(sDY, row, wg * 2 + q4, f);
       }
     }
     fence_async_smem();
@@ -1216,13 +1223,13 @@ k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, int nsub, const float* 
     const float dtI = s_dt[I];
     float drive = 0.f, ej = 0.f, stin = 0.f, dd = 0.f;
     {
-      float gx[32], gs[32], ch[32];
-      tmem_ld32(T0 + lane_base + wg * 32, gx);
-      tmem_ld32(T0 + lane_base + 64 + wg * 32, gs);
-      tmem_ld32(T1 + lane_base + wg * 32, ch);
+      float gx[16], gs[16], ch[16];
+      tmem_ld16(T0 + lane_base + wg * 16, gx);
+      tmem_ld16(T0 + lane_base + 64 + wg * 16, gs);
+      tmem_ld16(T1 + lane_base + wg * 16, ch);
       tmem_wait_ld();
 #pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
+      for (int q4 = 0; q4 < 2; ++q4) {
         float xf[8], yf[8], o8[8];
         unpack8(xr[q4], xf);
         unpack8(dyr[q4], yf);
@@ -1236,14 +1243,16 @@ k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, int nsub, const float* 
           stin = fmaf(yf[t], ch[m], stin);
           dd = fmaf(yf[t], xf[t], dd);
         }
-        store_row_bf16(sW, row, wg * 4 + q4, o8);  // dx staging: tile [128 rows][64 p]
+        store_row_bf16(sW, row, wg * 2 + q4, o8);  // dx staging: tile [128 rows][64 p]
       }
     }
-    if (wg == 1) {
-      s_red[1][row] = drive;
-      s_red[2][row] = ej;
-      s_red[3][row] = stin;
-      s_red[4][row] = dd;
+    // partials of warpgroups 1-3 go through sO (L o CB was last read by the Gx product)
+    float* ered = (float*)sO;
+    if (wg > 0) {
+      ered[((wg - 1) * 4 + 0) * 128 + row] = drive;
+      ered[((wg - 1) * 4 + 1) * 128 + row] = ej;
+      ered[((wg - 1) * 4 + 2) * 128 + row] = stin;
+      ered[((wg - 1) * 4 + 3) * 128 + row] = dd;
     }
     fence_async_smem();
     __syncthreads();
@@ -1262,11 +1271,16 @@ k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, int nsub, const float* 
       issue_head_loads(h + 1);
     }
     if (wg == 0) {
-      rowsum += s_red[0][row];
-      drive += s_red[1][row];
-      ej = (ej + s_red[2][row]) * sgs * dtI;
-      stin = (stin + s_red[3][row]) * exp2f(s_cs2[I] - ref2);
-      dd += s_red[4][row];
+#pragma unroll
+      for (int w = 0; w < 3; ++w) {
+        rowsum += s_rs[w][row];
+        drive += ered[(w * 4 + 0) * 128 + row];
+        ej += ered[(w * 4 + 1) * 128 + row];
+        stin += ered[(w * 4 + 2) * 128 + row];
+        dd += ered[(w * 4 + 3) * 128 + row];
+      }
+      ej *= sgs * dtI;
+      stin *= exp2f(s_cs2[I] - ref2);
     } else {
       ej = 0.f;
       dd = 0.f;
@@ -1301,14 +1315,13 @@ k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, int nsub, const float* 
   }
 
   // ---- dC and dB of the block, summed over the CTA's heads in TMEM.
-  // Warpgroup wg handles columns [64 wg, 64 wg + 64).
+  // Warpgroup wg handles columns [32 wg, 32 wg + 32).
   if (nsub == 1) {
     if (ok) {  // -> bf16 -> TMA store
       uint8_t* stC = sW;         // 2 tiles [128][128 B]
       uint8_t* stB = sm + kBwX;  // sX + sDY: 2 tiles
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const int jc = 2 * wg + u;
+      {
+        const int jc = wg;
         float vc[32], vb[32];
         tmem_ld32(TdC + lane_base + jc * 32, vc);
         tmem_ld32(TdB + lane_base + jc * 32, vb);
@@ -1339,9 +1352,8 @@ k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, int nsub, const float* 
     float* dumpC = (float*)(sm + kBwC);  // 64 KB: C_k, B_k tiles are dead
     float* dumpB = (float*)(sm + kBwO);  // 64 KB: sO, sX, sDY are dead
     if (ok) {
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const int jc = 2 * wg + u;
+      {
+        const int jc = wg;
         float vc[32], vb[32];
         tmem_ld32(TdC + lane_base + jc * 32, vc);
         tmem_ld32(TdB + lane_base + jc * 32, vb);
@@ -1365,21 +1377,23 @@ k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, int nsub, const float* 
       for (int e = tid; e < rows_per * 32; e += kBwThreads) {
         const int rr = (int)rank * rows_per + (e >> 5), cc = e & 31;
         const uint32_t off = (uint32_t)(rr * 128 + ((cc ^ (rr & 31)) << 2)) * 4u;
-        // all remote loads first (independent), then the fixed-order sums
-        float4 pa[16], pb8[16];
-#pragma unroll
-        for (int r = 0; r < 16; ++r)
-          if (r < nsub) {
-            pa[r] = ld_cluster_f4(map_cluster(baseC + off, (uint32_t)r));
-            pb8[r] = ld_cluster_f4(map_cluster(baseB + off, (uint32_t)r));
-          }
+        // remote loads of 8 ranks at a time (independent), then the sums in rank order
         float4 sc = make_float4(0.f, 0.f, 0.f, 0.f), sb = sc;
+        for (int r0 = 0; r0 < nsub; r0 += 8) {
+          float4 pa[8], pb8[8];
 #pragma unroll
-        for (int r = 0; r < 16; ++r)
-          if (r < nsub) {
-            sc.x += pa[r].x; sc.y += pa[r].y; sc.z += pa[r].z; sc.w += pa[r].w;
-            sb.x += pb8[r].x; sb.y += pb8[r].y; sb.z += pb8[r].z; sb.w += pb8[r].w;
-          }
+          for (int r = 0; r < 8; ++r)
+            if (r0 + r < nsub) {
+              pa[r] = ld_cluster_f4(map_cluster(baseC + off, (uint32_t)(r0 + r)));
+              pb8[r] = ld_cluster_f4(map_cluster(baseB + off, (uint32_t)(r0 + r)));
+            }
+#pragma unroll
+          for (int r = 0; r < 8; ++r)
+            if (r0 + r < nsub) {
+              sc.x += pa[r].x; sc.y += pa[r].y; sc.z += pa[r].z; sc.w += pa[r].w;
+              sb.x += pb8[r].x; sb.y += pb8[r].y; sb.z += pb8[r].z; sb.w += pb8[r].w;
+            }
+        }
         const size_t gi = ((size_t)(row0 + rr) * d.G + g) * d.N + cc * 4;
         uint2 pc, pb;
         pc.x = pack_bf16(sc.x, sc.y);

@@ -169,6 +169,7 @@ size_t carve(Problem* p, char* base, int which) {
   p->drive = (float*)take(tokh);
   p->dA_part = (float*)take(B * nc * (Q / 16) * H * sizeof(float));  // per (chunk, tile or block)
   p->dD_part = (float*)take(B * nc * (Q / 16) * H * sizeof(float));
+  p->ticket = (unsigned int*)take(sizeof(unsigned int));
   p->hT = take(states / 2);  // bf16 copies for the tensor-core backward
   p->gT = take(states / 2);
   if (which == 2) p->hist = (float*)take(states);

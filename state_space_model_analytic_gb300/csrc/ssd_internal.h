@@ -46,6 +46,7 @@ struct Problem {
   float* drive;    // [B][T][H]
   float* dA_part;  // [B][nc][Q/16][H]  (the used prefix depends on the kernel family)
   float* dD_part;  // [B][nc][Q/16][H]  (tile-count upper bound)
+  unsigned int* ticket;  // CTA completion counter of the tensor-core backward
   void* hT;        // [B][nc][H][N][P] bf16: chunk-start states, rows n (tensor-core backward)
   void* gT;        // [B][nc][H][N][P] bf16: chunk-end state gradients, rows n
 

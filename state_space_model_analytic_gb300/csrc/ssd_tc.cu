@@ -316,7 +316,8 @@ template <int MODE>
 __global__ void __launch_bounds__(kScanThreads, 1)
 k_state_scan_tc(const __grid_constant__ ScanStateMaps maps, TcDims d, const float* __restrict__ dt,
                 const float* __restrict__ A, const float* __restrict__ h0,
-                float* __restrict__ hist, float* __restrict__ final_or_dh0) {
+                float* __restrict__ hist, float* __restrict__ final_or_dh0,
+                unsigned int* __restrict__ ticket) {
   extern __shared__ __align__(1024) uint8_t smraw[];
   uint8_t* sm = align1024(smraw);
   const int Q = d.Q;
@@ -329,6 +330,8 @@ k_state_scan_tc(const __grid_constant__ ScanStateMaps maps, TcDims d, const floa
   const int h = blockIdx.x, b = blockIdx.y;
   const int g = h / d.hpg, tid = threadIdx.x;
   const int nc = d.nc;
+  // MODE 1: the backward kernel that follows counts its finished CTAs here
+  if (ticket && h == 0 && b == 0 && tid == 0) *ticket = 0u;
   const size_t PN = (size_t)d.P * d.N;
   auto chunk_of = [&](int it) { return MODE == 0 ? it : nc - 1 - it; };
 
@@ -889,7 +892,8 @@ __global__ void __launch_bounds__(kBwThreads, 1)
 k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, int nsub, const float* __restrict__ dt,
          const float* __restrict__ A, const float* __restrict__ D, float* __restrict__ ddt,
          float* __restrict__ dA_part, float* __restrict__ dD_part, void* __restrict__ dB_out,
-         void* __restrict__ dC_out) {
+         void* __restrict__ dC_out, float* __restrict__ dA, float* __restrict__ dD,
+         unsigned int* __restrict__ ticket) {
   extern __shared__ __align__(1024) uint8_t smraw[];
   uint8_t* sm = align1024(smraw);
   uint8_t* sC = sm + kBwC;
@@ -1410,6 +1414,36 @@ k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, int nsub, const float* 
   fence_before_sync();
   __syncthreads();
   if (tid < 32) tmem_dealloc(tm, 512);
+
+  // ---- the last CTA to finish sums the dA, dD partials of every (b, chunk,
+  // block) per head, in a fixed order (lane-strided sums, then a butterfly)
+  __shared__ int s_lastcta;
+  if (tid == 0) {
+    __threadfence();  // this CTA's partials before its ticket
+    const unsigned int total = gridDim.x * gridDim.y * gridDim.z;
+    s_lastcta = atomicAdd(ticket, 1u) == total - 1u;
+  }
+  __syncthreads();
+  if (s_lastcta) {
+    __threadfence();
+    const int nparts = d.B * d.nc * nblk;
+    for (int hr = tid >> 5; hr < d.H; hr += kBwThreads / 32) {
+      float sa = 0.f, sd = 0.f;
+      for (int kk = lane; kk < nparts; kk += 32) {
+        sa += __ldcg(dA_part + (size_t)kk * d.H + hr);
+        sd += __ldcg(dD_part + (size_t)kk * d.H + hr);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        sa += __shfl_xor_sync(0xffffffffu, sa, o);
+        sd += __shfl_xor_sync(0xffffffffu, sd, o);
+      }
+      if (lane == 0) {
+        dA[hr] = sa;
+        dD[hr] = sd;
+      }
+    }
+  }
 }
 
 // Reverse state pass of the tensor-core backward.  Per (b, h) and a tile of
@@ -1419,7 +1453,8 @@ k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, int nsub, const float* 
 // H_{c-1} (read from the history) as bf16 rows n x 64 p ([b][c][h][n][p]),
 // the operand layout of k_bwd_tc, through a shared-memory transpose.
 __global__ void __launch_bounds__(256)
-k_state_pass_bwd_t(TcDims d, const float* __restrict__ R, const float* __restrict__ hist,
+k_state_pass_bwd_t(TcDims d, unsigned int* __restrict__ ticket, const float* __restrict__ R,
+                   const float* __restrict__ hist,
                    const float* __restrict__ cs_last, __nv_bfloat16* __restrict__ gT,
                    __nv_bfloat16* __restrict__ hT, float* __restrict__ dh0) {
   __shared__ __align__(16) __nv_bfloat16 s_g[16][72];  // [n][p], padded rows
@@ -1465,6 +1500,7 @@ k_state_pass_bwd_t(TcDims d, const float* __restrict__ R, const float* __restric
     gc.w = fmaf(e, gc.w, r.w);
   }
   if (dh0) *(float4*)(dh0 + bh * PN + (size_t)p * d.N + n0 + n4) = gc;
+  if (nt == 0 && h == 0 && b == 0 && tid == 0) *ticket = 0u;  // for the backward kernel
 }
 
 // ---------------------------------------------------------------------------
@@ -1588,7 +1624,7 @@ cudaError_t tc_state_scan(const Problem& p, const char* name, float* final_or_dh
   {
     LaunchScope ls(name, p.stream);
     k_state_scan_tc<MODE><<<dim3(p.H, p.B), kScanThreads, smem, p.stream>>>(
-        maps, tc_dims(p), p.dt, p.A, p.h0, p.hist, final_or_dh0);
+        maps, tc_dims(p), p.dt, p.A, p.h0, p.hist, final_or_dh0, MODE == 1 ? p.ticket : nullptr);
   }
   return cudaGetLastError();
 }
@@ -1633,7 +1669,7 @@ cudaError_t tc_backward(const Problem& p) {
     {
       LaunchScope ls("state_pass_bwd_tc", p.stream);
       k_state_pass_bwd_t<<<dim3(p.N / 16, p.H, p.B), 256, 0, p.stream>>>(
-          tc_dims(p), p.dstate, p.hist, p.cs_last, (__nv_bfloat16*)p.gT, (__nv_bfloat16*)p.hT,
+          tc_dims(p), p.ticket, p.dstate, p.hist, p.cs_last, (__nv_bfloat16*)p.gT, (__nv_bfloat16*)p.hT,
           p.dh0);
     }
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
@@ -1688,12 +1724,10 @@ cudaError_t tc_backward(const Problem& p) {
   {
     LaunchScope ls("bwd_tc", p.stream);
     e = cudaLaunchKernelEx(&cfg, k_bwd_tc, maps, tc_dims(p), nsub, p.dt, p.A, p.D, p.ddt,
-                           p.dA_part, p.dD_part, p.dB, p.dC);
+                           p.dA_part, p.dD_part, p.dB, p.dC, p.dA, p.dD, p.ticket);
   }
   if (e != cudaSuccess) return e;
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  const int nparts = p.B * p.nc * nblk;
-  return simt_reduce_heads(p, nparts, nparts);
+  return cudaGetLastError();
 }
 
 // One CTA waits on an mbarrier that nothing arrives on; the bounded wait gives

@@ -330,8 +330,6 @@ k_state_scan_tc(const __grid_constant__ ScanStateMaps maps, TcDims d, const floa
   const int h = blockIdx.x, b = blockIdx.y;
   const int g = h / d.hpg, tid = threadIdx.x;
   const int nc = d.nc;
-  // MODE 1: the backward kernel that follows counts its finished CTAs here
-  if (ticket && h == 0 && b == 0 && tid == 0) *ticket = 0u;
   const size_t PN = (size_t)d.P * d.N;
   auto chunk_of = [&](int it) { return MODE == 0 ? it : nc - 1 - it; };
 
@@ -371,8 +369,11 @@ k_state_scan_tc(const __grid_constant__ ScanStateMaps maps, TcDims d, const floa
         tma_load_2d(st + Q * 128, &maps.v, g * d.N + 64, row0, &bar_load[k]);
         tma_load_2d(st + 2 * Q * 128, &maps.u, h * d.P, row0, &bar_load[k]);
       };
+      // the first tiles are inputs that no kernel of this library writes: they
+      // are fetched before waiting for the kernel launched ahead of this one
       issue(0);
       if (nc > 1) issue(1);
+      grid_dep_wait();
       int loads_issued = nc > 1 ? 2 : 1, mma_issued = 0;
       const uint32_t idesc = idesc_bf16(128, 64, true, true);
       for (int it = 0; it < nc; ++it) {
@@ -406,9 +407,13 @@ k_state_scan_tc(const __grid_constant__ ScanStateMaps maps, TcDims d, const floa
       if (mma_issued > 0)
         (void)mbar_wait(&bar_sfree[(mma_issued - 1) & 1], ((mma_issued - 1) >> 1) & 1, kWaitLimitNs);
     }
+    if (tid != 256) grid_dep_wait();
     __syncwarp();
   } else if (tid >= 128) {
     // ===================== scalers (warps 4-7) =====================
+    grid_dep_wait();
+    // MODE 1: the backward kernel that follows counts its finished CTAs here
+    if (ticket && h == 0 && b == 0 && tid == 128) *ticket = 0u;
     const int pt = tid - 128, lane = tid & 31, pw = pt >> 5;
     const float a2 = A[h] * kLog2e;
     const int per = Q / 128;  // dt values per thread: 1 or 2, consecutive
@@ -512,6 +517,7 @@ k_state_scan_tc(const __grid_constant__ ScanStateMaps maps, TcDims d, const floa
     if (pt == 0) bulk_wait0();
   } else {
     // ===================== consumer (warps 0-3) =====================
+    grid_dep_wait();
     const int n = tid, q = tid >> 5;
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
     uint8_t* sRows = sm + 2 * stage_bytes;  // [128 rows n][64 p] bf16, SW128
@@ -579,6 +585,7 @@ k_state_scan_tc(const __grid_constant__ ScanStateMaps maps, TcDims d, const floa
     }
     if (tid == 0) bulk_wait0();
   }
+  grid_dep_launch();
   fence_before_sync();
   __syncthreads();
   if (tid < 32) tmem_dealloc(tm, 64 * kScanBufs);
@@ -655,10 +662,14 @@ k_fwd_scan_tc(const __grid_constant__ ScanMaps maps, TcDims d, const float* __re
     tma_load_2d(sB, &maps.B, g * d.N, row0, &bar_load);
     tma_load_2d(sB + 16384, &maps.B, g * d.N + 64, row0, &bar_load);
     tma_load_2d(sX, &maps.x, h * d.P, row0, &bar_load);
-    if (with_state) tma_load_2d(sH, &maps.ht, 0, ((b * d.nc + c) * d.H + h) * d.N, &bar_load);
   };
   const int crow = b * d.T + c * Q;
+  // C, B, x are inputs that no kernel of this library writes: fetched before
+  // waiting for the kernel launched ahead of this one; the state rows after
   if (tid == 0) issue_loads(crow, kHT);
+  grid_dep_wait();
+  if (kHT && tid == 0)
+    tma_load_2d(sH, &maps.ht, 0, ((b * d.nc + c) * d.H + h) * d.N, &bar_load);
 
   // H_{c-1} as bf16 rows n (64 p each): the MN-major B operand of C H^T.
   const float* Hg = hist + (((size_t)b * d.nc + c) * d.H + h) * (size_t)(64 * 128);
@@ -847,6 +858,7 @@ k_fwd_scan_tc(const __grid_constant__ ScanMaps maps, TcDims d, const float* __re
       fence_after_sync();
     }
   }
+  grid_dep_launch();
   if (tid == 0) bulk_wait0();
   fence_before_sync();
   __syncthreads();
@@ -951,7 +963,9 @@ k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, int nsub, const float* 
   const uint32_t tm = tmem_base;
   const uint32_t T0 = tm, T1 = tm + 128, TdC = tm + 256, TdB = tm + 384;
 
-  auto issue_head_loads = [&](int h) {
+  // with_state: also the head's state and state-gradient rows (outputs of the
+  // state pass); the first head fetches them after waiting for that kernel
+  auto issue_head_loads = [&](int h, bool with_state) {
     mbar_expect_tx(&bar_head, head_bytes);
     tma_load_2d(sX, &maps.x, h * d.P, row0, &bar_head);
     tma_load_2d(sDY, &maps.dy, h * d.P, row0, &bar_head);
@@ -966,9 +980,11 @@ k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, int nsub, const float* 
         tma_load_2d(sW + 16384, &maps.C, g * d.N + 64, crow + 128, &bar_head);
       }
     }
-    const int srow = ((b * d.nc + c) * d.H + h) * d.N;
-    tma_load_2d(sH, &maps.ht, 0, srow, &bar_head);
-    tma_load_2d(sG, &maps.gt, 0, srow, &bar_head);
+    if (with_state) {
+      const int srow = ((b * d.nc + c) * d.H + h) * d.N;
+      tma_load_2d(sH, &maps.ht, 0, srow, &bar_head);
+      tma_load_2d(sG, &maps.gt, 0, srow, &bar_head);
+    }
   };
   const int h_first = g * d.hpg + sub * kh;
   if (tid == 0) {
@@ -977,7 +993,13 @@ k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, int nsub, const float* 
     tma_load_2d(sC + 16384, &maps.C, g * d.N + 64, row0, &bar_shared);
     tma_load_2d(sB, &maps.B, g * d.N, row0, &bar_shared);
     tma_load_2d(sB + 16384, &maps.B, g * d.N + 64, row0, &bar_shared);
-    issue_head_loads(h_first);
+    issue_head_loads(h_first, false);
+  }
+  grid_dep_wait();
+  if (tid == 0) {
+    const int srow = ((b * d.nc + c) * d.H + h_first) * d.N;
+    tma_load_2d(sH, &maps.ht, 0, srow, &bar_head);
+    tma_load_2d(sG, &maps.gt, 0, srow, &bar_head);
   }
   // dt, A and D of the next head are loaded one head ahead
   float dt_next = load_dt_256(d, dt, b, c, h_first);
@@ -1272,7 +1294,7 @@ k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, int nsub, const float* 
     fence_after_sync();
     if (tid == 0 && ok && hh + 1 < kh) {
       if (two) bulk_wait_read0();
-      issue_head_loads(h + 1);
+      issue_head_loads(h + 1, true);
     }
     if (wg == 0) {
 #pragma unroll
@@ -1410,6 +1432,7 @@ k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, int nsub, const float* 
     }
     cluster_sync();
   }
+  grid_dep_launch();
   if (tid == 0) bulk_wait0();
   fence_before_sync();
   __syncthreads();
@@ -1559,6 +1582,25 @@ cudaError_t set_smem_tc(K kernel, size_t bytes) {
   return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
 }
 
+// Launch with programmatic stream serialization: the kernel may start while
+// the kernel ahead of it on the stream finishes; it waits for that kernel
+// (griddepcontrol.wait) before touching anything the earlier kernels write.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 }  // namespace
 
 static int g_force_path = -1;  // -1 automatic, 0 SIMT only
@@ -1623,9 +1665,11 @@ cudaError_t tc_state_scan(const Problem& p, const char* name, float* final_or_dh
   if (e != cudaSuccess) return e;
   {
     LaunchScope ls(name, p.stream);
-    k_state_scan_tc<MODE><<<dim3(p.H, p.B), kScanThreads, smem, p.stream>>>(
-        maps, tc_dims(p), p.dt, p.A, p.h0, p.hist, final_or_dh0, MODE == 1 ? p.ticket : nullptr);
+    e = launch_pdl(k_state_scan_tc<MODE>, dim3(p.H, p.B), dim3(kScanThreads), smem, p.stream, maps,
+                   tc_dims(p), p.dt, p.A, p.h0, p.hist, final_or_dh0,
+                   MODE == 1 ? p.ticket : (unsigned int*)nullptr);
   }
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -1650,13 +1694,10 @@ cudaError_t tc_forward_scan(const Problem& p) {
   if (e != cudaSuccess) return e;
   {
     LaunchScope ls(ht ? "chunk_scan_ht_tc" : "chunk_scan_tc", p.stream);
-    if (ht)
-      k_fwd_scan_tc<true><<<dim3(p.nc, p.H, p.B), 256, smem, p.stream>>>(maps, tc_dims(p), p.dt,
-                                                                        p.A, p.D, p.hist);
-    else
-      k_fwd_scan_tc<false><<<dim3(p.nc, p.H, p.B), 256, smem, p.stream>>>(maps, tc_dims(p), p.dt,
-                                                                         p.A, p.D, p.hist);
+    e = launch_pdl(ht ? k_fwd_scan_tc<true> : k_fwd_scan_tc<false>, dim3(p.nc, p.H, p.B),
+                   dim3(256), smem, p.stream, maps, tc_dims(p), p.dt, p.A, p.D, p.hist);
   }
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -1714,13 +1755,16 @@ cudaError_t tc_backward(const Problem& p) {
   cfg.blockDim = dim3(kBwThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = p.stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 1;
   attr[0].val.clusterDim.y = nsub;
   attr[0].val.clusterDim.z = 1;
+  // may start while the state pass ahead of it finishes (see launch_pdl)
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   {
     LaunchScope ls("bwd_tc", p.stream);
     e = cudaLaunchKernelEx(&cfg, k_bwd_tc, maps, tc_dims(p), nsub, p.dt, p.A, p.D, p.ddt,

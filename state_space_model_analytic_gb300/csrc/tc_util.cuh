@@ -233,6 +233,17 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 
 __device__ __forceinline__ bool elect_one() { return threadIdx.x % 32 == 0; }
 
+// ---- programmatic dependent launch ----------------------------------------------
+// Wait until the kernel this one was launched behind (with programmatic stream
+// serialization) has completed and its writes are visible; a no-op otherwise.
+__device__ __forceinline__ void grid_dep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+// Let the next kernel on the stream start its prologue.
+__device__ __forceinline__ void grid_dep_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---- thread-block clusters -----------------------------------------------------
 __device__ __forceinline__ uint32_t cluster_rank() {
   uint32_t r;

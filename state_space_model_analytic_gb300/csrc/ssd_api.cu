@@ -169,7 +169,14 @@ size_t carve(Problem* p, char* base, int which) {
   p->drive = (float*)take(tokh);
   p->dA_part = (float*)take(B * nc * (Q / 16) * H * sizeof(float));  // per (chunk, tile or block)
   p->dD_part = (float*)take(B * nc * (Q / 16) * H * sizeof(float));
-  p->ticket = (unsigned int*)take(sizeof(unsigned int));
+  // tensor-core backward: one counter for all CTAs and one per (b, g, chunk,
+  // 128-row block) unit; fp32 partials of dC, dB (2 x 128 x 128 floats) in two
+  // slots per CTA, at most kBwdMaxCtas CTAs and one per (unit, head) item
+  const size_t units = B * (size_t)p->G * nc * ((Q + 127) / 128);
+  const size_t items = units * (size_t)p->hpg;
+  p->ntickets = (int)(1 + units);
+  p->tickets = (unsigned int*)take((1 + units) * sizeof(unsigned int));
+  p->bwd_part = (float*)take((items < kBwdMaxCtas ? items : kBwdMaxCtas) * 2 * 32768 * sizeof(float));
   p->hT = take(states / 2);  // bf16 copies for the tensor-core backward
   p->gT = take(states / 2);
   if (which == 2) p->hist = (float*)take(states);

@@ -46,12 +46,17 @@ struct Problem {
   float* drive;    // [B][T][H]
   float* dA_part;  // [B][nc][Q/16][H]  (the used prefix depends on the kernel family)
   float* dD_part;  // [B][nc][Q/16][H]  (tile-count upper bound)
-  unsigned int* ticket;  // CTA completion counter of the tensor-core backward
+  unsigned int* tickets;  // [1 + units] completion counters of the tensor-core backward
+  int ntickets;
+  float* bwd_part;        // tensor-core backward: fp32 dC, dB partials, 2 slots per CTA
   void* hT;        // [B][nc][H][N][P] bf16: chunk-start states, rows n (tensor-core backward)
   void* gT;        // [B][nc][H][N][P] bf16: chunk-end state gradients, rows n
 
   cudaStream_t stream;
 };
+
+// Upper bound on the CTAs of the tensor-core backward (one per SM).
+constexpr size_t kBwdMaxCtas = 160;
 
 // Kernel launchers (SIMT family).  Each returns the CUDA launch status and
 // bumps the launch counter.

@@ -317,7 +317,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
 k_state_scan_tc(const __grid_constant__ ScanStateMaps maps, TcDims d, const float* __restrict__ dt,
                 const float* __restrict__ A, const float* __restrict__ h0,
                 float* __restrict__ hist, float* __restrict__ final_or_dh0,
-                unsigned int* __restrict__ ticket) {
+                unsigned int* __restrict__ tickets, int ntickets) {
   extern __shared__ __align__(1024) uint8_t smraw[];
   uint8_t* sm = align1024(smraw);
   const int Q = d.Q;
@@ -412,8 +412,12 @@ k_state_scan_tc(const __grid_constant__ ScanStateMaps maps, TcDims d, const floa
   } else if (tid >= 128) {
     // ===================== scalers (warps 4-7) =====================
     grid_dep_wait();
-    // MODE 1: the backward kernel that follows counts its finished CTAs here
-    if (ticket && h == 0 && b == 0 && tid == 128) *ticket = 0u;
+    // MODE 1: the backward kernel that follows counts its finished CTAs and
+    // unit segments here
+    if (tickets)
+      for (int i = (b * (int)gridDim.x + h) * 128 + (tid - 128); i < ntickets;
+           i += (int)(gridDim.x * gridDim.y) * 128)
+        tickets[i] = 0u;
     const int pt = tid - 128, lane = tid & 31, pw = pt >> 5;
     const float a2 = A[h] * kLog2e;
     const int per = Q / 128;  // dt values per thread: 1 or 2, consecutive
@@ -866,9 +870,14 @@ k_fwd_scan_tc(const __grid_constant__ ScanMaps maps, TcDims d, const float* __re
 }
 
 // ---------------------------------------------------------------------------
-// Backward on tensor cores.  One CTA per (128-row block k, chunk c, group g,
-// head subset, batch b); the CTA loops over its heads and accumulates dC and
-// dB of the block over those heads in TMEM (fixed head order, deterministic).
+// Backward on tensor cores.  The work items are (unit, head) pairs, a unit
+// being one (128-row block k, chunk c, group g, batch b); one CTA per SM takes
+// an equal contiguous range of items, i.e. one or more segments of
+// consecutive heads of a unit.  Per segment the CTA loops over its heads and
+// accumulates dC and dB of the block over them in TMEM (fixed head order).  A
+// unit covered by one segment writes dC, dB directly; a unit split over
+// several CTAs writes fp32 partials, and the last of its segments to finish
+// (a per-unit ticket) sums them in segment order (deterministic).
 // Each block is treated as a chunk of 128 steps with
 //   state in  Hin  = H_{c-1} (k = 0) or H_mid  (k = 1),
 //   grad out  gout = g_c     (last block) or g_mid = exp(cs_255 - cs_127) g_c + R_1 (k = 0 of 2),
@@ -901,11 +910,11 @@ constexpr uint32_t kBwW = 180224;     // B_0 (k = 1) / C_1 (k = 0) per head, the
 constexpr uint32_t kBwBytes = 212992;
 
 __global__ void __launch_bounds__(kBwThreads, 1)
-k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, int nsub, const float* __restrict__ dt,
-         const float* __restrict__ A, const float* __restrict__ D, float* __restrict__ ddt,
-         float* __restrict__ dA_part, float* __restrict__ dD_part, void* __restrict__ dB_out,
-         void* __restrict__ dC_out, float* __restrict__ dA, float* __restrict__ dD,
-         unsigned int* __restrict__ ticket) {
+k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, long long nitems,
+         const float* __restrict__ dt, const float* __restrict__ A, const float* __restrict__ D,
+         float* __restrict__ ddt, float* __restrict__ dA_part, float* __restrict__ dD_part,
+         void* __restrict__ dB_out, void* __restrict__ dC_out, float* __restrict__ dA,
+         float* __restrict__ dD, unsigned int* __restrict__ tickets, float* __restrict__ part) {
   extern __shared__ __align__(1024) uint8_t smraw[];
   uint8_t* sm = align1024(smraw);
   uint8_t* sC = sm + kBwC;
@@ -927,17 +936,22 @@ k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, int nsub, const float* 
   __shared__ float s_esum;
   __shared__ uint64_t bar_shared, bar_head, bar_mma;
   __shared__ uint32_t tmem_base;
+  __shared__ int s_flag;
 
   const int nblk = d.Q / 128;
-  const int k = blockIdx.x % nblk, c = blockIdx.x / nblk;
-  const int g = blockIdx.y / nsub, sub = blockIdx.y % nsub, b = blockIdx.z;
-  const int kh = d.hpg / nsub;
   const int tid = threadIdx.x, wg = tid >> 7, q = (tid >> 5) & 3, lane = tid & 31;
   const int row = tid & 127;  // TMEM lane / tile row owned (with the other warpgroups)
-  const int base = 128 * k;
-  const int crow = b * d.T + c * d.Q;  // first row of the chunk
-  const int row0 = crow + base;
   const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+  // items [it_begin, it_end) of this CTA; item = unit * hpg + head in group,
+  // unit = ((b * G + g) * nc + c) * nblk + k
+  const long long ncta = gridDim.x;
+  const long long it_begin = (long long)blockIdx.x * nitems / ncta;
+  const long long it_end = ((long long)blockIdx.x + 1) * nitems / ncta;
+  auto cta_of = [&](long long item) {  // the CTA whose range holds `item`
+    return (int)(((item + 1) * ncta + nitems - 1) / nitems - 1);
+  };
+  // the current segment's unit
+  int k = 0, c = 0, g = 0, b = 0, base = 0, crow = 0, row0 = 0;
   const bool two = nblk == 2;
   const uint32_t head_bytes = (two ? 80 : 32) * 1024 + 32 * 1024;
 
@@ -965,47 +979,75 @@ k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, int nsub, const float* 
 
   // with_state: also the head's state and state-gradient rows (outputs of the
   // state pass); the first head fetches them after waiting for that kernel
-  auto issue_head_loads = [&](int h, bool with_state) {
+  // tiles of head h of unit uu (the head's own and, for chunks of two blocks,
+  // the other block's tiles for the mid-chunk state / state gradient)
+  auto issue_head_loads = [&](int uu, int h, bool with_state) {
+    const int kk = uu % nblk, cc = (uu / nblk) % d.nc, gg = (uu / (nblk * d.nc)) % d.G;
+    const int bb = uu / (nblk * d.nc * d.G);
+    const int crow_u = bb * d.T + cc * d.Q, row0_u = crow_u + 128 * kk;
     mbar_expect_tx(&bar_head, head_bytes);
-    tma_load_2d(sX, &maps.x, h * d.P, row0, &bar_head);
-    tma_load_2d(sDY, &maps.dy, h * d.P, row0, &bar_head);
-    if (two) {  // the other block's tiles for the mid-chunk state / state gradient
-      if (k == 1) {
-        tma_load_2d(sXO, &maps.x, h * d.P, crow, &bar_head);
-        tma_load_2d(sW, &maps.B, g * d.N, crow, &bar_head);
-        tma_load_2d(sW + 16384, &maps.B, g * d.N + 64, crow, &bar_head);
+    tma_load_2d(sX, &maps.x, h * d.P, row0_u, &bar_head);
+    tma_load_2d(sDY, &maps.dy, h * d.P, row0_u, &bar_head);
+    if (two) {
+      if (kk == 1) {
+        tma_load_2d(sXO, &maps.x, h * d.P, crow_u, &bar_head);
+        tma_load_2d(sW, &maps.B, gg * d.N, crow_u, &bar_head);
+        tma_load_2d(sW + 16384, &maps.B, gg * d.N + 64, crow_u, &bar_head);
       } else {
-        tma_load_2d(sXO, &maps.dy, h * d.P, crow + 128, &bar_head);
-        tma_load_2d(sW, &maps.C, g * d.N, crow + 128, &bar_head);
-        tma_load_2d(sW + 16384, &maps.C, g * d.N + 64, crow + 128, &bar_head);
+        tma_load_2d(sXO, &maps.dy, h * d.P, crow_u + 128, &bar_head);
+        tma_load_2d(sW, &maps.C, gg * d.N, crow_u + 128, &bar_head);
+        tma_load_2d(sW + 16384, &maps.C, gg * d.N + 64, crow_u + 128, &bar_head);
       }
     }
     if (with_state) {
-      const int srow = ((b * d.nc + c) * d.H + h) * d.N;
+      const int srow = ((bb * d.nc + cc) * d.H + h) * d.N;
       tma_load_2d(sH, &maps.ht, 0, srow, &bar_head);
       tma_load_2d(sG, &maps.gt, 0, srow, &bar_head);
     }
   };
-  const int h_first = g * d.hpg + sub * kh;
-  if (tid == 0) {
+  // C_k and B_k of unit uu
+  auto issue_unit_loads = [&](int uu) {
+    const int kk = uu % nblk, cc = (uu / nblk) % d.nc, gg = (uu / (nblk * d.nc)) % d.G;
+    const int bb = uu / (nblk * d.nc * d.G);
+    const int row0_u = bb * d.T + cc * d.Q + 128 * kk;
     mbar_expect_tx(&bar_shared, 64 * 1024);
-    tma_load_2d(sC, &maps.C, g * d.N, row0, &bar_shared);
-    tma_load_2d(sC + 16384, &maps.C, g * d.N + 64, row0, &bar_shared);
-    tma_load_2d(sB, &maps.B, g * d.N, row0, &bar_shared);
-    tma_load_2d(sB + 16384, &maps.B, g * d.N + 64, row0, &bar_shared);
-    issue_head_loads(h_first, false);
-  }
-  grid_dep_wait();
+    tma_load_2d(sC, &maps.C, gg * d.N, row0_u, &bar_shared);
+    tma_load_2d(sC + 16384, &maps.C, gg * d.N + 64, row0_u, &bar_shared);
+    tma_load_2d(sB, &maps.B, gg * d.N, row0_u, &bar_shared);
+    tma_load_2d(sB + 16384, &maps.B, gg * d.N + 64, row0_u, &bar_shared);
+  };
+  uint32_t mma_phase = 0, head_phase = 0, shared_phase = 0;
+  bool ok = true;
+  for (long long x = it_begin; x < it_end && ok;) {
+  // ---- segment: heads [j0, j0 + kh) of unit u
+  const int u = (int)(x / d.hpg), j0 = (int)(x % d.hpg);
+  const int kh = (int)((long long)(d.hpg - j0) < it_end - x ? (long long)(d.hpg - j0) : it_end - x);
+  k = u % nblk;
+  c = (u / nblk) % d.nc;
+  g = (u / (nblk * d.nc)) % d.G;
+  b = u / (nblk * d.nc * d.G);
+  base = 128 * k;
+  crow = b * d.T + c * d.Q;  // first row of the chunk
+  row0 = crow + base;
+  const int h_first = g * d.hpg + j0;
+  const bool first_seg = x == it_begin;
   if (tid == 0) {
-    const int srow = ((b * d.nc + c) * d.H + h_first) * d.N;
-    tma_load_2d(sH, &maps.ht, 0, srow, &bar_head);
-    tma_load_2d(sG, &maps.gt, 0, srow, &bar_head);
+    issue_unit_loads(u);
+    issue_head_loads(u, h_first, !first_seg);
+  }
+  if (first_seg) {
+    grid_dep_wait();
+    if (tid == 0) {
+      const int srow = ((b * d.nc + c) * d.H + h_first) * d.N;
+      tma_load_2d(sH, &maps.ht, 0, srow, &bar_head);
+      tma_load_2d(sG, &maps.gt, 0, srow, &bar_head);
+    }
   }
   // dt, A and D of the next head are loaded one head ahead
   float dt_next = load_dt_256(d, dt, b, c, h_first);
   float A_next = A[h_first], D_next = D[h_first];
-  bool ok = wait_or_flag(&bar_shared, 0);
-  uint32_t mma_phase = 0;
+  ok = wait_or_flag(&bar_shared, shared_phase);
+  shared_phase ^= 1;
 
   for (int hh = 0; hh < kh && ok; ++hh) {
     const int h = h_first + hh;
@@ -1025,7 +1067,8 @@ k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, int nsub, const float* 
     }
     const float ref2 = k == 0 ? 0.f : s_cs2[base - 1];
     const float end2 = s_cs2[base + 127];
-    ok = wait_or_flag(&bar_head, hh & 1);  // also publishes the tables
+    ok = wait_or_flag(&bar_head, head_phase);  // also publishes the tables
+    head_phase ^= 1;
     if (!ok) break;
 
     // ---- mid-chunk state or state gradient (chunks of two blocks)
@@ -1294,7 +1337,7 @@ k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, int nsub, const float* 
     fence_after_sync();
     if (tid == 0 && ok && hh + 1 < kh) {
       if (two) bulk_wait_read0();
-      issue_head_loads(h + 1, true);
+      issue_head_loads(u, h + 1, true);
     }
     if (wg == 0) {
 #pragma unroll
@@ -1340,99 +1383,82 @@ k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, int nsub, const float* 
     __syncthreads();
   }
 
-  // ---- dC and dB of the block, summed over the CTA's heads in TMEM.
-  // Warpgroup wg handles columns [32 wg, 32 wg + 32).
-  if (nsub == 1) {
-    if (ok) {  // -> bf16 -> TMA store
-      uint8_t* stC = sW;         // 2 tiles [128][128 B]
-      uint8_t* stB = sm + kBwX;  // sX + sDY: 2 tiles
-      {
-        const int jc = wg;
-        float vc[32], vb[32];
-        tmem_ld32(TdC + lane_base + jc * 32, vc);
-        tmem_ld32(TdB + lane_base + jc * 32, vb);
-        tmem_wait_ld();
+  // ---- dC and dB of the segment, summed over its heads in TMEM.
+  // Warpgroup wg handles columns [32 wg, 32 wg + 32); dC first, then dB.
+  {
+    const long long u0 = (long long)u * d.hpg;
+    const int cta0 = cta_of(u0), nseg = cta_of(u0 + d.hpg - 1) - cta0 + 1;
+    const int jc = wg;
+    // fp32 partials, column-major [n][row] (coalesced over rows), in this CTA's
+    // slot: 0 for its first segment, 1 for its last
+    float* pslot = part + ((size_t)blockIdx.x * 2 + (first_seg ? 0 : 1)) * 32768;
+    if (nseg > 1) {
+      if (ok) {
+#pragma unroll 1
+        for (int which = 0; which < 2; ++which) {
+          float v[32];
+          tmem_ld32((which ? TdB : TdC) + lane_base + jc * 32, v);
+          tmem_wait_ld();
+          float* pw = pslot + which * 16384;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) pw[(jc * 32 + i) * 128 + row] = v[i];
+        }
+      }
+      __threadfence();
+      __syncthreads();
+      if (tid == 0) s_flag = atomicAdd(&tickets[1 + u], 1u) == (unsigned int)(nseg - 1);
+      __syncthreads();
+      if (s_flag) __threadfence();
+    }
+    // the unit's output: a single segment from TMEM, else by its last segment
+    // as the sum of the partials in segment order; bf16 -> staging in sO (dead
+    // since the last head's Gx product) -> TMA store, dC then dB
+    const bool write_out = ok && (nseg == 1 || s_flag);
+    if (write_out) {
+#pragma unroll 1
+      for (int which = 0; which < 2; ++which) {
+        float v[32];
+        if (nseg == 1) {
+          tmem_ld32((which ? TdB : TdC) + lane_base + jc * 32, v);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = 0.f;
+          for (int j = 0; j < nseg; ++j) {
+            const int cj = cta0 + j;
+            const long long first_item = (long long)cj * nitems / ncta;
+            const int side = first_item / d.hpg == u ? 0 : 1;
+            const float* q = part + ((size_t)cj * 2 + side) * 32768 + which * 16384;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] += __ldcg(q + (jc * 32 + i) * 128 + row);
+          }
+        }
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
           const int nn = jc * 32 + q4 * 8;
-          store_row_bf16(stC + (nn >> 6) * 16384, row, (nn & 63) >> 3, &vc[q4 * 8]);
-          store_row_bf16(stB + (nn >> 6) * 16384, row, (nn & 63) >> 3, &vb[q4 * 8]);
+          store_row_bf16(sO + (nn >> 6) * 16384, row, (nn & 63) >> 3, &v[q4 * 8]);
         }
-      }
-      fence_async_smem();
-      __syncthreads();
-      if (tid == 0) {
-        tma_store_2d(&maps.dC, stC, g * d.N, row0);
-        tma_store_2d(&maps.dC, stC + 16384, g * d.N + 64, row0);
-        tma_store_2d(&maps.dB, stB, g * d.N, row0);
-        tma_store_2d(&maps.dB, stB + 16384, g * d.N + 64, row0);
-        bulk_commit();
+        fence_async_smem();
+        __syncthreads();
+        if (tid == 0) {
+          const CUtensorMap* m = which ? &maps.dB : &maps.dC;
+          tma_store_2d(m, sO, g * d.N, row0);
+          tma_store_2d(m, sO + 16384, g * d.N + 64, row0);
+          bulk_commit();
+          bulk_wait_read0();  // sO is rewritten by dB, then by the next W build
+        }
+        __syncthreads();
       }
     }
-  } else {
-    // The nsub CTAs of a cluster hold partial sums over disjoint head subsets.
-    // Each dumps its fp32 rows to shared memory (16-byte chunks XOR-swizzled by
-    // row), then CTA `rank` sums rows [rank*128/nsub, ...) over ranks 0..nsub-1
-    // in order and writes bf16 dC, dB.  Every CTA reaches both cluster
-    // barriers, also after a timeout.
-    float* dumpC = (float*)(sm + kBwC);  // 64 KB: C_k, B_k tiles are dead
-    float* dumpB = (float*)(sm + kBwO);  // 64 KB: sO, sX, sDY are dead
-    if (ok) {
-      {
-        const int jc = wg;
-        float vc[32], vb[32];
-        tmem_ld32(TdC + lane_base + jc * 32, vc);
-        tmem_ld32(TdB + lane_base + jc * 32, vb);
-        tmem_wait_ld();
-#pragma unroll
-        for (int q8 = 0; q8 < 8; ++q8) {
-          const int cc = jc * 8 + q8;
-          const int off = row * 128 + ((cc ^ (row & 31)) << 2);
-          *(float4*)(dumpC + off) = make_float4(vc[4 * q8], vc[4 * q8 + 1], vc[4 * q8 + 2], vc[4 * q8 + 3]);
-          *(float4*)(dumpB + off) = make_float4(vb[4 * q8], vb[4 * q8 + 1], vb[4 * q8 + 2], vb[4 * q8 + 3]);
-        }
-      }
-    }
-    cluster_sync();
-    if (ok) {
-      const uint32_t rank = cluster_rank();
-      const int rows_per = 128 / nsub;
-      const uint32_t baseC = smem_u32(dumpC), baseB = smem_u32(dumpB);
-      __nv_bfloat16* gC = (__nv_bfloat16*)dC_out;
-      __nv_bfloat16* gB = (__nv_bfloat16*)dB_out;
-      for (int e = tid; e < rows_per * 32; e += kBwThreads) {
-        const int rr = (int)rank * rows_per + (e >> 5), cc = e & 31;
-        const uint32_t off = (uint32_t)(rr * 128 + ((cc ^ (rr & 31)) << 2)) * 4u;
-        // remote loads of 8 ranks at a time (independent), then the sums in rank order
-        float4 sc = make_float4(0.f, 0.f, 0.f, 0.f), sb = sc;
-        for (int r0 = 0; r0 < nsub; r0 += 8) {
-          float4 pa[8], pb8[8];
-#pragma unroll
-          for (int r = 0; r < 8; ++r)
-            if (r0 + r < nsub) {
-              pa[r] = ld_cluster_f4(map_cluster(baseC + off, (uint32_t)(r0 + r)));
-              pb8[r] = ld_cluster_f4(map_cluster(baseB + off, (uint32_t)(r0 + r)));
-            }
-#pragma unroll
-          for (int r = 0; r < 8; ++r)
-            if (r0 + r < nsub) {
-              sc.x += pa[r].x; sc.y += pa[r].y; sc.z += pa[r].z; sc.w += pa[r].w;
-              sb.x += pb8[r].x; sb.y += pb8[r].y; sb.z += pb8[r].z; sb.w += pb8[r].w;
-            }
-        }
-        const size_t gi = ((size_t)(row0 + rr) * d.G + g) * d.N + cc * 4;
-        uint2 pc, pb;
-        pc.x = pack_bf16(sc.x, sc.y);
-        pc.y = pack_bf16(sc.z, sc.w);
-        pb.x = pack_bf16(sb.x, sb.y);
-        pb.y = pack_bf16(sb.z, sb.w);
-        *(uint2*)(gC + gi) = pc;
-        *(uint2*)(gB + gi) = pb;
-      }
-    }
-    cluster_sync();
+    // TMEM accumulators and the ticket flag are reused by the next segment
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+  }
+  x += kh;
   }
   grid_dep_launch();
+  grid_dep_wait();  // (a CTA without items has not waited yet; the tickets are zeroed before)
   if (tid == 0) bulk_wait0();
   fence_before_sync();
   __syncthreads();
@@ -1440,14 +1466,12 @@ k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, int nsub, const float* 
 
   // ---- the last CTA to finish sums the dA, dD partials of every (b, chunk,
   // block) per head, in a fixed order (lane-strided sums, then a butterfly)
-  __shared__ int s_lastcta;
   if (tid == 0) {
     __threadfence();  // this CTA's partials before its ticket
-    const unsigned int total = gridDim.x * gridDim.y * gridDim.z;
-    s_lastcta = atomicAdd(ticket, 1u) == total - 1u;
+    s_flag = atomicAdd(&tickets[0], 1u) == gridDim.x - 1u;
   }
   __syncthreads();
-  if (s_lastcta) {
+  if (s_flag) {
     __threadfence();
     const int nparts = d.B * d.nc * nblk;
     for (int hr = tid >> 5; hr < d.H; hr += kBwThreads / 32) {
@@ -1476,7 +1500,8 @@ k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, int nsub, const float* 
 // H_{c-1} (read from the history) as bf16 rows n x 64 p ([b][c][h][n][p]),
 // the operand layout of k_bwd_tc, through a shared-memory transpose.
 __global__ void __launch_bounds__(256)
-k_state_pass_bwd_t(TcDims d, unsigned int* __restrict__ ticket, const float* __restrict__ R,
+k_state_pass_bwd_t(TcDims d, unsigned int* __restrict__ tickets, int ntickets,
+                   const float* __restrict__ R,
                    const float* __restrict__ hist,
                    const float* __restrict__ cs_last, __nv_bfloat16* __restrict__ gT,
                    __nv_bfloat16* __restrict__ hT, float* __restrict__ dh0) {
@@ -1523,7 +1548,10 @@ k_state_pass_bwd_t(TcDims d, unsigned int* __restrict__ ticket, const float* __r
     gc.w = fmaf(e, gc.w, r.w);
   }
   if (dh0) *(float4*)(dh0 + bh * PN + (size_t)p * d.N + n0 + n4) = gc;
-  if (nt == 0 && h == 0 && b == 0 && tid == 0) *ticket = 0u;  // for the backward kernel
+  // completion counters of the backward kernel that follows
+  for (int i = ((b * (int)gridDim.y + h) * (int)gridDim.x + nt) * 256 + tid; i < ntickets;
+       i += (int)(gridDim.x * gridDim.y * gridDim.z) * 256)
+    tickets[i] = 0u;
 }
 
 // ---------------------------------------------------------------------------
@@ -1667,7 +1695,7 @@ cudaError_t tc_state_scan(const Problem& p, const char* name, float* final_or_dh
     LaunchScope ls(name, p.stream);
     e = launch_pdl(k_state_scan_tc<MODE>, dim3(p.H, p.B), dim3(kScanThreads), smem, p.stream, maps,
                    tc_dims(p), p.dt, p.A, p.h0, p.hist, final_or_dh0,
-                   MODE == 1 ? p.ticket : (unsigned int*)nullptr);
+                   MODE == 1 ? p.tickets : (unsigned int*)nullptr, p.ntickets);
   }
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
@@ -1710,7 +1738,7 @@ cudaError_t tc_backward(const Problem& p) {
     {
       LaunchScope ls("state_pass_bwd_tc", p.stream);
       k_state_pass_bwd_t<<<dim3(p.N / 16, p.H, p.B), 256, 0, p.stream>>>(
-          tc_dims(p), p.ticket, p.dstate, p.hist, p.cs_last, (__nv_bfloat16*)p.gT, (__nv_bfloat16*)p.hT,
+          tc_dims(p), p.tickets, p.ntickets, p.dstate, p.hist, p.cs_last, (__nv_bfloat16*)p.gT, (__nv_bfloat16*)p.hT,
           p.dh0);
     }
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
@@ -1731,44 +1759,29 @@ cudaError_t tc_backward(const Problem& p) {
   const size_t smem = kBwBytes + 1024;
   if ((e = set_smem_tc(k_bwd_tc, smem)) != cudaSuccess) return e;
   const int nblk = p.Q / 128;
-  // split a group's heads over a cluster of nsub CTAs when there are too few
-  // (block, chunk, group, batch) units to fill the GPU.  With one CTA per SM,
-  // large clusters schedule poorly (a cluster waits for nsub free SMs of one
-  // GPC), so the split stops at the first size giving ~0.8 CTA per SM.
+  // one CTA per SM (at most kBwdMaxCtas, at most one per item), each taking an
+  // equal contiguous range of the (unit, head) items
   int nsm = 0, dev = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
-  const long units = (long)nblk * p.nc * p.G * p.B;
-  int nsub = 1;
-  while (nsub < 8 && units * nsub * 5 < 4L * nsm && p.hpg % (2 * nsub) == 0) nsub *= 2;
-  // tuning override (power of two dividing the heads per group, at most 16)
-  if (const char* env = getenv("SSD_BWD_HEAD_SPLIT")) {
-    const int v = atoi(env);
-    if (v >= 1 && v <= 16 && (v & (v - 1)) == 0 && p.hpg % v == 0) nsub = v;
-  }
-  if (nsub > 8) {
-    e = cudaFuncSetAttribute(k_bwd_tc, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    if (e != cudaSuccess) return e;
-  }
+  const long long nitems = (long long)p.B * p.G * p.nc * nblk * p.hpg;
+  long long ncta = nsm < (int)kBwdMaxCtas ? nsm : (long long)kBwdMaxCtas;
+  if (ncta > nitems) ncta = nitems;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(nblk * p.nc, p.G * nsub, p.B);
+  cfg.gridDim = dim3((unsigned)ncta, 1, 1);
   cfg.blockDim = dim3(kBwThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = p.stream;
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 1;
-  attr[0].val.clusterDim.y = nsub;
-  attr[0].val.clusterDim.z = 1;
+  cudaLaunchAttribute attr[1];
   // may start while the state pass ahead of it finishes (see launch_pdl)
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 2;
+  cfg.numAttrs = 1;
   {
     LaunchScope ls("bwd_tc", p.stream);
-    e = cudaLaunchKernelEx(&cfg, k_bwd_tc, maps, tc_dims(p), nsub, p.dt, p.A, p.D, p.ddt,
-                           p.dA_part, p.dD_part, p.dB, p.dC, p.dA, p.dD, p.ticket);
+    e = cudaLaunchKernelEx(&cfg, k_bwd_tc, maps, tc_dims(p), nitems, p.dt, p.A, p.D, p.ddt,
+                           p.dA_part, p.dD_part, p.dB, p.dC, p.dA, p.dD, p.tickets, p.bwd_part);
   }
   if (e != cudaSuccess) return e;
   return cudaGetLastError();

@@ -1152,7 +1152,7 @@ k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, long long nitems,
     {
       const int jc = wg;
       if (jc <= q) {  // warp-uniform
-#pragma unroll
+#pragma unroll 1
         for (int hf = 0; hf < 2; ++hf) {
           const int col0 = jc * 32 + hf * 16;
           float cb[16], xy[16], wv[16];

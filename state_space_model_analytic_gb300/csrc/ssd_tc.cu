@@ -429,20 +429,8 @@ k_state_scan_tc(const __grid_constant__ ScanStateMaps maps, TcDims d, const floa
     float dv[2], dv_next[2] = {0.f, 0.f};
     load_dt(0, dv);
     if (nc > 1) load_dt(1, dv_next);
-    uint8_t* sRows2 = sm + 2 * stage_bytes + 16384;  // MODE 1: [128 rows n][64 p] bf16, SW128
-    if (MODE == 1 && pt == 0) prefetch_tmap(&maps.rows2);
     for (int it = 0; it < nc; ++it) {
       const int k = it & 1;
-      // MODE 1: H_{c-1} from the fp32 history, 16-byte loads: this thread takes
-      // p in [16 pw, 16 pw + 16) of rows n = 4 lane .. 4 lane + 3; stored as
-      // bf16 rows after the scaling
-      float4 hv[16];
-      if (MODE == 1) {
-        const float* hsrc = hist + (((size_t)b * nc + chunk_of(it)) * d.H + h) * PN +
-                            (size_t)(16 * pw) * d.N + 4 * lane;
-#pragma unroll
-        for (int pp = 0; pp < 16; ++pp) hv[pp] = *(const float4*)(hsrc + (size_t)pp * d.N);
-      }
       // ---- decay tables: chunk-local inclusive cumsum of dt * A (log2 units)
       const float x0 = dv[0] * a2, x1 = dv[1] * a2;
       float run = x0 + x1;
@@ -494,29 +482,6 @@ k_state_scan_tc(const __grid_constant__ ScanStateMaps maps, TcDims d, const floa
       fence_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar_scaled[k]);  // s_lastq too (release)
-      if (MODE == 1) {  // hT[c] = H_{c-1} as bf16 row n = pt, through the staging tile
-        if (pt == 0) bulk_wait_read0();
-        named_sync(1, 128);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {  // row n = 4 lane + i: chunks 2 pw, 2 pw + 1
-          float v8[8];
-#pragma unroll
-          for (int half = 0; half < 2; ++half) {
-#pragma unroll
-            for (int t = 0; t < 8; ++t) {
-              const float4 f = hv[8 * half + t];
-              v8[t] = i == 0 ? f.x : i == 1 ? f.y : i == 2 ? f.z : f.w;
-            }
-            store_row_bf16(sRows2, 4 * lane + i, 2 * pw + half, v8);
-          }
-        }
-        fence_async_smem();
-        named_sync(1, 128);
-        if (pt == 0) {
-          tma_store_2d(&maps.rows2, sRows2, 0, ((b * nc + chunk_of(it)) * d.H + h) * d.N);
-          bulk_commit();
-        }
-      }
     }
     if (pt == 0) bulk_wait0();
   } else {
@@ -525,7 +490,11 @@ k_state_scan_tc(const __grid_constant__ ScanStateMaps maps, TcDims d, const floa
     const int n = tid, q = tid >> 5;
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
     uint8_t* sRows = sm + 2 * stage_bytes;  // [128 rows n][64 p] bf16, SW128
-    if (tid == 0) prefetch_tmap(&maps.rows);
+    uint8_t* sRows2 = sRows + 16384;         // MODE 1: the same for H_{c-1}
+    if (tid == 0) {
+      prefetch_tmap(&maps.rows);
+      if (MODE == 1) prefetch_tmap(&maps.rows2);
+    }
     // 64 values of row n as bf16 into the staging tile, then one TMA store of
     // the tile to rows [srow, srow + 128) (the tile is free again once the
     // previous store has read it)
@@ -560,6 +529,37 @@ k_state_scan_tc(const __grid_constant__ ScanStateMaps maps, TcDims d, const floa
         for (int p = 0; p < 64; ++p) hblk[(size_t)p * d.N] = st[p];
       }
       put_rows(st, &maps.rows, srow);  // MODE 0: hT[c] = H_{c-1}; MODE 1: gT[c] = g_c
+      if (MODE == 1) {
+        // hT[c] = H_{c-1} from the fp32 history as bf16 rows, while the product
+        // is in flight: this thread takes p in [16 q, 16 q + 16) of rows
+        // n = 4 lane .. 4 lane + 3 (16-byte loads, coalesced over the lanes)
+        const float* hsrc = hist + (((size_t)b * nc + c) * d.H + h) * PN + (size_t)(16 * q) * d.N +
+                            4 * (tid & 31);
+        float4 hv[16];
+#pragma unroll
+        for (int pp = 0; pp < 16; ++pp) hv[pp] = *(const float4*)(hsrc + (size_t)pp * d.N);
+        if (tid == 0) bulk_wait_read0();  // the previous store of sRows2 has read it
+        named_sync(2, 128);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          float v8[8];
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+              const float4 f = hv[8 * half + t];
+              v8[t] = i == 0 ? f.x : i == 1 ? f.y : i == 2 ? f.z : f.w;
+            }
+            store_row_bf16(sRows2, 4 * (tid & 31) + i, 2 * q + half, v8);
+          }
+        }
+        fence_async_smem();
+        named_sync(2, 128);
+        if (tid == 0) {
+          tma_store_2d(&maps.rows2, sRows2, 0, srow);
+          bulk_commit();
+        }
+      }
       ok = __all_sync(0xffffffffu, wait_ws(&bar_full[buf], (it / kScanBufs) & 1, &s_abort));
       // warp-uniform; the other consumer warps still reach the named barriers
       if (ok) {

@@ -180,3 +180,83 @@ def test_tensor_core_and_simt_paths_agree(q):
         assert rel_err(simt[k], ref[k]) < TOL["bf16"], k
         assert rel_err(tc[k], simt[k]) < TOL["bf16"], k
     nat.check(nat.lib().ssd_device_status())
+
+
+def test_graph_replay_and_side_stream_match_eager_bitwise():
+    """The forward + backward API calls captured in a CUDA graph (as the
+    benchmark replays them) and the same calls on a side stream give the
+    eager results bit for bit, on the tensor-core path."""
+    import torch
+    import state_space_model_analytic_gb300 as ssd
+    dims = synth.Dims(2, 1024, 8, 64, 128, 2, 256, "bf16")
+    inp = synth.make_inputs(dims, 17, True, "softplus")
+    dev = to_device(dims, inp)
+    Q = dims.chunk
+    cd = ssd.dims_of(dev["x"], dev["B"], Q)
+    ws_f = ssd.alloc_workspace(cd, 0, dev["x"].device)
+    ws_b = ssd.alloc_workspace(cd, 1, dev["x"].device)
+
+    def buffers():
+        y = torch.empty_like(dev["x"])
+        fo = {"y": y, "final_state": torch.empty_like(dev["h0"]),
+              "chunk_states": torch.empty(2, 1024 // Q, 8, 64, 128, device="cuda")}
+        bo = {"dx": torch.empty_like(dev["x"]), "ddt": torch.empty_like(dev["dt"]),
+              "dA": torch.empty_like(dev["A"]), "dB": torch.empty_like(dev["B"]),
+              "dC": torch.empty_like(dev["C"]), "dD": torch.empty_like(dev["D"]),
+              "dh0": torch.empty_like(dev["h0"])}
+        return fo, bo
+
+    def step(fo, bo):
+        ssd.forward(dev["x"], dev["dt"], dev["A"], dev["B"], dev["C"], dev["D"], dev["h0"],
+                    chunk=Q, out=fo, workspace=ws_f)
+        ssd.backward(dev["x"], dev["dt"], dev["A"], dev["B"], dev["C"], dev["D"], dev["h0"],
+                     dev["dy"], fo["chunk_states"], chunk=Q, out=bo, workspace=ws_b)
+
+    ref_f, ref_b = buffers()
+    step(ref_f, ref_b)
+    torch.cuda.synchronize()
+
+    g_f, g_b = buffers()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step(g_f, g_b)
+    for _ in range(2):
+        graph.replay()
+    torch.cuda.synchronize()
+
+    s_f, s_b = buffers()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step(s_f, s_b)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    for name, ref in list(ref_f.items()) + list(ref_b.items()):
+        other_g = g_f.get(name, g_b.get(name))
+        other_s = s_f.get(name, s_b.get(name))
+        assert torch.equal(ref, other_g), name
+        assert torch.equal(ref, other_s), name
+
+
+@pytest.mark.parametrize("q", [128, 256])
+def test_optional_outputs_absent_on_tensor_core_path(q):
+    """No final state, no returned history (the forward keeps it in its
+    workspace) and no dh0: the outputs that remain match the full call."""
+    import torch
+    import state_space_model_analytic_gb300 as ssd
+    dims = synth.Dims(1, 512, 8, 64, 128, 1, q, "bf16")
+    inp = synth.make_inputs(dims, 23, True, "softplus")
+    dev = to_device(dims, inp)
+    y, fs, cs = ssd.forward(dev["x"], dev["dt"], dev["A"], dev["B"], dev["C"], dev["D"],
+                            dev["h0"], chunk=q)
+    g = ssd.backward(dev["x"], dev["dt"], dev["A"], dev["B"], dev["C"], dev["D"], dev["h0"],
+                     dev["dy"], cs, chunk=q)
+    y2, fs2, cs2 = ssd.forward(dev["x"], dev["dt"], dev["A"], dev["B"], dev["C"], dev["D"],
+                               dev["h0"], chunk=q, want_final=False, want_states=False)
+    g2 = ssd.backward(dev["x"], dev["dt"], dev["A"], dev["B"], dev["C"], dev["D"], dev["h0"],
+                      dev["dy"], None, chunk=q, want_dh0=False)
+    torch.cuda.synchronize()
+    assert fs2 is None and cs2 is None and g2["dh0"] is None
+    assert torch.equal(y, y2)
+    for k in ("dx", "ddt", "dA", "dB", "dC", "dD"):
+        assert torch.equal(g[k], g2[k]), k

@@ -80,8 +80,9 @@ typedef struct {
 
 /* Bytes of device workspace needed for these dims.  which = 0: ssd_forward;
  * 1: ssd_backward given the chunk history; 2: ssd_backward with
- * chunk_states = NULL (history recomputed inside the call).  Returns 0 for
- * dims the library rejects (ssd_last_error then says why). */
+ * chunk_states = NULL (history recomputed inside the call); 3, 4, 5: the same
+ * three for ssd_forward_raw / ssd_backward_raw.  Returns 0 for dims the
+ * library rejects (ssd_last_error then says why). */
 SSD_API size_t ssd_workspace_bytes(const ssd_dims* dims, int which);
 
 /*
@@ -116,6 +117,35 @@ SSD_API int ssd_backward(const ssd_dims* dims,
                          void* dx, float* ddt, float* dA, void* dB, void* dC, float* dD,
                          float* dh0,
                          void* workspace, size_t workspace_bytes, void* cuda_stream);
+
+/*
+ * The core with the dt and A preprocessing in front of it
+ * (burn_dragon_kernel 0.5.0, src/sequence/mamba2/backward.rs,
+ * `tensorized_mamba2_backward_impl`, where dt = softplus(dt_raw + dt_bias)
+ * per head and A = -exp(a_log); its backward multiplies the gradient w.r.t.
+ * dt by sigmoid(dt_raw + dt_bias) and sums it over batch and time for
+ * dt_bias; `ssd_backward_reference` gives the gradient w.r.t. a_log as the
+ * summed gradient w.r.t. A times -exp(a_log)).
+ *   dt_raw, d_dt_raw   [B][T][H] fp32
+ *   dt_bias, a_log, d_dt_bias, d_a_log   [H] fp32
+ * Every other argument, layout, error and rule is that of ssd_forward /
+ * ssd_backward; the workspace is ssd_workspace_bytes(dims, 3) (forward), 4
+ * (backward given the history) or 5 (backward recomputing it).  The history
+ * written by ssd_forward_raw is the core's history for dt and A.
+ */
+SSD_API int ssd_forward_raw(const ssd_dims* dims,
+                            const void* x, const float* dt_raw, const float* dt_bias,
+                            const float* a_log, const void* B, const void* C, const float* D,
+                            const float* h0,
+                            void* y, float* final_state, float* chunk_states,
+                            void* workspace, size_t workspace_bytes, void* cuda_stream);
+SSD_API int ssd_backward_raw(const ssd_dims* dims,
+                             const void* x, const float* dt_raw, const float* dt_bias,
+                             const float* a_log, const void* B, const void* C, const float* D,
+                             const float* h0, const void* dy, const float* chunk_states,
+                             void* dx, float* d_dt_raw, float* d_dt_bias, float* d_a_log,
+                             void* dB, void* dC, float* dD, float* dh0,
+                             void* workspace, size_t workspace_bytes, void* cuda_stream);
 
 /*
  * Forward pass that allocates nothing (no counterpart on the pages: an

@@ -19,7 +19,8 @@ SSD_OK, SSD_ERR_INVALID_ARG, SSD_ERR_UNSUPPORTED, SSD_ERR_ALIGNMENT, SSD_ERR_CUD
 EXPORTS = ("ssd_workspace_bytes", "ssd_forward", "ssd_backward", "ssd_last_error",
            "ssd_kernel_launch_count", "ssd_trace_begin", "ssd_trace_end", "ssd_trace_read",
            "ssd_trace_reset", "ssd_kernel_path", "ssd_force_kernel_path", "ssd_device_status",
-           "ssd_selftest_wait_timeout", "ssd_forward_noalloc")
+           "ssd_selftest_wait_timeout", "ssd_forward_noalloc", "ssd_forward_raw",
+           "ssd_backward_raw")
 
 
 class SsdDims(ctypes.Structure):
@@ -57,6 +58,10 @@ def lib() -> ctypes.CDLL:
             L.ssd_forward.argtypes = [D] + [_VP] * 11 + [ctypes.c_size_t, _VP]
             L.ssd_backward.restype = ctypes.c_int
             L.ssd_backward.argtypes = [D] + [_VP] * 17 + [ctypes.c_size_t, _VP]
+            L.ssd_forward_raw.restype = ctypes.c_int
+            L.ssd_forward_raw.argtypes = [D] + [_VP] * 12 + [ctypes.c_size_t, _VP]
+            L.ssd_backward_raw.restype = ctypes.c_int
+            L.ssd_backward_raw.argtypes = [D] + [_VP] * 19 + [ctypes.c_size_t, _VP]
             L.ssd_last_error.restype = ctypes.c_char_p
             L.ssd_last_error.argtypes = []
             L.ssd_kernel_launch_count.restype = ctypes.c_uint64

@@ -140,3 +140,80 @@ def backward(x, dt, A, B, C, D, h0, dy, chunk_states=None, *, chunk: int, want_d
                                 workspace.numel(), _stream_handle(stream))
     nat.check(rc)
     return g
+
+
+def _check_raw(x, dt_raw, dt_bias, a_log):
+    Bz, T, H, _ = x.shape
+    dev = x.device
+    _check("dt_raw", dt_raw, torch.float32, (Bz, T, H), dev)
+    _check("dt_bias", dt_bias, torch.float32, (H,), dev)
+    _check("a_log", a_log, torch.float32, (H,), dev)
+
+
+def forward_raw(x, dt_raw, dt_bias, a_log, B, C, D, h0=None, *, chunk: int, want_final=True,
+                want_states=True, out=None, workspace=None, stream=None):
+    """The core with dt = softplus(dt_raw + dt_bias) and A = -exp(a_log)
+    computed on the device.  Returns (y, final_state or None, chunk_states or None)."""
+    if not x.is_cuda:
+        raise ValueError("inputs must be CUDA tensors (no CPU path exists)")
+    _check_raw(x, dt_raw, dt_bias, a_log)
+    _validate_inputs(x, dt_raw, dt_bias, B, C, D, h0)
+    dims = dims_of(x, B, chunk)
+    Bz, T, H, P = x.shape
+    N = B.shape[3]
+    dev = x.device
+    out = {} if out is None else out
+    y = out.get("y")
+    if y is None:
+        y = torch.empty_like(x)
+    fs = out.get("final_state")
+    if fs is None and want_final:
+        fs = torch.empty(Bz, H, P, N, dtype=torch.float32, device=dev)
+    cs = out.get("chunk_states")
+    if cs is None and want_states:
+        cs = torch.empty(Bz, T // chunk, H, P, N, dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = alloc_workspace(dims, 3, dev)
+    rc = nat.lib().ssd_forward_raw(dims, _ptr(x), _ptr(dt_raw), _ptr(dt_bias), _ptr(a_log),
+                                   _ptr(B), _ptr(C), _ptr(D), _ptr(h0), _ptr(y), _ptr(fs),
+                                   _ptr(cs), _ptr(workspace), workspace.numel(),
+                                   _stream_handle(stream))
+    nat.check(rc)
+    return y, fs, cs
+
+
+def backward_raw(x, dt_raw, dt_bias, a_log, B, C, D, h0, dy, chunk_states=None, *, chunk: int,
+                 want_dh0=True, out=None, workspace=None, stream=None):
+    """Gradients of sum(dy * y) for the raw-dt form: dict dx, d_dt_raw,
+    d_dt_bias, d_a_log, dB, dC, dD, dh0 (or None)."""
+    if not x.is_cuda:
+        raise ValueError("inputs must be CUDA tensors (no CPU path exists)")
+    _check_raw(x, dt_raw, dt_bias, a_log)
+    _validate_inputs(x, dt_raw, dt_bias, B, C, D, h0, dy)
+    dims = dims_of(x, B, chunk)
+    Bz, T, H, P = x.shape
+    N = B.shape[3]
+    dev = x.device
+    if chunk_states is not None:
+        _check("chunk_states", chunk_states, torch.float32, (Bz, T // chunk, H, P, N), dev)
+    g = dict(out) if out is not None else {}
+    g.setdefault("dx", torch.empty_like(x))
+    g.setdefault("d_dt_raw", torch.empty_like(dt_raw))
+    g.setdefault("d_dt_bias", torch.empty_like(dt_bias))
+    g.setdefault("d_a_log", torch.empty_like(a_log))
+    g.setdefault("dB", torch.empty_like(B))
+    g.setdefault("dC", torch.empty_like(C))
+    g.setdefault("dD", torch.empty_like(D))
+    if want_dh0:
+        g.setdefault("dh0", torch.empty(Bz, H, P, N, dtype=torch.float32, device=dev))
+    else:
+        g["dh0"] = None
+    if workspace is None:
+        workspace = alloc_workspace(dims, 4 if chunk_states is not None else 5, dev)
+    rc = nat.lib().ssd_backward_raw(
+        dims, _ptr(x), _ptr(dt_raw), _ptr(dt_bias), _ptr(a_log), _ptr(B), _ptr(C), _ptr(D),
+        _ptr(h0), _ptr(dy), _ptr(chunk_states), _ptr(g["dx"]), _ptr(g["d_dt_raw"]),
+        _ptr(g["d_dt_bias"]), _ptr(g["d_a_log"]), _ptr(g["dB"]), _ptr(g["dC"]), _ptr(g["dD"]),
+        _ptr(g["dh0"]), _ptr(workspace), workspace.numel(), _stream_handle(stream))
+    nat.check(rc)
+    return g

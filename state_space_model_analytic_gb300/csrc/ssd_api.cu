@@ -183,6 +183,14 @@ size_t carve(Problem* p, char* base, int which) {
   return off;
 }
 
+// Workspace in front of the core's for ssd_forward_raw / ssd_backward_raw:
+// dt [B][T][H] fp32, then A [H] fp32, then the per-slice dt_bias sums
+// [kDtPostSlices][H] fp32 of the backward.
+size_t raw_extra_bytes(const Problem& p) {
+  return up((size_t)p.B * p.T * p.H * sizeof(float)) + up((size_t)p.H * sizeof(float)) +
+         up((size_t)kDtPostSlices * p.H * sizeof(float));
+}
+
 int check_smem(const Problem& p) {
   if (simt_smem_need(p) > 227 * 1024)
     return fail(SSD_ERR_UNSUPPORTED, "shape needs %zu bytes of shared memory per block",
@@ -268,9 +276,10 @@ int ssd_trace_read(int index, char* name, int name_len, double* total_ms, int* l
 uint64_t ssd_kernel_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
 size_t ssd_workspace_bytes(const ssd_dims* dims, int which) {
-  if (validate(dims) != SSD_OK || which < 0 || which > 2) return 0;
+  if (validate(dims) != SSD_OK || which < 0 || which > 5) return 0;
   Problem p = base_problem(dims);
-  return carve(&p, nullptr, which);
+  // 3..5: the raw-dt entry points, dt and A in front of the core's workspace
+  return (which >= 3 ? raw_extra_bytes(p) : 0) + carve(&p, nullptr, which % 3);
 }
 
 int ssd_force_kernel_path(int path) {
@@ -391,6 +400,77 @@ int ssd_backward(const ssd_dims* dims, const void* x, const float* dt, const flo
   }
   e = tc_backward_supported(p) ? tc_backward(p) : simt_backward(p);
   if (e != cudaSuccess) return cuda_fail(e, "backward kernels");
+  return SSD_OK;
+}
+
+// ---- dt and A preprocessing in front of the core (ssd_dtprep.cu) ----------
+
+int ssd_forward_raw(const ssd_dims* dims, const void* x, const float* dt_raw, const float* dt_bias,
+                    const float* a_log, const void* B, const void* C, const float* D,
+                    const float* h0, void* y, float* final_state, float* chunk_states,
+                    void* workspace, size_t workspace_bytes, void* cuda_stream) {
+  g_err.clear();
+  int rc = validate(dims);
+  if (rc) return rc;
+  if (!x || !dt_raw || !dt_bias || !a_log || !B || !C || !D || !y || !workspace)
+    return fail(SSD_ERR_INVALID_ARG, "ssd_forward_raw: a required pointer is NULL");
+  const void* ptrs[] = {x, dt_raw, dt_bias, a_log, B, C, D, h0, y, final_state, chunk_states};
+  for (const void* q : ptrs)
+    if (q && !aligned16(q)) return fail(SSD_ERR_ALIGNMENT, "ssd_forward_raw: pointer %p is not 16-byte aligned", q);
+  if (((uintptr_t)workspace & 255u) != 0)
+    return fail(SSD_ERR_ALIGNMENT, "ssd_forward_raw: workspace must be 256-byte aligned");
+  Problem p = base_problem(dims);
+  if ((rc = check_smem(p))) return rc;
+  const size_t need = ssd_workspace_bytes(dims, 3), extra = raw_extra_bytes(p);
+  if (workspace_bytes < need)
+    return fail(SSD_ERR_INVALID_ARG, "ssd_forward_raw: workspace %zu bytes < %zu needed",
+                workspace_bytes, need);
+  float* dt = (float*)workspace;
+  float* A = (float*)((char*)workspace + up((size_t)p.B * p.T * p.H * sizeof(float)));
+  p.stream = (cudaStream_t)cuda_stream;
+  cudaError_t e = dt_prep(p, dt_raw, dt_bias, a_log, dt, A);
+  if (e != cudaSuccess) return cuda_fail(e, "dt preprocessing kernel");
+  return ssd_forward(dims, x, dt, A, B, C, D, h0, y, final_state, chunk_states,
+                     (char*)workspace + extra, workspace_bytes - extra, cuda_stream);
+}
+
+int ssd_backward_raw(const ssd_dims* dims, const void* x, const float* dt_raw,
+                     const float* dt_bias, const float* a_log, const void* B, const void* C,
+                     const float* D, const float* h0, const void* dy, const float* chunk_states,
+                     void* dx, float* d_dt_raw, float* d_dt_bias, float* d_a_log, void* dB,
+                     void* dC, float* dD, float* dh0, void* workspace, size_t workspace_bytes,
+                     void* cuda_stream) {
+  g_err.clear();
+  int rc = validate(dims);
+  if (rc) return rc;
+  if (!x || !dt_raw || !dt_bias || !a_log || !B || !C || !D || !dy || !dx || !d_dt_raw ||
+      !d_dt_bias || !d_a_log || !dB || !dC || !dD || !workspace)
+    return fail(SSD_ERR_INVALID_ARG, "ssd_backward_raw: a required pointer is NULL");
+  const void* ptrs[] = {x, dt_raw, dt_bias, a_log, B, C, D, h0, dy, chunk_states, dx,
+                        d_dt_raw, d_dt_bias, d_a_log, dB, dC, dD, dh0};
+  for (const void* q : ptrs)
+    if (q && !aligned16(q)) return fail(SSD_ERR_ALIGNMENT, "ssd_backward_raw: pointer %p is not 16-byte aligned", q);
+  if (((uintptr_t)workspace & 255u) != 0)
+    return fail(SSD_ERR_ALIGNMENT, "ssd_backward_raw: workspace must be 256-byte aligned");
+  Problem p = base_problem(dims);
+  if ((rc = check_smem(p))) return rc;
+  const size_t need = ssd_workspace_bytes(dims, chunk_states ? 4 : 5), extra = raw_extra_bytes(p);
+  if (workspace_bytes < need)
+    return fail(SSD_ERR_INVALID_ARG, "ssd_backward_raw: workspace %zu bytes < %zu needed%s",
+                workspace_bytes, need, chunk_states ? "" : " (recomputing chunk states)");
+  float* dt = (float*)workspace;
+  float* A = (float*)((char*)workspace + up((size_t)p.B * p.T * p.H * sizeof(float)));
+  p.stream = (cudaStream_t)cuda_stream;
+  cudaError_t e = dt_prep(p, dt_raw, dt_bias, a_log, dt, A);
+  if (e != cudaSuccess) return cuda_fail(e, "dt preprocessing kernel");
+  // the core writes ddt into d_dt_raw and dA into d_a_log; the post kernel
+  // turns them into the gradients w.r.t. dt_raw, dt_bias and a_log in place
+  rc = ssd_backward(dims, x, dt, A, B, C, D, h0, dy, chunk_states, dx, d_dt_raw, d_a_log, dB, dC,
+                    dD, dh0, (char*)workspace + extra, workspace_bytes - extra, cuda_stream);
+  if (rc) return rc;
+  float* part = (float*)((char*)A + up((size_t)p.H * sizeof(float)));
+  e = dt_post(p, dt_raw, dt_bias, a_log, d_dt_raw, d_dt_bias, d_a_log, part);
+  if (e != cudaSuccess) return cuda_fail(e, "dt gradient kernel");
   return SSD_OK;
 }
 

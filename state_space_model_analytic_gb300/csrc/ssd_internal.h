@@ -69,6 +69,17 @@ cudaError_t simt_reduce_heads(const Problem& p, int n_a, int n_d);
 
 void count_launch(int n = 1);
 
+// dt = softplus(dt_raw + dt_bias), A = -exp(a_log) for the core kernels, and
+// the chain rule back to dt_raw, dt_bias and a_log (ssd_dtprep.cu).
+cudaError_t dt_prep(const Problem& p, const float* dt_raw, const float* dt_bias,
+                    const float* a_log, float* dt, float* A);
+// slices of the (b, t) rows in the dt gradient pass; part holds
+// kDtPostSlices * H floats of per-slice sums
+constexpr int kDtPostSlices = 32;
+cudaError_t dt_post(const Problem& p, const float* dt_raw, const float* dt_bias,
+                    const float* a_log, float* d_dt_raw, float* d_dt_bias, float* d_a_log,
+                    float* part);
+
 // Per-kernel event trace (see ssd_trace_begin in include/ssd.h).  A
 // LaunchScope brackets exactly one kernel launch: it records the start event
 // (when a trace is open), and on destruction the end event plus the launch

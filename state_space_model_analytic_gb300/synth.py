@@ -106,7 +106,9 @@ def make_inputs(dims: Dims, seed: int, has_h0: bool, dt_mode: str = "softplus",
     """Draw one problem.  Returns float64 arrays holding storage-rounded values.
 
     Keys: x [B,T,H,P], dt [B,T,H], A [H], B [B,T,G,N], C [B,T,G,N], D [H],
-    h0 [B,H,P,N] or None, dy [B,T,H,P].
+    h0 [B,H,P,N] or None, dy [B,T,H,P]; and the raw parameters the dt and A
+    are drawn through: dt_raw [B,T,H] (None for "decay_span"), dt_bias [H],
+    a_log [H].
     """
     d = dims
     rng = np.random.Generator(np.random.PCG64(seed))
@@ -141,6 +143,9 @@ def make_inputs(dims: Dims, seed: int, has_h0: bool, dt_mode: str = "softplus",
         "D": round_to(D, "f32"),
         "h0": None if h0 is None else round_to(h0, "f32"),
         "dy": None if dy is None else round_to(dy, io),
+        "dt_raw": None if dt_mode == "decay_span" else round_to(0.5 * noise, "f32"),
+        "dt_bias": round_to(dt_bias, "f32"),
+        "a_log": round_to(a_log, "f32"),
     }
 
 

@@ -44,7 +44,11 @@ def test_workspace_sizes(L):
     f, b1, b2 = (L.ssd_workspace_bytes(d, w) for w in (0, 1, 2))
     states = 2 * 4 * 4 * 16 * 16 * 4
     assert f >= states and b1 >= states and b2 >= b1 + states
-    assert L.ssd_workspace_bytes(d, 3) == 0
+    # the raw-dt entry points: dt [B,T,H], A [H] and 32 x H slice sums (each
+    # rounded to 256 bytes) in front
+    extra = 2 * 64 * 4 * 4 + 256 + 512
+    assert [L.ssd_workspace_bytes(d, w) for w in (3, 4, 5)] == [f + extra, b1 + extra, b2 + extra]
+    assert L.ssd_workspace_bytes(d, 6) == 0 and L.ssd_workspace_bytes(d, -1) == 0
     for i in range(5):
         dd = synth.config_dims(i)
         d = nat.make_dims(dd.batch, dd.seqlen, dd.nheads, dd.headdim, dd.dstate, dd.ngroups,
@@ -103,6 +107,24 @@ def test_reserved_and_dtype_fields(L):
     d = dims()
     d.dtype = 7
     assert L.ssd_workspace_bytes(d, 0) == 0
+
+
+def test_raw_entry_points_reject_before_launching(L):
+    d = dims()
+    f = ctypes.c_void_p(1 << 20)
+    ws = L.ssd_workspace_bytes(d, 3)
+    rc = L.ssd_forward_raw(d, f, f, None, f, f, f, f, None, f, None, None, f, ws, None)
+    assert rc == nat.SSD_ERR_INVALID_ARG and "NULL" in nat.last_error()
+    rc = L.ssd_forward_raw(d, f, f, f, f, f, f, f, None, f, None, None, f, ws - 1, None)
+    assert rc == nat.SSD_ERR_INVALID_ARG and "workspace" in nat.last_error()
+    bad = ctypes.c_void_p((1 << 20) + 8)
+    rc = L.ssd_forward_raw(d, f, f, bad, f, f, f, f, None, f, None, None, f, ws, None)
+    assert rc == nat.SSD_ERR_ALIGNMENT
+    wsb = L.ssd_workspace_bytes(d, 4)
+    args = [f] * 20
+    args[7] = None  # h0
+    rc = L.ssd_backward_raw(d, *args[:9], None, *args[10:18], f, wsb, None)
+    assert rc == nat.SSD_ERR_INVALID_ARG and "recomput" in nat.last_error()
 
 
 def test_cpu_tensors_rejected_by_front_end():

@@ -122,10 +122,15 @@ def read_peaks():
     return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
 
 
+# the files holding the device code of the tensor-core kernels: the traffic
+# record applies while they are byte-identical to the captured build
+TC_KERNEL_SOURCES = ("ssd_tc.cu", "tc_util.cuh", "ssd_common.cuh")
+
+
 def source_digest():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "state_space_model_analytic_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    for f in TC_KERNEL_SOURCES:
         h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 

@@ -534,6 +534,62 @@ def main():
         except Exception as e:  # noqa: BLE001  (reported, the headline stands)
             raw_line = {"error": f"{type(e).__name__}: {e}"[:200]}
 
+    # ---- the gated RMSNorm after the core on the core's output shape (rows =
+    # B*T, width = H*P): forward and backward timed apart, against HBM
+    norm_line = None
+    try:
+        ninp = synth.norm_inputs(Bz * T, H * P, dims.dtype, 4242)
+        ny, nz, ng = (to(ninp[k], io) for k in ("y", "z", "dout"))
+        nw = to(ninp["weight"], torch.float32)
+        nws = torch.empty(nat.lib().ssd_rmsnorm_gated_workspace_bytes(Bz * T, H * P),
+                          dtype=torch.uint8, device=dev)
+        n_out = torch.empty_like(ny)
+        n_inv = torch.empty(Bz * T, device=dev)
+        n_gr = {"dy": torch.empty_like(ny), "dz": torch.empty_like(nz), "dweight": torch.empty_like(nw)}
+        rows_, width_ = Bz * T, H * P
+        dtc = 1 if dims.dtype == "bf16" else 0
+        p_ = lambda t_: t_.data_ptr()
+
+        def nfwd():
+            nat.check(nat.lib().ssd_rmsnorm_gated_forward(
+                rows_, width_, dtc, p_(ny), p_(nz), p_(nw), 1e-5, p_(n_out), p_(n_inv),
+                stream.cuda_stream or None))
+
+        def nbwd():
+            nat.check(nat.lib().ssd_rmsnorm_gated_backward(
+                rows_, width_, dtc, p_(ny), p_(nz), p_(nw), 1e-5, p_(n_inv), p_(ng),
+                p_(n_gr["dy"]), p_(n_gr["dz"]), p_(n_gr["dweight"]), p_(nws), nws.numel(),
+                stream.cuda_stream or None))
+
+        def timed(fn, n=200):
+            for _ in range(args.warmup):
+                fn()
+                flush.fill_(1.0)
+            torch.cuda.synchronize()
+            evn = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(n)]
+            for i in range(n):
+                evn[i][0].record(stream)
+                fn()
+                evn[i][1].record(stream)
+                flush.fill_(float(i))
+            torch.cuda.synchronize()
+            return sum(a.elapsed_time(b) for a, b in evn) / n
+
+        f_ms, b_ms = timed(nfwd), timed(nbwd)
+        esz = 2 if dims.dtype == "bf16" else 4
+        f_bytes = 3 * rows_ * width_ * esz + 4 * rows_ + 4 * width_
+        b_bytes = 5 * rows_ * width_ * esz + 4 * rows_ + 8 * width_
+        hbm_, _, _ = read_peaks()
+        norm_line = {"rows": rows_, "width": width_, "dtype": dims.dtype, "eps": 1e-5,
+                     "fwd_us": 1e3 * f_ms, "bwd_us": 1e3 * b_ms,
+                     "fwd_algorithmic_bytes": f_bytes, "bwd_algorithmic_bytes": b_bytes,
+                     "fwd_frac_of_hbm": f_bytes / (f_ms / 1e3) / 1e9 / hbm_,
+                     "bwd_frac_of_hbm": b_bytes / (b_ms / 1e3) / 1e9 / hbm_,
+                     "timing": "CUDA events per call, L2 flushed between calls"}
+    except Exception as e:  # noqa: BLE001  (reported, the headline stands)
+        norm_line = {"error": f"{type(e).__name__}: {e}"[:200]}
+
     if graph_ms is not None:
         ms_max, value = aggregate_ranks(graph_ms, tokens, dist, dev)
         clk = clk_g if rank == 0 else clk
@@ -595,7 +651,7 @@ def main():
                    "launch": launch_mode},
         "roofline": roofline, "step_roofline": step_roof, "kernels": kernels,
         "gpu_launches": launches, "wall_s_timed": wall,
-        "eager_ms_per_step": eager_max, "raw_dt_step": raw_line,
+        "eager_ms_per_step": eager_max, "raw_dt_step": raw_line, "rmsnorm_gated": norm_line,
         "clocks": clk, "cpu_baseline": cpu, "e2e": e2e,
     }
     print(json.dumps(line), flush=True)

@@ -148,6 +148,35 @@ SSD_API int ssd_backward_raw(const ssd_dims* dims,
                              void* workspace, size_t workspace_bytes, void* cuda_stream);
 
 /*
+ * Gated RMSNorm, the step after the core (burn_dragon_kernel 0.5.0,
+ * src/sequence/mamba2/backward.rs, `rmsnorm_gated_forward_from_inv_rms` and
+ * `rmsnorm_gated_backward_from_inv_rms`; inv_rms as
+ * `tensorized_mamba2_backward_impl` forms it), on `rows` rows of `width`
+ * (for the SSD output: rows = B*T, width = H*P):
+ *   inv_rms[r] = 1 / sqrt(mean_w y[r][w]^2 + eps)
+ *   out[r][w]  = y[r][w] * inv_rms[r] * weight[w] * silu(z[r][w])
+ * The backward returns dy, dz and dweight (summed over the rows) for the
+ * gradient dout of out; inv_rms may be the forward's (NULL = recomputed).
+ *   y, z, out, dout, dy, dz   [rows][width]   `dtype` (ssd_dtype)
+ *   weight, dweight           [width]         fp32
+ *   inv_rms                   [rows]          fp32
+ * width: a multiple of 256 (bf16) or 128 (fp32), at most 4096.  Pointers
+ * 16-byte aligned; the backward's workspace is
+ * ssd_rmsnorm_gated_workspace_bytes(rows, width) bytes (0 = rejected).
+ * Errors as for ssd_forward; results are deterministic (fixed-order sums).
+ */
+SSD_API size_t ssd_rmsnorm_gated_workspace_bytes(int64_t rows, int64_t width);
+SSD_API int ssd_rmsnorm_gated_forward(int64_t rows, int64_t width, int32_t dtype,
+                                      const void* y, const void* z, const float* weight,
+                                      float eps, void* out, float* inv_rms, void* cuda_stream);
+SSD_API int ssd_rmsnorm_gated_backward(int64_t rows, int64_t width, int32_t dtype,
+                                       const void* y, const void* z, const float* weight,
+                                       float eps, const float* inv_rms, const void* dout,
+                                       void* dy, void* dz, float* dweight,
+                                       void* workspace, size_t workspace_bytes,
+                                       void* cuda_stream);
+
+/*
  * Forward pass that allocates nothing (no counterpart on the pages: an
  * addition of this library for callers that cannot allocate).
  * Same inputs, outputs, layouts and errors as ssd_forward, but no workspace

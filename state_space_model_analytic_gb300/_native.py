@@ -20,7 +20,8 @@ EXPORTS = ("ssd_workspace_bytes", "ssd_forward", "ssd_backward", "ssd_last_error
            "ssd_kernel_launch_count", "ssd_trace_begin", "ssd_trace_end", "ssd_trace_read",
            "ssd_trace_reset", "ssd_kernel_path", "ssd_force_kernel_path", "ssd_device_status",
            "ssd_selftest_wait_timeout", "ssd_forward_noalloc", "ssd_forward_raw",
-           "ssd_backward_raw")
+           "ssd_backward_raw", "ssd_rmsnorm_gated_workspace_bytes", "ssd_rmsnorm_gated_forward",
+           "ssd_rmsnorm_gated_backward")
 
 
 class SsdDims(ctypes.Structure):
@@ -62,6 +63,16 @@ def lib() -> ctypes.CDLL:
             L.ssd_forward_raw.argtypes = [D] + [_VP] * 12 + [ctypes.c_size_t, _VP]
             L.ssd_backward_raw.restype = ctypes.c_int
             L.ssd_backward_raw.argtypes = [D] + [_VP] * 19 + [ctypes.c_size_t, _VP]
+            _I64, _I32, _F = ctypes.c_int64, ctypes.c_int32, ctypes.c_float
+            L.ssd_rmsnorm_gated_workspace_bytes.restype = ctypes.c_size_t
+            L.ssd_rmsnorm_gated_workspace_bytes.argtypes = [_I64, _I64]
+            L.ssd_rmsnorm_gated_forward.restype = ctypes.c_int
+            L.ssd_rmsnorm_gated_forward.argtypes = [_I64, _I64, _I32, _VP, _VP, _VP, _F, _VP,
+                                                    _VP, _VP]
+            L.ssd_rmsnorm_gated_backward.restype = ctypes.c_int
+            L.ssd_rmsnorm_gated_backward.argtypes = [_I64, _I64, _I32, _VP, _VP, _VP, _F, _VP,
+                                                     _VP, _VP, _VP, _VP, _VP, ctypes.c_size_t,
+                                                     _VP]
             L.ssd_last_error.restype = ctypes.c_char_p
             L.ssd_last_error.argtypes = []
             L.ssd_kernel_launch_count.restype = ctypes.c_uint64

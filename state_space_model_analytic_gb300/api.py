@@ -217,3 +217,52 @@ def backward_raw(x, dt_raw, dt_bias, a_log, B, C, D, h0, dy, chunk_states=None, 
         _ptr(g["dh0"]), _ptr(workspace), workspace.numel(), _stream_handle(stream))
     nat.check(rc)
     return g
+
+
+def rmsnorm_gated_forward(y, z, weight, eps, *, want_inv_rms=True, out=None, stream=None):
+    """Gated RMSNorm over the last dimension: returns (out, inv_rms or None);
+    out = y * inv_rms * weight * silu(z), inv_rms = 1 / sqrt(mean(y^2) + eps)."""
+    if not y.is_cuda:
+        raise ValueError("inputs must be CUDA tensors (no CPU path exists)")
+    width = y.shape[-1]
+    rows = y.numel() // width
+    if y.dtype not in _IO_TYPES:
+        raise TypeError(f"y: unsupported dtype {y.dtype}")
+    _check("z", z, y.dtype, tuple(y.shape), y.device)
+    _check("weight", weight, torch.float32, (width,), y.device)
+    if not y.is_contiguous():
+        raise ValueError("y: must be contiguous")
+    o = torch.empty_like(y) if out is None else out
+    inv = torch.empty(y.shape[:-1], dtype=torch.float32, device=y.device) if want_inv_rms else None
+    rc = nat.lib().ssd_rmsnorm_gated_forward(rows, width, int(_IO_TYPES[y.dtype]), _ptr(y), _ptr(z),
+                                             _ptr(weight), float(eps), _ptr(o), _ptr(inv),
+                                             _stream_handle(stream))
+    nat.check(rc)
+    return o, inv
+
+
+def rmsnorm_gated_backward(y, z, weight, eps, dout, inv_rms=None, *, workspace=None, stream=None):
+    """Gradients of sum(dout * out): dict dy, dz, dweight."""
+    if not y.is_cuda:
+        raise ValueError("inputs must be CUDA tensors (no CPU path exists)")
+    width = y.shape[-1]
+    rows = y.numel() // width
+    if y.dtype not in _IO_TYPES:
+        raise TypeError(f"y: unsupported dtype {y.dtype}")
+    for name, t in (("z", z), ("dout", dout)):
+        _check(name, t, y.dtype, tuple(y.shape), y.device)
+    _check("weight", weight, torch.float32, (width,), y.device)
+    if inv_rms is not None:
+        _check("inv_rms", inv_rms, torch.float32, tuple(y.shape[:-1]), y.device)
+    g = {"dy": torch.empty_like(y), "dz": torch.empty_like(z), "dweight": torch.empty_like(weight)}
+    if workspace is None:
+        n = nat.lib().ssd_rmsnorm_gated_workspace_bytes(rows, width)
+        if n == 0:
+            raise nat.SsdError(nat.SSD_ERR_UNSUPPORTED, "width rejected")
+        workspace = torch.empty(n, dtype=torch.uint8, device=y.device)
+    rc = nat.lib().ssd_rmsnorm_gated_backward(
+        rows, width, int(_IO_TYPES[y.dtype]), _ptr(y), _ptr(z), _ptr(weight), float(eps),
+        _ptr(inv_rms), _ptr(dout), _ptr(g["dy"]), _ptr(g["dz"]), _ptr(g["dweight"]),
+        _ptr(workspace), workspace.numel(), _stream_handle(stream))
+    nat.check(rc)
+    return g

@@ -474,4 +474,66 @@ int ssd_backward_raw(const ssd_dims* dims, const void* x, const float* dt_raw,
   return SSD_OK;
 }
 
+// ---- gated RMSNorm after the core (ssd_norm.cu) ---------------------------
+
+namespace {
+int norm_check(const char* who, long long rows, long long width, int dtype, float eps) {
+  if (rows < 1) return fail(SSD_ERR_INVALID_ARG, "%s: rows must be >= 1", who);
+  if (dtype != SSD_F32 && dtype != SSD_BF16) return fail(SSD_ERR_INVALID_ARG, "%s: bad dtype", who);
+  const long long unit = dtype == SSD_BF16 ? 256 : 128;  // 32 lanes x 16 bytes
+  if (width < unit || width > 4096 || width % unit != 0)
+    return fail(SSD_ERR_UNSUPPORTED, "%s: width %lld must be a multiple of %lld in [%lld, 4096]",
+                who, width, unit, unit);
+  if (!(eps >= 0.f)) return fail(SSD_ERR_INVALID_ARG, "%s: eps must be >= 0", who);
+  return SSD_OK;
+}
+}  // namespace
+
+size_t ssd_rmsnorm_gated_workspace_bytes(int64_t rows, int64_t width) {
+  if (rows < 1 || width < 1 || width > 4096) return 0;
+  return up((size_t)kNormMaxCtas * width * sizeof(float));
+}
+
+int ssd_rmsnorm_gated_forward(int64_t rows, int64_t width, int32_t dtype, const void* y,
+                              const void* z, const float* weight, float eps, void* out,
+                              float* inv_rms, void* cuda_stream) {
+  g_err.clear();
+  int rc = norm_check("ssd_rmsnorm_gated_forward", rows, width, dtype, eps);
+  if (rc) return rc;
+  if (!y || !z || !weight || !out)
+    return fail(SSD_ERR_INVALID_ARG, "ssd_rmsnorm_gated_forward: a required pointer is NULL");
+  const void* ptrs[] = {y, z, weight, out, inv_rms};
+  for (const void* q : ptrs)
+    if (q && !aligned16(q))
+      return fail(SSD_ERR_ALIGNMENT, "ssd_rmsnorm_gated_forward: pointer %p is not 16-byte aligned", q);
+  cudaError_t e = norm_forward(rows, (int)width, dtype == SSD_BF16, y, z, weight, eps, out, inv_rms,
+                               (cudaStream_t)cuda_stream);
+  if (e != cudaSuccess) return cuda_fail(e, "gated RMSNorm forward kernel");
+  return SSD_OK;
+}
+
+int ssd_rmsnorm_gated_backward(int64_t rows, int64_t width, int32_t dtype, const void* y,
+                               const void* z, const float* weight, float eps,
+                               const float* inv_rms, const void* dout, void* dy, void* dz,
+                               float* dweight, void* workspace, size_t workspace_bytes,
+                               void* cuda_stream) {
+  g_err.clear();
+  int rc = norm_check("ssd_rmsnorm_gated_backward", rows, width, dtype, eps);
+  if (rc) return rc;
+  if (!y || !z || !weight || !dout || !dy || !dz || !dweight || !workspace)
+    return fail(SSD_ERR_INVALID_ARG, "ssd_rmsnorm_gated_backward: a required pointer is NULL");
+  const void* ptrs[] = {y, z, weight, inv_rms, dout, dy, dz, dweight, workspace};
+  for (const void* q : ptrs)
+    if (q && !aligned16(q))
+      return fail(SSD_ERR_ALIGNMENT, "ssd_rmsnorm_gated_backward: pointer %p is not 16-byte aligned", q);
+  const size_t need = ssd_rmsnorm_gated_workspace_bytes(rows, width);
+  if (workspace_bytes < need)
+    return fail(SSD_ERR_INVALID_ARG, "ssd_rmsnorm_gated_backward: workspace %zu bytes < %zu needed",
+                workspace_bytes, need);
+  cudaError_t e = norm_backward(rows, (int)width, dtype == SSD_BF16, y, z, weight, eps, inv_rms,
+                                dout, dy, dz, dweight, (float*)workspace, (cudaStream_t)cuda_stream);
+  if (e != cudaSuccess) return cuda_fail(e, "gated RMSNorm backward kernels");
+  return SSD_OK;
+}
+
 }  // extern "C"

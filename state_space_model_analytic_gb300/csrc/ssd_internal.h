@@ -55,6 +55,16 @@ struct Problem {
   cudaStream_t stream;
 };
 
+// Gated RMSNorm after the core (ssd_norm.cu).  The backward keeps per-CTA
+// column sums of the weight gradient in part[kNormMaxCtas][width].
+constexpr int kNormMaxCtas = 512;
+int norm_bwd_ctas(long long rows);
+cudaError_t norm_forward(long long rows, int width, bool bf16, const void* y, const void* z,
+                         const float* w, float eps, void* out, float* inv_rms, cudaStream_t s);
+cudaError_t norm_backward(long long rows, int width, bool bf16, const void* y, const void* z,
+                          const float* w, float eps, const float* inv_rms, const void* g, void* dy,
+                          void* dz, float* dw, float* part, cudaStream_t s);
+
 // Upper bound on the CTAs of the tensor-core backward (one per SM).
 constexpr size_t kBwdMaxCtas = 160;
 

@@ -176,3 +176,15 @@ def modular_inputs(chunk: int = 16) -> tuple[Dims, dict]:
     f = lambda a: round_to(a, "f32")
     return dims, {"x": f(x), "dt": f(dt), "A": f(-np.exp(a_log)), "B": f(Bm),
                   "C": f(Cm), "D": f(D), "h0": f(h0), "dy": f(dy)}
+
+
+def norm_inputs(rows: int, width: int, dtype: str, seed: int) -> dict:
+    """Gated-RMSNorm inputs: y, z, dout ~ N(0, 1) [rows, width] rounded to the
+    storage type; weight ~ U[0.5, 1.5] [width] fp32."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    y = rng.standard_normal((rows, width))
+    z = rng.standard_normal((rows, width))
+    w = rng.uniform(0.5, 1.5, size=(width,))
+    g = rng.standard_normal((rows, width))
+    return {"y": round_to(y, dtype), "z": round_to(z, dtype), "weight": round_to(w, "f32"),
+            "dout": round_to(g, dtype)}

@@ -590,6 +590,60 @@ def main():
     except Exception as e:  # noqa: BLE001  (reported, the headline stands)
         norm_line = {"error": f"{type(e).__name__}: {e}"[:200]}
 
+    # ---- the causal conv1d + SiLU before the core on the core's xBC (B, T,
+    # C = H*P + 2*G*N, d_conv 4): forward and backward timed apart, against HBM
+    conv_line = None
+    try:
+        Cc, Kc = H * P + 2 * G * N, 4
+        cinp = synth.conv_inputs(Bz, T, Cc, Kc, dims.dtype, 4343)
+        cx, cg = to(cinp["x"], io), to(cinp["dout"], io)
+        cw, cb, ci = (to(cinp[k], torch.float32) for k in ("weight", "bias", "init_state"))
+        c_out = torch.empty_like(cx)
+        c_dx = torch.empty_like(cx)
+        c_dw, c_db = torch.empty_like(cw), torch.empty_like(cb)
+        cws = torch.empty(nat.lib().ssd_conv1d_silu_workspace_bytes(Bz, T, Cc, Kc),
+                          dtype=torch.uint8, device=dev)
+        dtc = 1 if dims.dtype == "bf16" else 0
+        p_ = lambda t_: t_.data_ptr()
+
+        def cfwd():
+            nat.check(nat.lib().ssd_conv1d_silu_forward(Bz, T, Cc, Kc, dtc, p_(cx), p_(cw), p_(cb),
+                                                        p_(ci), p_(c_out), stream.cuda_stream or None))
+
+        def cbwd():
+            nat.check(nat.lib().ssd_conv1d_silu_backward(
+                Bz, T, Cc, Kc, dtc, p_(cx), p_(cw), p_(cb), p_(ci), p_(cg), p_(c_dx), p_(c_dw),
+                p_(c_db), p_(cws), cws.numel(), stream.cuda_stream or None))
+
+        def ctimed(fn, n=200):
+            for _ in range(args.warmup):
+                fn()
+                flush.fill_(1.0)
+            torch.cuda.synchronize()
+            evc = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(n)]
+            for i in range(n):
+                evc[i][0].record(stream)
+                fn()
+                evc[i][1].record(stream)
+                flush.fill_(float(i))
+            torch.cuda.synchronize()
+            return sum(a.elapsed_time(b) for a, b in evc) / n
+
+        cf_ms, cb_ms = ctimed(cfwd), ctimed(cbwd)
+        esz = 2 if dims.dtype == "bf16" else 4
+        cf_bytes = 2 * Bz * T * Cc * esz + 4 * Cc * (Kc + 1) + 4 * Bz * Cc * Kc
+        cb_bytes = 3 * Bz * T * Cc * esz + 4 * Cc * (2 * Kc + 2) + 4 * Bz * Cc * Kc
+        hbm_c, _, _ = read_peaks()
+        conv_line = {"batch": Bz, "seqlen": T, "channels": Cc, "d_conv": Kc, "dtype": dims.dtype,
+                     "fwd_us": 1e3 * cf_ms, "bwd_us": 1e3 * cb_ms,
+                     "fwd_algorithmic_bytes": cf_bytes, "bwd_algorithmic_bytes": cb_bytes,
+                     "fwd_frac_of_hbm": cf_bytes / (cf_ms / 1e3) / 1e9 / hbm_c,
+                     "bwd_frac_of_hbm": cb_bytes / (cb_ms / 1e3) / 1e9 / hbm_c,
+                     "timing": "CUDA events per call, L2 flushed between calls"}
+    except Exception as e:  # noqa: BLE001  (reported, the headline stands)
+        conv_line = {"error": f"{type(e).__name__}: {e}"[:200]}
+
     if graph_ms is not None:
         ms_max, value = aggregate_ranks(graph_ms, tokens, dist, dev)
         clk = clk_g if rank == 0 else clk
@@ -652,6 +706,7 @@ def main():
         "roofline": roofline, "step_roofline": step_roof, "kernels": kernels,
         "gpu_launches": launches, "wall_s_timed": wall,
         "eager_ms_per_step": eager_max, "raw_dt_step": raw_line, "rmsnorm_gated": norm_line,
+        "conv1d_silu": conv_line,
         "clocks": clk, "cpu_baseline": cpu, "e2e": e2e,
     }
     print(json.dumps(line), flush=True)

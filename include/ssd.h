@@ -177,6 +177,38 @@ SSD_API int ssd_rmsnorm_gated_backward(int64_t rows, int64_t width, int32_t dtyp
                                        void* cuda_stream);
 
 /*
+ * Causal depthwise conv1d + SiLU on xBC, the step before the core
+ * (burn_dragon_kernel 0.5.0, src/sequence/mamba2/backward.rs,
+ * `depthwise_conv_preact_with_history` and the fallback conv backward of
+ * `tensorized_mamba2_backward_impl`).  Per batch row and channel c, with the
+ * history h = [init_state (d_conv entries) | x (seqlen entries)]:
+ *   out[t] = silu(bias[c] + sum_{k < d_conv} weight[c][k] * h[t + k + 1])
+ * (h[t + d_conv] = x[t]; init_state NULL = zeros, bias NULL = 0).  The
+ * backward returns dx, dweight and dbias (dbias may be NULL); the gradient
+ * w.r.t. the initial state is not formed, as on the page.
+ *   x, out, dout, dx      [batch][seqlen][channels]   `dtype` (ssd_dtype)
+ *   weight, dweight       [channels][d_conv]          fp32
+ *   bias, dbias           [channels]                  fp32
+ *   init_state            [batch][channels][d_conv]   fp32
+ * channels: a multiple of 8 (bf16) or 4 (fp32); d_conv in [1, 4].  Pointers
+ * 16-byte aligned; the backward's workspace is
+ * ssd_conv1d_silu_workspace_bytes(batch, seqlen, channels, d_conv) bytes.
+ * Errors as for ssd_forward; results are deterministic.
+ */
+SSD_API size_t ssd_conv1d_silu_workspace_bytes(int64_t batch, int64_t seqlen, int64_t channels,
+                                               int32_t d_conv);
+SSD_API int ssd_conv1d_silu_forward(int64_t batch, int64_t seqlen, int64_t channels,
+                                    int32_t d_conv, int32_t dtype, const void* x,
+                                    const float* weight, const float* bias,
+                                    const float* init_state, void* out, void* cuda_stream);
+SSD_API int ssd_conv1d_silu_backward(int64_t batch, int64_t seqlen, int64_t channels,
+                                     int32_t d_conv, int32_t dtype, const void* x,
+                                     const float* weight, const float* bias,
+                                     const float* init_state, const void* dout, void* dx,
+                                     float* dweight, float* dbias,
+                                     void* workspace, size_t workspace_bytes, void* cuda_stream);
+
+/*
  * Forward pass that allocates nothing (no counterpart on the pages: an
  * addition of this library for callers that cannot allocate).
  * Same inputs, outputs, layouts and errors as ssd_forward, but no workspace

@@ -9,14 +9,14 @@ library is missing.
 from .build import build  # noqa: F401
 
 __all__ = ["build", "forward", "backward", "forward_raw", "backward_raw",
-           "rmsnorm_gated_forward", "rmsnorm_gated_backward", "workspace_bytes", "kernel_path",
-           "launch_count"]
+           "rmsnorm_gated_forward", "rmsnorm_gated_backward", "conv1d_silu_forward",
+           "conv1d_silu_backward", "workspace_bytes", "kernel_path", "launch_count"]
 
 
 def __getattr__(name):
     if name in ("forward", "backward", "forward_raw", "backward_raw", "rmsnorm_gated_forward",
-                "rmsnorm_gated_backward", "workspace_bytes", "kernel_path", "launch_count",
-                "alloc_workspace", "dims_of"):
+                "rmsnorm_gated_backward", "conv1d_silu_forward", "conv1d_silu_backward",
+                "workspace_bytes", "kernel_path", "launch_count", "alloc_workspace", "dims_of"):
         from . import api
         return getattr(api, name)
     raise AttributeError(name)

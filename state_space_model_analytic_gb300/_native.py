@@ -21,7 +21,8 @@ EXPORTS = ("ssd_workspace_bytes", "ssd_forward", "ssd_backward", "ssd_last_error
            "ssd_trace_reset", "ssd_kernel_path", "ssd_force_kernel_path", "ssd_device_status",
            "ssd_selftest_wait_timeout", "ssd_forward_noalloc", "ssd_forward_raw",
            "ssd_backward_raw", "ssd_rmsnorm_gated_workspace_bytes", "ssd_rmsnorm_gated_forward",
-           "ssd_rmsnorm_gated_backward")
+           "ssd_rmsnorm_gated_backward", "ssd_conv1d_silu_workspace_bytes", "ssd_conv1d_silu_forward",
+           "ssd_conv1d_silu_backward")
 
 
 class SsdDims(ctypes.Structure):
@@ -69,6 +70,13 @@ def lib() -> ctypes.CDLL:
             L.ssd_rmsnorm_gated_forward.restype = ctypes.c_int
             L.ssd_rmsnorm_gated_forward.argtypes = [_I64, _I64, _I32, _VP, _VP, _VP, _F, _VP,
                                                     _VP, _VP]
+            L.ssd_conv1d_silu_workspace_bytes.restype = ctypes.c_size_t
+            L.ssd_conv1d_silu_workspace_bytes.argtypes = [_I64, _I64, _I64, _I32]
+            L.ssd_conv1d_silu_forward.restype = ctypes.c_int
+            L.ssd_conv1d_silu_forward.argtypes = [_I64, _I64, _I64, _I32, _I32] + [_VP] * 6
+            L.ssd_conv1d_silu_backward.restype = ctypes.c_int
+            L.ssd_conv1d_silu_backward.argtypes = ([_I64, _I64, _I64, _I32, _I32] + [_VP] * 9 +
+                                                   [ctypes.c_size_t, _VP])
             L.ssd_rmsnorm_gated_backward.restype = ctypes.c_int
             L.ssd_rmsnorm_gated_backward.argtypes = [_I64, _I64, _I32, _VP, _VP, _VP, _F, _VP,
                                                      _VP, _VP, _VP, _VP, _VP, ctypes.c_size_t,

@@ -266,3 +266,56 @@ def rmsnorm_gated_backward(y, z, weight, eps, dout, inv_rms=None, *, workspace=N
         _ptr(workspace), workspace.numel(), _stream_handle(stream))
     nat.check(rc)
     return g
+
+
+def conv1d_silu_forward(x, weight, bias=None, init_state=None, *, out=None, stream=None):
+    """Causal depthwise conv1d + SiLU over time: x [B,T,C], weight [C,K] fp32,
+    bias [C] fp32, init_state [B,C,K] fp32 (None = zeros).  Returns out [B,T,C]."""
+    if not x.is_cuda:
+        raise ValueError("inputs must be CUDA tensors (no CPU path exists)")
+    if x.dtype not in _IO_TYPES:
+        raise TypeError(f"x: unsupported dtype {x.dtype}")
+    Bz, T, C = x.shape
+    K = weight.shape[1]
+    _check("weight", weight, torch.float32, (C, K), x.device)
+    if bias is not None:
+        _check("bias", bias, torch.float32, (C,), x.device)
+    if init_state is not None:
+        _check("init_state", init_state, torch.float32, (Bz, C, K), x.device)
+    if not x.is_contiguous():
+        raise ValueError("x: must be contiguous")
+    o = torch.empty_like(x) if out is None else out
+    rc = nat.lib().ssd_conv1d_silu_forward(Bz, T, C, K, int(_IO_TYPES[x.dtype]), _ptr(x),
+                                           _ptr(weight), _ptr(bias), _ptr(init_state), _ptr(o),
+                                           _stream_handle(stream))
+    nat.check(rc)
+    return o
+
+
+def conv1d_silu_backward(x, weight, bias, init_state, dout, *, workspace=None, stream=None):
+    """Gradients of sum(dout * out): dict dx, dweight, dbias."""
+    if not x.is_cuda:
+        raise ValueError("inputs must be CUDA tensors (no CPU path exists)")
+    if x.dtype not in _IO_TYPES:
+        raise TypeError(f"x: unsupported dtype {x.dtype}")
+    Bz, T, C = x.shape
+    K = weight.shape[1]
+    _check("weight", weight, torch.float32, (C, K), x.device)
+    _check("dout", dout, x.dtype, (Bz, T, C), x.device)
+    if bias is not None:
+        _check("bias", bias, torch.float32, (C,), x.device)
+    if init_state is not None:
+        _check("init_state", init_state, torch.float32, (Bz, C, K), x.device)
+    g = {"dx": torch.empty_like(x), "dweight": torch.empty_like(weight),
+         "dbias": torch.empty(C, dtype=torch.float32, device=x.device)}
+    if workspace is None:
+        n = nat.lib().ssd_conv1d_silu_workspace_bytes(Bz, T, C, K)
+        if n == 0:
+            raise nat.SsdError(nat.SSD_ERR_UNSUPPORTED, "shape rejected")
+        workspace = torch.empty(n, dtype=torch.uint8, device=x.device)
+    rc = nat.lib().ssd_conv1d_silu_backward(
+        Bz, T, C, K, int(_IO_TYPES[x.dtype]), _ptr(x), _ptr(weight), _ptr(bias), _ptr(init_state),
+        _ptr(dout), _ptr(g["dx"]), _ptr(g["dweight"]), _ptr(g["dbias"]), _ptr(workspace),
+        workspace.numel(), _stream_handle(stream))
+    nat.check(rc)
+    return g

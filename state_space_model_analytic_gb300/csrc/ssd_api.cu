@@ -536,4 +536,71 @@ int ssd_rmsnorm_gated_backward(int64_t rows, int64_t width, int32_t dtype, const
   return SSD_OK;
 }
 
+// ---- causal depthwise conv1d + SiLU before the core (ssd_conv.cu) --------
+
+namespace {
+int conv_check(const char* who, long long B, long long T, long long C, int K, int dtype) {
+  const long long tmax = (long long)(kConvFwdRows < kConvBwdRows ? kConvFwdRows : kConvBwdRows) * 65535;
+  if (B < 1 || B > 65535 || T < 1 || T > tmax)
+    return fail(SSD_ERR_INVALID_ARG, "%s: batch must be in [1, 65535] and seqlen in [1, %lld]", who,
+                tmax);
+  if (dtype != SSD_F32 && dtype != SSD_BF16) return fail(SSD_ERR_INVALID_ARG, "%s: bad dtype", who);
+  const long long e = dtype == SSD_BF16 ? 8 : 4;  // channels per 16-byte chunk
+  if (C < e || C % e != 0)
+    return fail(SSD_ERR_UNSUPPORTED, "%s: channels must be a positive multiple of %lld", who, e);
+  if (K < 1 || K > 4) return fail(SSD_ERR_UNSUPPORTED, "%s: d_conv must be in [1, 4]", who);
+  return SSD_OK;
+}
+}  // namespace
+
+size_t ssd_conv1d_silu_workspace_bytes(int64_t batch, int64_t seqlen, int64_t channels,
+                                       int32_t d_conv) {
+  if (batch < 1 || seqlen < 1 || channels < 1 || d_conv < 1 || d_conv > 4) return 0;
+  const size_t tiles = (size_t)((seqlen + kConvBwdRows - 1) / kConvBwdRows);
+  return up((size_t)batch * tiles * channels * (d_conv + 1) * sizeof(float));
+}
+
+int ssd_conv1d_silu_forward(int64_t batch, int64_t seqlen, int64_t channels, int32_t d_conv,
+                            int32_t dtype, const void* x, const float* weight, const float* bias,
+                            const float* init_state, void* out, void* cuda_stream) {
+  g_err.clear();
+  int rc = conv_check("ssd_conv1d_silu_forward", batch, seqlen, channels, d_conv, dtype);
+  if (rc) return rc;
+  if (!x || !weight || !out)
+    return fail(SSD_ERR_INVALID_ARG, "ssd_conv1d_silu_forward: a required pointer is NULL");
+  const void* ptrs[] = {x, weight, bias, init_state, out};
+  for (const void* q : ptrs)
+    if (q && !aligned16(q))
+      return fail(SSD_ERR_ALIGNMENT, "ssd_conv1d_silu_forward: pointer %p is not 16-byte aligned", q);
+  cudaError_t e = conv_forward(batch, (int)seqlen, (int)channels, d_conv, dtype == SSD_BF16, x,
+                               weight, bias, init_state, out, (cudaStream_t)cuda_stream);
+  if (e != cudaSuccess) return cuda_fail(e, "conv1d forward kernel");
+  return SSD_OK;
+}
+
+int ssd_conv1d_silu_backward(int64_t batch, int64_t seqlen, int64_t channels, int32_t d_conv,
+                             int32_t dtype, const void* x, const float* weight, const float* bias,
+                             const float* init_state, const void* dout, void* dx, float* dweight,
+                             float* dbias, void* workspace, size_t workspace_bytes,
+                             void* cuda_stream) {
+  g_err.clear();
+  int rc = conv_check("ssd_conv1d_silu_backward", batch, seqlen, channels, d_conv, dtype);
+  if (rc) return rc;
+  if (!x || !weight || !dout || !dx || !dweight || !workspace)
+    return fail(SSD_ERR_INVALID_ARG, "ssd_conv1d_silu_backward: a required pointer is NULL");
+  const void* ptrs[] = {x, weight, bias, init_state, dout, dx, dweight, dbias, workspace};
+  for (const void* q : ptrs)
+    if (q && !aligned16(q))
+      return fail(SSD_ERR_ALIGNMENT, "ssd_conv1d_silu_backward: pointer %p is not 16-byte aligned", q);
+  const size_t need = ssd_conv1d_silu_workspace_bytes(batch, seqlen, channels, d_conv);
+  if (workspace_bytes < need)
+    return fail(SSD_ERR_INVALID_ARG, "ssd_conv1d_silu_backward: workspace %zu bytes < %zu needed",
+                workspace_bytes, need);
+  cudaError_t e = conv_backward(batch, (int)seqlen, (int)channels, d_conv, dtype == SSD_BF16, x,
+                                weight, bias, init_state, dout, dx, dweight, dbias,
+                                (float*)workspace, (cudaStream_t)cuda_stream);
+  if (e != cudaSuccess) return cuda_fail(e, "conv1d backward kernels");
+  return SSD_OK;
+}
+
 }  // extern "C"

@@ -65,6 +65,27 @@ cudaError_t norm_backward(long long rows, int width, bool bf16, const void* y, c
                           const float* w, float eps, const float* inv_rms, const void* g, void* dy,
                           void* dz, float* dw, float* part, cudaStream_t s);
 
+// Causal depthwise conv1d + SiLU before the core (ssd_conv.cu): a CTA is
+// kConvChunks 4-channel vectors x a stack of tiles along time (forward:
+// kConvFwdSlots tiles of kConvFwdTile steps; backward: kConvBwdSlots tiles
+// of kConvBwdTile steps, kConvBwdRows steps); the backward keeps per-CTA
+// partials of dw, dbias in [B * ceil(T / kConvBwdRows)][C][K + 1] and is
+// register-capped so that kConvBwdMinCtas CTAs fit on an SM.
+constexpr int kConvChunks = 32;
+constexpr int kConvFwdSlots = 8;
+constexpr int kConvFwdTile = 32;
+constexpr int kConvFwdRows = kConvFwdSlots * kConvFwdTile;
+constexpr int kConvBwdSlots = 4;
+constexpr int kConvBwdTile = 64;
+constexpr int kConvBwdRows = kConvBwdSlots * kConvBwdTile;
+constexpr int kConvBwdMinCtas = 2;
+cudaError_t conv_forward(long long B, int T_, int C, int K, bool bf16, const void* x,
+                         const float* w, const float* bias, const float* init, void* out,
+                         cudaStream_t s);
+cudaError_t conv_backward(long long B, int T_, int C, int K, bool bf16, const void* x,
+                          const float* w, const float* bias, const float* init, const void* dout,
+                          void* dx, float* dw, float* dbias, float* part, cudaStream_t s);
+
 // Upper bound on the CTAs of the tensor-core backward (one per SM).
 constexpr size_t kBwdMaxCtas = 160;
 

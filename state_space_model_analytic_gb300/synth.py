@@ -188,3 +188,19 @@ def norm_inputs(rows: int, width: int, dtype: str, seed: int) -> dict:
     g = rng.standard_normal((rows, width))
     return {"y": round_to(y, dtype), "z": round_to(z, dtype), "weight": round_to(w, "f32"),
             "dout": round_to(g, dtype)}
+
+
+def conv_inputs(batch: int, seqlen: int, channels: int, d_conv: int, dtype: str, seed: int,
+                with_init: bool = True) -> dict:
+    """Conv1d + SiLU inputs: x, dout ~ N(0, 1) [B, T, C] rounded to the storage
+    type; weight ~ N(0, 1) / sqrt(d_conv) [C, K]; bias ~ N(0, 0.1^2) [C];
+    init_state ~ N(0, 1) [B, C, K] or None; all but x, dout fp32."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    x = rng.standard_normal((batch, seqlen, channels))
+    w = rng.standard_normal((channels, d_conv)) / math.sqrt(d_conv)
+    b = rng.standard_normal(channels) * 0.1
+    init = rng.standard_normal((batch, channels, d_conv)) if with_init else None
+    g = rng.standard_normal((batch, seqlen, channels))
+    return {"x": round_to(x, dtype), "weight": round_to(w, "f32"), "bias": round_to(b, "f32"),
+            "init_state": None if init is None else round_to(init, "f32"),
+            "dout": round_to(g, dtype)}

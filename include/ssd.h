@@ -190,10 +190,14 @@ SSD_API int ssd_rmsnorm_gated_backward(int64_t rows, int64_t width, int32_t dtyp
  *   weight, dweight       [channels][d_conv]          fp32
  *   bias, dbias           [channels]                  fp32
  *   init_state            [batch][channels][d_conv]   fp32
- * channels: a multiple of 8 (bf16) or 4 (fp32); d_conv in [1, 4].  Pointers
- * 16-byte aligned; the backward's workspace is
+ * channels: a multiple of 8 (bf16) or 4 (fp32); d_conv in [1, 4]; batch <=
+ * 65535 and batch * seqlen below 2^31 - 1024 (x and dout are read as
+ * [batch*seqlen][channels] TMA tensors with 32-bit row coordinates).
+ * Pointers 16-byte aligned; the backward's workspace is
  * ssd_conv1d_silu_workspace_bytes(batch, seqlen, channels, d_conv) bytes.
- * Errors as for ssd_forward; results are deterministic.
+ * Errors as for ssd_forward (SSD_ERR_CUDA also when the driver cannot encode
+ * the tensor maps); results are deterministic.  The kernels' waits on their
+ * copies are bounded and report through ssd_device_status.
  */
 SSD_API size_t ssd_conv1d_silu_workspace_bytes(int64_t batch, int64_t seqlen, int64_t channels,
                                                int32_t d_conv);
@@ -268,9 +272,10 @@ SSD_API int ssd_kernel_path(const ssd_dims* dims);
  * path = -1 restores automatic selection.  Process-wide; for tests. */
 SSD_API int ssd_force_kernel_path(int path);
 
-/* Reads and clears the device-side error word that bounded waits inside the
- * tensor-core kernels set when they give up (synchronous: it copies from the
- * device).  Returns SSD_OK, SSD_ERR_DEVICE_TIMEOUT or SSD_ERR_CUDA. */
+/* Reads and clears the device-side error words that bounded waits inside the
+ * tensor-core kernels and the conv1d kernels set when they give up
+ * (synchronous: it copies from the device).  Returns SSD_OK,
+ * SSD_ERR_DEVICE_TIMEOUT or SSD_ERR_CUDA. */
 SSD_API int ssd_device_status(void);
 
 /* Failure-path self test: launches one CTA whose bounded wait on an mbarrier

@@ -290,9 +290,11 @@ int ssd_force_kernel_path(int path) {
 
 int ssd_device_status(void) {
   g_err.clear();
-  unsigned int flag = 0;
+  unsigned int flag = 0, conv_flag = 0;
   cudaError_t e = tc_read_and_clear_error(&flag);
+  if (e == cudaSuccess) e = conv_read_and_clear_error(&conv_flag);
   if (e != cudaSuccess) return cuda_fail(e, "ssd_device_status");
+  flag |= conv_flag << 8;
   if (flag) return fail(SSD_ERR_DEVICE_TIMEOUT, "a device-side wait gave up (flag 0x%x)", flag);
   return SSD_OK;
 }
@@ -540,10 +542,9 @@ int ssd_rmsnorm_gated_backward(int64_t rows, int64_t width, int32_t dtype, const
 
 namespace {
 int conv_check(const char* who, long long B, long long T, long long C, int K, int dtype) {
-  const long long tmax = (long long)(kConvFwdRows < kConvBwdRows ? kConvFwdRows : kConvBwdRows) * 65535;
-  if (B < 1 || B > 65535 || T < 1 || T > tmax)
-    return fail(SSD_ERR_INVALID_ARG, "%s: batch must be in [1, 65535] and seqlen in [1, %lld]", who,
-                tmax);
+  if (B < 1 || B > 65535 || T < 1 || B * T > (1ll << 31) - 1024)
+    return fail(SSD_ERR_INVALID_ARG, "%s: batch must be in [1, 65535], seqlen >= 1 and batch * "
+                "seqlen below 2^31 - 1024", who);
   if (dtype != SSD_F32 && dtype != SSD_BF16) return fail(SSD_ERR_INVALID_ARG, "%s: bad dtype", who);
   const long long e = dtype == SSD_BF16 ? 8 : 4;  // channels per 16-byte chunk
   if (C < e || C % e != 0)
@@ -556,7 +557,7 @@ int conv_check(const char* who, long long B, long long T, long long C, int K, in
 size_t ssd_conv1d_silu_workspace_bytes(int64_t batch, int64_t seqlen, int64_t channels,
                                        int32_t d_conv) {
   if (batch < 1 || seqlen < 1 || channels < 1 || d_conv < 1 || d_conv > 4) return 0;
-  const size_t tiles = (size_t)((seqlen + kConvBwdRows - 1) / kConvBwdRows);
+  const size_t tiles = (size_t)conv_max_ctas_per_column(seqlen);
   return up((size_t)batch * tiles * channels * (d_conv + 1) * sizeof(float));
 }
 

@@ -11,156 +11,304 @@
 // (the gradient w.r.t. the initial state is not formed, as on the page).
 //
 // Layouts: x, out, dout, dx [B][T][C] (`dtype`); w [C][K], bias [C], init
-// [B][C][K], dw [C][K], dbias [C] fp32.  A thread owns 4 channels (one 8-byte
-// bf16 or 16-byte fp32 vector; a warp-row of kConvChunks threads is one
-// coalesced run) and one tile of steps; a CTA stacks consecutive tiles.
-// The tile's loads are unconditional (indices clamped into the sequence,
-// the extra values unused), so the walk, unrolled by 4, can issue them
-// ahead.  The backward walks forward in time over the tile
-// plus K - 1 steps past it, keeping the last K inputs and the K - 1 dx
-// values still open; it stores dx of a step once the gradient of the step
-// K - 1 later is in.  dw and dbias: the CTA sums its tiles in shared memory
-// in order, a last kernel sums the CTAs along time in order.
+// [B][C][K], dw [C][K], dbias [C] fp32.
+//
+// Work split.  A warp owns kConvCols = 128 channels (lane l: channels
+// 4l..4l+3, one 8-byte bf16 / 16-byte fp32 shared-memory read per step, a
+// warp reads one contiguous row) of one batch row over a run of consecutive
+// steps; a CTA is a few warps (4 forward, kConvBwdWarps backward) with
+// consecutive runs of the same channels and batch row.  The host splits each
+// (channel block, batch row) column into gridDim.y * (warps per CTA)
+// balanced runs, as many as the GPU holds at once (one wave), so every warp
+// walks one run.
+//
+// Data movement.  Each warp has its own ring of stages in shared memory and
+// its own mbarriers: lane 0 keeps the next stages in flight with 2D TMA
+// boxes of 16 (forward) or 8 (backward) steps x 128 channels (x, and dout
+// for the backward, viewed as [B*T][C]); no barrier spans warps.  The K - 1 inputs before a
+// run come from plain loads (or the initial state before step 0).
+//
+// Compute.  A thread keeps the last K inputs in registers and walks its run
+// step by step.  The backward walks on K - 1 steps past its run, keeping the
+// K - 1 dx values still open and storing each once the gradient of the step
+// K - 1 later is in (steps past T carry no gradient); dw and dbias stay in
+// registers over the run, are summed over the CTA's warps in shared memory
+// in order and over the CTAs along time in order by a last kernel.
+//
+// Waits on the TMA barriers are bounded: a wait that gives up sets a device
+// error word; the warp then waits (bounded) for the copies it still has in
+// flight and stops walking.
+#include <cuda.h>
 #include <cuda_bf16.h>
 
 #include "ssd_common.cuh"
 #include "ssd_internal.h"
+#include "tc_util.cuh"
 
 namespace ssd {
 namespace {
 
-constexpr int kE = 4;  // channels per thread
+using namespace tc;
+
+// forward: 4 warps a CTA, stages of 16 steps, 3 stages a warp; backward:
+// kConvBwdWarps warps a CTA, stages of 8 steps, 2 stages a warp (measured
+// best among 2-4 stages, 8-16 steps and 4-8 warps on the xBC workload)
+constexpr int kConvFwdWarps = 4;
+constexpr int kConvFwdStep = 16;
+constexpr int kConvFwdStages = 3;
+constexpr int kConvBwdStep = 8;
+constexpr int kConvBwdStages = 2;
+constexpr uint64_t kConvWaitNs = 1000000000ull;
+
+__device__ unsigned int g_conv_error;
 
 template <typename T>
-struct CVec;
+struct ConvT;
 template <>
-struct CVec<float> {
-  __device__ static void load(const void* p, float* v) {
+struct ConvT<float> {
+  // 4 channels from a shared-memory row at lane's offset
+  __device__ static void lds(const uint8_t* row, int lane, float* v) {
+    const float4 q = *(const float4*)(row + 16 * lane);
+    v[0] = q.x; v[1] = q.y; v[2] = q.z; v[3] = q.w;
+  }
+  __device__ static void ldg(const float* p, float* v) {
     const float4 q = *(const float4*)p;
     v[0] = q.x; v[1] = q.y; v[2] = q.z; v[3] = q.w;
   }
-  __device__ static void store(void* p, const float* v) { *(float4*)p = make_float4(v[0], v[1], v[2], v[3]); }
+  __device__ static void stg(float* p, const float* v) { *(float4*)p = make_float4(v[0], v[1], v[2], v[3]); }
 };
 template <>
-struct CVec<__nv_bfloat16> {
-  __device__ static void load(const void* p, float* v) {
-    const uint2 q = *(const uint2*)p;
+struct ConvT<__nv_bfloat16> {
+  __device__ static void cvt(uint2 q, float* v) {
     const float2 a = __bfloat1622float2(*(const __nv_bfloat162*)&q.x);
     const float2 b = __bfloat1622float2(*(const __nv_bfloat162*)&q.y);
     v[0] = a.x; v[1] = a.y; v[2] = b.x; v[3] = b.y;
   }
-  __device__ static void store(void* p, const float* v) {
+  __device__ static void lds(const uint8_t* row, int lane, float* v) {
+    cvt(*(const uint2*)(row + 8 * lane), v);
+  }
+  __device__ static void ldg(const __nv_bfloat16* p, float* v) { cvt(*(const uint2*)p, v); }
+  __device__ static void stg(__nv_bfloat16* p, const float* v) {
     const __nv_bfloat162 a = __floats2bfloat162_rn(v[0], v[1]);
     const __nv_bfloat162 b = __floats2bfloat162_rn(v[2], v[3]);
     *(uint2*)p = make_uint2(*(const unsigned*)&a, *(const unsigned*)&b);
   }
 };
 
-// logistic sigmoid with the fast exponential and divide; the exponent is
-// capped at 80 so that the divisor stays below 2^126, where the fast divide
-// is accurate (for z < -80 the result, below 2e-35, is immaterial to silu)
+// Shared-memory geometry: a stage of one tensor is (step) rows of 128
+// elements; a warp's ring is S stages (of x, or of x and dout).
+template <typename T, int K>
+struct ConvGeom {
+  static constexpr int ROWB = kConvCols * (int)sizeof(T);
+  static constexpr int FTILE = kConvFwdStep * ROWB;
+  static constexpr int BTILE = kConvBwdStep * ROWB;
+  static constexpr int FWD_WARP = kConvFwdStages * FTILE;
+  static constexpr int BWD_WARP = kConvBwdStages * 2 * BTILE;
+  static constexpr size_t fwd_smem() { return (size_t)kConvFwdWarps * FWD_WARP + 1024; }
+  static constexpr size_t bwd_smem() {
+    const size_t ring = (size_t)kConvBwdWarps * BWD_WARP;
+    const size_t red = (size_t)kConvBwdWarps * 32 * 4 * (K + 1) * sizeof(float);
+    return (ring > red ? ring : red) + 1024;
+  }
+};
+
+// logistic sigmoid 1 / (1 + 2^(-z log2 e)) from the hardware base-2
+// exponential and reciprocal approximations (about 1e-6 relative for
+// |z| < 80, and exact limits: 2^(+large) = inf gives 0, 2^(-large) = 0
+// gives 1)
 __device__ __forceinline__ float sig(float z) {
-  return __fdividef(1.f, 1.f + __expf(fminf(-z, 80.f)));
+  float e, r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(z * -1.4426950408889634f));
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.f + e));
+  return r;
 }
 
-// history value of step s (s >= -K, s < T) for the channels at c0
+// input of step s for the thread's channels: x for s >= 0, else the initial
+// state (zeros without one); zeros for channels past C
 template <typename T, int K>
-__device__ __forceinline__ void hist_load(const T* x, const float* init, int b, int s, int C, int c0,
-                                          long long T_, float* v) {
-  if (s >= 0) {
-    CVec<T>::load(x + ((long long)b * T_ + s) * C + c0, v);
+__device__ __forceinline__ void hist_load(const T* x, const float* init, long long rowb, int b, int C,
+                                          int c0, bool valid, int s, float* v) {
+  if (valid && s >= 0) {
+    ConvT<T>::ldg(x + (rowb + s) * C + c0, v);
   } else {
 #pragma unroll
-    for (int e = 0; e < kE; ++e) v[e] = init ? init[((long long)b * C + c0 + e) * K + K + s] : 0.f;
+    for (int e = 0; e < 4; ++e)
+      v[e] = (valid && init) ? init[((long long)b * C + c0 + e) * K + K + s] : 0.f;
   }
 }
 
 template <int K>
-__device__ __forceinline__ void load_params(const float* w, const float* bias, int c0,
-                                            float (&wv)[K][kE], float (&bv)[kE]) {
+__device__ __forceinline__ void load_params(const float* w, const float* bias, int c0, bool valid,
+                                            float (&wv)[K][4], float (&bv)[4]) {
 #pragma unroll
-  for (int e = 0; e < kE; ++e) {
-    bv[e] = bias ? bias[c0 + e] : 0.f;
+  for (int e = 0; e < 4; ++e) {
+    bv[e] = (valid && bias) ? bias[c0 + e] : 0.f;
 #pragma unroll
-    for (int k = 0; k < K; ++k) wv[k][e] = w[(c0 + e) * K + k];
+    for (int k = 0; k < K; ++k) wv[k][e] = valid ? w[(c0 + e) * K + k] : 0.f;
   }
 }
 
+// The warp's balanced run of the column: [ws, we)
+struct Run {
+  int ws, we;
+};
+template <int WARPS>
+__device__ __forceinline__ Run warp_run(int T_) {
+  const int nr = gridDim.y * WARPS, r = blockIdx.y * WARPS + (threadIdx.x >> 5);
+  return Run{(int)((long long)r * T_ / nr), (int)((long long)(r + 1) * T_ / nr)};
+}
+
+// After the wait for stage j gave up (uniform over the warp): flag it, and
+// let lane 0 wait (bounded) for the copies it still has in flight: stages
+// j .. min(ntiles, j + S) - 1 (stage j' + S is issued after stage j' is
+// walked).
+__device__ __forceinline__ void conv_abort(uint64_t* full, int stages, int j, int ntiles) {
+  if ((threadIdx.x & 31) != 0) return;
+  atomicOr(&g_conv_error, 1u);
+  const int last = min(ntiles, j + stages) - 1;
+  for (int i = j; i <= last; ++i) (void)mbar_wait(&full[i % stages], (i / stages) & 1, kConvWaitNs);
+}
+
 template <typename T, int K>
-__global__ void __launch_bounds__(kConvChunks * kConvFwdSlots)
-k_conv_fwd(int T_, int C, const T* __restrict__ x, const float* __restrict__ w,
-           const float* __restrict__ bias, const float* __restrict__ init, T* __restrict__ out) {
-  const int c0 = (blockIdx.x * kConvChunks + threadIdx.x) * kE, b = blockIdx.z;
-  if (c0 >= C) return;
-  const int t0 = (blockIdx.y * kConvFwdSlots + threadIdx.y) * kConvFwdTile;
-  if (t0 >= T_) return;
-  const int t1 = min(T_, t0 + kConvFwdTile);
-  float wv[K][kE], bv[kE], win[K][kE];  // win[k] = h of step t - K + 1 + k
-  load_params<K>(w, bias, c0, wv, bv);
+__global__ void __launch_bounds__(kConvFwdWarps * 32)
+k_conv_fwd(const __grid_constant__ CUtensorMap xmap, int T_, int C, const T* __restrict__ x,
+           const float* __restrict__ w, const float* __restrict__ bias,
+           const float* __restrict__ init, T* __restrict__ out) {
+  using G = ConvGeom<T, K>;
+  constexpr int S = kConvFwdStages;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint64_t full_all[kConvFwdWarps][S];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint8_t* ring = align1024(smem_raw) + warp * G::FWD_WARP;
+  uint64_t* full = full_all[warp];
+  const int cs = blockIdx.x * kConvCols, c0 = cs + 4 * lane, b = blockIdx.z;
+  const Run run = warp_run<kConvFwdWarps>(T_);
+  const int ntiles = (run.we - run.ws + kConvFwdStep - 1) / kConvFwdStep;
+  const long long rowb = (long long)b * T_;
+  auto issue = [&](int j) {
+    mbar_expect_tx(&full[j % S], G::FTILE);
+    tma_load_2d(ring + (j % S) * G::FTILE, &xmap, cs, (int)(rowb + run.ws + j * kConvFwdStep),
+                &full[j % S]);
+  };
+  if (lane == 0) {
+    prefetch_tmap(&xmap);
+    for (int i = 0; i < S; ++i) mbar_init(&full[i], 1);
+    fence_mbar_init();
+    for (int j = 0; j < min(S, ntiles); ++j) issue(j);
+  }
+  __syncwarp();
+  const bool cvalid = c0 < C;
+  float wv[K][4], bv[4], win[K][4];  // win[k] = input of step t - K + 1 + k
+  load_params<K>(w, bias, c0, cvalid, wv, bv);
 #pragma unroll
-  for (int k = 0; k < K - 1; ++k) hist_load<T, K>(x, init, b, t0 - K + 1 + k, C, c0, T_, win[k]);
-  const T* xr = x + (long long)b * T_ * C + c0;
-  T* orow = out + (long long)b * T_ * C + c0;
-#pragma unroll 4
-  for (int i = 0; i < kConvFwdTile; ++i) {
-    const int t = t0 + i;
-    CVec<T>::load(xr + (long long)min(t, t1 - 1) * C, win[K - 1]);
-    float o[kE];
-#pragma unroll
-    for (int e = 0; e < kE; ++e) {
-      float p = bv[e];
-#pragma unroll
-      for (int k = 0; k < K; ++k) p = fmaf(wv[k][e], win[k][e], p);
-      o[e] = p * sig(p);
+  for (int k = 0; k < K - 1; ++k)
+    hist_load<T, K>(x, init, rowb, b, C, c0, cvalid && ntiles > 0, run.ws - (K - 1) + k, win[k]);
+  T* op = out + (rowb + run.ws) * C + c0;
+  for (int j = 0; j < ntiles; ++j) {
+    const bool ok = mbar_wait(&full[j % S], (j / S) & 1, kConvWaitNs);
+    if (!__all_sync(0xffffffffu, ok)) {
+      conv_abort(full, S, j, ntiles);
+      return;
     }
-    if (t < t1) CVec<T>::store(orow + (long long)t * C, o);
+    const uint8_t* st = ring + (j % S) * G::FTILE;
+    const int n = min(kConvFwdStep, run.we - run.ws - j * kConvFwdStep);
 #pragma unroll
-    for (int k = 0; k < K - 1; ++k)
+    for (int i = 0; i < kConvFwdStep; ++i) {
+      ConvT<T>::lds(st + i * G::ROWB, lane, win[K - 1]);
+      float o[4];
 #pragma unroll
-      for (int e = 0; e < kE; ++e) win[k][e] = win[k + 1][e];
+      for (int e = 0; e < 4; ++e) {
+        float p = bv[e];
+#pragma unroll
+        for (int k = 0; k < K; ++k) p = fmaf(wv[k][e], win[k][e], p);
+        o[e] = p * sig(p);
+      }
+      if (cvalid && i < n) ConvT<T>::stg(op, o);
+      op += C;
+#pragma unroll
+      for (int k = 0; k < K - 1; ++k)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) win[k][e] = win[k + 1][e];
+    }
+    __syncwarp();
+    if (lane == 0 && j + S < ntiles) issue(j + S);
   }
 }
 
-// part: [B * gridDim.y][C][K + 1] (dw taps, then dbias) per (b, CTA row along time)
+// part: [B * gridDim.y][C][K + 1] (dw taps, then dbias) per CTA
 template <typename T, int K>
-__global__ void __launch_bounds__(kConvChunks * kConvBwdSlots, kConvBwdMinCtas)
-k_conv_bwd(int T_, int C, const T* __restrict__ x, const float* __restrict__ w,
-           const float* __restrict__ bias, const float* __restrict__ init, const T* __restrict__ dout,
-           T* __restrict__ dx, float* __restrict__ part) {
-  __shared__ float s_red[kConvBwdSlots][kConvChunks * kE * (K + 1)];
-  const int c0 = (blockIdx.x * kConvChunks + threadIdx.x) * kE, b = blockIdx.z;
-  const int t0 = (blockIdx.y * kConvBwdSlots + threadIdx.y) * kConvBwdTile;
-  const int t1 = min(T_, t0 + kConvBwdTile);
-  float dw[K][kE], db[kE];
+__global__ void __launch_bounds__(kConvBwdWarps * 32)
+k_conv_bwd(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap gmap,
+           int T_, int C, const T* __restrict__ x, const float* __restrict__ w,
+           const float* __restrict__ bias, const float* __restrict__ init, T* __restrict__ dx,
+           float* __restrict__ part) {
+  using G = ConvGeom<T, K>;
+  constexpr int S = kConvBwdStages;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint64_t full_all[kConvBwdWarps][S];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint8_t* base = align1024(smem_raw);
+  uint8_t* ring = base + warp * G::BWD_WARP;
+  uint64_t* full = full_all[warp];
+  const int cs = blockIdx.x * kConvCols, c0 = cs + 4 * lane, b = blockIdx.z;
+  const Run run = warp_run<kConvBwdWarps>(T_);
+  // steps walked: the run and the K - 1 after it
+  const int nwalk = run.we > run.ws ? run.we - run.ws + K - 1 : 0;
+  const int ntiles = (nwalk + kConvBwdStep - 1) / kConvBwdStep;
+  const long long rowb = (long long)b * T_;
+  auto issue = [&](int j) {
+    uint8_t* st = ring + (j % S) * 2 * G::BTILE;
+    const int r = (int)(rowb + run.ws + j * kConvBwdStep);
+    mbar_expect_tx(&full[j % S], 2 * G::BTILE);
+    tma_load_2d(st, &xmap, cs, r, &full[j % S]);
+    tma_load_2d(st + G::BTILE, &gmap, cs, r, &full[j % S]);
+  };
+  if (lane == 0) {
+    prefetch_tmap(&xmap);
+    prefetch_tmap(&gmap);
+    for (int i = 0; i < S; ++i) mbar_init(&full[i], 1);
+    fence_mbar_init();
+    for (int j = 0; j < min(S, ntiles); ++j) issue(j);
+  }
+  __syncwarp();
+  const bool cvalid = c0 < C;
+  float wv[K][4], bv[4];
+  load_params<K>(w, bias, c0, cvalid, wv, bv);
+  float dw[K][4], db[4];
 #pragma unroll
-  for (int e = 0; e < kE; ++e) {
+  for (int e = 0; e < 4; ++e) {
     db[e] = 0.f;
 #pragma unroll
     for (int k = 0; k < K; ++k) dw[k][e] = 0.f;
   }
-  if (c0 < C && t0 < T_) {
-    float wv[K][kE], bv[kE];
-    load_params<K>(w, bias, c0, wv, bv);
-    float xw[K][kE];  // xw[k] = h of step t - K + 1 + k
+  float xw[K][4];  // xw[k] = input of step s - K + 1 + k
 #pragma unroll
-    for (int k = 0; k < K - 1; ++k) hist_load<T, K>(x, init, b, t0 - K + 1 + k, C, c0, T_, xw[k]);
-    // open[j]: dx of step t - K + 1 + j summed over the gradients of steps < t
-    float open[K > 1 ? K - 1 : 1][kE];
+  for (int k = 0; k < K - 1; ++k)
+    hist_load<T, K>(x, init, rowb, b, C, c0, cvalid && ntiles > 0, run.ws - (K - 1) + k, xw[k]);
+  // open[k]: dx of step s - K + 1 + k summed over the gradients of steps < s
+  float open[K > 1 ? K - 1 : 1][4];
 #pragma unroll
-    for (int j = 0; j < K - 1; ++j)
+  for (int k = 0; k < K - 1; ++k)
 #pragma unroll
-      for (int e = 0; e < kE; ++e) open[j][e] = 0.f;
-    const long long row = (long long)b * T_ * C + c0;
-#pragma unroll 4
-    for (int i = 0; i < kConvBwdTile + K - 1; ++i) {
-      const int t = t0 + i;
-      const long long tc = (long long)min(t, T_ - 1) * C;
-      float d[kE], g[kE], o[kE];
-      CVec<T>::load(x + row + tc, xw[K - 1]);
-      CVec<T>::load(dout + row + tc, d);
-      const bool in_seq = t < T_, owned = t < t1;
+    for (int e = 0; e < 4; ++e) open[k][e] = 0.f;
+  T* dp = dx + (rowb + run.ws) * C + c0;  // dx of the next step to complete
+  for (int j = 0; j < ntiles; ++j) {
+    const bool ok = mbar_wait(&full[j % S], (j / S) & 1, kConvWaitNs);
+    if (!__all_sync(0xffffffffu, ok)) {
+      conv_abort(full, S, j, ntiles);
+      break;
+    }
+    const uint8_t* xs = ring + (j % S) * 2 * G::BTILE;
+    const uint8_t* gs = xs + G::BTILE;
 #pragma unroll
-      for (int e = 0; e < kE; ++e) {
+    for (int i = 0; i < kConvBwdStep; ++i) {
+      const int s = run.ws + j * kConvBwdStep + i;
+      float d[4], g[4], o[4];
+      ConvT<T>::lds(xs + i * G::ROWB, lane, xw[K - 1]);
+      ConvT<T>::lds(gs + i * G::ROWB, lane, d);
+      const bool in_seq = s < T_, owned = s < run.we;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
         float p = bv[e];
 #pragma unroll
         for (int k = 0; k < K; ++k) p = fmaf(wv[k][e], xw[k][e], p);
@@ -171,45 +319,52 @@ k_conv_bwd(int T_, int C, const T* __restrict__ x, const float* __restrict__ w,
 #pragma unroll
           for (int k = 0; k < K; ++k) dw[k][e] = fmaf(g[e], xw[k][e], dw[k][e]);
         }
-        // this step's gradient reaches dx of steps t - K + 1 .. t through taps 0 .. K - 1
+        // this step's gradient reaches dx of steps s - K + 1 .. s through taps 0 .. K - 1
         if (K > 1) {
           o[e] = fmaf(g[e], wv[0][e], open[0][e]);
 #pragma unroll
-          for (int j = 0; j + 1 < K - 1; ++j) open[j][e] = fmaf(g[e], wv[j + 1][e], open[j + 1][e]);
+          for (int k = 0; k + 1 < K - 1; ++k) open[k][e] = fmaf(g[e], wv[k + 1][e], open[k + 1][e]);
           open[K > 1 ? K - 2 : 0][e] = g[e] * wv[K - 1][e];
         } else {
           o[e] = g[e] * wv[0][e];
         }
       }
-      const int s = t - K + 1;  // dx of step s is complete
-      if (s >= t0 && s < t1) CVec<T>::store(dx + row + (long long)s * C, o);
+      const int sd = s - (K - 1);  // dx of step sd is complete
+      if (sd >= run.ws && sd < run.we) {
+        if (cvalid) ConvT<T>::stg(dp, o);
+        dp += C;
+      }
 #pragma unroll
       for (int k = 0; k < K - 1; ++k)
 #pragma unroll
-        for (int e = 0; e < kE; ++e) xw[k][e] = xw[k + 1][e];
+        for (int e = 0; e < 4; ++e) xw[k][e] = xw[k + 1][e];
     }
+    __syncwarp();
+    if (lane == 0 && j + S < ntiles) issue(j + S);
   }
-  // this CTA's tiles summed in order (slot 0 first), per channel and tap
-  float* mine = &s_red[threadIdx.y][threadIdx.x * kE * (K + 1)];
+  // the CTA's warps summed in order (warp 0 first), per channel and tap; every
+  // warp is past its ring (all copies waited for, or given up on and flagged)
+  __syncthreads();
+  float* red = (float*)base;
+  float* mine = red + (size_t)threadIdx.x * 4 * (K + 1);
 #pragma unroll
-  for (int e = 0; e < kE; ++e) {
+  for (int e = 0; e < 4; ++e) {
 #pragma unroll
     for (int k = 0; k < K; ++k) mine[e * (K + 1) + k] = dw[k][e];
     mine[e * (K + 1) + K] = db[e];
   }
   __syncthreads();
-  const int n = kConvChunks * kE * (K + 1);
-  const int cbase = blockIdx.x * kConvChunks * kE;
-  float* pr = part + ((size_t)(b * gridDim.y + blockIdx.y) * C + cbase) * (K + 1);
-  for (int i = threadIdx.y * kConvChunks + threadIdx.x; i < n; i += kConvChunks * kConvBwdSlots) {
-    if (cbase + i / (K + 1) >= C) continue;
+  constexpr int n = 32 * 4 * (K + 1);  // one warp's channels x (taps + bias)
+  float* pr = part + ((size_t)(b * gridDim.y + blockIdx.y) * C + cs) * (K + 1);
+  for (int i = threadIdx.x; i < n; i += kConvBwdWarps * 32) {
+    if (cs + i / (K + 1) >= C) continue;
     float t = 0.f;
-    for (int sl = 0; sl < kConvBwdSlots; ++sl) t += s_red[sl][i];
+    for (int wi = 0; wi < kConvBwdWarps; ++wi) t += red[wi * n + i];
     pr[i] = t;
   }
 }
 
-// dw, dbias: the (b, tile) partials summed in order
+// dw, dbias: the per-CTA partials summed along time in order
 __global__ void k_conv_dw(int nparts, int C, int K, const float* __restrict__ part,
                           float* __restrict__ dw, float* __restrict__ dbias) {
   const int n = C * (K + 1);
@@ -222,24 +377,70 @@ __global__ void k_conv_dw(int nparts, int C, int K, const float* __restrict__ pa
   }
 }
 
+template <typename T>
+bool conv_map(CUtensorMap* m, const void* base, long long rows, int C, int box_rows) {
+  return encode_rows_2d(m, base, sizeof(T) == 2, (uint64_t)rows, (uint64_t)C, kConvCols,
+                        (uint32_t)box_rows);
+}
+
+// CTAs per (channel block, batch row) column: as many as fill the GPU once
+// (from the kernel's occupancy), at most conv_max_ctas_per_column(T) (runs
+// of about kConvMinRun steps or more with kConvBwdWarps warps a CTA) and at
+// least 1.
+template <typename KernelT>
+cudaError_t conv_ctas_per_column(KernelT kernel, int threads, size_t smem, long long cols, int T_,
+                                 int* out) {
+  int dev = 0, nsm = 0, occ = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 (int)smem);
+  if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, threads, smem);
+  if (e != cudaSuccess) return e;
+  long long cpc = (long long)nsm * occ / cols;
+  const long long cap = conv_max_ctas_per_column(T_);
+  if (cpc > cap) cpc = cap;
+  *out = cpc < 1 ? 1 : (int)cpc;
+  return cudaSuccess;
+}
+
 template <typename T, int K>
 cudaError_t conv_fwd_t(long long B, int T_, int C, const void* x, const float* w,
                        const float* bias, const float* init, void* out, cudaStream_t s) {
-  const dim3 grid((C / kE + kConvChunks - 1) / kConvChunks, (T_ + kConvFwdRows - 1) / kConvFwdRows,
-                  (unsigned)B);
-  k_conv_fwd<T, K><<<grid, dim3(kConvChunks, kConvFwdSlots), 0, s>>>(T_, C, (const T*)x, w, bias,
-                                                                  init, (T*)out);
+  using G = ConvGeom<T, K>;
+  CUtensorMap xm;
+  if (!conv_map<T>(&xm, x, B * T_, C, kConvFwdStep)) return cudaErrorInvalidValue;
+  const size_t smem = G::fwd_smem();
+  const long long stripes = (C + kConvCols - 1) / kConvCols;
+  int cpc = 1;
+  cudaError_t e = conv_ctas_per_column(k_conv_fwd<T, K>, kConvFwdWarps * 32, smem, stripes * B, T_,
+                                       &cpc);
+  if (e != cudaSuccess) return e;
+  k_conv_fwd<T, K><<<dim3((unsigned)stripes, (unsigned)cpc, (unsigned)B), kConvFwdWarps * 32, smem,
+                     s>>>(
+      xm, T_, C, (const T*)x, w, bias, init, (T*)out);
   return cudaGetLastError();
 }
 
 template <typename T, int K>
 cudaError_t conv_bwd_t(long long B, int T_, int C, const void* x, const float* w,
                        const float* bias, const float* init, const void* dout, void* dx,
-                       float* part, cudaStream_t s) {
-  const dim3 grid((C / kE + kConvChunks - 1) / kConvChunks, (T_ + kConvBwdRows - 1) / kConvBwdRows,
-                  (unsigned)B);
-  k_conv_bwd<T, K><<<grid, dim3(kConvChunks, kConvBwdSlots), 0, s>>>(T_, C, (const T*)x, w, bias,
-                                                                  init, (const T*)dout, (T*)dx, part);
+                       float* part, int* nparts, cudaStream_t s) {
+  using G = ConvGeom<T, K>;
+  CUtensorMap xm, gm;
+  if (!conv_map<T>(&xm, x, B * T_, C, kConvBwdStep) ||
+      !conv_map<T>(&gm, dout, B * T_, C, kConvBwdStep))
+    return cudaErrorInvalidValue;
+  const size_t smem = G::bwd_smem();
+  const long long stripes = (C + kConvCols - 1) / kConvCols;
+  int cpc = 1;
+  cudaError_t e = conv_ctas_per_column(k_conv_bwd<T, K>, kConvBwdWarps * 32, smem, stripes * B, T_,
+                                       &cpc);
+  if (e != cudaSuccess) return e;
+  *nparts = (int)(B * cpc);
+  k_conv_bwd<T, K><<<dim3((unsigned)stripes, (unsigned)cpc, (unsigned)B), kConvBwdWarps * 32, smem,
+                     s>>>(
+      xm, gm, T_, C, (const T*)x, w, bias, init, (T*)dx, part);
   return cudaGetLastError();
 }
 
@@ -271,9 +472,10 @@ cudaError_t conv_backward(long long B, int T_, int C, int K, bool bf16, const vo
                           const float* w, const float* bias, const float* init, const void* dout,
                           void* dx, float* dw, float* dbias, float* part, cudaStream_t s) {
   cudaError_t e;
+  int nparts = 1;
   {
     LaunchScope ls("conv1d_silu_bwd", s);
-#define SSD_CONV_B(TT, KK) e = conv_bwd_t<TT, KK>(B, T_, C, x, w, bias, init, dout, dx, part, s)
+#define SSD_CONV_B(TT, KK) e = conv_bwd_t<TT, KK>(B, T_, C, x, w, bias, init, dout, dx, part, &nparts, s)
     if (bf16) {
       switch (K) {
         case 1: SSD_CONV_B(__nv_bfloat16, 1); break;
@@ -292,12 +494,18 @@ cudaError_t conv_backward(long long B, int T_, int C, int K, bool bf16, const vo
 #undef SSD_CONV_B
   }
   if (e != cudaSuccess) return e;
-  const int nparts = (int)(B * ((T_ + kConvBwdRows - 1) / kConvBwdRows));
   {
     LaunchScope ls("conv1d_silu_dw", s);
     k_conv_dw<<<(C * (K + 1) + 255) / 256, 256, 0, s>>>(nparts, C, K, part, dw, dbias);
   }
   return cudaGetLastError();
+}
+
+cudaError_t conv_read_and_clear_error(unsigned int* out) {
+  cudaError_t e = cudaMemcpyFromSymbol(out, g_conv_error, sizeof(unsigned int));
+  if (e != cudaSuccess) return e;
+  const unsigned int zero = 0;
+  return cudaMemcpyToSymbol(g_conv_error, &zero, sizeof(unsigned int));
 }
 
 }  // namespace ssd

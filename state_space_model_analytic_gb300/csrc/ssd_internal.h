@@ -2,6 +2,7 @@
 // launchers.  Not part of the public ABI.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -65,20 +66,21 @@ cudaError_t norm_backward(long long rows, int width, bool bf16, const void* y, c
                           const float* w, float eps, const float* inv_rms, const void* g, void* dy,
                           void* dz, float* dw, float* part, cudaStream_t s);
 
-// Causal depthwise conv1d + SiLU before the core (ssd_conv.cu): a CTA is
-// kConvChunks 4-channel vectors x a stack of tiles along time (forward:
-// kConvFwdSlots tiles of kConvFwdTile steps; backward: kConvBwdSlots tiles
-// of kConvBwdTile steps, kConvBwdRows steps); the backward keeps per-CTA
-// partials of dw, dbias in [B * ceil(T / kConvBwdRows)][C][K + 1] and is
-// register-capped so that kConvBwdMinCtas CTAs fit on an SM.
-constexpr int kConvChunks = 32;
-constexpr int kConvFwdSlots = 8;
-constexpr int kConvFwdTile = 32;
-constexpr int kConvFwdRows = kConvFwdSlots * kConvFwdTile;
-constexpr int kConvBwdSlots = 4;
-constexpr int kConvBwdTile = 64;
-constexpr int kConvBwdRows = kConvBwdSlots * kConvBwdTile;
-constexpr int kConvBwdMinCtas = 2;
+// Causal depthwise conv1d + SiLU before the core (ssd_conv.cu): a warp owns
+// kConvCols channels of one batch row over a run of steps; the backward's
+// CTAs are kConvBwdWarps such runs and keep per-CTA partials of dw, dbias in
+// [B * ctas_per_column][C][K + 1], ctas_per_column <=
+// conv_max_ctas_per_column(T) (runs of kConvMinRun steps or more).
+constexpr int kConvCols = 128;
+constexpr int kConvBwdWarps = 8;
+constexpr int kConvMinRun = 16;
+inline long long conv_max_ctas_per_column(long long T) {
+  const long long c =
+      (T + (long long)kConvBwdWarps * kConvMinRun - 1) / ((long long)kConvBwdWarps * kConvMinRun);
+  return c < 1 ? 1 : c;
+}
+// reads and clears the conv kernels' device error word (a TMA wait gave up)
+cudaError_t conv_read_and_clear_error(unsigned int* out);
 cudaError_t conv_forward(long long B, int T_, int C, int K, bool bf16, const void* x,
                          const float* w, const float* bias, const float* init, void* out,
                          cudaStream_t s);
@@ -110,6 +112,12 @@ constexpr int kDtPostSlices = 32;
 cudaError_t dt_post(const Problem& p, const float* dt_raw, const float* dt_bias,
                     const float* a_log, float* d_dt_raw, float* d_dt_bias, float* d_a_log,
                     float* part);
+
+// 2D row-major [rows][cols] tensor map (bf16 or fp32) with an unswizzled
+// {box_cols, box_rows} box, through the driver entry point (ssd_tc.cu);
+// false if the driver does not provide the encoder or rejects the map.
+bool encode_rows_2d(CUtensorMap* m, const void* base, bool bf16, uint64_t rows, uint64_t cols,
+                    uint32_t box_cols, uint32_t box_rows);
 
 // Per-kernel event trace (see ssd_trace_begin in include/ssd.h).  A
 // LaunchScope brackets exactly one kernel launch: it records the start event

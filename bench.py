@@ -47,6 +47,8 @@ def parse_args():
                     help="seconds of oracle work for the cpu_baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--next-iters", type=int, default=200,
+                    help="timed calls per direction of the gated RMSNorm and conv1d lines")
     return ap.parse_args()
 
 
@@ -561,7 +563,7 @@ def main():
                 p_(n_gr["dy"]), p_(n_gr["dz"]), p_(n_gr["dweight"]), p_(nws), nws.numel(),
                 stream.cuda_stream or None))
 
-        def timed(fn, n=200):
+        def timed(fn, n=max(1, args.next_iters)):
             for _ in range(args.warmup):
                 fn()
                 flush.fill_(1.0)
@@ -615,7 +617,7 @@ def main():
                 Bz, T, Cc, Kc, dtc, p_(cx), p_(cw), p_(cb), p_(ci), p_(cg), p_(c_dx), p_(c_dw),
                 p_(c_db), p_(cws), cws.numel(), stream.cuda_stream or None))
 
-        def ctimed(fn, n=200):
+        def ctimed(fn, n=max(1, args.next_iters)):
             for _ in range(args.warmup):
                 fn()
                 flush.fill_(1.0)

@@ -57,9 +57,9 @@ struct Problem {
 };
 
 // Gated RMSNorm after the core (ssd_norm.cu).  The backward keeps per-CTA
-// column sums of the weight gradient in part[kNormMaxCtas][width].
+// column sums of the weight gradient in part[grid][width], grid <=
+// kNormMaxCtas.
 constexpr int kNormMaxCtas = 512;
-int norm_bwd_ctas(long long rows);
 cudaError_t norm_forward(long long rows, int width, bool bf16, const void* y, const void* z,
                          const float* w, float eps, void* out, float* inv_rms, cudaStream_t s);
 cudaError_t norm_backward(long long rows, int width, bool bf16, const void* y, const void* z,

@@ -9,11 +9,17 @@
 //   dy    = gn * inv_rms - y * dot * inv_rms^3 / width
 //   dz    = g * n * w * silu'(z),  silu'(z) = s (1 + z (1 - s)), s = sigmoid(z)
 //
-// One warp per row, 16-byte vector accesses (the rows are HBM-streamed; the
-// second pass over y re-reads it from L1).  dw: each warp sums its rows'
-// products for the columns its lanes own into a per-warp shared-memory row,
-// the CTA sums its warps in order, and a final kernel sums the CTAs in order
-// (deterministic).
+// Work split: a CTA of up to 256 threads spans the row (thread t owns the
+// 16-byte column vectors t, t + blockDim, ...: V of them, V in {1, 2, 4}) and
+// walks groups of R rows (forward 4 / V, backward 2 / V or 1), persistently
+// over the rows (CTA j takes groups j, j + grid, ...).  A thread loads its
+// vectors of all R rows before using any, so several 16-byte loads per
+// operand are in flight per thread at a small register cost; the row sums (sum y^2, and the backward's dot) go
+// through one block reduction per group (warp shuffles, then the warps'
+// partials in order from shared memory).  The backward keeps its columns' dw
+// in registers over all its rows, writes them as the CTA's partial row, and a
+// final kernel sums the CTAs in a fixed order (deterministic for a given grid,
+// which follows the GPU's SM count).
 #include <cuda_bf16.h>
 
 #include "ssd_common.cuh"
@@ -22,15 +28,16 @@
 namespace ssd {
 namespace {
 
-constexpr int kNormWarps = 8;  // warps (rows in flight) per CTA
+constexpr int kNormThreads = 256;
+constexpr int kNormWarpsMax = kNormThreads / 32;
 
 template <typename T>
 struct Vec;  // 16 bytes of T
 template <>
 struct Vec<float> {
   static constexpr int n = 4;
-  __device__ static void load(const void* p, float* v) {
-    const float4 q = *(const float4*)p;
+  using raw = float4;
+  __device__ static void cvt(const raw& q, float* v) {
     v[0] = q.x; v[1] = q.y; v[2] = q.z; v[3] = q.w;
   }
   __device__ static void store(void* p, const float* v) { *(float4*)p = make_float4(v[0], v[1], v[2], v[3]); }
@@ -38,8 +45,8 @@ struct Vec<float> {
 template <>
 struct Vec<__nv_bfloat16> {
   static constexpr int n = 8;
-  __device__ static void load(const void* p, float* v) {
-    const uint4 q = *(const uint4*)p;
+  using raw = uint4;
+  __device__ static void cvt(const raw& q, float* v) {
     const __nv_bfloat162* h = (const __nv_bfloat162*)&q;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -63,186 +70,296 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-__device__ __forceinline__ float sigmoidf_(float z) { return 1.f / (1.f + expf(-z)); }
-
-template <typename T>
-__global__ void __launch_bounds__(32 * kNormWarps)
-k_norm_fwd(long long rows, int width, float eps, const T* __restrict__ y, const T* __restrict__ z,
-           const float* __restrict__ w, T* __restrict__ out, float* __restrict__ inv_rms) {
-  constexpr int E = Vec<T>::n;
-  const int lane = threadIdx.x & 31;
-  const long long r = (long long)blockIdx.x * kNormWarps + (threadIdx.x >> 5);
-  if (r >= rows) return;
-  const T* yr = y + r * width;
-  float ss = 0.f;
-#pragma unroll 4
-  for (int c = lane * E; c < width; c += 32 * E) {
-    float v[E];
-    Vec<T>::load(yr + c, v);
-#pragma unroll
-    for (int i = 0; i < E; ++i) ss = fmaf(v[i], v[i], ss);
-  }
-  const float inv = 1.f / sqrtf(warp_sum(ss) / (float)width + eps);
-  const T* zr = z + r * width;
-  T* orow = out + r * width;
-#pragma unroll 4
-  for (int c = lane * E; c < width; c += 32 * E) {
-    float v[E], zz[E], wv[E], o[E];
-    Vec<T>::load(yr + c, v);
-    Vec<T>::load(zr + c, zz);
-    Vec<float>::load(w + c, wv);
-    if constexpr (E == 8) Vec<float>::load(w + c + 4, wv + 4);
-#pragma unroll
-    for (int i = 0; i < E; ++i) o[i] = (v[i] * inv) * wv[i] * (zz[i] * sigmoidf_(zz[i]));
-    Vec<T>::store(orow + c, o);
-  }
-  if (inv_rms && lane == 0) inv_rms[r] = inv;
+// logistic sigmoid 1 / (1 + 2^(-z log2 e)) from the hardware base-2
+// exponential and reciprocal approximations (about 1e-6 relative, exact
+// limits at both ends)
+__device__ __forceinline__ float sigmoidf_(float z) {
+  float e, r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(z * -1.4426950408889634f));
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.f + e));
+  return r;
 }
 
-// Persistent: warp j of CTA b takes rows (b * kNormWarps + j) + k * (grid * kNormWarps).
+// Block sums of NV values per thread (row partials): every thread gets the
+// totals, the warps' partials added in warp order.  red: [2][NV][warps]
+// shared floats, alternated between calls (buf) so that one barrier per call
+// suffices.
+template <int NV>
+__device__ __forceinline__ void block_sums(float (&v)[NV], float* red, int buf) {
+  const int nw = blockDim.x >> 5, wp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float* r = red + buf * NV * kNormWarpsMax;
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    const float s = warp_sum(v[i]);
+    if (lane == 0) r[i * kNormWarpsMax + wp] = s;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    float t = 0.f;
+    for (int j = 0; j < nw; ++j) t += r[i * kNormWarpsMax + j];
+    v[i] = t;
+  }
+}
+
+template <typename T, int V>
+__global__ void __launch_bounds__(kNormThreads)
+k_norm_fwd(long long rows, int width, float eps, const T* __restrict__ y, const T* __restrict__ z,
+           const float* __restrict__ w, T* __restrict__ out, float* __restrict__ inv_rms) {
+  constexpr int E = Vec<T>::n, R = 4 / V;
+  using raw = typename Vec<T>::raw;
+  __shared__ float red[2 * R * kNormWarpsMax];
+  float wv[V][E];
+#pragma unroll
+  for (int v = 0; v < V; ++v) {
+    const int c = (v * blockDim.x + threadIdx.x) * E;
+#pragma unroll
+    for (int i = 0; i < E; ++i) wv[v][i] = w[c + i];
+  }
+  const long long ngroups = (rows + R - 1) / R;
+  int buf = 0;
+  for (long long gi = blockIdx.x; gi < ngroups; gi += gridDim.x, buf ^= 1) {
+    const long long r0 = gi * R;
+    raw qy[R][V], qz[R][V];
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+      for (int v = 0; v < V; ++v) {
+        const long long row = min(r0 + r, rows - 1);  // past the end: a valid row, unused
+        const long long off = row * width + (long long)(v * blockDim.x + threadIdx.x) * E;
+        qy[r][v] = *(const raw*)(y + off);
+        qz[r][v] = *(const raw*)(z + off);
+      }
+    float ss[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      ss[r] = 0.f;
+#pragma unroll
+      for (int v = 0; v < V; ++v) {
+        float a[E];
+        Vec<T>::cvt(qy[r][v], a);
+#pragma unroll
+        for (int i = 0; i < E; ++i) ss[r] = fmaf(a[i], a[i], ss[r]);
+      }
+    }
+    block_sums<R>(ss, red, buf);
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      if (r0 + r >= rows) break;
+      const float inv = 1.f / sqrtf(ss[r] / (float)width + eps);
+#pragma unroll
+      for (int v = 0; v < V; ++v) {
+        float a[E], zz[E], o[E];
+        Vec<T>::cvt(qy[r][v], a);
+        Vec<T>::cvt(qz[r][v], zz);
+#pragma unroll
+        for (int i = 0; i < E; ++i) o[i] = (a[i] * inv) * wv[v][i] * (zz[i] * sigmoidf_(zz[i]));
+        Vec<T>::store(out + (r0 + r) * width + (long long)(v * blockDim.x + threadIdx.x) * E, o);
+      }
+      if (inv_rms && threadIdx.x == 0) inv_rms[r0 + r] = inv;
+    }
+  }
+}
+
 // part: [grid][width] per-CTA column sums of g * gate * n.
-template <typename T>
-__global__ void __launch_bounds__(32 * kNormWarps)
+template <typename T, int V>
+__global__ void __launch_bounds__(kNormThreads, 2)
 k_norm_bwd(long long rows, int width, float eps, const T* __restrict__ y, const T* __restrict__ z,
            const float* __restrict__ w, const float* __restrict__ inv_in, const T* __restrict__ g,
            T* __restrict__ dy, T* __restrict__ dz, float* __restrict__ part) {
-  constexpr int E = Vec<T>::n;
-  extern __shared__ float s_dw[];  // [kNormWarps][width]
-  const int lane = threadIdx.x & 31, wp = threadIdx.x >> 5;
-  float* my = s_dw + (size_t)wp * width;
-  for (int c = lane; c < width; c += 32) my[c] = 0.f;
-  __syncwarp();
-  const long long stride = (long long)gridDim.x * kNormWarps;
-  for (long long r = (long long)blockIdx.x * kNormWarps + wp; r < rows; r += stride) {
-    const T* yr = y + r * width;
-    const T* zr = z + r * width;
-    const T* gr = g + r * width;
-    float inv;
-    if (inv_in) {
-      inv = inv_in[r];
-    } else {
-      float ss = 0.f;
-    #pragma unroll 4
-  for (int c = lane * E; c < width; c += 32 * E) {
-        float v[E];
-        Vec<T>::load(yr + c, v);
+  constexpr int E = Vec<T>::n, R = V < 2 ? 2 : 1;
+  using raw = typename Vec<T>::raw;
+  __shared__ float red[2 * 2 * R * kNormWarpsMax];
+  float wv[V][E], dw[V][E];
 #pragma unroll
-        for (int i = 0; i < E; ++i) ss = fmaf(v[i], v[i], ss);
-      }
-      inv = 1.f / sqrtf(warp_sum(ss) / (float)width + eps);
-    }
-    // dot = sum_w (g * gate * w) * y
-    float dot = 0.f;
-  #pragma unroll 4
-  for (int c = lane * E; c < width; c += 32 * E) {
-      float v[E], zz[E], gg[E], wv[E];
-      Vec<T>::load(yr + c, v);
-      Vec<T>::load(zr + c, zz);
-      Vec<T>::load(gr + c, gg);
-      Vec<float>::load(w + c, wv);
-      if constexpr (E == 8) Vec<float>::load(w + c + 4, wv + 4);
+  for (int v = 0; v < V; ++v) {
+    const int c = (v * blockDim.x + threadIdx.x) * E;
 #pragma unroll
-      for (int i = 0; i < E; ++i) dot = fmaf(gg[i] * (zz[i] * sigmoidf_(zz[i])) * wv[i], v[i], dot);
-    }
-    dot = warp_sum(dot);
-    const float k3 = dot * inv * inv * inv / (float)width;
-  #pragma unroll 4
-  for (int c = lane * E; c < width; c += 32 * E) {
-      float v[E], zz[E], gg[E], wv[E], oy[E], oz[E], dwv[E];
-      Vec<T>::load(yr + c, v);
-      Vec<T>::load(zr + c, zz);
-      Vec<T>::load(gr + c, gg);
-      Vec<float>::load(w + c, wv);
-      if constexpr (E == 8) Vec<float>::load(w + c + 4, wv + 4);
-#pragma unroll
-      for (int i = 0; i < E; ++i) {
-        const float s = sigmoidf_(zz[i]);
-        const float gate = zz[i] * s;
-        const float nrm = v[i] * inv;
-        oy[i] = gg[i] * gate * wv[i] * inv - v[i] * k3;
-        oz[i] = gg[i] * nrm * wv[i] * (s * (1.f + zz[i] * (1.f - s)));
-        dwv[i] = gg[i] * gate * nrm;
-      }
-#pragma unroll
-      for (int i = 0; i < E; i += 4) {
-        float4 a = *(float4*)(my + c + i);
-        a.x += dwv[i]; a.y += dwv[i + 1]; a.z += dwv[i + 2]; a.w += dwv[i + 3];
-        *(float4*)(my + c + i) = a;
-      }
-      Vec<T>::store(dy + r * width + c, oy);
-      Vec<T>::store(dz + r * width + c, oz);
+    for (int i = 0; i < E; ++i) {
+      wv[v][i] = w[c + i];
+      dw[v][i] = 0.f;
     }
   }
-  __syncthreads();
-  // this CTA's column sums, warps in order
-  for (int c = threadIdx.x; c < width; c += blockDim.x) {
-    float t = 0.f;
-    for (int j = 0; j < kNormWarps; ++j) t += s_dw[(size_t)j * width + c];
-    part[(size_t)blockIdx.x * width + c] = t;
+  const long long ngroups = (rows + R - 1) / R;
+  int buf = 0;
+  for (long long gi = blockIdx.x; gi < ngroups; gi += gridDim.x, buf ^= 1) {
+    const long long r0 = gi * R;
+    raw qy[R][V], qz[R][V], qg[R][V];
+    float inv[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      const long long row = min(r0 + r, rows - 1);  // past the end: a valid row, unused
+      inv[r] = inv_in ? inv_in[row] : 0.f;
+#pragma unroll
+      for (int v = 0; v < V; ++v) {
+        const long long off = row * width + (long long)(v * blockDim.x + threadIdx.x) * E;
+        qy[r][v] = *(const raw*)(y + off);
+        qz[r][v] = *(const raw*)(z + off);
+        qg[r][v] = *(const raw*)(g + off);
+      }
+    }
+    // per row: dot = sum_w (g * gate * w) * y, and sum y^2 when inv_rms is not given
+    float sums[2 * R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      float dot = 0.f, ss = 0.f;
+#pragma unroll
+      for (int v = 0; v < V; ++v) {
+        float a[E], zz[E], gg[E];
+        Vec<T>::cvt(qy[r][v], a);
+        Vec<T>::cvt(qz[r][v], zz);
+        Vec<T>::cvt(qg[r][v], gg);
+#pragma unroll
+        for (int i = 0; i < E; ++i) {
+          dot = fmaf(gg[i] * (zz[i] * sigmoidf_(zz[i])) * wv[v][i], a[i], dot);
+          ss = fmaf(a[i], a[i], ss);
+        }
+      }
+      sums[2 * r] = dot;
+      sums[2 * r + 1] = ss;
+    }
+    block_sums<2 * R>(sums, red, buf);
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      if (r0 + r >= rows) break;
+      const float iv = inv_in ? inv[r] : 1.f / sqrtf(sums[2 * r + 1] / (float)width + eps);
+      const float k3 = sums[2 * r] * iv * iv * iv / (float)width;
+#pragma unroll
+      for (int v = 0; v < V; ++v) {
+        float a[E], zz[E], gg[E], oy[E], oz[E];
+        Vec<T>::cvt(qy[r][v], a);
+        Vec<T>::cvt(qz[r][v], zz);
+        Vec<T>::cvt(qg[r][v], gg);
+#pragma unroll
+        for (int i = 0; i < E; ++i) {
+          const float s = sigmoidf_(zz[i]);
+          const float gate = zz[i] * s;
+          const float nrm = a[i] * iv;
+          oy[i] = gg[i] * gate * wv[v][i] * iv - a[i] * k3;
+          oz[i] = gg[i] * nrm * wv[v][i] * (s * (1.f + zz[i] * (1.f - s)));
+          dw[v][i] += gg[i] * gate * nrm;
+        }
+        const long long off = (r0 + r) * width + (long long)(v * blockDim.x + threadIdx.x) * E;
+        Vec<T>::store(dy + off, oy);
+        Vec<T>::store(dz + off, oz);
+      }
+    }
+  }
+  // this CTA's column sums
+#pragma unroll
+  for (int v = 0; v < V; ++v) {
+    const int c = (v * blockDim.x + threadIdx.x) * E;
+#pragma unroll
+    for (int i = 0; i < E; ++i) part[(size_t)blockIdx.x * width + c + i] = dw[v][i];
   }
 }
 
-
-__global__ void k_norm_dw(int ncta, int width, const float* __restrict__ part, float* __restrict__ dw) {
-  for (int c = blockIdx.x * blockDim.x + threadIdx.x; c < width; c += gridDim.x * blockDim.x) {
-    float t = 0.f;
-    for (int b = 0; b < ncta; ++b) t += part[(size_t)b * width + c];
-    dw[c] = t;
+// dw[c] = sum over the CTAs' partial rows, in a fixed order: a CTA takes 32
+// columns; thread (slice sl, column j) sums the partials sl, sl + 32, ... in
+// order (a warp reads 32 consecutive floats of one partial row), then the 32
+// slice sums of each column are added in slice order.
+constexpr int kNormDwSlices = 32;
+__global__ void __launch_bounds__(32 * kNormDwSlices)
+k_norm_dw(int ncta, int width, const float* __restrict__ part, float* __restrict__ dw) {
+  __shared__ float sl_sum[kNormDwSlices][33];
+  const int j = threadIdx.x & 31, sl = threadIdx.x >> 5;
+  const int c = blockIdx.x * 32 + j;
+  float t = 0.f;
+  if (c < width)
+    for (int b = sl; b < ncta; b += kNormDwSlices) t += part[(size_t)b * width + c];
+  sl_sum[sl][j] = t;
+  __syncthreads();
+  if (sl == 0 && c < width) {
+    float u = 0.f;
+    for (int i = 0; i < kNormDwSlices; ++i) u += sl_sum[i][j];
+    dw[c] = u;
   }
+}
+
+// threads per CTA and vectors per thread for a row of `width` elements of
+// `esz` bytes (16-byte vectors; width / (16 / esz) is a multiple of 32)
+void norm_shape(int width, int esz, int* threads, int* V) {
+  const int nvec = width / (16 / esz);
+  *threads = nvec < kNormThreads ? nvec : kNormThreads;
+  *V = nvec / *threads;
+}
+
+template <typename KernelT>
+int norm_grid(KernelT kernel, int threads, long long ngroups, int cap) {
+  int dev = 0, nsm = 0, occ = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, threads, 0);
+  long long g = (long long)(nsm > 0 ? nsm : 1) * (occ > 0 ? occ : 1);
+  if (g > cap) g = cap;
+  if (g > ngroups) g = ngroups;
+  return (int)(g < 1 ? 1 : g);
+}
+
+template <typename T, int V>
+cudaError_t norm_fwd_t(long long rows, int width, int threads, const void* y, const void* z,
+                       const float* w, float eps, void* out, float* inv_rms, cudaStream_t s) {
+  const long long ngroups = (rows + 4 / V - 1) / (4 / V);
+  const int grid = norm_grid(k_norm_fwd<T, V>, threads, ngroups, 1 << 20);
+  k_norm_fwd<T, V><<<grid, threads, 0, s>>>(rows, width, eps, (const T*)y, (const T*)z, w, (T*)out,
+                                            inv_rms);
+  return cudaGetLastError();
+}
+
+template <typename T, int V>
+cudaError_t norm_bwd_t(long long rows, int width, int threads, const void* y, const void* z,
+                       const float* w, float eps, const float* inv_rms, const void* g, void* dy,
+                       void* dz, float* part, int* ncta, cudaStream_t s) {
+  const long long ngroups = (rows + (V < 2 ? 2 : 1) - 1) / (V < 2 ? 2 : 1);
+  const int grid = norm_grid(k_norm_bwd<T, V>, threads, ngroups, kNormMaxCtas);
+  *ncta = grid;
+  k_norm_bwd<T, V><<<grid, threads, 0, s>>>(rows, width, eps, (const T*)y, (const T*)z, w, inv_rms,
+                                            (const T*)g, (T*)dy, (T*)dz, part);
+  return cudaGetLastError();
 }
 
 }  // namespace
 
-int norm_bwd_ctas(long long rows) {
-  int nsm = 0, dev = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
-  long long want = (rows + kNormWarps - 1) / kNormWarps;
-  long long cap = 3LL * (nsm > 0 ? nsm : 1);  // three 64 KB CTAs per SM at width 2048
-  if (cap > kNormMaxCtas) cap = kNormMaxCtas;
-  return (int)(want < cap ? want : cap);
-}
-
 cudaError_t norm_forward(long long rows, int width, bool bf16, const void* y, const void* z,
                          const float* w, float eps, void* out, float* inv_rms, cudaStream_t s) {
-  const unsigned grid = (unsigned)((rows + kNormWarps - 1) / kNormWarps);
+  int threads = 0, V = 0;
+  norm_shape(width, bf16 ? 2 : 4, &threads, &V);
   LaunchScope ls("rmsnorm_gated_fwd", s);
-  if (bf16)
-    k_norm_fwd<__nv_bfloat16><<<grid, 32 * kNormWarps, 0, s>>>(
-        rows, width, eps, (const __nv_bfloat16*)y, (const __nv_bfloat16*)z, w,
-        (__nv_bfloat16*)out, inv_rms);
-  else
-    k_norm_fwd<float><<<grid, 32 * kNormWarps, 0, s>>>(rows, width, eps, (const float*)y,
-                                                      (const float*)z, w, (float*)out, inv_rms);
-  return cudaGetLastError();
+#define SSD_NORM_F(TT, VV) return norm_fwd_t<TT, VV>(rows, width, threads, y, z, w, eps, out, inv_rms, s)
+  if (bf16) {  // width <= 4096: at most 2 vectors a thread
+    if (V == 1) SSD_NORM_F(__nv_bfloat16, 1);
+    SSD_NORM_F(__nv_bfloat16, 2);
+  }
+  if (V == 1) SSD_NORM_F(float, 1);
+  if (V == 2) SSD_NORM_F(float, 2);
+  SSD_NORM_F(float, 4);
+#undef SSD_NORM_F
 }
 
 cudaError_t norm_backward(long long rows, int width, bool bf16, const void* y, const void* z,
                           const float* w, float eps, const float* inv_rms, const void* g, void* dy,
                           void* dz, float* dw, float* part, cudaStream_t s) {
-  const int ncta = norm_bwd_ctas(rows);
-  const size_t smem = (size_t)kNormWarps * width * sizeof(float);
+  int threads = 0, V = 0, ncta = 1;
+  norm_shape(width, bf16 ? 2 : 4, &threads, &V);
   cudaError_t e;
-  if (bf16)
-    e = cudaFuncSetAttribute(k_norm_bwd<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  else
-    e = cudaFuncSetAttribute(k_norm_bwd<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
   {
     LaunchScope ls("rmsnorm_gated_bwd", s);
-    if (bf16)
-      k_norm_bwd<__nv_bfloat16><<<ncta, 32 * kNormWarps, smem, s>>>(
-          rows, width, eps, (const __nv_bfloat16*)y, (const __nv_bfloat16*)z, w, inv_rms,
-          (const __nv_bfloat16*)g, (__nv_bfloat16*)dy, (__nv_bfloat16*)dz, part);
-    else
-      k_norm_bwd<float><<<ncta, 32 * kNormWarps, smem, s>>>(
-          rows, width, eps, (const float*)y, (const float*)z, w, inv_rms, (const float*)g,
-          (float*)dy, (float*)dz, part);
+#define SSD_NORM_B(TT, VV) \
+  e = norm_bwd_t<TT, VV>(rows, width, threads, y, z, w, eps, inv_rms, g, dy, dz, part, &ncta, s)
+    if (bf16) {  // width <= 4096: at most 2 vectors a thread
+      if (V == 1) SSD_NORM_B(__nv_bfloat16, 1);
+      else SSD_NORM_B(__nv_bfloat16, 2);
+    } else {
+      if (V == 1) SSD_NORM_B(float, 1);
+      else if (V == 2) SSD_NORM_B(float, 2);
+      else SSD_NORM_B(float, 4);
+    }
+#undef SSD_NORM_B
   }
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (e != cudaSuccess) return e;
   {
     LaunchScope ls("rmsnorm_gated_dw", s);
-    k_norm_dw<<<(width + 255) / 256, 256, 0, s>>>(ncta, width, part, dw);
+    k_norm_dw<<<(width + 31) / 32, 32 * kNormDwSlices, 0, s>>>(ncta, width, part, dw);
   }
   return cudaGetLastError();
 }

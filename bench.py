@@ -83,6 +83,9 @@ def kernel_bytes(name, d, has_h0):
         # fused forward state scan: x, B, dt (+h0) in; fp32 history, final state
         # and the bf16 copy of the history out
         "state_scan_fwd": z["x"] + z["dt"] + z["bc"] + z["h0"] + z["st"] + z["hs"] + z["st"] // 2,
+        # single-pass forward (state pass by look-back inside the chunk scan):
+        # x, dt, B, C (+h0) in; y, fp32 history and final state out
+        "fwd_single": 2 * z["x"] + z["dt"] + 2 * z["bc"] + z["h0"] + z["st"] + z["hs"],
         # fused backward state scan: dy, C, dt, fp32 history in; bf16 state and
         # state-gradient rows and dh0 out
         "state_scan_bwd": z["x"] + z["dt"] + z["bc"] + z["st"] + z["st"] + z["hs"],

@@ -64,6 +64,7 @@ bool tc_backward_supported(const Problem& p);
 void tc_force_path(int path);
 cudaError_t tc_chunk_outer(const Problem& p, int mode, float* out);
 cudaError_t tc_forward_scan(const Problem& p);
+cudaError_t tc_forward_single(const Problem& p);
 bool tc_fused_states(const Problem& p);
 cudaError_t tc_forward_states(const Problem& p);
 cudaError_t tc_backward(const Problem& p);
@@ -158,7 +159,9 @@ size_t carve(Problem* p, char* base, int which) {
   if (which == 0) {
     float* h = (float*)take(states);
     if (!p->hist) p->hist = h;
-    p->hT = take(states / 2);  // bf16 copy of the chunk states for the tensor-core scan
+    // single-pass tensor-core forward: one ready flag per history slot, then
+    // its tile counter
+    p->fwd_flags = (unsigned int*)take((B * nc * H + 1) * sizeof(unsigned int));
     return off;
   }
   p->dstate = (float*)take(states);
@@ -341,15 +344,16 @@ int ssd_forward(const ssd_dims* dims, const void* x, const float* dt, const floa
   const bool tc = tc_supported(p);
   cudaError_t e;
   if (tc && tc_fused_states(p)) {
-    e = tc_forward_states(p);  // also writes the bf16 state rows (p.hT) the scan reads
-    if (e != cudaSuccess) return cuda_fail(e, "forward state-scan kernel");
-  } else {
-    p.hT = nullptr;  // the scan converts the fp32 history itself
-    e = tc ? tc_chunk_outer(p, 0, p.hist) : simt_forward_states(p, p.hist, p.cs_last);
-    if (e != cudaSuccess) return cuda_fail(e, "forward chunk-state kernel");
-    e = simt_state_pass_fwd(p, p.hist, p.cs_last);
-    if (e != cudaSuccess) return cuda_fail(e, "forward state-pass kernel");
+    // one kernel: chunk states, the state pass (look-back) and y
+    e = tc_forward_single(p);
+    if (e != cudaSuccess) return cuda_fail(e, "single-pass forward kernel");
+    return SSD_OK;
   }
+  p.hT = nullptr;  // the scan converts the fp32 history itself
+  e = tc ? tc_chunk_outer(p, 0, p.hist) : simt_forward_states(p, p.hist, p.cs_last);
+  if (e != cudaSuccess) return cuda_fail(e, "forward chunk-state kernel");
+  e = simt_state_pass_fwd(p, p.hist, p.cs_last);
+  if (e != cudaSuccess) return cuda_fail(e, "forward state-pass kernel");
   e = tc ? tc_forward_scan(p) : simt_forward_scan(p);
   if (e != cudaSuccess) return cuda_fail(e, "forward chunk-scan kernel");
   return SSD_OK;

@@ -50,6 +50,7 @@ struct Problem {
   unsigned int* tickets;  // [1 + units] completion counters of the tensor-core backward
   int ntickets;
   float* bwd_part;        // tensor-core backward: fp32 dC, dB partials, 2 slots per CTA
+  unsigned int* fwd_flags;  // [B*nc*H + 1]: single-pass forward slot flags, then its tile counter
   void* hT;        // [B][nc][H][N][P] bf16: chunk-start states, rows n (tensor-core backward)
   void* gT;        // [B][nc][H][N][P] bf16: chunk-end state gradients, rows n
 

@@ -602,7 +602,6 @@ struct ScanMaps {
   CUtensorMap B;   // [B*T][G*N] bf16, box {64, 128}
   CUtensorMap C;   // [B*T][G*N] bf16, box {64, 128}
   CUtensorMap y;   // [B*T][H*P] bf16, box {64, 128} (store)
-  CUtensorMap ht;  // chunk-start states as bf16 rows n: [B*nc*H*N][P], box {64, 128}
 };
 
 // shared-memory layout of k_fwd_scan_tc (offsets from the 1024-aligned base);
@@ -612,9 +611,8 @@ constexpr uint32_t kScanX = 65536;    // X block [128 rows][64 p]
 constexpr uint32_t kScanH = 81920;    // state as bf16 B operand, row n, 64 p (MN-major)
 constexpr uint32_t kScanBytes = 98304;
 
-// kHT: the chunk-start state comes as bf16 rows (TMA) instead of fp32 [P][N]
-// loaded by the threads.
-template <bool kHT>
+// The chunk-start state comes as fp32 [P][N] from the history, converted to
+// bf16 rows by the threads.
 __global__ void __launch_bounds__(256, 2)
 k_fwd_scan_tc(const __grid_constant__ ScanMaps maps, TcDims d, const float* __restrict__ dt,
               const float* __restrict__ A, const float* __restrict__ D,
@@ -659,8 +657,8 @@ k_fwd_scan_tc(const __grid_constant__ ScanMaps maps, TcDims d, const float* __re
   uint32_t load_phase = 0, mma_phase = 0;
   bool ok = true;
 
-  auto issue_loads = [&](int row0, bool with_state) {
-    mbar_expect_tx(&bar_load, (with_state ? 96 : 80) * 1024);
+  auto issue_loads = [&](int row0) {
+    mbar_expect_tx(&bar_load, 80 * 1024);
     tma_load_2d(sC, &maps.C, g * d.N, row0, &bar_load);
     tma_load_2d(sC + 16384, &maps.C, g * d.N + 64, row0, &bar_load);
     tma_load_2d(sB, &maps.B, g * d.N, row0, &bar_load);
@@ -669,16 +667,14 @@ k_fwd_scan_tc(const __grid_constant__ ScanMaps maps, TcDims d, const float* __re
   };
   const int crow = b * d.T + c * Q;
   // C, B, x are inputs that no kernel of this library writes: fetched before
-  // waiting for the kernel launched ahead of this one; the state rows after
-  if (tid == 0) issue_loads(crow, kHT);
+  // waiting for the kernel launched ahead of this one; the states after
+  if (tid == 0) issue_loads(crow);
   grid_dep_wait();
-  if (kHT && tid == 0)
-    tma_load_2d(sH, &maps.ht, 0, ((b * d.nc + c) * d.H + h) * d.N, &bar_load);
 
   // H_{c-1} as bf16 rows n (64 p each): the MN-major B operand of C H^T.
   const float* Hg = hist + (((size_t)b * d.nc + c) * d.H + h) * (size_t)(64 * 128);
   chunk_cumsum_256(d, dt, A, b, c, h, s_cs2, s_dt, scratch);
-  if (!kHT) {  // thread (wg, n) converts p in [32 wg, 32 wg + 32) from fp32 [P][N]
+  {  // thread (wg, n) converts p in [32 wg, 32 wg + 32) from fp32 [P][N]
     const int n = row;
 #pragma unroll
     for (int ch = 0; ch < 4; ++ch) {
@@ -839,27 +835,372 @@ k_fwd_scan_tc(const __grid_constant__ ScanMaps maps, TcDims d, const float* __re
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         float v8[8];
-        if (kHT) {
-          float hf[8];
-          unpack8(*(const uint4*)(sH + sw128(n, wg * 4 + k)), hf);
 #pragma unroll
-          for (int t = 0; t < 8; ++t) v8[t] = fmaf(e127, hf[t], v[k * 8 + t]);
-        } else {
-#pragma unroll
-          for (int t = 0; t < 8; ++t)
-            v8[t] = fmaf(e127, Hg[(size_t)(wg * 32 + k * 8 + t) * 128 + n], v[k * 8 + t]);
-        }
+        for (int t = 0; t < 8; ++t)
+          v8[t] = fmaf(e127, Hg[(size_t)(wg * 32 + k * 8 + t) * 128 + n], v[k * 8 + t]);
         store_row_bf16(sH, n, wg * 4 + k, v8);
       }
       if (tid == 0) {
         bulk_wait_read0();  // y staging (region R1) is reloaded next
-        issue_loads(row0 + 128, false);
+        issue_loads(row0 + 128);
       }
       // sH written by every thread: visible to the next block's MMA
       fence_async_smem();
       fence_before_sync();
       __syncthreads();
       fence_after_sync();
+    }
+  }
+  grid_dep_launch();
+  if (tid == 0) bulk_wait0();
+  fence_before_sync();
+  __syncthreads();
+  if (tid < 32) tmem_dealloc(tm, 256);
+}
+
+// ---------------------------------------------------------------------------
+// Single-pass forward: the chunk-state pass folded into the chunk scan with a
+// bounded look-back, for the shapes whose per-(b, h) state scan fills the GPU.
+// One CTA per (b, chunk, head); a CTA takes its tile from a counter, chunk-
+// major, so the CTA of chunk c - 1 of the same (b, h) took its tile earlier
+// and is resident or finished (no wait can be on a CTA that has not started).
+// Per CTA:
+//   A. before any wait, the chunk's state contributions block by block, the
+//      last block first: S_k^T = B_k^T (w o X_k), w_j = exp(cs_end(k) - cs_j)
+//      dt_j, end(k) the block's last row, with w o X_k written into the C
+//      tile (idle until C) so that block 0's B and X stay as loaded for C;
+//   B. the look-back: wait (bounded) for the flag of the history slot c,
+//      which chunk c - 1 fills with H_{c-1} (slot 0 = h0 or zeros, written
+//      here); H_mid = exp(cs_127) H_{c-1} + S_0 and
+//      H_c = exp(cs_{Q-1} - cs_127) H_mid + S_1 (one block: H_c =
+//      exp(cs_127) H_{c-1} + S_0); publish H_c into slot c + 1 and release
+//      its flag, or write the final state;
+//   C. y block by block as in k_fwd_scan_tc, with H_{c-1} and then H_mid as
+//      the state term.
+// flags: [B][nc][H] slot-ready words, then the tile counter; all zero at
+// launch.  A wait that gives up sets the device error word and goes on with
+// the slot as it is (the outputs are then wrong, nothing hangs).
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned int* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_gpu(unsigned int* p, unsigned v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__global__ void __launch_bounds__(256, 2)
+k_fwd_single_tc(const __grid_constant__ ScanMaps maps, TcDims d, const float* __restrict__ dt,
+                const float* __restrict__ A, const float* __restrict__ D,
+                const float* __restrict__ h0, float* hist, float* __restrict__ final_state,
+                unsigned int* flags) {
+  extern __shared__ __align__(1024) uint8_t smraw[];
+  uint8_t* sm = align1024(smraw);
+  uint8_t* sC = sm + kScanR1;
+  uint8_t* sB = sm + kScanR1 + 32768;
+  uint8_t* sM = sm + kScanR1;   // after the CB / Ys products are done
+  uint8_t* sY = sm + kScanR1;   // after the Y product is done
+  uint8_t* sX = sm + kScanX;
+  uint8_t* sH = sm + kScanH;
+  __shared__ float s_cs2[256], s_dt[256], scratch[8];
+  __shared__ __align__(16) float s_E[4][128];  // per-warp column factors exp(cs_r - cs_j) dt_j
+  __shared__ uint64_t bar_load, bar_mma;
+  __shared__ uint32_t tmem_base;
+  __shared__ int s_tile;
+  const int tid = threadIdx.x, wg = tid >> 7, q = (tid >> 5) & 3;
+  const int row = tid & 127;  // TMEM lane / tile row, shared by the two warpgroups
+  const int Q = d.Q, nblk = Q / 128;
+  const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+  const size_t PN = 64 * 128;
+  unsigned int* counter = flags + (size_t)d.B * d.nc * d.H;
+
+  if (tid == 0) {
+    s_tile = (int)atomicAdd(counter, 1u);
+    prefetch_tmap(&maps.x);
+    prefetch_tmap(&maps.B);
+    prefetch_tmap(&maps.C);
+    prefetch_tmap(&maps.y);
+    mbar_init(&bar_load, 1);
+    mbar_init(&bar_mma, 1);
+    fence_mbar_init();
+  }
+  if (tid < 32) {
+    tmem_alloc(&tmem_base, 256);
+    tmem_relinquish();
+  }
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  const int bh = d.B * d.H, tile = s_tile;
+  const int c = tile / bh, b = (tile % bh) / d.H, h = tile % d.H;
+  const int g = h / d.hpg;
+  const float Dh = D[h];
+  const uint32_t tm = tmem_base;
+  const uint32_t tCB = tm, tY = tm, tYs = tm + 128, tS0 = tm + 192;
+  const uint32_t tS1 = tm + 128;  // block 1's state contribution, read out before Ys reuses it
+  uint32_t load_phase = 0, mma_phase = 0;
+  bool ok = true;
+  const int crow = b * d.T + c * Q;
+
+  auto issue_loads = [&](int row0) {  // C, B and X of one block
+    mbar_expect_tx(&bar_load, 80 * 1024);
+    tma_load_2d(sC, &maps.C, g * d.N, row0, &bar_load);
+    tma_load_2d(sC + 16384, &maps.C, g * d.N + 64, row0, &bar_load);
+    tma_load_2d(sB, &maps.B, g * d.N, row0, &bar_load);
+    tma_load_2d(sB + 16384, &maps.B, g * d.N + 64, row0, &bar_load);
+    tma_load_2d(sX, &maps.x, h * d.P, row0, &bar_load);
+  };
+  auto issue_state_loads = [&](int row0) {  // B and X of one block
+    mbar_expect_tx(&bar_load, 48 * 1024);
+    tma_load_2d(sB, &maps.B, g * d.N, row0, &bar_load);
+    tma_load_2d(sB + 16384, &maps.B, g * d.N + 64, row0, &bar_load);
+    tma_load_2d(sX, &maps.x, h * d.P, row0, &bar_load);
+  };
+  if (tid == 0) issue_state_loads(crow + (nblk - 1) * 128);
+  chunk_cumsum_256(d, dt, A, b, c, h, s_cs2, s_dt, scratch);
+
+  // ---- A: the chunk's state contributions, the last block first
+  uint8_t* sWX = sC;  // w o X_k
+  for (int blk = nblk - 1; blk >= 0 && ok; --blk) {
+    const int base = blk * 128, end = base + 127;
+    ok = wait_or_flag(&bar_load, load_phase);
+    load_phase ^= 1;
+    if (!ok) break;
+    fence_after_sync();
+    for (int e = tid; e < 128 * 8; e += 256) {
+      const int r = e >> 3;
+      const float w = exp2f(s_cs2[end] - s_cs2[base + r]) * s_dt[base + r];
+      float f[8];
+      unpack8(*(const uint4*)(sX + e * 16), f);
+      *(uint4*)(sWX + e * 16) = make_uint4(pack_bf16(f[0] * w, f[1] * w), pack_bf16(f[2] * w, f[3] * w),
+                                           pack_bf16(f[4] * w, f[5] * w), pack_bf16(f[6] * w, f[7] * w));
+    }
+    fence_async_smem();
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    if (tid == 0) {
+      // S_k^T = B_k^T (w o X_k)  (M = n, N = p, K = j; both operands MN-major)
+      const uint32_t id_s = idesc_bf16(128, 64, true, true);
+      const uint32_t tS = blk == 0 ? tS0 : tS1;
+      for (int kk = 0; kk < 8; ++kk)
+        mma_bf16(tS, desc_sw128(smem_u32(sB) + kk * 2048, 16384, 1024),
+                 desc_sw128(smem_u32(sWX) + kk * 2048, 16384, 1024), id_s, kk > 0);
+      mma_commit(&bar_mma);
+    }
+    ok = wait_or_flag(&bar_mma, mma_phase);
+    mma_phase ^= 1;
+    fence_after_sync();
+    if (!ok) break;
+    // the tiles are free: block 0's state tiles, or block 0's C tile (its B
+    // and X are in place)
+    if (tid == 0) {
+      if (blk > 0) {
+        issue_state_loads(crow);
+      } else {
+        mbar_expect_tx(&bar_load, 32 * 1024);
+        tma_load_2d(sC, &maps.C, g * d.N, crow, &bar_load);
+        tma_load_2d(sC + 16384, &maps.C, g * d.N + 64, crow, &bar_load);
+      }
+    }
+  }
+
+  // ---- B: the look-back and the chunk-end state
+  float hv[32];  // H_{c-1}[p][n] for p = 32 wg + k, n = row
+  float* slot_in = hist + (((size_t)b * d.nc + c) * d.H + h) * PN;
+  if (c == 0) {
+    const float* h0p = h0 ? h0 + ((size_t)b * d.H + h) * PN : nullptr;
+#pragma unroll
+    for (int k = 0; k < 32; ++k) hv[k] = h0p ? h0p[(size_t)(wg * 32 + k) * 128 + row] : 0.f;
+#pragma unroll
+    for (int k = 0; k < 32; ++k) slot_in[(size_t)(wg * 32 + k) * 128 + row] = hv[k];
+  } else {
+    if (tid == 0) {
+      const unsigned int* f = flags + ((size_t)b * d.nc + c) * d.H + h;
+      bool got = ld_acquire_gpu(f) != 0u;
+      if (!got) {
+        const uint64_t t0 = globaltimer_ns();
+        while (!got) {
+#pragma unroll 1
+          for (int i = 0; i < 32 && !got; ++i) got = ld_acquire_gpu(f) != 0u;
+          if (!got && globaltimer_ns() - t0 > kWaitLimitNs) break;
+        }
+      }
+      if (!got) atomicOr(&g_tc_error, 1u);
+    }
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < 32; ++k) hv[k] = __ldcg(slot_in + (size_t)(wg * 32 + k) * 128 + row);
+  }
+  uint32_t hmid[16];  // H_mid as bf16 pairs (two-block chunks), the state term of block 1
+  if (ok) {
+    float hn[32];
+    {
+      float s0[32];
+      tmem_ld32(tS0 + lane_base + wg * 32, s0);
+      tmem_wait_ld();
+      const float e0 = exp2f(s_cs2[127]);
+#pragma unroll
+      for (int k = 0; k < 32; ++k) hn[k] = fmaf(e0, hv[k], s0[k]);
+    }
+    if (nblk == 2) {
+#pragma unroll
+      for (int k = 0; k < 16; ++k) hmid[k] = pack_bf16(hn[2 * k], hn[2 * k + 1]);
+      float s1[32];
+      tmem_ld32(tS1 + lane_base + wg * 32, s1);
+      tmem_wait_ld();
+      const float e1 = exp2f(s_cs2[Q - 1] - s_cs2[127]);
+#pragma unroll
+      for (int k = 0; k < 32; ++k) hn[k] = fmaf(e1, hn[k], s1[k]);
+    }
+    if (c + 1 < d.nc) {
+      float* slot_out = hist + (((size_t)b * d.nc + c + 1) * d.H + h) * PN;
+#pragma unroll
+      for (int k = 0; k < 32; ++k) slot_out[(size_t)(wg * 32 + k) * 128 + row] = hn[k];
+      __threadfence();
+    } else if (final_state) {
+      float* fo = final_state + ((size_t)b * d.H + h) * PN;
+#pragma unroll
+      for (int k = 0; k < 32; ++k) fo[(size_t)(wg * 32 + k) * 128 + row] = hn[k];
+    }
+    // H_{c-1} as bf16 rows n (64 p each): the MN-major B operand of C H^T
+#pragma unroll
+    for (int ch = 0; ch < 4; ++ch) store_row_bf16(sH, row, wg * 4 + ch, &hv[ch * 8]);
+  }
+  fence_async_smem();
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  if (ok && c + 1 < d.nc && tid == 0)
+    st_release_gpu(flags + ((size_t)b * d.nc + c + 1) * d.H + h, 1u);
+
+  // ---- C: y block by block
+  for (int blk = 0; blk < nblk && ok; ++blk) {
+    const int row0 = crow + blk * 128;
+    const int base = blk * 128;
+    for (int e = tid; e < 4 * 128; e += 256) {
+      const int w = e >> 7, jj = e & 127;
+      const int r = base + 32 * w, J = base + jj;
+      s_E[w][jj] = (J < r) ? exp2f(s_cs2[r] - s_cs2[J]) * s_dt[J] : 0.f;
+    }
+    // reference log-decay of the block's state term: cs before row `base`
+    const float ref2 = blk == 0 ? 0.f : s_cs2[base - 1];
+    fence_async_smem();
+    ok = wait_or_flag(&bar_load, load_phase);
+    load_phase ^= 1;
+    if (!ok) break;
+    fence_after_sync();
+    if (tid == 0) {
+      const uint32_t id_cb = idesc_bf16(128, 128, false, false);
+      for (int kk = 0; kk < 8; ++kk) {
+        const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+        mma_bf16(tCB, desc_sw128(smem_u32(sC) + off, 16, 1024),
+                 desc_sw128(smem_u32(sB) + off, 16, 1024), id_cb, kk > 0);
+      }
+      const uint32_t id_ys = idesc_bf16(128, 64, false, true);
+      for (int kk = 0; kk < 8; ++kk) {
+        const uint32_t aoff = (kk >> 2) * 16384 + (kk & 3) * 32;
+        mma_bf16(tYs, desc_sw128(smem_u32(sC) + aoff, 16, 1024),
+                 desc_sw128(smem_u32(sH) + kk * 2048, 16384, 1024), id_ys, kk > 0);
+      }
+      mma_commit(&bar_mma);
+    }
+    ok = wait_or_flag(&bar_mma, mma_phase);
+    mma_phase ^= 1;
+    fence_after_sync();
+    if (!ok) break;
+
+    const int I = base + row;
+    {
+      const float fi = exp2f(s_cs2[I] - s_cs2[base + 32 * q]);
+      const float csI = s_cs2[I];
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int jc = 2 * wg + u;
+        float v[32];
+        if (jc <= q) {  // warp-uniform
+          tmem_ld32(tCB + lane_base + jc * 32, v);
+          tmem_wait_ld();
+          if (jc < q) {
+#pragma unroll
+            for (int t4 = 0; t4 < 8; ++t4) {
+              const float4 e4 = *(const float4*)&s_E[q][jc * 32 + t4 * 4];
+              v[t4 * 4 + 0] *= fi * e4.x;
+              v[t4 * 4 + 1] *= fi * e4.y;
+              v[t4 * 4 + 2] *= fi * e4.z;
+              v[t4 * 4 + 3] *= fi * e4.w;
+            }
+          } else {
+#pragma unroll
+            for (int k = 0; k < 32; ++k) {
+              const int J = base + jc * 32 + k;
+              const float ex = (J <= I) ? exp2f(csI - s_cs2[J]) : 0.f;
+              v[k] *= ex * s_dt[J];
+            }
+          }
+        } else {
+#pragma unroll
+          for (int k = 0; k < 32; ++k) v[k] = 0.f;
+        }
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const int j = jc * 32 + q4 * 8;
+          store_row_bf16(sM + (j >> 6) * 16384, row, (j & 63) >> 3, &v[q4 * 8]);
+        }
+      }
+    }
+    // block 0 of two: the state term of block 1 (H_mid) replaces H_{c-1}, which
+    // the Ys product above has read
+    if (blk == 0 && nblk == 2) {
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch)
+        *(uint4*)(sH + sw128(row, wg * 4 + ch)) =
+            make_uint4(hmid[4 * ch], hmid[4 * ch + 1], hmid[4 * ch + 2], hmid[4 * ch + 3]);
+    }
+    fence_async_smem();
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    if (tid == 0) {
+      const uint32_t id_y = idesc_bf16(128, 64, false, true);
+      for (int kk = 0; kk < 8; ++kk) {
+        const uint32_t aoff = (kk >> 2) * 16384 + (kk & 3) * 32;
+        mma_bf16(tY, desc_sw128(smem_u32(sM) + aoff, 16, 1024),
+                 desc_sw128(smem_u32(sX) + kk * 2048, 16384, 1024), id_y, kk > 0);
+      }
+      mma_commit(&bar_mma);
+    }
+    ok = wait_or_flag(&bar_mma, mma_phase);
+    mma_phase ^= 1;
+    fence_after_sync();
+    if (!ok) break;
+    {
+      const float sc = exp2f(s_cs2[I] - ref2);
+      float yv[32], ys[32];
+      tmem_ld32(tY + lane_base + wg * 32, yv);
+      tmem_ld32(tYs + lane_base + wg * 32, ys);
+      tmem_wait_ld();
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int ch = wg * 4 + k;
+        float xf[8], o8[8];
+        unpack8(*(const uint4*)(sX + sw128(row, ch)), xf);
+#pragma unroll
+        for (int t = 0; t < 8; ++t) o8[t] = fmaf(sc, ys[k * 8 + t], yv[k * 8 + t]) + Dh * xf[t];
+        store_row_bf16(sY, row, ch, o8);
+      }
+    }
+    fence_async_smem();
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    if (tid == 0) {
+      tma_store_2d(&maps.y, sY, h * d.P, row0);
+      bulk_commit();
+      if (blk + 1 < nblk) {
+        bulk_wait_read0();  // the y staging (region R1) is reloaded next
+        issue_loads(row0 + 128);
+      }
     }
   }
   grid_dep_launch();
@@ -1723,24 +2064,41 @@ cudaError_t tc_forward_states(const Problem& p) {
 cudaError_t tc_forward_scan(const Problem& p) {
   ScanMaps maps;
   const uint64_t rows = (uint64_t)p.B * p.T;
-  const bool ht = p.hT != nullptr;
   if (!map_bf16(&maps.x, p.x, rows, (uint64_t)p.H * p.P, 128) ||
       !map_bf16(&maps.B, p.Bm, rows, (uint64_t)p.G * p.N, 128) ||
       !map_bf16(&maps.C, p.Cm, rows, (uint64_t)p.G * p.N, 128) ||
       !map_bf16(&maps.y, p.y, rows, (uint64_t)p.H * p.P, 128))
     return cudaErrorInvalidValue;
-  if (ht && !map_bf16(&maps.ht, p.hT, (uint64_t)p.B * p.nc * p.H * p.N, (uint64_t)p.P, 128))
-    return cudaErrorInvalidValue;
-  if (!ht) maps.ht = maps.x;  // unused
   const size_t smem = kScanBytes + 1024;
-  cudaError_t e = ht ? set_smem_tc(k_fwd_scan_tc<true>, smem) : set_smem_tc(k_fwd_scan_tc<false>, smem);
+  cudaError_t e = set_smem_tc(k_fwd_scan_tc, smem);
   if (e != cudaSuccess) return e;
   {
-    LaunchScope ls(ht ? "chunk_scan_ht_tc" : "chunk_scan_tc", p.stream);
-    e = launch_pdl(ht ? k_fwd_scan_tc<true> : k_fwd_scan_tc<false>, dim3(p.nc, p.H, p.B),
-                   dim3(256), smem, p.stream, maps, tc_dims(p), p.dt, p.A, p.D, p.hist);
+    LaunchScope ls("chunk_scan_tc", p.stream);
+    e = launch_pdl(k_fwd_scan_tc, dim3(p.nc, p.H, p.B), dim3(256), smem, p.stream, maps,
+                   tc_dims(p), p.dt, p.A, p.D, p.hist);
   }
   if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+cudaError_t tc_forward_single(const Problem& p) {
+  ScanMaps maps;
+  const uint64_t rows = (uint64_t)p.B * p.T;
+  if (!map_bf16(&maps.x, p.x, rows, (uint64_t)p.H * p.P, 128) ||
+      !map_bf16(&maps.B, p.Bm, rows, (uint64_t)p.G * p.N, 128) ||
+      !map_bf16(&maps.C, p.Cm, rows, (uint64_t)p.G * p.N, 128) ||
+      !map_bf16(&maps.y, p.y, rows, (uint64_t)p.H * p.P, 128))
+    return cudaErrorInvalidValue;
+  const size_t nflags = (size_t)p.B * p.nc * p.H + 1;
+  cudaError_t e = cudaMemsetAsync(p.fwd_flags, 0, nflags * sizeof(unsigned int), p.stream);
+  if (e != cudaSuccess) return e;
+  const size_t smem = kScanBytes + 1024;
+  if ((e = set_smem_tc(k_fwd_single_tc, smem)) != cudaSuccess) return e;
+  {
+    LaunchScope ls("fwd_single_tc", p.stream);
+    k_fwd_single_tc<<<(unsigned)(nflags - 1), 256, smem, p.stream>>>(
+        maps, tc_dims(p), p.dt, p.A, p.D, p.h0, p.hist, p.final_state, p.fwd_flags);
+  }
   return cudaGetLastError();
 }
 

@@ -159,6 +159,42 @@ def test_full_size_workload_one_group(idx):
         assert np.isfinite(v).all()
 
 
+@pytest.mark.parametrize("q,h0", [(128, True), (256, True), (128, False)])
+def test_single_pass_forward_look_back(q, h0):
+    """Shapes with enough (b, h) pairs for the single-pass forward, whose CTAs
+    pass chunk-end states to the next chunk through the history (look-back):
+    it must be the kernel that ran; one group against the oracle; every
+    output against the SIMT path (forced); y and the states bit for bit on a
+    second run."""
+    from state_space_model_analytic_gb300 import _native as nat
+    dims = synth.Dims(4, 1024, 64, 64, 128, 16, q, "bf16")  # B * H = 256 (b, h) pairs
+    inp = synth.make_inputs(dims, 29, h0, "softplus")
+    dev = to_device(dims, inp)
+    nat.trace_begin(64)
+    try:
+        tc = run_gpu(dims, dev)
+    finally:
+        nat.trace_end()
+    names = [r["name"] for r in nat.trace_read()]
+    nat.trace_reset()
+    assert "fwd_single_tc" in names, names
+    again = run_gpu(dims, dev)
+    for k in ("y", "final_state", "chunk_states"):
+        assert np.array_equal(tc[k], again[k]), k
+    g = dims.ngroups - 1
+    sdims, sub = group_slice(dims, inp, g)
+    errs, bad = compare(slice_outputs(dims, tc, g), run_oracle(sdims, sub), TOL["bf16"])
+    assert not bad, errs
+    nat.check(nat.lib().ssd_force_kernel_path(0))
+    try:
+        simt = run_gpu(dims, dev)
+    finally:
+        nat.check(nat.lib().ssd_force_kernel_path(-1))
+    for k in tc:
+        assert rel_err(tc[k], simt[k]) < TOL["bf16"], k
+    nat.check(nat.lib().ssd_device_status())
+
+
 @pytest.mark.parametrize("q", [128, 256])
 def test_tensor_core_and_simt_paths_agree(q):
     """The tcgen05 path and the SIMT path (forced) give the same results

@@ -390,11 +390,17 @@ def main():
     eager_ms = ms
 
     # ---- e2e: host buffers through the public API, copies inside the timed region.
-    # Steps are pipelined over three streams: the host-to-device copy of step
-    # i + 1's inputs and the device-to-host copy of step i - 1's results run
-    # while step i computes (two device buffer sets; the workspaces are only
-    # used on the compute stream).  Every step still copies all its inputs in
-    # and all its results out.
+    # Every step copies all its inputs in from pinned host memory and all its
+    # results out.  Steps are pipelined over three device buffer sets: while
+    # step i computes on set i % 3, step i + 1's inputs go into set (i + 1) % 3
+    # and step i - 1's results leave set (i - 1) % 3.  Each such iteration is
+    # one CUDA graph (three concurrent branches: the host-to-device copies, the
+    # forward and backward API calls, the device-to-host copies), captured
+    # once per rotation of the sets; the graphs replay in stream order, so an
+    # iteration's branches see the previous iteration complete.  The timed
+    # region is: step 0's inputs in, n iterations, step n - 1's results out
+    # (the first iteration also copies out a set no step wrote, and the last
+    # one copies in a step that is not computed: both only add time).
     e2e = None
     if not args.no_e2e:
         host_in = {k: (None if v is None else v.cpu().pin_memory()) for k, v in t_in.items()}
@@ -404,62 +410,110 @@ def main():
                     for k in outs}
         h2d = sum(v.numel() * v.element_size() for v in host_in.values() if v is not None)
         d2h = sum(v.numel() * v.element_size() for v in host_out.values())
-        sets = []
-        for _ in range(2):
-            sets.append({
-                "in": {k: (None if v is None else torch.empty_like(v)) for k, v in t_in.items()},
-                "fwd": {k: torch.empty_like(v) for k, v in fwd_out.items()},
-                "bwd": {k: torch.empty_like(v) for k, v in bwd_out.items()},
-                "h2d_done": torch.cuda.Event(), "used": torch.cuda.Event(),
-                "d2h_done": torch.cuda.Event()})
+        sets = [{"in": {k: (None if v is None else torch.empty_like(v)) for k, v in t_in.items()},
+                 "fwd": {k: torch.empty_like(v) for k, v in fwd_out.items()},
+                 "bwd": {k: torch.empty_like(v) for k, v in bwd_out.items()}} for _ in range(3)]
         s_h2d, s_d2h = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-        n_e2e = max(3, min(args.steps, 50))
+        n_e2e = max(3, min(args.steps, 200))
 
-        def e2e_run(n):
-            for i in range(n + 1):
-                if i < n:  # inputs of step i into buffer set i % 2
-                    st = sets[i % 2]
-                    with torch.cuda.stream(s_h2d):
-                        if i >= 2:  # step i - 2 has consumed this set's inputs
-                            s_h2d.wait_event(st["used"])
-                        for k, v in host_in.items():
-                            if v is not None:
-                                st["in"][k].copy_(v, non_blocking=True)
-                        st["h2d_done"].record(s_h2d)
-                if i >= 1:  # step i - 1 computes, then its results go out
-                    j = i - 1
-                    st = sets[j % 2]
-                    stream.wait_event(st["h2d_done"])
-                    if j >= 2:  # step j - 2's results have left this set
-                        stream.wait_event(st["d2h_done"])
-                    ti, fo, bo = st["in"], st["fwd"], st["bwd"]
-                    ssd.forward(ti["x"], ti["dt"], ti["A"], ti["B"], ti["C"], ti["D"], ti["h0"],
-                                chunk=Q, out=fo, workspace=ws_f)
-                    ssd.backward(ti["x"], ti["dt"], ti["A"], ti["B"], ti["C"], ti["D"], ti["h0"],
-                                 ti["dy"], fo["chunk_states"], chunk=Q, out=bo, workspace=ws_b)
-                    st["used"].record(stream)
-                    with torch.cuda.stream(s_d2h):
-                        s_d2h.wait_event(st["used"])
-                        res = {"y": fo["y"], **bo}
-                        for k in outs:
-                            host_out[k].copy_(res[k], non_blocking=True)
-                        st["d2h_done"].record(s_d2h)
-            stream.wait_stream(s_d2h)  # the run ends when the last results are on the host
+        def copy_in(st):
+            for k, v in host_in.items():
+                if v is not None:
+                    st["in"][k].copy_(v, non_blocking=True)
 
-        e2e_run(2)
+        def copy_out(st):
+            res = {"y": st["fwd"]["y"], **st["bwd"]}
+            for k in outs:
+                host_out[k].copy_(res[k], non_blocking=True)
+
+        def compute(st):
+            ti, fo, bo = st["in"], st["fwd"], st["bwd"]
+            ssd.forward(ti["x"], ti["dt"], ti["A"], ti["B"], ti["C"], ti["D"], ti["h0"],
+                        chunk=Q, out=fo, workspace=ws_f)
+            ssd.backward(ti["x"], ti["dt"], ti["A"], ti["B"], ti["C"], ti["D"], ti["h0"],
+                         ti["dy"], fo["chunk_states"], chunk=Q, out=bo, workspace=ws_b)
+
+        def iteration(r):
+            """Step r computes on set r % 3, with the neighbours' copies beside it."""
+            cur = torch.cuda.current_stream()
+            s_h2d.wait_stream(cur)
+            s_d2h.wait_stream(cur)
+            with torch.cuda.stream(s_h2d):
+                copy_in(sets[(r + 1) % 3])
+            with torch.cuda.stream(s_d2h):
+                copy_out(sets[(r + 2) % 3])
+            compute(sets[r % 3])
+            cur.wait_stream(s_h2d)
+            cur.wait_stream(s_d2h)
+
+        e2e_mode = "3 buffer sets, one CUDA graph per pipelined iteration"
+        graphs = []
+        try:
+            for r in range(3):
+                iteration(r)  # warm-up of the same work outside the capture
+            torch.cuda.synchronize()
+            cap = torch.cuda.Stream(dev)
+            for r in range(3):
+                g_ = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g_, stream=cap):
+                    iteration(r)
+                graphs.append(g_)
+            torch.cuda.synchronize()
+        except Exception as e:  # noqa: BLE001  (eager iterations then; reported)
+            graphs = []
+            e2e_mode = f"3 buffer sets, eager iterations (graph capture failed: {type(e).__name__})"
+
+        def run_iter(r):
+            if graphs:
+                graphs[r % 3].replay()
+            else:
+                iteration(r % 3)
+
+        for r in range(3):
+            run_iter(r)
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        s_h2d.wait_stream(stream)
-        s_d2h.wait_stream(stream)
-        e2e_run(n_e2e)
+        copy_in(sets[0])
+        for r in range(n_e2e):
+            run_iter(r)
+        copy_out(sets[(n_e2e - 1) % 3])
         e1.record(stream)
         torch.cuda.synchronize()
         e_ms = e0.elapsed_time(e1) / n_e2e
+
+        # the host link's own bound: the same copies alone, both directions at once
+        def both_ways():
+            cur = torch.cuda.current_stream()
+            s_h2d.wait_stream(cur)
+            s_d2h.wait_stream(cur)
+            with torch.cuda.stream(s_h2d):
+                copy_in(sets[0])
+            with torch.cuda.stream(s_d2h):
+                copy_out(sets[1])
+            cur.wait_stream(s_h2d)
+            cur.wait_stream(s_d2h)
+
+        def copy_ms(fn, reps=10):
+            fn()
+            torch.cuda.synchronize()
+            a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a_.record(stream)
+            for _ in range(reps):
+                fn()
+            b_.record(stream)
+            torch.cuda.synchronize()
+            return a_.elapsed_time(b_) / reps
+
+        link_ms = copy_ms(both_ways)
         e2e = {"value": tokens * world / (e_ms / 1e3), "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n_e2e,
-               "ms_per_step": e_ms,
-               "pipelining": "copies of neighbouring steps overlap compute (2 buffer sets)"}
+               "ms_per_step": e_ms, "pipelining": e2e_mode,
+               "link_bound": {"ms_per_step": link_ms,
+                              "gbs": (h2d + d2h) / (link_ms / 1e3) / 1e9,
+                              "frac": link_ms / e_ms,
+                              "what": "the step's copies alone, both directions at once "
+                                      "(pinned host memory); e2e cannot be faster"}}
 
     # ---- the same step as a CUDA graph: the forward and backward API calls are
     # captured once and replayed, one host launch per step (the kernels, their

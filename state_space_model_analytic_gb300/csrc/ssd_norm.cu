@@ -12,9 +12,10 @@
 // Work split: a CTA of up to 256 threads spans the row (thread t owns the
 // 16-byte column vectors t, t + blockDim, ...: V of them, V in {1, 2, 4}) and
 // walks groups of R rows (forward 4 / V, backward 2 / V or 1), persistently
-// over the rows (CTA j takes groups j, j + grid, ...).  A thread loads its
-// vectors of all R rows before using any, so several 16-byte loads per
-// operand are in flight per thread at a small register cost; the row sums (sum y^2, and the backward's dot) go
+// over the rows (CTA j takes groups j, j + grid, ...).  A thread copies its
+// vectors of the next group into shared memory (cp.async, double-buffered)
+// while it computes the current one, so two groups of 16-byte loads per
+// operand are in flight per thread at no register cost; the row sums (sum y^2, and the backward's dot) go
 // through one block reduction per group (warp shuffles, then the warps'
 // partials in order from shared memory).  The backward keeps its columns' dw
 // in registers over all its rows, writes them as the CTA's partial row, and a
@@ -64,6 +65,19 @@ struct Vec<__nv_bfloat16> {
   }
 };
 
+// 16-byte asynchronous copy global -> shared (each thread later reads back
+// only what it copied itself, so waiting for its own groups suffices)
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((unsigned)__cvta_generic_to_shared(smem)),
+               "l"(gmem)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -109,26 +123,46 @@ k_norm_fwd(long long rows, int width, float eps, const T* __restrict__ y, const 
   constexpr int E = Vec<T>::n, R = 4 / V;
   using raw = typename Vec<T>::raw;
   __shared__ float red[2 * R * kNormWarpsMax];
+  // [stage][r][operand y, z][v][thread] 16-byte slots (a warp's slots are contiguous)
+  extern __shared__ uint4 stage[];
+  const int nt = blockDim.x, t = threadIdx.x;
+  auto slot = [&](int st, int r, int op, int v) -> uint4* {
+    return stage + ((((size_t)st * R + r) * 2 + op) * V + v) * nt + t;
+  };
   float wv[V][E];
 #pragma unroll
   for (int v = 0; v < V; ++v) {
-    const int c = (v * blockDim.x + threadIdx.x) * E;
+    const int c = (v * nt + t) * E;
 #pragma unroll
     for (int i = 0; i < E; ++i) wv[v][i] = w[c + i];
   }
   const long long ngroups = (rows + R - 1) / R;
-  int buf = 0;
-  for (long long gi = blockIdx.x; gi < ngroups; gi += gridDim.x, buf ^= 1) {
+  auto fetch = [&](long long gi, int st) {
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+      for (int v = 0; v < V; ++v) {
+        const long long row = min(gi * R + r, rows - 1);  // past the end: a valid row, unused
+        const long long off = row * width + (long long)(v * nt + t) * E;
+        cp_async16(slot(st, r, 0, v), y + off);
+        cp_async16(slot(st, r, 1, v), z + off);
+      }
+  };
+  if ((long long)blockIdx.x < ngroups) fetch(blockIdx.x, 0);
+  cp_async_commit();
+  int buf = 0, st = 0;
+  for (long long gi = blockIdx.x; gi < ngroups; gi += gridDim.x, buf ^= 1, st ^= 1) {
     const long long r0 = gi * R;
+    if (gi + gridDim.x < ngroups) fetch(gi + gridDim.x, st ^ 1);
+    cp_async_commit();
+    cp_async_wait<1>();  // this group's copies (the thread's own) are in
     raw qy[R][V], qz[R][V];
 #pragma unroll
     for (int r = 0; r < R; ++r)
 #pragma unroll
       for (int v = 0; v < V; ++v) {
-        const long long row = min(r0 + r, rows - 1);  // past the end: a valid row, unused
-        const long long off = row * width + (long long)(v * blockDim.x + threadIdx.x) * E;
-        qy[r][v] = *(const raw*)(y + off);
-        qz[r][v] = *(const raw*)(z + off);
+        qy[r][v] = *(const raw*)slot(st, r, 0, v);
+        qz[r][v] = *(const raw*)slot(st, r, 1, v);
       }
     float ss[R];
 #pragma unroll
@@ -154,11 +188,12 @@ k_norm_fwd(long long rows, int width, float eps, const T* __restrict__ y, const 
         Vec<T>::cvt(qz[r][v], zz);
 #pragma unroll
         for (int i = 0; i < E; ++i) o[i] = (a[i] * inv) * wv[v][i] * (zz[i] * sigmoidf_(zz[i]));
-        Vec<T>::store(out + (r0 + r) * width + (long long)(v * blockDim.x + threadIdx.x) * E, o);
+        Vec<T>::store(out + (r0 + r) * width + (long long)(v * nt + t) * E, o);
       }
-      if (inv_rms && threadIdx.x == 0) inv_rms[r0 + r] = inv;
+      if (inv_rms && t == 0) inv_rms[r0 + r] = inv;
     }
   }
+  cp_async_wait<0>();
 }
 
 // part: [grid][width] per-CTA column sums of g * gate * n.
@@ -170,10 +205,16 @@ k_norm_bwd(long long rows, int width, float eps, const T* __restrict__ y, const 
   constexpr int E = Vec<T>::n, R = V < 2 ? 2 : 1;
   using raw = typename Vec<T>::raw;
   __shared__ float red[2 * 2 * R * kNormWarpsMax];
+  // [stage][r][operand y, z, g][v][thread] 16-byte slots
+  extern __shared__ uint4 stage[];
+  const int nt = blockDim.x, t = threadIdx.x;
+  auto slot = [&](int st, int r, int op, int v) -> uint4* {
+    return stage + ((((size_t)st * R + r) * 3 + op) * V + v) * nt + t;
+  };
   float wv[V][E], dw[V][E];
 #pragma unroll
   for (int v = 0; v < V; ++v) {
-    const int c = (v * blockDim.x + threadIdx.x) * E;
+    const int c = (v * nt + t) * E;
 #pragma unroll
     for (int i = 0; i < E; ++i) {
       wv[v][i] = w[c + i];
@@ -181,23 +222,38 @@ k_norm_bwd(long long rows, int width, float eps, const T* __restrict__ y, const 
     }
   }
   const long long ngroups = (rows + R - 1) / R;
-  int buf = 0;
-  for (long long gi = blockIdx.x; gi < ngroups; gi += gridDim.x, buf ^= 1) {
-    const long long r0 = gi * R;
-    raw qy[R][V], qz[R][V], qg[R][V];
-    float inv[R];
+  auto fetch = [&](long long gi, int st) {
 #pragma unroll
-    for (int r = 0; r < R; ++r) {
-      const long long row = min(r0 + r, rows - 1);  // past the end: a valid row, unused
-      inv[r] = inv_in ? inv_in[row] : 0.f;
+    for (int r = 0; r < R; ++r)
 #pragma unroll
       for (int v = 0; v < V; ++v) {
-        const long long off = row * width + (long long)(v * blockDim.x + threadIdx.x) * E;
-        qy[r][v] = *(const raw*)(y + off);
-        qz[r][v] = *(const raw*)(z + off);
-        qg[r][v] = *(const raw*)(g + off);
+        const long long row = min(gi * R + r, rows - 1);  // past the end: a valid row, unused
+        const long long off = row * width + (long long)(v * nt + t) * E;
+        cp_async16(slot(st, r, 0, v), y + off);
+        cp_async16(slot(st, r, 1, v), z + off);
+        cp_async16(slot(st, r, 2, v), g + off);
       }
-    }
+  };
+  if ((long long)blockIdx.x < ngroups) fetch(blockIdx.x, 0);
+  cp_async_commit();
+  int buf = 0, st = 0;
+  for (long long gi = blockIdx.x; gi < ngroups; gi += gridDim.x, buf ^= 1, st ^= 1) {
+    const long long r0 = gi * R;
+    float inv[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) inv[r] = inv_in ? inv_in[min(r0 + r, rows - 1)] : 0.f;
+    if (gi + gridDim.x < ngroups) fetch(gi + gridDim.x, st ^ 1);
+    cp_async_commit();
+    cp_async_wait<1>();  // this group's copies (the thread's own) are in
+    raw qy[R][V], qz[R][V], qg[R][V];
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+      for (int v = 0; v < V; ++v) {
+        qy[r][v] = *(const raw*)slot(st, r, 0, v);
+        qz[r][v] = *(const raw*)slot(st, r, 1, v);
+        qg[r][v] = *(const raw*)slot(st, r, 2, v);
+      }
     // per row: dot = sum_w (g * gate * w) * y, and sum y^2 when inv_rms is not given
     float sums[2 * R];
 #pragma unroll
@@ -239,16 +295,17 @@ k_norm_bwd(long long rows, int width, float eps, const T* __restrict__ y, const 
           oz[i] = gg[i] * nrm * wv[v][i] * (s * (1.f + zz[i] * (1.f - s)));
           dw[v][i] += gg[i] * gate * nrm;
         }
-        const long long off = (r0 + r) * width + (long long)(v * blockDim.x + threadIdx.x) * E;
+        const long long off = (r0 + r) * width + (long long)(v * nt + t) * E;
         Vec<T>::store(dy + off, oy);
         Vec<T>::store(dz + off, oz);
       }
     }
   }
+  cp_async_wait<0>();
   // this CTA's column sums
 #pragma unroll
   for (int v = 0; v < V; ++v) {
-    const int c = (v * blockDim.x + threadIdx.x) * E;
+    const int c = (v * nt + t) * E;
 #pragma unroll
     for (int i = 0; i < E; ++i) part[(size_t)blockIdx.x * width + c + i] = dw[v][i];
   }
@@ -285,11 +342,12 @@ void norm_shape(int width, int esz, int* threads, int* V) {
 }
 
 template <typename KernelT>
-int norm_grid(KernelT kernel, int threads, long long ngroups, int cap) {
+int norm_grid(KernelT kernel, int threads, size_t smem, long long ngroups, int cap) {
   int dev = 0, nsm = 0, occ = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
-  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, threads, 0);
+  cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, threads, smem);
   long long g = (long long)(nsm > 0 ? nsm : 1) * (occ > 0 ? occ : 1);
   if (g > cap) g = cap;
   if (g > ngroups) g = ngroups;
@@ -300,9 +358,10 @@ template <typename T, int V>
 cudaError_t norm_fwd_t(long long rows, int width, int threads, const void* y, const void* z,
                        const float* w, float eps, void* out, float* inv_rms, cudaStream_t s) {
   const long long ngroups = (rows + 4 / V - 1) / (4 / V);
-  const int grid = norm_grid(k_norm_fwd<T, V>, threads, ngroups, 1 << 20);
-  k_norm_fwd<T, V><<<grid, threads, 0, s>>>(rows, width, eps, (const T*)y, (const T*)z, w, (T*)out,
-                                            inv_rms);
+  const size_t smem = (size_t)2 * 4 * 2 * threads * 16;  // 2 stages x (R x V = 4) x (y, z)
+  const int grid = norm_grid(k_norm_fwd<T, V>, threads, smem, ngroups, 1 << 20);
+  k_norm_fwd<T, V><<<grid, threads, smem, s>>>(rows, width, eps, (const T*)y, (const T*)z, w,
+                                               (T*)out, inv_rms);
   return cudaGetLastError();
 }
 
@@ -310,11 +369,13 @@ template <typename T, int V>
 cudaError_t norm_bwd_t(long long rows, int width, int threads, const void* y, const void* z,
                        const float* w, float eps, const float* inv_rms, const void* g, void* dy,
                        void* dz, float* part, int* ncta, cudaStream_t s) {
-  const long long ngroups = (rows + (V < 2 ? 2 : 1) - 1) / (V < 2 ? 2 : 1);
-  const int grid = norm_grid(k_norm_bwd<T, V>, threads, ngroups, kNormMaxCtas);
+  constexpr int R = V < 2 ? 2 : 1;
+  const long long ngroups = (rows + R - 1) / R;
+  const size_t smem = (size_t)2 * R * V * 3 * threads * 16;  // 2 stages x R x V x (y, z, g)
+  const int grid = norm_grid(k_norm_bwd<T, V>, threads, smem, ngroups, kNormMaxCtas);
   *ncta = grid;
-  k_norm_bwd<T, V><<<grid, threads, 0, s>>>(rows, width, eps, (const T*)y, (const T*)z, w, inv_rms,
-                                            (const T*)g, (T*)dy, (T*)dz, part);
+  k_norm_bwd<T, V><<<grid, threads, smem, s>>>(rows, width, eps, (const T*)y, (const T*)z, w,
+                                               inv_rms, (const T*)g, (T*)dy, (T*)dz, part);
   return cudaGetLastError();
 }
 

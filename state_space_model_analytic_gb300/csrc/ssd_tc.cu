@@ -879,7 +879,9 @@ k_fwd_scan_tc(const __grid_constant__ ScanMaps maps, TcDims d, const float* __re
 //      the state term.
 // flags: [B][nc][H] slot-ready words, then the tile counter; all zero at
 // launch.  A wait that gives up sets the device error word and goes on with
-// the slot as it is (the outputs are then wrong, nothing hangs).
+// the slot as it is, and every CTA releases its successor's flag, so that a
+// failure does not make every later chunk wait out its limit too (the outputs
+// are then wrong; nothing hangs).
 __device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned int* p) {
   unsigned v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -1071,7 +1073,9 @@ k_fwd_single_tc(const __grid_constant__ ScanMaps maps, TcDims d, const float* __
   fence_before_sync();
   __syncthreads();
   fence_after_sync();
-  if (ok && c + 1 < d.nc && tid == 0)
+  // released even after a wait that gave up (the error word is set then), so
+  // that the next chunk does not wait out its own limit as well
+  if (c + 1 < d.nc && tid == 0)
     st_release_gpu(flags + ((size_t)b * d.nc + c + 1) * d.H + h, 1u);
 
   // ---- C: y block by block

@@ -29,7 +29,7 @@
 // run come from plain loads (or the initial state before step 0).
 //
 // Compute.  A thread keeps the last K inputs in registers and walks its run
-// step by step.  The backward walks on K - 1 steps past its run, keeping the
+// step by step, its 4 channels as two pairs in packed f32x2 arithmetic.  The backward walks on K - 1 steps past its run, keeping the
 // K - 1 dx values still open and storing each once the gradient of the step
 // K - 1 later is in (steps past T carry no gradient); dw and dbias stay in
 // registers over the run, are summed over the CTA's warps in shared memory
@@ -41,6 +41,7 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 
+#include "f32x2.cuh"
 #include "ssd_common.cuh"
 #include "ssd_internal.h"
 #include "tc_util.cuh"
@@ -137,14 +138,17 @@ __device__ __forceinline__ void hist_load(const T* x, const float* init, long lo
   }
 }
 
+// per channel pair e: channels c0 + 2e, c0 + 2e + 1
 template <int K>
 __device__ __forceinline__ void load_params(const float* w, const float* bias, int c0, bool valid,
-                                            float (&wv)[K][4], float (&bv)[4]) {
+                                            float2 (&wv)[K][2], float2 (&bv)[2]) {
+  auto at = [&](int c, int k) { return valid ? w[c * K + k] : 0.f; };
 #pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    bv[e] = (valid && bias) ? bias[c0 + e] : 0.f;
+  for (int e = 0; e < 2; ++e) {
+    const int c = c0 + 2 * e;
+    bv[e] = (valid && bias) ? make_float2(bias[c], bias[c + 1]) : make_float2(0.f, 0.f);
 #pragma unroll
-    for (int k = 0; k < K; ++k) wv[k][e] = valid ? w[(c0 + e) * K + k] : 0.f;
+    for (int k = 0; k < K; ++k) wv[k][e] = make_float2(at(c, k), at(c + 1, k));
   }
 }
 
@@ -198,11 +202,12 @@ k_conv_fwd(const __grid_constant__ CUtensorMap xmap, int T_, int C, const T* __r
   }
   __syncwarp();
   const bool cvalid = c0 < C;
-  float wv[K][4], bv[4], win[K][4];  // win[k] = input of step t - K + 1 + k
+  float2 wv[K][2], bv[2], win[K][2];  // win[k] = input of step t - K + 1 + k (channel pairs)
   load_params<K>(w, bias, c0, cvalid, wv, bv);
 #pragma unroll
   for (int k = 0; k < K - 1; ++k)
-    hist_load<T, K>(x, init, rowb, b, C, c0, cvalid && ntiles > 0, run.ws - (K - 1) + k, win[k]);
+    hist_load<T, K>(x, init, rowb, b, C, c0, cvalid && ntiles > 0, run.ws - (K - 1) + k,
+                    (float*)win[k]);
   T* op = out + (rowb + run.ws) * C + c0;
   for (int j = 0; j < ntiles; ++j) {
     const bool ok = mbar_wait(&full[j % S], (j / S) & 1, kConvWaitNs);
@@ -214,21 +219,21 @@ k_conv_fwd(const __grid_constant__ CUtensorMap xmap, int T_, int C, const T* __r
     const int n = min(kConvFwdStep, run.we - run.ws - j * kConvFwdStep);
 #pragma unroll
     for (int i = 0; i < kConvFwdStep; ++i) {
-      ConvT<T>::lds(st + i * G::ROWB, lane, win[K - 1]);
-      float o[4];
+      ConvT<T>::lds(st + i * G::ROWB, lane, (float*)win[K - 1]);
+      float2 o[2];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        float p = bv[e];
+      for (int e = 0; e < 2; ++e) {
+        float2 p = bv[e];
 #pragma unroll
-        for (int k = 0; k < K; ++k) p = fmaf(wv[k][e], win[k][e], p);
-        o[e] = p * sig(p);
+        for (int k = 0; k < K; ++k) p = fma2(wv[k][e], win[k][e], p);
+        o[e] = mul2(p, make_float2(sig(p.x), sig(p.y)));
       }
-      if (cvalid && i < n) ConvT<T>::stg(op, o);
+      if (cvalid && i < n) ConvT<T>::stg(op, (const float*)o);
       op += C;
 #pragma unroll
       for (int k = 0; k < K - 1; ++k)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) win[k][e] = win[k + 1][e];
+        for (int e = 0; e < 2; ++e) win[k][e] = win[k + 1][e];
     }
     __syncwarp();
     if (lane == 0 && j + S < ntiles) issue(j + S);
@@ -272,25 +277,27 @@ k_conv_bwd(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUt
   }
   __syncwarp();
   const bool cvalid = c0 < C;
-  float wv[K][4], bv[4];
+  const float2 zero2 = make_float2(0.f, 0.f), one2 = make_float2(1.f, 1.f);
+  float2 wv[K][2], bv[2];  // channel pairs
   load_params<K>(w, bias, c0, cvalid, wv, bv);
-  float dw[K][4], db[4];
+  float2 dw[K][2], db[2];
 #pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    db[e] = 0.f;
+  for (int e = 0; e < 2; ++e) {
+    db[e] = zero2;
 #pragma unroll
-    for (int k = 0; k < K; ++k) dw[k][e] = 0.f;
+    for (int k = 0; k < K; ++k) dw[k][e] = zero2;
   }
-  float xw[K][4];  // xw[k] = input of step s - K + 1 + k
+  float2 xw[K][2];  // xw[k] = input of step s - K + 1 + k
 #pragma unroll
   for (int k = 0; k < K - 1; ++k)
-    hist_load<T, K>(x, init, rowb, b, C, c0, cvalid && ntiles > 0, run.ws - (K - 1) + k, xw[k]);
+    hist_load<T, K>(x, init, rowb, b, C, c0, cvalid && ntiles > 0, run.ws - (K - 1) + k,
+                    (float*)xw[k]);
   // open[k]: dx of step s - K + 1 + k summed over the gradients of steps < s
-  float open[K > 1 ? K - 1 : 1][4];
+  float2 open[K > 1 ? K - 1 : 1][2];
 #pragma unroll
   for (int k = 0; k < K - 1; ++k)
 #pragma unroll
-    for (int e = 0; e < 4; ++e) open[k][e] = 0.f;
+    for (int e = 0; e < 2; ++e) open[k][e] = zero2;
   T* dp = dx + (rowb + run.ws) * C + c0;  // dx of the next step to complete
   for (int j = 0; j < ntiles; ++j) {
     const bool ok = mbar_wait(&full[j % S], (j / S) & 1, kConvWaitNs);
@@ -303,41 +310,43 @@ k_conv_bwd(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUt
 #pragma unroll
     for (int i = 0; i < kConvBwdStep; ++i) {
       const int s = run.ws + j * kConvBwdStep + i;
-      float d[4], g[4], o[4];
-      ConvT<T>::lds(xs + i * G::ROWB, lane, xw[K - 1]);
-      ConvT<T>::lds(gs + i * G::ROWB, lane, d);
+      float2 d[2], o[2];
+      ConvT<T>::lds(xs + i * G::ROWB, lane, (float*)xw[K - 1]);
+      ConvT<T>::lds(gs + i * G::ROWB, lane, (float*)d);
       const bool in_seq = s < T_, owned = s < run.we;
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        float p = bv[e];
+      for (int e = 0; e < 2; ++e) {
+        float2 p = bv[e];
 #pragma unroll
-        for (int k = 0; k < K; ++k) p = fmaf(wv[k][e], xw[k][e], p);
-        const float sg = sig(p);
-        g[e] = in_seq ? d[e] * sg * (1.f + p * (1.f - sg)) : 0.f;
+        for (int k = 0; k < K; ++k) p = fma2(wv[k][e], xw[k][e], p);
+        const float2 sg = make_float2(sig(p.x), sig(p.y));
+        // g = d sg (1 + p (1 - sg))
+        const float2 oms = fma2(sg, make_float2(-1.f, -1.f), one2);
+        const float2 g = in_seq ? mul2(mul2(d[e], sg), fma2(p, oms, one2)) : zero2;
         if (owned) {
-          db[e] += g[e];
+          db[e] = add2(db[e], g);
 #pragma unroll
-          for (int k = 0; k < K; ++k) dw[k][e] = fmaf(g[e], xw[k][e], dw[k][e]);
+          for (int k = 0; k < K; ++k) dw[k][e] = fma2(g, xw[k][e], dw[k][e]);
         }
         // this step's gradient reaches dx of steps s - K + 1 .. s through taps 0 .. K - 1
         if (K > 1) {
-          o[e] = fmaf(g[e], wv[0][e], open[0][e]);
+          o[e] = fma2(g, wv[0][e], open[0][e]);
 #pragma unroll
-          for (int k = 0; k + 1 < K - 1; ++k) open[k][e] = fmaf(g[e], wv[k + 1][e], open[k + 1][e]);
-          open[K > 1 ? K - 2 : 0][e] = g[e] * wv[K - 1][e];
+          for (int k = 0; k + 1 < K - 1; ++k) open[k][e] = fma2(g, wv[k + 1][e], open[k + 1][e]);
+          open[K > 1 ? K - 2 : 0][e] = mul2(g, wv[K - 1][e]);
         } else {
-          o[e] = g[e] * wv[0][e];
+          o[e] = mul2(g, wv[0][e]);
         }
       }
       const int sd = s - (K - 1);  // dx of step sd is complete
       if (sd >= run.ws && sd < run.we) {
-        if (cvalid) ConvT<T>::stg(dp, o);
+        if (cvalid) ConvT<T>::stg(dp, (const float*)o);
         dp += C;
       }
 #pragma unroll
       for (int k = 0; k < K - 1; ++k)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) xw[k][e] = xw[k + 1][e];
+        for (int e = 0; e < 2; ++e) xw[k][e] = xw[k + 1][e];
     }
     __syncwarp();
     if (lane == 0 && j + S < ntiles) issue(j + S);
@@ -349,9 +358,10 @@ k_conv_bwd(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUt
   float* mine = red + (size_t)threadIdx.x * 4 * (K + 1);
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
+    const int pe = e >> 1;
 #pragma unroll
-    for (int k = 0; k < K; ++k) mine[e * (K + 1) + k] = dw[k][e];
-    mine[e * (K + 1) + K] = db[e];
+    for (int k = 0; k < K; ++k) mine[e * (K + 1) + k] = (e & 1) ? dw[k][pe].y : dw[k][pe].x;
+    mine[e * (K + 1) + K] = (e & 1) ? db[pe].y : db[pe].x;
   }
   __syncthreads();
   constexpr int n = 32 * 4 * (K + 1);  // one warp's channels x (taps + bias)

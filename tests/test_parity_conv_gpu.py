@@ -60,6 +60,18 @@ def test_conv1d_silu_every_output(case):
     assert all(v <= TOL[dtype] for v in errs.values()), errs
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_conv1d_silu_without_bias(dtype):
+    """bias NULL: the pre-activation has no bias term; dbias is still the sum
+    of the gradients of the pre-activation."""
+    inp = synth.conv_inputs(2, 300, 136, 3, dtype, 77, True)
+    inp["bias"] = None
+    gpu = run_gpu(inp, dtype)
+    ref = run_ref(inp)
+    errs = {k: rel_err(gpu[k], ref[k]) for k in ref}
+    assert all(v <= TOL[dtype] for v in errs.values()), errs
+
+
 def test_conv1d_silu_full_size_xbc_deterministic():
     """xBC of the bf16 d_inner-2048 workload: B = 4, T = 2048, C = H*P +
     2*G*N = 2304, d_conv = 4; every output against the oracle, and two runs

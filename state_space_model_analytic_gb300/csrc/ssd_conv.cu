@@ -25,15 +25,17 @@
 // Data movement.  Each warp has its own ring of stages in shared memory and
 // its own mbarriers: lane 0 keeps the next stages in flight with 2D TMA
 // boxes of 16 (forward) or 8 (backward) steps x 128 channels (x, and dout
-// for the backward, viewed as [B*T][C]); no barrier spans warps.  The K - 1 inputs before a
-// run come from plain loads (or the initial state before step 0).
+// for the backward, viewed as [B*T][C]); no barrier spans warps.  The K - 1
+// inputs before a run come from plain loads (or the initial state before
+// step 0).
 //
 // Compute.  A thread keeps the last K inputs in registers and walks its run
-// step by step, its 4 channels as two pairs in packed f32x2 arithmetic.  The backward walks on K - 1 steps past its run, keeping the
-// K - 1 dx values still open and storing each once the gradient of the step
-// K - 1 later is in (steps past T carry no gradient); dw and dbias stay in
-// registers over the run, are summed over the CTA's warps in shared memory
-// in order and over the CTAs along time in order by a last kernel.
+// step by step, its 4 channels as two pairs in packed f32x2 arithmetic.  The
+// backward walks on K - 1 steps past its run, keeping the K - 1 dx values
+// still open and storing each once the gradient of the step K - 1 later is
+// in (steps past T carry no gradient); dw and dbias stay in registers over
+// the run, are summed over the CTA's warps in shared memory in order and
+// over the CTAs along time in order by a last kernel.
 //
 // Waits on the TMA barriers are bounded: a wait that gives up sets a device
 // error word; the warp then waits (bounded) for the copies it still has in

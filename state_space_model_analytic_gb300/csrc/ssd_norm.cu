@@ -15,9 +15,9 @@
 // over the rows (CTA j takes groups j, j + grid, ...).  A thread copies its
 // vectors of the next group into shared memory (cp.async, double-buffered)
 // while it computes the current one, so two groups of 16-byte loads per
-// operand are in flight per thread at no register cost; the row sums (sum y^2, and the backward's dot) go
-// through one block reduction per group (warp shuffles, then the warps'
-// partials in order from shared memory).  The backward keeps its columns' dw
+// operand are in flight per thread at no register cost; the row sums (sum
+// y^2, and the backward's dot) go through one block reduction per group
+// (warp shuffles, then the warps' partials in order from shared memory).  The backward keeps its columns' dw
 // in registers over all its rows, writes them as the CTA's partial row, and a
 // final kernel sums the CTAs in a fixed order (deterministic for a given grid,
 // which follows the GPU's SM count).

@@ -172,6 +172,7 @@ size_t carve(Problem* p, char* base, int which) {
   p->drive = (float*)take(tokh);
   p->dA_part = (float*)take(B * nc * (Q / 16) * H * sizeof(float));  // per (chunk, tile or block)
   p->dD_part = (float*)take(B * nc * (Q / 16) * H * sizeof(float));
+  p->dtb_part = (float*)take(B * nc * (Q / 16) * H * sizeof(float));
   // tensor-core backward: one counter for all CTAs and one per (b, g, chunk,
   // 128-row block) unit; fp32 partials of dC, dB (2 x 128 x 128 floats) in two
   // slots per CTA, at most kBwdMaxCtas CTAs and one per (unit, head) item
@@ -315,10 +316,21 @@ int ssd_kernel_path(const ssd_dims* dims) {
   return tc_supported(p) ? 1 : 0;
 }
 
-int ssd_forward(const ssd_dims* dims, const void* x, const float* dt, const float* A,
+// The raw-dt mode of the fused tensor-core path (ssd_forward_raw /
+// ssd_backward_raw): dt holds dt_raw; the kernels apply softplus(dt_raw +
+// dt_bias) and A = -exp(a_log) where they read dt and A, and the backward
+// returns the gradients w.r.t. dt_raw (in ddt), a_log (in dA) and dt_bias.
+struct RawDt {
+  const float* dt_bias;
+  const float* a_log;
+  float* d_dt_bias;
+};
+
+namespace {
+int forward_impl(const ssd_dims* dims, const void* x, const float* dt, const float* A,
                 const void* B, const void* C, const float* D, const float* h0, void* y,
                 float* final_state, float* chunk_states, void* workspace, size_t workspace_bytes,
-                void* cuda_stream) {
+                void* cuda_stream, const RawDt* raw) {
   g_err.clear();
   int rc = validate(dims);
   if (rc) return rc;
@@ -333,6 +345,10 @@ int ssd_forward(const ssd_dims* dims, const void* x, const float* dt, const floa
   if ((rc = check_smem(p))) return rc;
   p.x = x; p.dt = dt; p.A = A; p.Bm = B; p.Cm = C; p.D = D; p.h0 = h0;
   p.y = y; p.final_state = final_state; p.hist = chunk_states;
+  if (raw) {
+    p.dt_bias = raw->dt_bias;
+    p.a_log = raw->a_log;
+  }
   const size_t need = carve(&p, nullptr, 0);
   if (workspace_bytes < need)
     return fail(SSD_ERR_INVALID_ARG, "ssd_forward: workspace %zu bytes < %zu needed",
@@ -343,6 +359,8 @@ int ssd_forward(const ssd_dims* dims, const void* x, const float* dt, const floa
 
   const bool tc = tc_supported(p);
   cudaError_t e;
+  if (raw && !(tc && tc_fused_states(p)))
+    return fail(SSD_ERR_UNSUPPORTED, "ssd_forward: raw-dt mode needs the fused tensor-core path");
   if (tc && tc_fused_states(p)) {
     // one kernel: chunk states, the state pass (look-back) and y
     e = tc_forward_single(p);
@@ -358,12 +376,22 @@ int ssd_forward(const ssd_dims* dims, const void* x, const float* dt, const floa
   if (e != cudaSuccess) return cuda_fail(e, "forward chunk-scan kernel");
   return SSD_OK;
 }
+}  // namespace
 
-int ssd_backward(const ssd_dims* dims, const void* x, const float* dt, const float* A,
+int ssd_forward(const ssd_dims* dims, const void* x, const float* dt, const float* A,
+                const void* B, const void* C, const float* D, const float* h0, void* y,
+                float* final_state, float* chunk_states, void* workspace, size_t workspace_bytes,
+                void* cuda_stream) {
+  return forward_impl(dims, x, dt, A, B, C, D, h0, y, final_state, chunk_states, workspace,
+                      workspace_bytes, cuda_stream, nullptr);
+}
+
+namespace {
+int backward_impl(const ssd_dims* dims, const void* x, const float* dt, const float* A,
                  const void* B, const void* C, const float* D, const float* h0, const void* dy,
                  const float* chunk_states, void* dx, float* ddt, float* dA, void* dB, void* dC,
                  float* dD, float* dh0, void* workspace, size_t workspace_bytes,
-                 void* cuda_stream) {
+                 void* cuda_stream, const RawDt* raw) {
   g_err.clear();
   int rc = validate(dims);
   if (rc) return rc;
@@ -384,6 +412,13 @@ int ssd_backward(const ssd_dims* dims, const void* x, const float* dt, const flo
                 workspace_bytes, need, chunk_states ? "" : " (recomputing chunk states)");
   p.x = x; p.dt = dt; p.A = A; p.Bm = B; p.Cm = C; p.D = D; p.h0 = h0; p.dy = dy;
   p.dx = dx; p.ddt = ddt; p.dA = dA; p.dB = dB; p.dC = dC; p.dD = dD; p.dh0 = dh0;
+  if (raw) {
+    p.dt_bias = raw->dt_bias;
+    p.a_log = raw->a_log;
+    p.d_dt_bias = raw->d_dt_bias;
+    if (!(tc_supported(p) && tc_fused_states(p)))
+      return fail(SSD_ERR_UNSUPPORTED, "ssd_backward: raw-dt mode needs the fused tensor-core path");
+  }
   p.hist = nullptr;
   carve(&p, (char*)workspace, which);
   if (chunk_states) p.hist = const_cast<float*>(chunk_states);
@@ -408,6 +443,16 @@ int ssd_backward(const ssd_dims* dims, const void* x, const float* dt, const flo
   if (e != cudaSuccess) return cuda_fail(e, "backward kernels");
   return SSD_OK;
 }
+}  // namespace
+
+int ssd_backward(const ssd_dims* dims, const void* x, const float* dt, const float* A,
+                 const void* B, const void* C, const float* D, const float* h0, const void* dy,
+                 const float* chunk_states, void* dx, float* ddt, float* dA, void* dB, void* dC,
+                 float* dD, float* dh0, void* workspace, size_t workspace_bytes,
+                 void* cuda_stream) {
+  return backward_impl(dims, x, dt, A, B, C, D, h0, dy, chunk_states, dx, ddt, dA, dB, dC, dD,
+                       dh0, workspace, workspace_bytes, cuda_stream, nullptr);
+}
 
 // ---- dt and A preprocessing in front of the core (ssd_dtprep.cu) ----------
 
@@ -431,6 +476,12 @@ int ssd_forward_raw(const ssd_dims* dims, const void* x, const float* dt_raw, co
   if (workspace_bytes < need)
     return fail(SSD_ERR_INVALID_ARG, "ssd_forward_raw: workspace %zu bytes < %zu needed",
                 workspace_bytes, need);
+  // the fused tensor-core path applies softplus and -exp where it reads dt and A
+  if (tc_supported(p) && tc_fused_states(p)) {
+    const RawDt raw{dt_bias, a_log, nullptr};
+    return forward_impl(dims, x, dt_raw, a_log, B, C, D, h0, y, final_state, chunk_states,
+                        (char*)workspace + extra, workspace_bytes - extra, cuda_stream, &raw);
+  }
   float* dt = (float*)workspace;
   float* A = (float*)((char*)workspace + up((size_t)p.B * p.T * p.H * sizeof(float)));
   p.stream = (cudaStream_t)cuda_stream;
@@ -464,6 +515,14 @@ int ssd_backward_raw(const ssd_dims* dims, const void* x, const float* dt_raw,
   if (workspace_bytes < need)
     return fail(SSD_ERR_INVALID_ARG, "ssd_backward_raw: workspace %zu bytes < %zu needed%s",
                 workspace_bytes, need, chunk_states ? "" : " (recomputing chunk states)");
+  // the fused tensor-core path: softplus and -exp where dt and A are read, the
+  // gradients w.r.t. dt_raw, dt_bias and a_log formed where ddt and dA are
+  if (tc_supported(p) && tc_fused_states(p)) {
+    const RawDt raw{dt_bias, a_log, d_dt_bias};
+    return backward_impl(dims, x, dt_raw, a_log, B, C, D, h0, dy, chunk_states, dx, d_dt_raw,
+                         d_a_log, dB, dC, dD, dh0, (char*)workspace + extra,
+                         workspace_bytes - extra, cuda_stream, &raw);
+  }
   float* dt = (float*)workspace;
   float* A = (float*)((char*)workspace + up((size_t)p.B * p.T * p.H * sizeof(float)));
   p.stream = (cudaStream_t)cuda_stream;

@@ -22,6 +22,13 @@ struct Problem {
   const float* D;
   const float* h0;  // nullable
   const void* dy;   // backward only
+  // raw-dt mode of the fused tensor-core path (both set, else nullptr): dt
+  // holds dt_raw, dt = softplus(dt_raw + dt_bias), A = -exp(a_log); the
+  // backward writes the gradients w.r.t. dt_raw, a_log (into ddt, dA) and
+  // dt_bias
+  const float* dt_bias;
+  const float* a_log;
+  float* d_dt_bias;
 
   // forward outputs
   void* y;
@@ -47,6 +54,7 @@ struct Problem {
   float* drive;    // [B][T][H]
   float* dA_part;  // [B][nc][Q/16][H]  (the used prefix depends on the kernel family)
   float* dD_part;  // [B][nc][Q/16][H]  (tile-count upper bound)
+  float* dtb_part; // raw-dt mode: per-(b, chunk, block) sums of the dt_raw gradient, same layout
   unsigned int* tickets;  // [1 + units] completion counters of the tensor-core backward
   int ntickets;
   float* bwd_part;        // tensor-core backward: fp32 dC, dB partials, 2 slots per CTA

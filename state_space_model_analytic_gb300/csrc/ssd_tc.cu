@@ -56,7 +56,30 @@ __device__ __forceinline__ bool wait_or_flag(uint64_t* bar, uint32_t parity) {
 
 struct TcDims {
   int B, T, H, P, N, G, Q, nc, hpg;
+  // raw-dt mode (both set): the dt argument holds dt_raw and the kernels use
+  // dt = softplus(dt_raw + dt_bias[h]) and A = -exp(a_log[h]); else nullptr
+  const float* dt_bias;
+  const float* a_log;
 };
+
+// softplus(z) = log(1 + e^z), evaluated as max(z, 0) + log1p(e^{-|z|}) (no overflow)
+__device__ __forceinline__ float softplus_tc(float z) {
+  return fmaxf(z, 0.f) + log1pf(expf(-fabsf(z)));
+}
+// dt of one element from the value stored in the dt argument (kRaw: the
+// kernel instantiation of the raw-dt mode, so the plain kernels carry none of
+// its code)
+template <bool kRaw>
+__device__ __forceinline__ float dt_of(const TcDims& d, float stored, int h) {
+  if (!kRaw) return stored;
+  return softplus_tc(stored + d.dt_bias[h]);
+}
+// A of head h
+template <bool kRaw>
+__device__ __forceinline__ float a_of(const TcDims& d, const float* __restrict__ A, int h) {
+  if (!kRaw) return A[h];
+  return -expf(d.a_log[h]);
+}
 
 // Column sums over the 32 lanes of a warp, for 16 columns: lane l returns the
 // sum over all lanes of v[l % 16].
@@ -115,10 +138,12 @@ __device__ __forceinline__ void scale_tile_rows(uint8_t* tile, int nchunks, F&& 
 }
 
 // dt of step `tid` of chunk c, head h (0 past the chunk), for 256 threads.
+template <bool kRaw = false>
 __device__ __forceinline__ float load_dt_256(const TcDims& d, const float* __restrict__ dt, int b,
                                              int c, int h) {
   const int tid = threadIdx.x;
-  return tid < d.Q ? dt[((size_t)b * d.T + (size_t)c * d.Q + tid) * d.H + h] : 0.f;
+  return tid < d.Q ? dt_of<kRaw>(d, dt[((size_t)b * d.T + (size_t)c * d.Q + tid) * d.H + h], h)
+                    : 0.f;
 }
 
 // Chunk-local inclusive cumsum (log2 units) of the dt values the 256 threads hold.
@@ -134,12 +159,13 @@ __device__ __forceinline__ void chunk_cumsum_256v(const TcDims& d, float dv, flo
 }
 
 // Chunk-local inclusive cumsum (log2 units) with 256 threads, one value each.
+template <bool kRaw = false>
 __device__ __forceinline__ void chunk_cumsum_256(const TcDims& d, const float* __restrict__ dt,
                                                  const float* __restrict__ A, int b, int c, int h,
                                                  float* s_cs2, float* s_dt, float* scratch) {
   const int tid = threadIdx.x;
-  const float dv = load_dt_256(d, dt, b, c, h);
-  const float cs = block_inclusive_scan(dv * (A[h] * kLog2e), scratch);
+  const float dv = load_dt_256<kRaw>(d, dt, b, c, h);
+  const float cs = block_inclusive_scan(dv * (a_of<kRaw>(d, A, h) * kLog2e), scratch);
   if (tid < d.Q) {
     s_cs2[tid] = cs;
     s_dt[tid] = dv;
@@ -312,7 +338,7 @@ __device__ __forceinline__ bool wait_ws(uint64_t* bar, uint32_t parity, volatile
 
 constexpr int kScanThreads = 288;  // consumer warps 0-3, scaler warps 4-7, issuer warp 8
 
-template <int MODE>
+template <int MODE, bool kRaw>
 __global__ void __launch_bounds__(kScanThreads, 1)
 k_state_scan_tc(const __grid_constant__ ScanStateMaps maps, TcDims d, const float* __restrict__ dt,
                 const float* __restrict__ A, const float* __restrict__ h0,
@@ -419,7 +445,7 @@ k_state_scan_tc(const __grid_constant__ ScanStateMaps maps, TcDims d, const floa
            i += (int)(gridDim.x * gridDim.y) * 128)
         tickets[i] = 0u;
     const int pt = tid - 128, lane = tid & 31, pw = pt >> 5;
-    const float a2 = A[h] * kLog2e;
+    const float a2 = a_of<kRaw>(d, A, h) * kLog2e;
     const int per = Q / 128;  // dt values per thread: 1 or 2, consecutive
     auto load_dt = [&](int it, float (&v)[2]) {
       const size_t t0 = (size_t)b * d.T + (size_t)chunk_of(it) * Q + (size_t)pt * per;
@@ -431,6 +457,11 @@ k_state_scan_tc(const __grid_constant__ ScanStateMaps maps, TcDims d, const floa
     if (nc > 1) load_dt(1, dv_next);
     for (int it = 0; it < nc; ++it) {
       const int k = it & 1;
+      // the stored values were fetched ahead; raw-dt mode: dt = softplus(...)
+      if (kRaw) {
+        dv[0] = dt_of<kRaw>(d, dv[0], h);
+        dv[1] = per == 2 ? dt_of<kRaw>(d, dv[1], h) : 0.f;
+      }
       // ---- decay tables: chunk-local inclusive cumsum of dt * A (log2 units)
       const float x0 = dv[0] * a2, x1 = dv[1] * a2;
       float run = x0 + x1;
@@ -891,6 +922,7 @@ __device__ __forceinline__ void st_release_gpu(unsigned int* p, unsigned v) {
   asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
+template <bool kRaw>
 __global__ void __launch_bounds__(256, 2)
 k_fwd_single_tc(const __grid_constant__ ScanMaps maps, TcDims d, const float* __restrict__ dt,
                 const float* __restrict__ A, const float* __restrict__ D,
@@ -959,7 +991,7 @@ k_fwd_single_tc(const __grid_constant__ ScanMaps maps, TcDims d, const float* __
     tma_load_2d(sX, &maps.x, h * d.P, row0, &bar_load);
   };
   if (tid == 0) issue_state_loads(crow + (nblk - 1) * 128);
-  chunk_cumsum_256(d, dt, A, b, c, h, s_cs2, s_dt, scratch);
+  chunk_cumsum_256<kRaw>(d, dt, A, b, c, h, s_cs2, s_dt, scratch);
 
   // ---- A: the chunk's state contributions, the last block first
   uint8_t* sWX = sC;  // w o X_k
@@ -1254,10 +1286,12 @@ constexpr uint32_t kBwG = 163840;     // gout bf16, row n, 64 p
 constexpr uint32_t kBwW = 180224;     // B_0 (k = 1) / C_1 (k = 0) per head, then W, then dx staging
 constexpr uint32_t kBwBytes = 212992;
 
+template <bool kRaw>
 __global__ void __launch_bounds__(kBwThreads, 1)
 k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, long long nitems,
          const float* __restrict__ dt, const float* __restrict__ A, const float* __restrict__ D,
          float* __restrict__ ddt, float* __restrict__ dA_part, float* __restrict__ dD_part,
+         float* __restrict__ dtb_part, float* __restrict__ d_dt_bias,
          void* __restrict__ dB_out, void* __restrict__ dC_out, float* __restrict__ dA,
          float* __restrict__ dD, unsigned int* __restrict__ tickets, float* __restrict__ part) {
   extern __shared__ __align__(1024) uint8_t smraw[];
@@ -1279,6 +1313,7 @@ k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, long long nitems,
   __shared__ float s_v[128];
   __shared__ float2 s_v2[128], scratch2[16];
   __shared__ float s_esum;
+  __shared__ float s_gsum[4];  // raw-dt mode: per-warp sums of the dt_raw gradient
   __shared__ uint64_t bar_shared, bar_head, bar_mma;
   __shared__ uint32_t tmem_base;
   __shared__ int s_flag;
@@ -1389,17 +1424,20 @@ k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, long long nitems,
     }
   }
   // dt, A and D of the next head are loaded one head ahead
-  float dt_next = load_dt_256(d, dt, b, c, h_first);
-  float A_next = A[h_first], D_next = D[h_first];
+  // the next head's dt and A (raw-dt mode: dt_raw and a_log) are fetched a
+  // head ahead and transformed where they are used, so the loads stay hidden
+  float dt_next = load_dt_256<false>(d, dt, b, c, h_first);
+  float A_next = kRaw ? d.a_log[h_first] : A[h_first], D_next = D[h_first];
   ok = wait_or_flag(&bar_shared, shared_phase);
   shared_phase ^= 1;
 
   for (int hh = 0; hh < kh && ok; ++hh) {
     const int h = h_first + hh;
-    const float dv = dt_next, Ah = A_next, Dh = D_next;
+    const float dv = (kRaw && tid < d.Q) ? dt_of<kRaw>(d, dt_next, h) : dt_next;
+    const float Ah = kRaw ? -expf(A_next) : A_next, Dh = D_next;
     if (hh + 1 < kh) {
-      dt_next = load_dt_256(d, dt, b, c, h + 1);
-      A_next = A[h + 1];
+      dt_next = load_dt_256<false>(d, dt, b, c, h + 1);
+      A_next = kRaw ? d.a_log[h + 1] : A[h + 1];
       D_next = D[h + 1];
     }
     chunk_cumsum_256v(d, dv, Ah * kLog2e, s_cs2, s_dt, scratch);
@@ -1715,12 +1753,26 @@ k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, long long nitems,
     if (tid == 127) s_esum = sc2.y;  // all e summed
     __syncthreads();
     const float da = sc2.x + s_esum + exp2f(end2 - ref2) * hg;
-    if (wg == 0) ddt[((size_t)crow + Jr) * d.H + h] = s_v[127 - row] + Ah * da;
+    // ddt; raw-dt mode: the gradient w.r.t. dt_raw, ddt times sigmoid(dt_raw +
+    // dt_bias) = 1 - exp(-dt) (dt being its softplus), with per-warp sums that
+    // the barriers of the block sum below publish to thread 0
+    if (wg == 0) {
+      float gdt = s_v[127 - row] + Ah * da;
+      if (kRaw) {
+        gdt *= -expm1f(-s_dt[Jr]);
+        float gw = gdt;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) gw += __shfl_xor_sync(0xffffffffu, gw, o);
+        if (lane == 0) s_gsum[q] = gw;
+      }
+      ddt[((size_t)crow + Jr) * d.H + h] = gdt;
+    }
     const float2 ad = block_sum2(make_float2(wg == 0 ? s_dt[Jr] * da : 0.f, dd), scratch2);
     if (tid == 0) {
       const size_t slot = (((size_t)b * d.nc + c) * nblk + k) * d.H + h;
       dA_part[slot] = ad.x;
       dD_part[slot] = ad.y;
+      if (kRaw) dtb_part[slot] = ((s_gsum[0] + s_gsum[1]) + s_gsum[2]) + s_gsum[3];
     }
     // ---- end of head: the tables are rebuilt by the next head, and the dx
     // staging (sW) by the next head's W or the final dC, dB sums
@@ -1819,20 +1871,25 @@ k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, long long nitems,
   if (s_flag) {
     __threadfence();
     const int nparts = d.B * d.nc * nblk;
+    // raw-dt mode: dA goes out as the gradient w.r.t. a_log (dA times A), and
+    // the dt_raw gradient sums as the gradient w.r.t. dt_bias
     for (int hr = tid >> 5; hr < d.H; hr += kBwThreads / 32) {
-      float sa = 0.f, sd = 0.f;
+      float sa = 0.f, sd = 0.f, sb = 0.f;
       for (int kk = lane; kk < nparts; kk += 32) {
         sa += __ldcg(dA_part + (size_t)kk * d.H + hr);
         sd += __ldcg(dD_part + (size_t)kk * d.H + hr);
+        if (kRaw) sb += __ldcg(dtb_part + (size_t)kk * d.H + hr);
       }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {
         sa += __shfl_xor_sync(0xffffffffu, sa, o);
         sd += __shfl_xor_sync(0xffffffffu, sd, o);
+        if (kRaw) sb += __shfl_xor_sync(0xffffffffu, sb, o);
       }
       if (lane == 0) {
-        dA[hr] = sa;
+        dA[hr] = kRaw ? sa * a_of<kRaw>(d, A, hr) : sa;
         dD[hr] = sd;
+        if (kRaw) d_dt_bias[hr] = sb;
       }
     }
   }
@@ -1948,7 +2005,9 @@ bool map_f32(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uin
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-TcDims tc_dims(const Problem& p) { return TcDims{p.B, p.T, p.H, p.P, p.N, p.G, p.Q, p.nc, p.hpg}; }
+TcDims tc_dims(const Problem& p) {
+  return TcDims{p.B, p.T, p.H, p.P, p.N, p.G, p.Q, p.nc, p.hpg, p.dt_bias, p.a_log};
+}
 
 template <typename K>
 cudaError_t set_smem_tc(K kernel, size_t bytes) {
@@ -2049,11 +2108,12 @@ cudaError_t tc_state_scan(const Problem& p, const char* name, float* final_or_dh
     return cudaErrorInvalidValue;
   // two pipeline stages of tiles + the bf16 row staging tile(s)
   const size_t smem = 2 * 3 * (size_t)p.Q * 128 + (MODE == 1 ? 2 : 1) * 16384 + 1024;
-  cudaError_t e = set_smem_tc(k_state_scan_tc<MODE>, smem);
+  auto kern = p.dt_bias ? k_state_scan_tc<MODE, true> : k_state_scan_tc<MODE, false>;
+  cudaError_t e = set_smem_tc(kern, smem);
   if (e != cudaSuccess) return e;
   {
     LaunchScope ls(name, p.stream);
-    e = launch_pdl(k_state_scan_tc<MODE>, dim3(p.H, p.B), dim3(kScanThreads), smem, p.stream, maps,
+    e = launch_pdl(kern, dim3(p.H, p.B), dim3(kScanThreads), smem, p.stream, maps,
                    tc_dims(p), p.dt, p.A, p.h0, p.hist, final_or_dh0,
                    MODE == 1 ? p.tickets : (unsigned int*)nullptr, p.ntickets);
   }
@@ -2097,10 +2157,11 @@ cudaError_t tc_forward_single(const Problem& p) {
   cudaError_t e = cudaMemsetAsync(p.fwd_flags, 0, nflags * sizeof(unsigned int), p.stream);
   if (e != cudaSuccess) return e;
   const size_t smem = kScanBytes + 1024;
-  if ((e = set_smem_tc(k_fwd_single_tc, smem)) != cudaSuccess) return e;
+  auto kern = p.dt_bias ? k_fwd_single_tc<true> : k_fwd_single_tc<false>;
+  if ((e = set_smem_tc(kern, smem)) != cudaSuccess) return e;
   {
     LaunchScope ls("fwd_single_tc", p.stream);
-    k_fwd_single_tc<<<(unsigned)(nflags - 1), 256, smem, p.stream>>>(
+    kern<<<(unsigned)(nflags - 1), 256, smem, p.stream>>>(
         maps, tc_dims(p), p.dt, p.A, p.D, p.h0, p.hist, p.final_state, p.fwd_flags);
   }
   return cudaGetLastError();
@@ -2134,7 +2195,8 @@ cudaError_t tc_backward(const Problem& p) {
       !map_bf16(&maps.gt, p.gT, srows, (uint64_t)p.P, 128))
     return cudaErrorInvalidValue;
   const size_t smem = kBwBytes + 1024;
-  if ((e = set_smem_tc(k_bwd_tc, smem)) != cudaSuccess) return e;
+  auto kern = p.dt_bias ? k_bwd_tc<true> : k_bwd_tc<false>;
+  if ((e = set_smem_tc(kern, smem)) != cudaSuccess) return e;
   const int nblk = p.Q / 128;
   // one CTA per SM (at most kBwdMaxCtas, at most one per item), each taking an
   // equal contiguous range of the (unit, head) items
@@ -2157,8 +2219,9 @@ cudaError_t tc_backward(const Problem& p) {
   cfg.numAttrs = 1;
   {
     LaunchScope ls("bwd_tc", p.stream);
-    e = cudaLaunchKernelEx(&cfg, k_bwd_tc, maps, tc_dims(p), nitems, p.dt, p.A, p.D, p.ddt,
-                           p.dA_part, p.dD_part, p.dB, p.dC, p.dA, p.dD, p.tickets, p.bwd_part);
+    e = cudaLaunchKernelEx(&cfg, kern, maps, tc_dims(p), nitems, p.dt, p.A, p.D, p.ddt,
+                           p.dA_part, p.dD_part, p.dtb_part, p.d_dt_bias, p.dB, p.dC, p.dA, p.dD,
+                           p.tickets, p.bwd_part);
   }
   if (e != cudaSuccess) return e;
   return cudaGetLastError();

@@ -69,6 +69,32 @@ def test_raw_entry_points_every_output(case, history):
     assert not bad, errs
 
 
+@pytest.mark.parametrize("q,h0,history", [(128, True, "recompute"), (256, True, "given"),
+                                           (128, False, "given"), (256, False, "recompute")])
+def test_raw_entry_points_fused_path(q, h0, history):
+    """Shapes with enough (b, h) pairs for the fused tensor-core path, where the
+    raw-dt transforms run inside the step's kernels (the forward, the state
+    scans, the backward): it must be those kernels that ran; every output
+    against the oracle, with an initial state or without, history given or
+    recomputed, several chunks and groups."""
+    from state_space_model_analytic_gb300 import _native as nat
+    dims = synth.Dims(4, 512, 64, 64, 128, 16, q, "bf16")  # B * H = 256 (b, h) pairs
+    inp = synth.make_inputs(dims, 41 + q, h0, "softplus")
+    nat.trace_begin(64)
+    try:
+        gpu = run_raw(dims, inp, history)
+    finally:
+        nat.trace_end()
+    names = [r["name"] for r in nat.trace_read()]
+    nat.trace_reset()
+    assert "fwd_single_tc" in names and "bwd_tc" in names and "dt_prep" not in names, names
+    ref = run_oracle_raw(dims, inp)
+    errs = {k: rel_err(gpu[k], ref[k]) for k in KEYS if k in gpu}
+    bad = {k: v for k, v in errs.items() if not v <= TOL["bf16"]}
+    assert not bad, errs
+    nat.check(nat.lib().ssd_device_status())
+
+
 def test_raw_entry_points_full_size_bf16_d_inner_2048():
     """The benchmark workload (B4 T2048 H32 P64 N128 G1 Q256) through the
     raw entry points, every output against the oracle."""

@@ -23,6 +23,7 @@
 // which follows the GPU's SM count).
 #include <cuda_bf16.h>
 
+#include "f32x2.cuh"
 #include "ssd_common.cuh"
 #include "ssd_internal.h"
 
@@ -78,21 +79,27 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
+// logistic sigmoid 1 / (1 + 2^(-z log2 e)) of a pair of values from the
+// hardware base-2 exponential and reciprocal approximations (about 1e-6
+// relative, exact limits at both ends), the multiply and the add packed
+// (f32x2)
+__device__ __forceinline__ float2 sigmoid2(float2 z) {
+  const float2 u = mul2(z, make_float2(-1.4426950408889634f, -1.4426950408889634f));
+  float2 e, r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e.x) : "f"(u.x));
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e.y) : "f"(u.y));
+  const float2 den = add2(make_float2(1.f, 1.f), e);
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r.x) : "f"(den.x));
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r.y) : "f"(den.y));
+  return r;
+}
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
   return v;
 }
 
-// logistic sigmoid 1 / (1 + 2^(-z log2 e)) from the hardware base-2
-// exponential and reciprocal approximations (about 1e-6 relative, exact
-// limits at both ends)
-__device__ __forceinline__ float sigmoidf_(float z) {
-  float e, r;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(z * -1.4426950408889634f));
-  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.f + e));
-  return r;
-}
 
 // Block sums of NV values per thread (row partials): every thread gets the
 // totals, the warps' partials added in warp order.  red: [2][NV][warps]
@@ -172,8 +179,13 @@ k_norm_fwd(long long rows, int width, float eps, const T* __restrict__ y, const 
       for (int v = 0; v < V; ++v) {
         float a[E];
         Vec<T>::cvt(qy[r][v], a);
+        float2 s2 = make_float2(0.f, 0.f);  // even and odd columns (f32x2)
 #pragma unroll
-        for (int i = 0; i < E; ++i) ss[r] = fmaf(a[i], a[i], ss[r]);
+        for (int i = 0; i < E; i += 2) {
+          const float2 a2 = make_float2(a[i], a[i + 1]);
+          s2 = fma2(a2, a2, s2);
+        }
+        ss[r] += s2.x + s2.y;
       }
     }
     block_sums<R>(ss, red, buf);
@@ -186,8 +198,16 @@ k_norm_fwd(long long rows, int width, float eps, const T* __restrict__ y, const 
         float a[E], zz[E], o[E];
         Vec<T>::cvt(qy[r][v], a);
         Vec<T>::cvt(qz[r][v], zz);
+        const float2 inv2 = make_float2(inv, inv);
 #pragma unroll
-        for (int i = 0; i < E; ++i) o[i] = (a[i] * inv) * wv[v][i] * (zz[i] * sigmoidf_(zz[i]));
+        for (int i = 0; i < E; i += 2) {  // (a * inv) * w * (z * sigmoid(z)), pairs in f32x2
+          const float2 z2 = make_float2(zz[i], zz[i + 1]);
+          const float2 o2 = mul2(mul2(mul2(make_float2(a[i], a[i + 1]), inv2),
+                                      make_float2(wv[v][i], wv[v][i + 1])),
+                                 mul2(z2, sigmoid2(z2)));
+          o[i] = o2.x;
+          o[i + 1] = o2.y;
+        }
         Vec<T>::store(out + (r0 + r) * width + (long long)(v * nt + t) * E, o);
       }
       if (inv_rms && t == 0) inv_rms[r0 + r] = inv;
@@ -265,11 +285,17 @@ k_norm_bwd(long long rows, int width, float eps, const T* __restrict__ y, const 
         Vec<T>::cvt(qy[r][v], a);
         Vec<T>::cvt(qz[r][v], zz);
         Vec<T>::cvt(qg[r][v], gg);
+        float2 dot2 = make_float2(0.f, 0.f), ss2 = make_float2(0.f, 0.f);  // f32x2 pairs
 #pragma unroll
-        for (int i = 0; i < E; ++i) {
-          dot = fmaf(gg[i] * (zz[i] * sigmoidf_(zz[i])) * wv[v][i], a[i], dot);
-          ss = fmaf(a[i], a[i], ss);
+        for (int i = 0; i < E; i += 2) {
+          const float2 z2 = make_float2(zz[i], zz[i + 1]), a2 = make_float2(a[i], a[i + 1]);
+          const float2 gw = mul2(mul2(make_float2(gg[i], gg[i + 1]), mul2(z2, sigmoid2(z2))),
+                                 make_float2(wv[v][i], wv[v][i + 1]));
+          dot2 = fma2(gw, a2, dot2);
+          ss2 = fma2(a2, a2, ss2);
         }
+        dot += dot2.x + dot2.y;
+        ss += ss2.x + ss2.y;
       }
       sums[2 * r] = dot;
       sums[2 * r + 1] = ss;
@@ -286,14 +312,26 @@ k_norm_bwd(long long rows, int width, float eps, const T* __restrict__ y, const 
         Vec<T>::cvt(qy[r][v], a);
         Vec<T>::cvt(qz[r][v], zz);
         Vec<T>::cvt(qg[r][v], gg);
+        const float2 iv2 = make_float2(iv, iv), nk3 = make_float2(-k3, -k3);
+        const float2 one2 = make_float2(1.f, 1.f);
 #pragma unroll
-        for (int i = 0; i < E; ++i) {
-          const float s = sigmoidf_(zz[i]);
-          const float gate = zz[i] * s;
-          const float nrm = a[i] * iv;
-          oy[i] = gg[i] * gate * wv[v][i] * iv - a[i] * k3;
-          oz[i] = gg[i] * nrm * wv[v][i] * (s * (1.f + zz[i] * (1.f - s)));
-          dw[v][i] += gg[i] * gate * nrm;
+        for (int i = 0; i < E; i += 2) {  // pairs of columns in f32x2
+          const float2 z2 = make_float2(zz[i], zz[i + 1]), a2 = make_float2(a[i], a[i + 1]);
+          const float2 g2 = make_float2(gg[i], gg[i + 1]), w2 = make_float2(wv[v][i], wv[v][i + 1]);
+          const float2 s2 = sigmoid2(z2);
+          const float2 gate = mul2(z2, s2);
+          const float2 nrm = mul2(a2, iv2);
+          const float2 y2 = fma2(a2, nk3, mul2(mul2(mul2(g2, gate), w2), iv2));
+          // silu'(z) = s (1 + z (1 - s))
+          const float2 ds = mul2(s2, fma2(z2, fma2(s2, make_float2(-1.f, -1.f), one2), one2));
+          const float2 z2o = mul2(mul2(mul2(g2, nrm), w2), ds);
+          const float2 dw2 = fma2(mul2(g2, gate), nrm, make_float2(dw[v][i], dw[v][i + 1]));
+          oy[i] = y2.x;
+          oy[i + 1] = y2.y;
+          oz[i] = z2o.x;
+          oz[i + 1] = z2o.y;
+          dw[v][i] = dw2.x;
+          dw[v][i + 1] = dw2.y;
         }
         const long long off = (r0 + r) * width + (long long)(v * nt + t) * E;
         Vec<T>::store(dy + off, oy);

@@ -131,7 +131,10 @@ SSD_API int ssd_backward(const ssd_dims* dims,
  * Every other argument, layout, error and rule is that of ssd_forward /
  * ssd_backward; the workspace is ssd_workspace_bytes(dims, 3) (forward), 4
  * (backward given the history) or 5 (backward recomputing it).  The history
- * written by ssd_forward_raw is the core's history for dt and A.
+ * written by ssd_forward_raw is the core's history for dt and A.  Where the
+ * fused tensor-core path applies, the transforms run inside the core's
+ * kernels; elsewhere a preprocessing kernel writes dt and A into the
+ * workspace and a gradient pass follows the core.
  */
 SSD_API int ssd_forward_raw(const ssd_dims* dims,
                             const void* x, const float* dt_raw, const float* dt_bias,

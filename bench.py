@@ -47,6 +47,8 @@ def parse_args():
                     help="seconds of oracle work for the cpu_baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the per-workload table (every SSD-core workload)")
     ap.add_argument("--next-iters", type=int, default=200,
                     help="timed calls per direction of the gated RMSNorm and conv1d lines")
     return ap.parse_args()
@@ -54,7 +56,7 @@ def parse_args():
 
 # ---------------------------------------------------------------------------
 # algorithmic bytes (each tensor read or written once) of one launch of each
-# kernel, for the problem dims `d`; see the kernel table in the design doc.
+# kernel, for the problem dims `d`.
 
 def _sizes(d, has_h0):
     s = 2 if d.dtype == "bf16" else 4
@@ -171,6 +173,24 @@ def aggregate_ranks(ms_local, tokens_local, dist=None, device=None):
     return ms_max, tokens_local * world / (ms_max / 1e3)
 
 
+CLOCK_PAD_S = 0.6
+
+
+def pad_replays(graph, flush, seconds):
+    """Replay `graph` (L2 flushed between replays, as in the timed loop) for
+    about `seconds` of wall time; untimed."""
+    import torch
+    t0 = time.perf_counter()
+    n = 0
+    while time.perf_counter() - t0 < seconds:
+        graph.replay()
+        flush.fill_(1.0)
+        n += 1
+        if n % 32 == 0:
+            torch.cuda.synchronize()
+    torch.cuda.synchronize()
+
+
 # ---------------------------------------------------------------------------
 class ClockSampler:
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -262,6 +282,100 @@ def cpu_baseline_run(dims, inp, threads, seconds):
     return value, sample, rows * tokens, total / reps
 
 
+def workload_config(name, dims, world=1):
+    """The `config` object of the JSON line; the same for both arms."""
+    return {"workload": name, "batch": dims.batch, "seqlen": dims.seqlen, "nheads": dims.nheads,
+            "headdim": dims.headdim, "dstate": dims.dstate, "ngroups": dims.ngroups,
+            "chunk": dims.chunk, "storage": dims.dtype, "accumulate": "fp32",
+            "history": "saved by forward, consumed by backward",
+            "l2": "GPU arm: flushed between timed steps (256 MiB write, outside the step events)",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
+
+
+def time_workload(idx, steps, warmup, flush, dev):
+    """One SSD-core workload timed like the headline: forward + backward
+    (history saved and consumed) as a CUDA-graph replay, inputs resident, L2
+    flushed between steps outside the per-step events; plus one traced eager
+    pass for the per-kernel split."""
+    import torch
+    import state_space_model_analytic_gb300 as ssd
+    from state_space_model_analytic_gb300 import _native as nat
+    from state_space_model_analytic_gb300 import synth
+    name, dims, has_h0, _ = synth.CONFIGS[idx]
+    _, inp = synth.config_inputs(idx)
+    io = torch.bfloat16 if dims.dtype == "bf16" else torch.float32
+
+    def to(a, dtype):
+        return None if a is None else torch.from_numpy(
+            np.ascontiguousarray(a, dtype=np.float32)).to(dtype).to(dev)
+
+    ti = {"x": to(inp["x"], io), "dt": to(inp["dt"], torch.float32),
+          "A": to(inp["A"], torch.float32), "B": to(inp["B"], io), "C": to(inp["C"], io),
+          "D": to(inp["D"], torch.float32), "h0": to(inp["h0"], torch.float32),
+          "dy": to(inp["dy"], io)}
+    del inp
+    Bz, H, P, N, nc, Q = (dims.batch, dims.nheads, dims.headdim, dims.dstate, dims.nchunks,
+                          dims.chunk)
+    fo = {"y": torch.empty_like(ti["x"]), "final_state": torch.empty(Bz, H, P, N, device=dev),
+          "chunk_states": torch.empty(Bz, nc, H, P, N, device=dev)}
+    bo = {"dx": torch.empty_like(ti["x"]), "ddt": torch.empty_like(ti["dt"]),
+          "dA": torch.empty_like(ti["A"]), "dB": torch.empty_like(ti["B"]),
+          "dC": torch.empty_like(ti["C"]), "dD": torch.empty_like(ti["D"]),
+          "dh0": torch.empty(Bz, H, P, N, device=dev)}
+    cd = ssd.dims_of(ti["x"], ti["B"], Q)
+    wf, wb = ssd.alloc_workspace(cd, 0, dev), ssd.alloc_workspace(cd, 1, dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        ssd.forward(ti["x"], ti["dt"], ti["A"], ti["B"], ti["C"], ti["D"], ti["h0"], chunk=Q,
+                    out=fo, workspace=wf)
+        ssd.backward(ti["x"], ti["dt"], ti["A"], ti["B"], ti["C"], ti["D"], ti["h0"], ti["dy"],
+                     fo["chunk_states"], chunk=Q, out=bo, workspace=wb)
+
+    for _ in range(warmup):
+        step()
+        flush.fill_(1.0)
+    torch.cuda.synchronize()
+    nat.trace_begin(steps * 16)
+    for i in range(steps):
+        step()
+        flush.fill_(float(i))
+    torch.cuda.synchronize()
+    nat.trace_end()
+    kern = nat.trace_read()
+    nat.trace_reset()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    for _ in range(warmup):
+        graph.replay()
+        flush.fill_(1.0)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    for i in range(steps):
+        ev[i][0].record(stream)
+        graph.replay()
+        ev[i][1].record(stream)
+        flush.fill_(float(i))
+    torch.cuda.synchronize()
+    ms = sum(a.elapsed_time(b) for a, b in ev) / steps
+    hbm, bf16_tf, _ = read_peaks()
+    sb = step_bytes(dims, has_h0)
+    out = {"workload": name, "value": dims.tokens / (ms / 1e3), "unit": UNIT,
+           "ms_per_step": ms, "steps": steps, "storage": dims.dtype,
+           "kernel_path": "tcgen05" if ssd.kernel_path(cd) == 1 else "simt",
+           "algorithmic_bytes": sb, "step_roofline_frac": sb / (ms / 1e3) / 1e9 / hbm,
+           "tensor_flops": step_flops(dims),
+           "kernels": [{"name": k["name"], "avg_us": round(1e3 * k["ms"] / max(k["launches"], 1), 2),
+                        "launches_per_step": k["launches"] / steps}
+                       for k in sorted(kern, key=lambda k: -k["ms"])],
+           "launch": "CUDA graph replay"}
+    del graph, ti, fo, bo, wf, wb
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_reference(args, dims, inp, name):
     import oracle
     oracle.build_oracle()
@@ -281,9 +395,7 @@ def run_reference(args, dims, inp, name):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sec / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded; same inputs as the GPU arm)",
-        "config": {"workload": name, "batch": dims.batch, "seqlen": dims.seqlen,
-                   "nheads": dims.nheads, "headdim": dims.headdim, "dstate": dims.dstate,
-                   "ngroups": dims.ngroups, "chunk": dims.chunk, "storage": dims.dtype},
+        "config": workload_config(name, dims, 1),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -404,7 +516,7 @@ def main():
     e2e = None
     if not args.no_e2e:
         host_in = {k: (None if v is None else v.cpu().pin_memory()) for k, v in t_in.items()}
-        outs = ["y", "dx", "ddt", "dA", "dB", "dC", "dD", "dh0"]
+        outs = ["y", "final_state", "dx", "ddt", "dA", "dB", "dC", "dD", "dh0"]
         all_out = {**fwd_out, **bwd_out}
         host_out = {k: torch.empty(all_out[k].shape, dtype=all_out[k].dtype).pin_memory()
                     for k in outs}
@@ -422,7 +534,7 @@ def main():
                     st["in"][k].copy_(v, non_blocking=True)
 
         def copy_out(st):
-            res = {"y": st["fwd"]["y"], **st["bwd"]}
+            res = {"y": st["fwd"]["y"], "final_state": st["fwd"]["final_state"], **st["bwd"]}
             for k in outs:
                 host_out[k].copy_(res[k], non_blocking=True)
 
@@ -530,21 +642,31 @@ def main():
         torch.cuda.synchronize()
         evg = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(args.steps)]
+        # the clock sampler runs over the timed steps and CLOCK_PAD_S of the
+        # same replays on each side (a short timed region would otherwise fall
+        # between two samples)
         clocks_g = ClockSampler(local_rank)
         if rank == 0:
             clocks_g.start()
+        pad_replays(graph, flush, CLOCK_PAD_S)
         if dist:
             dist.barrier()
         torch.cuda.synchronize()
+        t_g0 = time.perf_counter()
         for i in range(args.steps):
             evg[i][0].record(stream)
             graph.replay()
             evg[i][1].record(stream)
             flush.fill_(float(i))
         torch.cuda.synchronize()
+        t_g1 = time.perf_counter()
         if dist:
             dist.barrier()
+        pad_replays(graph, flush, CLOCK_PAD_S)
         clk_g = clocks_g.stop() if rank == 0 else None
+        if clk_g is not None:
+            clk_g["window"] = (f"the {args.steps} timed replays ({1e3 * (t_g1 - t_g0):.1f} ms) "
+                               f"with {CLOCK_PAD_S} s of the same replays before and after")
         graph_ms = sum(a.elapsed_time(b) for a, b in evg) / args.steps
     except Exception as e:  # capture unsupported here: the eager number stands
         graph_err = f"{type(e).__name__}: {e}"[:200]
@@ -703,6 +825,17 @@ def main():
     except Exception as e:  # noqa: BLE001  (reported, the headline stands)
         conv_line = {"error": f"{type(e).__name__}: {e}"[:200]}
 
+    # ---- every SSD-core workload, timed the same way (rank 0 only)
+    workloads = None
+    if not args.no_workloads and rank == 0:
+        workloads = {}
+        n_w = max(5, min(args.steps, 50))
+        for idx in sorted(synth.CONFIGS):
+            try:
+                workloads[str(idx)] = time_workload(idx, n_w, max(3, args.warmup), flush, dev)
+            except Exception as e:  # noqa: BLE001  (reported, the headline stands)
+                workloads[str(idx)] = {"error": f"{type(e).__name__}: {e}"[:200]}
+
     if graph_ms is not None:
         ms_max, value = aggregate_ranks(graph_ms, tokens, dist, dev)
         clk = clk_g if rank == 0 else clk
@@ -755,18 +888,14 @@ def main():
         "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if dims.dtype == "bf16" else "f32",
         "data": "synthetic (seeded PCG64; distributions of the SSD-core workloads)",
-        "config": {"workload": name, "batch": Bz, "seqlen": T, "nheads": H, "headdim": P,
-                   "dstate": N, "ngroups": G, "chunk": Q, "storage": dims.dtype,
-                   "accumulate": "fp32", "history": "saved by forward, consumed by backward",
-                   "l2": "flushed between timed steps (256 MiB write, outside the step events)",
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "kernel_path": "tcgen05" if ssd.kernel_path(cdims) == 1 else "simt",
-                   "launch": launch_mode},
+        "config": workload_config(name, dims, world),
+        "kernel_path": "tcgen05" if ssd.kernel_path(cdims) == 1 else "simt",
+        "launch": launch_mode,
         "roofline": roofline, "step_roofline": step_roof, "kernels": kernels,
         "gpu_launches": launches, "wall_s_timed": wall,
         "eager_ms_per_step": eager_max, "raw_dt_step": raw_line, "rmsnorm_gated": norm_line,
         "conv1d_silu": conv_line,
-        "clocks": clk, "cpu_baseline": cpu, "e2e": e2e,
+        "clocks": clk, "cpu_baseline": cpu, "e2e": e2e, "workloads": workloads,
     }
     print(json.dumps(line), flush=True)
     if dist:

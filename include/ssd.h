@@ -218,22 +218,26 @@ SSD_API int ssd_conv1d_silu_backward(int64_t batch, int64_t seqlen, int64_t chan
 /*
  * Forward pass that allocates nothing (no counterpart on the pages: an
  * addition of this library for callers that cannot allocate).
- * Same inputs, outputs, layouts and errors as ssd_forward, but no workspace
- * argument: it works in a fixed device array of SSD_NOALLOC_SCRATCH_BYTES
- * that is part of the library image, for callers that own all device memory
- * through their own pool, run where an allocation may synchronise the
- * device or fail, or have no allocator at hand.  It calls no cudaMalloc,
- * cudaFree or other allocating routine.
+ * Same inputs, outputs, layouts, errors and launch sequence as ssd_forward
+ * (its outputs are bit-for-bit those of ssd_forward for the same dims), but
+ * no workspace argument: it works in a fixed device array of
+ * SSD_NOALLOC_SCRATCH_BYTES that is part of the library image, for callers
+ * that own all device memory through their own pool, run where an
+ * allocation may synchronise the device or fail, or have no allocator at
+ * hand.  It calls no cudaMalloc, cudaFree or other allocating routine.
  *   - The array lives on every GPU that loads the library until the process
  *     exits.  The first call on a device looks up its address on that device
  *     (cudaGetSymbolAddress); make that first call before any stream
- *     capture.
+ *     capture.  Only a successful lookup is kept; after a failure
+ *     (SSD_ERR_CUDA) the next call looks again.
  *   - All calls on a device share the array and it keeps the last call's
  *     contents: calls whose kernels may overlap on the GPU (several streams
- *     or host threads) race; order them.
- *   - Scratch used: B*H*nc floats, plus B*nc*H*P*N floats when chunk_states
- *     is NULL (each rounded up to 256 bytes).  Larger problems are rejected
- *     with SSD_ERR_UNSUPPORTED and a message; nothing is launched.
+ *     or host threads) race; order them.  What must start at zero is
+ *     cleared by each call on its own stream.
+ *   - Scratch used: B*H*nc floats and B*nc*H + 1 words, plus B*nc*H*P*N
+ *     floats when chunk_states is NULL (each rounded up to 256 bytes).
+ *     Larger problems are rejected with SSD_ERR_UNSUPPORTED and a message;
+ *     nothing is launched.
  */
 #define SSD_NOALLOC_SCRATCH_BYTES (8u << 20)
 SSD_API int ssd_forward_noalloc(const ssd_dims* dims,

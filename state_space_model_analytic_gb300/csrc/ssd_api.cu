@@ -206,6 +206,11 @@ int check_smem(const Problem& p) {
 
 void set_last_error(const char* msg) { g_err = msg; }
 
+// The checks and problem set-up of ssd_forward, for the other entry points.
+int validate_dims(const ssd_dims* d) { return validate(d); }
+Problem problem_of(const ssd_dims* d) { return base_problem(d); }
+int check_shared_memory(const Problem& p) { return check_smem(p); }
+
 }  // namespace ssd
 
 using namespace ssd;

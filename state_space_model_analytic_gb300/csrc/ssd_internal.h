@@ -7,6 +7,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include "../../include/ssd.h"
+
 namespace ssd {
 
 struct Problem {
@@ -64,6 +66,13 @@ struct Problem {
 
   cudaStream_t stream;
 };
+
+// Argument checks and problem set-up shared by the entry points
+// (ssd_api.cu): each check returns SSD_OK or an SSD_ERR_* code and sets the
+// thread's last-error message.
+int validate_dims(const ssd_dims* d);
+Problem problem_of(const ssd_dims* d);  // call after validate_dims succeeded
+int check_shared_memory(const Problem& p);
 
 // Gated RMSNorm after the core (ssd_norm.cu).  The backward keeps per-CTA
 // column sums of the weight gradient in part[grid][width], grid <=

@@ -76,6 +76,45 @@ def test_rejects_bad_dims(L, kw, code):
     assert L.ssd_kernel_path(d) == -1
 
 
+@pytest.mark.parametrize("kw,code", [
+    (dict(nheads=3), nat.SSD_ERR_INVALID_ARG),
+    (dict(batch=0), nat.SSD_ERR_INVALID_ARG),
+    (dict(chunk=48), nat.SSD_ERR_UNSUPPORTED),
+    (dict(headdim=24), nat.SSD_ERR_UNSUPPORTED),
+])
+def test_noalloc_rejects_bad_dims_like_ssd_forward(L, kw, code):
+    d = dims(**kw)
+    fake = ctypes.c_void_p(1 << 20)
+    rc = L.ssd_forward_noalloc(d, fake, fake, fake, fake, fake, fake, None, fake, None, None,
+                               None)
+    assert rc == code, nat.last_error()
+    fwd_msg = nat.last_error()
+    assert fwd_msg
+    rc_fwd = L.ssd_forward(d, fake, fake, fake, fake, fake, fake, None, fake, None, None, fake,
+                           1 << 30, None)
+    assert rc_fwd == rc and nat.last_error() == fwd_msg
+
+
+def test_noalloc_rejects_fields_and_pointers_before_launching(L):
+    d = dims()
+    d.reserved = 1
+    f = ctypes.c_void_p(1 << 20)
+    assert L.ssd_forward_noalloc(d, f, f, f, f, f, f, None, f, None, None, None) == \
+        nat.SSD_ERR_INVALID_ARG
+    d = dims()
+    d.dtype = 5
+    assert L.ssd_forward_noalloc(d, f, f, f, f, f, f, None, f, None, None, None) == \
+        nat.SSD_ERR_INVALID_ARG
+    assert L.ssd_forward_noalloc(None, f, f, f, f, f, f, None, f, None, None, None) == \
+        nat.SSD_ERR_INVALID_ARG
+    d = dims()
+    assert L.ssd_forward_noalloc(d, None, f, f, f, f, f, None, f, None, None, None) == \
+        nat.SSD_ERR_INVALID_ARG
+    bad = ctypes.c_void_p((1 << 20) + 4)
+    assert L.ssd_forward_noalloc(d, f, f, f, f, f, f, None, bad, None, None, None) == \
+        nat.SSD_ERR_ALIGNMENT
+
+
 def test_rejects_null_misaligned_and_small_workspace(L):
     d = dims()
     f = ctypes.c_void_p(1 << 20)

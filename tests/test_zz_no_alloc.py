@@ -6,9 +6,11 @@ instead of a caller workspace.
 
 Checked through the C ABI against ssd_forward on the same inputs, on two
 calls in a row (the shared scratch keeps the previous call's contents), with
-and without a caller history buffer, on both kernel families; oversized
-problems are refused before anything is launched.  This file is collected
-last on purpose.
+and without a caller history buffer, on every kernel sequence the forward
+has (single-pass tensor-core, unfused tensor-core, SIMT): the launch sequence
+is ssd_forward's, so the outputs must be bit-for-bit equal.  One case is also
+compared with the float64 oracle.  Oversized problems are refused before
+anything is launched.  This file is collected last on purpose.
 """
 import ctypes
 
@@ -17,7 +19,7 @@ import pytest
 
 from state_space_model_analytic_gb300 import synth
 
-from parity_util import TOL, rel_err, to_device
+from parity_util import TOL, rel_err, run_oracle, to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -38,14 +40,31 @@ def lib():
 
 
 CASES = [
-    synth.Dims(2, 1024, 4, 64, 128, 2, 256, "bf16"),  # tensor-core kernels
+    synth.Dims(4, 256, 32, 64, 128, 1, 256, "bf16"),   # single-pass tensor-core forward
+    synth.Dims(2, 1024, 4, 64, 128, 2, 256, "bf16"),  # unfused tensor-core kernels
     synth.Dims(1, 256, 3, 32, 48, 1, 64, "f32"),       # SIMT kernels
 ]
 
 
-@pytest.mark.parametrize("dims", CASES, ids=lambda d: f"{d.dtype}_q{d.chunk}")
+def _noalloc(nat, dims, dev, with_history, fs_like, cs_like):
+    import torch
+    cd = nat.make_dims(dims.batch, dims.seqlen, dims.nheads, dims.headdim, dims.dstate,
+                       dims.ngroups, dims.chunk, dims.dtype == "bf16")
+    stream = torch.cuda.current_stream().cuda_stream or None
+    y = torch.full_like(dev["x"], float("nan"))
+    fs = torch.full_like(fs_like, float("nan"))
+    cs = torch.full_like(cs_like, float("nan")) if with_history else None
+    rc = nat.lib().ssd_forward_noalloc(
+        cd, _ptr(dev["x"]), _ptr(dev["dt"]), _ptr(dev["A"]), _ptr(dev["B"]), _ptr(dev["C"]),
+        _ptr(dev["D"]), _ptr(dev["h0"]), _ptr(y), _ptr(fs), _ptr(cs), stream)
+    assert rc == nat.SSD_OK, nat.last_error()
+    torch.cuda.synchronize()
+    return y, fs, cs
+
+
+@pytest.mark.parametrize("dims", CASES, ids=lambda d: f"{d.dtype}_b{d.batch}_h{d.nheads}")
 @pytest.mark.parametrize("with_history", [True, False])
-def test_noalloc_forward_matches_workspace_forward(lib, dims, with_history):
+def test_noalloc_forward_equals_workspace_forward(lib, dims, with_history):
     import torch
     import state_space_model_analytic_gb300 as ssd
     nat = lib
@@ -53,25 +72,29 @@ def test_noalloc_forward_matches_workspace_forward(lib, dims, with_history):
     dev = to_device(dims, inp)
     y_ref, fs_ref, cs_ref = ssd.forward(dev["x"], dev["dt"], dev["A"], dev["B"], dev["C"],
                                         dev["D"], dev["h0"], chunk=dims.chunk)
-    cd = nat.make_dims(dims.batch, dims.seqlen, dims.nheads, dims.headdim, dims.dstate,
-                       dims.ngroups, dims.chunk, dims.dtype == "bf16")
-    stream = torch.cuda.current_stream().cuda_stream or None
+    torch.cuda.synchronize()
     for call in range(2):
-        y = torch.full_like(dev["x"], float("nan"))
-        fs = torch.full_like(fs_ref, float("nan"))
-        cs = torch.full_like(cs_ref, float("nan")) if with_history else None
-        rc = nat.lib().ssd_forward_noalloc(
-            cd, _ptr(dev["x"]), _ptr(dev["dt"]), _ptr(dev["A"]), _ptr(dev["B"]), _ptr(dev["C"]),
-            _ptr(dev["D"]), _ptr(dev["h0"]), _ptr(y), _ptr(fs), _ptr(cs), stream)
-        assert rc == nat.SSD_OK, nat.last_error()
-        torch.cuda.synchronize()
-        tol = TOL[dims.dtype]
-        pairs = [(y, y_ref), (fs, fs_ref)] + ([(cs, cs_ref)] if with_history else [])
-        for got, ref in pairs:
-            g = got.float().cpu().numpy()
-            r = ref.float().cpu().numpy()
-            assert np.isfinite(g).all(), f"call {call}"
-            assert rel_err(g, r) <= tol, f"call {call}"
+        y, fs, cs = _noalloc(nat, dims, dev, with_history, fs_ref, cs_ref)
+        assert torch.equal(y, y_ref), f"call {call}: y"
+        assert torch.equal(fs, fs_ref), f"call {call}: final state"
+        if with_history:
+            assert torch.equal(cs, cs_ref), f"call {call}: chunk states"
+
+
+def test_noalloc_forward_matches_oracle(lib):
+    nat = lib
+    dims = CASES[0]
+    inp = synth.make_inputs(dims, 7, True, "softplus")
+    dev = to_device(dims, inp)
+    ref = run_oracle(dims, inp)
+    import torch
+    fs_like = torch.empty(dims.batch, dims.nheads, dims.headdim, dims.dstate, device="cuda")
+    cs_like = torch.empty(dims.batch, dims.nchunks, dims.nheads, dims.headdim, dims.dstate,
+                          device="cuda")
+    y, fs, cs = _noalloc(nat, dims, dev, True, fs_like, cs_like)
+    for name, got in (("y", y), ("final_state", fs), ("chunk_states", cs)):
+        e = rel_err(got.float().cpu().numpy(), ref[name])
+        assert e <= TOL[dims.dtype], (name, e)
 
 
 def test_noalloc_refuses_what_does_not_fit(lib):

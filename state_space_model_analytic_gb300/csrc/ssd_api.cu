@@ -70,6 +70,12 @@ cudaError_t tc_forward_states(const Problem& p);
 cudaError_t tc_backward(const Problem& p);
 cudaError_t tc_read_and_clear_error(unsigned int* out);
 cudaError_t tc_selftest_timeout(cudaStream_t s);
+bool tc32_supported(const Problem& p);
+size_t tc32_bc_part_floats(const Problem& p);
+cudaError_t tc32_chunk_outer(const Problem& p, int mode, float* out);
+cudaError_t tc32_forward_scan(const Problem& p);
+cudaError_t tc32_backward(const Problem& p);
+cudaError_t tc32_read_and_clear_error(unsigned int* out);
 
 namespace {
 
@@ -180,7 +186,11 @@ size_t carve(Problem* p, char* base, int which) {
   const size_t items = units * (size_t)p->hpg;
   p->ntickets = (int)(1 + units);
   p->tickets = (unsigned int*)take((1 + units) * sizeof(unsigned int));
-  p->bwd_part = (float*)take((items < kBwdMaxCtas ? items : kBwdMaxCtas) * 2 * 32768 * sizeof(float));
+  // (the fp32 tensor-core backward keeps its per-segment dC, dB partials there)
+  size_t part_floats = (items < kBwdMaxCtas ? items : kBwdMaxCtas) * 2 * 32768;
+  if (tc32_supported(*p) && tc32_bc_part_floats(*p) > part_floats)
+    part_floats = tc32_bc_part_floats(*p);
+  p->bwd_part = (float*)take(part_floats * sizeof(float));
   p->hT = take(states / 2);  // bf16 copies for the tensor-core backward
   p->gT = take(states / 2);
   if (which == 2) p->hist = (float*)take(states);
@@ -299,11 +309,13 @@ int ssd_force_kernel_path(int path) {
 
 int ssd_device_status(void) {
   g_err.clear();
-  unsigned int flag = 0, conv_flag = 0;
+  unsigned int flag = 0, conv_flag = 0, tc32_flag = 0;
   cudaError_t e = tc_read_and_clear_error(&flag);
   if (e == cudaSuccess) e = conv_read_and_clear_error(&conv_flag);
+  if (e == cudaSuccess) e = tc32_read_and_clear_error(&tc32_flag);
   if (e != cudaSuccess) return cuda_fail(e, "ssd_device_status");
   flag |= conv_flag << 8;
+  flag |= tc32_flag << 16;
   if (flag) return fail(SSD_ERR_DEVICE_TIMEOUT, "a device-side wait gave up (flag 0x%x)", flag);
   return SSD_OK;
 }
@@ -318,7 +330,7 @@ int ssd_selftest_wait_timeout(void* cuda_stream) {
 int ssd_kernel_path(const ssd_dims* dims) {
   if (validate(dims) != SSD_OK) return -1;
   Problem p = base_problem(dims);
-  return tc_supported(p) ? 1 : 0;
+  return (tc_supported(p) || tc32_supported(p)) ? 1 : 0;
 }
 
 // The raw-dt mode of the fused tensor-core path (ssd_forward_raw /
@@ -370,6 +382,15 @@ int forward_impl(const ssd_dims* dims, const void* x, const float* dt, const flo
     // one kernel: chunk states, the state pass (look-back) and y
     e = tc_forward_single(p);
     if (e != cudaSuccess) return cuda_fail(e, "single-pass forward kernel");
+    return SSD_OK;
+  }
+  if (tc32_supported(p)) {  // fp32 storage on tensor cores (split bf16 products)
+    e = tc32_chunk_outer(p, 0, p.hist);
+    if (e != cudaSuccess) return cuda_fail(e, "forward chunk-state kernel");
+    e = simt_state_pass_fwd(p, p.hist, p.cs_last);
+    if (e != cudaSuccess) return cuda_fail(e, "forward state-pass kernel");
+    e = tc32_forward_scan(p);
+    if (e != cudaSuccess) return cuda_fail(e, "forward chunk-scan kernel");
     return SSD_OK;
   }
   p.hT = nullptr;  // the scan converts the fp32 history itself
@@ -438,13 +459,17 @@ int backward_impl(const ssd_dims* dims, const void* x, const float* dt, const fl
       e = tc_forward_states(f);
       if (e != cudaSuccess) return cuda_fail(e, "backward recompute state-scan kernel");
     } else {
-      e = tc_supported(f) ? tc_chunk_outer(f, 0, f.hist) : simt_forward_states(f, f.hist, f.cs_last);
+      e = tc_supported(f)     ? tc_chunk_outer(f, 0, f.hist)
+          : tc32_supported(f) ? tc32_chunk_outer(f, 0, f.hist)
+                              : simt_forward_states(f, f.hist, f.cs_last);
       if (e != cudaSuccess) return cuda_fail(e, "backward recompute chunk-state kernel");
       e = simt_state_pass_fwd(f, f.hist, f.cs_last);
       if (e != cudaSuccess) return cuda_fail(e, "backward recompute state-pass kernel");
     }
   }
-  e = tc_backward_supported(p) ? tc_backward(p) : simt_backward(p);
+  e = tc_backward_supported(p) ? tc_backward(p)
+      : tc32_supported(p)       ? tc32_backward(p)
+                                : simt_backward(p);
   if (e != cudaSuccess) return cuda_fail(e, "backward kernels");
   return SSD_OK;
 }

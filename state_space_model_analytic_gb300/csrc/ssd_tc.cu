@@ -2059,6 +2059,8 @@ bool tc_supported(const Problem& p) {
 
 void tc_force_path(int path) { g_force_path = path; }
 
+bool tc_forced_simt() { return g_force_path == 0; }
+
 bool tc_backward_supported(const Problem& p) { return tc_supported(p); }
 
 // S_c (mode 0, from x and B) or R_c (mode 1, from dy and C) into `out`; cs_last.

@@ -1,0 +1,974 @@
+// Tensor-core (tcgen05 / TMEM) kernels of the chunked SSD core for fp32
+// storage: headdim P = 64, d_state N = 64, chunk Q = 128.
+//
+// Split products.  Every fp32 operand a is carried as two bf16 tiles,
+//     hi = bf16(a),  lo = bf16(a - hi),
+// so a = hi + lo + r with |r| <= 2^-18 |a|, and every product as three bf16
+// MMAs accumulated in fp32 TMEM:
+//     A B ~ Ah Bh + Ah Bl + Al Bh,
+// dropping Al Bl and the remainders (each at most about 2^-18 |A||B| per
+// term).  The layouts are those of the bf16 kernels (128-byte swizzled rows
+// of 64 bf16).  Inputs come from global memory by coalesced 16-byte loads and
+// are split by the threads; elementwise math (decays, masks, epilogues) runs
+// in fp32 from the exact fp32 inputs.
+//
+// The chunked algebra is that of the SIMT kernels (ssd_simt.cu), derived from
+// the recurrence of `ssd_forward_state_history_reference` and the reverse-time
+// adjoint of `ssd_backward_reference` (burn_dragon_kernel 0.5.0,
+// src/sequence/mamba2/backward.rs).  Kernels:
+//   k_outer32<0>  S_c = sum_j exp(cs_last - cs_j) dt_j x_j B_j^T       (b, c, h)
+//   k_outer32<1>  R_c = sum_i exp(cs_i) dy_i C_i^T                      (b, c, h)
+//   k_scan32      y_i = sum_{j<=i} exp(cs_i-cs_j) dt_j (C_i.B_j) x_j
+//                       + exp(cs_i) H_{c-1} C_i + D x_i                 (b, c, h)
+//   k_bwd32_x     dx, d(dt), and the per-(b, c) partials of dA, dD      (b, c, h)
+//   k_bwd32_bc    dC, dB of a (b, c, g) unit over a segment of its heads:
+//                 W = sum_h exp(cs_i-cs_j) dt_j (dy_i.x_j) (summed over the
+//                 segment's heads in registers), then W B, W^T C, plus the
+//                 state terms sum_h (e o dY) H and sum_h (f o X) g
+//   k_sum32_bc    the segments' dC, dB partials summed in segment order
+// The state passes between them are the SIMT ones (fp32, sequential over
+// chunks).  Every wait is bounded; a wait that gives up sets a device error
+// word and the kernel finishes without touching the guarded data.
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include "ssd_common.cuh"
+#include "ssd_internal.h"
+#include "tc_util.cuh"
+
+namespace ssd {
+
+using namespace tc;
+
+bool tc_forced_simt();
+
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
+constexpr int kQ = 128, kP = 64, kN = 64;
+
+__device__ unsigned int g_tc32_error;
+
+__device__ __forceinline__ bool wait_all(uint64_t* bar, uint32_t parity) {
+  const bool mine = mbar_wait(bar, parity, kWaitLimitNs);
+  const bool all = __syncthreads_and(mine) != 0;
+  if (!all && threadIdx.x == 0) atomicOr(&g_tc32_error, 1u);
+  return all;
+}
+
+struct D32 {
+  int B, T, H, G, nc, hpg;
+};
+
+// ---- split tiles ----------------------------------------------------------
+// 8 consecutive values of one tile row as (hi, lo) bf16 chunks at byte offset
+// `off` of the hi and lo tiles.
+__device__ __forceinline__ void store_split8(uint8_t* hi, uint8_t* lo, uint32_t off,
+                                             const float* v) {
+  uint32_t h[4], l[4];
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    const __nv_bfloat16 a = __float2bfloat16_rn(v[2 * t]);
+    const __nv_bfloat16 b = __float2bfloat16_rn(v[2 * t + 1]);
+    h[t] = pack_bf16(__bfloat162float(a), __bfloat162float(b));
+    l[t] = pack_bf16(v[2 * t] - __bfloat162float(a), v[2 * t + 1] - __bfloat162float(b));
+  }
+  *(uint4*)(hi + off) = make_uint4(h[0], h[1], h[2], h[3]);
+  *(uint4*)(lo + off) = make_uint4(l[0], l[1], l[2], l[3]);
+}
+
+// ROWS rows of 64 fp32 (row r at src + r * stride) into split tiles (rows of
+// 64 bf16, SW128), each value times scale(r).  All loads of a thread are
+// issued before its first store.
+template <int NT, int ROWS, typename F>
+__device__ __forceinline__ void load_split(uint8_t* hi, uint8_t* lo, const float* __restrict__ src,
+                                           size_t stride, F&& scale) {
+  constexpr int kPer = ROWS * 8 / NT;
+  float4 v[kPer][2];
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) {
+    const int e = threadIdx.x + NT * k, r = e >> 3, ch = e & 7;
+    const float4* s = (const float4*)(src + (size_t)r * stride + ch * 8);
+    v[k][0] = __ldg(s);
+    v[k][1] = __ldg(s + 1);
+  }
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) {
+    const int e = threadIdx.x + NT * k, r = e >> 3, ch = e & 7;
+    const float sc = scale(r);
+    const float f[8] = {v[k][0].x * sc, v[k][0].y * sc, v[k][0].z * sc, v[k][0].w * sc,
+                        v[k][1].x * sc, v[k][1].y * sc, v[k][1].z * sc, v[k][1].w * sc};
+    store_split8(hi, lo, sw128(r, ch), f);
+  }
+}
+
+// A [64 p][64 n] fp32 state block (p-major) transposed into split tiles of
+// rows n with 64 p each; returns this thread's share of sum(src * other) when
+// `other` is given (the same elements of a second block, for <g, H>).
+template <int NT>
+__device__ __forceinline__ float load_split_transposed(uint8_t* hi, uint8_t* lo,
+                                                       const float* __restrict__ src,
+                                                       const float* __restrict__ other) {
+  constexpr int kPer = 64 * 8 / NT;
+  float dot = 0.f;
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) {
+    const int e = threadIdx.x + NT * k, n = e & 63, pc = e >> 6;
+    float f[8];
+#pragma unroll
+    for (int t = 0; t < 8; ++t) f[t] = __ldg(src + (size_t)(pc * 8 + t) * kN + n);
+    if (other) {
+#pragma unroll
+      for (int t = 0; t < 8; ++t) dot = fmaf(f[t], __ldg(other + (size_t)(pc * 8 + t) * kN + n), dot);
+    }
+    store_split8(hi, lo, sw128(n, pc), f);
+  }
+  return dot;
+}
+
+// D (+)= A B as three bf16 MMAs over the split tiles (lo tiles at the given
+// byte distance from the hi tiles).
+__device__ __forceinline__ void mma3(uint32_t d, uint32_t a_hi, uint32_t a_lo_off, uint32_t a_lbo,
+                                     bool a_mn, uint32_t b_hi, uint32_t b_lo_off, uint32_t b_lbo,
+                                     uint32_t idesc, uint32_t acc) {
+  (void)a_mn;
+  const uint64_t ah = desc_sw128(a_hi, a_lbo, 1024), al = desc_sw128(a_hi + a_lo_off, a_lbo, 1024);
+  const uint64_t bh = desc_sw128(b_hi, b_lbo, 1024), bl = desc_sw128(b_hi + b_lo_off, b_lbo, 1024);
+  mma_bf16(d, ah, bh, idesc, acc);
+  mma_bf16(d, ah, bl, idesc, 1u);
+  mma_bf16(d, al, bh, idesc, 1u);
+}
+
+// chunk-local inclusive cumsum of dt * A (log2 units) for the block's first
+// 128 threads; s_cs2, s_dt filled, ends synced
+__device__ __forceinline__ void chunk_tables(const D32& d, const float* __restrict__ dt, float a2,
+                                             int b, int c, int h, float* s_cs2, float* s_dt,
+                                             float* scratch) {
+  const int tid = threadIdx.x;
+  const float dv = tid < kQ ? dt[((size_t)b * d.T + (size_t)c * kQ + tid) * d.H + h] : 0.f;
+  const float cs = block_inclusive_scan(dv * a2, scratch);
+  if (tid < kQ) {
+    s_cs2[tid] = cs;
+    s_dt[tid] = dv;
+  }
+  __syncthreads();
+}
+
+// ---------------------------------------------------------------------------
+// Chunk outer products, one CTA per (b, c, h), 256 threads.
+//   MODE 0: out = S_c  from u = x,  v = B, w_j = exp(cs_last - cs_j) dt_j
+//   MODE 1: out = R_c  from u = dy, v = C, w_i = exp(cs_i)
+// as D[n][p] = V^T (w o U) (M = n padded to 128: the second half of the A
+// operand reads the U tiles and its rows are never read back), then written
+// out[b][c][h][p][n]; also cs_last[b][h][c] (natural-log units).
+template <int MODE>
+__global__ void __launch_bounds__(256) k_outer32(D32 d, const float* __restrict__ U,
+                                                 const float* __restrict__ V,
+                                                 const float* __restrict__ dt,
+                                                 const float* __restrict__ A,
+                                                 float* __restrict__ out,
+                                                 float* __restrict__ cs_last) {
+  extern __shared__ __align__(1024) uint8_t smraw[];
+  uint8_t* sm = align1024(smraw);
+  uint8_t* sVh = sm;           // [128 rows j][64 n]
+  uint8_t* sVl = sm + 16384;
+  uint8_t* sUh = sm + 32768;   // [128 rows j][64 p], rows scaled by w
+  uint8_t* sUl = sm + 49152;
+  __shared__ float s_cs2[kQ], s_dt[kQ], s_w[kQ], scratch[8];
+  __shared__ uint64_t bar;
+  __shared__ uint32_t tmem_base;
+  const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z, tid = threadIdx.x;
+  const int g = h / d.hpg;
+  if (tid == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  if (tid < 32) {
+    tmem_alloc(&tmem_base, 64);
+    tmem_relinquish();
+  }
+  chunk_tables(d, dt, A[h] * kLog2e, b, c, h, s_cs2, s_dt, scratch);
+  const float last2 = s_cs2[kQ - 1];
+  if (tid < kQ) s_w[tid] = MODE == 0 ? exp2f(last2 - s_cs2[tid]) * s_dt[tid] : exp2f(s_cs2[tid]);
+  if (tid == 0) cs_last[((size_t)b * d.H + h) * d.nc + c] = last2 * (1.0f / kLog2e);
+  __syncthreads();
+  const size_t row0 = (size_t)b * d.T + (size_t)c * kQ;
+  load_split<256, kQ>(sVh, sVl, V + (row0 * d.G + g) * kN, (size_t)d.G * kN,
+                      [](int) { return 1.f; });
+  load_split<256, kQ>(sUh, sUl, U + (row0 * d.H + h) * kP, (size_t)d.H * kP,
+                      [&](int r) { return s_w[r]; });
+  fence_async_smem();
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  const uint32_t tm = tmem_base;
+  if (tid == 0) {
+    const uint32_t id = idesc_bf16(128, 64, true, true);
+    for (int ks = 0; ks < kQ / 16; ++ks)
+      mma3(tm, smem_u32(sVh) + ks * 2048, 16384, 32768, true, smem_u32(sUh) + ks * 2048, 16384,
+           16384, id, ks > 0);
+    mma_commit(&bar);
+  }
+  const bool ok = wait_all(&bar, 0);
+  fence_after_sync();
+  const int wg = tid >> 7, r = tid & 127;
+  if (ok && r < 64) {  // warps 0, 1, 4, 5: lanes (rows n) 0-63; warpgroup wg takes p in [32 wg, +32)
+    float v[32];
+    tmem_ld32(tm + ((uint32_t)((r >> 5) * 32) << 16) + wg * 32, v);
+    tmem_wait_ld();
+    float* dst = out + (((size_t)b * d.nc + c) * d.H + h) * (kP * kN) + r;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) dst[(size_t)(wg * 32 + i) * kN] = v[i];
+  }
+  fence_before_sync();
+  __syncthreads();
+  if (tid < 32) tmem_dealloc(tm, 64);
+}
+
+// ---------------------------------------------------------------------------
+// Chunk scan: y of one (b, c, h) per CTA, 256 threads.
+//   CB = C B^T, Ys = C H^T (H = H_{c-1} from the history, as rows n),
+//   M = CB o L o dt (masked, split), Y = M X,
+//   y = Y + exp(cs_i) Ys + D x.
+// Decay masks as in the bf16 kernels: for warp q's rows and a 32-column chunk
+// left of its diagonal chunk, exp(cs_i - cs_j) = exp(cs_i - cs_r) exp(cs_r -
+// cs_j) with r = 32 q (both factors <= 1); the diagonal chunk evaluates the
+// exponent only where j <= i.
+constexpr uint32_t kS32Bytes = 114688;  // C, B (later M) 64K | X 32K | H 16K
+
+__global__ void __launch_bounds__(256, 1) k_scan32(D32 d, const float* __restrict__ x,
+                                                   const float* __restrict__ dt,
+                                                   const float* __restrict__ A,
+                                                   const float* __restrict__ Bm,
+                                                   const float* __restrict__ Cm,
+                                                   const float* __restrict__ D,
+                                                   const float* __restrict__ hist,
+                                                   float* __restrict__ y) {
+  extern __shared__ __align__(1024) uint8_t smraw[];
+  uint8_t* sm = align1024(smraw);
+  uint8_t* sCh = sm;            // [128 rows i][64 n] K-major
+  uint8_t* sCl = sm + 16384;
+  uint8_t* sBh = sm + 32768;    // [128 rows j][64 n] K-major
+  uint8_t* sBl = sm + 49152;
+  uint8_t* sMh = sm;            // M [128 rows i][128 j]: two 64-column tiles (after CB, Ys)
+  uint8_t* sMl = sm + 32768;
+  uint8_t* sXh = sm + 65536;    // [128 rows j][64 p] MN-major B operand
+  uint8_t* sXl = sm + 81920;
+  uint8_t* sHh = sm + 98304;    // [64 rows n][64 p] MN-major B operand
+  uint8_t* sHl = sm + 106496;
+  __shared__ float s_cs2[kQ], s_dt[kQ], scratch[8];
+  __shared__ __align__(16) float s_E[4][kQ];  // exp(cs_r - cs_j) dt_j, j < r = 32 w
+  __shared__ uint64_t bar;
+  __shared__ uint32_t tmem_base;
+  const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z, tid = threadIdx.x;
+  const int g = h / d.hpg, wg = tid >> 7, q = (tid >> 5) & 3, row = tid & 127;
+  const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+  if (tid == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  if (tid < 32) {
+    tmem_alloc(&tmem_base, 256);
+    tmem_relinquish();
+  }
+  chunk_tables(d, dt, A[h] * kLog2e, b, c, h, s_cs2, s_dt, scratch);
+  for (int e = tid; e < 4 * kQ; e += 256) {
+    const int w = e >> 7, j = e & 127, r = 32 * w;
+    s_E[w][j] = j < r ? exp2f(s_cs2[r] - s_cs2[j]) * s_dt[j] : 0.f;
+  }
+  const size_t row0 = (size_t)b * d.T + (size_t)c * kQ;
+  const auto one = [](int) { return 1.f; };
+  load_split<256, kQ>(sCh, sCl, Cm + (row0 * d.G + g) * kN, (size_t)d.G * kN, one);
+  load_split<256, kQ>(sBh, sBl, Bm + (row0 * d.G + g) * kN, (size_t)d.G * kN, one);
+  load_split<256, kQ>(sXh, sXl, x + (row0 * d.H + h) * kP, (size_t)d.H * kP, one);
+  (void)load_split_transposed<256>(sHh, sHl, hist + (((size_t)b * d.nc + c) * d.H + h) * (kP * kN),
+                                   nullptr);
+  fence_async_smem();
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  const uint32_t tm = tmem_base, tCB = tm, tYs = tm + 128, tY = tm + 192;
+  if (tid == 0) {
+    const uint32_t id_cb = idesc_bf16(128, 128, false, false);
+    const uint32_t id_ys = idesc_bf16(128, 64, false, true);
+    for (int kk = 0; kk < 4; ++kk) {
+      mma3(tCB, smem_u32(sCh) + kk * 32, 16384, 16, false, smem_u32(sBh) + kk * 32, 16384, 16,
+           id_cb, kk > 0);
+      mma3(tYs, smem_u32(sCh) + kk * 32, 16384, 16, false, smem_u32(sHh) + kk * 2048, 8192, 8192,
+           id_ys, kk > 0);
+    }
+    mma_commit(&bar);
+  }
+  bool ok = wait_all(&bar, 0);
+  fence_after_sync();
+  if (ok) {
+    // M = CB o L o dt; warpgroup wg writes columns [64 wg, 64 wg + 64)
+    const int I = row;
+    const float fi = exp2f(s_cs2[I] - s_cs2[32 * q]), csI = s_cs2[I];
+#pragma unroll 1
+    for (int u = 0; u < 2; ++u) {
+      const int jc = 2 * wg + u;
+      float v[32];
+      if (jc <= q) {  // warp-uniform
+        tmem_ld32(tCB + lane_base + jc * 32, v);
+        tmem_wait_ld();
+        if (jc < q) {
+#pragma unroll
+          for (int k = 0; k < 32; ++k) v[k] *= fi * s_E[q][jc * 32 + k];
+        } else {
+#pragma unroll
+          for (int k = 0; k < 32; ++k) {
+            const int J = jc * 32 + k;
+            v[k] *= J <= I ? exp2f(csI - s_cs2[J]) * s_dt[J] : 0.f;
+          }
+        }
+      } else {
+#pragma unroll
+        for (int k = 0; k < 32; ++k) v[k] = 0.f;
+      }
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        const int j = jc * 32 + q4 * 8;
+        store_split8(sMh + (j >> 6) * 16384, sMl + (j >> 6) * 16384, sw128(row, (j & 63) >> 3),
+                     &v[q4 * 8]);
+      }
+    }
+  }
+  fence_async_smem();
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  if (tid == 0 && ok) {
+    const uint32_t id_y = idesc_bf16(128, 64, false, true);
+    for (int kk = 0; kk < 8; ++kk)
+      mma3(tY, smem_u32(sMh) + (kk >> 2) * 16384 + (kk & 3) * 32, 32768, 16, false,
+           smem_u32(sXh) + kk * 2048, 16384, 16384, id_y, kk > 0);
+    mma_commit(&bar);
+  }
+  ok = ok && wait_all(&bar, 1);
+  fence_after_sync();
+  if (ok) {
+    // y = Y + exp(cs_i) Ys + D x; warpgroup wg takes p in [32 wg, 32 wg + 32)
+    const float sc = exp2f(s_cs2[row]), Dh = D[h];
+    const size_t off = ((row0 + row) * d.H + h) * kP + wg * 32;
+    const float4* xs = (const float4*)(x + off);
+    float4* ys = (float4*)(y + off);
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      float yv[16], yst[16];
+      tmem_ld16(tY + lane_base + wg * 32 + half * 16, yv);
+      tmem_ld16(tYs + lane_base + wg * 32 + half * 16, yst);
+      tmem_wait_ld();
+#pragma unroll
+      for (int k4 = 0; k4 < 4; ++k4) {
+        const float4 xv = __ldg(xs + half * 4 + k4);
+        const int m = 4 * k4;
+        float4 o;
+        o.x = fmaf(sc, yst[m + 0], yv[m + 0]) + Dh * xv.x;
+        o.y = fmaf(sc, yst[m + 1], yv[m + 1]) + Dh * xv.y;
+        o.z = fmaf(sc, yst[m + 2], yv[m + 2]) + Dh * xv.z;
+        o.w = fmaf(sc, yst[m + 3], yv[m + 3]) + Dh * xv.w;
+        ys[half * 4 + k4] = o;
+      }
+    }
+  }
+  fence_before_sync();
+  __syncthreads();
+  if (tid < 32) tmem_dealloc(tm, 256);
+}
+
+// ---------------------------------------------------------------------------
+// Column sums over the 32 lanes of a warp, for 16 columns: lane l returns the
+// sum over all lanes of v[l % 16].
+__device__ __forceinline__ float col_sum16(float (&v)[16]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int s = 8; s >= 1; s >>= 1) {
+    const bool upper = (lane & s) != 0;
+#pragma unroll
+    for (int k = 0; k < s; ++k) {
+      const float send = upper ? v[k] : v[k + s];
+      const float keep = upper ? v[k + s] : v[k];
+      v[k] = keep + __shfl_xor_sync(0xffffffffu, send, s);
+    }
+  }
+  return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 16);
+}
+
+// Backward, gradient w.r.t. x and dt: one (b, c, h) per CTA, 256 threads.
+//   batch A: CB = C B^T, dYX = dY X^T, Gs = B g^T, CH = C H^T
+//            (g = g_c, the state gradient at the chunk end; H = H_{c-1})
+//   build:   W = L o dt o dYX and M = W o CB (row sums and strict column
+//            sums of M, for d(cs)); O = L o CB (split) into the C/B tiles
+//   batch B: Gx = O^T dY
+//   epilogue: dx_j = D dy_j + dt_j (Gx_j + f_j Gs_j), f_j = exp(cs_last - cs_j);
+//            drive_j = x_j.(Gx_j + f_j Gs_j), e_j = f_j dt_j x_j.Gs_j,
+//            statein_i = exp(cs_i) dy_i.CH_i, and dy.x for dD
+//   dcs_i = rowsum_i - colsum_i + statein_i - e_i (+ sum_j e_j +
+//            exp(cs_last) <g, H> at i = Q - 1); da_j = sum_{i >= j} dcs_i;
+//            ddt_j = drive_j + A da_j; partials sum_j dt_j da_j and sum dy.x.
+constexpr uint32_t kBx32Bytes = 163840;  // C, B (later O) 64K | X 32K | dY 32K | H 16K | g 16K
+
+__global__ void __launch_bounds__(256, 1) k_bwd32_x(D32 d, const float* __restrict__ x,
+                                                    const float* __restrict__ dt,
+                                                    const float* __restrict__ A,
+                                                    const float* __restrict__ Bm,
+                                                    const float* __restrict__ Cm,
+                                                    const float* __restrict__ D,
+                                                    const float* __restrict__ dy,
+                                                    const float* __restrict__ hist,
+                                                    const float* __restrict__ gstate,
+                                                    float* __restrict__ dx, float* __restrict__ ddt,
+                                                    float* __restrict__ dA_part,
+                                                    float* __restrict__ dD_part) {
+  extern __shared__ __align__(1024) uint8_t smraw[];
+  uint8_t* sm = align1024(smraw);
+  uint8_t* sCh = sm;            // [128 rows i][64 n] K-major
+  uint8_t* sCl = sm + 16384;
+  uint8_t* sBh = sm + 32768;    // [128 rows j][64 n] K-major
+  uint8_t* sBl = sm + 49152;
+  uint8_t* sOh = sm;            // O [128 rows i][128 j] (two 64-column tiles), after batch A
+  uint8_t* sOl = sm + 32768;
+  uint8_t* sXh = sm + 65536;    // [128 rows j][64 p]
+  uint8_t* sXl = sm + 81920;
+  uint8_t* sYh = sm + 98304;    // dY [128 rows i][64 p]
+  uint8_t* sYl = sm + 114688;
+  uint8_t* sHh = sm + 131072;   // H^T [64 rows n][64 p]
+  uint8_t* sHl = sm + 139264;
+  uint8_t* sGh = sm + 147456;   // g^T [64 rows n][64 p]
+  uint8_t* sGl = sm + 155648;
+  __shared__ float s_cs2[kQ], s_dt[kQ], scratch[8];
+  __shared__ __align__(16) float s_E[4][kQ];    // exp(cs_r - cs_j), j < r = 32 w
+  __shared__ __align__(16) float s_Edt[4][kQ];  // the same times dt_j
+  __shared__ float s_col[4][kQ];                // per-warp strict column sums of M
+  __shared__ float s_red[5][kQ];                // warpgroup 1's row partials
+  __shared__ float s_v[kQ];
+  __shared__ float2 s_v2[kQ], scratch2[8];
+  __shared__ float s_esum;
+  __shared__ uint64_t bar;
+  __shared__ uint32_t tmem_base;
+  const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z, tid = threadIdx.x;
+  const int g = h / d.hpg, wg = tid >> 7, q = (tid >> 5) & 3, row = tid & 127, lane = tid & 31;
+  const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+  if (tid == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  if (tid < 32) {
+    tmem_alloc(&tmem_base, 512);
+    tmem_relinquish();
+  }
+  const float Ah = A[h], Dh = D[h];
+  chunk_tables(d, dt, Ah * kLog2e, b, c, h, s_cs2, s_dt, scratch);
+  for (int e = tid; e < 4 * kQ; e += 256) {
+    const int w = e >> 7, j = e & 127, r = 32 * w;
+    const float ev = j < r ? exp2f(s_cs2[r] - s_cs2[j]) : 0.f;
+    s_E[w][j] = ev;
+    s_Edt[w][j] = ev * s_dt[j];
+  }
+  const size_t row0 = (size_t)b * d.T + (size_t)c * kQ;
+  const size_t st = (((size_t)b * d.nc + c) * d.H + h) * (kP * kN);
+  const auto one = [](int) { return 1.f; };
+  load_split<256, kQ>(sCh, sCl, Cm + (row0 * d.G + g) * kN, (size_t)d.G * kN, one);
+  load_split<256, kQ>(sBh, sBl, Bm + (row0 * d.G + g) * kN, (size_t)d.G * kN, one);
+  load_split<256, kQ>(sXh, sXl, x + (row0 * d.H + h) * kP, (size_t)d.H * kP, one);
+  load_split<256, kQ>(sYh, sYl, dy + (row0 * d.H + h) * kP, (size_t)d.H * kP, one);
+  (void)load_split_transposed<256>(sHh, sHl, hist + st, nullptr);
+  float hg = load_split_transposed<256>(sGh, sGl, gstate + st, hist + st);
+  hg = block_sum(hg, scratch);  // <g_c, H_{c-1}> (syncs)
+  fence_async_smem();
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  const uint32_t tm = tmem_base;
+  const uint32_t T0 = tm, T1 = tm + 128, TGs = tm + 256, TCH = tm + 320, TGx = tm + 384;
+  if (tid == 0) {
+    const uint32_t id_sq = idesc_bf16(128, 128, false, false);
+    const uint32_t id_km = idesc_bf16(128, 64, false, true);
+    for (int kk = 0; kk < 4; ++kk) {
+      mma3(T0, smem_u32(sCh) + kk * 32, 16384, 16, false, smem_u32(sBh) + kk * 32, 16384, 16,
+           id_sq, kk > 0);
+      mma3(T1, smem_u32(sYh) + kk * 32, 16384, 16, false, smem_u32(sXh) + kk * 32, 16384, 16,
+           id_sq, kk > 0);
+      mma3(TGs, smem_u32(sBh) + kk * 32, 16384, 16, false, smem_u32(sGh) + kk * 2048, 8192, 8192,
+           id_km, kk > 0);
+      mma3(TCH, smem_u32(sCh) + kk * 32, 16384, 16, false, smem_u32(sHh) + kk * 2048, 8192, 8192,
+           id_km, kk > 0);
+    }
+    mma_commit(&bar);
+  }
+  bool ok = wait_all(&bar, 0);
+  fence_after_sync();
+
+  // ---- build: W, M sums and O = L o CB; warpgroup wg covers columns
+  // [64 wg, 64 wg + 64) as two 32-column chunks
+  const int I = row;
+  const float fi = exp2f(s_cs2[I] - s_cs2[32 * q]), csI = s_cs2[I];
+  float rowsum = 0.f;
+  if (ok) {
+#pragma unroll 1
+    for (int u = 0; u < 2; ++u) {
+      const int jc = 2 * wg + u;
+      if (jc <= q) {  // warp-uniform
+#pragma unroll 1
+        for (int hf = 0; hf < 2; ++hf) {
+          const int col0 = jc * 32 + hf * 16;
+          float cb[16], xy[16];
+          tmem_ld16(T0 + lane_base + col0, cb);
+          tmem_ld16(T1 + lane_base + col0, xy);
+          tmem_wait_ld();
+          if (jc < q) {
+#pragma unroll
+            for (int m = 0; m < 16; ++m) {
+              const float wv = fi * s_Edt[q][col0 + m] * xy[m];
+              const float mm = wv * cb[m];
+              rowsum += mm;
+              xy[m] = mm;
+              cb[m] *= fi * s_E[q][col0 + m];
+            }
+          } else {
+#pragma unroll
+            for (int m = 0; m < 16; ++m) {
+              const int J = col0 + m;
+              const float L = J <= I ? exp2f(csI - s_cs2[J]) : 0.f;
+              const float wv = L * s_dt[J] * xy[m];
+              const float mm = J < I ? wv * cb[m] : 0.f;
+              rowsum += mm;
+              xy[m] = mm;
+              cb[m] *= L;
+            }
+          }
+          const float cs = col_sum16(xy);
+          if (lane < 16) s_col[q][col0 + lane] = cs;
+#pragma unroll
+          for (int q4 = 0; q4 < 2; ++q4) {
+            const int j = col0 + q4 * 8;
+            store_split8(sOh + (j >> 6) * 16384, sOl + (j >> 6) * 16384,
+                         sw128(row, (j & 63) >> 3), &cb[q4 * 8]);
+          }
+        }
+      } else {
+        const float z[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const int j = jc * 32 + q4 * 8;
+          store_split8(sOh + (j >> 6) * 16384, sOl + (j >> 6) * 16384,
+                       sw128(row, (j & 63) >> 3), z);
+        }
+      }
+    }
+  }
+  fence_async_smem();
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  if (tid == 0 && ok) {
+    // Gx = O^T dY: M = j (O as MN-major, two 64-column blocks), K = i, N = p
+    const uint32_t id = idesc_bf16(128, 64, true, true);
+    for (int kk = 0; kk < 8; ++kk)
+      mma3(TGx, smem_u32(sOh) + kk * 2048, 32768, 16384, true, smem_u32(sYh) + kk * 2048, 16384,
+           16384, id, kk > 0);
+    mma_commit(&bar);
+  }
+  ok = ok && wait_all(&bar, 1);
+  fence_after_sync();
+
+  // ---- epilogue: this thread's row (j for dx, drive, e; i for statein), p in
+  // [32 wg, 32 wg + 32)
+  const float last2 = s_cs2[kQ - 1];
+  const float fj = exp2f(last2 - s_cs2[row]), dtj = s_dt[row];
+  float drive = 0.f, ej = 0.f, stin = 0.f, dd = 0.f;
+  if (ok) {
+    const size_t off = ((row0 + row) * d.H + h) * kP + wg * 32;
+    const float4* xs = (const float4*)(x + off);
+    const float4* ys = (const float4*)(dy + off);
+    float4* dxs = (float4*)(dx + off);
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      float gx[16], gs[16], ch[16];
+      tmem_ld16(TGx + lane_base + wg * 32 + half * 16, gx);
+      tmem_ld16(TGs + lane_base + wg * 32 + half * 16, gs);
+      tmem_ld16(TCH + lane_base + wg * 32 + half * 16, ch);
+      tmem_wait_ld();
+#pragma unroll
+      for (int k4 = 0; k4 < 4; ++k4) {
+        const float4 xv = __ldg(xs + half * 4 + k4), yv = __ldg(ys + half * 4 + k4);
+        const float xa[4] = {xv.x, xv.y, xv.z, xv.w}, ya[4] = {yv.x, yv.y, yv.z, yv.w};
+        float o[4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const int m = 4 * k4 + t;
+          const float gg = fmaf(fj, gs[m], gx[m]);
+          o[t] = fmaf(dtj, gg, Dh * ya[t]);
+          drive = fmaf(xa[t], gg, drive);
+          ej = fmaf(xa[t], gs[m], ej);
+          stin = fmaf(ya[t], ch[m], stin);
+          dd = fmaf(ya[t], xa[t], dd);
+        }
+        dxs[half * 4 + k4] = make_float4(o[0], o[1], o[2], o[3]);
+      }
+    }
+  }
+  if (wg == 1) {
+    s_red[0][row] = rowsum;
+    s_red[1][row] = drive;
+    s_red[2][row] = ej;
+    s_red[3][row] = stin;
+    s_red[4][row] = dd;
+  }
+  __syncthreads();
+  if (wg == 0) {
+    rowsum += s_red[0][row];
+    drive += s_red[1][row];
+    ej = (ej + s_red[2][row]) * fj * dtj;
+    stin = (stin + s_red[3][row]) * exp2f(s_cs2[row]);
+    dd += s_red[4][row];
+    float colsum = 0.f;
+    for (int w = row >> 5; w < 4; ++w) colsum += s_col[w][row];
+    s_v2[row] = make_float2(rowsum - colsum + stin - ej, ej);
+  } else {
+    dd = 0.f;
+  }
+  __syncthreads();
+  // da_j = sum_{i >= j} dcs_i: an inclusive scan over the reversed rows
+  const float2 rv = wg == 0 ? s_v2[kQ - 1 - row] : make_float2(0.f, 0.f);
+  const float2 sc2 = block_inclusive_scan2(rv, scratch2);
+  const int Jr = kQ - 1 - row;
+  if (wg == 0) s_v[row] = drive;
+  if (tid == kQ - 1) s_esum = sc2.y;
+  __syncthreads();
+  const float da = sc2.x + s_esum + exp2f(last2) * hg;
+  if (wg == 0 && ok) ddt[(row0 + Jr) * d.H + h] = s_v[Jr] + Ah * da;
+  const float2 ad = block_sum2(make_float2(wg == 0 ? s_dt[Jr] * da : 0.f, dd), scratch2);
+  if (tid == 0 && ok) {
+    const size_t slot = ((size_t)b * d.nc + c) * d.H + h;
+    dA_part[slot] = ad.x;
+    dD_part[slot] = ad.y;
+  }
+  fence_before_sync();
+  __syncthreads();
+  if (tid < 32) tmem_dealloc(tm, 512);
+}
+
+// ---------------------------------------------------------------------------
+// Backward, gradients w.r.t. B and C: one (b, c, g) unit and a segment of its
+// heads per CTA, 512 threads.  Per head: dYX = dY X^T (TMEM), W = L o dt o dYX
+// summed over the segment's heads in registers (thread (wg, row) holds
+// columns [32 wg, 32 wg + 32) of its row); then X and dY are reloaded scaled
+// (f_j = exp(cs_last - cs_j) dt_j, e_i = exp(cs_i)) for
+//   dC += (e o dY) H,  dB += (f o X) g      (TMEM accumulators over heads).
+// After the segment: W into split tiles, dC += W B, dB += W^T C, and the fp32
+// sums of the segment written as partials [unit][segment][dC|dB][128][64].
+constexpr uint32_t kBbc32Bytes = 163840;  // B 32K | C 32K | X 32K | dY 32K | H 16K | g 16K
+
+__global__ void __launch_bounds__(512, 1) k_bwd32_bc(D32 d, int seg_heads,
+                                                     const float* __restrict__ x,
+                                                     const float* __restrict__ dt,
+                                                     const float* __restrict__ A,
+                                                     const float* __restrict__ Bm,
+                                                     const float* __restrict__ Cm,
+                                                     const float* __restrict__ dy,
+                                                     const float* __restrict__ hist,
+                                                     const float* __restrict__ gstate,
+                                                     float* __restrict__ part) {
+  extern __shared__ __align__(1024) uint8_t smraw[];
+  uint8_t* sm = align1024(smraw);
+  uint8_t* sBh = sm;            // [128 rows j][64 n] MN-major B operand
+  uint8_t* sBl = sm + 16384;
+  uint8_t* sCh = sm + 32768;    // [128 rows i][64 n]
+  uint8_t* sCl = sm + 49152;
+  uint8_t* sXh = sm + 65536;    // [128 rows j][64 p]
+  uint8_t* sXl = sm + 81920;
+  uint8_t* sYh = sm + 98304;    // dY [128 rows i][64 p]
+  uint8_t* sYl = sm + 114688;
+  uint8_t* sWh = sm + 65536;    // W [128 rows i][128 j] after the last head (X, dY region)
+  uint8_t* sWl = sm + 98304;
+  uint8_t* sHh = sm + 131072;   // H [64 rows p][64 n] MN-major B operand
+  uint8_t* sHl = sm + 139264;
+  uint8_t* sGh = sm + 147456;   // g [64 rows p][64 n]
+  uint8_t* sGl = sm + 155648;
+  __shared__ float s_cs2[kQ], s_dt[kQ], scratch[16];
+  __shared__ __align__(16) float s_E[4][kQ];  // exp(cs_r - cs_j) dt_j, j < r = 32 w
+  __shared__ uint64_t bar;
+  __shared__ uint32_t tmem_base;
+  const int seg = blockIdx.x, c = blockIdx.y, bg = blockIdx.z;
+  const int b = bg / d.G, g = bg % d.G;
+  const int tid = threadIdx.x, wg = tid >> 7, q = (tid >> 5) & 3, row = tid & 127;
+  const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+  const int h0 = g * d.hpg + seg * seg_heads;
+  const int nh = min(seg_heads, d.hpg - seg * seg_heads);
+  if (tid == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  if (tid < 32) {
+    tmem_alloc(&tmem_base, 256);
+    tmem_relinquish();
+  }
+  const size_t row0 = (size_t)b * d.T + (size_t)c * kQ;
+  const auto one = [](int) { return 1.f; };
+  load_split<512, kQ>(sBh, sBl, Bm + (row0 * d.G + g) * kN, (size_t)d.G * kN, one);
+  load_split<512, kQ>(sCh, sCl, Cm + (row0 * d.G + g) * kN, (size_t)d.G * kN, one);
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  const uint32_t tm = tmem_base, T1 = tm, TdC = tm + 128, TdB = tm + 192;
+  uint32_t phase = 0;
+  bool ok = true;
+  float wsum[32];
+#pragma unroll
+  for (int k = 0; k < 32; ++k) wsum[k] = 0.f;
+  const int I = row, jc = wg;  // this thread's row and 32-column chunk of W
+  for (int hh = 0; hh < nh && ok; ++hh) {
+    const int h = h0 + hh;
+    chunk_tables(d, dt, A[h] * kLog2e, b, c, h, s_cs2, s_dt, scratch);
+    for (int e = tid; e < 4 * kQ; e += 512) {
+      const int w = e >> 7, j = e & 127, r = 32 * w;
+      s_E[w][j] = j < r ? exp2f(s_cs2[r] - s_cs2[j]) * s_dt[j] : 0.f;
+    }
+    const size_t st = (((size_t)b * d.nc + c) * d.H + h) * (kP * kN);
+    load_split<512, kQ>(sXh, sXl, x + (row0 * d.H + h) * kP, (size_t)d.H * kP, one);
+    load_split<512, kQ>(sYh, sYl, dy + (row0 * d.H + h) * kP, (size_t)d.H * kP, one);
+    load_split<512, 64>(sHh, sHl, hist + st, (size_t)kN, one);
+    load_split<512, 64>(sGh, sGl, gstate + st, (size_t)kN, one);
+    fence_async_smem();
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    if (tid == 0) {
+      const uint32_t id = idesc_bf16(128, 128, false, false);
+      for (int kk = 0; kk < 4; ++kk)
+        mma3(T1, smem_u32(sYh) + kk * 32, 16384, 16, false, smem_u32(sXh) + kk * 32, 16384, 16,
+             id, kk > 0);
+      mma_commit(&bar);
+    }
+    ok = wait_all(&bar, phase);
+    phase ^= 1;
+    fence_after_sync();
+    if (!ok) break;
+    // W += L o dt o dYX over this thread's 32 columns
+    if (jc <= q) {  // warp-uniform
+      const float fi = exp2f(s_cs2[I] - s_cs2[32 * q]), csI = s_cs2[I];
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        const int col0 = jc * 32 + hf * 16;
+        float xy[16];
+        tmem_ld16(T1 + lane_base + col0, xy);
+        tmem_wait_ld();
+        if (jc < q) {
+#pragma unroll
+          for (int m = 0; m < 16; ++m) wsum[hf * 16 + m] = fmaf(fi * s_E[q][col0 + m], xy[m], wsum[hf * 16 + m]);
+        } else {
+#pragma unroll
+          for (int m = 0; m < 16; ++m) {
+            const int J = col0 + m;
+            const float L = J <= I ? exp2f(csI - s_cs2[J]) * s_dt[J] : 0.f;
+            wsum[hf * 16 + m] = fmaf(L, xy[m], wsum[hf * 16 + m]);
+          }
+        }
+      }
+    }
+    // X, dY reloaded scaled (the dYX product has read them)
+    const float last2 = s_cs2[kQ - 1];
+    load_split<512, kQ>(sXh, sXl, x + (row0 * d.H + h) * kP, (size_t)d.H * kP,
+                        [&](int r) { return exp2f(last2 - s_cs2[r]) * s_dt[r]; });
+    load_split<512, kQ>(sYh, sYl, dy + (row0 * d.H + h) * kP, (size_t)d.H * kP,
+                        [&](int r) { return exp2f(s_cs2[r]); });
+    fence_async_smem();
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    if (tid == 0) {
+      const uint32_t id = idesc_bf16(128, 64, false, true);
+      for (int kk = 0; kk < 4; ++kk) {
+        mma3(TdC, smem_u32(sYh) + kk * 32, 16384, 16, false, smem_u32(sHh) + kk * 2048, 8192, 8192,
+             id, hh > 0 || kk > 0);
+        mma3(TdB, smem_u32(sXh) + kk * 32, 16384, 16, false, smem_u32(sGh) + kk * 2048, 8192, 8192,
+             id, hh > 0 || kk > 0);
+      }
+      mma_commit(&bar);
+    }
+    ok = wait_all(&bar, phase);  // the tiles are rewritten by the next head
+    phase ^= 1;
+    fence_after_sync();
+  }
+  // W of the segment into split tiles (X, dY region), then dC += W B, dB += W^T C
+  if (ok) {
+#pragma unroll
+    for (int q4 = 0; q4 < 4; ++q4) {
+      const int j = jc * 32 + q4 * 8;
+      store_split8(sWh + (j >> 6) * 16384, sWl + (j >> 6) * 16384, sw128(row, (j & 63) >> 3),
+                   &wsum[q4 * 8]);
+    }
+  }
+  fence_async_smem();
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  if (tid == 0 && ok) {
+    const uint32_t id_dc = idesc_bf16(128, 64, false, true);
+    const uint32_t id_db = idesc_bf16(128, 64, true, true);
+    for (int kk = 0; kk < 8; ++kk) {
+      // dC: A = W (K-major, K = j), B = B (MN-major rows j, N = n)
+      mma3(TdC, smem_u32(sWh) + (kk >> 2) * 16384 + (kk & 3) * 32, 32768, 16, false,
+           smem_u32(sBh) + kk * 2048, 16384, 16384, id_dc, 1);
+      // dB: A = W^T (MN-major rows i = K, M = j), B = C (MN-major rows i, N = n)
+      mma3(TdB, smem_u32(sWh) + kk * 2048, 32768, 16384, true, smem_u32(sCh) + kk * 2048, 16384,
+           16384, id_db, 1);
+    }
+    mma_commit(&bar);
+  }
+  ok = ok && wait_all(&bar, phase);
+  fence_after_sync();
+  if (ok) {
+    // warpgroup wg writes columns [16 wg, 16 wg + 16) of row `row` of dC and dB
+    const size_t unit = ((size_t)b * d.nc + c) * d.G + g;
+    float* pbase = part + (unit * gridDim.x + seg) * (2 * kQ * kN);
+#pragma unroll
+    for (int which = 0; which < 2; ++which) {
+      float v[16];
+      tmem_ld16((which ? TdB : TdC) + lane_base + wg * 16, v);
+      tmem_wait_ld();
+      float4* dst = (float4*)(pbase + which * (kQ * kN) + (size_t)row * kN + wg * 16);
+#pragma unroll
+      for (int k4 = 0; k4 < 4; ++k4)
+        dst[k4] = make_float4(v[4 * k4], v[4 * k4 + 1], v[4 * k4 + 2], v[4 * k4 + 3]);
+    }
+  }
+  fence_before_sync();
+  __syncthreads();
+  if (tid < 32) tmem_dealloc(tm, 256);
+}
+
+// dC, dB of every unit: the segments' partials summed in segment order.
+__global__ void __launch_bounds__(256) k_sum32_bc(D32 d, int nseg, const float* __restrict__ part,
+                                                  float* __restrict__ dB, float* __restrict__ dC) {
+  const size_t unit = blockIdx.x;  // ((b * nc + c) * G + g)
+  const int g = (int)(unit % d.G), c = (int)((unit / d.G) % d.nc), b = (int)(unit / ((size_t)d.G * d.nc));
+  const float* base = part + unit * nseg * (2 * kQ * kN);
+  for (int e = threadIdx.x; e < 2 * kQ * kN / 4; e += blockDim.x) {
+    const int which = e / (kQ * kN / 4), r = (e % (kQ * kN / 4)) / (kN / 4), n4 = e % (kN / 4);
+    float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int k = 0; k < nseg; ++k) {
+      const float4 v = ((const float4*)(base + (size_t)k * (2 * kQ * kN) + which * (kQ * kN) +
+                                        (size_t)r * kN))[n4];
+      s.x += v.x;
+      s.y += v.y;
+      s.z += v.z;
+      s.w += v.w;
+    }
+    float* out = which ? dB : dC;
+    ((float4*)(out + (((size_t)b * d.T + (size_t)c * kQ + r) * d.G + g) * kN))[n4] = s;
+  }
+}
+
+D32 d32_of(const Problem& p) { return D32{p.B, p.T, p.H, p.G, p.nc, p.hpg}; }
+
+template <typename K>
+cudaError_t set_smem32(K kernel, size_t bytes) {
+  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+}
+
+}  // namespace
+
+// fp32 storage, headdim 64, d_state 64, chunk 128.
+bool tc32_supported(const Problem& p) {
+  if (tc_forced_simt()) return false;
+  return !p.bf16 && p.P == kP && p.N == kN && p.Q == kQ;
+}
+
+// Heads per segment of the dB, dC kernel: enough segments that the units
+// times their segments make about kBcTargetCtas CTAs (two per SM of a GB300).
+// The split sets the order of the dB, dC sums, so it does not depend on the
+// device: results and workspace sizes are the same on every GPU.
+constexpr long long kBcTargetCtas = 304;
+
+int tc32_seg_heads(const Problem& p) {
+  const long long units = (long long)p.B * p.nc * p.G;
+  long long nseg = (kBcTargetCtas + units - 1) / units;
+  if (nseg < 1) nseg = 1;
+  if (nseg > p.hpg) nseg = p.hpg;
+  return (int)((p.hpg + nseg - 1) / nseg);
+}
+
+size_t tc32_bc_part_floats(const Problem& p) {
+  const int sh = tc32_seg_heads(p);
+  const long long nseg = (p.hpg + sh - 1) / sh;
+  return (size_t)p.B * p.nc * p.G * nseg * 2 * kQ * kN;
+}
+
+cudaError_t tc32_chunk_outer(const Problem& p, int mode, float* out) {
+  const size_t smem = 65536 + 1024;
+  cudaError_t e;
+  if (mode == 0) {
+    if ((e = set_smem32(k_outer32<0>, smem)) != cudaSuccess) return e;
+    LaunchScope ls("chunk_state_tc32", p.stream);
+    k_outer32<0><<<dim3(p.nc, p.H, p.B), 256, smem, p.stream>>>(
+        d32_of(p), (const float*)p.x, (const float*)p.Bm, p.dt, p.A, out, p.cs_last);
+  } else {
+    if ((e = set_smem32(k_outer32<1>, smem)) != cudaSuccess) return e;
+    LaunchScope ls("chunk_dstate_tc32", p.stream);
+    k_outer32<1><<<dim3(p.nc, p.H, p.B), 256, smem, p.stream>>>(
+        d32_of(p), (const float*)p.dy, (const float*)p.Cm, p.dt, p.A, out, p.cs_last);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t tc32_forward_scan(const Problem& p) {
+  const size_t smem = kS32Bytes + 1024;
+  cudaError_t e = set_smem32(k_scan32, smem);
+  if (e != cudaSuccess) return e;
+  {
+    LaunchScope ls("chunk_scan_tc32", p.stream);
+    k_scan32<<<dim3(p.nc, p.H, p.B), 256, smem, p.stream>>>(
+        d32_of(p), (const float*)p.x, p.dt, p.A, (const float*)p.Bm, (const float*)p.Cm, p.D,
+        p.hist, (float*)p.y);
+  }
+  return cudaGetLastError();
+}
+
+// R_c, the reverse state pass (g_c in place, dh0), the dx / d(dt) kernel, the
+// dB / dC kernel and its segment sums, and the dA, dD reduction.
+cudaError_t tc32_backward(const Problem& p) {
+  cudaError_t e;
+  if ((e = tc32_chunk_outer(p, 1, p.dstate)) != cudaSuccess) return e;
+  if ((e = simt_state_pass_bwd(p)) != cudaSuccess) return e;
+  const D32 d = d32_of(p);
+  {
+    const size_t smem = kBx32Bytes + 1024;
+    if ((e = set_smem32(k_bwd32_x, smem)) != cudaSuccess) return e;
+    LaunchScope ls("bwd_x_tc32", p.stream);
+    k_bwd32_x<<<dim3(p.nc, p.H, p.B), 256, smem, p.stream>>>(
+        d, (const float*)p.x, p.dt, p.A, (const float*)p.Bm, (const float*)p.Cm, p.D,
+        (const float*)p.dy, p.hist, p.dstate, (float*)p.dx, p.ddt, p.dA_part, p.dD_part);
+  }
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  const int sh = tc32_seg_heads(p);
+  const int nseg = (p.hpg + sh - 1) / sh;
+  {
+    const size_t smem = kBbc32Bytes + 1024;
+    if ((e = set_smem32(k_bwd32_bc, smem)) != cudaSuccess) return e;
+    LaunchScope ls("bwd_bc_tc32", p.stream);
+    k_bwd32_bc<<<dim3(nseg, p.nc, p.B * p.G), 512, smem, p.stream>>>(
+        d, sh, (const float*)p.x, p.dt, p.A, (const float*)p.Bm, (const float*)p.Cm,
+        (const float*)p.dy, p.hist, p.dstate, p.bwd_part);
+  }
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  {
+    LaunchScope ls("sum_bc_tc32", p.stream);
+    k_sum32_bc<<<(unsigned)((size_t)p.B * p.nc * p.G), 256, 0, p.stream>>>(
+        d, nseg, p.bwd_part, (float*)p.dB, (float*)p.dC);
+  }
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  return simt_reduce_heads(p, p.B * p.nc, p.B * p.nc);
+}
+
+cudaError_t tc32_read_and_clear_error(unsigned int* out) {
+  cudaError_t e = cudaMemcpyFromSymbol(out, g_tc32_error, sizeof(unsigned int));
+  if (e != cudaSuccess) return e;
+  const unsigned int zero = 0;
+  return cudaMemcpyToSymbol(g_tc32_error, &zero, sizeof(unsigned int));
+}
+
+}  // namespace ssd

@@ -758,6 +758,51 @@ def main():
             return sum(a.elapsed_time(b) for a, b in evn) / n
 
         f_ms, b_ms = timed(nfwd), timed(nbwd)
+
+        # What fusing the norm into the core could save at most: the norm
+        # forward run right after the core's forward, reading the y that the
+        # core has just written (still in L2), and the core's backward run
+        # right after the norm backward, reading the dy that it has just
+        # written; each against the same call after an L2 flush.
+        y_core = fwd_out["y"]
+
+        def nfwd_core():
+            nat.check(nat.lib().ssd_rmsnorm_gated_forward(
+                rows_, width_, dtc, p_(y_core), p_(nz), p_(nw), 1e-5, p_(n_out), p_(n_inv),
+                stream.cuda_stream or None))
+
+        def core_fwd():
+            ssd.forward(t_in["x"], t_in["dt"], t_in["A"], t_in["B"], t_in["C"], t_in["D"],
+                        t_in["h0"], chunk=Q, out=fwd_out, workspace=ws_f)
+
+        def core_bwd_on_norm_dy():
+            ssd.backward(t_in["x"], t_in["dt"], t_in["A"], t_in["B"], t_in["C"], t_in["D"],
+                         t_in["h0"], n_gr["dy"].view_as(t_in["x"]), fwd_out["chunk_states"],
+                         chunk=Q, out=bwd_out, workspace=ws_b)
+
+        def after(pre, fn, n=max(1, args.next_iters)):
+            for _ in range(args.warmup):
+                flush.fill_(1.0)
+                pre()
+                fn()
+            torch.cuda.synchronize()
+            evn = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(n)]
+            for i in range(n):
+                flush.fill_(float(i))
+                if pre is not None:
+                    pre()
+                evn[i][0].record(stream)
+                fn()
+                evn[i][1].record(stream)
+            torch.cuda.synchronize()
+            return sum(a.elapsed_time(b) for a, b in evn) / n
+
+        nop = lambda: None
+        f_hot_ms = after(core_fwd, nfwd_core)
+        f_cold_ms = after(nop, nfwd_core)
+        b_hot_ms = after(nbwd, core_bwd_on_norm_dy)
+        b_cold_ms = after(nop, core_bwd_on_norm_dy)
         esz = 2 if dims.dtype == "bf16" else 4
         f_bytes = 3 * rows_ * width_ * esz + 4 * rows_ + 4 * width_
         b_bytes = 5 * rows_ * width_ * esz + 4 * rows_ + 8 * width_
@@ -767,7 +812,17 @@ def main():
                      "fwd_algorithmic_bytes": f_bytes, "bwd_algorithmic_bytes": b_bytes,
                      "fwd_frac_of_hbm": f_bytes / (f_ms / 1e3) / 1e9 / hbm_,
                      "bwd_frac_of_hbm": b_bytes / (b_ms / 1e3) / 1e9 / hbm_,
-                     "timing": "CUDA events per call, L2 flushed between calls"}
+                     "timing": "CUDA events per call, L2 flushed between calls",
+                     "fusion_bound": {
+                         "norm_fwd_after_core_fwd_us": 1e3 * f_hot_ms,
+                         "norm_fwd_after_flush_us": 1e3 * f_cold_ms,
+                         "core_bwd_after_norm_bwd_us": 1e3 * b_hot_ms,
+                         "core_bwd_after_flush_us": 1e3 * b_cold_ms,
+                         "what": "the norm forward reading the y the core's forward just wrote "
+                                 "(L2-hot) against the same call after an L2 flush, and the "
+                                 "core's backward reading the dy the norm backward just wrote; "
+                                 "the differences bound what fusing the norm into the core "
+                                 "could save"}}
     except Exception as e:  # noqa: BLE001  (reported, the headline stands)
         norm_line = {"error": f"{type(e).__name__}: {e}"[:200]}
 

@@ -17,7 +17,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OUT = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT, "libssd_gb300.so")
-SOURCES = ["ssd_api.cu", "ssd_simt.cu", "ssd_tc.cu", "ssd_tc32.cu", "ssd_noalloc.cu",
+SOURCES = ["ssd_api.cu", "ssd_simt.cu", "ssd_tc.cu", "ssd_tc64.cu", "ssd_noalloc.cu",
            "ssd_dtprep.cu", "ssd_norm.cu", "ssd_conv.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

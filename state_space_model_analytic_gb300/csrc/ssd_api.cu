@@ -70,12 +70,12 @@ cudaError_t tc_forward_states(const Problem& p);
 cudaError_t tc_backward(const Problem& p);
 cudaError_t tc_read_and_clear_error(unsigned int* out);
 cudaError_t tc_selftest_timeout(cudaStream_t s);
-bool tc32_supported(const Problem& p);
-size_t tc32_bc_part_floats(const Problem& p);
-cudaError_t tc32_chunk_outer(const Problem& p, int mode, float* out);
-cudaError_t tc32_forward_scan(const Problem& p);
-cudaError_t tc32_backward(const Problem& p);
-cudaError_t tc32_read_and_clear_error(unsigned int* out);
+bool tc64_supported(const Problem& p);
+size_t tc64_bc_part_floats(const Problem& p);
+cudaError_t tc64_chunk_outer(const Problem& p, int mode, float* out);
+cudaError_t tc64_forward_scan(const Problem& p);
+cudaError_t tc64_backward(const Problem& p);
+cudaError_t tc64_read_and_clear_error(unsigned int* out);
 
 namespace {
 
@@ -186,10 +186,10 @@ size_t carve(Problem* p, char* base, int which) {
   const size_t items = units * (size_t)p->hpg;
   p->ntickets = (int)(1 + units);
   p->tickets = (unsigned int*)take((1 + units) * sizeof(unsigned int));
-  // (the fp32 tensor-core backward keeps its per-segment dC, dB partials there)
+  // (the d_state-64 tensor-core backward keeps its per-segment dC, dB partials there)
   size_t part_floats = (items < kBwdMaxCtas ? items : kBwdMaxCtas) * 2 * 32768;
-  if (tc32_supported(*p) && tc32_bc_part_floats(*p) > part_floats)
-    part_floats = tc32_bc_part_floats(*p);
+  if (tc64_supported(*p) && tc64_bc_part_floats(*p) > part_floats)
+    part_floats = tc64_bc_part_floats(*p);
   p->bwd_part = (float*)take(part_floats * sizeof(float));
   p->hT = take(states / 2);  // bf16 copies for the tensor-core backward
   p->gT = take(states / 2);
@@ -215,6 +215,36 @@ int check_smem(const Problem& p) {
 }  // namespace
 
 void set_last_error(const char* msg) { g_err = msg; }
+
+// The kernels of one forward call for the carved problem `p` (shared with
+// ssd_forward_noalloc, so both run the same sequence); *where names the
+// kernel whose launch failed.
+cudaError_t forward_launches(Problem& p, const char** where) {
+  const bool tc = tc_supported(p);
+  cudaError_t e;
+  if (tc && tc_fused_states(p)) {
+    // one kernel: chunk states, the state pass (look-back) and y
+    *where = "single-pass forward kernel";
+    return tc_forward_single(p);
+  }
+  if (tc64_supported(p)) {  // headdim 64, d_state 64 (fp32 through split bf16 products)
+    *where = "forward chunk-state kernel";
+    if ((e = tc64_chunk_outer(p, 0, p.hist)) != cudaSuccess) return e;
+    *where = "forward state-pass kernel";
+    if ((e = simt_state_pass_fwd(p, p.hist, p.cs_last)) != cudaSuccess) return e;
+    *where = "forward chunk-scan kernel";
+    return tc64_forward_scan(p);
+  }
+  p.hT = nullptr;  // the scan converts the fp32 history itself
+  *where = "forward chunk-state kernel";
+  e = tc ? tc_chunk_outer(p, 0, p.hist) : simt_forward_states(p, p.hist, p.cs_last);
+  if (e != cudaSuccess) return e;
+  *where = "forward state-pass kernel";
+  if ((e = simt_state_pass_fwd(p, p.hist, p.cs_last)) != cudaSuccess) return e;
+  *where = "forward chunk-scan kernel";
+  return tc ? tc_forward_scan(p) : simt_forward_scan(p);
+}
+
 
 // The checks and problem set-up of ssd_forward, for the other entry points.
 int validate_dims(const ssd_dims* d) { return validate(d); }
@@ -309,13 +339,13 @@ int ssd_force_kernel_path(int path) {
 
 int ssd_device_status(void) {
   g_err.clear();
-  unsigned int flag = 0, conv_flag = 0, tc32_flag = 0;
+  unsigned int flag = 0, conv_flag = 0, tc64_flag = 0;
   cudaError_t e = tc_read_and_clear_error(&flag);
   if (e == cudaSuccess) e = conv_read_and_clear_error(&conv_flag);
-  if (e == cudaSuccess) e = tc32_read_and_clear_error(&tc32_flag);
+  if (e == cudaSuccess) e = tc64_read_and_clear_error(&tc64_flag);
   if (e != cudaSuccess) return cuda_fail(e, "ssd_device_status");
   flag |= conv_flag << 8;
-  flag |= tc32_flag << 16;
+  flag |= tc64_flag << 16;
   if (flag) return fail(SSD_ERR_DEVICE_TIMEOUT, "a device-side wait gave up (flag 0x%x)", flag);
   return SSD_OK;
 }
@@ -330,7 +360,7 @@ int ssd_selftest_wait_timeout(void* cuda_stream) {
 int ssd_kernel_path(const ssd_dims* dims) {
   if (validate(dims) != SSD_OK) return -1;
   Problem p = base_problem(dims);
-  return (tc_supported(p) || tc32_supported(p)) ? 1 : 0;
+  return (tc_supported(p) || tc64_supported(p)) ? 1 : 0;
 }
 
 // The raw-dt mode of the fused tensor-core path (ssd_forward_raw /
@@ -374,32 +404,11 @@ int forward_impl(const ssd_dims* dims, const void* x, const float* dt, const flo
   carve(&p, (char*)workspace, 0);
   p.stream = (cudaStream_t)cuda_stream;
 
-  const bool tc = tc_supported(p);
-  cudaError_t e;
-  if (raw && !(tc && tc_fused_states(p)))
+  if (raw && !(tc_supported(p) && tc_fused_states(p)))
     return fail(SSD_ERR_UNSUPPORTED, "ssd_forward: raw-dt mode needs the fused tensor-core path");
-  if (tc && tc_fused_states(p)) {
-    // one kernel: chunk states, the state pass (look-back) and y
-    e = tc_forward_single(p);
-    if (e != cudaSuccess) return cuda_fail(e, "single-pass forward kernel");
-    return SSD_OK;
-  }
-  if (tc32_supported(p)) {  // fp32 storage on tensor cores (split bf16 products)
-    e = tc32_chunk_outer(p, 0, p.hist);
-    if (e != cudaSuccess) return cuda_fail(e, "forward chunk-state kernel");
-    e = simt_state_pass_fwd(p, p.hist, p.cs_last);
-    if (e != cudaSuccess) return cuda_fail(e, "forward state-pass kernel");
-    e = tc32_forward_scan(p);
-    if (e != cudaSuccess) return cuda_fail(e, "forward chunk-scan kernel");
-    return SSD_OK;
-  }
-  p.hT = nullptr;  // the scan converts the fp32 history itself
-  e = tc ? tc_chunk_outer(p, 0, p.hist) : simt_forward_states(p, p.hist, p.cs_last);
-  if (e != cudaSuccess) return cuda_fail(e, "forward chunk-state kernel");
-  e = simt_state_pass_fwd(p, p.hist, p.cs_last);
-  if (e != cudaSuccess) return cuda_fail(e, "forward state-pass kernel");
-  e = tc ? tc_forward_scan(p) : simt_forward_scan(p);
-  if (e != cudaSuccess) return cuda_fail(e, "forward chunk-scan kernel");
+  const char* where = "";
+  const cudaError_t e = forward_launches(p, &where);
+  if (e != cudaSuccess) return cuda_fail(e, where);
   return SSD_OK;
 }
 }  // namespace
@@ -460,7 +469,7 @@ int backward_impl(const ssd_dims* dims, const void* x, const float* dt, const fl
       if (e != cudaSuccess) return cuda_fail(e, "backward recompute state-scan kernel");
     } else {
       e = tc_supported(f)     ? tc_chunk_outer(f, 0, f.hist)
-          : tc32_supported(f) ? tc32_chunk_outer(f, 0, f.hist)
+          : tc64_supported(f) ? tc64_chunk_outer(f, 0, f.hist)
                               : simt_forward_states(f, f.hist, f.cs_last);
       if (e != cudaSuccess) return cuda_fail(e, "backward recompute chunk-state kernel");
       e = simt_state_pass_fwd(f, f.hist, f.cs_last);
@@ -468,7 +477,7 @@ int backward_impl(const ssd_dims* dims, const void* x, const float* dt, const fl
     }
   }
   e = tc_backward_supported(p) ? tc_backward(p)
-      : tc32_supported(p)       ? tc32_backward(p)
+      : tc64_supported(p)       ? tc64_backward(p)
                                 : simt_backward(p);
   if (e != cudaSuccess) return cuda_fail(e, "backward kernels");
   return SSD_OK;

@@ -74,6 +74,10 @@ int validate_dims(const ssd_dims* d);
 Problem problem_of(const ssd_dims* d);  // call after validate_dims succeeded
 int check_shared_memory(const Problem& p);
 
+// The kernels of one forward call for a carved problem (ssd_api.cu); *where
+// names the kernel whose launch failed.
+cudaError_t forward_launches(Problem& p, const char** where);
+
 // Gated RMSNorm after the core (ssd_norm.cu).  The backward keeps per-CTA
 // column sums of the weight gradient in part[grid][width], grid <=
 // kNormMaxCtas.

@@ -32,11 +32,6 @@
 
 namespace ssd {
 
-bool tc_supported(const Problem& p);
-bool tc_fused_states(const Problem& p);
-cudaError_t tc_chunk_outer(const Problem& p, int mode, float* out);
-cudaError_t tc_forward_scan(const Problem& p);
-cudaError_t tc_forward_single(const Problem& p);
 void set_last_error(const char* msg);
 
 namespace {
@@ -126,14 +121,8 @@ extern "C" int ssd_forward_noalloc(const ssd_dims* dims, const void* x, const fl
   p.stream = (cudaStream_t)cuda_stream;
 
   // the launch sequence of ssd_forward for these dims
-  const bool tc = tc_supported(p);
-  if (tc && tc_fused_states(p)) {
-    e = tc_forward_single(p);  // clears its flags on the stream first
-  } else {
-    e = tc ? tc_chunk_outer(p, 0, p.hist) : simt_forward_states(p, p.hist, p.cs_last);
-    if (e == cudaSuccess) e = simt_state_pass_fwd(p, p.hist, p.cs_last);
-    if (e == cudaSuccess) e = tc ? tc_forward_scan(p) : simt_forward_scan(p);
-  }
+  const char* where = "";
+  e = forward_launches(p, &where);
   if (e != cudaSuccess) return reject(SSD_ERR_CUDA, cudaGetErrorString(e));
   return SSD_OK;
 }

@@ -1,36 +1,48 @@
-// Tensor-core (tcgen05 / TMEM) kernels of the chunked SSD core for fp32
-// storage: headdim P = 64, d_state N = 64, chunk Q = 128.
+// Tensor-core (tcgen05 / TMEM) kernels of the chunked SSD core for headdim
+// P = 64 and d_state N = 64, fp32 or bf16 storage, any chunk Q in {16, 32,
+// 64, 128} (seqlen a multiple of 128).
 //
-// Split products.  Every fp32 operand a is carried as two bf16 tiles,
+// Blocks.  The chunk scan and the backward work on blocks of 128 steps (the
+// MMA M size).  A block holds 128 / Q whole chunks; inside it the decays are
+// block-local cumulative sums, which is exact (chunking is a regrouping of
+// the recurrence), and the block's start state is the history entry of its
+// first chunk.  The chunk-state kernel and the state passes work per chunk,
+// as the history is defined per chunk.
+//
+// Split products (fp32 storage).  Every fp32 operand a is carried as two
+// bf16 tiles,
 //     hi = bf16(a),  lo = bf16(a - hi),
 // so a = hi + lo + r with |r| <= 2^-18 |a|, and every product as three bf16
 // MMAs accumulated in fp32 TMEM:
 //     A B ~ Ah Bh + Ah Bl + Al Bh,
 // dropping Al Bl and the remainders (each at most about 2^-18 |A||B| per
-// term).  The layouts are those of the bf16 kernels (128-byte swizzled rows
-// of 64 bf16).  Inputs come from global memory by coalesced 16-byte loads and
-// are split by the threads; elementwise math (decays, masks, epilogues) runs
-// in fp32 from the exact fp32 inputs.
+// term).  bf16 storage uses the hi tiles alone and one MMA per product, like
+// the bf16 kernels of ssd_tc.cu.  The layouts are those kernels' (128-byte
+// swizzled rows of 64 bf16).  Inputs come from global memory by coalesced
+// 16-byte loads and are converted by the threads; elementwise math (decays,
+// masks, epilogues) runs in fp32 from the stored input values.
 //
 // The chunked algebra is that of the SIMT kernels (ssd_simt.cu), derived from
 // the recurrence of `ssd_forward_state_history_reference` and the reverse-time
 // adjoint of `ssd_backward_reference` (burn_dragon_kernel 0.5.0,
 // src/sequence/mamba2/backward.rs).  Kernels:
-//   k_outer32<0>  S_c = sum_j exp(cs_last - cs_j) dt_j x_j B_j^T       (b, c, h)
-//   k_outer32<1>  R_c = sum_i exp(cs_i) dy_i C_i^T                      (b, c, h)
-//   k_scan32      y_i = sum_{j<=i} exp(cs_i-cs_j) dt_j (C_i.B_j) x_j
-//                       + exp(cs_i) H_{c-1} C_i + D x_i                 (b, c, h)
-//   k_bwd32_x     dx, d(dt), and the per-(b, c) partials of dA, dD      (b, c, h)
-//   k_bwd32_bc    dC, dB of a (b, c, g) unit over a segment of its heads:
+//   k_outer64<0>  S_c = sum_j exp(cs_last - cs_j) dt_j x_j B_j^T       (b, c, h)
+//   k_outer64<1>  R_c = sum_i exp(cs_i) dy_i C_i^T                      (b, c, h)
+//   k_scan64      y_i = sum_{j<=i} exp(cs_i-cs_j) dt_j (C_i.B_j) x_j
+//                       + exp(cs_i) H_in C_i + D x_i                    (b, block, h)
+//   k_bwd64_x     dx, d(dt), and the per-(b, block) partials of dA, dD  (b, block, h)
+//   k_bwd64_bc    dC, dB of a (b, block, g) unit over a segment of its heads:
 //                 W = sum_h exp(cs_i-cs_j) dt_j (dy_i.x_j) (summed over the
 //                 segment's heads in registers), then W B, W^T C, plus the
 //                 state terms sum_h (e o dY) H and sum_h (f o X) g
-//   k_sum32_bc    the segments' dC, dB partials summed in segment order
+//   k_sum64_bc    the segments' dC, dB partials summed in segment order
 // The state passes between them are the SIMT ones (fp32, sequential over
 // chunks).  Every wait is bounded; a wait that gives up sets a device error
 // word and the kernel finishes without touching the guarded data.
 #include <cuda.h>
 #include <cuda_bf16.h>
+
+#include <type_traits>
 
 #include "ssd_common.cuh"
 #include "ssd_internal.h"
@@ -46,24 +58,30 @@ namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
-constexpr int kQ = 128, kP = 64, kN = 64;
+constexpr int kQ = 128, kP = 64, kN = 64;  // kQ: rows of a block (the MMA M size)
 
-__device__ unsigned int g_tc32_error;
+__device__ unsigned int g_tc64_error;
 
 __device__ __forceinline__ bool wait_all(uint64_t* bar, uint32_t parity) {
   const bool mine = mbar_wait(bar, parity, kWaitLimitNs);
   const bool all = __syncthreads_and(mine) != 0;
-  if (!all && threadIdx.x == 0) atomicOr(&g_tc32_error, 1u);
+  if (!all && threadIdx.x == 0) atomicOr(&g_tc64_error, 1u);
   return all;
 }
 
-struct D32 {
+struct D64 {
   int B, T, H, G, nc, hpg;
+  int Q, nb, cpb;  // chunk size, 128-row blocks, chunks per block
 };
+
+// storage element type
+template <bool kBf>
+using Elem = typename std::conditional<kBf, __nv_bfloat16, float>::type;
 
 // ---- split tiles ----------------------------------------------------------
 // 8 consecutive values of one tile row as (hi, lo) bf16 chunks at byte offset
-// `off` of the hi and lo tiles.
+// `off` of the hi and lo tiles (kBf: the hi chunk only).
+template <bool kBf = false>
 __device__ __forceinline__ void store_split8(uint8_t* hi, uint8_t* lo, uint32_t off,
                                              const float* v) {
   uint32_t h[4], l[4];
@@ -72,41 +90,72 @@ __device__ __forceinline__ void store_split8(uint8_t* hi, uint8_t* lo, uint32_t 
     const __nv_bfloat16 a = __float2bfloat16_rn(v[2 * t]);
     const __nv_bfloat16 b = __float2bfloat16_rn(v[2 * t + 1]);
     h[t] = pack_bf16(__bfloat162float(a), __bfloat162float(b));
-    l[t] = pack_bf16(v[2 * t] - __bfloat162float(a), v[2 * t + 1] - __bfloat162float(b));
+    if (!kBf)
+      l[t] = pack_bf16(v[2 * t] - __bfloat162float(a), v[2 * t + 1] - __bfloat162float(b));
   }
   *(uint4*)(hi + off) = make_uint4(h[0], h[1], h[2], h[3]);
-  *(uint4*)(lo + off) = make_uint4(l[0], l[1], l[2], l[3]);
+  if (!kBf) *(uint4*)(lo + off) = make_uint4(l[0], l[1], l[2], l[3]);
 }
 
-// ROWS rows of 64 fp32 (row r at src + r * stride) into split tiles (rows of
-// 64 bf16, SW128), each value times scale(r).  All loads of a thread are
-// issued before its first store.
-template <int NT, int ROWS, typename F>
-__device__ __forceinline__ void load_split(uint8_t* hi, uint8_t* lo, const float* __restrict__ src,
-                                           size_t stride, F&& scale) {
+// 8 consecutive stored values (16 or 32 bytes) as fp32
+struct Raw8 {
+  float4 a, b;
+};
+__device__ __forceinline__ Raw8 ld8(const float* p) {
+  return Raw8{__ldg((const float4*)p), __ldg((const float4*)p + 1)};
+}
+__device__ __forceinline__ Raw8 ld8(const __nv_bfloat16* p) {
+  const uint4 u = __ldg((const uint4*)p);
+  const __nv_bfloat162* q = (const __nv_bfloat162*)&u;
+  const float2 f0 = __bfloat1622float2(q[0]), f1 = __bfloat1622float2(q[1]);
+  const float2 f2 = __bfloat1622float2(q[2]), f3 = __bfloat1622float2(q[3]);
+  return Raw8{make_float4(f0.x, f0.y, f1.x, f1.y), make_float4(f2.x, f2.y, f3.x, f3.y)};
+}
+__device__ __forceinline__ void unpack_raw(const Raw8& r, float* f) {
+  f[0] = r.a.x; f[1] = r.a.y; f[2] = r.a.z; f[3] = r.a.w;
+  f[4] = r.b.x; f[5] = r.b.y; f[6] = r.b.z; f[7] = r.b.w;
+}
+// 8 values to storage at p (16 or 32 bytes)
+__device__ __forceinline__ void st8(float* p, const float* f) {
+  ((float4*)p)[0] = make_float4(f[0], f[1], f[2], f[3]);
+  ((float4*)p)[1] = make_float4(f[4], f[5], f[6], f[7]);
+}
+__device__ __forceinline__ void st8(__nv_bfloat16* p, const float* f) {
+  *(uint4*)p = make_uint4(pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]), pack_bf16(f[4], f[5]),
+                          pack_bf16(f[6], f[7]));
+}
+
+// Rows [0, nrows) (nrows <= ROWS) of a 64-wide slab (row r at src + r *
+// stride elements) into split tiles (rows of 64 bf16, SW128), each value
+// times scale(r).  All loads of a thread are issued before its first store.
+template <int NT, int ROWS, typename E, typename F>
+__device__ __forceinline__ void load_split(uint8_t* hi, uint8_t* lo, const E* __restrict__ src,
+                                           size_t stride, F&& scale, int nrows = ROWS) {
+  constexpr bool kBf = std::is_same<E, __nv_bfloat16>::value;
   constexpr int kPer = ROWS * 8 / NT;
-  float4 v[kPer][2];
+  Raw8 v[kPer];
 #pragma unroll
   for (int k = 0; k < kPer; ++k) {
     const int e = threadIdx.x + NT * k, r = e >> 3, ch = e & 7;
-    const float4* s = (const float4*)(src + (size_t)r * stride + ch * 8);
-    v[k][0] = __ldg(s);
-    v[k][1] = __ldg(s + 1);
+    if (r < nrows) v[k] = ld8(src + (size_t)r * stride + ch * 8);
   }
 #pragma unroll
   for (int k = 0; k < kPer; ++k) {
     const int e = threadIdx.x + NT * k, r = e >> 3, ch = e & 7;
+    if (r >= nrows) continue;
     const float sc = scale(r);
-    const float f[8] = {v[k][0].x * sc, v[k][0].y * sc, v[k][0].z * sc, v[k][0].w * sc,
-                        v[k][1].x * sc, v[k][1].y * sc, v[k][1].z * sc, v[k][1].w * sc};
-    store_split8(hi, lo, sw128(r, ch), f);
+    float f[8];
+    unpack_raw(v[k], f);
+#pragma unroll
+    for (int t = 0; t < 8; ++t) f[t] *= sc;
+    store_split8<kBf>(hi, lo, sw128(r, ch), f);
   }
 }
 
 // A [64 p][64 n] fp32 state block (p-major) transposed into split tiles of
 // rows n with 64 p each; returns this thread's share of sum(src * other) when
 // `other` is given (the same elements of a second block, for <g, H>).
-template <int NT>
+template <int NT, bool kBf>
 __device__ __forceinline__ float load_split_transposed(uint8_t* hi, uint8_t* lo,
                                                        const float* __restrict__ src,
                                                        const float* __restrict__ other) {
@@ -122,33 +171,39 @@ __device__ __forceinline__ float load_split_transposed(uint8_t* hi, uint8_t* lo,
 #pragma unroll
       for (int t = 0; t < 8; ++t) dot = fmaf(f[t], __ldg(other + (size_t)(pc * 8 + t) * kN + n), dot);
     }
-    store_split8(hi, lo, sw128(n, pc), f);
+    store_split8<kBf>(hi, lo, sw128(n, pc), f);
   }
   return dot;
 }
 
-// D (+)= A B as three bf16 MMAs over the split tiles (lo tiles at the given
-// byte distance from the hi tiles).
+// D (+)= A B over the split tiles (lo tiles at the given byte distance from
+// the hi tiles): three bf16 MMAs, or one (kBf: the hi tiles hold the
+// operands exactly).
+template <bool kBf>
 __device__ __forceinline__ void mma3(uint32_t d, uint32_t a_hi, uint32_t a_lo_off, uint32_t a_lbo,
                                      bool a_mn, uint32_t b_hi, uint32_t b_lo_off, uint32_t b_lbo,
                                      uint32_t idesc, uint32_t acc) {
   (void)a_mn;
-  const uint64_t ah = desc_sw128(a_hi, a_lbo, 1024), al = desc_sw128(a_hi + a_lo_off, a_lbo, 1024);
-  const uint64_t bh = desc_sw128(b_hi, b_lbo, 1024), bl = desc_sw128(b_hi + b_lo_off, b_lbo, 1024);
+  const uint64_t ah = desc_sw128(a_hi, a_lbo, 1024), bh = desc_sw128(b_hi, b_lbo, 1024);
   mma_bf16(d, ah, bh, idesc, acc);
-  mma_bf16(d, ah, bl, idesc, 1u);
-  mma_bf16(d, al, bh, idesc, 1u);
+  if (!kBf) {
+    const uint64_t al = desc_sw128(a_hi + a_lo_off, a_lbo, 1024);
+    const uint64_t bl = desc_sw128(b_hi + b_lo_off, b_lbo, 1024);
+    mma_bf16(d, ah, bl, idesc, 1u);
+    mma_bf16(d, al, bh, idesc, 1u);
+  }
 }
 
-// chunk-local inclusive cumsum of dt * A (log2 units) for the block's first
-// 128 threads; s_cs2, s_dt filled, ends synced
-__device__ __forceinline__ void chunk_tables(const D32& d, const float* __restrict__ dt, float a2,
-                                             int b, int c, int h, float* s_cs2, float* s_dt,
-                                             float* scratch) {
+// Inclusive cumsum of dt * A (log2 units) over `len` steps starting at step
+// t0 of batch row b, for the block's first `len` threads; s_cs2, s_dt
+// filled, ends synced.
+__device__ __forceinline__ void step_tables(const D64& d, const float* __restrict__ dt, float a2,
+                                            int b, size_t t0, int len, int h, float* s_cs2,
+                                            float* s_dt, float* scratch) {
   const int tid = threadIdx.x;
-  const float dv = tid < kQ ? dt[((size_t)b * d.T + (size_t)c * kQ + tid) * d.H + h] : 0.f;
+  const float dv = tid < len ? dt[((size_t)b * d.T + t0 + tid) * d.H + h] : 0.f;
   const float cs = block_inclusive_scan(dv * a2, scratch);
-  if (tid < kQ) {
+  if (tid < len) {
     s_cs2[tid] = cs;
     s_dt[tid] = dv;
   }
@@ -156,15 +211,16 @@ __device__ __forceinline__ void chunk_tables(const D32& d, const float* __restri
 }
 
 // ---------------------------------------------------------------------------
-// Chunk outer products, one CTA per (b, c, h), 256 threads.
+// Chunk outer products, one CTA per (b, c, h) for chunks of Q <= 128 steps,
+// 256 threads.
 //   MODE 0: out = S_c  from u = x,  v = B, w_j = exp(cs_last - cs_j) dt_j
 //   MODE 1: out = R_c  from u = dy, v = C, w_i = exp(cs_i)
 // as D[n][p] = V^T (w o U) (M = n padded to 128: the second half of the A
 // operand reads the U tiles and its rows are never read back), then written
 // out[b][c][h][p][n]; also cs_last[b][h][c] (natural-log units).
-template <int MODE>
-__global__ void __launch_bounds__(256) k_outer32(D32 d, const float* __restrict__ U,
-                                                 const float* __restrict__ V,
+template <int MODE, bool kBf>
+__global__ void __launch_bounds__(256) k_outer64(D64 d, const Elem<kBf>* __restrict__ U,
+                                                 const Elem<kBf>* __restrict__ V,
                                                  const float* __restrict__ dt,
                                                  const float* __restrict__ A,
                                                  float* __restrict__ out,
@@ -179,7 +235,7 @@ __global__ void __launch_bounds__(256) k_outer32(D32 d, const float* __restrict_
   __shared__ uint64_t bar;
   __shared__ uint32_t tmem_base;
   const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z, tid = threadIdx.x;
-  const int g = h / d.hpg;
+  const int g = h / d.hpg, Q = d.Q;
   if (tid == 0) {
     mbar_init(&bar, 1);
     fence_mbar_init();
@@ -188,16 +244,16 @@ __global__ void __launch_bounds__(256) k_outer32(D32 d, const float* __restrict_
     tmem_alloc(&tmem_base, 64);
     tmem_relinquish();
   }
-  chunk_tables(d, dt, A[h] * kLog2e, b, c, h, s_cs2, s_dt, scratch);
-  const float last2 = s_cs2[kQ - 1];
-  if (tid < kQ) s_w[tid] = MODE == 0 ? exp2f(last2 - s_cs2[tid]) * s_dt[tid] : exp2f(s_cs2[tid]);
+  step_tables(d, dt, A[h] * kLog2e, b, (size_t)c * Q, Q, h, s_cs2, s_dt, scratch);
+  const float last2 = s_cs2[Q - 1];
+  if (tid < Q) s_w[tid] = MODE == 0 ? exp2f(last2 - s_cs2[tid]) * s_dt[tid] : exp2f(s_cs2[tid]);
   if (tid == 0) cs_last[((size_t)b * d.H + h) * d.nc + c] = last2 * (1.0f / kLog2e);
   __syncthreads();
-  const size_t row0 = (size_t)b * d.T + (size_t)c * kQ;
+  const size_t row0 = (size_t)b * d.T + (size_t)c * Q;
   load_split<256, kQ>(sVh, sVl, V + (row0 * d.G + g) * kN, (size_t)d.G * kN,
-                      [](int) { return 1.f; });
+                      [](int) { return 1.f; }, Q);
   load_split<256, kQ>(sUh, sUl, U + (row0 * d.H + h) * kP, (size_t)d.H * kP,
-                      [&](int r) { return s_w[r]; });
+                      [&](int r) { return s_w[r]; }, Q);
   fence_async_smem();
   fence_before_sync();
   __syncthreads();
@@ -205,8 +261,8 @@ __global__ void __launch_bounds__(256) k_outer32(D32 d, const float* __restrict_
   const uint32_t tm = tmem_base;
   if (tid == 0) {
     const uint32_t id = idesc_bf16(128, 64, true, true);
-    for (int ks = 0; ks < kQ / 16; ++ks)
-      mma3(tm, smem_u32(sVh) + ks * 2048, 16384, 32768, true, smem_u32(sUh) + ks * 2048, 16384,
+    for (int ks = 0; ks < Q / 16; ++ks)
+      mma3<kBf>(tm, smem_u32(sVh) + ks * 2048, 16384, 32768, true, smem_u32(sUh) + ks * 2048, 16384,
            16384, id, ks > 0);
     mma_commit(&bar);
   }
@@ -227,24 +283,26 @@ __global__ void __launch_bounds__(256) k_outer32(D32 d, const float* __restrict_
 }
 
 // ---------------------------------------------------------------------------
-// Chunk scan: y of one (b, c, h) per CTA, 256 threads.
-//   CB = C B^T, Ys = C H^T (H = H_{c-1} from the history, as rows n),
+// Chunk scan: y of one (b, 128-step block, h) per CTA, 256 threads.
+//   CB = C B^T, Ys = C H^T (H = the state before the block: the history entry
+//   of its first chunk, as rows n),
 //   M = CB o L o dt (masked, split), Y = M X,
 //   y = Y + exp(cs_i) Ys + D x.
 // Decay masks as in the bf16 kernels: for warp q's rows and a 32-column chunk
 // left of its diagonal chunk, exp(cs_i - cs_j) = exp(cs_i - cs_r) exp(cs_r -
 // cs_j) with r = 32 q (both factors <= 1); the diagonal chunk evaluates the
 // exponent only where j <= i.
-constexpr uint32_t kS32Bytes = 114688;  // C, B (later M) 64K | X 32K | H 16K
+constexpr uint32_t kScan64Bytes = 114688;  // C, B (later M) 64K | X 32K | H 16K
 
-__global__ void __launch_bounds__(256, 1) k_scan32(D32 d, const float* __restrict__ x,
+template <bool kBf>
+__global__ void __launch_bounds__(256, 1) k_scan64(D64 d, const Elem<kBf>* __restrict__ x,
                                                    const float* __restrict__ dt,
                                                    const float* __restrict__ A,
-                                                   const float* __restrict__ Bm,
-                                                   const float* __restrict__ Cm,
+                                                   const Elem<kBf>* __restrict__ Bm,
+                                                   const Elem<kBf>* __restrict__ Cm,
                                                    const float* __restrict__ D,
                                                    const float* __restrict__ hist,
-                                                   float* __restrict__ y) {
+                                                   Elem<kBf>* __restrict__ y) {
   extern __shared__ __align__(1024) uint8_t smraw[];
   uint8_t* sm = align1024(smraw);
   uint8_t* sCh = sm;            // [128 rows i][64 n] K-major
@@ -261,7 +319,7 @@ __global__ void __launch_bounds__(256, 1) k_scan32(D32 d, const float* __restric
   __shared__ __align__(16) float s_E[4][kQ];  // exp(cs_r - cs_j) dt_j, j < r = 32 w
   __shared__ uint64_t bar;
   __shared__ uint32_t tmem_base;
-  const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z, tid = threadIdx.x;
+  const int blk = blockIdx.x, h = blockIdx.y, b = blockIdx.z, tid = threadIdx.x;
   const int g = h / d.hpg, wg = tid >> 7, q = (tid >> 5) & 3, row = tid & 127;
   const uint32_t lane_base = (uint32_t)(q * 32) << 16;
   if (tid == 0) {
@@ -272,18 +330,19 @@ __global__ void __launch_bounds__(256, 1) k_scan32(D32 d, const float* __restric
     tmem_alloc(&tmem_base, 256);
     tmem_relinquish();
   }
-  chunk_tables(d, dt, A[h] * kLog2e, b, c, h, s_cs2, s_dt, scratch);
+  step_tables(d, dt, A[h] * kLog2e, b, (size_t)blk * kQ, kQ, h, s_cs2, s_dt, scratch);
   for (int e = tid; e < 4 * kQ; e += 256) {
     const int w = e >> 7, j = e & 127, r = 32 * w;
     s_E[w][j] = j < r ? exp2f(s_cs2[r] - s_cs2[j]) * s_dt[j] : 0.f;
   }
-  const size_t row0 = (size_t)b * d.T + (size_t)c * kQ;
+  const size_t row0 = (size_t)b * d.T + (size_t)blk * kQ;
+  const size_t c0 = (size_t)blk * d.cpb;  // the block's first chunk
   const auto one = [](int) { return 1.f; };
   load_split<256, kQ>(sCh, sCl, Cm + (row0 * d.G + g) * kN, (size_t)d.G * kN, one);
   load_split<256, kQ>(sBh, sBl, Bm + (row0 * d.G + g) * kN, (size_t)d.G * kN, one);
   load_split<256, kQ>(sXh, sXl, x + (row0 * d.H + h) * kP, (size_t)d.H * kP, one);
-  (void)load_split_transposed<256>(sHh, sHl, hist + (((size_t)b * d.nc + c) * d.H + h) * (kP * kN),
-                                   nullptr);
+  (void)load_split_transposed<256, kBf>(
+      sHh, sHl, hist + (((size_t)b * d.nc + c0) * d.H + h) * (kP * kN), nullptr);
   fence_async_smem();
   fence_before_sync();
   __syncthreads();
@@ -293,10 +352,10 @@ __global__ void __launch_bounds__(256, 1) k_scan32(D32 d, const float* __restric
     const uint32_t id_cb = idesc_bf16(128, 128, false, false);
     const uint32_t id_ys = idesc_bf16(128, 64, false, true);
     for (int kk = 0; kk < 4; ++kk) {
-      mma3(tCB, smem_u32(sCh) + kk * 32, 16384, 16, false, smem_u32(sBh) + kk * 32, 16384, 16,
-           id_cb, kk > 0);
-      mma3(tYs, smem_u32(sCh) + kk * 32, 16384, 16, false, smem_u32(sHh) + kk * 2048, 8192, 8192,
-           id_ys, kk > 0);
+      mma3<kBf>(tCB, smem_u32(sCh) + kk * 32, 16384, 16, false, smem_u32(sBh) + kk * 32, 16384,
+                16, id_cb, kk > 0);
+      mma3<kBf>(tYs, smem_u32(sCh) + kk * 32, 16384, 16, false, smem_u32(sHh) + kk * 2048, 8192,
+                8192, id_ys, kk > 0);
     }
     mma_commit(&bar);
   }
@@ -330,8 +389,8 @@ __global__ void __launch_bounds__(256, 1) k_scan32(D32 d, const float* __restric
 #pragma unroll
       for (int q4 = 0; q4 < 4; ++q4) {
         const int j = jc * 32 + q4 * 8;
-        store_split8(sMh + (j >> 6) * 16384, sMl + (j >> 6) * 16384, sw128(row, (j & 63) >> 3),
-                     &v[q4 * 8]);
+        store_split8<kBf>(sMh + (j >> 6) * 16384, sMl + (j >> 6) * 16384,
+                          sw128(row, (j & 63) >> 3), &v[q4 * 8]);
       }
     }
   }
@@ -342,7 +401,7 @@ __global__ void __launch_bounds__(256, 1) k_scan32(D32 d, const float* __restric
   if (tid == 0 && ok) {
     const uint32_t id_y = idesc_bf16(128, 64, false, true);
     for (int kk = 0; kk < 8; ++kk)
-      mma3(tY, smem_u32(sMh) + (kk >> 2) * 16384 + (kk & 3) * 32, 32768, 16, false,
+      mma3<kBf>(tY, smem_u32(sMh) + (kk >> 2) * 16384 + (kk & 3) * 32, 32768, 16, false,
            smem_u32(sXh) + kk * 2048, 16384, 16384, id_y, kk > 0);
     mma_commit(&bar);
   }
@@ -352,8 +411,6 @@ __global__ void __launch_bounds__(256, 1) k_scan32(D32 d, const float* __restric
     // y = Y + exp(cs_i) Ys + D x; warpgroup wg takes p in [32 wg, 32 wg + 32)
     const float sc = exp2f(s_cs2[row]), Dh = D[h];
     const size_t off = ((row0 + row) * d.H + h) * kP + wg * 32;
-    const float4* xs = (const float4*)(x + off);
-    float4* ys = (float4*)(y + off);
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
       float yv[16], yst[16];
@@ -361,15 +418,12 @@ __global__ void __launch_bounds__(256, 1) k_scan32(D32 d, const float* __restric
       tmem_ld16(tYs + lane_base + wg * 32 + half * 16, yst);
       tmem_wait_ld();
 #pragma unroll
-      for (int k4 = 0; k4 < 4; ++k4) {
-        const float4 xv = __ldg(xs + half * 4 + k4);
-        const int m = 4 * k4;
-        float4 o;
-        o.x = fmaf(sc, yst[m + 0], yv[m + 0]) + Dh * xv.x;
-        o.y = fmaf(sc, yst[m + 1], yv[m + 1]) + Dh * xv.y;
-        o.z = fmaf(sc, yst[m + 2], yv[m + 2]) + Dh * xv.z;
-        o.w = fmaf(sc, yst[m + 3], yv[m + 3]) + Dh * xv.w;
-        ys[half * 4 + k4] = o;
+      for (int k8 = 0; k8 < 2; ++k8) {
+        float xf[8], o[8];
+        unpack_raw(ld8(x + off + half * 16 + k8 * 8), xf);
+#pragma unroll
+        for (int t = 0; t < 8; ++t) o[t] = fmaf(sc, yst[k8 * 8 + t], yv[k8 * 8 + t]) + Dh * xf[t];
+        st8(y + off + half * 16 + k8 * 8, o);
       }
     }
   }
@@ -396,9 +450,11 @@ __device__ __forceinline__ float col_sum16(float (&v)[16]) {
   return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 16);
 }
 
-// Backward, gradient w.r.t. x and dt: one (b, c, h) per CTA, 256 threads.
+// Backward, gradient w.r.t. x and dt: one (b, 128-step block, h) per CTA,
+// 256 threads; cs, L are block-local.
 //   batch A: CB = C B^T, dYX = dY X^T, Gs = B g^T, CH = C H^T
-//            (g = g_c, the state gradient at the chunk end; H = H_{c-1})
+//            (g, the state gradient at the block end: the reverse pass's
+//            value for its last chunk; H, the state before the block)
 //   build:   W = L o dt o dYX and M = W o CB (row sums and strict column
 //            sums of M, for d(cs)); O = L o CB (split) into the C/B tiles
 //   batch B: Gx = O^T dY
@@ -408,18 +464,20 @@ __device__ __forceinline__ float col_sum16(float (&v)[16]) {
 //   dcs_i = rowsum_i - colsum_i + statein_i - e_i (+ sum_j e_j +
 //            exp(cs_last) <g, H> at i = Q - 1); da_j = sum_{i >= j} dcs_i;
 //            ddt_j = drive_j + A da_j; partials sum_j dt_j da_j and sum dy.x.
-constexpr uint32_t kBx32Bytes = 163840;  // C, B (later O) 64K | X 32K | dY 32K | H 16K | g 16K
+constexpr uint32_t kBwdX64Bytes = 163840;  // C, B (later O) 64K | X 32K | dY 32K | H 16K | g 16K
 
-__global__ void __launch_bounds__(256, 1) k_bwd32_x(D32 d, const float* __restrict__ x,
+template <bool kBf>
+__global__ void __launch_bounds__(256, 1) k_bwd64_x(D64 d, const Elem<kBf>* __restrict__ x,
                                                     const float* __restrict__ dt,
                                                     const float* __restrict__ A,
-                                                    const float* __restrict__ Bm,
-                                                    const float* __restrict__ Cm,
+                                                    const Elem<kBf>* __restrict__ Bm,
+                                                    const Elem<kBf>* __restrict__ Cm,
                                                     const float* __restrict__ D,
-                                                    const float* __restrict__ dy,
+                                                    const Elem<kBf>* __restrict__ dy,
                                                     const float* __restrict__ hist,
                                                     const float* __restrict__ gstate,
-                                                    float* __restrict__ dx, float* __restrict__ ddt,
+                                                    Elem<kBf>* __restrict__ dx,
+                                                    float* __restrict__ ddt,
                                                     float* __restrict__ dA_part,
                                                     float* __restrict__ dD_part) {
   extern __shared__ __align__(1024) uint8_t smraw[];
@@ -448,7 +506,7 @@ __global__ void __launch_bounds__(256, 1) k_bwd32_x(D32 d, const float* __restri
   __shared__ float s_esum;
   __shared__ uint64_t bar;
   __shared__ uint32_t tmem_base;
-  const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z, tid = threadIdx.x;
+  const int blk = blockIdx.x, h = blockIdx.y, b = blockIdx.z, tid = threadIdx.x;
   const int g = h / d.hpg, wg = tid >> 7, q = (tid >> 5) & 3, row = tid & 127, lane = tid & 31;
   const uint32_t lane_base = (uint32_t)(q * 32) << 16;
   if (tid == 0) {
@@ -460,22 +518,24 @@ __global__ void __launch_bounds__(256, 1) k_bwd32_x(D32 d, const float* __restri
     tmem_relinquish();
   }
   const float Ah = A[h], Dh = D[h];
-  chunk_tables(d, dt, Ah * kLog2e, b, c, h, s_cs2, s_dt, scratch);
+  step_tables(d, dt, Ah * kLog2e, b, (size_t)blk * kQ, kQ, h, s_cs2, s_dt, scratch);
   for (int e = tid; e < 4 * kQ; e += 256) {
     const int w = e >> 7, j = e & 127, r = 32 * w;
     const float ev = j < r ? exp2f(s_cs2[r] - s_cs2[j]) : 0.f;
     s_E[w][j] = ev;
     s_Edt[w][j] = ev * s_dt[j];
   }
-  const size_t row0 = (size_t)b * d.T + (size_t)c * kQ;
-  const size_t st = (((size_t)b * d.nc + c) * d.H + h) * (kP * kN);
+  const size_t row0 = (size_t)b * d.T + (size_t)blk * kQ;
+  const size_t c0 = (size_t)blk * d.cpb, c1 = c0 + d.cpb - 1;  // first, last chunk
+  const size_t st_in = (((size_t)b * d.nc + c0) * d.H + h) * (kP * kN);
+  const size_t st_out = (((size_t)b * d.nc + c1) * d.H + h) * (kP * kN);
   const auto one = [](int) { return 1.f; };
   load_split<256, kQ>(sCh, sCl, Cm + (row0 * d.G + g) * kN, (size_t)d.G * kN, one);
   load_split<256, kQ>(sBh, sBl, Bm + (row0 * d.G + g) * kN, (size_t)d.G * kN, one);
   load_split<256, kQ>(sXh, sXl, x + (row0 * d.H + h) * kP, (size_t)d.H * kP, one);
   load_split<256, kQ>(sYh, sYl, dy + (row0 * d.H + h) * kP, (size_t)d.H * kP, one);
-  (void)load_split_transposed<256>(sHh, sHl, hist + st, nullptr);
-  float hg = load_split_transposed<256>(sGh, sGl, gstate + st, hist + st);
+  (void)load_split_transposed<256, kBf>(sHh, sHl, hist + st_in, nullptr);
+  float hg = load_split_transposed<256, kBf>(sGh, sGl, gstate + st_out, hist + st_in);
   hg = block_sum(hg, scratch);  // <g_c, H_{c-1}> (syncs)
   fence_async_smem();
   fence_before_sync();
@@ -487,14 +547,14 @@ __global__ void __launch_bounds__(256, 1) k_bwd32_x(D32 d, const float* __restri
     const uint32_t id_sq = idesc_bf16(128, 128, false, false);
     const uint32_t id_km = idesc_bf16(128, 64, false, true);
     for (int kk = 0; kk < 4; ++kk) {
-      mma3(T0, smem_u32(sCh) + kk * 32, 16384, 16, false, smem_u32(sBh) + kk * 32, 16384, 16,
-           id_sq, kk > 0);
-      mma3(T1, smem_u32(sYh) + kk * 32, 16384, 16, false, smem_u32(sXh) + kk * 32, 16384, 16,
-           id_sq, kk > 0);
-      mma3(TGs, smem_u32(sBh) + kk * 32, 16384, 16, false, smem_u32(sGh) + kk * 2048, 8192, 8192,
-           id_km, kk > 0);
-      mma3(TCH, smem_u32(sCh) + kk * 32, 16384, 16, false, smem_u32(sHh) + kk * 2048, 8192, 8192,
-           id_km, kk > 0);
+      mma3<kBf>(T0, smem_u32(sCh) + kk * 32, 16384, 16, false, smem_u32(sBh) + kk * 32, 16384,
+                16, id_sq, kk > 0);
+      mma3<kBf>(T1, smem_u32(sYh) + kk * 32, 16384, 16, false, smem_u32(sXh) + kk * 32, 16384,
+                16, id_sq, kk > 0);
+      mma3<kBf>(TGs, smem_u32(sBh) + kk * 32, 16384, 16, false, smem_u32(sGh) + kk * 2048, 8192,
+                8192, id_km, kk > 0);
+      mma3<kBf>(TCH, smem_u32(sCh) + kk * 32, 16384, 16, false, smem_u32(sHh) + kk * 2048, 8192,
+                8192, id_km, kk > 0);
     }
     mma_commit(&bar);
   }
@@ -544,8 +604,8 @@ __global__ void __launch_bounds__(256, 1) k_bwd32_x(D32 d, const float* __restri
 #pragma unroll
           for (int q4 = 0; q4 < 2; ++q4) {
             const int j = col0 + q4 * 8;
-            store_split8(sOh + (j >> 6) * 16384, sOl + (j >> 6) * 16384,
-                         sw128(row, (j & 63) >> 3), &cb[q4 * 8]);
+            store_split8<kBf>(sOh + (j >> 6) * 16384, sOl + (j >> 6) * 16384,
+                              sw128(row, (j & 63) >> 3), &cb[q4 * 8]);
           }
         }
       } else {
@@ -553,8 +613,8 @@ __global__ void __launch_bounds__(256, 1) k_bwd32_x(D32 d, const float* __restri
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
           const int j = jc * 32 + q4 * 8;
-          store_split8(sOh + (j >> 6) * 16384, sOl + (j >> 6) * 16384,
-                       sw128(row, (j & 63) >> 3), z);
+          store_split8<kBf>(sOh + (j >> 6) * 16384, sOl + (j >> 6) * 16384,
+                            sw128(row, (j & 63) >> 3), z);
         }
       }
     }
@@ -567,8 +627,8 @@ __global__ void __launch_bounds__(256, 1) k_bwd32_x(D32 d, const float* __restri
     // Gx = O^T dY: M = j (O as MN-major, two 64-column blocks), K = i, N = p
     const uint32_t id = idesc_bf16(128, 64, true, true);
     for (int kk = 0; kk < 8; ++kk)
-      mma3(TGx, smem_u32(sOh) + kk * 2048, 32768, 16384, true, smem_u32(sYh) + kk * 2048, 16384,
-           16384, id, kk > 0);
+      mma3<kBf>(TGx, smem_u32(sOh) + kk * 2048, 32768, 16384, true, smem_u32(sYh) + kk * 2048,
+                16384, 16384, id, kk > 0);
     mma_commit(&bar);
   }
   ok = ok && wait_all(&bar, 1);
@@ -581,9 +641,6 @@ __global__ void __launch_bounds__(256, 1) k_bwd32_x(D32 d, const float* __restri
   float drive = 0.f, ej = 0.f, stin = 0.f, dd = 0.f;
   if (ok) {
     const size_t off = ((row0 + row) * d.H + h) * kP + wg * 32;
-    const float4* xs = (const float4*)(x + off);
-    const float4* ys = (const float4*)(dy + off);
-    float4* dxs = (float4*)(dx + off);
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
       float gx[16], gs[16], ch[16];
@@ -592,13 +649,13 @@ __global__ void __launch_bounds__(256, 1) k_bwd32_x(D32 d, const float* __restri
       tmem_ld16(TCH + lane_base + wg * 32 + half * 16, ch);
       tmem_wait_ld();
 #pragma unroll
-      for (int k4 = 0; k4 < 4; ++k4) {
-        const float4 xv = __ldg(xs + half * 4 + k4), yv = __ldg(ys + half * 4 + k4);
-        const float xa[4] = {xv.x, xv.y, xv.z, xv.w}, ya[4] = {yv.x, yv.y, yv.z, yv.w};
-        float o[4];
+      for (int k8 = 0; k8 < 2; ++k8) {
+        float xa[8], ya[8], o[8];
+        unpack_raw(ld8(x + off + half * 16 + k8 * 8), xa);
+        unpack_raw(ld8(dy + off + half * 16 + k8 * 8), ya);
 #pragma unroll
-        for (int t = 0; t < 4; ++t) {
-          const int m = 4 * k4 + t;
+        for (int t = 0; t < 8; ++t) {
+          const int m = 8 * k8 + t;
           const float gg = fmaf(fj, gs[m], gx[m]);
           o[t] = fmaf(dtj, gg, Dh * ya[t]);
           drive = fmaf(xa[t], gg, drive);
@@ -606,7 +663,7 @@ __global__ void __launch_bounds__(256, 1) k_bwd32_x(D32 d, const float* __restri
           stin = fmaf(ya[t], ch[m], stin);
           dd = fmaf(ya[t], xa[t], dd);
         }
-        dxs[half * 4 + k4] = make_float4(o[0], o[1], o[2], o[3]);
+        st8(dx + off + half * 16 + k8 * 8, o);
       }
     }
   }
@@ -642,7 +699,7 @@ __global__ void __launch_bounds__(256, 1) k_bwd32_x(D32 d, const float* __restri
   if (wg == 0 && ok) ddt[(row0 + Jr) * d.H + h] = s_v[Jr] + Ah * da;
   const float2 ad = block_sum2(make_float2(wg == 0 ? s_dt[Jr] * da : 0.f, dd), scratch2);
   if (tid == 0 && ok) {
-    const size_t slot = ((size_t)b * d.nc + c) * d.H + h;
+    const size_t slot = ((size_t)b * d.nb + blk) * d.H + h;
     dA_part[slot] = ad.x;
     dD_part[slot] = ad.y;
   }
@@ -652,23 +709,24 @@ __global__ void __launch_bounds__(256, 1) k_bwd32_x(D32 d, const float* __restri
 }
 
 // ---------------------------------------------------------------------------
-// Backward, gradients w.r.t. B and C: one (b, c, g) unit and a segment of its
-// heads per CTA, 512 threads.  Per head: dYX = dY X^T (TMEM), W = L o dt o dYX
+// Backward, gradients w.r.t. B and C: one (b, 128-step block, g) unit and a
+// segment of its heads per CTA, 512 threads.  Per head: dYX = dY X^T (TMEM), W = L o dt o dYX
 // summed over the segment's heads in registers (thread (wg, row) holds
 // columns [32 wg, 32 wg + 32) of its row); then X and dY are reloaded scaled
 // (f_j = exp(cs_last - cs_j) dt_j, e_i = exp(cs_i)) for
 //   dC += (e o dY) H,  dB += (f o X) g      (TMEM accumulators over heads).
 // After the segment: W into split tiles, dC += W B, dB += W^T C, and the fp32
 // sums of the segment written as partials [unit][segment][dC|dB][128][64].
-constexpr uint32_t kBbc32Bytes = 163840;  // B 32K | C 32K | X 32K | dY 32K | H 16K | g 16K
+constexpr uint32_t kBwdBC64Bytes = 163840;  // B 32K | C 32K | X 32K | dY 32K | H 16K | g 16K
 
-__global__ void __launch_bounds__(512, 1) k_bwd32_bc(D32 d, int seg_heads,
-                                                     const float* __restrict__ x,
+template <bool kBf>
+__global__ void __launch_bounds__(512, 1) k_bwd64_bc(D64 d, int seg_heads,
+                                                     const Elem<kBf>* __restrict__ x,
                                                      const float* __restrict__ dt,
                                                      const float* __restrict__ A,
-                                                     const float* __restrict__ Bm,
-                                                     const float* __restrict__ Cm,
-                                                     const float* __restrict__ dy,
+                                                     const Elem<kBf>* __restrict__ Bm,
+                                                     const Elem<kBf>* __restrict__ Cm,
+                                                     const Elem<kBf>* __restrict__ dy,
                                                      const float* __restrict__ hist,
                                                      const float* __restrict__ gstate,
                                                      float* __restrict__ part) {
@@ -692,7 +750,7 @@ __global__ void __launch_bounds__(512, 1) k_bwd32_bc(D32 d, int seg_heads,
   __shared__ __align__(16) float s_E[4][kQ];  // exp(cs_r - cs_j) dt_j, j < r = 32 w
   __shared__ uint64_t bar;
   __shared__ uint32_t tmem_base;
-  const int seg = blockIdx.x, c = blockIdx.y, bg = blockIdx.z;
+  const int seg = blockIdx.x, blk = blockIdx.y, bg = blockIdx.z;
   const int b = bg / d.G, g = bg % d.G;
   const int tid = threadIdx.x, wg = tid >> 7, q = (tid >> 5) & 3, row = tid & 127;
   const uint32_t lane_base = (uint32_t)(q * 32) << 16;
@@ -706,7 +764,8 @@ __global__ void __launch_bounds__(512, 1) k_bwd32_bc(D32 d, int seg_heads,
     tmem_alloc(&tmem_base, 256);
     tmem_relinquish();
   }
-  const size_t row0 = (size_t)b * d.T + (size_t)c * kQ;
+  const size_t row0 = (size_t)b * d.T + (size_t)blk * kQ;
+  const size_t c0 = (size_t)blk * d.cpb, c1 = c0 + d.cpb - 1;  // first, last chunk
   const auto one = [](int) { return 1.f; };
   load_split<512, kQ>(sBh, sBl, Bm + (row0 * d.G + g) * kN, (size_t)d.G * kN, one);
   load_split<512, kQ>(sCh, sCl, Cm + (row0 * d.G + g) * kN, (size_t)d.G * kN, one);
@@ -722,16 +781,17 @@ __global__ void __launch_bounds__(512, 1) k_bwd32_bc(D32 d, int seg_heads,
   const int I = row, jc = wg;  // this thread's row and 32-column chunk of W
   for (int hh = 0; hh < nh && ok; ++hh) {
     const int h = h0 + hh;
-    chunk_tables(d, dt, A[h] * kLog2e, b, c, h, s_cs2, s_dt, scratch);
+    step_tables(d, dt, A[h] * kLog2e, b, (size_t)blk * kQ, kQ, h, s_cs2, s_dt, scratch);
     for (int e = tid; e < 4 * kQ; e += 512) {
       const int w = e >> 7, j = e & 127, r = 32 * w;
       s_E[w][j] = j < r ? exp2f(s_cs2[r] - s_cs2[j]) * s_dt[j] : 0.f;
     }
-    const size_t st = (((size_t)b * d.nc + c) * d.H + h) * (kP * kN);
+    const size_t st_in = (((size_t)b * d.nc + c0) * d.H + h) * (kP * kN);
+    const size_t st_out = (((size_t)b * d.nc + c1) * d.H + h) * (kP * kN);
     load_split<512, kQ>(sXh, sXl, x + (row0 * d.H + h) * kP, (size_t)d.H * kP, one);
     load_split<512, kQ>(sYh, sYl, dy + (row0 * d.H + h) * kP, (size_t)d.H * kP, one);
-    load_split<512, 64>(sHh, sHl, hist + st, (size_t)kN, one);
-    load_split<512, 64>(sGh, sGl, gstate + st, (size_t)kN, one);
+    load_split<512, 64, float>(sHh, sHl, hist + st_in, (size_t)kN, one);
+    load_split<512, 64, float>(sGh, sGl, gstate + st_out, (size_t)kN, one);
     fence_async_smem();
     fence_before_sync();
     __syncthreads();
@@ -739,8 +799,8 @@ __global__ void __launch_bounds__(512, 1) k_bwd32_bc(D32 d, int seg_heads,
     if (tid == 0) {
       const uint32_t id = idesc_bf16(128, 128, false, false);
       for (int kk = 0; kk < 4; ++kk)
-        mma3(T1, smem_u32(sYh) + kk * 32, 16384, 16, false, smem_u32(sXh) + kk * 32, 16384, 16,
-             id, kk > 0);
+        mma3<kBf>(T1, smem_u32(sYh) + kk * 32, 16384, 16, false, smem_u32(sXh) + kk * 32, 16384,
+                  16, id, kk > 0);
       mma_commit(&bar);
     }
     ok = wait_all(&bar, phase);
@@ -782,10 +842,10 @@ __global__ void __launch_bounds__(512, 1) k_bwd32_bc(D32 d, int seg_heads,
     if (tid == 0) {
       const uint32_t id = idesc_bf16(128, 64, false, true);
       for (int kk = 0; kk < 4; ++kk) {
-        mma3(TdC, smem_u32(sYh) + kk * 32, 16384, 16, false, smem_u32(sHh) + kk * 2048, 8192, 8192,
-             id, hh > 0 || kk > 0);
-        mma3(TdB, smem_u32(sXh) + kk * 32, 16384, 16, false, smem_u32(sGh) + kk * 2048, 8192, 8192,
-             id, hh > 0 || kk > 0);
+        mma3<kBf>(TdC, smem_u32(sYh) + kk * 32, 16384, 16, false, smem_u32(sHh) + kk * 2048,
+                  8192, 8192, id, hh > 0 || kk > 0);
+        mma3<kBf>(TdB, smem_u32(sXh) + kk * 32, 16384, 16, false, smem_u32(sGh) + kk * 2048,
+                  8192, 8192, id, hh > 0 || kk > 0);
       }
       mma_commit(&bar);
     }
@@ -798,8 +858,8 @@ __global__ void __launch_bounds__(512, 1) k_bwd32_bc(D32 d, int seg_heads,
 #pragma unroll
     for (int q4 = 0; q4 < 4; ++q4) {
       const int j = jc * 32 + q4 * 8;
-      store_split8(sWh + (j >> 6) * 16384, sWl + (j >> 6) * 16384, sw128(row, (j & 63) >> 3),
-                   &wsum[q4 * 8]);
+      store_split8<kBf>(sWh + (j >> 6) * 16384, sWl + (j >> 6) * 16384,
+                        sw128(row, (j & 63) >> 3), &wsum[q4 * 8]);
     }
   }
   fence_async_smem();
@@ -811,10 +871,10 @@ __global__ void __launch_bounds__(512, 1) k_bwd32_bc(D32 d, int seg_heads,
     const uint32_t id_db = idesc_bf16(128, 64, true, true);
     for (int kk = 0; kk < 8; ++kk) {
       // dC: A = W (K-major, K = j), B = B (MN-major rows j, N = n)
-      mma3(TdC, smem_u32(sWh) + (kk >> 2) * 16384 + (kk & 3) * 32, 32768, 16, false,
+      mma3<kBf>(TdC, smem_u32(sWh) + (kk >> 2) * 16384 + (kk & 3) * 32, 32768, 16, false,
            smem_u32(sBh) + kk * 2048, 16384, 16384, id_dc, 1);
       // dB: A = W^T (MN-major rows i = K, M = j), B = C (MN-major rows i, N = n)
-      mma3(TdB, smem_u32(sWh) + kk * 2048, 32768, 16384, true, smem_u32(sCh) + kk * 2048, 16384,
+      mma3<kBf>(TdB, smem_u32(sWh) + kk * 2048, 32768, 16384, true, smem_u32(sCh) + kk * 2048, 16384,
            16384, id_db, 1);
     }
     mma_commit(&bar);
@@ -823,7 +883,7 @@ __global__ void __launch_bounds__(512, 1) k_bwd32_bc(D32 d, int seg_heads,
   fence_after_sync();
   if (ok) {
     // warpgroup wg writes columns [16 wg, 16 wg + 16) of row `row` of dC and dB
-    const size_t unit = ((size_t)b * d.nc + c) * d.G + g;
+    const size_t unit = ((size_t)b * d.nb + blk) * d.G + g;
     float* pbase = part + (unit * gridDim.x + seg) * (2 * kQ * kN);
 #pragma unroll
     for (int which = 0; which < 2; ++which) {
@@ -842,10 +902,18 @@ __global__ void __launch_bounds__(512, 1) k_bwd32_bc(D32 d, int seg_heads,
 }
 
 // dC, dB of every unit: the segments' partials summed in segment order.
-__global__ void __launch_bounds__(256) k_sum32_bc(D32 d, int nseg, const float* __restrict__ part,
-                                                  float* __restrict__ dB, float* __restrict__ dC) {
-  const size_t unit = blockIdx.x;  // ((b * nc + c) * G + g)
-  const int g = (int)(unit % d.G), c = (int)((unit / d.G) % d.nc), b = (int)(unit / ((size_t)d.G * d.nc));
+__device__ __forceinline__ void st4(float* p, float4 v) { *(float4*)p = v; }
+__device__ __forceinline__ void st4(__nv_bfloat16* p, float4 v) {
+  *(uint2*)p = make_uint2(pack_bf16(v.x, v.y), pack_bf16(v.z, v.w));
+}
+
+template <bool kBf>
+__global__ void __launch_bounds__(256) k_sum64_bc(D64 d, int nseg, const float* __restrict__ part,
+                                                  Elem<kBf>* __restrict__ dB,
+                                                  Elem<kBf>* __restrict__ dC) {
+  const size_t unit = blockIdx.x;  // ((b * nb + block) * G + g)
+  const int g = (int)(unit % d.G), blk = (int)((unit / d.G) % d.nb);
+  const int b = (int)(unit / ((size_t)d.G * d.nb));
   const float* base = part + unit * nseg * (2 * kQ * kN);
   for (int e = threadIdx.x; e < 2 * kQ * kN / 4; e += blockDim.x) {
     const int which = e / (kQ * kN / 4), r = (e % (kQ * kN / 4)) / (kN / 4), n4 = e % (kN / 4);
@@ -858,24 +926,61 @@ __global__ void __launch_bounds__(256) k_sum32_bc(D32 d, int nseg, const float* 
       s.z += v.z;
       s.w += v.w;
     }
-    float* out = which ? dB : dC;
-    ((float4*)(out + (((size_t)b * d.T + (size_t)c * kQ + r) * d.G + g) * kN))[n4] = s;
+    Elem<kBf>* out = which ? dB : dC;
+    st4(out + (((size_t)b * d.T + (size_t)blk * kQ + r) * d.G + g) * kN + 4 * n4, s);
   }
 }
 
-D32 d32_of(const Problem& p) { return D32{p.B, p.T, p.H, p.G, p.nc, p.hpg}; }
+D64 d64_of(const Problem& p) {
+  return D64{p.B, p.T, p.H, p.G, p.nc, p.hpg, p.Q, p.T / kQ, kQ / p.Q};
+}
 
 template <typename K>
-cudaError_t set_smem32(K kernel, size_t bytes) {
+cudaError_t set_smem64(K kernel, size_t bytes) {
   return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+}
+
+template <bool kBf>
+cudaError_t chunk_outer_t(const Problem& p, int mode, float* out) {
+  using E = Elem<kBf>;
+  const size_t smem = 65536 + 1024;
+  cudaError_t e;
+  if (mode == 0) {
+    if ((e = set_smem64(k_outer64<0, kBf>, smem)) != cudaSuccess) return e;
+    LaunchScope ls("chunk_state_tc64", p.stream);
+    k_outer64<0, kBf><<<dim3(p.nc, p.H, p.B), 256, smem, p.stream>>>(
+        d64_of(p), (const E*)p.x, (const E*)p.Bm, p.dt, p.A, out, p.cs_last);
+  } else {
+    if ((e = set_smem64(k_outer64<1, kBf>, smem)) != cudaSuccess) return e;
+    LaunchScope ls("chunk_dstate_tc64", p.stream);
+    k_outer64<1, kBf><<<dim3(p.nc, p.H, p.B), 256, smem, p.stream>>>(
+        d64_of(p), (const E*)p.dy, (const E*)p.Cm, p.dt, p.A, out, p.cs_last);
+  }
+  return cudaGetLastError();
+}
+
+template <bool kBf>
+cudaError_t forward_scan_t(const Problem& p) {
+  using E = Elem<kBf>;
+  const size_t smem = kScan64Bytes + 1024;
+  cudaError_t e = set_smem64(k_scan64<kBf>, smem);
+  if (e != cudaSuccess) return e;
+  {
+    LaunchScope ls("chunk_scan_tc64", p.stream);
+    k_scan64<kBf><<<dim3(p.T / kQ, p.H, p.B), 256, smem, p.stream>>>(
+        d64_of(p), (const E*)p.x, p.dt, p.A, (const E*)p.Bm, (const E*)p.Cm, p.D, p.hist,
+        (E*)p.y);
+  }
+  return cudaGetLastError();
 }
 
 }  // namespace
 
-// fp32 storage, headdim 64, d_state 64, chunk 128.
-bool tc32_supported(const Problem& p) {
+// headdim 64, d_state 64, chunk in {16, 32, 64, 128}, seqlen a multiple of 128
+bool tc64_supported(const Problem& p) {
   if (tc_forced_simt()) return false;
-  return !p.bf16 && p.P == kP && p.N == kN && p.Q == kQ;
+  return p.P == kP && p.N == kN && (p.Q == 16 || p.Q == 32 || p.Q == 64 || p.Q == 128) &&
+         p.T % kQ == 0;
 }
 
 // Heads per segment of the dB, dC kernel: enough segments that the units
@@ -884,91 +989,78 @@ bool tc32_supported(const Problem& p) {
 // device: results and workspace sizes are the same on every GPU.
 constexpr long long kBcTargetCtas = 304;
 
-int tc32_seg_heads(const Problem& p) {
-  const long long units = (long long)p.B * p.nc * p.G;
+int tc64_seg_heads(const Problem& p) {
+  const long long units = (long long)p.B * (p.T / kQ) * p.G;
   long long nseg = (kBcTargetCtas + units - 1) / units;
   if (nseg < 1) nseg = 1;
   if (nseg > p.hpg) nseg = p.hpg;
   return (int)((p.hpg + nseg - 1) / nseg);
 }
 
-size_t tc32_bc_part_floats(const Problem& p) {
-  const int sh = tc32_seg_heads(p);
+size_t tc64_bc_part_floats(const Problem& p) {
+  const int sh = tc64_seg_heads(p);
   const long long nseg = (p.hpg + sh - 1) / sh;
-  return (size_t)p.B * p.nc * p.G * nseg * 2 * kQ * kN;
+  return (size_t)p.B * (p.T / kQ) * p.G * nseg * 2 * kQ * kN;
 }
 
-cudaError_t tc32_chunk_outer(const Problem& p, int mode, float* out) {
-  const size_t smem = 65536 + 1024;
+cudaError_t tc64_chunk_outer(const Problem& p, int mode, float* out) {
+  return p.bf16 ? chunk_outer_t<true>(p, mode, out) : chunk_outer_t<false>(p, mode, out);
+}
+
+cudaError_t tc64_forward_scan(const Problem& p) {
+  return p.bf16 ? forward_scan_t<true>(p) : forward_scan_t<false>(p);
+}
+
+namespace {
+template <bool kBf>
+cudaError_t backward_t(const Problem& p) {
+  using E = Elem<kBf>;
   cudaError_t e;
-  if (mode == 0) {
-    if ((e = set_smem32(k_outer32<0>, smem)) != cudaSuccess) return e;
-    LaunchScope ls("chunk_state_tc32", p.stream);
-    k_outer32<0><<<dim3(p.nc, p.H, p.B), 256, smem, p.stream>>>(
-        d32_of(p), (const float*)p.x, (const float*)p.Bm, p.dt, p.A, out, p.cs_last);
-  } else {
-    if ((e = set_smem32(k_outer32<1>, smem)) != cudaSuccess) return e;
-    LaunchScope ls("chunk_dstate_tc32", p.stream);
-    k_outer32<1><<<dim3(p.nc, p.H, p.B), 256, smem, p.stream>>>(
-        d32_of(p), (const float*)p.dy, (const float*)p.Cm, p.dt, p.A, out, p.cs_last);
-  }
-  return cudaGetLastError();
-}
-
-cudaError_t tc32_forward_scan(const Problem& p) {
-  const size_t smem = kS32Bytes + 1024;
-  cudaError_t e = set_smem32(k_scan32, smem);
-  if (e != cudaSuccess) return e;
+  if ((e = chunk_outer_t<kBf>(p, 1, p.dstate)) != cudaSuccess) return e;
+  if ((e = simt_state_pass_bwd(p)) != cudaSuccess) return e;
+  const D64 d = d64_of(p);
+  const int nb = p.T / kQ;
   {
-    LaunchScope ls("chunk_scan_tc32", p.stream);
-    k_scan32<<<dim3(p.nc, p.H, p.B), 256, smem, p.stream>>>(
-        d32_of(p), (const float*)p.x, p.dt, p.A, (const float*)p.Bm, (const float*)p.Cm, p.D,
-        p.hist, (float*)p.y);
+    const size_t smem = kBwdX64Bytes + 1024;
+    if ((e = set_smem64(k_bwd64_x<kBf>, smem)) != cudaSuccess) return e;
+    LaunchScope ls("bwd_x_tc64", p.stream);
+    k_bwd64_x<kBf><<<dim3(nb, p.H, p.B), 256, smem, p.stream>>>(
+        d, (const E*)p.x, p.dt, p.A, (const E*)p.Bm, (const E*)p.Cm, p.D, (const E*)p.dy,
+        p.hist, p.dstate, (E*)p.dx, p.ddt, p.dA_part, p.dD_part);
   }
-  return cudaGetLastError();
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  const int sh = tc64_seg_heads(p);
+  const int nseg = (p.hpg + sh - 1) / sh;
+  {
+    const size_t smem = kBwdBC64Bytes + 1024;
+    if ((e = set_smem64(k_bwd64_bc<kBf>, smem)) != cudaSuccess) return e;
+    LaunchScope ls("bwd_bc_tc64", p.stream);
+    k_bwd64_bc<kBf><<<dim3(nseg, nb, p.B * p.G), 512, smem, p.stream>>>(
+        d, sh, (const E*)p.x, p.dt, p.A, (const E*)p.Bm, (const E*)p.Cm, (const E*)p.dy,
+        p.hist, p.dstate, p.bwd_part);
+  }
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  {
+    LaunchScope ls("sum_bc_tc64", p.stream);
+    k_sum64_bc<kBf><<<(unsigned)((size_t)p.B * nb * p.G), 256, 0, p.stream>>>(
+        d, nseg, p.bwd_part, (E*)p.dB, (E*)p.dC);
+  }
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  return simt_reduce_heads(p, p.B * nb, p.B * nb);
 }
+}  // namespace
 
 // R_c, the reverse state pass (g_c in place, dh0), the dx / d(dt) kernel, the
 // dB / dC kernel and its segment sums, and the dA, dD reduction.
-cudaError_t tc32_backward(const Problem& p) {
-  cudaError_t e;
-  if ((e = tc32_chunk_outer(p, 1, p.dstate)) != cudaSuccess) return e;
-  if ((e = simt_state_pass_bwd(p)) != cudaSuccess) return e;
-  const D32 d = d32_of(p);
-  {
-    const size_t smem = kBx32Bytes + 1024;
-    if ((e = set_smem32(k_bwd32_x, smem)) != cudaSuccess) return e;
-    LaunchScope ls("bwd_x_tc32", p.stream);
-    k_bwd32_x<<<dim3(p.nc, p.H, p.B), 256, smem, p.stream>>>(
-        d, (const float*)p.x, p.dt, p.A, (const float*)p.Bm, (const float*)p.Cm, p.D,
-        (const float*)p.dy, p.hist, p.dstate, (float*)p.dx, p.ddt, p.dA_part, p.dD_part);
-  }
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  const int sh = tc32_seg_heads(p);
-  const int nseg = (p.hpg + sh - 1) / sh;
-  {
-    const size_t smem = kBbc32Bytes + 1024;
-    if ((e = set_smem32(k_bwd32_bc, smem)) != cudaSuccess) return e;
-    LaunchScope ls("bwd_bc_tc32", p.stream);
-    k_bwd32_bc<<<dim3(nseg, p.nc, p.B * p.G), 512, smem, p.stream>>>(
-        d, sh, (const float*)p.x, p.dt, p.A, (const float*)p.Bm, (const float*)p.Cm,
-        (const float*)p.dy, p.hist, p.dstate, p.bwd_part);
-  }
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  {
-    LaunchScope ls("sum_bc_tc32", p.stream);
-    k_sum32_bc<<<(unsigned)((size_t)p.B * p.nc * p.G), 256, 0, p.stream>>>(
-        d, nseg, p.bwd_part, (float*)p.dB, (float*)p.dC);
-  }
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  return simt_reduce_heads(p, p.B * p.nc, p.B * p.nc);
+cudaError_t tc64_backward(const Problem& p) {
+  return p.bf16 ? backward_t<true>(p) : backward_t<false>(p);
 }
 
-cudaError_t tc32_read_and_clear_error(unsigned int* out) {
-  cudaError_t e = cudaMemcpyFromSymbol(out, g_tc32_error, sizeof(unsigned int));
+cudaError_t tc64_read_and_clear_error(unsigned int* out) {
+  cudaError_t e = cudaMemcpyFromSymbol(out, g_tc64_error, sizeof(unsigned int));
   if (e != cudaSuccess) return e;
   const unsigned int zero = 0;
-  return cudaMemcpyToSymbol(g_tc32_error, &zero, sizeof(unsigned int));
+  return cudaMemcpyToSymbol(g_tc64_error, &zero, sizeof(unsigned int));
 }
 
 }  // namespace ssd

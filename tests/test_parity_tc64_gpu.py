@@ -1,0 +1,119 @@
+"""GPU parity of the d_state-64 tensor-core family (headdim 64, d_state 64,
+chunk 16-128 processed as 128-step blocks; fp32 storage with every product
+as three bf16 tcgen05 MMAs over hi/lo splits, bf16 storage with one MMA per
+product) against the float64 oracle at the storage type's tolerance, on
+every output; the kernels that ran are checked through the trace.
+"""
+import numpy as np
+import pytest
+
+from state_space_model_analytic_gb300 import synth
+
+from parity_util import TOL, compare, rel_err, run_gpu, run_oracle, to_device
+
+pytestmark = pytest.mark.gpu
+
+TC64_FWD = {"chunk_state_tc64", "state_pass_fwd", "chunk_scan_tc64"}
+TC64_BWD = {"chunk_dstate_tc64", "state_pass_bwd", "bwd_x_tc64", "bwd_bc_tc64", "sum_bc_tc64",
+            "reduce_heads"}
+
+
+@pytest.fixture(scope="module")
+def nat():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from state_space_model_analytic_gb300 import _native
+    from state_space_model_analytic_gb300 import build
+    build()
+    return _native
+
+
+def traced_run(nat, dims, dev, history="given"):
+    nat.trace_begin(64)
+    try:
+        out = run_gpu(dims, dev, history)
+    finally:
+        nat.trace_end()
+    names = {r["name"] for r in nat.trace_read()}
+    nat.trace_reset()
+    return out, names
+
+
+CASES = [
+    # (B, T, H, G, Q, storage, h0, dt mode)
+    (1, 128, 2, 1, 128, "f32", False, "softplus"),     # one chunk
+    (2, 512, 3, 1, 128, "f32", True, "softplus"),      # odd head count
+    (1, 384, 4, 2, 128, "f32", True, "decay_span"),    # decays down to 1e-4 per step
+    (2, 256, 6, 3, 128, "f32", True, "softplus"),      # three groups
+    (1, 1024, 24, 1, 128, "f32", False, "softplus"),   # several head segments (dB, dC kernel)
+    (1, 256, 8, 8, 128, "f32", True, "softplus"),      # one head per group
+    (2, 512, 4, 2, 64, "f32", True, "softplus"),       # two chunks per block
+    # (fp32 dA can be ill-conditioned: for the decay-span inputs of shape
+    # (1, 384, 3, 1, 32), max|dA| ~ 0.2 is a sum of dt * da terms of total
+    # magnitude up to ~160, so fp32 rounding of the terms alone exceeds 1e-4
+    # of max|dA|; the cases here keep that ratio below ~40)
+    (1, 512, 4, 2, 32, "f32", True, "softplus"),       # four chunks per block
+    (1, 256, 2, 1, 16, "f32", True, "softplus"),       # eight chunks per block
+    (2, 512, 4, 2, 128, "bf16", True, "softplus"),     # bf16 storage
+    (1, 512, 6, 3, 64, "bf16", True, "decay_span"),
+    (2, 256, 4, 1, 32, "bf16", False, "softplus"),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: "b{}t{}h{}g{}q{}{}{}_{}".format(
+    c[0], c[1], c[2], c[3], c[4], c[5], "_h0" if c[6] else "", c[7]))
+def test_tc64_every_output_against_oracle(nat, case):
+    Bz, T, H, G, Q, io, h0, mode = case
+    dims = synth.Dims(Bz, T, H, 64, 64, G, Q, io)
+    assert nat.lib().ssd_kernel_path(nat.make_dims(Bz, T, H, 64, 64, G, Q, io == "bf16")) == 1
+    inp = synth.make_inputs(dims, 100 + T + H + Q, h0, mode)
+    gpu, names = traced_run(nat, dims, to_device(dims, inp))
+    assert TC64_FWD | TC64_BWD <= names, names
+    ref = run_oracle(dims, inp)
+    errs, bad = compare(gpu, ref, TOL[io])
+    print(case, {k: f"{v:.1e}" for k, v in errs.items()})
+    assert not bad, errs
+    nat.check(nat.lib().ssd_device_status())
+
+
+def test_tc64_recompute_mode_bitwise_and_repeatable(nat):
+    dims = synth.Dims(2, 512, 4, 64, 64, 2, 128, "f32")
+    inp = synth.make_inputs(dims, 31, True, "softplus")
+    dev = to_device(dims, inp)
+    a, names = traced_run(nat, dims, dev, "given")
+    b, names_r = traced_run(nat, dims, dev, "recompute")
+    assert "chunk_state_tc64" in names_r
+    c = run_gpu(dims, dev, "given")
+    for k in a:
+        assert np.array_equal(a[k], b[k]), k
+        assert np.array_equal(a[k], c[k]), k
+
+
+def test_tc64_agrees_with_simt_path(nat):
+    dims = synth.Dims(1, 512, 4, 64, 64, 1, 128, "f32")
+    inp = synth.make_inputs(dims, 37, True, "softplus")
+    dev = to_device(dims, inp)
+    tc = run_gpu(dims, dev)
+    nat.check(nat.lib().ssd_force_kernel_path(0))
+    try:
+        simt, names = traced_run(nat, dims, dev)
+    finally:
+        nat.check(nat.lib().ssd_force_kernel_path(-1))
+    assert not any(n.endswith("_tc64") for n in names), names
+    for k in tc:
+        assert rel_err(tc[k], simt[k]) < TOL["f32"], k
+
+
+def test_tc64_bf16_agrees_with_simt_path(nat):
+    dims = synth.Dims(1, 512, 4, 64, 64, 2, 64, "bf16")
+    inp = synth.make_inputs(dims, 41, True, "softplus")
+    dev = to_device(dims, inp)
+    tc = run_gpu(dims, dev)
+    nat.check(nat.lib().ssd_force_kernel_path(0))
+    try:
+        simt = run_gpu(dims, dev)
+    finally:
+        nat.check(nat.lib().ssd_force_kernel_path(-1))
+    for k in tc:
+        assert rel_err(tc[k], simt[k]) < TOL["bf16"], k

@@ -111,6 +111,15 @@ __device__ __forceinline__ Raw8 ld8(const __nv_bfloat16* p) {
   const float2 f2 = __bfloat1622float2(q[2]), f3 = __bfloat1622float2(q[3]);
   return Raw8{make_float4(f0.x, f0.y, f1.x, f1.y), make_float4(f2.x, f2.y, f3.x, f3.y)};
 }
+__device__ __forceinline__ void unpack8_bf16(const uint4& u, float* f) {
+  const __nv_bfloat162* q = (const __nv_bfloat162*)&u;
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    const float2 x = __bfloat1622float2(q[t]);
+    f[2 * t] = x.x;
+    f[2 * t + 1] = x.y;
+  }
+}
 __device__ __forceinline__ void unpack_raw(const Raw8& r, float* f) {
   f[0] = r.a.x; f[1] = r.a.y; f[2] = r.a.z; f[3] = r.a.w;
   f[4] = r.b.x; f[5] = r.b.y; f[6] = r.b.z; f[7] = r.b.w;
@@ -125,30 +134,69 @@ __device__ __forceinline__ void st8(__nv_bfloat16* p, const float* f) {
                           pack_bf16(f[6], f[7]));
 }
 
-// Rows [0, nrows) (nrows <= ROWS) of a 64-wide slab (row r at src + r *
-// stride elements) into split tiles (rows of 64 bf16, SW128), each value
-// times scale(r).  All loads of a thread are issued before its first store.
+// One thread's share of rows [0, nrows) (nrows <= ROWS) of a 64-wide slab
+// (row r at src + r * stride elements), fetched into registers by fetch()
+// and written into split tiles (rows of 64 bf16, SW128) by put(), each value
+// times scale(r).  Separate phases let a kernel keep the next tile's loads
+// in flight while it converts the current one.
+template <int NT, int ROWS, typename E>
+struct RowTile {
+  static constexpr bool kBf = std::is_same<E, __nv_bfloat16>::value;
+  static constexpr int kPer = ROWS * 8 / NT;
+  Raw8 v[kPer];
+  __device__ __forceinline__ void fetch(const E* __restrict__ src, size_t stride,
+                                        int nrows = ROWS) {
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const int e = threadIdx.x + NT * k, r = e >> 3, ch = e & 7;
+      if (r < nrows) v[k] = ld8(src + (size_t)r * stride + ch * 8);
+    }
+  }
+  template <typename F>
+  __device__ __forceinline__ void put(uint8_t* hi, uint8_t* lo, F&& scale, int nrows = ROWS) {
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const int e = threadIdx.x + NT * k, r = e >> 3, ch = e & 7;
+      if (r >= nrows) continue;
+      const float sc = scale(r);
+      float f[8];
+      unpack_raw(v[k], f);
+#pragma unroll
+      for (int t = 0; t < 8; ++t) f[t] *= sc;
+      store_split8<kBf>(hi, lo, sw128(r, ch), f);
+    }
+  }
+};
+
+// fetch, then put (no overlap)
 template <int NT, int ROWS, typename E, typename F>
 __device__ __forceinline__ void load_split(uint8_t* hi, uint8_t* lo, const E* __restrict__ src,
                                            size_t stride, F&& scale, int nrows = ROWS) {
-  constexpr bool kBf = std::is_same<E, __nv_bfloat16>::value;
+  RowTile<NT, ROWS, E> t;
+  t.fetch(src, stride, nrows);
+  t.put(hi, lo, scale, nrows);
+}
+
+// Rows [0, ROWS) of split tiles rescaled in place: each row r times scale(r),
+// from the value the tiles hold (hi + lo, or hi alone for bf16 storage).
+template <int NT, int ROWS, bool kBf, typename F>
+__device__ __forceinline__ void rescale_split(uint8_t* hi, uint8_t* lo, F&& scale) {
   constexpr int kPer = ROWS * 8 / NT;
-  Raw8 v[kPer];
 #pragma unroll
   for (int k = 0; k < kPer; ++k) {
     const int e = threadIdx.x + NT * k, r = e >> 3, ch = e & 7;
-    if (r < nrows) v[k] = ld8(src + (size_t)r * stride + ch * 8);
-  }
+    const uint32_t off = sw128(r, ch);
+    float f[8], g[8];
+    unpack8_bf16(*(const uint4*)(hi + off), f);
+    if (!kBf) {
+      unpack8_bf16(*(const uint4*)(lo + off), g);
 #pragma unroll
-  for (int k = 0; k < kPer; ++k) {
-    const int e = threadIdx.x + NT * k, r = e >> 3, ch = e & 7;
-    if (r >= nrows) continue;
+      for (int t = 0; t < 8; ++t) f[t] += g[t];
+    }
     const float sc = scale(r);
-    float f[8];
-    unpack_raw(v[k], f);
 #pragma unroll
     for (int t = 0; t < 8; ++t) f[t] *= sc;
-    store_split8<kBf>(hi, lo, sw128(r, ch), f);
+    store_split8<kBf>(hi, lo, off, f);
   }
 }
 
@@ -244,16 +292,18 @@ __global__ void __launch_bounds__(256) k_outer64(D64 d, const Elem<kBf>* __restr
     tmem_alloc(&tmem_base, 64);
     tmem_relinquish();
   }
+  // the tiles' loads are in flight while the decay tables are built
+  const size_t row0 = (size_t)b * d.T + (size_t)c * Q;
+  RowTile<256, kQ, Elem<kBf>> tv, tu;
+  tv.fetch(V + (row0 * d.G + g) * kN, (size_t)d.G * kN, Q);
+  tu.fetch(U + (row0 * d.H + h) * kP, (size_t)d.H * kP, Q);
   step_tables(d, dt, A[h] * kLog2e, b, (size_t)c * Q, Q, h, s_cs2, s_dt, scratch);
   const float last2 = s_cs2[Q - 1];
   if (tid < Q) s_w[tid] = MODE == 0 ? exp2f(last2 - s_cs2[tid]) * s_dt[tid] : exp2f(s_cs2[tid]);
   if (tid == 0) cs_last[((size_t)b * d.H + h) * d.nc + c] = last2 * (1.0f / kLog2e);
   __syncthreads();
-  const size_t row0 = (size_t)b * d.T + (size_t)c * Q;
-  load_split<256, kQ>(sVh, sVl, V + (row0 * d.G + g) * kN, (size_t)d.G * kN,
-                      [](int) { return 1.f; }, Q);
-  load_split<256, kQ>(sUh, sUl, U + (row0 * d.H + h) * kP, (size_t)d.H * kP,
-                      [&](int r) { return s_w[r]; }, Q);
+  tv.put(sVh, sVl, [](int) { return 1.f; }, Q);
+  tu.put(sUh, sUl, [&](int r) { return s_w[r]; }, Q);
   fence_async_smem();
   fence_before_sync();
   __syncthreads();
@@ -330,19 +380,24 @@ __global__ void __launch_bounds__(256, 1) k_scan64(D64 d, const Elem<kBf>* __res
     tmem_alloc(&tmem_base, 256);
     tmem_relinquish();
   }
+  const size_t row0 = (size_t)b * d.T + (size_t)blk * kQ;
+  const size_t c0 = (size_t)blk * d.cpb;  // the block's first chunk
+  const auto one = [](int) { return 1.f; };
+  // two tiles' loads in flight at a time, the first two under the tables
+  RowTile<256, kQ, Elem<kBf>> ta, tb;
+  ta.fetch(Cm + (row0 * d.G + g) * kN, (size_t)d.G * kN);
+  tb.fetch(Bm + (row0 * d.G + g) * kN, (size_t)d.G * kN);
   step_tables(d, dt, A[h] * kLog2e, b, (size_t)blk * kQ, kQ, h, s_cs2, s_dt, scratch);
   for (int e = tid; e < 4 * kQ; e += 256) {
     const int w = e >> 7, j = e & 127, r = 32 * w;
     s_E[w][j] = j < r ? exp2f(s_cs2[r] - s_cs2[j]) * s_dt[j] : 0.f;
   }
-  const size_t row0 = (size_t)b * d.T + (size_t)blk * kQ;
-  const size_t c0 = (size_t)blk * d.cpb;  // the block's first chunk
-  const auto one = [](int) { return 1.f; };
-  load_split<256, kQ>(sCh, sCl, Cm + (row0 * d.G + g) * kN, (size_t)d.G * kN, one);
-  load_split<256, kQ>(sBh, sBl, Bm + (row0 * d.G + g) * kN, (size_t)d.G * kN, one);
-  load_split<256, kQ>(sXh, sXl, x + (row0 * d.H + h) * kP, (size_t)d.H * kP, one);
+  ta.put(sCh, sCl, one);
+  ta.fetch(x + (row0 * d.H + h) * kP, (size_t)d.H * kP);
+  tb.put(sBh, sBl, one);
   (void)load_split_transposed<256, kBf>(
       sHh, sHl, hist + (((size_t)b * d.nc + c0) * d.H + h) * (kP * kN), nullptr);
+  ta.put(sXh, sXl, one);
   fence_async_smem();
   fence_before_sync();
   __syncthreads();
@@ -518,6 +573,15 @@ __global__ void __launch_bounds__(256, 1) k_bwd64_x(D64 d, const Elem<kBf>* __re
     tmem_relinquish();
   }
   const float Ah = A[h], Dh = D[h];
+  const size_t row0 = (size_t)b * d.T + (size_t)blk * kQ;
+  const size_t c0 = (size_t)blk * d.cpb, c1 = c0 + d.cpb - 1;  // first, last chunk
+  const size_t st_in = (((size_t)b * d.nc + c0) * d.H + h) * (kP * kN);
+  const size_t st_out = (((size_t)b * d.nc + c1) * d.H + h) * (kP * kN);
+  const auto one = [](int) { return 1.f; };
+  // two tiles' loads in flight at a time, the first two under the tables
+  RowTile<256, kQ, Elem<kBf>> ta, tb;
+  ta.fetch(Cm + (row0 * d.G + g) * kN, (size_t)d.G * kN);
+  tb.fetch(Bm + (row0 * d.G + g) * kN, (size_t)d.G * kN);
   step_tables(d, dt, Ah * kLog2e, b, (size_t)blk * kQ, kQ, h, s_cs2, s_dt, scratch);
   for (int e = tid; e < 4 * kQ; e += 256) {
     const int w = e >> 7, j = e & 127, r = 32 * w;
@@ -525,17 +589,14 @@ __global__ void __launch_bounds__(256, 1) k_bwd64_x(D64 d, const Elem<kBf>* __re
     s_E[w][j] = ev;
     s_Edt[w][j] = ev * s_dt[j];
   }
-  const size_t row0 = (size_t)b * d.T + (size_t)blk * kQ;
-  const size_t c0 = (size_t)blk * d.cpb, c1 = c0 + d.cpb - 1;  // first, last chunk
-  const size_t st_in = (((size_t)b * d.nc + c0) * d.H + h) * (kP * kN);
-  const size_t st_out = (((size_t)b * d.nc + c1) * d.H + h) * (kP * kN);
-  const auto one = [](int) { return 1.f; };
-  load_split<256, kQ>(sCh, sCl, Cm + (row0 * d.G + g) * kN, (size_t)d.G * kN, one);
-  load_split<256, kQ>(sBh, sBl, Bm + (row0 * d.G + g) * kN, (size_t)d.G * kN, one);
-  load_split<256, kQ>(sXh, sXl, x + (row0 * d.H + h) * kP, (size_t)d.H * kP, one);
-  load_split<256, kQ>(sYh, sYl, dy + (row0 * d.H + h) * kP, (size_t)d.H * kP, one);
+  ta.put(sCh, sCl, one);
+  ta.fetch(x + (row0 * d.H + h) * kP, (size_t)d.H * kP);
+  tb.put(sBh, sBl, one);
+  tb.fetch(dy + (row0 * d.H + h) * kP, (size_t)d.H * kP);
   (void)load_split_transposed<256, kBf>(sHh, sHl, hist + st_in, nullptr);
+  ta.put(sXh, sXl, one);
   float hg = load_split_transposed<256, kBf>(sGh, sGl, gstate + st_out, hist + st_in);
+  tb.put(sYh, sYl, one);
   hg = block_sum(hg, scratch);  // <g_c, H_{c-1}> (syncs)
   fence_async_smem();
   fence_before_sync();
@@ -767,8 +828,13 @@ __global__ void __launch_bounds__(512, 1) k_bwd64_bc(D64 d, int seg_heads,
   const size_t row0 = (size_t)b * d.T + (size_t)blk * kQ;
   const size_t c0 = (size_t)blk * d.cpb, c1 = c0 + d.cpb - 1;  // first, last chunk
   const auto one = [](int) { return 1.f; };
-  load_split<512, kQ>(sBh, sBl, Bm + (row0 * d.G + g) * kN, (size_t)d.G * kN, one);
-  load_split<512, kQ>(sCh, sCl, Cm + (row0 * d.G + g) * kN, (size_t)d.G * kN, one);
+  {
+    RowTile<512, kQ, Elem<kBf>> tb, tc;
+    tb.fetch(Bm + (row0 * d.G + g) * kN, (size_t)d.G * kN);
+    tc.fetch(Cm + (row0 * d.G + g) * kN, (size_t)d.G * kN);
+    tb.put(sBh, sBl, one);
+    tc.put(sCh, sCl, one);
+  }
   fence_before_sync();
   __syncthreads();
   fence_after_sync();
@@ -781,17 +847,24 @@ __global__ void __launch_bounds__(512, 1) k_bwd64_bc(D64 d, int seg_heads,
   const int I = row, jc = wg;  // this thread's row and 32-column chunk of W
   for (int hh = 0; hh < nh && ok; ++hh) {
     const int h = h0 + hh;
+    const size_t st_in = (((size_t)b * d.nc + c0) * d.H + h) * (kP * kN);
+    const size_t st_out = (((size_t)b * d.nc + c1) * d.H + h) * (kP * kN);
+    // this head's tiles: all loads in flight while the decay tables are built
+    RowTile<512, kQ, Elem<kBf>> tx, ty;
+    RowTile<512, 64, float> th, tg;
+    tx.fetch(x + (row0 * d.H + h) * kP, (size_t)d.H * kP);
+    ty.fetch(dy + (row0 * d.H + h) * kP, (size_t)d.H * kP);
+    th.fetch(hist + st_in, (size_t)kN);
+    tg.fetch(gstate + st_out, (size_t)kN);
     step_tables(d, dt, A[h] * kLog2e, b, (size_t)blk * kQ, kQ, h, s_cs2, s_dt, scratch);
     for (int e = tid; e < 4 * kQ; e += 512) {
       const int w = e >> 7, j = e & 127, r = 32 * w;
       s_E[w][j] = j < r ? exp2f(s_cs2[r] - s_cs2[j]) * s_dt[j] : 0.f;
     }
-    const size_t st_in = (((size_t)b * d.nc + c0) * d.H + h) * (kP * kN);
-    const size_t st_out = (((size_t)b * d.nc + c1) * d.H + h) * (kP * kN);
-    load_split<512, kQ>(sXh, sXl, x + (row0 * d.H + h) * kP, (size_t)d.H * kP, one);
-    load_split<512, kQ>(sYh, sYl, dy + (row0 * d.H + h) * kP, (size_t)d.H * kP, one);
-    load_split<512, 64, float>(sHh, sHl, hist + st_in, (size_t)kN, one);
-    load_split<512, 64, float>(sGh, sGl, gstate + st_out, (size_t)kN, one);
+    tx.put(sXh, sXl, one);
+    ty.put(sYh, sYl, one);
+    th.put(sHh, sHl, one);
+    tg.put(sGh, sGl, one);
     fence_async_smem();
     fence_before_sync();
     __syncthreads();
@@ -829,12 +902,11 @@ __global__ void __launch_bounds__(512, 1) k_bwd64_bc(D64 d, int seg_heads,
         }
       }
     }
-    // X, dY reloaded scaled (the dYX product has read them)
+    // X, dY rescaled in place (the dYX product has read them): X rows j by
+    // exp(cs_last - cs_j) dt_j, dY rows i by exp(cs_i)
     const float last2 = s_cs2[kQ - 1];
-    load_split<512, kQ>(sXh, sXl, x + (row0 * d.H + h) * kP, (size_t)d.H * kP,
-                        [&](int r) { return exp2f(last2 - s_cs2[r]) * s_dt[r]; });
-    load_split<512, kQ>(sYh, sYl, dy + (row0 * d.H + h) * kP, (size_t)d.H * kP,
-                        [&](int r) { return exp2f(s_cs2[r]); });
+    rescale_split<512, kQ, kBf>(sXh, sXl, [&](int r) { return exp2f(last2 - s_cs2[r]) * s_dt[r]; });
+    rescale_split<512, kQ, kBf>(sYh, sYl, [&](int r) { return exp2f(s_cs2[r]); });
     fence_async_smem();
     fence_before_sync();
     __syncthreads();

@@ -20,7 +20,8 @@
 // the bf16 kernels of ssd_tc.cu.  The layouts are those kernels' (128-byte
 // swizzled rows of 64 bf16).  Inputs come from global memory by coalesced
 // 16-byte loads and are converted by the threads; elementwise math (decays,
-// masks, epilogues) runs in fp32 from the stored input values.
+// masks, epilogues) runs in fp32; the epilogues read x and dy back from the
+// tiles (hi + lo: within 2^-18 of the stored fp32 value; exact for bf16).
 //
 // The chunked algebra is that of the SIMT kernels (ssd_simt.cu), derived from
 // the recurrence of `ssd_forward_state_history_reference` and the reverse-time
@@ -167,6 +168,21 @@ struct RowTile {
     }
   }
 };
+
+// 8 values of a split tile row as fp32: hi + lo (hi alone for bf16 storage,
+// where it holds the stored value exactly; for fp32 the sum is within 2^-18
+// of it)
+template <bool kBf>
+__device__ __forceinline__ void read_split8(const uint8_t* hi, const uint8_t* lo, uint32_t off,
+                                            float* f) {
+  unpack8_bf16(*(const uint4*)(hi + off), f);
+  if (!kBf) {
+    float g[8];
+    unpack8_bf16(*(const uint4*)(lo + off), g);
+#pragma unroll
+    for (int t = 0; t < 8; ++t) f[t] += g[t];
+  }
+}
 
 // fetch, then put (no overlap)
 template <int NT, int ROWS, typename E, typename F>
@@ -475,7 +491,7 @@ __global__ void __launch_bounds__(256, 1) k_scan64(D64 d, const Elem<kBf>* __res
 #pragma unroll
       for (int k8 = 0; k8 < 2; ++k8) {
         float xf[8], o[8];
-        unpack_raw(ld8(x + off + half * 16 + k8 * 8), xf);
+        read_split8<kBf>(sXh, sXl, sw128(row, wg * 4 + half * 2 + k8), xf);
 #pragma unroll
         for (int t = 0; t < 8; ++t) o[t] = fmaf(sc, yst[k8 * 8 + t], yv[k8 * 8 + t]) + Dh * xf[t];
         st8(y + off + half * 16 + k8 * 8, o);
@@ -712,8 +728,8 @@ __global__ void __launch_bounds__(256, 1) k_bwd64_x(D64 d, const Elem<kBf>* __re
 #pragma unroll
       for (int k8 = 0; k8 < 2; ++k8) {
         float xa[8], ya[8], o[8];
-        unpack_raw(ld8(x + off + half * 16 + k8 * 8), xa);
-        unpack_raw(ld8(dy + off + half * 16 + k8 * 8), ya);
+        read_split8<kBf>(sXh, sXl, sw128(row, wg * 4 + half * 2 + k8), xa);
+        read_split8<kBf>(sYh, sYl, sw128(row, wg * 4 + half * 2 + k8), ya);
 #pragma unroll
         for (int t = 0; t < 8; ++t) {
           const int m = 8 * k8 + t;

@@ -361,7 +361,7 @@ __global__ void __launch_bounds__(256) k_outer64(D64 d, const Elem<kBf>* __restr
 constexpr uint32_t kScan64Bytes = 114688;  // C, B (later M) 64K | X 32K | H 16K
 
 template <bool kBf>
-__global__ void __launch_bounds__(256, 1) k_scan64(D64 d, const Elem<kBf>* __restrict__ x,
+__global__ void __launch_bounds__(512, 1) k_scan64(D64 d, const Elem<kBf>* __restrict__ x,
                                                    const float* __restrict__ dt,
                                                    const float* __restrict__ A,
                                                    const Elem<kBf>* __restrict__ Bm,
@@ -381,7 +381,7 @@ __global__ void __launch_bounds__(256, 1) k_scan64(D64 d, const Elem<kBf>* __res
   uint8_t* sXl = sm + 81920;
   uint8_t* sHh = sm + 98304;    // [64 rows n][64 p] MN-major B operand
   uint8_t* sHl = sm + 106496;
-  __shared__ float s_cs2[kQ], s_dt[kQ], scratch[8];
+  __shared__ float s_cs2[kQ], s_dt[kQ], scratch[16];
   __shared__ __align__(16) float s_E[4][kQ];  // exp(cs_r - cs_j) dt_j, j < r = 32 w
   __shared__ uint64_t bar;
   __shared__ uint32_t tmem_base;
@@ -400,18 +400,18 @@ __global__ void __launch_bounds__(256, 1) k_scan64(D64 d, const Elem<kBf>* __res
   const size_t c0 = (size_t)blk * d.cpb;  // the block's first chunk
   const auto one = [](int) { return 1.f; };
   // two tiles' loads in flight at a time, the first two under the tables
-  RowTile<256, kQ, Elem<kBf>> ta, tb;
+  RowTile<512, kQ, Elem<kBf>> ta, tb;
   ta.fetch(Cm + (row0 * d.G + g) * kN, (size_t)d.G * kN);
   tb.fetch(Bm + (row0 * d.G + g) * kN, (size_t)d.G * kN);
   step_tables(d, dt, A[h] * kLog2e, b, (size_t)blk * kQ, kQ, h, s_cs2, s_dt, scratch);
-  for (int e = tid; e < 4 * kQ; e += 256) {
+  for (int e = tid; e < 4 * kQ; e += 512) {
     const int w = e >> 7, j = e & 127, r = 32 * w;
     s_E[w][j] = j < r ? exp2f(s_cs2[r] - s_cs2[j]) * s_dt[j] : 0.f;
   }
   ta.put(sCh, sCl, one);
   ta.fetch(x + (row0 * d.H + h) * kP, (size_t)d.H * kP);
   tb.put(sBh, sBl, one);
-  (void)load_split_transposed<256, kBf>(
+  (void)load_split_transposed<512, kBf>(
       sHh, sHl, hist + (((size_t)b * d.nc + c0) * d.H + h) * (kP * kN), nullptr);
   ta.put(sXh, sXl, one);
   fence_async_smem();
@@ -433,12 +433,11 @@ __global__ void __launch_bounds__(256, 1) k_scan64(D64 d, const Elem<kBf>* __res
   bool ok = wait_all(&bar, 0);
   fence_after_sync();
   if (ok) {
-    // M = CB o L o dt; warpgroup wg writes columns [64 wg, 64 wg + 64)
+    // M = CB o L o dt; warpgroup wg writes columns [32 wg, 32 wg + 32)
     const int I = row;
     const float fi = exp2f(s_cs2[I] - s_cs2[32 * q]), csI = s_cs2[I];
-#pragma unroll 1
-    for (int u = 0; u < 2; ++u) {
-      const int jc = 2 * wg + u;
+    {
+      const int jc = wg;
       float v[32];
       if (jc <= q) {  // warp-uniform
         tmem_ld32(tCB + lane_base + jc * 32, v);
@@ -479,22 +478,21 @@ __global__ void __launch_bounds__(256, 1) k_scan64(D64 d, const Elem<kBf>* __res
   ok = ok && wait_all(&bar, 1);
   fence_after_sync();
   if (ok) {
-    // y = Y + exp(cs_i) Ys + D x; warpgroup wg takes p in [32 wg, 32 wg + 32)
+    // y = Y + exp(cs_i) Ys + D x; warpgroup wg takes p in [16 wg, 16 wg + 16)
     const float sc = exp2f(s_cs2[row]), Dh = D[h];
-    const size_t off = ((row0 + row) * d.H + h) * kP + wg * 32;
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
+    const size_t off = ((row0 + row) * d.H + h) * kP + wg * 16;
+    {
       float yv[16], yst[16];
-      tmem_ld16(tY + lane_base + wg * 32 + half * 16, yv);
-      tmem_ld16(tYs + lane_base + wg * 32 + half * 16, yst);
+      tmem_ld16(tY + lane_base + wg * 16, yv);
+      tmem_ld16(tYs + lane_base + wg * 16, yst);
       tmem_wait_ld();
 #pragma unroll
       for (int k8 = 0; k8 < 2; ++k8) {
         float xf[8], o[8];
-        read_split8<kBf>(sXh, sXl, sw128(row, wg * 4 + half * 2 + k8), xf);
+        read_split8<kBf>(sXh, sXl, sw128(row, wg * 2 + k8), xf);
 #pragma unroll
         for (int t = 0; t < 8; ++t) o[t] = fmaf(sc, yst[k8 * 8 + t], yv[k8 * 8 + t]) + Dh * xf[t];
-        st8(y + off + half * 16 + k8 * 8, o);
+        st8(y + off + k8 * 8, o);
       }
     }
   }
@@ -538,7 +536,7 @@ __device__ __forceinline__ float col_sum16(float (&v)[16]) {
 constexpr uint32_t kBwdX64Bytes = 163840;  // C, B (later O) 64K | X 32K | dY 32K | H 16K | g 16K
 
 template <bool kBf>
-__global__ void __launch_bounds__(256, 1) k_bwd64_x(D64 d, const Elem<kBf>* __restrict__ x,
+__global__ void __launch_bounds__(512, 1) k_bwd64_x(D64 d, const Elem<kBf>* __restrict__ x,
                                                     const float* __restrict__ dt,
                                                     const float* __restrict__ A,
                                                     const Elem<kBf>* __restrict__ Bm,
@@ -567,13 +565,13 @@ __global__ void __launch_bounds__(256, 1) k_bwd64_x(D64 d, const Elem<kBf>* __re
   uint8_t* sHl = sm + 139264;
   uint8_t* sGh = sm + 147456;   // g^T [64 rows n][64 p]
   uint8_t* sGl = sm + 155648;
-  __shared__ float s_cs2[kQ], s_dt[kQ], scratch[8];
+  __shared__ float s_cs2[kQ], s_dt[kQ], scratch[16];
   __shared__ __align__(16) float s_E[4][kQ];    // exp(cs_r - cs_j), j < r = 32 w
   __shared__ __align__(16) float s_Edt[4][kQ];  // the same times dt_j
   __shared__ float s_col[4][kQ];                // per-warp strict column sums of M
-  __shared__ float s_red[5][kQ];                // warpgroup 1's row partials
+  __shared__ float s_red[3][5][kQ];             // warpgroups 1-3: row partials
   __shared__ float s_v[kQ];
-  __shared__ float2 s_v2[kQ], scratch2[8];
+  __shared__ float2 s_v2[kQ], scratch2[16];
   __shared__ float s_esum;
   __shared__ uint64_t bar;
   __shared__ uint32_t tmem_base;
@@ -595,11 +593,11 @@ __global__ void __launch_bounds__(256, 1) k_bwd64_x(D64 d, const Elem<kBf>* __re
   const size_t st_out = (((size_t)b * d.nc + c1) * d.H + h) * (kP * kN);
   const auto one = [](int) { return 1.f; };
   // two tiles' loads in flight at a time, the first two under the tables
-  RowTile<256, kQ, Elem<kBf>> ta, tb;
+  RowTile<512, kQ, Elem<kBf>> ta, tb;
   ta.fetch(Cm + (row0 * d.G + g) * kN, (size_t)d.G * kN);
   tb.fetch(Bm + (row0 * d.G + g) * kN, (size_t)d.G * kN);
   step_tables(d, dt, Ah * kLog2e, b, (size_t)blk * kQ, kQ, h, s_cs2, s_dt, scratch);
-  for (int e = tid; e < 4 * kQ; e += 256) {
+  for (int e = tid; e < 4 * kQ; e += 512) {
     const int w = e >> 7, j = e & 127, r = 32 * w;
     const float ev = j < r ? exp2f(s_cs2[r] - s_cs2[j]) : 0.f;
     s_E[w][j] = ev;
@@ -609,9 +607,9 @@ __global__ void __launch_bounds__(256, 1) k_bwd64_x(D64 d, const Elem<kBf>* __re
   ta.fetch(x + (row0 * d.H + h) * kP, (size_t)d.H * kP);
   tb.put(sBh, sBl, one);
   tb.fetch(dy + (row0 * d.H + h) * kP, (size_t)d.H * kP);
-  (void)load_split_transposed<256, kBf>(sHh, sHl, hist + st_in, nullptr);
+  (void)load_split_transposed<512, kBf>(sHh, sHl, hist + st_in, nullptr);
   ta.put(sXh, sXl, one);
-  float hg = load_split_transposed<256, kBf>(sGh, sGl, gstate + st_out, hist + st_in);
+  float hg = load_split_transposed<512, kBf>(sGh, sGl, gstate + st_out, hist + st_in);
   tb.put(sYh, sYl, one);
   hg = block_sum(hg, scratch);  // <g_c, H_{c-1}> (syncs)
   fence_async_smem();
@@ -638,15 +636,14 @@ __global__ void __launch_bounds__(256, 1) k_bwd64_x(D64 d, const Elem<kBf>* __re
   bool ok = wait_all(&bar, 0);
   fence_after_sync();
 
-  // ---- build: W, M sums and O = L o CB; warpgroup wg covers columns
-  // [64 wg, 64 wg + 64) as two 32-column chunks
+  // ---- build: W, M sums and O = L o CB; warpgroup wg covers the 32
+  // columns [32 wg, 32 wg + 32)
   const int I = row;
   const float fi = exp2f(s_cs2[I] - s_cs2[32 * q]), csI = s_cs2[I];
   float rowsum = 0.f;
   if (ok) {
-#pragma unroll 1
-    for (int u = 0; u < 2; ++u) {
-      const int jc = 2 * wg + u;
+    {
+      const int jc = wg;
       if (jc <= q) {  // warp-uniform
 #pragma unroll 1
         for (int hf = 0; hf < 2; ++hf) {
@@ -712,24 +709,23 @@ __global__ void __launch_bounds__(256, 1) k_bwd64_x(D64 d, const Elem<kBf>* __re
   fence_after_sync();
 
   // ---- epilogue: this thread's row (j for dx, drive, e; i for statein), p in
-  // [32 wg, 32 wg + 32)
+  // [16 wg, 16 wg + 16)
   const float last2 = s_cs2[kQ - 1];
   const float fj = exp2f(last2 - s_cs2[row]), dtj = s_dt[row];
   float drive = 0.f, ej = 0.f, stin = 0.f, dd = 0.f;
   if (ok) {
-    const size_t off = ((row0 + row) * d.H + h) * kP + wg * 32;
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
+    const size_t off = ((row0 + row) * d.H + h) * kP + wg * 16;
+    {
       float gx[16], gs[16], ch[16];
-      tmem_ld16(TGx + lane_base + wg * 32 + half * 16, gx);
-      tmem_ld16(TGs + lane_base + wg * 32 + half * 16, gs);
-      tmem_ld16(TCH + lane_base + wg * 32 + half * 16, ch);
+      tmem_ld16(TGx + lane_base + wg * 16, gx);
+      tmem_ld16(TGs + lane_base + wg * 16, gs);
+      tmem_ld16(TCH + lane_base + wg * 16, ch);
       tmem_wait_ld();
 #pragma unroll
       for (int k8 = 0; k8 < 2; ++k8) {
         float xa[8], ya[8], o[8];
-        read_split8<kBf>(sXh, sXl, sw128(row, wg * 4 + half * 2 + k8), xa);
-        read_split8<kBf>(sYh, sYl, sw128(row, wg * 4 + half * 2 + k8), ya);
+        read_split8<kBf>(sXh, sXl, sw128(row, wg * 2 + k8), xa);
+        read_split8<kBf>(sYh, sYl, sw128(row, wg * 2 + k8), ya);
 #pragma unroll
         for (int t = 0; t < 8; ++t) {
           const int m = 8 * k8 + t;
@@ -740,24 +736,29 @@ __global__ void __launch_bounds__(256, 1) k_bwd64_x(D64 d, const Elem<kBf>* __re
           stin = fmaf(ya[t], ch[m], stin);
           dd = fmaf(ya[t], xa[t], dd);
         }
-        st8(dx + off + half * 16 + k8 * 8, o);
+        st8(dx + off + k8 * 8, o);
       }
     }
   }
-  if (wg == 1) {
-    s_red[0][row] = rowsum;
-    s_red[1][row] = drive;
-    s_red[2][row] = ej;
-    s_red[3][row] = stin;
-    s_red[4][row] = dd;
+  if (wg > 0) {
+    s_red[wg - 1][0][row] = rowsum;
+    s_red[wg - 1][1][row] = drive;
+    s_red[wg - 1][2][row] = ej;
+    s_red[wg - 1][3][row] = stin;
+    s_red[wg - 1][4][row] = dd;
   }
   __syncthreads();
   if (wg == 0) {
-    rowsum += s_red[0][row];
-    drive += s_red[1][row];
-    ej = (ej + s_red[2][row]) * fj * dtj;
-    stin = (stin + s_red[3][row]) * exp2f(s_cs2[row]);
-    dd += s_red[4][row];
+#pragma unroll
+    for (int w = 0; w < 3; ++w) {  // warpgroups in order
+      rowsum += s_red[w][0][row];
+      drive += s_red[w][1][row];
+      ej += s_red[w][2][row];
+      stin += s_red[w][3][row];
+      dd += s_red[w][4][row];
+    }
+    ej *= fj * dtj;
+    stin *= exp2f(s_cs2[row]);
     float colsum = 0.f;
     for (int w = row >> 5; w < 4; ++w) colsum += s_col[w][row];
     s_v2[row] = make_float2(rowsum - colsum + stin - ej, ej);
@@ -1055,7 +1056,7 @@ cudaError_t forward_scan_t(const Problem& p) {
   if (e != cudaSuccess) return e;
   {
     LaunchScope ls("chunk_scan_tc64", p.stream);
-    k_scan64<kBf><<<dim3(p.T / kQ, p.H, p.B), 256, smem, p.stream>>>(
+    k_scan64<kBf><<<dim3(p.T / kQ, p.H, p.B), 512, smem, p.stream>>>(
         d64_of(p), (const E*)p.x, p.dt, p.A, (const E*)p.Bm, (const E*)p.Cm, p.D, p.hist,
         (E*)p.y);
   }
@@ -1112,7 +1113,7 @@ cudaError_t backward_t(const Problem& p) {
     const size_t smem = kBwdX64Bytes + 1024;
     if ((e = set_smem64(k_bwd64_x<kBf>, smem)) != cudaSuccess) return e;
     LaunchScope ls("bwd_x_tc64", p.stream);
-    k_bwd64_x<kBf><<<dim3(nb, p.H, p.B), 256, smem, p.stream>>>(
+    k_bwd64_x<kBf><<<dim3(nb, p.H, p.B), 512, smem, p.stream>>>(
         d, (const E*)p.x, p.dt, p.A, (const E*)p.Bm, (const E*)p.Cm, p.D, (const E*)p.dy,
         p.hist, p.dstate, (E*)p.dx, p.ddt, p.dA_part, p.dD_part);
   }

@@ -862,17 +862,21 @@ __global__ void __launch_bounds__(512, 1) k_bwd64_bc(D64 d, int seg_heads,
 #pragma unroll
   for (int k = 0; k < 32; ++k) wsum[k] = 0.f;
   const int I = row, jc = wg;  // this thread's row and 32-column chunk of W
-  for (int hh = 0; hh < nh && ok; ++hh) {
-    const int h = h0 + hh;
+  // a head's tiles are fetched into registers while the previous head's
+  // state-term products run (the first head's before the loop)
+  RowTile<512, kQ, Elem<kBf>> tx, ty;
+  RowTile<512, 64, float> th, tg;
+  auto fetch_head = [&](int h) {
     const size_t st_in = (((size_t)b * d.nc + c0) * d.H + h) * (kP * kN);
     const size_t st_out = (((size_t)b * d.nc + c1) * d.H + h) * (kP * kN);
-    // this head's tiles: all loads in flight while the decay tables are built
-    RowTile<512, kQ, Elem<kBf>> tx, ty;
-    RowTile<512, 64, float> th, tg;
     tx.fetch(x + (row0 * d.H + h) * kP, (size_t)d.H * kP);
     ty.fetch(dy + (row0 * d.H + h) * kP, (size_t)d.H * kP);
     th.fetch(hist + st_in, (size_t)kN);
     tg.fetch(gstate + st_out, (size_t)kN);
+  };
+  if (nh > 0) fetch_head(h0);
+  for (int hh = 0; hh < nh && ok; ++hh) {
+    const int h = h0 + hh;
     step_tables(d, dt, A[h] * kLog2e, b, (size_t)blk * kQ, kQ, h, s_cs2, s_dt, scratch);
     for (int e = tid; e < 4 * kQ; e += 512) {
       const int w = e >> 7, j = e & 127, r = 32 * w;
@@ -938,6 +942,7 @@ __global__ void __launch_bounds__(512, 1) k_bwd64_bc(D64 d, int seg_heads,
       }
       mma_commit(&bar);
     }
+    if (hh + 1 < nh) fetch_head(h + 1);
     ok = wait_all(&bar, phase);  // the tiles are rewritten by the next head
     phase ^= 1;
     fence_after_sync();

@@ -49,10 +49,10 @@ CASES = [
     (1, 1024, 24, 1, 128, "f32", False, "softplus"),   # several head segments (dB, dC kernel)
     (1, 256, 8, 8, 128, "f32", True, "softplus"),      # one head per group
     (2, 512, 4, 2, 64, "f32", True, "softplus"),       # two chunks per block
-    # (fp32 dA can be ill-conditioned: for the decay-span inputs of shape
-    # (1, 384, 3, 1, 32), max|dA| ~ 0.2 is a sum of dt * da terms of total
-    # magnitude up to ~160, so fp32 rounding of the terms alone exceeds 1e-4
-    # of max|dA|; the cases here keep that ratio below ~40)
+    # (fp32 dA is a sum with cancellation: on the decay-span inputs of shape
+    # (1, 384, 3, 1, 32), max|dA| ~ 0.2 while its terms total ~160, and dA
+    # measured 2.9e-4 against every other output below 1.5e-5; this case
+    # uses softplus inputs, decay spans stay covered at chunk 128 and 64)
     (1, 512, 4, 2, 32, "f32", True, "softplus"),       # four chunks per block
     (1, 256, 2, 1, 16, "f32", True, "softplus"),       # eight chunks per block
     (2, 512, 4, 2, 128, "bf16", True, "softplus"),     # bf16 storage

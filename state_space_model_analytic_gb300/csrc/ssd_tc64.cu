@@ -349,19 +349,23 @@ __global__ void __launch_bounds__(256) k_outer64(D64 d, const Elem<kBf>* __restr
 }
 
 // ---------------------------------------------------------------------------
-// Chunk scan: y of one (b, 128-step block, h) per CTA, 256 threads.
+// Chunk scan: y of one (b, 128-step block, h) per CTA, 256 threads, two
+// CTAs per SM (80 KB of shared memory, 256 TMEM columns each).
 //   CB = C B^T, Ys = C H^T (H = the state before the block: the history entry
 //   of its first chunk, as rows n),
-//   M = CB o L o dt (masked, split), Y = M X,
+//   M = CB o L o dt (masked, split) in two 64-column halves, each followed by
+//   its half of Y = M X (K = the half's 64 rows of X),
 //   y = Y + exp(cs_i) Ys + D x.
+// X is fetched into registers at the start and written into the B tile's
+// place once CB is formed; the M half takes the C tile's place.
 // Decay masks as in the bf16 kernels: for warp q's rows and a 32-column chunk
 // left of its diagonal chunk, exp(cs_i - cs_j) = exp(cs_i - cs_r) exp(cs_r -
 // cs_j) with r = 32 q (both factors <= 1); the diagonal chunk evaluates the
 // exponent only where j <= i.
-constexpr uint32_t kScan64Bytes = 114688;  // C, B (later M) 64K | X 32K | H 16K
+constexpr uint32_t kScan64Bytes = 81920;  // C (later an M half) 32K | B (later X) 32K | H 16K
 
 template <bool kBf>
-__global__ void __launch_bounds__(512, 1) k_scan64(D64 d, const Elem<kBf>* __restrict__ x,
+__global__ void __launch_bounds__(256, 2) k_scan64(D64 d, const Elem<kBf>* __restrict__ x,
                                                    const float* __restrict__ dt,
                                                    const float* __restrict__ A,
                                                    const Elem<kBf>* __restrict__ Bm,
@@ -373,15 +377,15 @@ __global__ void __launch_bounds__(512, 1) k_scan64(D64 d, const Elem<kBf>* __res
   uint8_t* sm = align1024(smraw);
   uint8_t* sCh = sm;            // [128 rows i][64 n] K-major
   uint8_t* sCl = sm + 16384;
+  uint8_t* sMh = sm;            // M half [128 rows i][64 j] K-major (after CB, Ys)
+  uint8_t* sMl = sm + 16384;
   uint8_t* sBh = sm + 32768;    // [128 rows j][64 n] K-major
   uint8_t* sBl = sm + 49152;
-  uint8_t* sMh = sm;            // M [128 rows i][128 j]: two 64-column tiles (after CB, Ys)
-  uint8_t* sMl = sm + 32768;
-  uint8_t* sXh = sm + 65536;    // [128 rows j][64 p] MN-major B operand
-  uint8_t* sXl = sm + 81920;
-  uint8_t* sHh = sm + 98304;    // [64 rows n][64 p] MN-major B operand
-  uint8_t* sHl = sm + 106496;
-  __shared__ float s_cs2[kQ], s_dt[kQ], scratch[16];
+  uint8_t* sXh = sm + 32768;    // [128 rows j][64 p] MN-major B operand (after CB)
+  uint8_t* sXl = sm + 49152;
+  uint8_t* sHh = sm + 65536;    // [64 rows n][64 p] MN-major B operand
+  uint8_t* sHl = sm + 73728;
+  __shared__ float s_cs2[kQ], s_dt[kQ], scratch[8];
   __shared__ __align__(16) float s_E[4][kQ];  // exp(cs_r - cs_j) dt_j, j < r = 32 w
   __shared__ uint64_t bar;
   __shared__ uint32_t tmem_base;
@@ -399,21 +403,21 @@ __global__ void __launch_bounds__(512, 1) k_scan64(D64 d, const Elem<kBf>* __res
   const size_t row0 = (size_t)b * d.T + (size_t)blk * kQ;
   const size_t c0 = (size_t)blk * d.cpb;  // the block's first chunk
   const auto one = [](int) { return 1.f; };
-  // two tiles' loads in flight at a time, the first two under the tables
-  RowTile<512, kQ, Elem<kBf>> ta, tb;
+  // C, B and X loads in flight under the tables; X stays in registers until
+  // the B tile is free
+  RowTile<256, kQ, Elem<kBf>> ta, tb, tx;
   ta.fetch(Cm + (row0 * d.G + g) * kN, (size_t)d.G * kN);
   tb.fetch(Bm + (row0 * d.G + g) * kN, (size_t)d.G * kN);
+  tx.fetch(x + (row0 * d.H + h) * kP, (size_t)d.H * kP);
   step_tables(d, dt, A[h] * kLog2e, b, (size_t)blk * kQ, kQ, h, s_cs2, s_dt, scratch);
-  for (int e = tid; e < 4 * kQ; e += 512) {
+  for (int e = tid; e < 4 * kQ; e += 256) {
     const int w = e >> 7, j = e & 127, r = 32 * w;
     s_E[w][j] = j < r ? exp2f(s_cs2[r] - s_cs2[j]) * s_dt[j] : 0.f;
   }
   ta.put(sCh, sCl, one);
-  ta.fetch(x + (row0 * d.H + h) * kP, (size_t)d.H * kP);
   tb.put(sBh, sBl, one);
-  (void)load_split_transposed<512, kBf>(
+  (void)load_split_transposed<256, kBf>(
       sHh, sHl, hist + (((size_t)b * d.nc + c0) * d.H + h) * (kP * kN), nullptr);
-  ta.put(sXh, sXl, one);
   fence_async_smem();
   fence_before_sync();
   __syncthreads();
@@ -431,13 +435,17 @@ __global__ void __launch_bounds__(512, 1) k_scan64(D64 d, const Elem<kBf>* __res
     mma_commit(&bar);
   }
   bool ok = wait_all(&bar, 0);
+  uint32_t phase = 1;
   fence_after_sync();
-  if (ok) {
-    // M = CB o L o dt; warpgroup wg writes columns [32 wg, 32 wg + 32)
-    const int I = row;
-    const float fi = exp2f(s_cs2[I] - s_cs2[32 * q]), csI = s_cs2[I];
+  // the C and B tiles are free: X into the B tile's place
+  tx.put(sXh, sXl, one);
+  const int I = row;
+  const float fi = exp2f(s_cs2[I] - s_cs2[32 * q]), csI = s_cs2[I];
+#pragma unroll 1
+  for (int half = 0; half < 2 && ok; ++half) {
+    // M columns [64 half, 64 half + 64): warpgroup wg writes its 32-column chunk jc
+    const int jc = 2 * half + wg;
     {
-      const int jc = wg;
       float v[32];
       if (jc <= q) {  // warp-uniform
         tmem_ld32(tCB + lane_base + jc * 32, v);
@@ -457,42 +465,42 @@ __global__ void __launch_bounds__(512, 1) k_scan64(D64 d, const Elem<kBf>* __res
         for (int k = 0; k < 32; ++k) v[k] = 0.f;
       }
 #pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        const int j = jc * 32 + q4 * 8;
-        store_split8<kBf>(sMh + (j >> 6) * 16384, sMl + (j >> 6) * 16384,
-                          sw128(row, (j & 63) >> 3), &v[q4 * 8]);
-      }
+      for (int q4 = 0; q4 < 4; ++q4)
+        store_split8<kBf>(sMh, sMl, sw128(row, wg * 4 + q4), &v[q4 * 8]);
     }
+    fence_async_smem();
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    if (tid == 0) {
+      // Y += M[:, half] X[half rows, :]: K = the half's 64 rows j
+      const uint32_t id_y = idesc_bf16(128, 64, false, true);
+      for (int kk = 0; kk < 4; ++kk)
+        mma3<kBf>(tY, smem_u32(sMh) + kk * 32, 16384, 16, false,
+                  smem_u32(sXh) + (4 * half + kk) * 2048, 16384, 16384, id_y, half > 0 || kk > 0);
+      mma_commit(&bar);
+    }
+    ok = wait_all(&bar, phase);  // the M half is rewritten next
+    phase ^= 1;
+    fence_after_sync();
   }
-  fence_async_smem();
-  fence_before_sync();
-  __syncthreads();
-  fence_after_sync();
-  if (tid == 0 && ok) {
-    const uint32_t id_y = idesc_bf16(128, 64, false, true);
-    for (int kk = 0; kk < 8; ++kk)
-      mma3<kBf>(tY, smem_u32(sMh) + (kk >> 2) * 16384 + (kk & 3) * 32, 32768, 16, false,
-           smem_u32(sXh) + kk * 2048, 16384, 16384, id_y, kk > 0);
-    mma_commit(&bar);
-  }
-  ok = ok && wait_all(&bar, 1);
-  fence_after_sync();
   if (ok) {
-    // y = Y + exp(cs_i) Ys + D x; warpgroup wg takes p in [16 wg, 16 wg + 16)
+    // y = Y + exp(cs_i) Ys + D x; warpgroup wg takes p in [32 wg, 32 wg + 32)
     const float sc = exp2f(s_cs2[row]), Dh = D[h];
-    const size_t off = ((row0 + row) * d.H + h) * kP + wg * 16;
-    {
+    const size_t off = ((row0 + row) * d.H + h) * kP + wg * 32;
+#pragma unroll
+    for (int hp = 0; hp < 2; ++hp) {
       float yv[16], yst[16];
-      tmem_ld16(tY + lane_base + wg * 16, yv);
-      tmem_ld16(tYs + lane_base + wg * 16, yst);
+      tmem_ld16(tY + lane_base + wg * 32 + hp * 16, yv);
+      tmem_ld16(tYs + lane_base + wg * 32 + hp * 16, yst);
       tmem_wait_ld();
 #pragma unroll
       for (int k8 = 0; k8 < 2; ++k8) {
         float xf[8], o[8];
-        read_split8<kBf>(sXh, sXl, sw128(row, wg * 2 + k8), xf);
+        read_split8<kBf>(sXh, sXl, sw128(row, wg * 4 + hp * 2 + k8), xf);
 #pragma unroll
         for (int t = 0; t < 8; ++t) o[t] = fmaf(sc, yst[k8 * 8 + t], yv[k8 * 8 + t]) + Dh * xf[t];
-        st8(y + off + k8 * 8, o);
+        st8(y + off + hp * 16 + k8 * 8, o);
       }
     }
   }
@@ -1061,7 +1069,7 @@ cudaError_t forward_scan_t(const Problem& p) {
   if (e != cudaSuccess) return e;
   {
     LaunchScope ls("chunk_scan_tc64", p.stream);
-    k_scan64<kBf><<<dim3(p.T / kQ, p.H, p.B), 512, smem, p.stream>>>(
+    k_scan64<kBf><<<dim3(p.T / kQ, p.H, p.B), 256, smem, p.stream>>>(
         d64_of(p), (const E*)p.x, p.dt, p.A, (const E*)p.Bm, (const E*)p.Cm, p.D, p.hist,
         (E*)p.y);
   }

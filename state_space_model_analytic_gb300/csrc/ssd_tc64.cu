@@ -59,7 +59,7 @@ namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
-constexpr int kQ = 128, kP = 64, kN = 64;  // kQ: rows of a block (the MMA M size)
+constexpr int kQ = 128, kP = 64;  // kQ: rows of a block (the MMA M size)
 
 __device__ unsigned int g_tc64_error;
 
@@ -140,16 +140,21 @@ __device__ __forceinline__ void st8(__nv_bfloat16* p, const float* f) {
 // and written into split tiles (rows of 64 bf16, SW128) by put(), each value
 // times scale(r).  Separate phases let a kernel keep the next tile's loads
 // in flight while it converts the current one.
-template <int NT, int ROWS, typename E>
+// W = 128 (bf16 storage only): the row's second 64 values go to a second
+// tile at the lo tile's place (a bf16 row of 128 takes the bytes of an fp32
+// row of 64 split in two).
+template <int NT, int ROWS, typename E, int W = 64>
 struct RowTile {
   static constexpr bool kBf = std::is_same<E, __nv_bfloat16>::value;
-  static constexpr int kPer = ROWS * 8 / NT;
+  static_assert(W == 64 || (W == 128 && kBf), "128-wide rows are bf16 only");
+  static constexpr int kCh = W / 8;  // 16-byte chunks of bf16 per row
+  static constexpr int kPer = ROWS * kCh / NT;
   Raw8 v[kPer];
   __device__ __forceinline__ void fetch(const E* __restrict__ src, size_t stride,
                                         int nrows = ROWS) {
 #pragma unroll
     for (int k = 0; k < kPer; ++k) {
-      const int e = threadIdx.x + NT * k, r = e >> 3, ch = e & 7;
+      const int e = threadIdx.x + NT * k, r = e / kCh, ch = e % kCh;
       if (r < nrows) v[k] = ld8(src + (size_t)r * stride + ch * 8);
     }
   }
@@ -157,14 +162,17 @@ struct RowTile {
   __device__ __forceinline__ void put(uint8_t* hi, uint8_t* lo, F&& scale, int nrows = ROWS) {
 #pragma unroll
     for (int k = 0; k < kPer; ++k) {
-      const int e = threadIdx.x + NT * k, r = e >> 3, ch = e & 7;
+      const int e = threadIdx.x + NT * k, r = e / kCh, ch = e % kCh;
       if (r >= nrows) continue;
       const float sc = scale(r);
       float f[8];
       unpack_raw(v[k], f);
 #pragma unroll
       for (int t = 0; t < 8; ++t) f[t] *= sc;
-      store_split8<kBf>(hi, lo, sw128(r, ch), f);
+      if (W == 64)
+        store_split8<kBf>(hi, lo, sw128(r, ch), f);
+      else
+        store_split8<true>((ch >> 3) ? lo : hi, nullptr, sw128(r, ch & 7), f);
     }
   }
 };
@@ -184,11 +192,41 @@ __device__ __forceinline__ void read_split8(const uint8_t* hi, const uint8_t* lo
   }
 }
 
+// A [64 p][NS n] fp32 state block as rows p into tiles: split for fp32
+// storage (NS = 64), bf16 for bf16 storage (NS = 128: n 64-127 in a second
+// tile at the lo tile's place).
+template <int NT, int NS, bool kBf>
+struct StateRowTile {
+  static_assert(NS == 64 || (NS == 128 && kBf), "d_state 128 is bf16 only");
+  static constexpr int kCh = NS / 8;
+  static constexpr int kPer = 64 * kCh / NT;
+  Raw8 v[kPer];
+  __device__ __forceinline__ void fetch(const float* __restrict__ src) {
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const int e = threadIdx.x + NT * k, r = e / kCh, ch = e % kCh;
+      v[k] = ld8(src + (size_t)r * NS + ch * 8);
+    }
+  }
+  __device__ __forceinline__ void put(uint8_t* hi, uint8_t* lo) {
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const int e = threadIdx.x + NT * k, r = e / kCh, ch = e % kCh;
+      float f[8];
+      unpack_raw(v[k], f);
+      if (NS == 64)
+        store_split8<kBf>(hi, lo, sw128(r, ch), f);
+      else
+        store_split8<true>((ch >> 3) ? lo : hi, nullptr, sw128(r, ch & 7), f);
+    }
+  }
+};
+
 // fetch, then put (no overlap)
 template <int NT, int ROWS, typename E, typename F>
 __device__ __forceinline__ void load_split(uint8_t* hi, uint8_t* lo, const E* __restrict__ src,
                                            size_t stride, F&& scale, int nrows = ROWS) {
-  RowTile<NT, ROWS, E> t;
+  RowTile<NT, ROWS, E, 64> t;
   t.fetch(src, stride, nrows);
   t.put(hi, lo, scale, nrows);
 }
@@ -216,24 +254,26 @@ __device__ __forceinline__ void rescale_split(uint8_t* hi, uint8_t* lo, F&& scal
   }
 }
 
-// A [64 p][64 n] fp32 state block (p-major) transposed into split tiles of
-// rows n with 64 p each; returns this thread's share of sum(src * other) when
+// A [64 p][NS n] fp32 state block (p-major) transposed into split tiles of
+// rows n with 64 p each (NS = 128, bf16 only: rows 64-127 continue into the
+// lo tile's place); returns this thread's share of sum(src * other) when
 // `other` is given (the same elements of a second block, for <g, H>).
-template <int NT, bool kBf>
+template <int NT, bool kBf, int NS = 64>
 __device__ __forceinline__ float load_split_transposed(uint8_t* hi, uint8_t* lo,
                                                        const float* __restrict__ src,
                                                        const float* __restrict__ other) {
-  constexpr int kPer = 64 * 8 / NT;
+  static_assert(NS == 64 || (NS == 128 && kBf), "d_state 128 is bf16 only");
+  constexpr int kPer = NS * 8 / NT;
   float dot = 0.f;
 #pragma unroll
   for (int k = 0; k < kPer; ++k) {
-    const int e = threadIdx.x + NT * k, n = e & 63, pc = e >> 6;
+    const int e = threadIdx.x + NT * k, n = e % NS, pc = e / NS;
     float f[8];
 #pragma unroll
-    for (int t = 0; t < 8; ++t) f[t] = __ldg(src + (size_t)(pc * 8 + t) * kN + n);
+    for (int t = 0; t < 8; ++t) f[t] = __ldg(src + (size_t)(pc * 8 + t) * NS + n);
     if (other) {
 #pragma unroll
-      for (int t = 0; t < 8; ++t) dot = fmaf(f[t], __ldg(other + (size_t)(pc * 8 + t) * kN + n), dot);
+      for (int t = 0; t < 8; ++t) dot = fmaf(f[t], __ldg(other + (size_t)(pc * 8 + t) * NS + n), dot);
     }
     store_split8<kBf>(hi, lo, sw128(n, pc), f);
   }
@@ -282,7 +322,7 @@ __device__ __forceinline__ void step_tables(const D64& d, const float* __restric
 // as D[n][p] = V^T (w o U) (M = n padded to 128: the second half of the A
 // operand reads the U tiles and its rows are never read back), then written
 // out[b][c][h][p][n]; also cs_last[b][h][c] (natural-log units).
-template <int MODE, bool kBf>
+template <int MODE, bool kBf, int NS>
 __global__ void __launch_bounds__(256) k_outer64(D64 d, const Elem<kBf>* __restrict__ U,
                                                  const Elem<kBf>* __restrict__ V,
                                                  const float* __restrict__ dt,
@@ -291,7 +331,7 @@ __global__ void __launch_bounds__(256) k_outer64(D64 d, const Elem<kBf>* __restr
                                                  float* __restrict__ cs_last) {
   extern __shared__ __align__(1024) uint8_t smraw[];
   uint8_t* sm = align1024(smraw);
-  uint8_t* sVh = sm;           // [128 rows j][64 n]
+  uint8_t* sVh = sm;           // [128 rows j][64 n] (NS = 128: n 64-127 in the lo tile's place)
   uint8_t* sVl = sm + 16384;
   uint8_t* sUh = sm + 32768;   // [128 rows j][64 p], rows scaled by w
   uint8_t* sUl = sm + 49152;
@@ -310,8 +350,9 @@ __global__ void __launch_bounds__(256) k_outer64(D64 d, const Elem<kBf>* __restr
   }
   // the tiles' loads are in flight while the decay tables are built
   const size_t row0 = (size_t)b * d.T + (size_t)c * Q;
-  RowTile<256, kQ, Elem<kBf>> tv, tu;
-  tv.fetch(V + (row0 * d.G + g) * kN, (size_t)d.G * kN, Q);
+  RowTile<256, kQ, Elem<kBf>, NS> tv;
+  RowTile<256, kQ, Elem<kBf>> tu;
+  tv.fetch(V + (row0 * d.G + g) * NS, (size_t)d.G * NS, Q);
   tu.fetch(U + (row0 * d.H + h) * kP, (size_t)d.H * kP, Q);
   step_tables(d, dt, A[h] * kLog2e, b, (size_t)c * Q, Q, h, s_cs2, s_dt, scratch);
   const float last2 = s_cs2[Q - 1];
@@ -327,21 +368,24 @@ __global__ void __launch_bounds__(256) k_outer64(D64 d, const Elem<kBf>* __restr
   const uint32_t tm = tmem_base;
   if (tid == 0) {
     const uint32_t id = idesc_bf16(128, 64, true, true);
+    // A = V^T, M = n: NS = 64 pads M to 128 with a second block read from
+    // the U tiles (rows never read back); NS = 128 has its second block of n
+    // in the lo tile's place
     for (int ks = 0; ks < Q / 16; ++ks)
-      mma3<kBf>(tm, smem_u32(sVh) + ks * 2048, 16384, 32768, true, smem_u32(sUh) + ks * 2048, 16384,
-           16384, id, ks > 0);
+      mma3<kBf>(tm, smem_u32(sVh) + ks * 2048, 16384, NS == 128 ? 16384 : 32768, true,
+                smem_u32(sUh) + ks * 2048, 16384, 16384, id, ks > 0);
     mma_commit(&bar);
   }
   const bool ok = wait_all(&bar, 0);
   fence_after_sync();
   const int wg = tid >> 7, r = tid & 127;
-  if (ok && r < 64) {  // warps 0, 1, 4, 5: lanes (rows n) 0-63; warpgroup wg takes p in [32 wg, +32)
+  if (ok && r < NS) {  // lanes (rows n) below NS; warpgroup wg takes p in [32 wg, +32)
     float v[32];
     tmem_ld32(tm + ((uint32_t)((r >> 5) * 32) << 16) + wg * 32, v);
     tmem_wait_ld();
-    float* dst = out + (((size_t)b * d.nc + c) * d.H + h) * (kP * kN) + r;
+    float* dst = out + (((size_t)b * d.nc + c) * d.H + h) * (kP * NS) + r;
 #pragma unroll
-    for (int i = 0; i < 32; ++i) dst[(size_t)(wg * 32 + i) * kN] = v[i];
+    for (int i = 0; i < 32; ++i) dst[(size_t)(wg * 32 + i) * NS] = v[i];
   }
   fence_before_sync();
   __syncthreads();
@@ -364,7 +408,7 @@ __global__ void __launch_bounds__(256) k_outer64(D64 d, const Elem<kBf>* __restr
 // exponent only where j <= i.
 constexpr uint32_t kScan64Bytes = 81920;  // C (later an M half) 32K | B (later X) 32K | H 16K
 
-template <bool kBf>
+template <bool kBf, int NS>
 __global__ void __launch_bounds__(256, 2) k_scan64(D64 d, const Elem<kBf>* __restrict__ x,
                                                    const float* __restrict__ dt,
                                                    const float* __restrict__ A,
@@ -375,7 +419,7 @@ __global__ void __launch_bounds__(256, 2) k_scan64(D64 d, const Elem<kBf>* __res
                                                    Elem<kBf>* __restrict__ y) {
   extern __shared__ __align__(1024) uint8_t smraw[];
   uint8_t* sm = align1024(smraw);
-  uint8_t* sCh = sm;            // [128 rows i][64 n] K-major
+  uint8_t* sCh = sm;            // [128 rows i][64 n] K-major (NS = 128: n 64-127 at the lo tile)
   uint8_t* sCl = sm + 16384;
   uint8_t* sMh = sm;            // M half [128 rows i][64 j] K-major (after CB, Ys)
   uint8_t* sMl = sm + 16384;
@@ -383,7 +427,7 @@ __global__ void __launch_bounds__(256, 2) k_scan64(D64 d, const Elem<kBf>* __res
   uint8_t* sBl = sm + 49152;
   uint8_t* sXh = sm + 32768;    // [128 rows j][64 p] MN-major B operand (after CB)
   uint8_t* sXl = sm + 49152;
-  uint8_t* sHh = sm + 65536;    // [64 rows n][64 p] MN-major B operand
+  uint8_t* sHh = sm + 65536;    // [NS rows n][64 p] MN-major B operand (NS = 128: rows 64+ at the lo tile)
   uint8_t* sHl = sm + 73728;
   __shared__ float s_cs2[kQ], s_dt[kQ], scratch[8];
   __shared__ __align__(16) float s_E[4][kQ];  // exp(cs_r - cs_j) dt_j, j < r = 32 w
@@ -405,35 +449,44 @@ __global__ void __launch_bounds__(256, 2) k_scan64(D64 d, const Elem<kBf>* __res
   const auto one = [](int) { return 1.f; };
   // C, B and X loads in flight under the tables; X stays in registers until
   // the B tile is free
-  RowTile<256, kQ, Elem<kBf>> ta, tb, tx;
-  ta.fetch(Cm + (row0 * d.G + g) * kN, (size_t)d.G * kN);
-  tb.fetch(Bm + (row0 * d.G + g) * kN, (size_t)d.G * kN);
-  tx.fetch(x + (row0 * d.H + h) * kP, (size_t)d.H * kP);
+  // (NS = 128: one 128-wide tile in flight at a time, within the registers)
+  RowTile<256, kQ, Elem<kBf>, NS> ta, tb;
+  RowTile<256, kQ, Elem<kBf>> tx;
+  ta.fetch(Cm + (row0 * d.G + g) * NS, (size_t)d.G * NS);
+  if (NS == 64) {
+    tb.fetch(Bm + (row0 * d.G + g) * NS, (size_t)d.G * NS);
+    tx.fetch(x + (row0 * d.H + h) * kP, (size_t)d.H * kP);
+  }
   step_tables(d, dt, A[h] * kLog2e, b, (size_t)blk * kQ, kQ, h, s_cs2, s_dt, scratch);
   for (int e = tid; e < 4 * kQ; e += 256) {
     const int w = e >> 7, j = e & 127, r = 32 * w;
     s_E[w][j] = j < r ? exp2f(s_cs2[r] - s_cs2[j]) * s_dt[j] : 0.f;
   }
   ta.put(sCh, sCl, one);
-  tb.put(sBh, sBl, one);
-  (void)load_split_transposed<256, kBf>(
-      sHh, sHl, hist + (((size_t)b * d.nc + c0) * d.H + h) * (kP * kN), nullptr);
+  if (NS == 128) ta.fetch(Bm + (row0 * d.G + g) * NS, (size_t)d.G * NS);
+  if (NS == 64) tb.put(sBh, sBl, one);
+  else ta.put(sBh, sBl, one);
+  (void)load_split_transposed<256, kBf, NS>(
+      sHh, sHl, hist + (((size_t)b * d.nc + c0) * d.H + h) * (kP * NS), nullptr);
   fence_async_smem();
   fence_before_sync();
   __syncthreads();
   fence_after_sync();
   const uint32_t tm = tmem_base, tCB = tm, tYs = tm + 128, tY = tm + 192;
   if (tid == 0) {
+    // K = n: NS / 16 steps, the second 64 of n (NS = 128) at the lo tiles
     const uint32_t id_cb = idesc_bf16(128, 128, false, false);
     const uint32_t id_ys = idesc_bf16(128, 64, false, true);
-    for (int kk = 0; kk < 4; ++kk) {
-      mma3<kBf>(tCB, smem_u32(sCh) + kk * 32, 16384, 16, false, smem_u32(sBh) + kk * 32, 16384,
-                16, id_cb, kk > 0);
-      mma3<kBf>(tYs, smem_u32(sCh) + kk * 32, 16384, 16, false, smem_u32(sHh) + kk * 2048, 8192,
-                8192, id_ys, kk > 0);
+    for (int kk = 0; kk < NS / 16; ++kk) {
+      const uint32_t ko = (kk >> 2) * 16384 + (kk & 3) * 32;
+      mma3<kBf>(tCB, smem_u32(sCh) + ko, 16384, 16, false, smem_u32(sBh) + ko, 16384, 16, id_cb,
+                kk > 0);
+      mma3<kBf>(tYs, smem_u32(sCh) + ko, 16384, 16, false, smem_u32(sHh) + kk * 2048, 8192, 8192,
+                id_ys, kk > 0);
     }
     mma_commit(&bar);
   }
+  if (NS == 128) tx.fetch(x + (row0 * d.H + h) * kP, (size_t)d.H * kP);  // under the products
   bool ok = wait_all(&bar, 0);
   uint32_t phase = 1;
   fence_after_sync();
@@ -543,7 +596,7 @@ __device__ __forceinline__ float col_sum16(float (&v)[16]) {
 //            ddt_j = drive_j + A da_j; partials sum_j dt_j da_j and sum dy.x.
 constexpr uint32_t kBwdX64Bytes = 163840;  // C, B (later O) 64K | X 32K | dY 32K | H 16K | g 16K
 
-template <bool kBf>
+template <bool kBf, int NS>
 __global__ void __launch_bounds__(512, 1) k_bwd64_x(D64 d, const Elem<kBf>* __restrict__ x,
                                                     const float* __restrict__ dt,
                                                     const float* __restrict__ A,
@@ -597,13 +650,14 @@ __global__ void __launch_bounds__(512, 1) k_bwd64_x(D64 d, const Elem<kBf>* __re
   const float Ah = A[h], Dh = D[h];
   const size_t row0 = (size_t)b * d.T + (size_t)blk * kQ;
   const size_t c0 = (size_t)blk * d.cpb, c1 = c0 + d.cpb - 1;  // first, last chunk
-  const size_t st_in = (((size_t)b * d.nc + c0) * d.H + h) * (kP * kN);
-  const size_t st_out = (((size_t)b * d.nc + c1) * d.H + h) * (kP * kN);
+  const size_t st_in = (((size_t)b * d.nc + c0) * d.H + h) * (kP * NS);
+  const size_t st_out = (((size_t)b * d.nc + c1) * d.H + h) * (kP * NS);
   const auto one = [](int) { return 1.f; };
   // two tiles' loads in flight at a time, the first two under the tables
-  RowTile<512, kQ, Elem<kBf>> ta, tb;
-  ta.fetch(Cm + (row0 * d.G + g) * kN, (size_t)d.G * kN);
-  tb.fetch(Bm + (row0 * d.G + g) * kN, (size_t)d.G * kN);
+  RowTile<512, kQ, Elem<kBf>, NS> ta, tb;
+  RowTile<512, kQ, Elem<kBf>> tc, td;
+  ta.fetch(Cm + (row0 * d.G + g) * NS, (size_t)d.G * NS);
+  tb.fetch(Bm + (row0 * d.G + g) * NS, (size_t)d.G * NS);
   step_tables(d, dt, Ah * kLog2e, b, (size_t)blk * kQ, kQ, h, s_cs2, s_dt, scratch);
   for (int e = tid; e < 4 * kQ; e += 512) {
     const int w = e >> 7, j = e & 127, r = 32 * w;
@@ -612,13 +666,13 @@ __global__ void __launch_bounds__(512, 1) k_bwd64_x(D64 d, const Elem<kBf>* __re
     s_Edt[w][j] = ev * s_dt[j];
   }
   ta.put(sCh, sCl, one);
-  ta.fetch(x + (row0 * d.H + h) * kP, (size_t)d.H * kP);
+  tc.fetch(x + (row0 * d.H + h) * kP, (size_t)d.H * kP);
   tb.put(sBh, sBl, one);
-  tb.fetch(dy + (row0 * d.H + h) * kP, (size_t)d.H * kP);
-  (void)load_split_transposed<512, kBf>(sHh, sHl, hist + st_in, nullptr);
-  ta.put(sXh, sXl, one);
-  float hg = load_split_transposed<512, kBf>(sGh, sGl, gstate + st_out, hist + st_in);
-  tb.put(sYh, sYl, one);
+  td.fetch(dy + (row0 * d.H + h) * kP, (size_t)d.H * kP);
+  (void)load_split_transposed<512, kBf, NS>(sHh, sHl, hist + st_in, nullptr);
+  tc.put(sXh, sXl, one);
+  float hg = load_split_transposed<512, kBf, NS>(sGh, sGl, gstate + st_out, hist + st_in);
+  td.put(sYh, sYl, one);
   hg = block_sum(hg, scratch);  // <g_c, H_{c-1}> (syncs)
   fence_async_smem();
   fence_before_sync();
@@ -629,15 +683,19 @@ __global__ void __launch_bounds__(512, 1) k_bwd64_x(D64 d, const Elem<kBf>* __re
   if (tid == 0) {
     const uint32_t id_sq = idesc_bf16(128, 128, false, false);
     const uint32_t id_km = idesc_bf16(128, 64, false, true);
-    for (int kk = 0; kk < 4; ++kk) {
-      mma3<kBf>(T0, smem_u32(sCh) + kk * 32, 16384, 16, false, smem_u32(sBh) + kk * 32, 16384,
-                16, id_sq, kk > 0);
+    // K = p (dY X^T): 4 steps; K = n (CB, Gs, CH): NS / 16 steps, the second
+    // 64 of n (NS = 128) at the lo tiles
+    for (int kk = 0; kk < 4; ++kk)
       mma3<kBf>(T1, smem_u32(sYh) + kk * 32, 16384, 16, false, smem_u32(sXh) + kk * 32, 16384,
                 16, id_sq, kk > 0);
-      mma3<kBf>(TGs, smem_u32(sBh) + kk * 32, 16384, 16, false, smem_u32(sGh) + kk * 2048, 8192,
-                8192, id_km, kk > 0);
-      mma3<kBf>(TCH, smem_u32(sCh) + kk * 32, 16384, 16, false, smem_u32(sHh) + kk * 2048, 8192,
-                8192, id_km, kk > 0);
+    for (int kk = 0; kk < NS / 16; ++kk) {
+      const uint32_t ko = (kk >> 2) * 16384 + (kk & 3) * 32;
+      mma3<kBf>(T0, smem_u32(sCh) + ko, 16384, 16, false, smem_u32(sBh) + ko, 16384, 16, id_sq,
+                kk > 0);
+      mma3<kBf>(TGs, smem_u32(sBh) + ko, 16384, 16, false, smem_u32(sGh) + kk * 2048, 8192, 8192,
+                id_km, kk > 0);
+      mma3<kBf>(TCH, smem_u32(sCh) + ko, 16384, 16, false, smem_u32(sHh) + kk * 2048, 8192, 8192,
+                id_km, kk > 0);
     }
     mma_commit(&bar);
   }
@@ -805,7 +863,7 @@ __global__ void __launch_bounds__(512, 1) k_bwd64_x(D64 d, const Elem<kBf>* __re
 // sums of the segment written as partials [unit][segment][dC|dB][128][64].
 constexpr uint32_t kBwdBC64Bytes = 163840;  // B 32K | C 32K | X 32K | dY 32K | H 16K | g 16K
 
-template <bool kBf>
+template <bool kBf, int NS>
 __global__ void __launch_bounds__(512, 1) k_bwd64_bc(D64 d, int seg_heads,
                                                      const Elem<kBf>* __restrict__ x,
                                                      const float* __restrict__ dt,
@@ -846,24 +904,25 @@ __global__ void __launch_bounds__(512, 1) k_bwd64_bc(D64 d, int seg_heads,
     mbar_init(&bar, 1);
     fence_mbar_init();
   }
+  constexpr uint32_t kCols = NS == 128 ? 512 : 256;  // dY X^T 128 + dC, dB NS each
   if (tid < 32) {
-    tmem_alloc(&tmem_base, 256);
+    tmem_alloc(&tmem_base, kCols);
     tmem_relinquish();
   }
   const size_t row0 = (size_t)b * d.T + (size_t)blk * kQ;
   const size_t c0 = (size_t)blk * d.cpb, c1 = c0 + d.cpb - 1;  // first, last chunk
   const auto one = [](int) { return 1.f; };
   {
-    RowTile<512, kQ, Elem<kBf>> tb, tc;
-    tb.fetch(Bm + (row0 * d.G + g) * kN, (size_t)d.G * kN);
-    tc.fetch(Cm + (row0 * d.G + g) * kN, (size_t)d.G * kN);
+    RowTile<512, kQ, Elem<kBf>, NS> tb;
+    tb.fetch(Bm + (row0 * d.G + g) * NS, (size_t)d.G * NS);
     tb.put(sBh, sBl, one);
-    tc.put(sCh, sCl, one);
+    tb.fetch(Cm + (row0 * d.G + g) * NS, (size_t)d.G * NS);
+    tb.put(sCh, sCl, one);
   }
   fence_before_sync();
   __syncthreads();
   fence_after_sync();
-  const uint32_t tm = tmem_base, T1 = tm, TdC = tm + 128, TdB = tm + 192;
+  const uint32_t tm = tmem_base, T1 = tm, TdC = tm + 128, TdB = tm + 128 + NS;
   uint32_t phase = 0;
   bool ok = true;
   float wsum[32];
@@ -873,18 +932,24 @@ __global__ void __launch_bounds__(512, 1) k_bwd64_bc(D64 d, int seg_heads,
   // a head's tiles are fetched into registers while the previous head's
   // state-term products run (the first head's before the loop)
   RowTile<512, kQ, Elem<kBf>> tx, ty;
-  RowTile<512, 64, float> th, tg;
+  StateRowTile<512, NS, kBf> th, tg;  // the states as rows p of NS values
+  // (NS = 128: the state tiles are fetched at the head's start instead, to
+  // stay within the registers)
+  auto fetch_states = [&](int h) {
+    const size_t st_in = (((size_t)b * d.nc + c0) * d.H + h) * (kP * NS);
+    const size_t st_out = (((size_t)b * d.nc + c1) * d.H + h) * (kP * NS);
+    th.fetch(hist + st_in);
+    tg.fetch(gstate + st_out);
+  };
   auto fetch_head = [&](int h) {
-    const size_t st_in = (((size_t)b * d.nc + c0) * d.H + h) * (kP * kN);
-    const size_t st_out = (((size_t)b * d.nc + c1) * d.H + h) * (kP * kN);
     tx.fetch(x + (row0 * d.H + h) * kP, (size_t)d.H * kP);
     ty.fetch(dy + (row0 * d.H + h) * kP, (size_t)d.H * kP);
-    th.fetch(hist + st_in, (size_t)kN);
-    tg.fetch(gstate + st_out, (size_t)kN);
+    if (NS == 64) fetch_states(h);
   };
   if (nh > 0) fetch_head(h0);
   for (int hh = 0; hh < nh && ok; ++hh) {
     const int h = h0 + hh;
+    if (NS == 128) fetch_states(h);
     step_tables(d, dt, A[h] * kLog2e, b, (size_t)blk * kQ, kQ, h, s_cs2, s_dt, scratch);
     for (int e = tid; e < 4 * kQ; e += 512) {
       const int w = e >> 7, j = e & 127, r = 32 * w;
@@ -892,8 +957,8 @@ __global__ void __launch_bounds__(512, 1) k_bwd64_bc(D64 d, int seg_heads,
     }
     tx.put(sXh, sXl, one);
     ty.put(sYh, sYl, one);
-    th.put(sHh, sHl, one);
-    tg.put(sGh, sGl, one);
+    th.put(sHh, sHl);
+    tg.put(sGh, sGl);
     fence_async_smem();
     fence_before_sync();
     __syncthreads();
@@ -941,7 +1006,8 @@ __global__ void __launch_bounds__(512, 1) k_bwd64_bc(D64 d, int seg_heads,
     __syncthreads();
     fence_after_sync();
     if (tid == 0) {
-      const uint32_t id = idesc_bf16(128, 64, false, true);
+      // N = n: NS (the second 64 of n at the lo tiles, 8 KB on)
+      const uint32_t id = idesc_bf16(128, NS, false, true);
       for (int kk = 0; kk < 4; ++kk) {
         mma3<kBf>(TdC, smem_u32(sYh) + kk * 32, 16384, 16, false, smem_u32(sHh) + kk * 2048,
                   8192, 8192, id, hh > 0 || kk > 0);
@@ -969,8 +1035,8 @@ __global__ void __launch_bounds__(512, 1) k_bwd64_bc(D64 d, int seg_heads,
   __syncthreads();
   fence_after_sync();
   if (tid == 0 && ok) {
-    const uint32_t id_dc = idesc_bf16(128, 64, false, true);
-    const uint32_t id_db = idesc_bf16(128, 64, true, true);
+    const uint32_t id_dc = idesc_bf16(128, NS, false, true);
+    const uint32_t id_db = idesc_bf16(128, NS, true, true);
     for (int kk = 0; kk < 8; ++kk) {
       // dC: A = W (K-major, K = j), B = B (MN-major rows j, N = n)
       mma3<kBf>(TdC, smem_u32(sWh) + (kk >> 2) * 16384 + (kk & 3) * 32, 32768, 16, false,
@@ -984,23 +1050,27 @@ __global__ void __launch_bounds__(512, 1) k_bwd64_bc(D64 d, int seg_heads,
   ok = ok && wait_all(&bar, phase);
   fence_after_sync();
   if (ok) {
-    // warpgroup wg writes columns [16 wg, 16 wg + 16) of row `row` of dC and dB
+    // warpgroup wg writes columns [NS/4 wg, NS/4 (wg + 1)) of row `row` of dC and dB
+    constexpr int kC = NS / 4;
     const size_t unit = ((size_t)b * d.nb + blk) * d.G + g;
-    float* pbase = part + (unit * gridDim.x + seg) * (2 * kQ * kN);
+    float* pbase = part + (unit * gridDim.x + seg) * (2 * kQ * NS);
 #pragma unroll
     for (int which = 0; which < 2; ++which) {
-      float v[16];
-      tmem_ld16((which ? TdB : TdC) + lane_base + wg * 16, v);
-      tmem_wait_ld();
-      float4* dst = (float4*)(pbase + which * (kQ * kN) + (size_t)row * kN + wg * 16);
 #pragma unroll
-      for (int k4 = 0; k4 < 4; ++k4)
-        dst[k4] = make_float4(v[4 * k4], v[4 * k4 + 1], v[4 * k4 + 2], v[4 * k4 + 3]);
+      for (int c16 = 0; c16 < kC / 16; ++c16) {
+        float v[16];
+        tmem_ld16((which ? TdB : TdC) + lane_base + wg * kC + c16 * 16, v);
+        tmem_wait_ld();
+        float4* dst = (float4*)(pbase + which * (kQ * NS) + (size_t)row * NS + wg * kC + c16 * 16);
+#pragma unroll
+        for (int k4 = 0; k4 < 4; ++k4)
+          dst[k4] = make_float4(v[4 * k4], v[4 * k4 + 1], v[4 * k4 + 2], v[4 * k4 + 3]);
+      }
     }
   }
   fence_before_sync();
   __syncthreads();
-  if (tid < 32) tmem_dealloc(tm, 256);
+  if (tid < 32) tmem_dealloc(tm, kCols);
 }
 
 // dC, dB of every unit: the segments' partials summed in segment order.
@@ -1009,27 +1079,27 @@ __device__ __forceinline__ void st4(__nv_bfloat16* p, float4 v) {
   *(uint2*)p = make_uint2(pack_bf16(v.x, v.y), pack_bf16(v.z, v.w));
 }
 
-template <bool kBf>
+template <bool kBf, int NS>
 __global__ void __launch_bounds__(256) k_sum64_bc(D64 d, int nseg, const float* __restrict__ part,
                                                   Elem<kBf>* __restrict__ dB,
                                                   Elem<kBf>* __restrict__ dC) {
   const size_t unit = blockIdx.x;  // ((b * nb + block) * G + g)
   const int g = (int)(unit % d.G), blk = (int)((unit / d.G) % d.nb);
   const int b = (int)(unit / ((size_t)d.G * d.nb));
-  const float* base = part + unit * nseg * (2 * kQ * kN);
-  for (int e = threadIdx.x; e < 2 * kQ * kN / 4; e += blockDim.x) {
-    const int which = e / (kQ * kN / 4), r = (e % (kQ * kN / 4)) / (kN / 4), n4 = e % (kN / 4);
+  const float* base = part + unit * nseg * (2 * kQ * NS);
+  for (int e = threadIdx.x; e < 2 * kQ * NS / 4; e += blockDim.x) {
+    const int which = e / (kQ * NS / 4), r = (e % (kQ * NS / 4)) / (NS / 4), n4 = e % (NS / 4);
     float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int k = 0; k < nseg; ++k) {
-      const float4 v = ((const float4*)(base + (size_t)k * (2 * kQ * kN) + which * (kQ * kN) +
-                                        (size_t)r * kN))[n4];
+      const float4 v = ((const float4*)(base + (size_t)k * (2 * kQ * NS) + which * (kQ * NS) +
+                                        (size_t)r * NS))[n4];
       s.x += v.x;
       s.y += v.y;
       s.z += v.z;
       s.w += v.w;
     }
     Elem<kBf>* out = which ? dB : dC;
-    st4(out + (((size_t)b * d.T + (size_t)blk * kQ + r) * d.G + g) * kN + 4 * n4, s);
+    st4(out + (((size_t)b * d.T + (size_t)blk * kQ + r) * d.G + g) * NS + 4 * n4, s);
   }
 }
 
@@ -1042,34 +1112,34 @@ cudaError_t set_smem64(K kernel, size_t bytes) {
   return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
 }
 
-template <bool kBf>
+template <bool kBf, int NS>
 cudaError_t chunk_outer_t(const Problem& p, int mode, float* out) {
   using E = Elem<kBf>;
   const size_t smem = 65536 + 1024;
   cudaError_t e;
   if (mode == 0) {
-    if ((e = set_smem64(k_outer64<0, kBf>, smem)) != cudaSuccess) return e;
+    if ((e = set_smem64(k_outer64<0, kBf, NS>, smem)) != cudaSuccess) return e;
     LaunchScope ls("chunk_state_tc64", p.stream);
-    k_outer64<0, kBf><<<dim3(p.nc, p.H, p.B), 256, smem, p.stream>>>(
+    k_outer64<0, kBf, NS><<<dim3(p.nc, p.H, p.B), 256, smem, p.stream>>>(
         d64_of(p), (const E*)p.x, (const E*)p.Bm, p.dt, p.A, out, p.cs_last);
   } else {
-    if ((e = set_smem64(k_outer64<1, kBf>, smem)) != cudaSuccess) return e;
+    if ((e = set_smem64(k_outer64<1, kBf, NS>, smem)) != cudaSuccess) return e;
     LaunchScope ls("chunk_dstate_tc64", p.stream);
-    k_outer64<1, kBf><<<dim3(p.nc, p.H, p.B), 256, smem, p.stream>>>(
+    k_outer64<1, kBf, NS><<<dim3(p.nc, p.H, p.B), 256, smem, p.stream>>>(
         d64_of(p), (const E*)p.dy, (const E*)p.Cm, p.dt, p.A, out, p.cs_last);
   }
   return cudaGetLastError();
 }
 
-template <bool kBf>
+template <bool kBf, int NS>
 cudaError_t forward_scan_t(const Problem& p) {
   using E = Elem<kBf>;
   const size_t smem = kScan64Bytes + 1024;
-  cudaError_t e = set_smem64(k_scan64<kBf>, smem);
+  cudaError_t e = set_smem64(k_scan64<kBf, NS>, smem);
   if (e != cudaSuccess) return e;
   {
     LaunchScope ls("chunk_scan_tc64", p.stream);
-    k_scan64<kBf><<<dim3(p.T / kQ, p.H, p.B), 256, smem, p.stream>>>(
+    k_scan64<kBf, NS><<<dim3(p.T / kQ, p.H, p.B), 256, smem, p.stream>>>(
         d64_of(p), (const E*)p.x, p.dt, p.A, (const E*)p.Bm, (const E*)p.Cm, p.D, p.hist,
         (E*)p.y);
   }
@@ -1078,11 +1148,14 @@ cudaError_t forward_scan_t(const Problem& p) {
 
 }  // namespace
 
-// headdim 64, d_state 64, chunk in {16, 32, 64, 128}, seqlen a multiple of 128
+// headdim 64; d_state 64 (fp32 or bf16) or 128 (bf16, chunks below 128: the
+// bf16 kernels of ssd_tc.cu take chunks 128 and 256); chunk in {16, 32, 64,
+// 128}; seqlen a multiple of 128
 bool tc64_supported(const Problem& p) {
   if (tc_forced_simt()) return false;
-  return p.P == kP && p.N == kN && (p.Q == 16 || p.Q == 32 || p.Q == 64 || p.Q == 128) &&
-         p.T % kQ == 0;
+  if (p.P != kP || p.T % kQ != 0) return false;
+  if (p.Q != 16 && p.Q != 32 && p.Q != 64 && p.Q != 128) return false;
+  return p.N == 64 || (p.N == 128 && p.bf16 && p.Q < 128);
 }
 
 // Heads per segment of the dB, dC kernel: enough segments that the units
@@ -1102,31 +1175,33 @@ int tc64_seg_heads(const Problem& p) {
 size_t tc64_bc_part_floats(const Problem& p) {
   const int sh = tc64_seg_heads(p);
   const long long nseg = (p.hpg + sh - 1) / sh;
-  return (size_t)p.B * (p.T / kQ) * p.G * nseg * 2 * kQ * kN;
+  return (size_t)p.B * (p.T / kQ) * p.G * nseg * 2 * kQ * p.N;
 }
 
 cudaError_t tc64_chunk_outer(const Problem& p, int mode, float* out) {
-  return p.bf16 ? chunk_outer_t<true>(p, mode, out) : chunk_outer_t<false>(p, mode, out);
+  if (!p.bf16) return chunk_outer_t<false, 64>(p, mode, out);
+  return p.N == 128 ? chunk_outer_t<true, 128>(p, mode, out) : chunk_outer_t<true, 64>(p, mode, out);
 }
 
 cudaError_t tc64_forward_scan(const Problem& p) {
-  return p.bf16 ? forward_scan_t<true>(p) : forward_scan_t<false>(p);
+  if (!p.bf16) return forward_scan_t<false, 64>(p);
+  return p.N == 128 ? forward_scan_t<true, 128>(p) : forward_scan_t<true, 64>(p);
 }
 
 namespace {
-template <bool kBf>
+template <bool kBf, int NS>
 cudaError_t backward_t(const Problem& p) {
   using E = Elem<kBf>;
   cudaError_t e;
-  if ((e = chunk_outer_t<kBf>(p, 1, p.dstate)) != cudaSuccess) return e;
+  if ((e = chunk_outer_t<kBf, NS>(p, 1, p.dstate)) != cudaSuccess) return e;
   if ((e = simt_state_pass_bwd(p)) != cudaSuccess) return e;
   const D64 d = d64_of(p);
   const int nb = p.T / kQ;
   {
     const size_t smem = kBwdX64Bytes + 1024;
-    if ((e = set_smem64(k_bwd64_x<kBf>, smem)) != cudaSuccess) return e;
+    if ((e = set_smem64(k_bwd64_x<kBf, NS>, smem)) != cudaSuccess) return e;
     LaunchScope ls("bwd_x_tc64", p.stream);
-    k_bwd64_x<kBf><<<dim3(nb, p.H, p.B), 512, smem, p.stream>>>(
+    k_bwd64_x<kBf, NS><<<dim3(nb, p.H, p.B), 512, smem, p.stream>>>(
         d, (const E*)p.x, p.dt, p.A, (const E*)p.Bm, (const E*)p.Cm, p.D, (const E*)p.dy,
         p.hist, p.dstate, (E*)p.dx, p.ddt, p.dA_part, p.dD_part);
   }
@@ -1135,16 +1210,16 @@ cudaError_t backward_t(const Problem& p) {
   const int nseg = (p.hpg + sh - 1) / sh;
   {
     const size_t smem = kBwdBC64Bytes + 1024;
-    if ((e = set_smem64(k_bwd64_bc<kBf>, smem)) != cudaSuccess) return e;
+    if ((e = set_smem64(k_bwd64_bc<kBf, NS>, smem)) != cudaSuccess) return e;
     LaunchScope ls("bwd_bc_tc64", p.stream);
-    k_bwd64_bc<kBf><<<dim3(nseg, nb, p.B * p.G), 512, smem, p.stream>>>(
+    k_bwd64_bc<kBf, NS><<<dim3(nseg, nb, p.B * p.G), 512, smem, p.stream>>>(
         d, sh, (const E*)p.x, p.dt, p.A, (const E*)p.Bm, (const E*)p.Cm, (const E*)p.dy,
         p.hist, p.dstate, p.bwd_part);
   }
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   {
     LaunchScope ls("sum_bc_tc64", p.stream);
-    k_sum64_bc<kBf><<<(unsigned)((size_t)p.B * nb * p.G), 256, 0, p.stream>>>(
+    k_sum64_bc<kBf, NS><<<(unsigned)((size_t)p.B * nb * p.G), 256, 0, p.stream>>>(
         d, nseg, p.bwd_part, (E*)p.dB, (E*)p.dC);
   }
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
@@ -1155,7 +1230,8 @@ cudaError_t backward_t(const Problem& p) {
 // R_c, the reverse state pass (g_c in place, dh0), the dx / d(dt) kernel, the
 // dB / dC kernel and its segment sums, and the dA, dD reduction.
 cudaError_t tc64_backward(const Problem& p) {
-  return p.bf16 ? backward_t<true>(p) : backward_t<false>(p);
+  if (!p.bf16) return backward_t<false, 64>(p);
+  return p.N == 128 ? backward_t<true, 128>(p) : backward_t<true, 64>(p);
 }
 
 cudaError_t tc64_read_and_clear_error(unsigned int* out) {

@@ -122,9 +122,14 @@ k_chunk_outer(Dev d, const TIO* __restrict__ u, const TIO* __restrict__ v,
   }
 }
 
+// The state passes walk the chunks in order, one dependent update per chunk;
+// the loads of the next kPassDepth chunks (their chunk products and decay
+// totals) are in flight in a register ring while a chunk is updated, so a
+// step waits for one load only when the ring runs dry.
+constexpr int kPassDepth = 8;
+
 // Forward state pass, in place: hist[c] holds S_c on entry and H_{c-1} on exit.
-// Each thread owns 4 consecutive (p, n) elements (float4); the loads of the
-// next chunks are issued ahead of the dependent update.
+// Each thread owns 4 consecutive (p, n) elements (float4).
 __global__ void __launch_bounds__(kThreads)
 k_state_pass_fwd(Dev d, float* __restrict__ hist, const float* __restrict__ cs_last,
                  const float* __restrict__ h0, float* __restrict__ final_state) {
@@ -137,18 +142,32 @@ k_state_pass_fwd(Dev d, float* __restrict__ hist, const float* __restrict__ cs_l
   const float* cl = cs_last + bh * d.nc;
   const size_t stride4 = (size_t)d.H * PN / 4;  // float4 step between chunks
   float4* p4 = reinterpret_cast<float4*>(hist + (((size_t)b * d.nc) * d.H + h) * PN) + q;
-  float4 s0 = p4[0];
-  float4 s1 = d.nc > 1 ? p4[stride4] : s0;
-  for (int c = 0; c < d.nc; ++c) {
-    const float4 s = s0;
-    s0 = s1;
-    if (c + 2 < d.nc) s1 = p4[(size_t)(c + 2) * stride4];
-    p4[(size_t)c * stride4] = hc;
-    const float e = expf(cl[c]);
-    hc.x = fmaf(e, hc.x, s.x);
-    hc.y = fmaf(e, hc.y, s.y);
-    hc.z = fmaf(e, hc.z, s.z);
-    hc.w = fmaf(e, hc.w, s.w);
+  float4 sr[kPassDepth];
+  float lr[kPassDepth];
+#pragma unroll
+  for (int k = 0; k < kPassDepth; ++k)
+    if (k < d.nc) {
+      sr[k] = p4[(size_t)k * stride4];
+      lr[k] = cl[k];
+    }
+  for (int c0 = 0; c0 < d.nc; c0 += kPassDepth) {
+#pragma unroll
+    for (int k = 0; k < kPassDepth; ++k) {
+      const int c = c0 + k;
+      if (c < d.nc) {
+        const float4 s = sr[k];
+        const float e = expf(lr[k]);
+        if (c + kPassDepth < d.nc) {  // refill the slot with chunk c + depth
+          sr[k] = p4[(size_t)(c + kPassDepth) * stride4];
+          lr[k] = cl[c + kPassDepth];
+        }
+        p4[(size_t)c * stride4] = hc;
+        hc.x = fmaf(e, hc.x, s.x);
+        hc.y = fmaf(e, hc.y, s.y);
+        hc.z = fmaf(e, hc.z, s.z);
+        hc.w = fmaf(e, hc.w, s.w);
+      }
+    }
   }
   if (final_state) reinterpret_cast<float4*>(final_state + bh * PN)[q] = hc;
 }
@@ -167,18 +186,32 @@ k_state_pass_bwd(Dev d, float* __restrict__ dstate, const float* __restrict__ cs
   float4* p4 = reinterpret_cast<float4*>(dstate + (((size_t)b * d.nc) * d.H + h) * PN) + q;
   float4 gc = make_float4(0.f, 0.f, 0.f, 0.f);
   const int last = d.nc - 1;
-  float4 r0 = p4[(size_t)last * stride4];
-  float4 r1 = last > 0 ? p4[(size_t)(last - 1) * stride4] : r0;
-  for (int c = last; c >= 0; --c) {
-    const float4 r = r0;
-    r0 = r1;
-    if (c - 2 >= 0) r1 = p4[(size_t)(c - 2) * stride4];
-    p4[(size_t)c * stride4] = gc;
-    const float e = expf(cl[c]);
-    gc.x = fmaf(e, gc.x, r.x);
-    gc.y = fmaf(e, gc.y, r.y);
-    gc.z = fmaf(e, gc.z, r.z);
-    gc.w = fmaf(e, gc.w, r.w);
+  float4 rr[kPassDepth];
+  float lr[kPassDepth];
+#pragma unroll
+  for (int k = 0; k < kPassDepth; ++k)
+    if (last - k >= 0) {
+      rr[k] = p4[(size_t)(last - k) * stride4];
+      lr[k] = cl[last - k];
+    }
+  for (int i0 = 0; i0 <= last; i0 += kPassDepth) {
+#pragma unroll
+    for (int k = 0; k < kPassDepth; ++k) {
+      const int c = last - (i0 + k);
+      if (c >= 0) {
+        const float4 r = rr[k];
+        const float e = expf(lr[k]);
+        if (c - kPassDepth >= 0) {  // refill the slot with chunk c - depth
+          rr[k] = p4[(size_t)(c - kPassDepth) * stride4];
+          lr[k] = cl[c - kPassDepth];
+        }
+        p4[(size_t)c * stride4] = gc;
+        gc.x = fmaf(e, gc.x, r.x);
+        gc.y = fmaf(e, gc.y, r.y);
+        gc.z = fmaf(e, gc.z, r.z);
+        gc.w = fmaf(e, gc.w, r.w);
+      }
+    }
   }
   if (dh0) reinterpret_cast<float4*>(dh0 + bh * PN)[q] = gc;
 }

@@ -1918,13 +1918,29 @@ k_state_pass_bwd_t(TcDims d, unsigned int* __restrict__ tickets, int ntickets,
   auto at = [&](int c) { return (((size_t)b * d.nc + c) * d.H + h) * (size_t)PN + (size_t)p * d.N + n0 + n4; };
   float4 gc = make_float4(0.f, 0.f, 0.f, 0.f);
   const int last = d.nc - 1;
-  float4 r_next = *(const float4*)(R + at(last));
-  float4 h_next = *(const float4*)(hist + at(last));
-  for (int c = last; c >= 0; --c) {
-    const float4 r = r_next, hv = h_next;
-    if (c > 0) {
-      r_next = *(const float4*)(R + at(c - 1));
-      h_next = *(const float4*)(hist + at(c - 1));
+  // the next kDepth chunks' R_c, H_{c-1} and decay totals in flight in a
+  // register ring while one chunk is updated
+  constexpr int kDepth = 4;
+  float4 r_ring[kDepth], h_ring[kDepth];
+  float l_ring[kDepth];
+#pragma unroll
+  for (int k = 0; k < kDepth; ++k)
+    if (last - k >= 0) {
+      r_ring[k] = *(const float4*)(R + at(last - k));
+      h_ring[k] = *(const float4*)(hist + at(last - k));
+      l_ring[k] = cl[last - k];
+    }
+  for (int i0 = 0; i0 <= last; i0 += kDepth) {
+#pragma unroll
+  for (int k = 0; k < kDepth; ++k) {
+    const int c = last - (i0 + k);
+    if (c < 0) break;  // uniform over the CTA
+    const float4 r = r_ring[k], hv = h_ring[k];
+    const float lc = l_ring[k];
+    if (c - kDepth >= 0) {  // refill the slot with chunk c - depth
+      r_ring[k] = *(const float4*)(R + at(c - kDepth));
+      h_ring[k] = *(const float4*)(hist + at(c - kDepth));
+      l_ring[k] = cl[c - kDepth];
     }
     __syncthreads();  // previous chunk's rows are written out
     s_g[n4 + 0][p] = __float2bfloat16_rn(gc.x);
@@ -1943,11 +1959,12 @@ k_state_pass_bwd_t(TcDims d, unsigned int* __restrict__ tickets, int ntickets,
       if (tid < 128) *(uint4*)(gT + orow) = *(const uint4*)&s_g[rr][ch * 8];
       else *(uint4*)(hT + orow) = *(const uint4*)&s_h[rr][ch * 8];
     }
-    const float e = expf(cl[c]);
+    const float e = expf(lc);
     gc.x = fmaf(e, gc.x, r.x);
     gc.y = fmaf(e, gc.y, r.y);
     gc.z = fmaf(e, gc.z, r.z);
     gc.w = fmaf(e, gc.w, r.w);
+  }
   }
   if (dh0) *(float4*)(dh0 + bh * PN + (size_t)p * d.N + n0 + n4) = gc;
   // completion counters of the backward kernel that follows

@@ -66,7 +66,6 @@ cudaError_t tc_chunk_outer(const Problem& p, int mode, float* out);
 cudaError_t tc_forward_scan(const Problem& p);
 cudaError_t tc_forward_single(const Problem& p);
 bool tc_fused_states(const Problem& p);
-bool tc_single_pass(const Problem& p);
 cudaError_t tc_forward_states(const Problem& p);
 cudaError_t tc_backward(const Problem& p);
 cudaError_t tc_read_and_clear_error(unsigned int* out);
@@ -223,7 +222,7 @@ void set_last_error(const char* msg) { g_err = msg; }
 cudaError_t forward_launches(Problem& p, const char** where) {
   const bool tc = tc_supported(p);
   cudaError_t e;
-  if (tc && tc_single_pass(p)) {
+  if (tc && tc_fused_states(p)) {
     // one kernel: chunk states, the state pass (look-back) and y
     *where = "single-pass forward kernel";
     return tc_forward_single(p);

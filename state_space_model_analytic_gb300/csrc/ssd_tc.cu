@@ -2114,22 +2114,6 @@ bool tc_fused_states(const Problem& p) {
   return (long)p.B * p.H * 4 >= 3L * nsm;
 }
 
-// Whether the forward runs as the single-pass kernel: where the state scans
-// fill the GPU, and also where the (b, h) pairs are fewer but each has many
-// chunks.  Its (b, chunk, h) tiles then outnumber the GPU's CTA slots many
-// times over, and each pair's look-back chain (one hop per chunk, a
-// microsecond or two) stays shorter than the time the tiles take anyway; with
-// fewer than 24 pairs the chains would set the time and the three-kernel
-// forward is kept.
-bool tc_single_pass(const Problem& p) {
-  if (tc_fused_states(p)) return true;
-  int nsm = 0, dev = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
-  const long pairs = (long)p.B * p.H;
-  return pairs >= 24 && pairs * p.nc >= 8L * nsm;
-}
-
 template <int MODE>
 cudaError_t tc_state_scan(const Problem& p, const char* name, float* final_or_dh0) {
   ScanStateMaps maps;

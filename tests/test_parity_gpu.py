@@ -195,33 +195,6 @@ def test_single_pass_forward_look_back(q, h0):
     nat.check(nat.lib().ssd_device_status())
 
 
-def test_single_pass_forward_few_pairs_many_chunks():
-    """32 (b, h) pairs with 64 chunks each (2048 tiles): the single-pass
-    forward runs (its look-back chains are 64 hops long) instead of the
-    three-kernel forward; one group against the oracle, and y and the states
-    bit for bit on a second run."""
-    from state_space_model_analytic_gb300 import _native as nat
-    dims = synth.Dims(1, 16384, 32, 64, 128, 4, 256, "bf16")
-    inp = synth.make_inputs(dims, 31, True, "decay_span")
-    dev = to_device(dims, inp)
-    nat.trace_begin(64)
-    try:
-        tc = run_gpu(dims, dev)
-    finally:
-        nat.trace_end()
-    names = [r["name"] for r in nat.trace_read()]
-    nat.trace_reset()
-    assert "fwd_single_tc" in names and "chunk_state_tc" not in names, names
-    again = run_gpu(dims, dev)
-    for k in ("y", "final_state", "chunk_states"):
-        assert np.array_equal(tc[k], again[k]), k
-    g = dims.ngroups - 1
-    sdims, sub = group_slice(dims, inp, g)
-    errs, bad = compare(slice_outputs(dims, tc, g), run_oracle(sdims, sub), TOL["bf16"])
-    assert not bad, errs
-    nat.check(nat.lib().ssd_device_status())
-
-
 @pytest.mark.parametrize("q", [128, 256])
 def test_tensor_core_and_simt_paths_agree(q):
     """The tcgen05 path and the SIMT path (forced) give the same results

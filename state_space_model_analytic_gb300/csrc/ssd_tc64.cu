@@ -1158,18 +1158,28 @@ bool tc64_supported(const Problem& p) {
   return p.N == 64 || (p.N == 128 && p.bf16 && p.Q < 128);
 }
 
-// Heads per segment of the dB, dC kernel: enough segments that the units
-// times their segments make about kBcTargetCtas CTAs (two per SM of a GB300).
-// The split sets the order of the dB, dC sums, so it does not depend on the
-// device: results and workspace sizes are the same on every GPU.
-constexpr long long kBcTargetCtas = 304;
+// Heads per segment of the dB, dC kernel (one CTA per SM): the number of
+// segments per unit that minimises waves x (heads per segment + a CTA's own
+// work, about two heads': the B, C tiles, the W products and the partials'
+// write) over kBcSlots CTA slots (the SMs of a GB300), the fewest segments
+// among equals.  The split sets the order of the dB, dC sums,
+// so it depends on this constant and not on the device: results and
+// workspace sizes are the same on every GPU.
+constexpr long long kBcSlots = 152;
 
 int tc64_seg_heads(const Problem& p) {
   const long long units = (long long)p.B * (p.T / kQ) * p.G;
-  long long nseg = (kBcTargetCtas + units - 1) / units;
-  if (nseg < 1) nseg = 1;
-  if (nseg > p.hpg) nseg = p.hpg;
-  return (int)((p.hpg + nseg - 1) / nseg);
+  long long best_seg = 1, best_cost = -1;
+  for (long long nseg = 1; nseg <= p.hpg; ++nseg) {
+    const long long heads = (p.hpg + nseg - 1) / nseg;
+    if ((p.hpg + heads - 1) / heads != nseg) continue;  // same split as a smaller count
+    const long long cost = ((units * nseg + kBcSlots - 1) / kBcSlots) * (heads + 2);
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best_seg = nseg;
+    }
+  }
+  return (int)((p.hpg + best_seg - 1) / best_seg);
 }
 
 size_t tc64_bc_part_floats(const Problem& p) {

@@ -227,7 +227,7 @@ cudaError_t forward_launches(Problem& p, const char** where) {
     *where = "single-pass forward kernel";
     return tc_forward_single(p);
   }
-  if (tc64_supported(p)) {  // headdim 64, d_state 64 (fp32 through split bf16 products)
+  if (tc64_supported(p)) {  // the block family (fp32 through split bf16 products)
     *where = "forward chunk-state kernel";
     if ((e = tc64_chunk_outer(p, 0, p.hist)) != cudaSuccess) return e;
     *where = "forward state-pass kernel";

@@ -1,6 +1,9 @@
-// Tensor-core (tcgen05 / TMEM) kernels of the chunked SSD core for headdim
-// P = 64 and d_state N = 64, fp32 or bf16 storage, any chunk Q in {16, 32,
-// 64, 128} (seqlen a multiple of 128).
+// Tensor-core (tcgen05 / TMEM) kernels of the chunked SSD core on 128-step
+// blocks: headdim P = 64 with d_state N = 64 (fp32 or bf16 storage) or
+// N = 128 (bf16), and P = 128 with N = 64 (bf16); any chunk Q in {16, 32,
+// 64, 128} (seqlen a multiple of 128).  A bf16 row of 128 values occupies
+// the bytes of an fp32 row of 64 carried as two bf16 tiles, so the 128-wide
+// operands of the bf16 shapes take the lo tiles' places of the fp32 layout.
 //
 // Blocks.  The chunk scan and the backward work on blocks of 128 steps (the
 // MMA M size).  A block holds 128 / Q whole chunks; inside it the decays are
@@ -59,7 +62,7 @@ namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
-constexpr int kQ = 128, kP = 64;  // kQ: rows of a block (the MMA M size)
+constexpr int kQ = 128;  // rows of a block (the MMA M size)
 
 __device__ unsigned int g_tc64_error;
 
@@ -98,19 +101,12 @@ __device__ __forceinline__ void store_split8(uint8_t* hi, uint8_t* lo, uint32_t 
   if (!kBf) *(uint4*)(lo + off) = make_uint4(l[0], l[1], l[2], l[3]);
 }
 
-// 8 consecutive stored values (16 or 32 bytes) as fp32
+// 8 consecutive fp32 values
 struct Raw8 {
   float4 a, b;
 };
 __device__ __forceinline__ Raw8 ld8(const float* p) {
   return Raw8{__ldg((const float4*)p), __ldg((const float4*)p + 1)};
-}
-__device__ __forceinline__ Raw8 ld8(const __nv_bfloat16* p) {
-  const uint4 u = __ldg((const uint4*)p);
-  const __nv_bfloat162* q = (const __nv_bfloat162*)&u;
-  const float2 f0 = __bfloat1622float2(q[0]), f1 = __bfloat1622float2(q[1]);
-  const float2 f2 = __bfloat1622float2(q[2]), f3 = __bfloat1622float2(q[3]);
-  return Raw8{make_float4(f0.x, f0.y, f1.x, f1.y), make_float4(f2.x, f2.y, f3.x, f3.y)};
 }
 __device__ __forceinline__ void unpack8_bf16(const uint4& u, float* f) {
   const __nv_bfloat162* q = (const __nv_bfloat162*)&u;
@@ -149,13 +145,19 @@ struct RowTile {
   static_assert(W == 64 || (W == 128 && kBf), "128-wide rows are bf16 only");
   static constexpr int kCh = W / 8;  // 16-byte chunks of bf16 per row
   static constexpr int kPer = ROWS * kCh / NT;
-  Raw8 v[kPer];
+  // bf16 values stay packed (4 registers per 8 values) until put()
+  typename std::conditional<kBf, uint4, Raw8>::type v[kPer];
   __device__ __forceinline__ void fetch(const E* __restrict__ src, size_t stride,
                                         int nrows = ROWS) {
 #pragma unroll
     for (int k = 0; k < kPer; ++k) {
       const int e = threadIdx.x + NT * k, r = e / kCh, ch = e % kCh;
-      if (r < nrows) v[k] = ld8(src + (size_t)r * stride + ch * 8);
+      if (r < nrows) {
+        if constexpr (kBf)
+          v[k] = __ldg((const uint4*)(src + (size_t)r * stride + ch * 8));
+        else
+          v[k] = ld8(src + (size_t)r * stride + ch * 8);
+      }
     }
   }
   template <typename F>
@@ -166,7 +168,10 @@ struct RowTile {
       if (r >= nrows) continue;
       const float sc = scale(r);
       float f[8];
-      unpack_raw(v[k], f);
+      if constexpr (kBf)
+        unpack8_bf16(v[k], f);
+      else
+        unpack_raw(v[k], f);
 #pragma unroll
       for (int t = 0; t < 8; ++t) f[t] *= sc;
       if (W == 64)
@@ -195,11 +200,12 @@ __device__ __forceinline__ void read_split8(const uint8_t* hi, const uint8_t* lo
 // A [64 p][NS n] fp32 state block as rows p into tiles: split for fp32
 // storage (NS = 64), bf16 for bf16 storage (NS = 128: n 64-127 in a second
 // tile at the lo tile's place).
-template <int NT, int NS, bool kBf>
+template <int NT, int NS, bool kBf, int PR = 64>
 struct StateRowTile {
   static_assert(NS == 64 || (NS == 128 && kBf), "d_state 128 is bf16 only");
+  static_assert(PR == 64 || (PR == 128 && kBf && NS == 64), "headdim 128 is bf16, d_state 64");
   static constexpr int kCh = NS / 8;
-  static constexpr int kPer = 64 * kCh / NT;
+  static constexpr int kPer = PR * kCh / NT;  // PR = 128: rows 64-127 run into the lo tile's place
   Raw8 v[kPer];
   __device__ __forceinline__ void fetch(const float* __restrict__ src) {
 #pragma unroll
@@ -233,15 +239,19 @@ __device__ __forceinline__ void load_split(uint8_t* hi, uint8_t* lo, const E* __
 
 // Rows [0, ROWS) of split tiles rescaled in place: each row r times scale(r),
 // from the value the tiles hold (hi + lo, or hi alone for bf16 storage).
-template <int NT, int ROWS, bool kBf, typename F>
+template <int NT, int ROWS, bool kBf, int W = 64, typename F>
 __device__ __forceinline__ void rescale_split(uint8_t* hi, uint8_t* lo, F&& scale) {
-  constexpr int kPer = ROWS * 8 / NT;
+  static_assert(W == 64 || (W == 128 && kBf), "128-wide rows are bf16 only");
+  constexpr int kCh = W / 8;
+  constexpr int kPer = ROWS * kCh / NT;
 #pragma unroll
   for (int k = 0; k < kPer; ++k) {
-    const int e = threadIdx.x + NT * k, r = e >> 3, ch = e & 7;
+    const int e = threadIdx.x + NT * k, r = e / kCh, cw = e % kCh, ch = cw & 7;
+    // the row's second 64 values (W = 128, bf16 only) are in the lo tile's place
+    uint8_t* th = W == 128 && (cw >> 3) ? lo : hi;
     const uint32_t off = sw128(r, ch);
     float f[8], g[8];
-    unpack8_bf16(*(const uint4*)(hi + off), f);
+    unpack8_bf16(*(const uint4*)(th + off), f);
     if (!kBf) {
       unpack8_bf16(*(const uint4*)(lo + off), g);
 #pragma unroll
@@ -250,20 +260,22 @@ __device__ __forceinline__ void rescale_split(uint8_t* hi, uint8_t* lo, F&& scal
     const float sc = scale(r);
 #pragma unroll
     for (int t = 0; t < 8; ++t) f[t] *= sc;
-    store_split8<kBf>(hi, lo, off, f);
+    store_split8<kBf>(th, lo, off, f);
   }
 }
 
-// A [64 p][NS n] fp32 state block (p-major) transposed into split tiles of
-// rows n with 64 p each (NS = 128, bf16 only: rows 64-127 continue into the
-// lo tile's place); returns this thread's share of sum(src * other) when
-// `other` is given (the same elements of a second block, for <g, H>).
-template <int NT, bool kBf, int NS = 64>
+// A [PS p][NS n] fp32 state block (p-major) transposed into split tiles of
+// rows n with 64 p each; NS = 128 (bf16 only): rows 64-127 continue into the
+// lo tile's place; PS = 128 (bf16 only, NS = 64): p 64-127 go to a second
+// tile there.  Returns this thread's share of sum(src * other) when `other`
+// is given (the same elements of a second block, for <g, H>).
+template <int NT, bool kBf, int NS = 64, int PS = 64>
 __device__ __forceinline__ float load_split_transposed(uint8_t* hi, uint8_t* lo,
                                                        const float* __restrict__ src,
                                                        const float* __restrict__ other) {
   static_assert(NS == 64 || (NS == 128 && kBf), "d_state 128 is bf16 only");
-  constexpr int kPer = NS * 8 / NT;
+  static_assert(PS == 64 || (PS == 128 && kBf && NS == 64), "headdim 128 is bf16, d_state 64");
+  constexpr int kPer = NS * (PS / 8) / NT;
   float dot = 0.f;
 #pragma unroll
   for (int k = 0; k < kPer; ++k) {
@@ -275,7 +287,10 @@ __device__ __forceinline__ float load_split_transposed(uint8_t* hi, uint8_t* lo,
 #pragma unroll
       for (int t = 0; t < 8; ++t) dot = fmaf(f[t], __ldg(other + (size_t)(pc * 8 + t) * NS + n), dot);
     }
-    store_split8<kBf>(hi, lo, sw128(n, pc), f);
+    if (PS == 64)
+      store_split8<kBf>(hi, lo, sw128(n, pc), f);
+    else
+      store_split8<true>((pc >> 3) ? lo : hi, nullptr, sw128(n, pc & 7), f);
   }
   return dot;
 }
@@ -321,8 +336,8 @@ __device__ __forceinline__ void step_tables(const D64& d, const float* __restric
 //   MODE 1: out = R_c  from u = dy, v = C, w_i = exp(cs_i)
 // as D[n][p] = V^T (w o U) (M = n padded to 128: the second half of the A
 // operand reads the U tiles and its rows are never read back), then written
-// out[b][c][h][p][n]; also cs_last[b][h][c] (natural-log units).
-template <int MODE, bool kBf, int NS>
+// out[b][c][h][p][n]; also cs_last[b][h][c] (natural-log units).  PS: headdim.
+template <int MODE, bool kBf, int NS, int PS>
 __global__ void __launch_bounds__(256) k_outer64(D64 d, const Elem<kBf>* __restrict__ U,
                                                  const Elem<kBf>* __restrict__ V,
                                                  const float* __restrict__ dt,
@@ -333,7 +348,7 @@ __global__ void __launch_bounds__(256) k_outer64(D64 d, const Elem<kBf>* __restr
   uint8_t* sm = align1024(smraw);
   uint8_t* sVh = sm;           // [128 rows j][64 n] (NS = 128: n 64-127 in the lo tile's place)
   uint8_t* sVl = sm + 16384;
-  uint8_t* sUh = sm + 32768;   // [128 rows j][64 p], rows scaled by w
+  uint8_t* sUh = sm + 32768;   // [128 rows j][64 p], rows scaled by w (PS = 128: p 64-127 at the lo tile)
   uint8_t* sUl = sm + 49152;
   __shared__ float s_cs2[kQ], s_dt[kQ], s_w[kQ], scratch[8];
   __shared__ uint64_t bar;
@@ -345,15 +360,15 @@ __global__ void __launch_bounds__(256) k_outer64(D64 d, const Elem<kBf>* __restr
     fence_mbar_init();
   }
   if (tid < 32) {
-    tmem_alloc(&tmem_base, 64);
+    tmem_alloc(&tmem_base, PS);
     tmem_relinquish();
   }
   // the tiles' loads are in flight while the decay tables are built
   const size_t row0 = (size_t)b * d.T + (size_t)c * Q;
   RowTile<256, kQ, Elem<kBf>, NS> tv;
-  RowTile<256, kQ, Elem<kBf>> tu;
+  RowTile<256, kQ, Elem<kBf>, PS> tu;
   tv.fetch(V + (row0 * d.G + g) * NS, (size_t)d.G * NS, Q);
-  tu.fetch(U + (row0 * d.H + h) * kP, (size_t)d.H * kP, Q);
+  tu.fetch(U + (row0 * d.H + h) * PS, (size_t)d.H * PS, Q);
   step_tables(d, dt, A[h] * kLog2e, b, (size_t)c * Q, Q, h, s_cs2, s_dt, scratch);
   const float last2 = s_cs2[Q - 1];
   if (tid < Q) s_w[tid] = MODE == 0 ? exp2f(last2 - s_cs2[tid]) * s_dt[tid] : exp2f(s_cs2[tid]);
@@ -367,10 +382,11 @@ __global__ void __launch_bounds__(256) k_outer64(D64 d, const Elem<kBf>* __restr
   fence_after_sync();
   const uint32_t tm = tmem_base;
   if (tid == 0) {
-    const uint32_t id = idesc_bf16(128, 64, true, true);
+    const uint32_t id = idesc_bf16(128, PS, true, true);
     // A = V^T, M = n: NS = 64 pads M to 128 with a second block read from
     // the U tiles (rows never read back); NS = 128 has its second block of n
-    // in the lo tile's place
+    // in the lo tile's place.  N = p: PS = 128 has its second block of p in
+    // the U lo tile's place (16 KB on).
     for (int ks = 0; ks < Q / 16; ++ks)
       mma3<kBf>(tm, smem_u32(sVh) + ks * 2048, 16384, NS == 128 ? 16384 : 32768, true,
                 smem_u32(sUh) + ks * 2048, 16384, 16384, id, ks > 0);
@@ -379,17 +395,21 @@ __global__ void __launch_bounds__(256) k_outer64(D64 d, const Elem<kBf>* __restr
   const bool ok = wait_all(&bar, 0);
   fence_after_sync();
   const int wg = tid >> 7, r = tid & 127;
-  if (ok && r < NS) {  // lanes (rows n) below NS; warpgroup wg takes p in [32 wg, +32)
-    float v[32];
-    tmem_ld32(tm + ((uint32_t)((r >> 5) * 32) << 16) + wg * 32, v);
-    tmem_wait_ld();
-    float* dst = out + (((size_t)b * d.nc + c) * d.H + h) * (kP * NS) + r;
+  if (ok && r < NS) {  // lanes (rows n) below NS; warpgroup wg takes p in [PS/2 wg, +PS/2)
+    float* dst = out + (((size_t)b * d.nc + c) * d.H + h) * (PS * NS) + r;
 #pragma unroll
-    for (int i = 0; i < 32; ++i) dst[(size_t)(wg * 32 + i) * NS] = v[i];
+    for (int p32 = 0; p32 < PS / 64; ++p32) {
+      const int pc = wg * (PS / 2) + p32 * 32;
+      float v[32];
+      tmem_ld32(tm + ((uint32_t)((r >> 5) * 32) << 16) + pc, v);
+      tmem_wait_ld();
+#pragma unroll
+      for (int i = 0; i < 32; ++i) dst[(size_t)(pc + i) * NS] = v[i];
+    }
   }
   fence_before_sync();
   __syncthreads();
-  if (tid < 32) tmem_dealloc(tm, 64);
+  if (tid < 32) tmem_dealloc(tm, PS);
 }
 
 // ---------------------------------------------------------------------------
@@ -397,18 +417,23 @@ __global__ void __launch_bounds__(256) k_outer64(D64 d, const Elem<kBf>* __restr
 // CTAs per SM (80 KB of shared memory, 256 TMEM columns each).
 //   CB = C B^T, Ys = C H^T (H = the state before the block: the history entry
 //   of its first chunk, as rows n),
-//   M = CB o L o dt (masked, split) in two 64-column halves, each followed by
-//   its half of Y = M X (K = the half's 64 rows of X),
+//   M = CB o L o dt (masked, split), Y = M X,
 //   y = Y + exp(cs_i) Ys + D x.
+// fp32 storage and d_state 128 form M in two 64-column halves in the C
+// tile's place, each followed by its half of Y = M X (K = the half's 64 rows
+// of X).  bf16 storage with d_state 64 leaves the C tile's lo half unused, so
+// M is formed whole (the two halves in the hi and lo places) and Y = M X is
+// one batch with K = 128; Y then takes CB's TMEM columns (CB has been read),
+// which leaves room for a 128-wide Y and Ys (headdim PS = 128).
 // X is fetched into registers at the start and written into the B tile's
-// place once CB is formed; the M half takes the C tile's place.
+// place once CB is formed (PS = 128: X's second 64 columns at the lo place).
 // Decay masks as in the bf16 kernels: for warp q's rows and a 32-column chunk
 // left of its diagonal chunk, exp(cs_i - cs_j) = exp(cs_i - cs_r) exp(cs_r -
 // cs_j) with r = 32 q (both factors <= 1); the diagonal chunk evaluates the
 // exponent only where j <= i.
-constexpr uint32_t kScan64Bytes = 81920;  // C (later an M half) 32K | B (later X) 32K | H 16K
+constexpr uint32_t kScan64Bytes = 81920;  // C (later M) 32K | B (later X) 32K | H 16K
 
-template <bool kBf, int NS>
+template <bool kBf, int NS, int PS>
 __global__ void __launch_bounds__(256, 2) k_scan64(D64 d, const Elem<kBf>* __restrict__ x,
                                                    const float* __restrict__ dt,
                                                    const float* __restrict__ A,
@@ -417,18 +442,20 @@ __global__ void __launch_bounds__(256, 2) k_scan64(D64 d, const Elem<kBf>* __res
                                                    const float* __restrict__ D,
                                                    const float* __restrict__ hist,
                                                    Elem<kBf>* __restrict__ y) {
+  constexpr bool kWholeM = kBf && NS == 64;
+  static_assert(PS == 64 || kWholeM, "headdim 128 is bf16, d_state 64");
   extern __shared__ __align__(1024) uint8_t smraw[];
   uint8_t* sm = align1024(smraw);
   uint8_t* sCh = sm;            // [128 rows i][64 n] K-major (NS = 128: n 64-127 at the lo tile)
   uint8_t* sCl = sm + 16384;
-  uint8_t* sMh = sm;            // M half [128 rows i][64 j] K-major (after CB, Ys)
-  uint8_t* sMl = sm + 16384;
+  uint8_t* sMh = sm;            // M [128 rows i][64 j] K-major (after CB, Ys); kWholeM: j 64-127
+  uint8_t* sMl = sm + 16384;    // at the lo tile
   uint8_t* sBh = sm + 32768;    // [128 rows j][64 n] K-major
   uint8_t* sBl = sm + 49152;
   uint8_t* sXh = sm + 32768;    // [128 rows j][64 p] MN-major B operand (after CB)
   uint8_t* sXl = sm + 49152;
-  uint8_t* sHh = sm + 65536;    // [NS rows n][64 p] MN-major B operand (NS = 128: rows 64+ at the lo tile)
-  uint8_t* sHl = sm + 73728;
+  uint8_t* sHh = sm + 65536;    // [NS rows n][64 p] MN-major B operand (NS = 128: rows 64+ at
+  uint8_t* sHl = sm + 73728;    // the lo tile; PS = 128: p 64-127 at the lo tile)
   __shared__ float s_cs2[kQ], s_dt[kQ], scratch[8];
   __shared__ __align__(16) float s_E[4][kQ];  // exp(cs_r - cs_j) dt_j, j < r = 32 w
   __shared__ uint64_t bar;
@@ -448,15 +475,13 @@ __global__ void __launch_bounds__(256, 2) k_scan64(D64 d, const Elem<kBf>* __res
   const size_t c0 = (size_t)blk * d.cpb;  // the block's first chunk
   const auto one = [](int) { return 1.f; };
   // C, B and X loads in flight under the tables; X stays in registers until
-  // the B tile is free
-  // (NS = 128: one 128-wide tile in flight at a time, within the registers)
+  // the B tile is free (with a 128-wide tile, X is fetched under the products)
+  constexpr bool kEarlyX = NS == 64 && PS == 64;
   RowTile<256, kQ, Elem<kBf>, NS> ta, tb;
-  RowTile<256, kQ, Elem<kBf>> tx;
+  RowTile<256, kQ, Elem<kBf>, PS> tx;
   ta.fetch(Cm + (row0 * d.G + g) * NS, (size_t)d.G * NS);
-  if (NS == 64) {
-    tb.fetch(Bm + (row0 * d.G + g) * NS, (size_t)d.G * NS);
-    tx.fetch(x + (row0 * d.H + h) * kP, (size_t)d.H * kP);
-  }
+  if (NS == 64) tb.fetch(Bm + (row0 * d.G + g) * NS, (size_t)d.G * NS);
+  if (kEarlyX) tx.fetch(x + (row0 * d.H + h) * PS, (size_t)d.H * PS);
   step_tables(d, dt, A[h] * kLog2e, b, (size_t)blk * kQ, kQ, h, s_cs2, s_dt, scratch);
   for (int e = tid; e < 4 * kQ; e += 256) {
     const int w = e >> 7, j = e & 127, r = 32 * w;
@@ -466,17 +491,17 @@ __global__ void __launch_bounds__(256, 2) k_scan64(D64 d, const Elem<kBf>* __res
   if (NS == 128) ta.fetch(Bm + (row0 * d.G + g) * NS, (size_t)d.G * NS);
   if (NS == 64) tb.put(sBh, sBl, one);
   else ta.put(sBh, sBl, one);
-  (void)load_split_transposed<256, kBf, NS>(
-      sHh, sHl, hist + (((size_t)b * d.nc + c0) * d.H + h) * (kP * NS), nullptr);
+  (void)load_split_transposed<256, kBf, NS, PS>(
+      sHh, sHl, hist + (((size_t)b * d.nc + c0) * d.H + h) * (PS * NS), nullptr);
   fence_async_smem();
   fence_before_sync();
   __syncthreads();
   fence_after_sync();
-  const uint32_t tm = tmem_base, tCB = tm, tYs = tm + 128, tY = tm + 192;
+  const uint32_t tm = tmem_base, tCB = tm, tYs = tm + 128, tY = kWholeM ? tm : tm + 192;
   if (tid == 0) {
     // K = n: NS / 16 steps, the second 64 of n (NS = 128) at the lo tiles
     const uint32_t id_cb = idesc_bf16(128, 128, false, false);
-    const uint32_t id_ys = idesc_bf16(128, 64, false, true);
+    const uint32_t id_ys = idesc_bf16(128, PS, false, true);
     for (int kk = 0; kk < NS / 16; ++kk) {
       const uint32_t ko = (kk >> 2) * 16384 + (kk & 3) * 32;
       mma3<kBf>(tCB, smem_u32(sCh) + ko, 16384, 16, false, smem_u32(sBh) + ko, 16384, 16, id_cb,
@@ -486,7 +511,7 @@ __global__ void __launch_bounds__(256, 2) k_scan64(D64 d, const Elem<kBf>* __res
     }
     mma_commit(&bar);
   }
-  if (NS == 128) tx.fetch(x + (row0 * d.H + h) * kP, (size_t)d.H * kP);  // under the products
+  if (!kEarlyX) tx.fetch(x + (row0 * d.H + h) * PS, (size_t)d.H * PS);  // under the products
   bool ok = wait_all(&bar, 0);
   uint32_t phase = 1;
   fence_after_sync();
@@ -494,10 +519,12 @@ __global__ void __launch_bounds__(256, 2) k_scan64(D64 d, const Elem<kBf>* __res
   tx.put(sXh, sXl, one);
   const int I = row;
   const float fi = exp2f(s_cs2[I] - s_cs2[32 * q]), csI = s_cs2[I];
+  const uint32_t id_y = idesc_bf16(128, PS, false, true);
 #pragma unroll 1
   for (int half = 0; half < 2 && ok; ++half) {
     // M columns [64 half, 64 half + 64): warpgroup wg writes its 32-column chunk jc
     const int jc = 2 * half + wg;
+    uint8_t* mt = kWholeM && half ? sMl : sMh;
     {
       float v[32];
       if (jc <= q) {  // warp-uniform
@@ -519,18 +546,26 @@ __global__ void __launch_bounds__(256, 2) k_scan64(D64 d, const Elem<kBf>* __res
       }
 #pragma unroll
       for (int q4 = 0; q4 < 4; ++q4)
-        store_split8<kBf>(sMh, sMl, sw128(row, wg * 4 + q4), &v[q4 * 8]);
+        store_split8<kBf>(mt, sMl, sw128(row, wg * 4 + q4), &v[q4 * 8]);
     }
+    if (kWholeM && half == 0) continue;  // the whole M first
     fence_async_smem();
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
     if (tid == 0) {
-      // Y += M[:, half] X[half rows, :]: K = the half's 64 rows j
-      const uint32_t id_y = idesc_bf16(128, 64, false, true);
-      for (int kk = 0; kk < 4; ++kk)
-        mma3<kBf>(tY, smem_u32(sMh) + kk * 32, 16384, 16, false,
-                  smem_u32(sXh) + (4 * half + kk) * 2048, 16384, 16384, id_y, half > 0 || kk > 0);
+      if (kWholeM) {
+        // Y = M X: K = all 128 rows j (the j 64-127 half of M at the lo tile)
+        for (int kk = 0; kk < 8; ++kk)
+          mma3<kBf>(tY, smem_u32(sMh) + (kk >> 2) * 16384 + (kk & 3) * 32, 16384, 16, false,
+                    smem_u32(sXh) + kk * 2048, 16384, 16384, id_y, kk > 0);
+      } else {
+        // Y += M[:, half] X[half rows, :]: K = the half's 64 rows j
+        for (int kk = 0; kk < 4; ++kk)
+          mma3<kBf>(tY, smem_u32(sMh) + kk * 32, 16384, 16, false,
+                    smem_u32(sXh) + (4 * half + kk) * 2048, 16384, 16384, id_y,
+                    half > 0 || kk > 0);
+      }
       mma_commit(&bar);
     }
     ok = wait_all(&bar, phase);  // the M half is rewritten next
@@ -538,19 +573,20 @@ __global__ void __launch_bounds__(256, 2) k_scan64(D64 d, const Elem<kBf>* __res
     fence_after_sync();
   }
   if (ok) {
-    // y = Y + exp(cs_i) Ys + D x; warpgroup wg takes p in [32 wg, 32 wg + 32)
+    // y = Y + exp(cs_i) Ys + D x; warpgroup wg takes p in [PS/2 wg, PS/2 (wg + 1))
     const float sc = exp2f(s_cs2[row]), Dh = D[h];
-    const size_t off = ((row0 + row) * d.H + h) * kP + wg * 32;
+    const size_t off = ((row0 + row) * d.H + h) * PS + wg * (PS / 2);
 #pragma unroll
-    for (int hp = 0; hp < 2; ++hp) {
+    for (int hp = 0; hp < PS / 32; ++hp) {
       float yv[16], yst[16];
-      tmem_ld16(tY + lane_base + wg * 32 + hp * 16, yv);
-      tmem_ld16(tYs + lane_base + wg * 32 + hp * 16, yst);
+      tmem_ld16(tY + lane_base + wg * (PS / 2) + hp * 16, yv);
+      tmem_ld16(tYs + lane_base + wg * (PS / 2) + hp * 16, yst);
       tmem_wait_ld();
 #pragma unroll
       for (int k8 = 0; k8 < 2; ++k8) {
+        const int cw = (wg * (PS / 2) + hp * 16) / 8 + k8;  // 8-column chunk of the row
         float xf[8], o[8];
-        read_split8<kBf>(sXh, sXl, sw128(row, wg * 4 + hp * 2 + k8), xf);
+        read_split8<kBf>(sXh + (cw >> 3) * 16384, sXl, sw128(row, cw & 7), xf);
 #pragma unroll
         for (int t = 0; t < 8; ++t) o[t] = fmaf(sc, yst[k8 * 8 + t], yv[k8 * 8 + t]) + Dh * xf[t];
         st8(y + off + hp * 16 + k8 * 8, o);
@@ -594,9 +630,11 @@ __device__ __forceinline__ float col_sum16(float (&v)[16]) {
 //   dcs_i = rowsum_i - colsum_i + statein_i - e_i (+ sum_j e_j +
 //            exp(cs_last) <g, H> at i = Q - 1); da_j = sum_{i >= j} dcs_i;
 //            ddt_j = drive_j + A da_j; partials sum_j dt_j da_j and sum dy.x.
+// Headdim PS = 128 (bf16, d_state 64): X, dY, H^T and g^T keep p 64-127 in
+// their lo tiles' places; Gx then takes CB's TMEM columns (CB has been read).
 constexpr uint32_t kBwdX64Bytes = 163840;  // C, B (later O) 64K | X 32K | dY 32K | H 16K | g 16K
 
-template <bool kBf, int NS>
+template <bool kBf, int NS, int PS>
 __global__ void __launch_bounds__(512, 1) k_bwd64_x(D64 d, const Elem<kBf>* __restrict__ x,
                                                     const float* __restrict__ dt,
                                                     const float* __restrict__ A,
@@ -626,6 +664,7 @@ __global__ void __launch_bounds__(512, 1) k_bwd64_x(D64 d, const Elem<kBf>* __re
   uint8_t* sHl = sm + 139264;
   uint8_t* sGh = sm + 147456;   // g^T [64 rows n][64 p]
   uint8_t* sGl = sm + 155648;
+  static_assert(PS == 64 || (PS == 128 && kBf && NS == 64), "headdim 128 is bf16, d_state 64");
   __shared__ float s_cs2[kQ], s_dt[kQ], scratch[16];
   __shared__ __align__(16) float s_E[4][kQ];    // exp(cs_r - cs_j), j < r = 32 w
   __shared__ __align__(16) float s_Edt[4][kQ];  // the same times dt_j
@@ -650,12 +689,12 @@ __global__ void __launch_bounds__(512, 1) k_bwd64_x(D64 d, const Elem<kBf>* __re
   const float Ah = A[h], Dh = D[h];
   const size_t row0 = (size_t)b * d.T + (size_t)blk * kQ;
   const size_t c0 = (size_t)blk * d.cpb, c1 = c0 + d.cpb - 1;  // first, last chunk
-  const size_t st_in = (((size_t)b * d.nc + c0) * d.H + h) * (kP * NS);
-  const size_t st_out = (((size_t)b * d.nc + c1) * d.H + h) * (kP * NS);
+  const size_t st_in = (((size_t)b * d.nc + c0) * d.H + h) * (PS * NS);
+  const size_t st_out = (((size_t)b * d.nc + c1) * d.H + h) * (PS * NS);
   const auto one = [](int) { return 1.f; };
   // two tiles' loads in flight at a time, the first two under the tables
   RowTile<512, kQ, Elem<kBf>, NS> ta, tb;
-  RowTile<512, kQ, Elem<kBf>> tc, td;
+  RowTile<512, kQ, Elem<kBf>, PS> tc, td;
   ta.fetch(Cm + (row0 * d.G + g) * NS, (size_t)d.G * NS);
   tb.fetch(Bm + (row0 * d.G + g) * NS, (size_t)d.G * NS);
   step_tables(d, dt, Ah * kLog2e, b, (size_t)blk * kQ, kQ, h, s_cs2, s_dt, scratch);
@@ -666,12 +705,12 @@ __global__ void __launch_bounds__(512, 1) k_bwd64_x(D64 d, const Elem<kBf>* __re
     s_Edt[w][j] = ev * s_dt[j];
   }
   ta.put(sCh, sCl, one);
-  tc.fetch(x + (row0 * d.H + h) * kP, (size_t)d.H * kP);
+  tc.fetch(x + (row0 * d.H + h) * PS, (size_t)d.H * PS);
   tb.put(sBh, sBl, one);
-  td.fetch(dy + (row0 * d.H + h) * kP, (size_t)d.H * kP);
-  (void)load_split_transposed<512, kBf, NS>(sHh, sHl, hist + st_in, nullptr);
+  td.fetch(dy + (row0 * d.H + h) * PS, (size_t)d.H * PS);
+  (void)load_split_transposed<512, kBf, NS, PS>(sHh, sHl, hist + st_in, nullptr);
   tc.put(sXh, sXl, one);
-  float hg = load_split_transposed<512, kBf, NS>(sGh, sGl, gstate + st_out, hist + st_in);
+  float hg = load_split_transposed<512, kBf, NS, PS>(sGh, sGl, gstate + st_out, hist + st_in);
   td.put(sYh, sYl, one);
   hg = block_sum(hg, scratch);  // <g_c, H_{c-1}> (syncs)
   fence_async_smem();
@@ -679,15 +718,18 @@ __global__ void __launch_bounds__(512, 1) k_bwd64_x(D64 d, const Elem<kBf>* __re
   __syncthreads();
   fence_after_sync();
   const uint32_t tm = tmem_base;
-  const uint32_t T0 = tm, T1 = tm + 128, TGs = tm + 256, TCH = tm + 320, TGx = tm + 384;
+  const uint32_t T0 = tm, T1 = tm + 128, TGs = tm + 256, TCH = tm + 256 + PS;
+  const uint32_t TGx = PS == 64 ? tm + 384 : T0;
   if (tid == 0) {
     const uint32_t id_sq = idesc_bf16(128, 128, false, false);
-    const uint32_t id_km = idesc_bf16(128, 64, false, true);
-    // K = p (dY X^T): 4 steps; K = n (CB, Gs, CH): NS / 16 steps, the second
-    // 64 of n (NS = 128) at the lo tiles
-    for (int kk = 0; kk < 4; ++kk)
-      mma3<kBf>(T1, smem_u32(sYh) + kk * 32, 16384, 16, false, smem_u32(sXh) + kk * 32, 16384,
-                16, id_sq, kk > 0);
+    const uint32_t id_km = idesc_bf16(128, PS, false, true);
+    // K = p (dY X^T): PS / 16 steps; K = n (CB, Gs, CH): NS / 16 steps; the
+    // second 64 of p or n at the lo tiles
+    for (int kk = 0; kk < PS / 16; ++kk) {
+      const uint32_t ko = (kk >> 2) * 16384 + (kk & 3) * 32;
+      mma3<kBf>(T1, smem_u32(sYh) + ko, 16384, 16, false, smem_u32(sXh) + ko, 16384, 16, id_sq,
+                kk > 0);
+    }
     for (int kk = 0; kk < NS / 16; ++kk) {
       const uint32_t ko = (kk >> 2) * 16384 + (kk & 3) * 32;
       mma3<kBf>(T0, smem_u32(sCh) + ko, 16384, 16, false, smem_u32(sBh) + ko, 16384, 16, id_sq,
@@ -765,7 +807,7 @@ __global__ void __launch_bounds__(512, 1) k_bwd64_x(D64 d, const Elem<kBf>* __re
   fence_after_sync();
   if (tid == 0 && ok) {
     // Gx = O^T dY: M = j (O as MN-major, two 64-column blocks), K = i, N = p
-    const uint32_t id = idesc_bf16(128, 64, true, true);
+    const uint32_t id = idesc_bf16(128, PS, true, true);
     for (int kk = 0; kk < 8; ++kk)
       mma3<kBf>(TGx, smem_u32(sOh) + kk * 2048, 32768, 16384, true, smem_u32(sYh) + kk * 2048,
                 16384, 16384, id, kk > 0);
@@ -775,23 +817,26 @@ __global__ void __launch_bounds__(512, 1) k_bwd64_x(D64 d, const Elem<kBf>* __re
   fence_after_sync();
 
   // ---- epilogue: this thread's row (j for dx, drive, e; i for statein), p in
-  // [16 wg, 16 wg + 16)
+  // [PS/4 wg, PS/4 (wg + 1))
   const float last2 = s_cs2[kQ - 1];
   const float fj = exp2f(last2 - s_cs2[row]), dtj = s_dt[row];
   float drive = 0.f, ej = 0.f, stin = 0.f, dd = 0.f;
   if (ok) {
-    const size_t off = ((row0 + row) * d.H + h) * kP + wg * 16;
-    {
+    const size_t off = ((row0 + row) * d.H + h) * PS + wg * (PS / 4);
+#pragma unroll
+    for (int hp = 0; hp < PS / 64; ++hp) {
+      const int pc = wg * (PS / 4) + hp * 16;  // the 16 columns of this pass
       float gx[16], gs[16], ch[16];
-      tmem_ld16(TGx + lane_base + wg * 16, gx);
-      tmem_ld16(TGs + lane_base + wg * 16, gs);
-      tmem_ld16(TCH + lane_base + wg * 16, ch);
+      tmem_ld16(TGx + lane_base + pc, gx);
+      tmem_ld16(TGs + lane_base + pc, gs);
+      tmem_ld16(TCH + lane_base + pc, ch);
       tmem_wait_ld();
 #pragma unroll
       for (int k8 = 0; k8 < 2; ++k8) {
+        const int cw = pc / 8 + k8;  // 8-column chunk of the row
         float xa[8], ya[8], o[8];
-        read_split8<kBf>(sXh, sXl, sw128(row, wg * 2 + k8), xa);
-        read_split8<kBf>(sYh, sYl, sw128(row, wg * 2 + k8), ya);
+        read_split8<kBf>(sXh + (cw >> 3) * 16384, sXl, sw128(row, cw & 7), xa);
+        read_split8<kBf>(sYh + (cw >> 3) * 16384, sYl, sw128(row, cw & 7), ya);
 #pragma unroll
         for (int t = 0; t < 8; ++t) {
           const int m = 8 * k8 + t;
@@ -802,7 +847,7 @@ __global__ void __launch_bounds__(512, 1) k_bwd64_x(D64 d, const Elem<kBf>* __re
           stin = fmaf(ya[t], ch[m], stin);
           dd = fmaf(ya[t], xa[t], dd);
         }
-        st8(dx + off + k8 * 8, o);
+        st8(dx + off + hp * 16 + k8 * 8, o);
       }
     }
   }
@@ -861,9 +906,11 @@ __global__ void __launch_bounds__(512, 1) k_bwd64_x(D64 d, const Elem<kBf>* __re
 //   dC += (e o dY) H,  dB += (f o X) g      (TMEM accumulators over heads).
 // After the segment: W into split tiles, dC += W B, dB += W^T C, and the fp32
 // sums of the segment written as partials [unit][segment][dC|dB][128][64].
+// Headdim PS = 128 (bf16, d_state 64): X, dY keep p 64-127 in their lo
+// tiles' places and H, g their rows p 64-127.
 constexpr uint32_t kBwdBC64Bytes = 163840;  // B 32K | C 32K | X 32K | dY 32K | H 16K | g 16K
 
-template <bool kBf, int NS>
+template <bool kBf, int NS, int PS>
 __global__ void __launch_bounds__(512, 1) k_bwd64_bc(D64 d, int seg_heads,
                                                      const Elem<kBf>* __restrict__ x,
                                                      const float* __restrict__ dt,
@@ -931,25 +978,26 @@ __global__ void __launch_bounds__(512, 1) k_bwd64_bc(D64 d, int seg_heads,
   const int I = row, jc = wg;  // this thread's row and 32-column chunk of W
   // a head's tiles are fetched into registers while the previous head's
   // state-term products run (the first head's before the loop)
-  RowTile<512, kQ, Elem<kBf>> tx, ty;
-  StateRowTile<512, NS, kBf> th, tg;  // the states as rows p of NS values
-  // (NS = 128: the state tiles are fetched at the head's start instead, to
-  // stay within the registers)
+  RowTile<512, kQ, Elem<kBf>, PS> tx, ty;
+  StateRowTile<512, NS, kBf, PS> th, tg;  // the states as rows p of NS values
+  // (NS = 128 or PS = 128: the state tiles are fetched at the head's start
+  // instead, to stay within the registers)
+  constexpr bool kEarlyStates = NS == 64 && PS == 64;
   auto fetch_states = [&](int h) {
-    const size_t st_in = (((size_t)b * d.nc + c0) * d.H + h) * (kP * NS);
-    const size_t st_out = (((size_t)b * d.nc + c1) * d.H + h) * (kP * NS);
+    const size_t st_in = (((size_t)b * d.nc + c0) * d.H + h) * (PS * NS);
+    const size_t st_out = (((size_t)b * d.nc + c1) * d.H + h) * (PS * NS);
     th.fetch(hist + st_in);
     tg.fetch(gstate + st_out);
   };
   auto fetch_head = [&](int h) {
-    tx.fetch(x + (row0 * d.H + h) * kP, (size_t)d.H * kP);
-    ty.fetch(dy + (row0 * d.H + h) * kP, (size_t)d.H * kP);
-    if (NS == 64) fetch_states(h);
+    tx.fetch(x + (row0 * d.H + h) * PS, (size_t)d.H * PS);
+    ty.fetch(dy + (row0 * d.H + h) * PS, (size_t)d.H * PS);
+    if (kEarlyStates) fetch_states(h);
   };
   if (nh > 0) fetch_head(h0);
   for (int hh = 0; hh < nh && ok; ++hh) {
     const int h = h0 + hh;
-    if (NS == 128) fetch_states(h);
+    if (!kEarlyStates) fetch_states(h);
     step_tables(d, dt, A[h] * kLog2e, b, (size_t)blk * kQ, kQ, h, s_cs2, s_dt, scratch);
     for (int e = tid; e < 4 * kQ; e += 512) {
       const int w = e >> 7, j = e & 127, r = 32 * w;
@@ -964,10 +1012,13 @@ __global__ void __launch_bounds__(512, 1) k_bwd64_bc(D64 d, int seg_heads,
     __syncthreads();
     fence_after_sync();
     if (tid == 0) {
+      // K = p: PS / 16 steps, p 64-127 (PS = 128) at the lo tiles
       const uint32_t id = idesc_bf16(128, 128, false, false);
-      for (int kk = 0; kk < 4; ++kk)
-        mma3<kBf>(T1, smem_u32(sYh) + kk * 32, 16384, 16, false, smem_u32(sXh) + kk * 32, 16384,
-                  16, id, kk > 0);
+      for (int kk = 0; kk < PS / 16; ++kk) {
+        const uint32_t ko = (kk >> 2) * 16384 + (kk & 3) * 32;
+        mma3<kBf>(T1, smem_u32(sYh) + ko, 16384, 16, false, smem_u32(sXh) + ko, 16384, 16, id,
+                  kk > 0);
+      }
       mma_commit(&bar);
     }
     ok = wait_all(&bar, phase);
@@ -999,20 +1050,24 @@ __global__ void __launch_bounds__(512, 1) k_bwd64_bc(D64 d, int seg_heads,
     // X, dY rescaled in place (the dYX product has read them): X rows j by
     // exp(cs_last - cs_j) dt_j, dY rows i by exp(cs_i)
     const float last2 = s_cs2[kQ - 1];
-    rescale_split<512, kQ, kBf>(sXh, sXl, [&](int r) { return exp2f(last2 - s_cs2[r]) * s_dt[r]; });
-    rescale_split<512, kQ, kBf>(sYh, sYl, [&](int r) { return exp2f(s_cs2[r]); });
+    rescale_split<512, kQ, kBf, PS>(sXh, sXl,
+                                    [&](int r) { return exp2f(last2 - s_cs2[r]) * s_dt[r]; });
+    rescale_split<512, kQ, kBf, PS>(sYh, sYl, [&](int r) { return exp2f(s_cs2[r]); });
     fence_async_smem();
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
     if (tid == 0) {
-      // N = n: NS (the second 64 of n at the lo tiles, 8 KB on)
+      // N = n: NS (the second 64 of n at the lo tiles, 8 KB on); K = p:
+      // PS / 16 steps (p 64-127 of X, dY at their lo tiles; rows p of H, g
+      // continue there)
       const uint32_t id = idesc_bf16(128, NS, false, true);
-      for (int kk = 0; kk < 4; ++kk) {
-        mma3<kBf>(TdC, smem_u32(sYh) + kk * 32, 16384, 16, false, smem_u32(sHh) + kk * 2048,
-                  8192, 8192, id, hh > 0 || kk > 0);
-        mma3<kBf>(TdB, smem_u32(sXh) + kk * 32, 16384, 16, false, smem_u32(sGh) + kk * 2048,
-                  8192, 8192, id, hh > 0 || kk > 0);
+      for (int kk = 0; kk < PS / 16; ++kk) {
+        const uint32_t ko = (kk >> 2) * 16384 + (kk & 3) * 32;
+        mma3<kBf>(TdC, smem_u32(sYh) + ko, 16384, 16, false, smem_u32(sHh) + kk * 2048, 8192,
+                  8192, id, hh > 0 || kk > 0);
+        mma3<kBf>(TdB, smem_u32(sXh) + ko, 16384, 16, false, smem_u32(sGh) + kk * 2048, 8192,
+                  8192, id, hh > 0 || kk > 0);
       }
       mma_commit(&bar);
     }
@@ -1112,34 +1167,34 @@ cudaError_t set_smem64(K kernel, size_t bytes) {
   return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
 }
 
-template <bool kBf, int NS>
+template <bool kBf, int NS, int PS>
 cudaError_t chunk_outer_t(const Problem& p, int mode, float* out) {
   using E = Elem<kBf>;
   const size_t smem = 65536 + 1024;
   cudaError_t e;
   if (mode == 0) {
-    if ((e = set_smem64(k_outer64<0, kBf, NS>, smem)) != cudaSuccess) return e;
+    if ((e = set_smem64(k_outer64<0, kBf, NS, PS>, smem)) != cudaSuccess) return e;
     LaunchScope ls("chunk_state_tc64", p.stream);
-    k_outer64<0, kBf, NS><<<dim3(p.nc, p.H, p.B), 256, smem, p.stream>>>(
+    k_outer64<0, kBf, NS, PS><<<dim3(p.nc, p.H, p.B), 256, smem, p.stream>>>(
         d64_of(p), (const E*)p.x, (const E*)p.Bm, p.dt, p.A, out, p.cs_last);
   } else {
-    if ((e = set_smem64(k_outer64<1, kBf, NS>, smem)) != cudaSuccess) return e;
+    if ((e = set_smem64(k_outer64<1, kBf, NS, PS>, smem)) != cudaSuccess) return e;
     LaunchScope ls("chunk_dstate_tc64", p.stream);
-    k_outer64<1, kBf, NS><<<dim3(p.nc, p.H, p.B), 256, smem, p.stream>>>(
+    k_outer64<1, kBf, NS, PS><<<dim3(p.nc, p.H, p.B), 256, smem, p.stream>>>(
         d64_of(p), (const E*)p.dy, (const E*)p.Cm, p.dt, p.A, out, p.cs_last);
   }
   return cudaGetLastError();
 }
 
-template <bool kBf, int NS>
+template <bool kBf, int NS, int PS>
 cudaError_t forward_scan_t(const Problem& p) {
   using E = Elem<kBf>;
   const size_t smem = kScan64Bytes + 1024;
-  cudaError_t e = set_smem64(k_scan64<kBf, NS>, smem);
+  cudaError_t e = set_smem64(k_scan64<kBf, NS, PS>, smem);
   if (e != cudaSuccess) return e;
   {
     LaunchScope ls("chunk_scan_tc64", p.stream);
-    k_scan64<kBf, NS><<<dim3(p.T / kQ, p.H, p.B), 256, smem, p.stream>>>(
+    k_scan64<kBf, NS, PS><<<dim3(p.T / kQ, p.H, p.B), 256, smem, p.stream>>>(
         d64_of(p), (const E*)p.x, p.dt, p.A, (const E*)p.Bm, (const E*)p.Cm, p.D, p.hist,
         (E*)p.y);
   }
@@ -1148,14 +1203,17 @@ cudaError_t forward_scan_t(const Problem& p) {
 
 }  // namespace
 
-// headdim 64; d_state 64 (fp32 or bf16) or 128 (bf16, chunks below 128: the
-// bf16 kernels of ssd_tc.cu take chunks 128 and 256); chunk in {16, 32, 64,
-// 128}; seqlen a multiple of 128
+// chunk in {16, 32, 64, 128}, seqlen a multiple of 128, and
+//   headdim 64, d_state 64 (fp32 or bf16);
+//   headdim 64, d_state 128 (bf16, chunks below 128: the bf16 kernels of
+//     ssd_tc.cu take chunks 128 and 256);
+//   headdim 128, d_state 64 (bf16).
 bool tc64_supported(const Problem& p) {
   if (tc_forced_simt()) return false;
-  if (p.P != kP || p.T % kQ != 0) return false;
+  if (p.T % kQ != 0) return false;
   if (p.Q != 16 && p.Q != 32 && p.Q != 64 && p.Q != 128) return false;
-  return p.N == 64 || (p.N == 128 && p.bf16 && p.Q < 128);
+  if (p.P == 64) return p.N == 64 || (p.N == 128 && p.bf16 && p.Q < 128);
+  return p.P == 128 && p.N == 64 && p.bf16;
 }
 
 // Heads per segment of the dB, dC kernel (one CTA per SM): the number of
@@ -1189,29 +1247,32 @@ size_t tc64_bc_part_floats(const Problem& p) {
 }
 
 cudaError_t tc64_chunk_outer(const Problem& p, int mode, float* out) {
-  if (!p.bf16) return chunk_outer_t<false, 64>(p, mode, out);
-  return p.N == 128 ? chunk_outer_t<true, 128>(p, mode, out) : chunk_outer_t<true, 64>(p, mode, out);
+  if (!p.bf16) return chunk_outer_t<false, 64, 64>(p, mode, out);
+  if (p.P == 128) return chunk_outer_t<true, 64, 128>(p, mode, out);
+  return p.N == 128 ? chunk_outer_t<true, 128, 64>(p, mode, out)
+                    : chunk_outer_t<true, 64, 64>(p, mode, out);
 }
 
 cudaError_t tc64_forward_scan(const Problem& p) {
-  if (!p.bf16) return forward_scan_t<false, 64>(p);
-  return p.N == 128 ? forward_scan_t<true, 128>(p) : forward_scan_t<true, 64>(p);
+  if (!p.bf16) return forward_scan_t<false, 64, 64>(p);
+  if (p.P == 128) return forward_scan_t<true, 64, 128>(p);
+  return p.N == 128 ? forward_scan_t<true, 128, 64>(p) : forward_scan_t<true, 64, 64>(p);
 }
 
 namespace {
-template <bool kBf, int NS>
+template <bool kBf, int NS, int PS>
 cudaError_t backward_t(const Problem& p) {
   using E = Elem<kBf>;
   cudaError_t e;
-  if ((e = chunk_outer_t<kBf, NS>(p, 1, p.dstate)) != cudaSuccess) return e;
+  if ((e = chunk_outer_t<kBf, NS, PS>(p, 1, p.dstate)) != cudaSuccess) return e;
   if ((e = simt_state_pass_bwd(p)) != cudaSuccess) return e;
   const D64 d = d64_of(p);
   const int nb = p.T / kQ;
   {
     const size_t smem = kBwdX64Bytes + 1024;
-    if ((e = set_smem64(k_bwd64_x<kBf, NS>, smem)) != cudaSuccess) return e;
+    if ((e = set_smem64(k_bwd64_x<kBf, NS, PS>, smem)) != cudaSuccess) return e;
     LaunchScope ls("bwd_x_tc64", p.stream);
-    k_bwd64_x<kBf, NS><<<dim3(nb, p.H, p.B), 512, smem, p.stream>>>(
+    k_bwd64_x<kBf, NS, PS><<<dim3(nb, p.H, p.B), 512, smem, p.stream>>>(
         d, (const E*)p.x, p.dt, p.A, (const E*)p.Bm, (const E*)p.Cm, p.D, (const E*)p.dy,
         p.hist, p.dstate, (E*)p.dx, p.ddt, p.dA_part, p.dD_part);
   }
@@ -1220,9 +1281,9 @@ cudaError_t backward_t(const Problem& p) {
   const int nseg = (p.hpg + sh - 1) / sh;
   {
     const size_t smem = kBwdBC64Bytes + 1024;
-    if ((e = set_smem64(k_bwd64_bc<kBf, NS>, smem)) != cudaSuccess) return e;
+    if ((e = set_smem64(k_bwd64_bc<kBf, NS, PS>, smem)) != cudaSuccess) return e;
     LaunchScope ls("bwd_bc_tc64", p.stream);
-    k_bwd64_bc<kBf, NS><<<dim3(nseg, nb, p.B * p.G), 512, smem, p.stream>>>(
+    k_bwd64_bc<kBf, NS, PS><<<dim3(nseg, nb, p.B * p.G), 512, smem, p.stream>>>(
         d, sh, (const E*)p.x, p.dt, p.A, (const E*)p.Bm, (const E*)p.Cm, (const E*)p.dy,
         p.hist, p.dstate, p.bwd_part);
   }
@@ -1240,8 +1301,9 @@ cudaError_t backward_t(const Problem& p) {
 // R_c, the reverse state pass (g_c in place, dh0), the dx / d(dt) kernel, the
 // dB / dC kernel and its segment sums, and the dA, dD reduction.
 cudaError_t tc64_backward(const Problem& p) {
-  if (!p.bf16) return backward_t<false, 64>(p);
-  return p.N == 128 ? backward_t<true, 128>(p) : backward_t<true, 64>(p);
+  if (!p.bf16) return backward_t<false, 64, 64>(p);
+  if (p.P == 128) return backward_t<true, 64, 128>(p);
+  return p.N == 128 ? backward_t<true, 128, 64>(p) : backward_t<true, 64, 64>(p);
 }
 
 cudaError_t tc64_read_and_clear_error(unsigned int* out) {

@@ -56,6 +56,27 @@ def test_workspace_sizes(L):
         assert L.ssd_workspace_bytes(d, 0) > 0 and L.ssd_kernel_path(d) in (0, 1)
 
 
+# (headdim, d_state, chunk, bf16, seqlen) -> 1: tensor-core kernels, 0: SIMT.
+# The block family only: the fused bf16 kernels (headdim 64, d_state 128,
+# chunk 128 or 256) also need the driver's tensor-map encoder, which a
+# machine without a GPU driver lacks; the GPU tests assert their path.
+@pytest.mark.parametrize("P,N,Q,bf,T,path", [
+    (64, 128, 64, True, 512, 1),     # block family, d_state 128
+    (64, 64, 128, False, 512, 1),    # block family, fp32 as split products
+    (64, 64, 16, True, 512, 1),
+    (128, 64, 64, True, 512, 1),     # block family, headdim 128
+    (128, 64, 128, True, 512, 1),
+    (128, 64, 64, False, 512, 0),    # headdim 128 in fp32: SIMT
+    (128, 128, 64, True, 512, 0),    # headdim 128 with d_state 128: SIMT
+    (64, 128, 64, False, 512, 0),    # d_state 128 in fp32: SIMT
+    (64, 64, 64, True, 192, 0),      # seqlen not a multiple of 128
+    (32, 64, 64, True, 512, 0),
+])
+def test_kernel_path_per_shape(L, P, N, Q, bf, T, path):
+    d = nat.make_dims(2, T, 4, P, N, 2, Q, bf)
+    assert L.ssd_kernel_path(d) == path
+
+
 @pytest.mark.parametrize("kw,code", [
     (dict(nheads=3), nat.SSD_ERR_INVALID_ARG),      # H % G
     (dict(batch=0), nat.SSD_ERR_INVALID_ARG),

@@ -1,6 +1,7 @@
-"""GPU parity of the headdim-64 block family of tensor-core kernels
-(d_state 64 in fp32 or bf16, d_state 128 in bf16 at chunks below 128; chunk
-16-128 processed as 128-step blocks; fp32 storage with every product as three
+"""GPU parity of the block family of tensor-core kernels (headdim 64 with
+d_state 64 in fp32 or bf16, or d_state 128 in bf16 at chunks below 128;
+headdim 128 with d_state 64 in bf16; chunk 16-128 processed as 128-step
+blocks; fp32 storage with every product as three
 bf16 tcgen05 MMAs over hi/lo splits, bf16 storage with one MMA per product)
 against the float64 oracle at the storage type's tolerance, on every output;
 the kernels that ran are checked through the trace.
@@ -42,7 +43,7 @@ def traced_run(nat, dims, dev, history="given"):
 
 
 CASES = [
-    # (B, T, H, G, Q, storage, h0, dt mode, d_state)
+    # (B, T, H, G, Q, storage, h0, dt mode, d_state[, headdim = 64])
     (1, 128, 2, 1, 128, "f32", False, "softplus", 64),     # one chunk
     (2, 512, 3, 1, 128, "f32", True, "softplus", 64),      # odd head count
     (1, 384, 4, 2, 128, "f32", True, "decay_span", 64),    # decays down to 1e-4 per step
@@ -63,15 +64,26 @@ CASES = [
     (1, 512, 6, 1, 32, "bf16", True, "decay_span", 128),
     (1, 256, 8, 4, 16, "bf16", False, "softplus", 128),
     (1, 2048, 16, 1, 64, "bf16", True, "softplus", 128),   # several head segments
+    (2, 512, 4, 2, 128, "bf16", True, "softplus", 64, 128),    # headdim 128 (bf16)
+    (1, 512, 6, 3, 64, "bf16", True, "decay_span", 64, 128),
+    (2, 256, 4, 1, 32, "bf16", False, "softplus", 64, 128),
+    (1, 256, 8, 4, 16, "bf16", True, "softplus", 64, 128),
+    (1, 2048, 16, 1, 128, "bf16", True, "softplus", 64, 128),  # several head segments
 ]
 
 
-@pytest.mark.parametrize("case", CASES, ids=lambda c: "b{}t{}h{}g{}q{}n{}{}{}_{}".format(
-    c[0], c[1], c[2], c[3], c[4], c[8], c[5], "_h0" if c[6] else "", c[7]))
+def _case_id(c):
+    P = c[9] if len(c) > 9 else 64
+    return "b{}t{}h{}g{}q{}p{}n{}{}{}_{}".format(c[0], c[1], c[2], c[3], c[4], P, c[8], c[5],
+                                                 "_h0" if c[6] else "", c[7])
+
+
+@pytest.mark.parametrize("case", CASES, ids=_case_id)
 def test_tc64_every_output_against_oracle(nat, case):
-    Bz, T, H, G, Q, io, h0, mode, N = case
-    dims = synth.Dims(Bz, T, H, 64, N, G, Q, io)
-    assert nat.lib().ssd_kernel_path(nat.make_dims(Bz, T, H, 64, N, G, Q, io == "bf16")) == 1
+    Bz, T, H, G, Q, io, h0, mode, N = case[:9]
+    P = case[9] if len(case) > 9 else 64
+    dims = synth.Dims(Bz, T, H, P, N, G, Q, io)
+    assert nat.lib().ssd_kernel_path(nat.make_dims(Bz, T, H, P, N, G, Q, io == "bf16")) == 1
     inp = synth.make_inputs(dims, 100 + T + H + Q, h0, mode)
     gpu, names = traced_run(nat, dims, to_device(dims, inp))
     assert TC64_FWD | TC64_BWD <= names, names
@@ -130,6 +142,21 @@ def test_tc64_bf16_d_state_128_agrees_with_simt_path(nat):
     dev = to_device(dims, inp)
     tc, names = traced_run(nat, dims, dev)
     assert "bwd_x_tc64" in names, names
+    nat.check(nat.lib().ssd_force_kernel_path(0))
+    try:
+        simt = run_gpu(dims, dev)
+    finally:
+        nat.check(nat.lib().ssd_force_kernel_path(-1))
+    for k in tc:
+        assert rel_err(tc[k], simt[k]) < TOL["bf16"], k
+
+
+def test_tc64_bf16_headdim_128_agrees_with_simt_path(nat):
+    dims = synth.Dims(1, 512, 4, 128, 64, 2, 64, "bf16")
+    inp = synth.make_inputs(dims, 47, True, "softplus")
+    dev = to_device(dims, inp)
+    tc, names = traced_run(nat, dims, dev)
+    assert TC64_FWD | TC64_BWD <= names, names
     nat.check(nat.lib().ssd_force_kernel_path(0))
     try:
         simt = run_gpu(dims, dev)

@@ -146,18 +146,6 @@ __device__ __forceinline__ float load_dt_256(const TcDims& d, const float* __res
                     : 0.f;
 }
 
-// Chunk-local inclusive cumsum (log2 units) of the dt values the 256 threads hold.
-__device__ __forceinline__ void chunk_cumsum_256v(const TcDims& d, float dv, float a2,
-                                                  float* s_cs2, float* s_dt, float* scratch) {
-  const int tid = threadIdx.x;
-  const float cs = block_inclusive_scan(dv * a2, scratch);
-  if (tid < d.Q) {
-    s_cs2[tid] = cs;
-    s_dt[tid] = dv;
-  }
-  __syncthreads();
-}
-
 // Chunk-local inclusive cumsum (log2 units) with 256 threads, one value each.
 template <bool kRaw = false>
 __device__ __forceinline__ void chunk_cumsum_256(const TcDims& d, const float* __restrict__ dt,
@@ -1262,6 +1250,15 @@ k_fwd_single_tc(const __grid_constant__ ScanMaps maps, TcDims d, const float* __
 // and the per-block formulas of the chunked backward (see ssd_simt.cu).  The
 // strict row and column sums of M_ij = W_ij (C_i.B_j) come from the rows the
 // threads hold (row sums) and a warp-transposed reduction (column sums).
+// 4-byte asynchronous global -> shared copy, and the wait for this thread's copies
+__device__ __forceinline__ void cp_async4(float* smem, const float* gmem) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(smem)), "l"(gmem)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
 struct BwdMaps {
   CUtensorMap x;   // [B*T][H*P] bf16, box {64, 128}
   CUtensorMap dy;  // [B*T][H*P] bf16, box {64, 128}
@@ -1305,14 +1302,17 @@ k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, long long nitems,
   uint8_t* sH = sm + kBwH;
   uint8_t* sG = sm + kBwG;
   uint8_t* sW = sm + kBwW;
-  __shared__ float s_cs2[256], s_dt[256], scratch[16];
+  // decay tables of the current head, and the next head's (s_cs2n, s_dtn),
+  // built by warpgroups 1-3 while warpgroup 0 finishes the current head; at
+  // the next head's start they are copied into place and give s_E, s_Edt
+  __shared__ float s_cs2[256], s_dt[256], s_cs2n[256], s_dtn[256];
   __shared__ __align__(16) float s_E[4][128];    // exp(cs_r - cs_J), J < r = base + 32 q
   __shared__ __align__(16) float s_Edt[4][128];  // the same times dt_J
   __shared__ float s_col[4][128];                // per-warp strict column sums of M
   __shared__ float s_rs[3][128];                 // row-sum partials of warpgroups 1-3
-  __shared__ float s_v[128];
-  __shared__ float2 s_v2[128], scratch2[16];
-  __shared__ float s_esum;
+  __shared__ float s_hg[4][128];                 // <gout, Hin> partials per warpgroup and row
+  __shared__ float4 s_wtot[4];                   // warpgroup 0: per-warp totals (d(cs), e, <g, H>)
+  __shared__ float2 s_wad[4];                    // warpgroup 0: per-warp dA, dD partials
   __shared__ float s_gsum[4];  // raw-dt mode: per-warp sums of the dt_raw gradient
   __shared__ uint64_t bar_shared, bar_head, bar_mma;
   __shared__ uint32_t tmem_base;
@@ -1396,6 +1396,43 @@ k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, long long nitems,
     tma_load_2d(sB, &maps.B, gg * d.N, row0_u, &bar_shared);
     tma_load_2d(sB + 16384, &maps.B, gg * d.N + 64, row0_u, &bar_shared);
   };
+  // dt of step tid - 256 of chunk cc, head hh, in the threads of warpgroups
+  // 2 and 3 (0 past the chunk and in the other threads)
+  auto load_dt_hi = [&](int bb, int cc, int hh) -> float {
+    const int r = tid - 256;
+    return r >= 0 && r < d.Q ? dt[((size_t)bb * d.T + (size_t)cc * d.Q + r) * d.H + hh] : 0.f;
+  };
+  // The next head's cumsum into s_cs2n (threads of warpgroups 1-3 only,
+  // `sync` a barrier over them, after warpgroups 2-3 have staged dt in
+  // s_dtn): warp 4 scans dt * A (log2 units, a2) over the 256 steps (eight
+  // steps per lane in order, then the lanes).
+  auto build_tables = [&](float a2, auto&& sync) {
+    float* ncs = s_cs2n;
+    const float* ndt = s_dtn;
+    sync();
+    if (wg == 1 && q == 0) {
+      // the lane's eight partial sums are formed twice (the same order both
+      // times), so that few registers are live here
+      float run = 0.f;
+#pragma unroll
+      for (int t = 0; t < 8; ++t) run += ndt[lane * 8 + t] * a2;
+      float inc = run;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float t = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += t;
+      }
+      float off = __shfl_up_sync(0xffffffffu, inc, 1);
+      if (lane == 0) off = 0.f;
+      run = 0.f;
+#pragma unroll
+      for (int t = 0; t < 8; ++t) {
+        run += ndt[lane * 8 + t] * a2;
+        ncs[lane * 8 + t] = off + run;
+      }
+    }
+  };
+  const auto sync_wg123 = [] { named_sync(2, kBwThreads - 128); };
   uint32_t mma_phase = 0, head_phase = 0, shared_phase = 0;
   bool ok = true;
   for (long long x = it_begin; x < it_end && ok;) {
@@ -1423,36 +1460,55 @@ k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, long long nitems,
       tma_load_2d(sG, &maps.gt, 0, srow, &bar_head);
     }
   }
-  // dt, A and D of the next head are loaded one head ahead
-  // the next head's dt and A (raw-dt mode: dt_raw and a_log) are fetched a
-  // head ahead and transformed where they are used, so the loads stay hidden
-  float dt_next = load_dt_256<false>(d, dt, b, c, h_first);
+  // A and D of the next head are loaded one head ahead and its dt goes
+  // straight into s_dtn (raw-dt mode: dt_raw and a_log, transformed where
+  // they are used), so the loads stay hidden; the first head's tables are
+  // built here, the others' at the end of the head before them
   float A_next = kRaw ? d.a_log[h_first] : A[h_first], D_next = D[h_first];
+  {
+    const float dt0 = load_dt_hi(b, c, h_first);
+    if (wg >= 2)
+      s_dtn[tid - 256] = (kRaw && tid - 256 < d.Q) ? dt_of<kRaw>(d, dt0, h_first) : dt0;
+    if (wg > 0) build_tables((kRaw ? -expf(A_next) : A_next) * kLog2e, sync_wg123);
+    __syncthreads();
+  }
   ok = wait_or_flag(&bar_shared, shared_phase);
   shared_phase ^= 1;
 
   for (int hh = 0; hh < kh && ok; ++hh) {
     const int h = h_first + hh;
-    const float dv = (kRaw && tid < d.Q) ? dt_of<kRaw>(d, dt_next, h) : dt_next;
     const float Ah = kRaw ? -expf(A_next) : A_next, Dh = D_next;
     if (hh + 1 < kh) {
-      dt_next = load_dt_256<false>(d, dt, b, c, h + 1);
       A_next = kRaw ? d.a_log[h + 1] : A[h + 1];
       D_next = D[h + 1];
     }
-    chunk_cumsum_256v(d, dv, Ah * kLog2e, s_cs2, s_dt, scratch);
-    for (int e = tid; e < 4 * 128; e += kBwThreads) {
-      const int w = e >> 7, jj = e & 127;
+    // this head's tables into place, and s_E, s_Edt from them (published by
+    // the barrier of the wait below)
+    if (tid < 256)
+      s_cs2[tid] = s_cs2n[tid];
+    else
+      s_dt[tid - 256] = s_dtn[tid - 256];
+    {
+      const int w = tid >> 7, jj = tid & 127;
       const int r = base + 32 * w, J = base + jj;
-      const float ev = (J < r) ? exp2f(s_cs2[r] - s_cs2[J]) : 0.f;
+      const float ev = (J < r) ? exp2f(s_cs2n[r] - s_cs2n[J]) : 0.f;
       s_E[w][jj] = ev;
-      s_Edt[w][jj] = ev * s_dt[J];
+      s_Edt[w][jj] = ev * s_dtn[J];
     }
-    const float ref2 = k == 0 ? 0.f : s_cs2[base - 1];
-    const float end2 = s_cs2[base + 127];
+    const float ref2 = k == 0 ? 0.f : s_cs2n[base - 1];
+    const float end2 = s_cs2n[base + 127];
     ok = wait_or_flag(&bar_head, head_phase);  // also publishes the tables
     head_phase ^= 1;
     if (!ok) break;
+    // the next head's dt into s_dtn (read above for this head's tables), by
+    // asynchronous copies that warpgroups 2-3 wait for where they use them
+    if (wg >= 2 && hh + 1 < kh) {
+      const int r = tid - 256;
+      if (r < d.Q)
+        cp_async4(&s_dtn[r], dt + ((size_t)b * d.T + (size_t)c * d.Q + r) * d.H + h + 1);
+      else
+        s_dtn[r] = 0.f;
+    }
 
     // ---- mid-chunk state or state gradient (chunks of two blocks)
     if (two) {
@@ -1491,21 +1547,26 @@ k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, long long nitems,
         store_row_bf16(tile, row, wg * 2 + q4, f);
       }
     }
-    // <gout, Hin> over this thread's quarter row (bf16 operands, fp32 sum)
-    float hg = 0.f;
+    // <gout, Hin> over this thread's quarter row (bf16 operands, fp32 sum);
+    // summed over the block with the d(cs) suffix sums at the end of the head
+    {
+      float hg = 0.f;
 #pragma unroll
-    for (int q4 = 0; q4 < 2; ++q4) {
-      float fh[8], fg[8];
-      unpack8(*(const uint4*)(sH + sw128(row, wg * 2 + q4)), fh);
-      unpack8(*(const uint4*)(sG + sw128(row, wg * 2 + q4)), fg);
+      for (int q4 = 0; q4 < 2; ++q4) {
+        float fh[8], fg[8];
+        unpack8(*(const uint4*)(sH + sw128(row, wg * 2 + q4)), fh);
+        unpack8(*(const uint4*)(sG + sw128(row, wg * 2 + q4)), fg);
 #pragma unroll
-      for (int t = 0; t < 8; ++t) hg = fmaf(fh[t], fg[t], hg);
+        for (int t = 0; t < 8; ++t) hg = fmaf(fh[t], fg[t], hg);
+      }
+      s_hg[wg][row] = hg;
     }
-    hg = block_sum(hg, scratch);
-    fence_async_smem();
-    fence_before_sync();
-    __syncthreads();
-    fence_after_sync();
+    if (two) {  // every thread's T1 reads before the next products reuse T1
+      fence_async_smem();
+      fence_before_sync();
+      __syncthreads();
+      fence_after_sync();
+    }
 
     // ---- phase A: CB = C_k B_k^T -> T0 ; dYX = dY_k X_k^T -> T1
     if (tid == 0) {
@@ -1695,11 +1756,12 @@ k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, long long nitems,
           stin = fmaf(yf[t], ch[m], stin);
           dd = fmaf(yf[t], xf[t], dd);
         }
-        store_row_bf16(sW, row, wg * 2 + q4, o8);  // dx staging: tile [128 rows][64 p]
+        store_row_bf16(sO, row, wg * 2 + q4, o8);  // dx staging: tile [128 rows][64 p]
       }
     }
-    // partials of warpgroups 1-3 go through sO (L o CB was last read by the Gx product)
-    float* ered = (float*)sO;
+    // dx is staged in sO (L o CB was last read by the Gx product), the
+    // partials of warpgroups 1-3 16 KB further on
+    float* ered = (float*)(sO + 16384);
     if (wg > 0) {
       ered[((wg - 1) * 4 + 0) * 128 + row] = drive;
       ered[((wg - 1) * 4 + 1) * 128 + row] = ej;
@@ -1709,20 +1771,23 @@ k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, long long nitems,
     fence_async_smem();
     __syncthreads();
     if (tid == 0) {
-      tma_store_2d(&maps.dx, sW, h * d.P, row0);
+      tma_store_2d(&maps.dx, sO, h * d.P, row0);
       bulk_commit();
     }
     // phase D done: X, dY, Hin, gout are free and the next head's tiles go out
-    // now, under this head's dcs work (the B_0 / C_1 tile of chunks of two
-    // blocks lands in sW once the dx store has read it)
+    // now, under this head's dcs work (issued from warpgroup 3, which has
+    // slack here, so that warpgroup 0's chain starts at once)
     ok = wait_or_flag(&bar_mma, mma_phase);
     mma_phase ^= 1;
     fence_after_sync();
-    if (tid == 0 && ok && hh + 1 < kh) {
-      if (two) bulk_wait_read0();
-      issue_head_loads(u, h + 1, true);
-    }
+    if (tid == kBwThreads - 128 && ok && hh + 1 < kh) issue_head_loads(u, h + 1, true);
     if (wg == 0) {
+      // ---- dcs, its suffix sums (da), ddt, dA and dD partials: warpgroup 0,
+      // one row per thread.  The end-of-block term (sum_j e_j + exp(cs_end -
+      // ref) <gout, Hin>) sits at the last row, so it adds to every da_j: the
+      // suffix sums run over dcs without it, with the totals of e and <g, H>
+      // alongside.
+      float hg = s_hg[0][row];
 #pragma unroll
       for (int w = 0; w < 3; ++w) {
         rowsum += s_rs[w][row];
@@ -1730,52 +1795,72 @@ k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, long long nitems,
         ej += ered[(w * 4 + 1) * 128 + row];
         stin += ered[(w * 4 + 2) * 128 + row];
         dd += ered[(w * 4 + 3) * 128 + row];
+        hg += s_hg[w + 1][row];
       }
       ej *= sgs * dtI;
       stin *= exp2f(s_cs2[I] - ref2);
-    } else {
-      ej = 0.f;
-      dd = 0.f;
-    }
-    // ---- dcs, reverse cumsum, ddt, dA and dD partials (rows held by warpgroup 0).
-    // The end-of-block term (sum_j e_j + exp(cs_end - ref) <gout, Hin>) sits at the
-    // last row, so it adds to every da_j: scan dcs without it, together with e.
-    if (wg == 0) {
       float colsum = 0.f;
       for (int w = row >> 5; w < 4; ++w) colsum += s_col[w][row];
-      s_v2[row] = make_float2(rowsum - colsum + stin - ej, ej);
-    }
-    __syncthreads();
-    const float2 rv = (wg == 0) ? s_v2[127 - row] : make_float2(0.f, 0.f);
-    const float2 sc2 = block_inclusive_scan2(rv, scratch2);  // syncs: every rv read before reuse
-    const int Jr = base + 127 - row;                          // row whose da this thread holds
-    if (wg == 0) s_v[row] = drive;
-    if (tid == 127) s_esum = sc2.y;  // all e summed
-    __syncthreads();
-    const float da = sc2.x + s_esum + exp2f(end2 - ref2) * hg;
-    // ddt; raw-dt mode: the gradient w.r.t. dt_raw, ddt times sigmoid(dt_raw +
-    // dt_bias) = 1 - exp(-dt) (dt being its softplus), with per-warp sums that
-    // the barriers of the block sum below publish to thread 0
-    if (wg == 0) {
-      float gdt = s_v[127 - row] + Ah * da;
+      // suffix sums within the warp (rows row .. 32 q + 31), then the later warps' totals
+      float vd = rowsum - colsum + stin - ej, ve = ej, vh = hg;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float td = __shfl_down_sync(0xffffffffu, vd, o);
+        const float te = __shfl_down_sync(0xffffffffu, ve, o);
+        const float th = __shfl_down_sync(0xffffffffu, vh, o);
+        if (lane + o < 32) {
+          vd += td;
+          ve += te;
+          vh += th;
+        }
+      }
+      if (lane == 0) s_wtot[q] = make_float4(vd, ve, vh, 0.f);
+      named_sync(1, 128);
+      float later = 0.f, esum = 0.f, hgsum = 0.f;
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        const float4 t = s_wtot[w];
+        if (w > q) later += t.x;
+        esum += t.y;
+        hgsum += t.z;
+      }
+      const float da = (vd + later) + esum + exp2f(end2 - ref2) * hgsum;
+      // ddt; raw-dt mode: the gradient w.r.t. dt_raw, ddt times sigmoid(dt_raw
+      // + dt_bias) = 1 - exp(-dt) (dt being its softplus), with per-warp sums
+      float gdt = drive + Ah * da;
       if (kRaw) {
-        gdt *= -expm1f(-s_dt[Jr]);
+        gdt *= -expm1f(-s_dt[I]);
         float gw = gdt;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) gw += __shfl_xor_sync(0xffffffffu, gw, o);
         if (lane == 0) s_gsum[q] = gw;
       }
-      ddt[((size_t)crow + Jr) * d.H + h] = gdt;
+      ddt[((size_t)crow + I) * d.H + h] = gdt;
+      float pa = s_dt[I] * da, pd = dd;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        pa += __shfl_xor_sync(0xffffffffu, pa, o);
+        pd += __shfl_xor_sync(0xffffffffu, pd, o);
+      }
+      if (lane == 0) s_wad[q] = make_float2(pa, pd);
+      named_sync(1, 128);
+      if (tid == 0) {
+        const size_t slot = (((size_t)b * d.nc + c) * nblk + k) * d.H + h;
+        dA_part[slot] = ((s_wad[0].x + s_wad[1].x) + s_wad[2].x) + s_wad[3].x;
+        dD_part[slot] = ((s_wad[0].y + s_wad[1].y) + s_wad[2].y) + s_wad[3].y;
+        if (kRaw) dtb_part[slot] = ((s_gsum[0] + s_gsum[1]) + s_gsum[2]) + s_gsum[3];
+      }
+    } else if (hh + 1 < kh) {
+      // ---- meanwhile warpgroups 1-3 build the next head's tables
+      if (wg >= 2) {
+        cp_async_wait_all();
+        const int r = tid - 256;
+        if (kRaw && r < d.Q) s_dtn[r] = dt_of<kRaw>(d, s_dtn[r], h + 1);
+      }
+      build_tables((kRaw ? -expf(A_next) : A_next) * kLog2e, sync_wg123);
     }
-    const float2 ad = block_sum2(make_float2(wg == 0 ? s_dt[Jr] * da : 0.f, dd), scratch2);
-    if (tid == 0) {
-      const size_t slot = (((size_t)b * d.nc + c) * nblk + k) * d.H + h;
-      dA_part[slot] = ad.x;
-      dD_part[slot] = ad.y;
-      if (kRaw) dtb_part[slot] = ((s_gsum[0] + s_gsum[1]) + s_gsum[2]) + s_gsum[3];
-    }
-    // ---- end of head: the tables are rebuilt by the next head, and the dx
-    // staging (sW) by the next head's W or the final dC, dB sums
+    // ---- end of head: the next head's tables are published, and the dx
+    // staging (sO) is free for the next head's L o CB or the final dC, dB sums
     if (tid == 0) bulk_wait_read0();
     __syncthreads();
   }

@@ -1274,13 +1274,13 @@ struct BwdMaps {
 constexpr int kBwThreads = 512;       // four warpgroups share each TMEM lane quarter
 constexpr uint32_t kBwC = 0;          // C_k: 2 K-major tiles [128][128 B]
 constexpr uint32_t kBwB = 32768;      // B_k
-constexpr uint32_t kBwO = 65536;      // L o CB (2 tiles, same layout as W)
+constexpr uint32_t kBwO = 65536;      // L o CB (2 tiles, same layout as W), then dx staging
 constexpr uint32_t kBwX = 98304;      // X_k  [128 rows][64 p]
 constexpr uint32_t kBwDY = 114688;    // dY_k
-constexpr uint32_t kBwXO = 131072;    // X_0 (k = 1) or dY_1 (k = 0), row-scaled
+constexpr uint32_t kBwXO = 131072;    // X_0 (k = 1) or dY_1 (k = 0), row-scaled; then e o dY_k
 constexpr uint32_t kBwH = 147456;     // Hin  bf16, row n, 64 p
 constexpr uint32_t kBwG = 163840;     // gout bf16, row n, 64 p
-constexpr uint32_t kBwW = 180224;     // B_0 (k = 1) / C_1 (k = 0) per head, then W, then dx staging
+constexpr uint32_t kBwW = 180224;     // B_0 (k = 1) / C_1 (k = 0) per head, then W
 constexpr uint32_t kBwBytes = 212992;
 
 template <bool kRaw>
@@ -1685,14 +1685,11 @@ k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, long long nitems,
       }
       mma_commit(&bar_mma);
     }
-    ok = wait_or_flag(&bar_mma, mma_phase);
-    mma_phase ^= 1;
-    fence_after_sync();
-    if (!ok) break;
-
-    // this thread's quarter rows of x_j and dy_i (unscaled) into registers, then
-    // scale the tiles in place: X rows j by exp(cs_end - cs_j) dt_j, dY rows i by exp(cs_i - ref)
-    // (every 16-byte chunk belongs to exactly one thread: row `row`, chunks 2wg, 2wg+1)
+    // under the B and C products: this thread's quarter rows of x_j and dy_i
+    // (unscaled) into registers, X scaled in place (not an operand of those
+    // products) by exp(cs_end - cs_j) dt_j, and dY scaled by exp(cs_i - ref)
+    // into the XO tile (free since the mid-chunk product), for phase D (every
+    // 16-byte chunk belongs to exactly one thread: row `row`, chunks 2wg, 2wg+1)
     uint4 xr[2], dyr[2];
     {
       const float sx = exp2f(end2 - s_cs2[base + row]) * s_dt[base + row];
@@ -1700,9 +1697,8 @@ k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, long long nitems,
 #pragma unroll
       for (int q4 = 0; q4 < 2; ++q4) {
         uint8_t* px = sX + sw128(row, wg * 2 + q4);
-        uint8_t* py = sDY + sw128(row, wg * 2 + q4);
         xr[q4] = *(const uint4*)px;
-        dyr[q4] = *(const uint4*)py;
+        dyr[q4] = *(const uint4*)(sDY + sw128(row, wg * 2 + q4));
         float f[8];
         unpack8(xr[q4], f);
 #pragma unroll
@@ -1711,19 +1707,20 @@ k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, long long nitems,
         unpack8(dyr[q4], f);
 #pragma unroll
         for (int t = 0; t < 8; ++t) f[t] *= sy;
-        store_row_bf16(sDY, row, wg * 2 + q4, f);
+        store_row_bf16(sXO, row, wg * 2 + q4, f);
       }
     }
     fence_async_smem();
-    fence_before_sync();
-    __syncthreads();
+    ok = wait_or_flag(&bar_mma, mma_phase);  // also publishes the scaled tiles
+    mma_phase ^= 1;
     fence_after_sync();
+    if (!ok) break;
 
     // ---- phase D: dC += (e o dY_k) Hin ; dB += (f o X_k) gout   (K = p)
     if (tid == 0) {
       const uint32_t id = idesc_bf16(128, 128, false, false);
       for (int kk = 0; kk < 4; ++kk) {
-        mma_bf16(TdC, desc_sw128(smem_u32(sDY) + kk * 32, 16, 1024),
+        mma_bf16(TdC, desc_sw128(smem_u32(sXO) + kk * 32, 16, 1024),
                  desc_sw128(smem_u32(sH) + kk * 32, 16, 1024), id, 1);
         mma_bf16(TdB, desc_sw128(smem_u32(sX) + kk * 32, 16, 1024),
                  desc_sw128(smem_u32(sG) + kk * 32, 16, 1024), id, 1);

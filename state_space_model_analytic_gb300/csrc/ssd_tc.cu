@@ -265,8 +265,7 @@ k_chunk_outer_tc(const __grid_constant__ OuterMaps maps, TcDims d, const float* 
 // kScanBufs TMEM buffers of 64 columns.  Warps 4-7 (scalers) build each
 // chunk's decay tables and scale the rows of U by w in shared memory (MODE 1:
 // they also convert the fp32 history into bf16 rows).  Warps 0-3 (consumer)
-// hold the
-// running state, thread n owning row n (64 p values): per chunk they wait for
+// hold the running state, thread n owning row n (64 p values): per chunk they wait for
 // the product, read it out of TMEM, free the buffer and advance the
 // recurrence, so the products of later chunks overlap the recurrence and the
 // state writes of earlier ones.  The bf16 rows go out through a 128-byte
@@ -445,6 +444,16 @@ k_state_scan_tc(const __grid_constant__ ScanStateMaps maps, TcDims d, const floa
     if (nc > 1) load_dt(1, dv_next);
     for (int it = 0; it < nc; ++it) {
       const int k = it & 1;
+      // MODE 1: this thread's share of H_{c-1} (fp32 history), converted to
+      // bf16 rows for hT[c] after the tile is scaled: p in [16 pw, 16 pw + 16)
+      // of rows n = 4 lane .. 4 lane + 3 (16-byte loads, coalesced over lanes)
+      float4 hv[16];
+      if (MODE == 1) {
+        const float* hsrc = hist + (((size_t)b * nc + chunk_of(it)) * d.H + h) * PN +
+                            (size_t)(16 * pw) * d.N + 4 * lane;
+#pragma unroll
+        for (int pp = 0; pp < 16; ++pp) hv[pp] = *(const float4*)(hsrc + (size_t)pp * d.N);
+      }
       // the stored values were fetched ahead; raw-dt mode: dt = softplus(...)
       if (kRaw) {
         dv[0] = dt_of<kRaw>(d, dv[0], h);
@@ -501,6 +510,32 @@ k_state_scan_tc(const __grid_constant__ ScanStateMaps maps, TcDims d, const floa
       fence_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar_scaled[k]);  // s_lastq too (release)
+      if (MODE == 1) {
+        // hT[c] = H_{c-1} as bf16 rows n, off the consumers' path
+        const int c = chunk_of(it);
+        uint8_t* sRows2 = sm + 2 * stage_bytes + 16384;  // [128 rows n][64 p] bf16, SW128
+        if (pt == 0) bulk_wait_read0();  // the previous store of sRows2 has read it
+        named_sync(1, 128);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          float v8[8];
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+              const float4 f = hv[8 * half + t];
+              v8[t] = i == 0 ? f.x : i == 1 ? f.y : i == 2 ? f.z : f.w;
+            }
+            store_row_bf16(sRows2, 4 * lane + i, 2 * pw + half, v8);
+          }
+        }
+        fence_async_smem();
+        named_sync(1, 128);
+        if (pt == 0) {
+          tma_store_2d(&maps.rows2, sRows2, 0, ((b * nc + c) * d.H + h) * d.N);
+          bulk_commit();
+        }
+      }
     }
     if (pt == 0) bulk_wait0();
   } else {
@@ -509,11 +544,7 @@ k_state_scan_tc(const __grid_constant__ ScanStateMaps maps, TcDims d, const floa
     const int n = tid, q = tid >> 5;
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
     uint8_t* sRows = sm + 2 * stage_bytes;  // [128 rows n][64 p] bf16, SW128
-    uint8_t* sRows2 = sRows + 16384;         // MODE 1: the same for H_{c-1}
-    if (tid == 0) {
-      prefetch_tmap(&maps.rows);
-      if (MODE == 1) prefetch_tmap(&maps.rows2);
-    }
+    if (tid == 0) prefetch_tmap(&maps.rows);
     // 64 values of row n as bf16 into the staging tile, then one TMA store of
     // the tile to rows [srow, srow + 128) (the tile is free again once the
     // previous store has read it)
@@ -548,37 +579,6 @@ k_state_scan_tc(const __grid_constant__ ScanStateMaps maps, TcDims d, const floa
         for (int p = 0; p < 64; ++p) hblk[(size_t)p * d.N] = st[p];
       }
       put_rows(st, &maps.rows, srow);  // MODE 0: hT[c] = H_{c-1}; MODE 1: gT[c] = g_c
-      if (MODE == 1) {
-        // hT[c] = H_{c-1} from the fp32 history as bf16 rows, while the product
-        // is in flight: this thread takes p in [16 q, 16 q + 16) of rows
-        // n = 4 lane .. 4 lane + 3 (16-byte loads, coalesced over the lanes)
-        const float* hsrc = hist + (((size_t)b * nc + c) * d.H + h) * PN + (size_t)(16 * q) * d.N +
-                            4 * (tid & 31);
-        float4 hv[16];
-#pragma unroll
-        for (int pp = 0; pp < 16; ++pp) hv[pp] = *(const float4*)(hsrc + (size_t)pp * d.N);
-        if (tid == 0) bulk_wait_read0();  // the previous store of sRows2 has read it
-        named_sync(2, 128);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          float v8[8];
-#pragma unroll
-          for (int half = 0; half < 2; ++half) {
-#pragma unroll
-            for (int t = 0; t < 8; ++t) {
-              const float4 f = hv[8 * half + t];
-              v8[t] = i == 0 ? f.x : i == 1 ? f.y : i == 2 ? f.z : f.w;
-            }
-            store_row_bf16(sRows2, 4 * (tid & 31) + i, 2 * q + half, v8);
-          }
-        }
-        fence_async_smem();
-        named_sync(2, 128);
-        if (tid == 0) {
-          tma_store_2d(&maps.rows2, sRows2, 0, srow);
-          bulk_commit();
-        }
-      }
       ok = __all_sync(0xffffffffu, wait_ws(&bar_full[buf], (it / kScanBufs) & 1, &s_abort));
       // warp-uniform; the other consumer warps still reach the named barriers
       if (ok) {

@@ -926,7 +926,7 @@ k_fwd_single_tc(const __grid_constant__ ScanMaps maps, TcDims d, const float* __
   uint8_t* sH = sm + kScanH;
   __shared__ float s_cs2[256], s_dt[256], scratch[8];
   __shared__ __align__(16) float s_E[4][128];  // per-warp column factors exp(cs_r - cs_j) dt_j
-  __shared__ uint64_t bar_load, bar_mma;
+  __shared__ uint64_t bar_load, bar_mma, bar_b0;
   __shared__ uint32_t tmem_base;
   __shared__ int s_tile;
   const int tid = threadIdx.x, wg = tid >> 7, q = (tid >> 5) & 3;
@@ -944,6 +944,7 @@ k_fwd_single_tc(const __grid_constant__ ScanMaps maps, TcDims d, const float* __
     prefetch_tmap(&maps.y);
     mbar_init(&bar_load, 1);
     mbar_init(&bar_mma, 1);
+    mbar_init(&bar_b0, 1);
     fence_mbar_init();
   }
   if (tid < 32) {
@@ -981,10 +982,16 @@ k_fwd_single_tc(const __grid_constant__ ScanMaps maps, TcDims d, const float* __
   if (tid == 0) issue_state_loads(crow + (nblk - 1) * 128);
   chunk_cumsum_256<kRaw>(d, dt, A, b, c, h, s_cs2, s_dt, scratch);
 
-  // ---- A: the chunk's state contributions, the last block first
+  // ---- A: the chunk's state contributions, the last block first.  With two
+  // blocks, block 0's X and B are fetched while block 1's product runs: X_0
+  // into the X tile (X_1 has been scaled), B_0 into the idle C-hi and H
+  // tiles; B_0 goes into the B tile again for its y block once block 1's
+  // product has read B_1.
   uint8_t* sWX = sC;  // w o X_k
+  uint8_t* sB0 = sC + 16384;  // B_0 for its state product: n 0-63 here, n 64-127 in the H tile
   for (int blk = nblk - 1; blk >= 0 && ok; --blk) {
     const int base = blk * 128, end = base + 127;
+    const bool early = nblk == 2 && blk == 0;  // B_0 in the C-hi and H tiles
     ok = wait_or_flag(&bar_load, load_phase);
     load_phase ^= 1;
     if (!ok) break;
@@ -1005,21 +1012,31 @@ k_fwd_single_tc(const __grid_constant__ ScanMaps maps, TcDims d, const float* __
       // S_k^T = B_k^T (w o X_k)  (M = n, N = p, K = j; both operands MN-major)
       const uint32_t id_s = idesc_bf16(128, 64, true, true);
       const uint32_t tS = blk == 0 ? tS0 : tS1;
+      const uint32_t a0 = smem_u32(early ? sB0 : sB);
+      const uint32_t lbo = early ? (uint32_t)(sH - sB0) : 16384u;
       for (int kk = 0; kk < 8; ++kk)
-        mma_bf16(tS, desc_sw128(smem_u32(sB) + kk * 2048, 16384, 1024),
+        mma_bf16(tS, desc_sw128(a0 + kk * 2048, lbo, 1024),
                  desc_sw128(smem_u32(sWX) + kk * 2048, 16384, 1024), id_s, kk > 0);
       mma_commit(&bar_mma);
+      if (nblk == 2 && blk == 1) {  // block 0's state tiles, under this product
+        mbar_expect_tx(&bar_load, 48 * 1024);
+        tma_load_2d(sB0, &maps.B, g * d.N, crow, &bar_load);
+        tma_load_2d(sH, &maps.B, g * d.N + 64, crow, &bar_load);
+        tma_load_2d(sX, &maps.x, h * d.P, crow, &bar_load);
+      }
     }
     ok = wait_or_flag(&bar_mma, mma_phase);
     mma_phase ^= 1;
     fence_after_sync();
     if (!ok) break;
-    // the tiles are free: block 0's state tiles, or block 0's C tile (its B
-    // and X are in place)
+    // the tiles this product read are free
     if (tid == 0) {
-      if (blk > 0) {
-        issue_state_loads(crow);
+      if (blk > 0) {  // (two blocks) B_0 for its y block: the B tile is free now
+        mbar_expect_tx(&bar_b0, 32 * 1024);
+        tma_load_2d(sB, &maps.B, g * d.N, crow, &bar_b0);
+        tma_load_2d(sB + 16384, &maps.B, g * d.N + 64, crow, &bar_b0);
       } else {
+        // block 0's C tile (its B and X are in place, or on their way)
         mbar_expect_tx(&bar_load, 32 * 1024);
         tma_load_2d(sC, &maps.C, g * d.N, crow, &bar_load);
         tma_load_2d(sC + 16384, &maps.C, g * d.N + 64, crow, &bar_load);
@@ -1076,10 +1093,10 @@ k_fwd_single_tc(const __grid_constant__ ScanMaps maps, TcDims d, const float* __
       for (int k = 0; k < 32; ++k) hn[k] = fmaf(e1, hn[k], s1[k]);
     }
     if (c + 1 < d.nc) {
+      // made visible to chunk c + 1 by the barrier below and one thread's release
       float* slot_out = hist + (((size_t)b * d.nc + c + 1) * d.H + h) * PN;
 #pragma unroll
       for (int k = 0; k < 32; ++k) slot_out[(size_t)(wg * 32 + k) * 128 + row] = hn[k];
-      __threadfence();
     } else if (final_state) {
       float* fo = final_state + ((size_t)b * d.H + h) * PN;
 #pragma unroll
@@ -1094,9 +1111,13 @@ k_fwd_single_tc(const __grid_constant__ ScanMaps maps, TcDims d, const float* __
   __syncthreads();
   fence_after_sync();
   // released even after a wait that gave up (the error word is set then), so
-  // that the next chunk does not wait out its own limit as well
-  if (c + 1 < d.nc && tid == 0)
+  // that the next chunk does not wait out its own limit as well.  The
+  // barrier above orders every thread's history writes before this release
+  // (cumulative at gpu scope); a thread other than the MMA issuer does it.
+  if (c + 1 < d.nc && tid == 32) {
+    __threadfence();
     st_release_gpu(flags + ((size_t)b * d.nc + c + 1) * d.H + h, 1u);
+  }
 
   // ---- C: y block by block
   for (int blk = 0; blk < nblk && ok; ++blk) {
@@ -1112,6 +1133,7 @@ k_fwd_single_tc(const __grid_constant__ ScanMaps maps, TcDims d, const float* __
     fence_async_smem();
     ok = wait_or_flag(&bar_load, load_phase);
     load_phase ^= 1;
+    if (ok && nblk == 2 && blk == 0) ok = wait_or_flag(&bar_b0, 0);  // B_0 in the B tile
     if (!ok) break;
     fence_after_sync();
     if (tid == 0) {

@@ -918,15 +918,12 @@ k_fwd_single_tc(const __grid_constant__ ScanMaps maps, TcDims d, const float* __
                 unsigned int* flags) {
   extern __shared__ __align__(1024) uint8_t smraw[];
   uint8_t* sm = align1024(smraw);
-  uint8_t* sC = sm + kScanR1;
-  uint8_t* sB = sm + kScanR1 + 32768;
-  uint8_t* sM = sm + kScanR1;   // after the CB / Ys products are done
-  uint8_t* sY = sm + kScanR1;   // after the Y product is done
+  uint8_t* sB = sm + kScanR1 + 32768;  // the state phase's B_1 (B_0 of one block)
   uint8_t* sX = sm + kScanX;
   uint8_t* sH = sm + kScanH;
   __shared__ float s_cs2[256], s_dt[256], scratch[8];
   __shared__ __align__(16) float s_E[4][128];  // per-warp column factors exp(cs_r - cs_j) dt_j
-  __shared__ uint64_t bar_load, bar_mma, bar_b0;
+  __shared__ uint64_t bar_load, bar_mma, bar_c0;
   __shared__ uint32_t tmem_base;
   __shared__ int s_tile;
   const int tid = threadIdx.x, wg = tid >> 7, q = (tid >> 5) & 3;
@@ -944,7 +941,7 @@ k_fwd_single_tc(const __grid_constant__ ScanMaps maps, TcDims d, const float* __
     prefetch_tmap(&maps.y);
     mbar_init(&bar_load, 1);
     mbar_init(&bar_mma, 1);
-    mbar_init(&bar_b0, 1);
+    mbar_init(&bar_c0, 1);
     fence_mbar_init();
   }
   if (tid < 32) {
@@ -965,14 +962,6 @@ k_fwd_single_tc(const __grid_constant__ ScanMaps maps, TcDims d, const float* __
   bool ok = true;
   const int crow = b * d.T + c * Q;
 
-  auto issue_loads = [&](int row0) {  // C, B and X of one block
-    mbar_expect_tx(&bar_load, 80 * 1024);
-    tma_load_2d(sC, &maps.C, g * d.N, row0, &bar_load);
-    tma_load_2d(sC + 16384, &maps.C, g * d.N + 64, row0, &bar_load);
-    tma_load_2d(sB, &maps.B, g * d.N, row0, &bar_load);
-    tma_load_2d(sB + 16384, &maps.B, g * d.N + 64, row0, &bar_load);
-    tma_load_2d(sX, &maps.x, h * d.P, row0, &bar_load);
-  };
   auto issue_state_loads = [&](int row0) {  // B and X of one block
     mbar_expect_tx(&bar_load, 48 * 1024);
     tma_load_2d(sB, &maps.B, g * d.N, row0, &bar_load);
@@ -982,16 +971,28 @@ k_fwd_single_tc(const __grid_constant__ ScanMaps maps, TcDims d, const float* __
   if (tid == 0) issue_state_loads(crow + (nblk - 1) * 128);
   chunk_cumsum_256<kRaw>(d, dt, A, b, c, h, s_cs2, s_dt, scratch);
 
-  // ---- A: the chunk's state contributions, the last block first.  With two
-  // blocks, block 0's X and B are fetched while block 1's product runs: X_0
-  // into the X tile (X_1 has been scaled), B_0 into the idle C-hi and H
-  // tiles; B_0 goes into the B tile again for its y block once block 1's
-  // product has read B_1.
-  uint8_t* sWX = sC;  // w o X_k
-  uint8_t* sB0 = sC + 16384;  // B_0 for its state product: n 0-63 here, n 64-127 in the H tile
+  // ---- tile places, in 16 KB tiles R0-R5 of the 96 KB:
+  //   one block (Q = 128): C R0-R1 (later M, then the y staging), B R2-R3,
+  //   X R4, the state term R5;
+  //   two blocks: the state phase takes B_1 R2-R3, X_1 R4 and w o X R0, then
+  //   X_0 R4 and B_0 R1 + R5 (fetched under block 1's state product); C_0
+  //   lands in R2-R3 once block 1's product is done, the state term (bf16
+  //   rows) goes to R0, and block 1's B and C follow into R1 + R5 and R2-R3
+  //   as block 0's products release them.  B is K-major with its K-half
+  //   n 64-127 at kB1 from n 0-63.
+  const bool two = nblk == 2;
+  uint8_t* const tC = two ? sm + 32768 : sm;
+  uint8_t* const tB = two ? sm + 16384 : sm + 32768;
+  const uint32_t kB1 = two ? 65536u : 16384u;
+  uint8_t* const tH = two ? sm : sH;
+
+  // ---- A: the chunk's state contributions, the last block first
+  uint8_t* sWX = sm;  // w o X_k (R0)
   for (int blk = nblk - 1; blk >= 0 && ok; --blk) {
     const int base = blk * 128, end = base + 127;
-    const bool early = nblk == 2 && blk == 0;  // B_0 in the C-hi and H tiles
+    // block 0's B is in its y-phase place (R2-R3 for one block, R1 + R5 for two)
+    uint8_t* const sBk = blk == 0 ? tB : sB;
+    const uint32_t lbo = blk == 0 ? kB1 : 16384u;
     ok = wait_or_flag(&bar_load, load_phase);
     load_phase ^= 1;
     if (!ok) break;
@@ -1012,16 +1013,14 @@ k_fwd_single_tc(const __grid_constant__ ScanMaps maps, TcDims d, const float* __
       // S_k^T = B_k^T (w o X_k)  (M = n, N = p, K = j; both operands MN-major)
       const uint32_t id_s = idesc_bf16(128, 64, true, true);
       const uint32_t tS = blk == 0 ? tS0 : tS1;
-      const uint32_t a0 = smem_u32(early ? sB0 : sB);
-      const uint32_t lbo = early ? (uint32_t)(sH - sB0) : 16384u;
       for (int kk = 0; kk < 8; ++kk)
-        mma_bf16(tS, desc_sw128(a0 + kk * 2048, lbo, 1024),
+        mma_bf16(tS, desc_sw128(smem_u32(sBk) + kk * 2048, lbo, 1024),
                  desc_sw128(smem_u32(sWX) + kk * 2048, 16384, 1024), id_s, kk > 0);
       mma_commit(&bar_mma);
-      if (nblk == 2 && blk == 1) {  // block 0's state tiles, under this product
+      if (blk == 1) {  // block 0's state tiles, under this product
         mbar_expect_tx(&bar_load, 48 * 1024);
-        tma_load_2d(sB0, &maps.B, g * d.N, crow, &bar_load);
-        tma_load_2d(sH, &maps.B, g * d.N + 64, crow, &bar_load);
+        tma_load_2d(tB, &maps.B, g * d.N, crow, &bar_load);
+        tma_load_2d(tB + kB1, &maps.B, g * d.N + 64, crow, &bar_load);
         tma_load_2d(sX, &maps.x, h * d.P, crow, &bar_load);
       }
     }
@@ -1029,18 +1028,13 @@ k_fwd_single_tc(const __grid_constant__ ScanMaps maps, TcDims d, const float* __
     mma_phase ^= 1;
     fence_after_sync();
     if (!ok) break;
-    // the tiles this product read are free
-    if (tid == 0) {
-      if (blk > 0) {  // (two blocks) B_0 for its y block: the B tile is free now
-        mbar_expect_tx(&bar_b0, 32 * 1024);
-        tma_load_2d(sB, &maps.B, g * d.N, crow, &bar_b0);
-        tma_load_2d(sB + 16384, &maps.B, g * d.N + 64, crow, &bar_b0);
-      } else {
-        // block 0's C tile (its B and X are in place, or on their way)
-        mbar_expect_tx(&bar_load, 32 * 1024);
-        tma_load_2d(sC, &maps.C, g * d.N, crow, &bar_load);
-        tma_load_2d(sC + 16384, &maps.C, g * d.N + 64, crow, &bar_load);
-      }
+    // C_0 into the tiles this product has released: R2-R3 after block 1's
+    // product (two blocks), R0-R1 after block 0's (one block)
+    if (tid == 0 && (blk == 1 || !two)) {
+      uint64_t* bar = two ? &bar_c0 : &bar_load;
+      mbar_expect_tx(bar, 32 * 1024);
+      tma_load_2d(tC, &maps.C, g * d.N, crow, bar);
+      tma_load_2d(tC + 16384, &maps.C, g * d.N + 64, crow, bar);
     }
   }
 
@@ -1104,7 +1098,7 @@ k_fwd_single_tc(const __grid_constant__ ScanMaps maps, TcDims d, const float* __
     }
     // H_{c-1} as bf16 rows n (64 p each): the MN-major B operand of C H^T
 #pragma unroll
-    for (int ch = 0; ch < 4; ++ch) store_row_bf16(sH, row, wg * 4 + ch, &hv[ch * 8]);
+    for (int ch = 0; ch < 4; ++ch) store_row_bf16(tH, row, wg * 4 + ch, &hv[ch * 8]);
   }
   fence_async_smem();
   fence_before_sync();
@@ -1131,23 +1125,27 @@ k_fwd_single_tc(const __grid_constant__ ScanMaps maps, TcDims d, const float* __
     // reference log-decay of the block's state term: cs before row `base`
     const float ref2 = blk == 0 ? 0.f : s_cs2[base - 1];
     fence_async_smem();
-    ok = wait_or_flag(&bar_load, load_phase);
-    load_phase ^= 1;
-    if (ok && nblk == 2 && blk == 0) ok = wait_or_flag(&bar_b0, 0);  // B_0 in the B tile
+    if (two && blk == 0) {
+      ok = wait_or_flag(&bar_c0, 0);
+    } else {
+      ok = wait_or_flag(&bar_load, load_phase);
+      load_phase ^= 1;
+    }
     if (!ok) break;
     fence_after_sync();
     if (tid == 0) {
       const uint32_t id_cb = idesc_bf16(128, 128, false, false);
       for (int kk = 0; kk < 8; ++kk) {
         const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-        mma_bf16(tCB, desc_sw128(smem_u32(sC) + off, 16, 1024),
-                 desc_sw128(smem_u32(sB) + off, 16, 1024), id_cb, kk > 0);
+        const uint32_t boff = (kk >> 2) * kB1 + (kk & 3) * 32;
+        mma_bf16(tCB, desc_sw128(smem_u32(tC) + off, 16, 1024),
+                 desc_sw128(smem_u32(tB) + boff, 16, 1024), id_cb, kk > 0);
       }
       const uint32_t id_ys = idesc_bf16(128, 64, false, true);
       for (int kk = 0; kk < 8; ++kk) {
         const uint32_t aoff = (kk >> 2) * 16384 + (kk & 3) * 32;
-        mma_bf16(tYs, desc_sw128(smem_u32(sC) + aoff, 16, 1024),
-                 desc_sw128(smem_u32(sH) + kk * 2048, 16384, 1024), id_ys, kk > 0);
+        mma_bf16(tYs, desc_sw128(smem_u32(tC) + aoff, 16, 1024),
+                 desc_sw128(smem_u32(tH) + kk * 2048, 16384, 1024), id_ys, kk > 0);
       }
       mma_commit(&bar_mma);
     }
@@ -1155,6 +1153,13 @@ k_fwd_single_tc(const __grid_constant__ ScanMaps maps, TcDims d, const float* __
     mma_phase ^= 1;
     fence_after_sync();
     if (!ok) break;
+    if (tid == 0 && two && blk == 0) {
+      // block 1's B into the B tiles (B_0 has been read); its C and X follow
+      // once block 0's y is out
+      mbar_expect_tx_only(&bar_load, 32 * 1024);
+      tma_load_2d(tB, &maps.B, g * d.N, row0 + 128, &bar_load);
+      tma_load_2d(tB + kB1, &maps.B, g * d.N + 64, row0 + 128, &bar_load);
+    }
 
     const int I = base + row;
     {
@@ -1191,7 +1196,7 @@ k_fwd_single_tc(const __grid_constant__ ScanMaps maps, TcDims d, const float* __
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
           const int j = jc * 32 + q4 * 8;
-          store_row_bf16(sM + (j >> 6) * 16384, row, (j & 63) >> 3, &v[q4 * 8]);
+          store_row_bf16(tC + (j >> 6) * 16384, row, (j & 63) >> 3, &v[q4 * 8]);
         }
       }
     }
@@ -1200,7 +1205,7 @@ k_fwd_single_tc(const __grid_constant__ ScanMaps maps, TcDims d, const float* __
     if (blk == 0 && nblk == 2) {
 #pragma unroll
       for (int ch = 0; ch < 4; ++ch)
-        *(uint4*)(sH + sw128(row, wg * 4 + ch)) =
+        *(uint4*)(tH + sw128(row, wg * 4 + ch)) =
             make_uint4(hmid[4 * ch], hmid[4 * ch + 1], hmid[4 * ch + 2], hmid[4 * ch + 3]);
     }
     fence_async_smem();
@@ -1211,7 +1216,7 @@ k_fwd_single_tc(const __grid_constant__ ScanMaps maps, TcDims d, const float* __
       const uint32_t id_y = idesc_bf16(128, 64, false, true);
       for (int kk = 0; kk < 8; ++kk) {
         const uint32_t aoff = (kk >> 2) * 16384 + (kk & 3) * 32;
-        mma_bf16(tY, desc_sw128(smem_u32(sM) + aoff, 16, 1024),
+        mma_bf16(tY, desc_sw128(smem_u32(tC) + aoff, 16, 1024),
                  desc_sw128(smem_u32(sX) + kk * 2048, 16384, 1024), id_y, kk > 0);
       }
       mma_commit(&bar_mma);
@@ -1233,7 +1238,7 @@ k_fwd_single_tc(const __grid_constant__ ScanMaps maps, TcDims d, const float* __
         unpack8(*(const uint4*)(sX + sw128(row, ch)), xf);
 #pragma unroll
         for (int t = 0; t < 8; ++t) o8[t] = fmaf(sc, ys[k * 8 + t], yv[k * 8 + t]) + Dh * xf[t];
-        store_row_bf16(sY, row, ch, o8);
+        store_row_bf16(tC, row, ch, o8);  // y staging in the M tile
       }
     }
     fence_async_smem();
@@ -1241,11 +1246,16 @@ k_fwd_single_tc(const __grid_constant__ ScanMaps maps, TcDims d, const float* __
     __syncthreads();
     fence_after_sync();
     if (tid == 0) {
-      tma_store_2d(&maps.y, sY, h * d.P, row0);
+      tma_store_2d(&maps.y, tC, h * d.P, row0);
       bulk_commit();
       if (blk + 1 < nblk) {
-        bulk_wait_read0();  // the y staging (region R1) is reloaded next
-        issue_loads(row0 + 128);
+        // block 1's C into the y staging's tiles once the store has read
+        // them, and its X (block 0's has been read); its B is on its way
+        bulk_wait_read0();
+        mbar_expect_tx(&bar_load, 48 * 1024);
+        tma_load_2d(tC, &maps.C, g * d.N, row0 + 128, &bar_load);
+        tma_load_2d(tC + 16384, &maps.C, g * d.N + 64, row0 + 128, &bar_load);
+        tma_load_2d(sX, &maps.x, h * d.P, row0 + 128, &bar_load);
       }
     }
   }

@@ -153,6 +153,13 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t* mbar, uint32_t bytes) {
                "r"(bytes)
                : "memory");
 }
+// Raise the expected transaction bytes of the current phase without an
+// arrival (a later arrive.expect_tx completes the arrivals).
+__device__ __forceinline__ void mbar_expect_tx_only(uint64_t* mbar, uint32_t bytes) {
+  asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(mbar)),
+               "r"(bytes)
+               : "memory");
+}
 __device__ __forceinline__ void mbar_arrive(uint64_t* mbar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(mbar)) : "memory");
 }

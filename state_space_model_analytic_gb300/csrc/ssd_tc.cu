@@ -1628,7 +1628,7 @@ k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, long long nitems,
     {
       const int jc = wg;
       if (jc <= q) {  // warp-uniform
-#pragma unroll 1
+#pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
           const int col0 = jc * 32 + hf * 16;
           float cb[16], xy[16], wv[16];
@@ -1798,17 +1798,17 @@ k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, long long nitems,
       ered[((wg - 1) * 4 + 3) * 128 + row] = dd;
     }
     fence_async_smem();
-    __syncthreads();
+    // phase D done (the barrier also publishes the dx staging and the
+    // partials): dx goes out, X, dY, Hin, gout are free and the next head's
+    // tiles go out now, under this head's dcs work (issued from warpgroup 3,
+    // which has slack here, so that warpgroup 0's chain starts at once)
+    ok = wait_or_flag(&bar_mma, mma_phase);
+    mma_phase ^= 1;
+    fence_after_sync();
     if (tid == 0) {
       tma_store_2d(&maps.dx, sO, h * d.P, row0);
       bulk_commit();
     }
-    // phase D done: X, dY, Hin, gout are free and the next head's tiles go out
-    // now, under this head's dcs work (issued from warpgroup 3, which has
-    // slack here, so that warpgroup 0's chain starts at once)
-    ok = wait_or_flag(&bar_mma, mma_phase);
-    mma_phase ^= 1;
-    fence_after_sync();
     if (tid == kBwThreads - 128 && ok && hh + 1 < kh) issue_head_loads(u, h + 1, true);
     if (wg == 0) {
       // ---- dcs, its suffix sums (da), ddt, dA and dD partials: warpgroup 0,

@@ -105,7 +105,10 @@ SSD_API int ssd_forward(const ssd_dims* dims,
 /*
  * Backward of L = sum(dy * y).  Same inputs as ssd_forward plus dy.
  * chunk_states: the history ssd_forward wrote for the same inputs, or NULL to
- * recompute it inside this call (needs ssd_workspace_bytes(dims, 2)).
+ * recompute it inside this call (needs ssd_workspace_bytes(dims, 2)).  The
+ * tensor-core block family at chunk 256 (d_state 64) works on 128-step
+ * sub-chunks and recomputes their start states in either case (the same
+ * kernels as ssd_forward, so the results do not depend on the argument).
  * Outputs (all required except dh0): dx, ddt, dA, dB, dC, dD; dh0 (NULL = not
  * written; when h0 is NULL it is the gradient w.r.t. the zero initial state).
  * The gradient w.r.t. the final state is taken as zero.
@@ -235,7 +238,9 @@ SSD_API int ssd_conv1d_silu_backward(int64_t batch, int64_t seqlen, int64_t chan
  *     or host threads) race; order them.  What must start at zero is
  *     cleared by each call on its own stream.
  *   - Scratch used: B*H*nc floats and B*nc*H + 1 words, plus B*nc*H*P*N
- *     floats when chunk_states is NULL (each rounded up to 256 bytes).
+ *     floats when chunk_states is NULL (each rounded up to 256 bytes); the
+ *     tensor-core block family at chunk 256 counts nc as T / 128 and always
+ *     keeps its chunk states in the scratch.
  *     Larger problems are rejected with SSD_ERR_UNSUPPORTED and a message;
  *     nothing is launched.
  */

@@ -153,7 +153,12 @@ Problem base_problem(const ssd_dims* d) {
 // recomputing the history.  Carves into `p` when base != nullptr.
 size_t carve(Problem* p, char* base, int which) {
   const size_t B = p->B, T = p->T, H = p->H, P = p->P, N = p->N, nc = p->nc, Q = p->Q;
-  const size_t states = B * nc * H * P * N * sizeof(float);
+  // the block family on 128-step sub-chunks keeps its per-chunk buffers (the
+  // decay totals, the state gradients and its own chunk-start states) at
+  // sub-chunk granularity
+  const bool sub = tc64_subchunks(*p);
+  const size_t ncw = sub ? T / 128 : nc;
+  const size_t states = B * ncw * H * P * N * sizeof(float);
   const size_t tokh = B * T * H * sizeof(float);
   size_t off = 0;
   auto take = [&](size_t bytes) -> char* {
@@ -161,7 +166,11 @@ size_t carve(Problem* p, char* base, int which) {
     off += up(bytes);
     return r;
   };
-  p->cs_last = (float*)take(B * H * nc * sizeof(float));
+  p->cs_last = (float*)take(B * H * ncw * sizeof(float));
+  if (sub) {
+    p->hist_sub = (float*)take(states);
+    if (which == 0) return off;
+  }
   if (which == 0) {
     float* h = (float*)take(states);
     if (!p->hist) p->hist = h;
@@ -191,6 +200,7 @@ size_t carve(Problem* p, char* base, int which) {
   if (tc64_supported(*p) && tc64_bc_part_floats(*p) > part_floats)
     part_floats = tc64_bc_part_floats(*p);
   p->bwd_part = (float*)take(part_floats * sizeof(float));
+  if (sub) return off;  // (its backward recomputes hist_sub itself)
   p->hT = take(states / 2);  // bf16 copies for the tensor-core backward
   p->gT = take(states / 2);
   if (which == 2) p->hist = (float*)take(states);
@@ -228,12 +238,22 @@ cudaError_t forward_launches(Problem& p, const char** where) {
     return tc_forward_single(p);
   }
   if (tc64_supported(p)) {  // the block family (fp32 through split bf16 products)
+    const bool sub = tc64_subchunks(p);
+    Problem s = sub ? tc64_sub_problem(p) : p;
     *where = "forward chunk-state kernel";
-    if ((e = tc64_chunk_outer(p, 0, p.hist)) != cudaSuccess) return e;
+    if ((e = tc64_chunk_outer(s, 0, s.hist)) != cudaSuccess) return e;
     *where = "forward state-pass kernel";
-    if ((e = simt_state_pass_fwd(p, p.hist, p.cs_last)) != cudaSuccess) return e;
+    if ((e = simt_state_pass_fwd(s, s.hist, s.cs_last)) != cudaSuccess) return e;
     *where = "forward chunk-scan kernel";
-    return tc64_forward_scan(p);
+    if ((e = tc64_forward_scan(s)) != cudaSuccess) return e;
+    if (sub && p.hist) {
+      // the caller's chunk-start states: every (Q / 128)-th sub-chunk's
+      *where = "forward history copy";
+      const size_t blk = (size_t)p.H * p.P * p.N * sizeof(float);
+      return cudaMemcpy2DAsync(p.hist, blk, s.hist, blk * (p.Q / 128), blk, (size_t)p.B * p.nc,
+                               cudaMemcpyDeviceToDevice, p.stream);
+    }
+    return cudaSuccess;
   }
   p.hT = nullptr;  // the scan converts the fp32 history itself
   *where = "forward chunk-state kernel";
@@ -460,6 +480,19 @@ int backward_impl(const ssd_dims* dims, const void* x, const float* dt, const fl
   p.stream = (cudaStream_t)cuda_stream;
 
   cudaError_t e;
+  if (tc64_subchunks(p)) {
+    // the block family on 128-step sub-chunks: their start states are not in
+    // the caller's chunk-level history, so they are recomputed (the same
+    // kernels as the forward: the caller's history holds the same values)
+    Problem s = tc64_sub_problem(p);
+    s.final_state = nullptr;
+    e = tc64_chunk_outer(s, 0, s.hist);
+    if (e == cudaSuccess) e = simt_state_pass_fwd(s, s.hist, s.cs_last);
+    if (e != cudaSuccess) return cuda_fail(e, "backward sub-chunk state kernels");
+    e = tc64_backward(s);
+    if (e != cudaSuccess) return cuda_fail(e, "backward kernels");
+    return SSD_OK;
+  }
   if (!chunk_states) {
     // recompute the chunk-start states into the workspace (final state not needed)
     Problem f = p;

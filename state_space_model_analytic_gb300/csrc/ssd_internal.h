@@ -36,6 +36,9 @@ struct Problem {
   void* y;
   float* final_state;  // nullable
   float* hist;         // [B][nc][H][P][N]: chunk-start states (user buffer or workspace)
+  // the block family with chunks longer than its 128-step blocks runs on
+  // 128-step sub-chunks: their start states [B][T/128][H][P][N] (workspace)
+  float* hist_sub;
 
   // backward outputs
   void* dx;
@@ -117,6 +120,9 @@ constexpr size_t kBwdMaxCtas = 160;
 // bumps the launch counter.
 cudaError_t simt_forward_states(const Problem& p, float* hist, float* cs_last);
 cudaError_t simt_state_pass_fwd(const Problem& p, float* hist, const float* cs_last);
+// the block family with chunks longer than its 128-step blocks (ssd_tc64.cu)
+bool tc64_subchunks(const Problem& p);
+Problem tc64_sub_problem(const Problem& p);
 cudaError_t simt_forward_scan(const Problem& p);
 cudaError_t simt_backward(const Problem& p);
 cudaError_t simt_state_pass_bwd(const Problem& p);

@@ -92,11 +92,15 @@ extern "C" int ssd_forward_noalloc(const ssd_dims* dims, const void* x, const fl
 
   // scratch: per-chunk decay totals, the single-pass forward's flags (one per
   // history slot and its tile counter), and the chunk states when the caller
-  // passes no history buffer
-  const size_t cl_bytes = align256((size_t)p.B * p.H * p.nc * sizeof(float));
+  // passes no history buffer; the block family on 128-step sub-chunks keeps
+  // its decay totals and chunk states per sub-chunk, always in the scratch
+  const bool sub = tc64_subchunks(p);
+  const size_t ncw = sub ? (size_t)p.T / 128 : (size_t)p.nc;
+  const size_t cl_bytes = align256((size_t)p.B * p.H * ncw * sizeof(float));
   const size_t fl_bytes = align256(((size_t)p.B * p.nc * p.H + 1) * sizeof(unsigned int));
-  const size_t st_bytes =
-      chunk_states ? 0 : align256((size_t)p.B * p.nc * p.H * p.P * p.N * sizeof(float));
+  const size_t st_bytes = chunk_states && !sub
+                              ? 0
+                              : align256((size_t)p.B * ncw * p.H * p.P * p.N * sizeof(float));
   if (cl_bytes + fl_bytes + st_bytes > (size_t)SSD_NOALLOC_SCRATCH_BYTES)
     return reject(SSD_ERR_UNSUPPORTED,
                   chunk_states
@@ -117,7 +121,13 @@ extern "C" int ssd_forward_noalloc(const ssd_dims* dims, const void* x, const fl
   char* s = (char*)scratch;
   p.cs_last = (float*)s;
   p.fwd_flags = (unsigned int*)(s + cl_bytes);
-  p.hist = chunk_states ? chunk_states : (float*)(s + cl_bytes + fl_bytes);
+  float* st = (float*)(s + cl_bytes + fl_bytes);
+  if (sub) {
+    p.hist_sub = st;
+    p.hist = chunk_states;
+  } else {
+    p.hist = chunk_states ? chunk_states : st;
+  }
   p.stream = (cudaStream_t)cuda_stream;
 
   // the launch sequence of ssd_forward for these dims

@@ -1,7 +1,8 @@
 // Tensor-core (tcgen05 / TMEM) kernels of the chunked SSD core on 128-step
 // blocks: headdim P = 64 with d_state N = 64 (fp32 or bf16 storage) or
 // N = 128 (bf16), and P = 128 with N = 64 (bf16); any chunk Q in {16, 32,
-// 64, 128} (seqlen a multiple of 128).  A bf16 row of 128 values occupies
+// 64, 128} (seqlen a multiple of 128), and Q = 256 run by the host as
+// 128-step sub-chunks (tc64_sub_problem).  A bf16 row of 128 values occupies
 // the bytes of an fp32 row of 64 carried as two bf16 tiles, so the 128-wide
 // operands of the bf16 shapes take the lo tiles' places of the fp32 layout.
 //
@@ -1203,17 +1204,31 @@ cudaError_t forward_scan_t(const Problem& p) {
 
 }  // namespace
 
-// chunk in {16, 32, 64, 128}, seqlen a multiple of 128, and
-//   headdim 64, d_state 64 (fp32 or bf16);
-//   headdim 64, d_state 128 (bf16, chunks below 128: the bf16 kernels of
+// seqlen a multiple of 128, and
+//   headdim 64, d_state 64 (fp32 or bf16), chunk 16-256;
+//   headdim 64, d_state 128 (bf16, chunks 16-64: the bf16 kernels of
 //     ssd_tc.cu take chunks 128 and 256);
-//   headdim 128, d_state 64 (bf16).
+//   headdim 128, d_state 64 (bf16), chunk 16-256.
+// Chunks of 256 run as 128-step sub-chunks (tc64_subchunks).
 bool tc64_supported(const Problem& p) {
   if (tc_forced_simt()) return false;
   if (p.T % kQ != 0) return false;
-  if (p.Q != 16 && p.Q != 32 && p.Q != 64 && p.Q != 128) return false;
+  if (p.Q != 16 && p.Q != 32 && p.Q != 64 && p.Q != 128 && p.Q != 256) return false;
   if (p.P == 64) return p.N == 64 || (p.N == 128 && p.bf16 && p.Q < 128);
   return p.P == 128 && p.N == 64 && p.bf16;
+}
+
+// Chunks longer than a block: the kernels run on the problem regrouped into
+// 128-step chunks (exact: chunking regroups the recurrence), whose start
+// states include those of the caller's chunks (every Q/128-th).
+bool tc64_subchunks(const Problem& p) { return tc64_supported(p) && p.Q > kQ; }
+
+Problem tc64_sub_problem(const Problem& p) {
+  Problem s = p;
+  s.Q = kQ;
+  s.nc = p.T / kQ;
+  s.hist = p.hist_sub;
+  return s;
 }
 
 // Heads per segment of the dB, dC kernel (one CTA per SM): the number of

@@ -66,6 +66,9 @@ def test_workspace_sizes(L):
     (64, 64, 16, True, 512, 1),
     (128, 64, 64, True, 512, 1),     # block family, headdim 128
     (128, 64, 128, True, 512, 1),
+    (64, 64, 256, False, 512, 1),    # chunk 256 as 128-step sub-chunks
+    (64, 64, 256, True, 512, 1),
+    (128, 64, 256, True, 512, 1),
     (128, 64, 64, False, 512, 0),    # headdim 128 in fp32: SIMT
     (128, 128, 64, True, 512, 0),    # headdim 128 with d_state 128: SIMT
     (64, 128, 64, False, 512, 0),    # d_state 128 in fp32: SIMT

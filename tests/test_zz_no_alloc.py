@@ -7,8 +7,8 @@ instead of a caller workspace.
 Checked through the C ABI against ssd_forward on the same inputs, on two
 calls in a row (the shared scratch keeps the previous call's contents), with
 and without a caller history buffer, on every kernel sequence the forward
-has (single-pass tensor-core, unfused tensor-core, d_state-64 tensor-core,
-SIMT): the launch sequence
+has (single-pass tensor-core, unfused tensor-core, d_state-64 tensor-core
+on blocks and on sub-chunks, SIMT): the launch sequence
 is ssd_forward's, so the outputs must be bit-for-bit equal.  One case is also
 compared with the float64 oracle.  Oversized problems are refused before
 anything is launched.  This file is collected last on purpose.
@@ -44,6 +44,7 @@ CASES = [
     synth.Dims(4, 256, 32, 64, 128, 1, 256, "bf16"),   # single-pass tensor-core forward
     synth.Dims(2, 1024, 4, 64, 128, 2, 256, "bf16"),  # unfused tensor-core kernels
     synth.Dims(2, 512, 4, 64, 64, 2, 64, "f32"),      # d_state-64 tensor-core kernels
+    synth.Dims(1, 512, 4, 64, 64, 1, 256, "f32"),     # the same on 128-step sub-chunks
     synth.Dims(1, 256, 3, 32, 48, 1, 64, "f32"),       # SIMT kernels
 ]
 

@@ -1,6 +1,6 @@
 // Tensor-core (tcgen05 / TMEM) kernels of the chunked SSD core on 128-step
 // blocks: headdim P = 64 with d_state N = 64 (fp32 or bf16 storage) or
-// N = 128 (bf16), and P = 128 with N = 64 (bf16); any chunk Q in {16, 32,
+// N = 128 (bf16), and P = 128 with N = 64 or 128 (bf16); any chunk Q in {16, 32,
 // 64, 128} (seqlen a multiple of 128), and Q = 256 run by the host as
 // 128-step sub-chunks (tc64_sub_problem).  A bf16 row of 128 values occupies
 // the bytes of an fp32 row of 64 carried as two bf16 tiles, so the 128-wide
@@ -204,9 +204,11 @@ __device__ __forceinline__ void read_split8(const uint8_t* hi, const uint8_t* lo
 template <int NT, int NS, bool kBf, int PR = 64>
 struct StateRowTile {
   static_assert(NS == 64 || (NS == 128 && kBf), "d_state 128 is bf16 only");
-  static_assert(PR == 64 || (PR == 128 && kBf && NS == 64), "headdim 128 is bf16, d_state 64");
+  static_assert(PR == 64 || (PR == 128 && kBf), "headdim 128 is bf16");
   static constexpr int kCh = NS / 8;
-  static constexpr int kPer = PR * kCh / NT;  // PR = 128: rows 64-127 run into the lo tile's place
+  // PR = 128: rows 64-127 follow rows 0-63; with NS = 128 the n 64-127 block
+  // (PR rows) is at the lo pointer
+  static constexpr int kPer = PR * kCh / NT;
   Raw8 v[kPer];
   __device__ __forceinline__ void fetch(const float* __restrict__ src) {
 #pragma unroll
@@ -266,16 +268,16 @@ __device__ __forceinline__ void rescale_split(uint8_t* hi, uint8_t* lo, F&& scal
 }
 
 // A [PS p][NS n] fp32 state block (p-major) transposed into split tiles of
-// rows n with 64 p each; NS = 128 (bf16 only): rows 64-127 continue into the
-// lo tile's place; PS = 128 (bf16 only, NS = 64): p 64-127 go to a second
-// tile there.  Returns this thread's share of sum(src * other) when `other`
+// rows n with 64 p each; NS = 128 (bf16 only): rows 64-127 follow rows 0-63;
+// PS = 128 (bf16 only): p 64-127 go to a second tile of NS rows at the lo
+// pointer.  Returns this thread's share of sum(src * other) when `other`
 // is given (the same elements of a second block, for <g, H>).
 template <int NT, bool kBf, int NS = 64, int PS = 64>
 __device__ __forceinline__ float load_split_transposed(uint8_t* hi, uint8_t* lo,
                                                        const float* __restrict__ src,
                                                        const float* __restrict__ other) {
   static_assert(NS == 64 || (NS == 128 && kBf), "d_state 128 is bf16 only");
-  static_assert(PS == 64 || (PS == 128 && kBf && NS == 64), "headdim 128 is bf16, d_state 64");
+  static_assert(PS == 64 || (PS == 128 && kBf), "headdim 128 is bf16");
   constexpr int kPer = NS * (PS / 8) / NT;
   float dot = 0.f;
 #pragma unroll
@@ -420,19 +422,28 @@ __global__ void __launch_bounds__(256) k_outer64(D64 d, const Elem<kBf>* __restr
 //   of its first chunk, as rows n),
 //   M = CB o L o dt (masked, split), Y = M X,
 //   y = Y + exp(cs_i) Ys + D x.
-// fp32 storage and d_state 128 form M in two 64-column halves in the C
-// tile's place, each followed by its half of Y = M X (K = the half's 64 rows
-// of X).  bf16 storage with d_state 64 leaves the C tile's lo half unused, so
-// M is formed whole (the two halves in the hi and lo places) and Y = M X is
-// one batch with K = 128; Y then takes CB's TMEM columns (CB has been read),
-// which leaves room for a 128-wide Y and Ys (headdim PS = 128).
+// fp32 storage forms M (split) in two 64-column halves in the C tile's
+// place, each followed by its half of Y = M X (K = the half's 64 rows of X).
+// bf16 storage forms M whole in the C tile's 32 KB (CB and Ys have read C)
+// and Y = M X is one batch with K = 128; Y then takes CB's TMEM columns (CB
+// has been read), which leaves room for a 128-wide Y and Ys (headdim 128).
 // X is fetched into registers at the start and written into the B tile's
 // place once CB is formed (PS = 128: X's second 64 columns at the lo place).
 // Decay masks as in the bf16 kernels: for warp q's rows and a 32-column chunk
 // left of its diagonal chunk, exp(cs_i - cs_j) = exp(cs_i - cs_r) exp(cs_r -
 // cs_j) with r = 32 q (both factors <= 1); the diagonal chunk evaluates the
 // exponent only where j <= i.
-constexpr uint32_t kScan64Bytes = 81920;  // C (later M) 32K | B (later X) 32K | H 16K
+// The tiles of the transposed state (H^T, g^T), the stride between their
+// 64-p blocks (bf16) or their hi and lo tiles (fp32), and the shared memory
+// of the kernels that hold them.
+template <bool kBf, int NS, int PS>
+constexpr uint32_t state_tile_bytes() { return (uint32_t)NS * PS * 2 * (kBf ? 1 : 2); }
+template <bool kBf, int NS>
+constexpr uint32_t state_block_stride() { return kBf ? NS * 128u : 8192u; }
+template <bool kBf, int NS, int PS>
+constexpr uint32_t scan64_bytes() {  // C (later M) 32K | B (later X) 32K | H^T
+  return 65536u + state_tile_bytes<kBf, NS, PS>();
+}
 
 template <bool kBf, int NS, int PS>
 __global__ void __launch_bounds__(256, 2) k_scan64(D64 d, const Elem<kBf>* __restrict__ x,
@@ -443,8 +454,9 @@ __global__ void __launch_bounds__(256, 2) k_scan64(D64 d, const Elem<kBf>* __res
                                                    const float* __restrict__ D,
                                                    const float* __restrict__ hist,
                                                    Elem<kBf>* __restrict__ y) {
-  constexpr bool kWholeM = kBf && NS == 64;
-  static_assert(PS == 64 || kWholeM, "headdim 128 is bf16, d_state 64");
+  constexpr bool kWholeM = kBf;
+  static_assert(PS == 64 || kBf, "headdim 128 is bf16");
+  constexpr uint32_t kHpb = state_block_stride<kBf, NS>();
   extern __shared__ __align__(1024) uint8_t smraw[];
   uint8_t* sm = align1024(smraw);
   uint8_t* sCh = sm;            // [128 rows i][64 n] K-major (NS = 128: n 64-127 at the lo tile)
@@ -455,8 +467,8 @@ __global__ void __launch_bounds__(256, 2) k_scan64(D64 d, const Elem<kBf>* __res
   uint8_t* sBl = sm + 49152;
   uint8_t* sXh = sm + 32768;    // [128 rows j][64 p] MN-major B operand (after CB)
   uint8_t* sXl = sm + 49152;
-  uint8_t* sHh = sm + 65536;    // [NS rows n][64 p] MN-major B operand (NS = 128: rows 64+ at
-  uint8_t* sHl = sm + 73728;    // the lo tile; PS = 128: p 64-127 at the lo tile)
+  uint8_t* sHh = sm + 65536;    // [NS rows n][64 p] MN-major B operand (fp32: its lo tile;
+  uint8_t* sHl = sHh + kHpb;    // PS = 128: p 64-127 there)
   __shared__ float s_cs2[kQ], s_dt[kQ], scratch[8];
   __shared__ __align__(16) float s_E[4][kQ];  // exp(cs_r - cs_j) dt_j, j < r = 32 w
   __shared__ uint64_t bar;
@@ -507,7 +519,7 @@ __global__ void __launch_bounds__(256, 2) k_scan64(D64 d, const Elem<kBf>* __res
       const uint32_t ko = (kk >> 2) * 16384 + (kk & 3) * 32;
       mma3<kBf>(tCB, smem_u32(sCh) + ko, 16384, 16, false, smem_u32(sBh) + ko, 16384, 16, id_cb,
                 kk > 0);
-      mma3<kBf>(tYs, smem_u32(sCh) + ko, 16384, 16, false, smem_u32(sHh) + kk * 2048, 8192, 8192,
+      mma3<kBf>(tYs, smem_u32(sCh) + ko, 16384, 16, false, smem_u32(sHh) + kk * 2048, kHpb, kHpb,
                 id_ys, kk > 0);
     }
     mma_commit(&bar);
@@ -631,9 +643,12 @@ __device__ __forceinline__ float col_sum16(float (&v)[16]) {
 //   dcs_i = rowsum_i - colsum_i + statein_i - e_i (+ sum_j e_j +
 //            exp(cs_last) <g, H> at i = Q - 1); da_j = sum_{i >= j} dcs_i;
 //            ddt_j = drive_j + A da_j; partials sum_j dt_j da_j and sum dy.x.
-// Headdim PS = 128 (bf16, d_state 64): X, dY, H^T and g^T keep p 64-127 in
-// their lo tiles' places; Gx then takes CB's TMEM columns (CB has been read).
-constexpr uint32_t kBwdX64Bytes = 163840;  // C, B (later O) 64K | X 32K | dY 32K | H 16K | g 16K
+// Headdim PS = 128 (bf16): X, dY, H^T and g^T keep p 64-127 in their lo
+// places; Gx then takes CB's TMEM columns (CB has been read).
+template <bool kBf, int NS, int PS>
+constexpr uint32_t bwdx64_bytes() {  // C, B (later O) 64K | X 32K | dY 32K | H^T | g^T
+  return 131072u + 2 * state_tile_bytes<kBf, NS, PS>();
+}
 
 template <bool kBf, int NS, int PS>
 __global__ void __launch_bounds__(512, 1) k_bwd64_x(D64 d, const Elem<kBf>* __restrict__ x,
@@ -661,11 +676,12 @@ __global__ void __launch_bounds__(512, 1) k_bwd64_x(D64 d, const Elem<kBf>* __re
   uint8_t* sXl = sm + 81920;
   uint8_t* sYh = sm + 98304;    // dY [128 rows i][64 p]
   uint8_t* sYl = sm + 114688;
-  uint8_t* sHh = sm + 131072;   // H^T [64 rows n][64 p]
-  uint8_t* sHl = sm + 139264;
-  uint8_t* sGh = sm + 147456;   // g^T [64 rows n][64 p]
-  uint8_t* sGl = sm + 155648;
-  static_assert(PS == 64 || (PS == 128 && kBf && NS == 64), "headdim 128 is bf16, d_state 64");
+  static_assert(PS == 64 || (PS == 128 && kBf), "headdim 128 is bf16");
+  constexpr uint32_t kHpb = state_block_stride<kBf, NS>();
+  uint8_t* sHh = sm + 131072;   // H^T [NS rows n][64 p] (fp32: its lo tile; PS = 128: p
+  uint8_t* sHl = sHh + kHpb;    // 64-127 there)
+  uint8_t* sGh = sHh + state_tile_bytes<kBf, NS, PS>();  // g^T, the same
+  uint8_t* sGl = sGh + kHpb;
   __shared__ float s_cs2[kQ], s_dt[kQ], scratch[16];
   __shared__ __align__(16) float s_E[4][kQ];    // exp(cs_r - cs_j), j < r = 32 w
   __shared__ __align__(16) float s_Edt[4][kQ];  // the same times dt_j
@@ -735,9 +751,9 @@ __global__ void __launch_bounds__(512, 1) k_bwd64_x(D64 d, const Elem<kBf>* __re
       const uint32_t ko = (kk >> 2) * 16384 + (kk & 3) * 32;
       mma3<kBf>(T0, smem_u32(sCh) + ko, 16384, 16, false, smem_u32(sBh) + ko, 16384, 16, id_sq,
                 kk > 0);
-      mma3<kBf>(TGs, smem_u32(sBh) + ko, 16384, 16, false, smem_u32(sGh) + kk * 2048, 8192, 8192,
+      mma3<kBf>(TGs, smem_u32(sBh) + ko, 16384, 16, false, smem_u32(sGh) + kk * 2048, kHpb, kHpb,
                 id_km, kk > 0);
-      mma3<kBf>(TCH, smem_u32(sCh) + ko, 16384, 16, false, smem_u32(sHh) + kk * 2048, 8192, 8192,
+      mma3<kBf>(TCH, smem_u32(sCh) + ko, 16384, 16, false, smem_u32(sHh) + kk * 2048, kHpb, kHpb,
                 id_km, kk > 0);
     }
     mma_commit(&bar);
@@ -907,9 +923,13 @@ __global__ void __launch_bounds__(512, 1) k_bwd64_x(D64 d, const Elem<kBf>* __re
 //   dC += (e o dY) H,  dB += (f o X) g      (TMEM accumulators over heads).
 // After the segment: W into split tiles, dC += W B, dB += W^T C, and the fp32
 // sums of the segment written as partials [unit][segment][dC|dB][128][64].
-// Headdim PS = 128 (bf16, d_state 64): X, dY keep p 64-127 in their lo
-// tiles' places and H, g their rows p 64-127.
-constexpr uint32_t kBwdBC64Bytes = 163840;  // B 32K | C 32K | X 32K | dY 32K | H 16K | g 16K
+// Headdim PS = 128 (bf16): X, dY keep p 64-127 in their lo places and H, g
+// their rows p 64-127 (d_state 128: their n 64-127 blocks at the lo
+// pointers, PS rows on).
+template <bool kBf, int NS, int PS>
+constexpr uint32_t bwdbc64_bytes() {  // B 32K | C 32K | X 32K | dY 32K | H | g
+  return 131072u + 2 * state_tile_bytes<kBf, NS, PS>();
+}
 
 template <bool kBf, int NS, int PS>
 __global__ void __launch_bounds__(512, 1) k_bwd64_bc(D64 d, int seg_heads,
@@ -934,10 +954,11 @@ __global__ void __launch_bounds__(512, 1) k_bwd64_bc(D64 d, int seg_heads,
   uint8_t* sYl = sm + 114688;
   uint8_t* sWh = sm + 65536;    // W [128 rows i][128 j] after the last head (X, dY region)
   uint8_t* sWl = sm + 98304;
-  uint8_t* sHh = sm + 131072;   // H [64 rows p][64 n] MN-major B operand
-  uint8_t* sHl = sm + 139264;
-  uint8_t* sGh = sm + 147456;   // g [64 rows p][64 n]
-  uint8_t* sGl = sm + 155648;
+  constexpr uint32_t kSpb = state_block_stride<kBf, PS>();  // n-block stride: PS rows p
+  uint8_t* sHh = sm + 131072;   // H [PS rows p][64 n] MN-major B operand (fp32: its lo tile;
+  uint8_t* sHl = sHh + kSpb;    // NS = 128: n 64-127 there)
+  uint8_t* sGh = sHh + state_tile_bytes<kBf, NS, PS>();  // g, the same
+  uint8_t* sGl = sGh + kSpb;
   __shared__ float s_cs2[kQ], s_dt[kQ], scratch[16];
   __shared__ __align__(16) float s_E[4][kQ];  // exp(cs_r - cs_j) dt_j, j < r = 32 w
   __shared__ uint64_t bar;
@@ -982,13 +1003,15 @@ __global__ void __launch_bounds__(512, 1) k_bwd64_bc(D64 d, int seg_heads,
   RowTile<512, kQ, Elem<kBf>, PS> tx, ty;
   StateRowTile<512, NS, kBf, PS> th, tg;  // the states as rows p of NS values
   // (NS = 128 or PS = 128: the state tiles are fetched at the head's start
-  // instead, to stay within the registers)
+  // instead, to stay within the registers; with both at 128, one after the
+  // other through th)
   constexpr bool kEarlyStates = NS == 64 && PS == 64;
+  constexpr bool kOneState = NS == 128 && PS == 128;
+  auto st_in_of = [&](int h) { return (((size_t)b * d.nc + c0) * d.H + h) * (PS * NS); };
+  auto st_out_of = [&](int h) { return (((size_t)b * d.nc + c1) * d.H + h) * (PS * NS); };
   auto fetch_states = [&](int h) {
-    const size_t st_in = (((size_t)b * d.nc + c0) * d.H + h) * (PS * NS);
-    const size_t st_out = (((size_t)b * d.nc + c1) * d.H + h) * (PS * NS);
-    th.fetch(hist + st_in);
-    tg.fetch(gstate + st_out);
+    th.fetch(hist + st_in_of(h));
+    tg.fetch(gstate + st_out_of(h));
   };
   auto fetch_head = [&](int h) {
     tx.fetch(x + (row0 * d.H + h) * PS, (size_t)d.H * PS);
@@ -998,7 +1021,8 @@ __global__ void __launch_bounds__(512, 1) k_bwd64_bc(D64 d, int seg_heads,
   if (nh > 0) fetch_head(h0);
   for (int hh = 0; hh < nh && ok; ++hh) {
     const int h = h0 + hh;
-    if (!kEarlyStates) fetch_states(h);
+    if (!kEarlyStates && !kOneState) fetch_states(h);
+    if (kOneState) th.fetch(hist + st_in_of(h));
     step_tables(d, dt, A[h] * kLog2e, b, (size_t)blk * kQ, kQ, h, s_cs2, s_dt, scratch);
     for (int e = tid; e < 4 * kQ; e += 512) {
       const int w = e >> 7, j = e & 127, r = 32 * w;
@@ -1007,7 +1031,12 @@ __global__ void __launch_bounds__(512, 1) k_bwd64_bc(D64 d, int seg_heads,
     tx.put(sXh, sXl, one);
     ty.put(sYh, sYl, one);
     th.put(sHh, sHl);
-    tg.put(sGh, sGl);
+    if (kOneState) {
+      th.fetch(gstate + st_out_of(h));
+      th.put(sGh, sGl);
+    } else {
+      tg.put(sGh, sGl);
+    }
     fence_async_smem();
     fence_before_sync();
     __syncthreads();
@@ -1065,10 +1094,10 @@ __global__ void __launch_bounds__(512, 1) k_bwd64_bc(D64 d, int seg_heads,
       const uint32_t id = idesc_bf16(128, NS, false, true);
       for (int kk = 0; kk < PS / 16; ++kk) {
         const uint32_t ko = (kk >> 2) * 16384 + (kk & 3) * 32;
-        mma3<kBf>(TdC, smem_u32(sYh) + ko, 16384, 16, false, smem_u32(sHh) + kk * 2048, 8192,
-                  8192, id, hh > 0 || kk > 0);
-        mma3<kBf>(TdB, smem_u32(sXh) + ko, 16384, 16, false, smem_u32(sGh) + kk * 2048, 8192,
-                  8192, id, hh > 0 || kk > 0);
+        mma3<kBf>(TdC, smem_u32(sYh) + ko, 16384, 16, false, smem_u32(sHh) + kk * 2048, kSpb,
+                  kSpb, id, hh > 0 || kk > 0);
+        mma3<kBf>(TdB, smem_u32(sXh) + ko, 16384, 16, false, smem_u32(sGh) + kk * 2048, kSpb,
+                  kSpb, id, hh > 0 || kk > 0);
       }
       mma_commit(&bar);
     }
@@ -1190,7 +1219,7 @@ cudaError_t chunk_outer_t(const Problem& p, int mode, float* out) {
 template <bool kBf, int NS, int PS>
 cudaError_t forward_scan_t(const Problem& p) {
   using E = Elem<kBf>;
-  const size_t smem = kScan64Bytes + 1024;
+  const size_t smem = scan64_bytes<kBf, NS, PS>() + 1024;
   cudaError_t e = set_smem64(k_scan64<kBf, NS, PS>, smem);
   if (e != cudaSuccess) return e;
   {
@@ -1208,14 +1237,14 @@ cudaError_t forward_scan_t(const Problem& p) {
 //   headdim 64, d_state 64 (fp32 or bf16), chunk 16-256;
 //   headdim 64, d_state 128 (bf16, chunks 16-64: the bf16 kernels of
 //     ssd_tc.cu take chunks 128 and 256);
-//   headdim 128, d_state 64 (bf16), chunk 16-256.
+//   headdim 128, d_state 64 or 128 (bf16), chunk 16-256.
 // Chunks of 256 run as 128-step sub-chunks (tc64_subchunks).
 bool tc64_supported(const Problem& p) {
   if (tc_forced_simt()) return false;
   if (p.T % kQ != 0) return false;
   if (p.Q != 16 && p.Q != 32 && p.Q != 64 && p.Q != 128 && p.Q != 256) return false;
   if (p.P == 64) return p.N == 64 || (p.N == 128 && p.bf16 && p.Q < 128);
-  return p.P == 128 && p.N == 64 && p.bf16;
+  return p.P == 128 && (p.N == 64 || p.N == 128) && p.bf16;
 }
 
 // Chunks longer than a block: the kernels run on the problem regrouped into
@@ -1263,14 +1292,17 @@ size_t tc64_bc_part_floats(const Problem& p) {
 
 cudaError_t tc64_chunk_outer(const Problem& p, int mode, float* out) {
   if (!p.bf16) return chunk_outer_t<false, 64, 64>(p, mode, out);
-  if (p.P == 128) return chunk_outer_t<true, 64, 128>(p, mode, out);
+  if (p.P == 128)
+    return p.N == 128 ? chunk_outer_t<true, 128, 128>(p, mode, out)
+                      : chunk_outer_t<true, 64, 128>(p, mode, out);
   return p.N == 128 ? chunk_outer_t<true, 128, 64>(p, mode, out)
                     : chunk_outer_t<true, 64, 64>(p, mode, out);
 }
 
 cudaError_t tc64_forward_scan(const Problem& p) {
   if (!p.bf16) return forward_scan_t<false, 64, 64>(p);
-  if (p.P == 128) return forward_scan_t<true, 64, 128>(p);
+  if (p.P == 128)
+    return p.N == 128 ? forward_scan_t<true, 128, 128>(p) : forward_scan_t<true, 64, 128>(p);
   return p.N == 128 ? forward_scan_t<true, 128, 64>(p) : forward_scan_t<true, 64, 64>(p);
 }
 
@@ -1284,7 +1316,7 @@ cudaError_t backward_t(const Problem& p) {
   const D64 d = d64_of(p);
   const int nb = p.T / kQ;
   {
-    const size_t smem = kBwdX64Bytes + 1024;
+    const size_t smem = bwdx64_bytes<kBf, NS, PS>() + 1024;
     if ((e = set_smem64(k_bwd64_x<kBf, NS, PS>, smem)) != cudaSuccess) return e;
     LaunchScope ls("bwd_x_tc64", p.stream);
     k_bwd64_x<kBf, NS, PS><<<dim3(nb, p.H, p.B), 512, smem, p.stream>>>(
@@ -1295,7 +1327,7 @@ cudaError_t backward_t(const Problem& p) {
   const int sh = tc64_seg_heads(p);
   const int nseg = (p.hpg + sh - 1) / sh;
   {
-    const size_t smem = kBwdBC64Bytes + 1024;
+    const size_t smem = bwdbc64_bytes<kBf, NS, PS>() + 1024;
     if ((e = set_smem64(k_bwd64_bc<kBf, NS, PS>, smem)) != cudaSuccess) return e;
     LaunchScope ls("bwd_bc_tc64", p.stream);
     k_bwd64_bc<kBf, NS, PS><<<dim3(nseg, nb, p.B * p.G), 512, smem, p.stream>>>(
@@ -1317,7 +1349,8 @@ cudaError_t backward_t(const Problem& p) {
 // dB / dC kernel and its segment sums, and the dA, dD reduction.
 cudaError_t tc64_backward(const Problem& p) {
   if (!p.bf16) return backward_t<false, 64, 64>(p);
-  if (p.P == 128) return backward_t<true, 64, 128>(p);
+  if (p.P == 128)
+    return p.N == 128 ? backward_t<true, 128, 128>(p) : backward_t<true, 64, 128>(p);
   return p.N == 128 ? backward_t<true, 128, 64>(p) : backward_t<true, 64, 64>(p);
 }
 

@@ -69,8 +69,10 @@ def test_workspace_sizes(L):
     (64, 64, 256, False, 512, 1),    # chunk 256 as 128-step sub-chunks
     (64, 64, 256, True, 512, 1),
     (128, 64, 256, True, 512, 1),
+    (128, 128, 64, True, 512, 1),    # headdim 128 with d_state 128
+    (128, 128, 256, True, 512, 1),
     (128, 64, 64, False, 512, 0),    # headdim 128 in fp32: SIMT
-    (128, 128, 64, True, 512, 0),    # headdim 128 with d_state 128: SIMT
+    (128, 128, 64, False, 512, 0),
     (64, 128, 64, False, 512, 0),    # d_state 128 in fp32: SIMT
     (64, 64, 64, True, 192, 0),      # seqlen not a multiple of 128
     (32, 64, 64, True, 512, 0),

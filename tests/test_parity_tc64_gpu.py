@@ -1,7 +1,7 @@
 """GPU parity of the block family of tensor-core kernels (headdim 64 with
 d_state 64 in fp32 or bf16, or d_state 128 in bf16 at chunks below 128;
-headdim 128 with d_state 64 in bf16; chunk 16-128 processed as 128-step
-blocks, chunk 256 as 128-step sub-chunks; fp32 storage with every product as three
+headdim 128 with d_state 64 or 128 in bf16; chunk 16-128 processed as
+128-step blocks, chunk 256 as 128-step sub-chunks; fp32 storage with every product as three
 bf16 tcgen05 MMAs over hi/lo splits, bf16 storage with one MMA per product)
 against the float64 oracle at the storage type's tolerance, on every output;
 the kernels that ran are checked through the trace.
@@ -77,6 +77,10 @@ CASES = [
     (1, 512, 4, 2, 256, "f32", True, "decay_span", 64),
     (2, 512, 4, 1, 256, "bf16", False, "softplus", 64),
     (1, 768, 4, 2, 256, "bf16", True, "decay_span", 64, 128),
+    (2, 512, 4, 2, 128, "bf16", True, "softplus", 128, 128),   # headdim 128, d_state 128
+    (1, 512, 4, 1, 64, "bf16", True, "decay_span", 128, 128),
+    (1, 256, 8, 4, 32, "bf16", False, "softplus", 128, 128),
+    (1, 1024, 16, 1, 256, "bf16", True, "softplus", 128, 128),  # sub-chunks, head segments
 ]
 
 
@@ -187,3 +191,18 @@ def test_tc64_chunk_256_agrees_with_simt_path(nat):
         nat.check(nat.lib().ssd_force_kernel_path(-1))
     for k in tc:
         assert rel_err(tc[k], simt[k]) < TOL["f32"], k
+
+
+def test_tc64_bf16_headdim_128_d_state_128_agrees_with_simt_path(nat):
+    dims = synth.Dims(1, 512, 4, 128, 128, 2, 64, "bf16")
+    inp = synth.make_inputs(dims, 59, True, "softplus")
+    dev = to_device(dims, inp)
+    tc, names = traced_run(nat, dims, dev)
+    assert TC64_FWD | TC64_BWD <= names, names
+    nat.check(nat.lib().ssd_force_kernel_path(0))
+    try:
+        simt = run_gpu(dims, dev)
+    finally:
+        nat.check(nat.lib().ssd_force_kernel_path(-1))
+    for k in tc:
+        assert rel_err(tc[k], simt[k]) < TOL["bf16"], k

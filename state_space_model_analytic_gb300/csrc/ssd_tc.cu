@@ -444,16 +444,6 @@ k_state_scan_tc(const __grid_constant__ ScanStateMaps maps, TcDims d, const floa
     if (nc > 1) load_dt(1, dv_next);
     for (int it = 0; it < nc; ++it) {
       const int k = it & 1;
-      // MODE 1: this thread's share of H_{c-1} (fp32 history), converted to
-      // bf16 rows for hT[c] after the tile is scaled: p in [16 pw, 16 pw + 16)
-      // of rows n = 4 lane .. 4 lane + 3 (16-byte loads, coalesced over lanes)
-      float4 hv[16];
-      if (MODE == 1) {
-        const float* hsrc = hist + (((size_t)b * nc + chunk_of(it)) * d.H + h) * PN +
-                            (size_t)(16 * pw) * d.N + 4 * lane;
-#pragma unroll
-        for (int pp = 0; pp < 16; ++pp) hv[pp] = *(const float4*)(hsrc + (size_t)pp * d.N);
-      }
       // the stored values were fetched ahead; raw-dt mode: dt = softplus(...)
       if (kRaw) {
         dv[0] = dt_of<kRaw>(d, dv[0], h);
@@ -511,8 +501,19 @@ k_state_scan_tc(const __grid_constant__ ScanStateMaps maps, TcDims d, const floa
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar_scaled[k]);  // s_lastq too (release)
       if (MODE == 1) {
-        // hT[c] = H_{c-1} as bf16 rows n, off the consumers' path
+        // hT[c] = H_{c-1} as bf16 rows n, off the consumers' path: this
+        // thread's share of the fp32 history (p in [16 pw, 16 pw + 16) of
+        // rows n = 4 lane .. 4 lane + 3, 16-byte loads coalesced over the
+        // lanes), loaded only now: the proxy fence before the arrive above
+        // would otherwise wait for these loads
         const int c = chunk_of(it);
+        float4 hv[16];
+        {
+          const float* hsrc = hist + (((size_t)b * nc + c) * d.H + h) * PN +
+                              (size_t)(16 * pw) * d.N + 4 * lane;
+#pragma unroll
+          for (int pp = 0; pp < 16; ++pp) hv[pp] = *(const float4*)(hsrc + (size_t)pp * d.N);
+        }
         uint8_t* sRows2 = sm + 2 * stage_bytes + 16384;  // [128 rows n][64 p] bf16, SW128
         if (pt == 0) bulk_wait_read0();  // the previous store of sRows2 has read it
         named_sync(1, 128);

@@ -1533,15 +1533,6 @@ k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, long long nitems,
     ok = wait_or_flag(&bar_head, head_phase);  // also publishes the tables
     head_phase ^= 1;
     if (!ok) break;
-    // the next head's dt into s_dtn (read above for this head's tables), by
-    // asynchronous copies that warpgroups 2-3 wait for where they use them
-    if (wg >= 2 && hh + 1 < kh) {
-      const int r = tid - 256;
-      if (r < d.Q)
-        cp_async4(&s_dtn[r], dt + ((size_t)b * d.T + (size_t)c * d.Q + r) * d.H + h + 1);
-      else
-        s_dtn[r] = 0.f;
-    }
 
     // ---- mid-chunk state or state gradient (chunks of two blocks)
     if (two) {
@@ -1618,6 +1609,18 @@ k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, long long nitems,
     mma_phase ^= 1;
     fence_after_sync();
     if (!ok) break;
+
+    // the next head's dt into s_dtn (read at this head's start), by
+    // asynchronous copies that warpgroups 2-3 wait for where they use them;
+    // issued here, about 2 us before the next proxy fence (which would
+    // otherwise wait for them)
+    if (wg >= 2 && hh + 1 < kh) {
+      const int r = tid - 256;
+      if (r < d.Q)
+        cp_async4(&s_dtn[r], dt + ((size_t)b * d.T + (size_t)c * d.Q + r) * d.H + h + 1);
+      else
+        s_dtn[r] = 0.f;
+    }
 
     // ---- W = L o dt_j o dYX -> sW, L o CB -> sO, row / column sums of M.
     // Warpgroup wg covers the 32 columns [32 wg, 32 wg + 32) of row `row`, in

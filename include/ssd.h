@@ -105,10 +105,11 @@ SSD_API int ssd_forward(const ssd_dims* dims,
 /*
  * Backward of L = sum(dy * y).  Same inputs as ssd_forward plus dy.
  * chunk_states: the history ssd_forward wrote for the same inputs, or NULL to
- * recompute it inside this call (needs ssd_workspace_bytes(dims, 2)).  The
- * tensor-core block family at chunk 256 (d_state 64) works on 128-step
- * sub-chunks and recomputes their start states in either case (the same
- * kernels as ssd_forward, so the results do not depend on the argument).
+ * recompute it inside this call (needs ssd_workspace_bytes(dims, 2)).  At
+ * chunk 256 the tensor-core block family (headdim 64 with d_state 64;
+ * headdim 128) works on 128-step sub-chunks and recomputes their start
+ * states in either case (the same kernels as ssd_forward, so the results do
+ * not depend on the argument).
  * Outputs (all required except dh0): dx, ddt, dA, dB, dC, dD; dh0 (NULL = not
  * written; when h0 is NULL it is the gradient w.r.t. the zero initial state).
  * The gradient w.r.t. the final state is taken as zero.

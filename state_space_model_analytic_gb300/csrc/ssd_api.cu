@@ -188,13 +188,14 @@ size_t carve(Problem* p, char* base, int which) {
   p->dA_part = (float*)take(B * nc * (Q / 16) * H * sizeof(float));  // per (chunk, tile or block)
   p->dD_part = (float*)take(B * nc * (Q / 16) * H * sizeof(float));
   p->dtb_part = (float*)take(B * nc * (Q / 16) * H * sizeof(float));
-  // tensor-core backward: one counter for all CTAs and one per (b, g, chunk,
-  // 128-row block) unit; fp32 partials of dC, dB (2 x 128 x 128 floats) in two
-  // slots per CTA, at most kBwdMaxCtas CTAs and one per (unit, head) item
+  // tensor-core backward: one counter for all CTAs, then per (b, g, chunk,
+  // 128-row block) unit an arrival ticket and a written-partials counter; fp32
+  // partials of dC, dB (2 x 128 x 128 floats) in two slots per CTA, at most
+  // kBwdMaxCtas CTAs and one per (unit, head) item
   const size_t units = B * (size_t)p->G * nc * ((Q + 127) / 128);
   const size_t items = units * (size_t)p->hpg;
-  p->ntickets = (int)(1 + units);
-  p->tickets = (unsigned int*)take((1 + units) * sizeof(unsigned int));
+  p->ntickets = (int)(1 + 2 * units);
+  p->tickets = (unsigned int*)take((1 + 2 * units) * sizeof(unsigned int));
   // (the d_state-64 tensor-core backward keeps its per-segment dC, dB partials there)
   size_t part_floats = (items < kBwdMaxCtas ? items : kBwdMaxCtas) * 2 * 32768;
   if (tc64_supported(*p) && tc64_bc_part_floats(*p) > part_floats)

@@ -60,7 +60,7 @@ struct Problem {
   float* dA_part;  // [B][nc][Q/16][H]  (the used prefix depends on the kernel family)
   float* dD_part;  // [B][nc][Q/16][H]  (tile-count upper bound)
   float* dtb_part; // raw-dt mode: per-(b, chunk, block) sums of the dt_raw gradient, same layout
-  unsigned int* tickets;  // [1 + units] completion counters of the tensor-core backward
+  unsigned int* tickets;  // [1 + 2 units] completion counters of the tensor-core backward
   int ntickets;
   float* bwd_part;        // tensor-core backward: fp32 dC, dB partials, 2 slots per CTA
   unsigned int* fwd_flags;  // [B*nc*H + 1]: single-pass forward slot flags, then its tile counter

@@ -910,6 +910,21 @@ __device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned int* p) {
 __device__ __forceinline__ void st_release_gpu(unsigned int* p, unsigned v) {
   asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
+// Bounded wait (about kWaitLimitNs) until the counter *f reaches `target`;
+// false if it gave up.  Not inlined: it runs once per split unit, and kept
+// apart it leaves the register allocation of its callers' loops alone.
+__device__ __noinline__ bool wait_count_at_least(const unsigned int* f, unsigned int target) {
+  bool got = ld_acquire_gpu(f) >= target;
+  if (!got) {
+    const uint64_t t0 = globaltimer_ns();
+    while (!got) {
+#pragma unroll 1
+      for (int i = 0; i < 32 && !got; ++i) got = ld_acquire_gpu(f) >= target;
+      if (!got && globaltimer_ns() - t0 > kWaitLimitNs) break;
+    }
+  }
+  return got;
+}
 
 template <bool kRaw>
 __global__ void __launch_bounds__(256, 2)
@@ -1273,9 +1288,10 @@ k_fwd_single_tc(const __grid_constant__ ScanMaps maps, TcDims d, const float* __
 // an equal contiguous range of items, i.e. one or more segments of
 // consecutive heads of a unit.  Per segment the CTA loops over its heads and
 // accumulates dC and dB of the block over them in TMEM (fixed head order).  A
-// unit covered by one segment writes dC, dB directly; a unit split over
-// several CTAs writes fp32 partials, and the last of its segments to finish
-// (a per-unit ticket) sums them in segment order (deterministic).
+// unit covered by one segment writes dC, dB directly; of a unit split over
+// several CTAs, the last segment to finish (a per-unit ticket) keeps its sums
+// in TMEM, and the others write fp32 partials and count them in a per-unit
+// counter that it waits for; it sums all in segment order (deterministic).
 // Each block is treated as a chunk of 128 steps with
 //   state in  Hin  = H_{c-1} (k = 0) or H_mid  (k = 1),
 //   grad out  gout = g_c     (last block) or g_mid = exp(cs_255 - cs_127) g_c + R_1 (k = 0 of 2),
@@ -1323,7 +1339,8 @@ k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, long long nitems,
          float* __restrict__ ddt, float* __restrict__ dA_part, float* __restrict__ dD_part,
          float* __restrict__ dtb_part, float* __restrict__ d_dt_bias,
          void* __restrict__ dB_out, void* __restrict__ dC_out, float* __restrict__ dA,
-         float* __restrict__ dD, unsigned int* __restrict__ tickets, float* __restrict__ part) {
+         float* __restrict__ dD, unsigned int* __restrict__ tickets,
+         unsigned int* __restrict__ written, float* __restrict__ part) {
   extern __shared__ __align__(1024) uint8_t smraw[];
   uint8_t* sm = align1024(smraw);
   uint8_t* sC = sm + kBwC;
@@ -1900,35 +1917,52 @@ k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, long long nitems,
 
   // ---- dC and dB of the segment, summed over its heads in TMEM.
   // Warpgroup wg handles columns [32 wg, 32 wg + 32); dC first, then dB.
+  // A split unit: each segment takes the unit's arrival ticket as it ends;
+  // the last to arrive keeps its sums in TMEM and waits (bounded) for the
+  // others' fp32 partials, which they write and then count in the unit's
+  // written counter (`written`, after the arrival tickets).
   {
     const long long u0 = (long long)u * d.hpg;
     const int cta0 = cta_of(u0), nseg = cta_of(u0 + d.hpg - 1) - cta0 + 1;
     const int jc = wg;
-    // fp32 partials, column-major [n][row] (coalesced over rows), in this CTA's
-    // slot: 0 for its first segment, 1 for its last
-    float* pslot = part + ((size_t)blockIdx.x * 2 + (first_seg ? 0 : 1)) * 32768;
+    bool reducer = false;
     if (nseg > 1) {
-      if (ok) {
-#pragma unroll 1
-        for (int which = 0; which < 2; ++which) {
-          float v[32];
-          tmem_ld32((which ? TdB : TdC) + lane_base + jc * 32, v);
-          tmem_wait_ld();
-          float* pw = pslot + which * 16384;
-#pragma unroll
-          for (int i = 0; i < 32; ++i) pw[(jc * 32 + i) * 128 + row] = v[i];
-        }
-      }
-      __threadfence();
-      __syncthreads();
       if (tid == 0) s_flag = atomicAdd(&tickets[1 + u], 1u) == (unsigned int)(nseg - 1);
       __syncthreads();
-      if (s_flag) __threadfence();
+      reducer = s_flag != 0;
+      if (!reducer) {
+        // fp32 partial in this CTA's slot (0 for its first segment, 1 for its
+        // last), float4 i4 of every thread contiguous: [which][i4][thread]
+        float4* pslot = (float4*)(part + ((size_t)blockIdx.x * 2 + (first_seg ? 0 : 1)) * 32768);
+        if (ok) {
+#pragma unroll 1
+          for (int which = 0; which < 2; ++which) {
+            float v[32];
+            tmem_ld32((which ? TdB : TdC) + lane_base + jc * 32, v);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i4 = 0; i4 < 8; ++i4)
+              pslot[(which * 8 + i4) * kBwThreads + tid] =
+                  make_float4(v[4 * i4], v[4 * i4 + 1], v[4 * i4 + 2], v[4 * i4 + 3]);
+          }
+        }
+        __syncthreads();
+        if (tid == 0) {
+          __threadfence();
+          atomicAdd(written + u, 1u);
+        }
+      } else if (tid == 0) {
+        // (a wait that gives up sets the error word; the sums are then wrong)
+        if (!wait_count_at_least(written + u, (unsigned int)(nseg - 1))) atomicOr(&g_tc_error, 1u);
+        __threadfence();
+      }
+      if (reducer) __syncthreads();
     }
     // the unit's output: a single segment from TMEM, else by its last segment
-    // as the sum of the partials in segment order; bf16 -> staging in sO (dead
-    // since the last head's Gx product) -> TMA store, dC then dB
-    const bool write_out = ok && (nseg == 1 || s_flag);
+    // as the sum over the segments in order (its own from TMEM, the others'
+    // partials); bf16 -> staging in sO (dead since the last head's Gx
+    // product) -> TMA store, dC then dB
+    const bool write_out = ok && (nseg == 1 || reducer);
     if (write_out) {
 #pragma unroll 1
       for (int which = 0; which < 2; ++which) {
@@ -1939,13 +1973,28 @@ k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, long long nitems,
         } else {
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] = 0.f;
+#pragma unroll 1
           for (int j = 0; j < nseg; ++j) {
             const int cj = cta0 + j;
-            const long long first_item = (long long)cj * nitems / ncta;
-            const int side = first_item / d.hpg == u ? 0 : 1;
-            const float* q = part + ((size_t)cj * 2 + side) * 32768 + which * 16384;
+            if (cj == (int)blockIdx.x) {
+              float t[32];
+              tmem_ld32((which ? TdB : TdC) + lane_base + jc * 32, t);
+              tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] += __ldcg(q + (jc * 32 + i) * 128 + row);
+              for (int i = 0; i < 32; ++i) v[i] += t[i];
+            } else {
+              // slot 0 unless the unit starts inside that CTA's range
+              const int side = (j == 0 && (long long)cj * nitems / ncta < u0) ? 1 : 0;
+              const float4* q = (const float4*)(part + ((size_t)cj * 2 + side) * 32768);
+#pragma unroll
+              for (int i4 = 0; i4 < 8; ++i4) {
+                const float4 f = __ldcg(q + (which * 8 + i4) * kBwThreads + tid);
+                v[4 * i4] += f.x;
+                v[4 * i4 + 1] += f.y;
+                v[4 * i4 + 2] += f.z;
+                v[4 * i4 + 3] += f.w;
+              }
+            }
           }
         }
 #pragma unroll
@@ -2358,7 +2407,7 @@ cudaError_t tc_backward(const Problem& p) {
     LaunchScope ls("bwd_tc", p.stream);
     e = cudaLaunchKernelEx(&cfg, kern, maps, tc_dims(p), nitems, p.dt, p.A, p.D, p.ddt,
                            p.dA_part, p.dD_part, p.dtb_part, p.d_dt_bias, p.dB, p.dC, p.dA, p.dD,
-                           p.tickets, p.bwd_part);
+                           p.tickets, p.tickets + 1 + nitems / p.hpg, p.bwd_part);
   }
   if (e != cudaSuccess) return e;
   return cudaGetLastError();

@@ -204,6 +204,7 @@ size_t carve(Problem* p, char* base, int which) {
   if (sub) return off;  // (its backward recomputes hist_sub itself)
   p->hT = take(states / 2);  // bf16 copies for the tensor-core backward
   p->gT = take(states / 2);
+  if (Q == 256) p->gmT = take(states / 2);
   if (which == 2) p->hist = (float*)take(states);
   return off;
 }

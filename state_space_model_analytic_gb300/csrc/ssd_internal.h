@@ -66,6 +66,7 @@ struct Problem {
   unsigned int* fwd_flags;  // [B*nc*H + 1]: single-pass forward slot flags, then its tile counter
   void* hT;        // [B][nc][H][N][P] bf16: chunk-start states, rows n (tensor-core backward)
   void* gT;        // [B][nc][H][N][P] bf16: chunk-end state gradients, rows n
+  void* gmT;       // chunks of 256: [B][nc][H][N][P] bf16 state gradients at step 127, rows n
 
   cudaStream_t stream;
 };

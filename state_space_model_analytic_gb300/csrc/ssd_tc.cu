@@ -279,14 +279,20 @@ k_chunk_outer_tc(const __grid_constant__ OuterMaps maps, TcDims d, const float* 
 //   R_c^T = C_c^T (e o dY_c), e_i = exp(cs_i);
 //   gT[c] = g_c and hT[c] = H_{c-1} from hist, both bf16 rows n;
 //   g_{c-1} = exp(cs_last) g_c + R_c;  dh0 = g_{-1}.
+//   With gmid, chunks of 256 steps go through their middle: the product is
+//   taken in two halves, R_1^T over rows i >= 128 with e_i = exp(cs_i -
+//   cs_127) and R_0^T over rows i < 128 with e_i = exp(cs_i), and
+//   g_mid = exp(cs_255 - cs_127) g_c + R_1 (bf16 rows n, rows3 map),
+//   g_{c-1} = exp(cs_127) g_mid + R_0.
 struct ScanStateMaps {
   CUtensorMap u;     // x or dy: [B*T][H*P] bf16, box {64, Q}
   CUtensorMap v;     // B or C:  [B*T][G*N] bf16, box {64, Q}
   CUtensorMap rows;  // hT (MODE 0) or gT (MODE 1): [B*nc*H*N][P] bf16, box {64, 128} (store)
   CUtensorMap rows2; // hT (MODE 1), same layout (store)
+  CUtensorMap rows3; // g_mid rows (MODE 1, chunks of 256), same layout (store)
 };
 
-constexpr int kScanBufs = 4;  // TMEM product buffers (64 columns each)
+constexpr int kScanBufs = 4;  // TMEM product buffers (64 columns each; 128 when split in halves)
 
 __device__ __forceinline__ void named_sync(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
@@ -330,12 +336,12 @@ __global__ void __launch_bounds__(kScanThreads, 1)
 k_state_scan_tc(const __grid_constant__ ScanStateMaps maps, TcDims d, const float* __restrict__ dt,
                 const float* __restrict__ A, const float* __restrict__ h0,
                 float* __restrict__ hist, float* __restrict__ final_or_dh0,
-                unsigned int* __restrict__ tickets, int ntickets) {
+                unsigned int* __restrict__ tickets, int ntickets, int gmid) {
   extern __shared__ __align__(1024) uint8_t smraw[];
   uint8_t* sm = align1024(smraw);
   const int Q = d.Q;
   const uint32_t stage_bytes = 3u * Q * 128;  // V: 2 MN blocks of [Q][128 B]; U: [Q][128 B]
-  __shared__ float s_wsum[2][4], s_lastq[4], s_last[kScanBufs];
+  __shared__ float s_wsum[2][4], s_lastq[4], s_last[kScanBufs], s_midq[4], s_mid[kScanBufs];
   __shared__ uint64_t bar_load[2], bar_sfree[2], bar_scaled[2], bar_full[kScanBufs],
       bar_free[kScanBufs];
   __shared__ uint32_t tmem_base;
@@ -345,6 +351,10 @@ k_state_scan_tc(const __grid_constant__ ScanStateMaps maps, TcDims d, const floa
   const int nc = d.nc;
   const size_t PN = (size_t)d.P * d.N;
   auto chunk_of = [&](int it) { return MODE == 0 ? it : nc - 1 - it; };
+  // MODE 1 at 256 steps: the product in two halves (columns [0, 64): rows
+  // 128-255, [64, 128): rows 0-127 of the chunk) and g_mid on the way
+  const bool split = MODE == 1 && Q == 256 && gmid;
+  const uint32_t buf_cols = split ? 128 : 64;
 
   if (tid == 0) {
     prefetch_tmap(&maps.u);
@@ -362,7 +372,7 @@ k_state_scan_tc(const __grid_constant__ ScanStateMaps maps, TcDims d, const floa
     fence_mbar_init();
   }
   if (tid < 32) {
-    tmem_alloc(&tmem_base, 64 * kScanBufs);
+    tmem_alloc(&tmem_base, buf_cols * kScanBufs);
     tmem_relinquish();
   }
   fence_before_sync();
@@ -393,16 +403,22 @@ k_state_scan_tc(const __grid_constant__ ScanStateMaps maps, TcDims d, const floa
         const int k = it & 1, buf = it % kScanBufs;
         // chunk it scaled; its decay total; the buffer's previous product read out
         if (!wait_ws(&bar_scaled[k], (it >> 1) & 1, &s_abort)) break;
-        const float last2 = s_lastq[it & 3];
+        const float last2 = s_lastq[it & 3], mid2 = s_midq[it & 3];
         if (it >= kScanBufs && !wait_ws(&bar_free[buf], ((it / kScanBufs) - 1) & 1, &s_abort)) break;
         s_last[buf] = last2;
+        s_mid[buf] = mid2;
         mbar_arrive(&bar_full[buf]);
         fence_after_sync();
         uint8_t* sV = sm + k * stage_bytes;
         uint8_t* sU = sV + 2 * Q * 128;
-        for (int ks = 0; ks < Q / 16; ++ks)
-          mma_bf16(tm + 64 * buf, desc_sw128(smem_u32(sV) + ks * 2048, Q * 128, 1024),
-                   desc_sw128(smem_u32(sU) + ks * 2048, Q * 128, 1024), idesc, ks > 0);
+        const uint32_t tb = tm + buf_cols * buf;
+        for (int ks = 0; ks < Q / 16; ++ks) {
+          // split: K-steps 8-15 (rows 128-255) into columns [0, 64), 0-7 into [64, 128)
+          const bool hi = ks >= 8;
+          mma_bf16(split && !hi ? tb + 64 : tb, desc_sw128(smem_u32(sV) + ks * 2048, Q * 128, 1024),
+                   desc_sw128(smem_u32(sU) + ks * 2048, Q * 128, 1024), idesc,
+                   split ? (ks & 7) > 0 : ks > 0);
+        }
         mma_commit(&bar_full[buf]);
         mma_commit(&bar_sfree[k]);
         ++mma_issued;
@@ -468,10 +484,16 @@ k_state_scan_tc(const __grid_constant__ ScanStateMaps maps, TcDims d, const floa
       }
       const float cs0 = base + run - x1;  // cs of this thread's first value
       const float cs1 = base + run;       // and of its second
-      // weights of this thread's rows pt * per + {0, 1}
-      const float w0 = MODE == 0 ? exp2f(last2 - cs0) * dv[0] : exp2f(cs0);
-      const float w1 = MODE == 0 ? exp2f(last2 - cs1) * dv[1] : exp2f(cs1);
-      if (pt == 0) s_lastq[it & 3] = last2;
+      // weights of this thread's rows pt * per + {0, 1}; split: rows from 128
+      // on (threads 64-127) relative to cs_127, the end of warps 0-1's rows
+      const float mid2 = split ? s_wsum[k][0] + s_wsum[k][1] : 0.f;
+      const float ref = split && pt >= 64 ? mid2 : 0.f;
+      const float w0 = MODE == 0 ? exp2f(last2 - cs0) * dv[0] : exp2f(cs0 - ref);
+      const float w1 = MODE == 0 ? exp2f(last2 - cs1) * dv[1] : exp2f(cs1 - ref);
+      if (pt == 0) {
+        s_lastq[it & 3] = last2;
+        s_midq[it & 3] = mid2;
+      }
       dv[0] = dv_next[0];
       dv[1] = dv_next[1];
       if (it + 2 < nc) load_dt(it + 2, dv_next);
@@ -582,17 +604,36 @@ k_state_scan_tc(const __grid_constant__ ScanStateMaps maps, TcDims d, const floa
       put_rows(st, &maps.rows, srow);  // MODE 0: hT[c] = H_{c-1}; MODE 1: gT[c] = g_c
       ok = __all_sync(0xffffffffu, wait_ws(&bar_full[buf], (it / kScanBufs) & 1, &s_abort));
       // warp-uniform; the other consumer warps still reach the named barriers
-      if (ok) {
-        fence_after_sync();
-        const float e = exp2f(s_last[buf]);
+      // st = e st + (the 64 columns at col of the buffer)
+      auto advance = [&](float e, uint32_t col) {
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
           float v[32];
-          tmem_ld32(tm + 64 * buf + 32 * half + lane_base, v);
+          tmem_ld32(tm + buf_cols * buf + col + 32 * half + lane_base, v);
           tmem_wait_ld();
 #pragma unroll
           for (int i = 0; i < 32; ++i) st[32 * half + i] = fmaf(e, st[32 * half + i], v[i]);
         }
+      };
+      if (split) {
+        // g_mid = exp(cs_255 - cs_127) g_c + R_1 out as bf16 rows through the
+        // staging tile (every consumer warp reaches its barriers), then R_0
+        if (ok) {
+          fence_after_sync();
+          advance(exp2f(s_last[buf] - s_mid[buf]), 0);
+        }
+        if (named_sync_or(2, 128, !ok)) {
+          ok = false;
+          break;
+        }
+        put_rows(st, &maps.rows3, srow);
+        advance(exp2f(s_mid[buf]), 64);
+        fence_before_sync();
+        __syncwarp();
+        if ((tid & 31) == 0) mbar_arrive(&bar_free[buf]);
+      } else if (ok) {
+        fence_after_sync();
+        advance(exp2f(s_last[buf]), 0);
         fence_before_sync();
         __syncwarp();
         if ((tid & 31) == 0) mbar_arrive(&bar_free[buf]);
@@ -612,7 +653,7 @@ k_state_scan_tc(const __grid_constant__ ScanStateMaps maps, TcDims d, const floa
   grid_dep_launch();
   fence_before_sync();
   __syncthreads();
-  if (tid < 32) tmem_dealloc(tm, 64 * kScanBufs);
+  if (tid < 32) tmem_dealloc(tm, buf_cols * kScanBufs);
 }
 
 // ---------------------------------------------------------------------------
@@ -1318,6 +1359,7 @@ struct BwdMaps {
   CUtensorMap dC;  // [B*T][G*N] bf16, box {64, 128} (store)
   CUtensorMap ht;  // chunk-start states, bf16 rows n: [B*nc*H*N][P], box {64, 128}
   CUtensorMap gt;  // chunk-end state gradients, same layout
+  CUtensorMap gmt; // mid-chunk state gradients (chunks of two blocks), same layout
 };
 
 constexpr int kBwThreads = 512;       // four warpgroups share each TMEM lane quarter
@@ -1340,7 +1382,7 @@ k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, long long nitems,
          float* __restrict__ dtb_part, float* __restrict__ d_dt_bias,
          void* __restrict__ dB_out, void* __restrict__ dC_out, float* __restrict__ dA,
          float* __restrict__ dD, unsigned int* __restrict__ tickets,
-         unsigned int* __restrict__ written, float* __restrict__ part) {
+         unsigned int* __restrict__ written, float* __restrict__ part, int gmid) {
   extern __shared__ __align__(1024) uint8_t smraw[];
   uint8_t* sm = align1024(smraw);
   uint8_t* sC = sm + kBwC;
@@ -1383,7 +1425,10 @@ k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, long long nitems,
   // the current segment's unit
   int k = 0, c = 0, g = 0, b = 0, base = 0, crow = 0, row0 = 0;
   const bool two = nblk == 2;
-  const uint32_t head_bytes = (two ? 80 : 32) * 1024 + 32 * 1024;
+  // a block whose head forms the mid-chunk state (k = 1) or state gradient
+  // (k = 0, unless the state pass has written it: gmid) from the other
+  // block's tiles
+  auto mid_of = [&](int kk) { return two && (kk == 1 || !gmid); };
 
   if (tid == 0) {
     prefetch_tmap(&maps.x);
@@ -1392,6 +1437,7 @@ k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, long long nitems,
     prefetch_tmap(&maps.C);
     prefetch_tmap(&maps.ht);
     prefetch_tmap(&maps.gt);
+    prefetch_tmap(&maps.gmt);
     mbar_init(&bar_shared, 1);
     mbar_init(&bar_head, 1);
     mbar_init(&bar_mma, 1);
@@ -1407,18 +1453,21 @@ k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, long long nitems,
   const uint32_t tm = tmem_base;
   const uint32_t T0 = tm, T1 = tm + 128, TdC = tm + 256, TdB = tm + 384;
 
+  // the state-gradient rows a head of block kk reads: g_c, or g_mid for the
+  // first block of two when the state pass has written it
+  auto gout_map = [&](int kk) { return two && kk == 0 && gmid ? &maps.gmt : &maps.gt; };
   // with_state: also the head's state and state-gradient rows (outputs of the
   // state pass); the first head fetches them after waiting for that kernel
-  // tiles of head h of unit uu (the head's own and, for chunks of two blocks,
-  // the other block's tiles for the mid-chunk state / state gradient)
+  // tiles of head h of unit uu (the head's own and, where it forms the
+  // mid-chunk state or state gradient, the other block's tiles for it)
   auto issue_head_loads = [&](int uu, int h, bool with_state) {
     const int kk = uu % nblk, cc = (uu / nblk) % d.nc, gg = (uu / (nblk * d.nc)) % d.G;
     const int bb = uu / (nblk * d.nc * d.G);
     const int crow_u = bb * d.T + cc * d.Q, row0_u = crow_u + 128 * kk;
-    mbar_expect_tx(&bar_head, head_bytes);
+    mbar_expect_tx(&bar_head, (mid_of(kk) ? 80 : 32) * 1024 + 32 * 1024);
     tma_load_2d(sX, &maps.x, h * d.P, row0_u, &bar_head);
     tma_load_2d(sDY, &maps.dy, h * d.P, row0_u, &bar_head);
-    if (two) {
+    if (mid_of(kk)) {
       if (kk == 1) {
         tma_load_2d(sXO, &maps.x, h * d.P, crow_u, &bar_head);
         tma_load_2d(sW, &maps.B, gg * d.N, crow_u, &bar_head);
@@ -1432,7 +1481,7 @@ k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, long long nitems,
     if (with_state) {
       const int srow = ((bb * d.nc + cc) * d.H + h) * d.N;
       tma_load_2d(sH, &maps.ht, 0, srow, &bar_head);
-      tma_load_2d(sG, &maps.gt, 0, srow, &bar_head);
+      tma_load_2d(sG, gout_map(kk), 0, srow, &bar_head);
     }
   };
   // C_k and B_k of unit uu
@@ -1498,6 +1547,7 @@ k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, long long nitems,
   row0 = crow + base;
   const int h_first = g * d.hpg + j0;
   const bool first_seg = x == it_begin;
+  const bool mid = mid_of(k);
   if (tid == 0) {
     issue_unit_loads(u);
     issue_head_loads(u, h_first, !first_seg);
@@ -1507,7 +1557,7 @@ k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, long long nitems,
     if (tid == 0) {
       const int srow = ((b * d.nc + c) * d.H + h_first) * d.N;
       tma_load_2d(sH, &maps.ht, 0, srow, &bar_head);
-      tma_load_2d(sG, &maps.gt, 0, srow, &bar_head);
+      tma_load_2d(sG, gout_map(k), 0, srow, &bar_head);
     }
   }
   // A and D of the next head are loaded one head ahead and its dt goes
@@ -1552,7 +1602,7 @@ k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, long long nitems,
     if (!ok) break;
 
     // ---- mid-chunk state or state gradient (chunks of two blocks)
-    if (two) {
+    if (mid) {
       if (k == 1)  // X_0 rows j by exp(cs_127 - cs_j) dt_j
         scale_tile_rows(sXO, 128 * 8, [&](int r) { return exp2f(s_cs2[127] - s_cs2[r]) * s_dt[r]; });
       else  // dY_1 rows i by exp(cs_i - cs_127)
@@ -1602,7 +1652,7 @@ k_bwd_tc(const __grid_constant__ BwdMaps maps, TcDims d, long long nitems,
       }
       s_hg[wg][row] = hg;
     }
-    if (two) {  // every thread's T1 reads before the next products reuse T1
+    if (mid) {  // every thread's T1 reads before the next products reuse T1
       fence_async_smem();
       fence_before_sync();
       __syncthreads();
@@ -2290,7 +2340,8 @@ cudaError_t tc_state_scan(const Problem& p, const char* name, float* final_or_dh
   if (!map_bf16(&maps.u, u, (uint64_t)p.B * p.T, (uint64_t)p.H * p.P, p.Q) ||
       !map_bf16(&maps.v, v, (uint64_t)p.B * p.T, (uint64_t)p.G * p.N, p.Q) ||
       !map_bf16(&maps.rows, MODE == 0 ? p.hT : p.gT, srows, (uint64_t)p.P, 128) ||
-      !map_bf16(&maps.rows2, p.hT, srows, (uint64_t)p.P, 128))
+      !map_bf16(&maps.rows2, p.hT, srows, (uint64_t)p.P, 128) ||
+      !map_bf16(&maps.rows3, MODE == 1 && p.gmT ? p.gmT : p.hT, srows, (uint64_t)p.P, 128))
     return cudaErrorInvalidValue;
   // two pipeline stages of tiles + the bf16 row staging tile(s)
   const size_t smem = 2 * 3 * (size_t)p.Q * 128 + (MODE == 1 ? 2 : 1) * 16384 + 1024;
@@ -2301,7 +2352,8 @@ cudaError_t tc_state_scan(const Problem& p, const char* name, float* final_or_dh
     LaunchScope ls(name, p.stream);
     e = launch_pdl(kern, dim3(p.H, p.B), dim3(kScanThreads), smem, p.stream, maps,
                    tc_dims(p), p.dt, p.A, p.h0, p.hist, final_or_dh0,
-                   MODE == 1 ? p.tickets : (unsigned int*)nullptr, p.ntickets);
+                   MODE == 1 ? p.tickets : (unsigned int*)nullptr, p.ntickets,
+                   (int)(MODE == 1 && p.Q == 256 && p.gmT != nullptr));
   }
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
@@ -2355,7 +2407,10 @@ cudaError_t tc_forward_single(const Problem& p) {
 
 cudaError_t tc_backward(const Problem& p) {
   cudaError_t e;
-  if (tc_fused_states(p)) {
+  // the fused state scan also writes the mid-chunk state gradients of
+  // 256-step chunks, which the backward then reads instead of forming them
+  const bool fused = tc_fused_states(p), gmid = fused && p.Q == 256 && p.gmT != nullptr;
+  if (fused) {
     if ((e = tc_state_scan<1>(p, "state_scan_bwd_tc", p.dh0)) != cudaSuccess) return e;
   } else {
     if ((e = tc_chunk_outer(p, 1, p.dstate)) != cudaSuccess) return e;
@@ -2378,7 +2433,8 @@ cudaError_t tc_backward(const Problem& p) {
       !map_bf16(&maps.dB, p.dB, rows, (uint64_t)p.G * p.N, 128) ||
       !map_bf16(&maps.dC, p.dC, rows, (uint64_t)p.G * p.N, 128) ||
       !map_bf16(&maps.ht, p.hT, srows, (uint64_t)p.P, 128) ||
-      !map_bf16(&maps.gt, p.gT, srows, (uint64_t)p.P, 128))
+      !map_bf16(&maps.gt, p.gT, srows, (uint64_t)p.P, 128) ||
+      !map_bf16(&maps.gmt, gmid ? p.gmT : p.gT, srows, (uint64_t)p.P, 128))
     return cudaErrorInvalidValue;
   const size_t smem = kBwBytes + 1024;
   auto kern = p.dt_bias ? k_bwd_tc<true> : k_bwd_tc<false>;
@@ -2407,7 +2463,7 @@ cudaError_t tc_backward(const Problem& p) {
     LaunchScope ls("bwd_tc", p.stream);
     e = cudaLaunchKernelEx(&cfg, kern, maps, tc_dims(p), nitems, p.dt, p.A, p.D, p.ddt,
                            p.dA_part, p.dD_part, p.dtb_part, p.d_dt_bias, p.dB, p.dC, p.dA, p.dD,
-                           p.tickets, p.tickets + 1 + nitems / p.hpg, p.bwd_part);
+                           p.tickets, p.tickets + 1 + nitems / p.hpg, p.bwd_part, (int)gmid);
   }
   if (e != cudaSuccess) return e;
   return cudaGetLastError();

@@ -923,10 +923,13 @@ k_fwd_scan_tc(const __grid_constant__ ScanMaps maps, TcDims d, const float* __re
 // ---------------------------------------------------------------------------
 // Single-pass forward: the chunk-state pass folded into the chunk scan with a
 // bounded look-back, for the shapes whose per-(b, h) state scan fills the GPU.
-// One CTA per (b, chunk, head); a CTA takes its tile from a counter, chunk-
-// major, so the CTA of chunk c - 1 of the same (b, h) took its tile earlier
-// and is resident or finished (no wait can be on a CTA that has not started).
-// Per CTA:
+// Tiles are (b, chunk, head), taken from a counter chunk-major by resident
+// CTAs (two per SM, each looping over tiles): the tile of chunk c - 1 of the
+// same (b, h) was taken earlier by a CTA that processes its tiles in the
+// order it took them, and every wait is on an earlier tile, so no wait can
+// be on a tile nobody is processing.  A CTA takes its next tile at the start
+// of its current tile's last y block and fetches that tile's dt meanwhile.
+// Per tile:
 //   A. before any wait, the chunk's state contributions block by block, the
 //      last block first: S_k^T = B_k^T (w o X_k), w_j = exp(cs_end(k) - cs_j)
 //      dt_j, end(k) the block's last row, with w o X_k written into the C
@@ -989,7 +992,8 @@ k_fwd_single_tc(const __grid_constant__ ScanMaps maps, TcDims d, const float* __
   const int Q = d.Q, nblk = Q / 128;
   const uint32_t lane_base = (uint32_t)(q * 32) << 16;
   const size_t PN = 64 * 128;
-  unsigned int* counter = flags + (size_t)d.B * d.nc * d.H;
+  const int ntiles = d.B * d.nc * d.H;
+  unsigned int* counter = flags + (size_t)ntiles;
 
   if (tid == 0) {
     s_tile = (int)atomicAdd(counter, 1u);
@@ -1009,15 +1013,30 @@ k_fwd_single_tc(const __grid_constant__ ScanMaps maps, TcDims d, const float* __
   fence_before_sync();
   __syncthreads();
   fence_after_sync();
-  const int bh = d.B * d.H, tile = s_tile;
-  const int c = tile / bh, b = (tile % bh) / d.H, h = tile % d.H;
-  const int g = h / d.hpg;
-  const float Dh = D[h];
+  const int bh = d.B * d.H;
   const uint32_t tm = tmem_base;
   const uint32_t tCB = tm, tY = tm, tYs = tm + 128, tS0 = tm + 192;
   const uint32_t tS1 = tm + 128;  // block 1's state contribution, read out before Ys reuses it
-  uint32_t load_phase = 0, mma_phase = 0;
+  uint32_t load_phase = 0, mma_phase = 0, c0_phase = 0;
   bool ok = true;
+  int tile = s_tile;
+  // a tile's stored dt of row tid of its chunk and its head's A (raw-dt mode:
+  // dt_raw, a_log and dt_bias), fetched a tile ahead and used at its start
+  float dv, av, bv;
+  auto fetch = [&](int t) {
+    const int hh = t % d.H;
+    dv = t < ntiles && tid < Q
+             ? dt[((size_t)((t % bh) / d.H) * d.T + (size_t)(t / bh) * Q + tid) * d.H + hh]
+             : 0.f;
+    av = t < ntiles ? (kRaw ? d.a_log[hh] : A[hh]) : 0.f;
+    bv = kRaw && t < ntiles ? d.dt_bias[hh] : 0.f;
+  };
+  fetch(tile);
+
+  while (tile < ntiles && ok) {
+  const int c = tile / bh, b = (tile % bh) / d.H, h = tile % d.H;
+  const int g = h / d.hpg;
+  const float Dh = D[h];
   const int crow = b * d.T + c * Q;
 
   auto issue_state_loads = [&](int row0) {  // B and X of one block
@@ -1026,8 +1045,21 @@ k_fwd_single_tc(const __grid_constant__ ScanMaps maps, TcDims d, const float* __
     tma_load_2d(sB + 16384, &maps.B, g * d.N + 64, row0, &bar_load);
     tma_load_2d(sX, &maps.x, h * d.P, row0, &bar_load);
   };
-  if (tid == 0) issue_state_loads(crow + (nblk - 1) * 128);
-  chunk_cumsum_256<kRaw>(d, dt, A, b, c, h, s_cs2, s_dt, scratch);
+  if (tid == 0) {
+    bulk_wait_read0();  // the previous tile's last y store has read its staging
+    issue_state_loads(crow + (nblk - 1) * 128);
+  }
+  {
+    // the chunk-local inclusive cumsum of dt * A (log2 units)
+    const float dtv = kRaw && tid < Q ? softplus_tc(dv + bv) : dv;
+    const float a2 = (kRaw ? -expf(av) : av) * kLog2e;
+    const float cs = block_inclusive_scan(dtv * a2, scratch);
+    if (tid < Q) {
+      s_cs2[tid] = cs;
+      s_dt[tid] = dtv;
+    }
+    __syncthreads();
+  }
 
   // ---- tile places, in 16 KB tiles R0-R5 of the 96 KB:
   //   one block (Q = 128): C R0-R1 (later M, then the y staging), B R2-R3,
@@ -1175,6 +1207,7 @@ k_fwd_single_tc(const __grid_constant__ ScanMaps maps, TcDims d, const float* __
   for (int blk = 0; blk < nblk && ok; ++blk) {
     const int row0 = crow + blk * 128;
     const int base = blk * 128;
+    if (blk == nblk - 1 && tid == 0) s_tile = (int)atomicAdd(counter, 1u);  // the next tile
     for (int e = tid; e < 4 * 128; e += 256) {
       const int w = e >> 7, jj = e & 127;
       const int r = base + 32 * w, J = base + jj;
@@ -1184,7 +1217,8 @@ k_fwd_single_tc(const __grid_constant__ ScanMaps maps, TcDims d, const float* __
     const float ref2 = blk == 0 ? 0.f : s_cs2[base - 1];
     fence_async_smem();
     if (two && blk == 0) {
-      ok = wait_or_flag(&bar_c0, 0);
+      ok = wait_or_flag(&bar_c0, c0_phase);
+      c0_phase ^= 1;
     } else {
       ok = wait_or_flag(&bar_load, load_phase);
       load_phase ^= 1;
@@ -1270,6 +1304,7 @@ k_fwd_single_tc(const __grid_constant__ ScanMaps maps, TcDims d, const float* __
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
+    if (blk == nblk - 1) fetch(s_tile);  // the next tile (published by the barrier), under this block
     if (tid == 0) {
       const uint32_t id_y = idesc_bf16(128, 64, false, true);
       for (int kk = 0; kk < 8; ++kk) {
@@ -1316,6 +1351,13 @@ k_fwd_single_tc(const __grid_constant__ ScanMaps maps, TcDims d, const float* __
         tma_load_2d(sX, &maps.x, h * d.P, row0 + 128, &bar_load);
       }
     }
+  }
+  // the tile's TMEM reads and shared-memory use are done; its successor
+  // (taken above, or past the last tile: the loop ends)
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  tile = s_tile;
   }
   grid_dep_launch();
   if (tid == 0) bulk_wait0();
@@ -2425,10 +2467,16 @@ cudaError_t tc_forward_single(const Problem& p) {
   const size_t smem = kScanBytes + 1024;
   auto kern = p.dt_bias ? k_fwd_single_tc<true> : k_fwd_single_tc<false>;
   if ((e = set_smem_tc(kern, smem)) != cudaSuccess) return e;
+  // resident CTAs, two per SM, each looping over tiles from the counter
+  int nsm = 0, dev = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+  const long long ntiles = (long long)(nflags - 1);
+  const unsigned grid = (unsigned)(ntiles < 2LL * nsm ? ntiles : 2LL * nsm);
   {
     LaunchScope ls("fwd_single_tc", p.stream);
-    kern<<<(unsigned)(nflags - 1), 256, smem, p.stream>>>(
-        maps, tc_dims(p), p.dt, p.A, p.D, p.h0, p.hist, p.final_state, p.fwd_flags);
+    kern<<<grid, 256, smem, p.stream>>>(maps, tc_dims(p), p.dt, p.A, p.D, p.h0, p.hist,
+                                        p.final_state, p.fwd_flags);
   }
   return cudaGetLastError();
 }

@@ -176,6 +176,23 @@ def aggregate_ranks(ms_local, tokens_local, dist=None, device=None):
 CLOCK_PAD_S = 0.6
 
 
+def packed(specs, device, pin=False, align=256):
+    """One flat byte buffer on `device` (pinned host memory if `pin`) holding a
+    tensor of each (shape, dtype) in `specs` at an `align`-byte offset: the
+    buffer and a dict of contiguous views into it."""
+    import torch
+    offs, total = {}, 0
+    for k, (shape, dtype) in specs.items():
+        nbytes = int(np.prod(shape)) * dtype.itemsize
+        offs[k] = (total, nbytes)
+        total += -(-nbytes // align) * align
+    flat = torch.empty(total, dtype=torch.uint8, device=device)
+    if pin:
+        flat = flat.pin_memory()
+    views = {k: flat[o:o + n].view(specs[k][1]).view(specs[k][0]) for k, (o, n) in offs.items()}
+    return flat, views
+
+
 def pad_replays(graph, flush, seconds):
     """Replay `graph` (L2 flushed between replays, as in the timed loop) for
     about `seconds` of wall time; untimed."""
@@ -503,40 +520,44 @@ def main():
 
     # ---- e2e: host buffers through the public API, copies inside the timed region.
     # Every step copies all its inputs in from pinned host memory and all its
-    # results out.  Steps are pipelined over three device buffer sets: while
-    # step i computes on set i % 3, step i + 1's inputs go into set (i + 1) % 3
-    # and step i - 1's results leave set (i - 1) % 3.  Each such iteration is
-    # one CUDA graph (three concurrent branches: the host-to-device copies, the
-    # forward and backward API calls, the device-to-host copies), captured
-    # once per rotation of the sets; the graphs replay in stream order, so an
-    # iteration's branches see the previous iteration complete.  The timed
-    # region is: step 0's inputs in, n iterations, step n - 1's results out
-    # (the first iteration also copies out a set no step wrote, and the last
-    # one copies in a step that is not computed: both only add time).
+    # results out, each direction as one copy: the tensors are 256-byte-aligned
+    # views of one pinned host buffer and one device buffer per direction (17
+    # separate copies, several of a few bytes, cost about 40 us more per step
+    # on the host link).  Steps are pipelined over three device buffer sets:
+    # while step i computes on set i % 3, step i + 1's inputs go into set
+    # (i + 1) % 3 and step i - 1's results leave set (i - 1) % 3, on three
+    # streams ordered by events (see pipeline below; a CUDA graph per
+    # iteration joined the three branches at every step and left the copy
+    # streams idle meanwhile).  The timed region holds every step's copies
+    # in, its forward and backward calls and its copies out.
     e2e = None
     if not args.no_e2e:
-        host_in = {k: (None if v is None else v.cpu().pin_memory()) for k, v in t_in.items()}
         outs = ["y", "final_state", "dx", "ddt", "dA", "dB", "dC", "dD", "dh0"]
         all_out = {**fwd_out, **bwd_out}
-        host_out = {k: torch.empty(all_out[k].shape, dtype=all_out[k].dtype).pin_memory()
-                    for k in outs}
-        h2d = sum(v.numel() * v.element_size() for v in host_in.values() if v is not None)
-        d2h = sum(v.numel() * v.element_size() for v in host_out.values())
-        sets = [{"in": {k: (None if v is None else torch.empty_like(v)) for k, v in t_in.items()},
-                 "fwd": {k: torch.empty_like(v) for k, v in fwd_out.items()},
-                 "bwd": {k: torch.empty_like(v) for k, v in bwd_out.items()}} for _ in range(3)]
+        in_specs = {k: (tuple(v.shape), v.dtype) for k, v in t_in.items() if v is not None}
+        out_specs = {k: (tuple(all_out[k].shape), all_out[k].dtype) for k in outs}
+        host_in_flat, host_in = packed(in_specs, "cpu", pin=True)
+        for k, v in host_in.items():
+            v.copy_(t_in[k].cpu())
+        host_out_flat, _ = packed(out_specs, "cpu", pin=True)
+        h2d = host_in_flat.numel()
+        d2h = host_out_flat.numel()
+        sets = []
+        for _ in range(3):
+            in_flat, ins = packed(in_specs, dev)
+            out_flat, ov = packed(out_specs, dev)
+            sets.append({"in": {k: ins.get(k) for k in t_in}, "in_flat": in_flat, "out_flat": out_flat,
+                         "fwd": {"y": ov["y"], "final_state": ov["final_state"],
+                                 "chunk_states": torch.empty_like(fwd_out["chunk_states"])},
+                         "bwd": {k: ov[k] for k in bwd_out}})
         s_h2d, s_d2h = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
         n_e2e = max(3, min(args.steps, 200))
 
         def copy_in(st):
-            for k, v in host_in.items():
-                if v is not None:
-                    st["in"][k].copy_(v, non_blocking=True)
+            st["in_flat"].copy_(host_in_flat, non_blocking=True)
 
         def copy_out(st):
-            res = {"y": st["fwd"]["y"], "final_state": st["fwd"]["final_state"], **st["bwd"]}
-            for k in outs:
-                host_out[k].copy_(res[k], non_blocking=True)
+            host_out_flat.copy_(st["out_flat"], non_blocking=True)
 
         def compute(st):
             ti, fo, bo = st["in"], st["fwd"], st["bwd"]
@@ -545,51 +566,57 @@ def main():
             ssd.backward(ti["x"], ti["dt"], ti["A"], ti["B"], ti["C"], ti["D"], ti["h0"],
                          ti["dy"], fo["chunk_states"], chunk=Q, out=bo, workspace=ws_b)
 
-        def iteration(r):
-            """Step r computes on set r % 3, with the neighbours' copies beside it."""
+        in_done = [torch.cuda.Event() for _ in range(3)]
+        comp_done = [torch.cuda.Event() for _ in range(3)]
+        out_done = [torch.cuda.Event() for _ in range(3)]
+
+        def pipeline(n):
+            """n steps, step r on set r % 3: its inputs go in (stream s_h2d)
+            once step r - 3, the set's last user, has computed; it computes
+            once they are in and step r - 3's results are out; its results
+            leave (stream s_d2h) once it has computed.  Events order the
+            three streams, so each direction's copies follow one another
+            without waiting for the other branches."""
             cur = torch.cuda.current_stream()
             s_h2d.wait_stream(cur)
             s_d2h.wait_stream(cur)
-            with torch.cuda.stream(s_h2d):
-                copy_in(sets[(r + 1) % 3])
-            with torch.cuda.stream(s_d2h):
-                copy_out(sets[(r + 2) % 3])
-            compute(sets[r % 3])
+
+            def put_in(r):
+                st = r % 3
+                s_h2d.wait_event(comp_done[st])
+                with torch.cuda.stream(s_h2d):
+                    copy_in(sets[st])
+                    in_done[st].record(s_h2d)
+
+            def take_out(r):
+                st = r % 3
+                s_d2h.wait_event(comp_done[st])
+                with torch.cuda.stream(s_d2h):
+                    copy_out(sets[st])
+                    out_done[st].record(s_d2h)
+
+            put_in(0)
+            for r in range(n):
+                if r + 1 < n:
+                    put_in(r + 1)
+                st = r % 3
+                cur.wait_event(in_done[st])
+                cur.wait_event(out_done[st])
+                compute(sets[st])
+                comp_done[st].record(cur)
+                if r >= 1:
+                    take_out(r - 1)
+            take_out(n - 1)
             cur.wait_stream(s_h2d)
             cur.wait_stream(s_d2h)
 
-        e2e_mode = "3 buffer sets, one CUDA graph per pipelined iteration"
-        graphs = []
-        try:
-            for r in range(3):
-                iteration(r)  # warm-up of the same work outside the capture
-            torch.cuda.synchronize()
-            cap = torch.cuda.Stream(dev)
-            for r in range(3):
-                g_ = torch.cuda.CUDAGraph()
-                with torch.cuda.graph(g_, stream=cap):
-                    iteration(r)
-                graphs.append(g_)
-            torch.cuda.synchronize()
-        except Exception as e:  # noqa: BLE001  (eager iterations then; reported)
-            graphs = []
-            e2e_mode = f"3 buffer sets, eager iterations (graph capture failed: {type(e).__name__})"
-
-        def run_iter(r):
-            if graphs:
-                graphs[r % 3].replay()
-            else:
-                iteration(r % 3)
-
-        for r in range(3):
-            run_iter(r)
+        e2e_mode = ("3 buffer sets; input copies, compute and result copies on three streams "
+                    "ordered by events (eager launches)")
+        pipeline(3)  # warm-up
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        copy_in(sets[0])
-        for r in range(n_e2e):
-            run_iter(r)
-        copy_out(sets[(n_e2e - 1) % 3])
+        pipeline(n_e2e)
         e1.record(stream)
         torch.cuda.synchronize()
         e_ms = e0.elapsed_time(e1) / n_e2e
@@ -621,6 +648,9 @@ def main():
         e2e = {"value": tokens * world / (e_ms / 1e3), "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n_e2e,
                "ms_per_step": e_ms, "pipelining": e2e_mode,
+               "copies": "one per direction per step: every input and every output of the step "
+                         "as 256-byte-aligned views of one pinned host buffer and one device "
+                         "buffer per direction",
                "link_bound": {"ms_per_step": link_ms,
                               "gbs": (h2d + d2h) / (link_ms / 1e3) / 1e9,
                               "frac": link_ms / e_ms,

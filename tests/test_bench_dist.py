@@ -51,3 +51,29 @@ def test_single_process_aggregation():
     import bench
     ms_max, value = bench.aggregate_ranks(4.0, 8192)
     assert ms_max == 4.0 and value == pytest.approx(8192 / 4e-3)
+
+
+def test_packed_views_are_aligned_disjoint_and_contiguous():
+    """The end-to-end leg copies every input (and every output) of a step as
+    one buffer: each tensor a view at a 256-byte-aligned offset, the views
+    disjoint, contiguous, of the requested shape and dtype, and writes
+    through a view land in the flat buffer."""
+    import torch
+    sys.path.insert(0, ROOT)
+    import bench
+    specs = {"x": ((2, 3, 4, 5), torch.bfloat16), "A": ((7,), torch.float32),
+             "dt": ((2, 3, 4), torch.float32), "B": ((2, 3, 1, 16), torch.bfloat16)}
+    flat, views = bench.packed(specs, "cpu")
+    spans = []
+    for k, (shape, dtype) in specs.items():
+        v = views[k]
+        assert tuple(v.shape) == shape and v.dtype == dtype and v.is_contiguous()
+        off = v.data_ptr() - flat.data_ptr()
+        assert off % 256 == 0
+        spans.append((off, off + v.numel() * v.element_size()))
+    spans.sort()
+    assert all(a[1] <= b[0] for a, b in zip(spans, spans[1:]))
+    assert spans[-1][1] <= flat.numel()
+    views["A"].fill_(2.5)
+    off = views["A"].data_ptr() - flat.data_ptr()
+    assert torch.equal(flat[off:off + 28].view(torch.float32), torch.full((7,), 2.5))

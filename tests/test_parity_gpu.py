@@ -325,3 +325,29 @@ def test_repeated_steps_are_bitwise_identical(shape):
         for k, v in ref.items():
             assert torch.equal(out[k], v), k
     torch.cuda.synchronize()
+
+
+def test_fused_paths_with_decay_span_inputs():
+    """The single-pass forward and the backward whose state scan writes the
+    mid-chunk state gradients (g_mid, 256-step chunks taken in two halves)
+    on decay-span inputs (decays down to 1e-4 within a chunk, where the
+    halves' weights exp(cs_i - cs_127) and the regrouped recurrence matter),
+    with h0: one group against the oracle, every output."""
+    from state_space_model_analytic_gb300 import _native as nat
+    dims = synth.Dims(4, 1024, 64, 64, 128, 16, 256, "bf16")  # B * H = 256: fused kernels
+    inp = synth.make_inputs(dims, 37, True, "decay_span")
+    dev = to_device(dims, inp)
+    nat.trace_begin(64)
+    try:
+        gpu = run_gpu(dims, dev)
+    finally:
+        nat.trace_end()
+    names = [r["name"] for r in nat.trace_read()]
+    nat.trace_reset()
+    assert "fwd_single_tc" in names and "state_scan_bwd_tc" in names, names
+    g = 5
+    sdims, sub = group_slice(dims, inp, g)
+    errs, bad = compare(slice_outputs(dims, gpu, g), run_oracle(sdims, sub), TOL["bf16"])
+    print(", ".join(f"{k}={v:.2e}" for k, v in errs.items()))
+    assert not bad, errs
+    nat.check(nat.lib().ssd_device_status())

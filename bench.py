@@ -551,7 +551,10 @@ def main():
                                  "chunk_states": torch.empty_like(fwd_out["chunk_states"])},
                          "bwd": {k: ov[k] for k in bwd_out}})
         s_h2d, s_d2h = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-        n_e2e = max(3, min(args.steps, 200))
+        # steady-state throughput of the pipelined stream: 200 steps (about
+        # 0.1 s) whatever --steps is; 20 steps measured 4 % slower, their
+        # pipeline's fill and drain not amortised
+        n_e2e = 200
 
         def copy_in(st):
             st["in_flat"].copy_(host_in_flat, non_blocking=True)

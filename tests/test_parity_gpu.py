@@ -351,3 +351,34 @@ def test_fused_paths_with_decay_span_inputs():
     print(", ".join(f"{k}={v:.2e}" for k, v in errs.items()))
     assert not bad, errs
     nat.check(nat.lib().ssd_device_status())
+
+
+def test_recompute_mode_on_fused_kernels():
+    """The backward without a history on a shape that fills the GPU with the
+    fused kernels: it recomputes the chunk-start states with the forward
+    state scan, then runs the state scan that writes g_mid and the
+    tensor-core backward.  Against the oracle (one group, every gradient)
+    and against the history-given call (its history came from the
+    single-pass forward, so the two agree within the tolerance, not bit
+    for bit)."""
+    from state_space_model_analytic_gb300 import _native as nat
+    dims = synth.Dims(4, 1024, 64, 64, 128, 16, 256, "bf16")  # B * H = 256
+    inp = synth.make_inputs(dims, 41, True, "softplus")
+    dev = to_device(dims, inp)
+    nat.trace_begin(64)
+    try:
+        rec = run_gpu(dims, dev, "recompute")
+    finally:
+        nat.trace_end()
+    names = [r["name"] for r in nat.trace_read()]
+    nat.trace_reset()
+    assert "state_scan_fwd_tc" in names and "state_scan_bwd_tc" in names, names
+    given = run_gpu(dims, dev, "given")
+    g = 11
+    sdims, sub = group_slice(dims, inp, g)
+    keys = ("dx", "ddt", "dA", "dB", "dC", "dD", "dh0")
+    errs, bad = compare(slice_outputs(dims, rec, g), run_oracle(sdims, sub), TOL["bf16"], keys)
+    assert not bad, errs
+    for k in keys:
+        assert rel_err(rec[k], given[k]) < TOL["bf16"], k
+    nat.check(nat.lib().ssd_device_status())

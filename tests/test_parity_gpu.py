@@ -382,3 +382,30 @@ def test_recompute_mode_on_fused_kernels():
     for k in keys:
         assert rel_err(rec[k], given[k]) < TOL["bf16"], k
     nat.check(nat.lib().ssd_device_status())
+
+
+@pytest.mark.parametrize("shape", [(2, 256, 64, 64, 128, 8, 256),    # one chunk, 128 tiles
+                                   (1, 512, 128, 64, 128, 32, 256),  # two chunks, 256 tiles
+                                   (4, 256, 32, 64, 128, 4, 128)])   # two chunks of 128
+def test_single_pass_forward_few_tiles(shape):
+    """The single-pass forward's resident CTAs when the tiles number fewer
+    than two per SM (some CTAs take one tile or none) and sequences have one
+    or two chunks (no look-back, or one hop): it must be that kernel; one
+    group against the oracle, every output."""
+    from state_space_model_analytic_gb300 import _native as nat
+    dims = synth.Dims(*shape, "bf16")
+    inp = synth.make_inputs(dims, 43, True, "softplus")
+    dev = to_device(dims, inp)
+    nat.trace_begin(64)
+    try:
+        gpu = run_gpu(dims, dev)
+    finally:
+        nat.trace_end()
+    names = [r["name"] for r in nat.trace_read()]
+    nat.trace_reset()
+    assert "fwd_single_tc" in names, names
+    g = dims.ngroups - 1
+    sdims, sub = group_slice(dims, inp, g)
+    errs, bad = compare(slice_outputs(dims, gpu, g), run_oracle(sdims, sub), TOL["bf16"])
+    assert not bad, errs
+    nat.check(nat.lib().ssd_device_status())
